@@ -1,0 +1,435 @@
+"""Benchmark of the sparse MLA decode on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+One step is one decode call over the whole workload (every row, head and key:
+gather, QK, row-max exchange, P, PV, split merge, epilogue). The default
+workload is the latency decode configuration (B=5 verify rows, H=64 heads,
+top-k 256, counts U[200,256] with one empty row, a 65536-row E4M3 pool).
+
+Timing: W untimed warm-up steps, then K timed steps between a barrier and
+torch.cuda.synchronize() on both sides. L2 is flushed before every step by
+reading a buffer twice the L2 size; each decode call is bracketed by CUDA
+events on the stream it is launched on, so ``ms_per_step`` is decode time only.
+``value`` is the gathered-KV throughput (576 bytes per (row, key)) of all
+ranks; ``e2e`` is the same metric through the public call with the step's
+inputs (q, indices, counts) copied from pinned host memory and its outputs
+(out, lse) copied back inside the timed region (the cache pool is resident).
+
+``--impl reference`` times the CPU oracle (the plain C restatement of the
+method) on the host cores, the only reference this method has.
+
+With N > 1 (torchrun, one process per GPU) every rank decodes its own replica
+of the workload; there is no data-path collective. Rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("sparse MLA decode µs/call and gathered-KV GB/s; % of HBM/FP8-MMA roofline")
+UNIT = "GB/s"
+DEFAULT_CONFIG = "latency"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+WORKLOAD_TEXT = {
+    "tiny": "tiny: B=2 rows, H=16, top-k 64, counts {64,37}, pool 4096x576 E4M3",
+    "latency": "latency decode: B=5 verify rows, H=64, top-k 256 (counts U[200,256], one row "
+               "count 0), pool 65536x576 E4M3",
+    "dsa": "DSA decode: B=64, H=128, top-k 2048 (counts U[1,2048], 4 rows 0), pool 262144x576 "
+           "E4M3, half of each row's keys from a 4096-row window",
+    "throughput": "throughput decode: B=256, H=128, top-k 2048 full, pool 1048576x576 E4M3, "
+                  "1% of rows x8",
+    "dense": "dense-as-sparse: 32 requests x 4 causal rows, L U[1024,8192], H=16, pool "
+             "262144x576 E4M3 shuffled",
+}
+
+
+def peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "source": "measured (MEASURED_PEAKS.json)"}
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "source": "fallback (no MEASURED_PEAKS.json)"}
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", rank=rank, world_size=world)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(value: float, world: int, device) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_stats(case) -> dict:
+    from sparse_mla_decode_gb300 import inputs
+    return inputs.algorithmic_bytes(case)
+
+
+def run_gpu(args, world, rank, local) -> dict | None:
+    import torch
+    from sparse_mla_decode_gb300 import binding, inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    case = inputs.config(args.config)
+    stats = workload_stats(case)
+    plan = binding.smd_plan(case.B, case.H, case.W).as_dict()
+
+    q = torch.from_numpy(case.q8).to(dev)
+    kv = torch.from_numpy(case.kv8).to(dev)
+    idx = torch.from_numpy(case.indices).to(dev)
+    cnt = torch.from_numpy(case.counts).to(dev)
+    out = torch.empty((case.B, case.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((case.B, case.H), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+
+    ptrs = (q.data_ptr(), kv.data_ptr(), case.N, idx.data_ptr(), case.W, cnt.data_ptr(),
+            case.B, case.H, case.sm_scale, case.q_scale, case.k_scale, out.data_ptr(),
+            lse.data_ptr(), status.data_ptr(), sptr)
+
+    def decode():
+        rc = binding.smd_sparse_mla_decode(*ptrs)
+        if rc != 0:
+            raise binding.SmdError(rc, "decode")
+
+    def l2_flush():
+        torch.sum(flush, dim=0, out=flush_out)
+
+    # Warm-up (also JIT/module load).
+    for _ in range(max(args.warmup, 3)):
+        l2_flush()
+        decode()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local).start() if rank == 0 else None
+    time.sleep(0.2 if sampler else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        l2_flush()
+        starts[i].record(stream)
+        decode()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop() if sampler else None
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms_local = float(np.mean(times_ms))
+    ms = reduce_max(ms_local, world, dev)
+
+    # ---- end to end through the public call: host buffers in, host buffers out.
+    hq = torch.from_numpy(case.q8).pin_memory()
+    hidx = torch.from_numpy(case.indices).pin_memory()
+    hcnt = torch.from_numpy(case.counts).pin_memory()
+    hout = torch.empty((case.B, case.H, 512), dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty((case.B, case.H), dtype=torch.float32).pin_memory()
+    dq, didx, dcnt = torch.empty_like(q), torch.empty_like(idx), torch.empty_like(cnt)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        didx.copy_(hidx, non_blocking=True)
+        dcnt.copy_(hcnt, non_blocking=True)
+        binding.sparse_mla_decode(dq, kv, didx, dcnt, case.sm_scale, case.q_scale, case.k_scale,
+                                  out=out, lse=lse, status=status)
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        l2_flush()
+        e2e_step()
+    torch.cuda.synchronize()
+    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        l2_flush()
+        e_starts[i].record(stream)
+        e2e_step()
+        e_ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = reduce_max(float(np.mean([s.elapsed_time(e) for s, e in zip(e_starts, e_ends)])),
+                        world, dev)
+    h2d = hq.numel() + hidx.numel() * 4 + hcnt.numel() * 4
+    d2h = hout.numel() * 2 + hlse.numel() * 4
+
+    if rank != 0:
+        return None
+
+    pk = peaks()
+    gathered = stats["kv_gathered"]
+    value = world * gathered / (ms * 1e-3) / 1e9
+    e2e_value = world * gathered / (e2e_ms * 1e-3) / 1e9
+    achieved = stats["total"] / (ms * 1e-3) / 1e9
+    fp8_peak_tflops = 2.0 * pk["bf16_tflops"]
+    t_hbm = stats["total"] / (pk["hbm_gbs"] * 1e9)
+    t_tc = stats["flops"] / (fp8_peak_tflops * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    traffic = load_traffic(args.config)
+    roofline = {
+        "bound": bound,
+        "achieved": round(achieved, 2) if bound == "hbm" else round(
+            stats["flops"] / (ms * 1e-3) / 1e12, 3),
+        "peak": pk["hbm_gbs"] if bound == "hbm" else fp8_peak_tflops,
+        "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+        "traffic": traffic,
+        "kernel": "mma_decode_kernel",
+        "algorithmic_bytes": stats["total"],
+        "algorithmic_flops": stats["flops"],
+        "t_roof_us": round(max(t_hbm, t_tc) * 1e6, 4),
+        "frac_of_roofline_time": round(max(t_hbm, t_tc) / (ms * 1e-3), 5),
+        "peak_source": pk["source"] + ("" if bound == "hbm" else
+                                       "; FP8 = 2 x measured BF16 (nominal ratio)"),
+    }
+    roofline["frac"] = round(roofline["achieved"] / roofline["peak"], 5)
+    cpu = cpu_baseline(case, stats, args.cpu_seconds) if world == 1 or rank == 0 else None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 6),
+        "us_per_call": round(ms * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "fp8_e4m3 (fp32 accumulate)",
+        "data": "synthetic (seeded numpy PCG64; E4M3 per-tensor scaled)",
+        "config": {
+            "workload": WORKLOAD_TEXT[args.config],
+            "name": args.config,
+            "B": case.B, "H": case.H, "top_k": case.W, "pool_rows": case.N,
+            "gathered_keys": case.gathered_rows(), "unique_rows": case.unique_rows(),
+            "l2": "flushed before every timed step (read of a 2x-L2 buffer, outside the events)",
+            "plan": plan,
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_value, 3), "unit": UNIT, "us_per_call": round(e2e_ms * 1e3, 3),
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "note": "q, indices, counts H2D from pinned memory; out, lse D2H; pool resident"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    return line
+
+
+def load_traffic(config: str):
+    """dram bytes per launch from the committed ncu summary of this kernel and
+    workload; None unless it was taken on the current kernel source."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", f"mma_decode_kernel_{config}.json")
+    src = os.path.join(ROOT, "sparse_mla_decode_gb300", "csrc", "smd_mma.cu")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+        if d.get("kernel_source_sha256_16") != digest:
+            return None
+        return d.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def cpu_baseline(case, stats, seconds: float) -> dict:
+    """The oracle, as it stands, on the host cores: repeats of the whole
+    workload (or a row sample of it) for about `seconds`."""
+    import oracle
+    from sparse_mla_decode_gb300 import inputs
+    cores = oracle.max_threads()
+    rows = np.arange(case.B)
+    # A row sample small enough for one call to take a few seconds at most.
+    per_row = 2 * case.H * 1088 * max(1, int(case.clamped_counts().mean()))
+    budget_rows = max(1, int(4e9 * cores / max(per_row, 1)))
+    if budget_rows < case.B:
+        rows = np.random.default_rng(0).choice(case.B, size=budget_rows, replace=False)
+    q8, idx, cnt = case.q8[rows], case.indices[rows], case.counts[rows]
+    gathered = 576 * int(np.clip(cnt.astype(np.int64), 0, case.W).sum())
+    reps, t_total = 0, 0.0
+    while t_total < seconds or reps < 1:
+        t0 = time.perf_counter()
+        oracle.sparse_mla_decode(q8, case.kv8, idx, cnt, case.sm_scale, case.q_scale,
+                                 case.k_scale, threads=cores)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    per_call = t_total / reps
+    sample = (f"{len(rows)} of {case.B} rows, {reps} repeats" if len(rows) < case.B
+              else f"whole workload, {reps} repeats")
+    return {"value": round(gathered / per_call / 1e9, 6), "unit": UNIT, "cores": cores,
+            "kind": "oracle", "sample": sample, "us_per_call_sample": round(per_call * 1e6, 1)}
+
+
+def run_reference(args, world, rank) -> dict | None:
+    if rank != 0:
+        return None
+    from sparse_mla_decode_gb300 import inputs
+    case = inputs.config(args.config)
+    stats = workload_stats(case)
+    import oracle
+    cores = oracle.max_threads()
+    for _ in range(args.warmup):
+        oracle.sparse_mla_decode(case.q8, case.kv8, case.indices, case.counts, case.sm_scale,
+                                 case.q_scale, case.k_scale, threads=cores)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.sparse_mla_decode(case.q8, case.kv8, case.indices, case.counts, case.sm_scale,
+                                 case.q_scale, case.k_scale, threads=cores)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * float(np.mean(times))
+    value = stats["kv_gathered"] / (ms * 1e-3) / 1e9
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "us_per_call": round(ms * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 sums, fp32 logits (CPU oracle)",
+        "data": "synthetic (seeded numpy PCG64)",
+        "config": {"workload": WORKLOAD_TEXT[args.config], "name": args.config,
+                   "B": case.B, "H": case.H, "top_k": case.W, "pool_rows": case.N},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "whole workload per step"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--impl", default="smd", choices=["smd", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    world, rank, local = (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+                          int(os.environ.get("LOCAL_RANK", "0")))
+    if args.impl == "reference":
+        if args.steps > 50 and args.config != "tiny":
+            args.steps = 50
+        line = run_reference(args, world, rank)
+    else:
+        world, rank, local = dist_setup(args.gpus)
+        line = run_gpu(args, world, rank, local)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if args.impl != "reference" and world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

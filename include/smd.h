@@ -1,0 +1,141 @@
+/*
+ * smd.h -- sparse MLA decode over an FP8 (E4M3) latent KV cache, for GB300
+ * (sm_103a). C ABI of libsmd.so.
+ *
+ * The operation (the "attn_sparse" page, SparseDcpDecode: module docstring
+ * paragraphs "Per CTA", "Precision" and "Rows of count 0"; run_sparse's
+ * argument list): for each query row b and head h, over the row's first
+ * n_b = clamp(counts[b], 0, W) key indices j_i = indices[b, i],
+ *
+ *   s_i  = fp32(lambda * fp32(sum_{c<576} q8[b,h,c] * kv8[j_i,c]))
+ *          lambda = fp32(sm_scale * q_scale * k_scale * log2(e))
+ *   m    = max_i s_i                       (the row maximum over ALL n_b keys)
+ *   P_i  = 2^(s_i - m + log2 448)          (fp32; P of the max key is 448)
+ *   P8_i = E4M3(P_i), round to nearest even, saturating
+ *   T    = sum_i P_i                       (fp32, unquantized P)
+ *   out[b,h,c] = BF16(k_scale * sum_i P8_i * kv8[j_i,c] / T),   c < 512
+ *   lse[b,h]   = ln 2 * (m - log2 448 + log2 T)                 (natural log)
+ *
+ * and rows with n_b = 0 write zeros and lse = -inf. The 576-byte cache row
+ * holds 512 latent columns (read by both products) followed by 64 columns
+ * read by the logits only. The keys of a row are split over the CTAs of a
+ * thread-block cluster; their partial sums merge in FP32 over distributed
+ * shared memory. The anchor m is the maximum over the whole row, exchanged
+ * across the cluster before any P is formed, so the result does not depend
+ * on the order of a row's indices beyond FP32 summation order.
+ *
+ * Memory: every pointer argument is DEVICE memory owned by the caller
+ * (cudaMalloc / torch). The library allocates nothing per call and keeps no
+ * per-call state; all calls are asynchronous on `stream`.
+ *
+ * Errors: argument and launch problems are returned synchronously as a
+ * negative smd_status (nothing is launched). Problems only the GPU can see
+ * (a bounded wait that ran out) are written to the optional device word
+ * `status` (left untouched on success; the caller zeroes it beforehand).
+ * Indices of valid entries must lie in [0, N); they are not checked.
+ */
+#ifndef SMD_H
+#define SMD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (NULL = the legacy default stream). */
+typedef struct CUstream_st* smd_stream_t;
+
+typedef enum {
+    SMD_OK = 0,
+    SMD_ERR_NULL = -1,    /* a required pointer is NULL                       */
+    SMD_ERR_SHAPE = -2,   /* H not a positive multiple of 16, B/W/N negative,
+                             N == 0 while B*W > 0, or W beyond the plan limit  */
+    SMD_ERR_ALIGN = -3,   /* q, kv_pool, out not 16-byte aligned; indices,
+                             counts, lse, status not 4-byte aligned            */
+    SMD_ERR_LAUNCH = -4,  /* the CUDA launch failed (cudaGetLastError)        */
+    SMD_ERR_TIMEOUT = -5, /* device status: a bounded wait ran out            */
+    SMD_ERR_PLAN = -6,    /* a forced plan is invalid for these shapes        */
+    SMD_ERR_DEVICE = -7   /* no usable sm_103 device / attribute query failed */
+} smd_status;
+
+/* Kernel families. */
+enum {
+    SMD_KERNEL_AUTO = 0,
+    SMD_KERNEL_MMA = 1   /* warp-level FP8 MMA, 16-head tiles */
+};
+
+/* A launch plan: how the work is laid out. `split` decides which keys each
+ * CTA sums (and so the FP32 summation grouping); `tiles` and `window` only
+ * decide layout, and plans that differ only in them give identical bits. */
+typedef struct {
+    int32_t kernel;      /* SMD_KERNEL_* */
+    int32_t split;       /* CTAs per cluster sharing one row: 1, 2, 4, 8, 16 */
+    int32_t tiles;       /* 16-head tiles per CTA (1 or 2)                   */
+    int32_t window;      /* keys resident in shared memory per pass (64k)    */
+    /* testing hooks (0 = off); only smd_sparse_mla_decode_ex reads them:    */
+    int32_t wait_budget_us; /* bound of every device wait (default 200 ms)   */
+    int32_t inject_stall;   /* 1: the query barrier expects 16 bytes that no
+                               copy delivers, so its wait runs out and the
+                               call reports SMD_ERR_TIMEOUT in `status`      */
+    /* filled in by smd_plan / smd_sparse_mla_decode_ex:                     */
+    int32_t key_cap;     /* most keys one CTA holds logits for               */
+    int32_t grid_x, grid_y, cluster_x, threads, smem_bytes;
+} smd_plan_t;
+
+/*
+ * The decode.
+ *   q        [B, H, 576] uint8 E4M3 codes, row-major (head stride 576 B,
+ *            row stride H*576 B). 16-byte aligned.
+ *   kv_pool  [N, 576] uint8 E4M3 codes (row stride 576 B). 16-byte aligned.
+ *   N        rows in kv_pool (>= 1 when B*W > 0; < 2^31).
+ *   indices  [B, W] int32, row-major; entries [0, counts[b]) of row b are
+ *            its keys (duplicates count twice); the rest are not read.
+ *   W        width of the index array (the top-k), >= 0.
+ *   counts   [B] int32; clamped to [0, W].
+ *   B, H     rows and heads; H a positive multiple of 16. B == 0 is a no-op.
+ *   sm_scale, q_scale, k_scale   softmax scale and the per-tensor E4M3
+ *            scales of q and of the cache.
+ *   out      [B, H, 512] bfloat16 (raw 16-bit storage). 16-byte aligned.
+ *   lse      [B, H] float32, natural log; -inf for empty rows.
+ *   status   optional device int32; a device-side failure writes an
+ *            smd_status there. May be NULL.
+ *   stream   CUDA stream the work is queued on.
+ * Returns SMD_OK or a negative smd_status.
+ */
+int smd_sparse_mla_decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
+                          const int32_t* indices, int32_t W, const int32_t* counts,
+                          int32_t B, int32_t H,
+                          float sm_scale, float q_scale, float k_scale,
+                          uint16_t* out, float* lse, int32_t* status,
+                          smd_stream_t stream);
+
+/* The plan smd_sparse_mla_decode would use for (B, H, W) on the current
+ * device. Host only; touches no device memory. */
+int smd_plan(int32_t B, int32_t H, int32_t W, smd_plan_t* plan);
+
+/* As smd_sparse_mla_decode, with the plan fields kernel/split/tiles/window
+ * taken from `force` (0 = the automatic choice for that field). Used by the
+ * tests to run every layout variant; `force` may be NULL. */
+int smd_sparse_mla_decode_ex(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
+                             const int32_t* indices, int32_t W, const int32_t* counts,
+                             int32_t B, int32_t H,
+                             float sm_scale, float q_scale, float k_scale,
+                             uint16_t* out, float* lse, int32_t* status,
+                             smd_stream_t stream, const smd_plan_t* force);
+
+/* The base-2 logit scale the kernels use: fp32(sm*q_s*k_s*log2 e),
+ * evaluated in double and rounded once. */
+float smd_scale_log2(float sm_scale, float q_scale, float k_scale);
+
+/* Static text for a status code. */
+const char* smd_status_str(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int smd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMD_H */

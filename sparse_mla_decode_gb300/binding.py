@@ -1,0 +1,182 @@
+"""ctypes binding of libsmd.so (include/smd.h), with the same names.
+
+Argument marshalling only: every step of the decode runs in the library's
+CUDA kernels. There is no CPU path; if the library cannot be built or loaded
+the import of a decode function raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from . import build as _build
+
+SMD_OK = 0
+SMD_ERR_NULL = -1
+SMD_ERR_SHAPE = -2
+SMD_ERR_ALIGN = -3
+SMD_ERR_LAUNCH = -4
+SMD_ERR_TIMEOUT = -5
+SMD_ERR_PLAN = -6
+SMD_ERR_DEVICE = -7
+
+SMD_KERNEL_AUTO = 0
+SMD_KERNEL_MMA = 1
+
+
+class SmdPlan(ctypes.Structure):
+    """smd_plan_t."""
+    _fields_ = [(name, ctypes.c_int32) for name in (
+        "kernel", "split", "tiles", "window", "wait_budget_us", "inject_stall", "key_cap",
+        "grid_x", "grid_y", "cluster_x", "threads", "smem_bytes")]
+
+    def as_dict(self) -> dict:
+        return {name: int(getattr(self, name)) for name, _ in self._fields_}
+
+
+class SmdError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        super().__init__(f"{what}: {smd_status_str(status)} ({status})" if what
+                         else f"{smd_status_str(status)} ({status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+_DECODE_ARGS = [
+    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,   # q, kv_pool, N
+    ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,   # indices, W, counts
+    ctypes.c_int32, ctypes.c_int32,                     # B, H
+    ctypes.c_float, ctypes.c_float, ctypes.c_float,     # sm_scale, q_scale, k_scale
+    ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,  # out, lse, status
+    ctypes.c_void_p,                                    # stream
+]
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (built in-tree on first use if missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            so = ctypes.CDLL(path)
+            so.smd_sparse_mla_decode.restype = ctypes.c_int
+            so.smd_sparse_mla_decode.argtypes = _DECODE_ARGS
+            so.smd_sparse_mla_decode_ex.restype = ctypes.c_int
+            so.smd_sparse_mla_decode_ex.argtypes = _DECODE_ARGS + [ctypes.POINTER(SmdPlan)]
+            so.smd_plan.restype = ctypes.c_int
+            so.smd_plan.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                    ctypes.POINTER(SmdPlan)]
+            so.smd_scale_log2.restype = ctypes.c_float
+            so.smd_scale_log2.argtypes = [ctypes.c_float] * 3
+            so.smd_status_str.restype = ctypes.c_char_p
+            so.smd_status_str.argtypes = [ctypes.c_int]
+            so.smd_version.restype = ctypes.c_int
+            so.smd_version.argtypes = []
+            _lib = so
+    return _lib
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+# ---- raw C-ABI calls (pointers as integers) -----------------------------------
+
+def smd_sparse_mla_decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale,
+                          out, lse, status, stream) -> int:
+    return lib().smd_sparse_mla_decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale,
+                                       q_scale, k_scale, out, lse, status, stream)
+
+
+def smd_sparse_mla_decode_ex(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale,
+                             out, lse, status, stream, force: SmdPlan | None) -> int:
+    ref = ctypes.byref(force) if force is not None else None
+    return lib().smd_sparse_mla_decode_ex(q, kv_pool, N, indices, W, counts, B, H, sm_scale,
+                                          q_scale, k_scale, out, lse, status, stream, ref)
+
+
+def smd_plan(B: int, H: int, W: int) -> SmdPlan:
+    p = SmdPlan()
+    rc = lib().smd_plan(B, H, W, ctypes.byref(p))
+    if rc != SMD_OK:
+        raise SmdError(rc, "smd_plan")
+    return p
+
+
+def smd_scale_log2(sm_scale: float, q_scale: float, k_scale: float) -> float:
+    return float(lib().smd_scale_log2(sm_scale, q_scale, k_scale))
+
+
+def smd_status_str(status: int) -> str:
+    return lib().smd_status_str(int(status)).decode()
+
+
+def smd_version() -> int:
+    return int(lib().smd_version())
+
+
+# ---- torch-level marshalling ----------------------------------------------------
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _bytes_view(t, name: str):
+    import torch
+    if t.dtype == torch.float8_e4m3fn:
+        t = t.view(torch.uint8)
+    if t.dtype != torch.uint8:
+        raise TypeError(f"{name}: expected uint8 / float8_e4m3fn, got {t.dtype}")
+    return t
+
+
+def sparse_mla_decode(q, kv_pool, indices, counts, sm_scale: float, q_scale: float,
+                      k_scale: float, out=None, lse=None, status=None, stream=None,
+                      plan: SmdPlan | dict | None = None):
+    """Decode on the GPU. q [B,H,576] and kv_pool [N,576] E4M3 (uint8 or
+    float8_e4m3fn), indices [B,W] int32, counts [B] int32, all CUDA tensors.
+    Returns (out [B,H,512] bfloat16, lse [B,H] float32). ``plan`` forces
+    plan fields (smd_sparse_mla_decode_ex); ``status`` is an optional int32
+    CUDA tensor that receives device-side errors."""
+    import torch
+
+    q = _bytes_view(q, "q")
+    kv_pool = _bytes_view(kv_pool, "kv_pool")
+    for name, t in (("q", q), ("kv_pool", kv_pool), ("indices", indices), ("counts", counts)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (the decode has no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if indices.dtype != torch.int32 or counts.dtype != torch.int32:
+        raise TypeError("indices and counts must be int32")
+    if q.dim() != 3 or q.shape[2] != 576 or kv_pool.dim() != 2 or kv_pool.shape[1] != 576:
+        raise ValueError("q must be [B,H,576] and kv_pool [N,576]")
+    B, H = int(q.shape[0]), int(q.shape[1])
+    W = int(indices.shape[1]) if indices.dim() == 2 else 0
+    if indices.dim() != 2 or indices.shape[0] < B or counts.shape[0] < B:
+        raise ValueError("indices must be [>=B, W] and counts [>=B]")
+    if out is None:
+        out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    args = (_ptr(q), _ptr(kv_pool), int(kv_pool.shape[0]), _ptr(indices), W, _ptr(counts), B, H,
+            float(sm_scale), float(q_scale), float(k_scale), _ptr(out), _ptr(lse), _ptr(status),
+            int(stream))
+    if plan is None:
+        rc = smd_sparse_mla_decode(*args)
+    else:
+        if isinstance(plan, dict):
+            p = SmdPlan()
+            for k, v in plan.items():
+                setattr(p, k, int(v))
+            plan = p
+        rc = smd_sparse_mla_decode_ex(*args, plan)
+    if rc != SMD_OK:
+        raise SmdError(rc, "smd_sparse_mla_decode")
+    return out, lse

@@ -1,0 +1,232 @@
+// C ABI of the sparse MLA decode library: argument checks, the launch plan
+// (split / tile / window choice keyed on heads, top-k width and batch) and
+// dispatch to the kernels. Host code only.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "smd.h"
+#include "smd_internal.h"
+#include "smd_ptx.cuh"
+
+namespace smd {
+namespace {
+
+constexpr int kMaxSmemBytes = 227 * 1024;  // dynamic shared memory per CTA on sm_103
+
+struct DeviceInfo {
+    int sm_count = 0;
+    int major = 0, minor = 0;
+    int smem_optin = 0;
+    bool ok = false;
+};
+
+DeviceInfo query_device() {
+    DeviceInfo d;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return d;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return d;
+    cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    d.ok = true;
+    return d;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+bool is_split(int s) { return s == 1 || s == 2 || s == 4 || s == 8 || s == 16; }
+
+// Most keys one CTA can hold logits for with `tiles` 16-head tiles and a
+// `window`-key buffer, under the shared-memory limit.
+int key_cap_limit(int tiles, int split, int window) {
+    // The layout grows by (16*tiles + 1) * 4 bytes per key of capacity.
+    const int base = mma_layout(tiles, split, window, 0).total;
+    const int per_key = (kHeadsPerTile * tiles + 1) * 4;
+    int cap = std::max(0, (kMaxSmemBytes - base) / per_key) / kChunk * kChunk;
+    while (cap > 0 && mma_layout(tiles, split, window, cap).total > kMaxSmemBytes) cap -= kChunk;
+    return cap;
+}
+
+// Fills the MMA kernel's plan. `force` fields that are non-zero override the
+// automatic choice. Returns an smd_status.
+int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_plan_t* out,
+             MmaConfig* cfg) {
+    int tiles = (H % 32 == 0) ? 2 : 1;
+    if (force && force->tiles) tiles = force->tiles;
+    if (tiles != 1 && tiles != 2) return SMD_ERR_PLAN;
+    if (H % (kHeadsPerTile * tiles) != 0) return SMD_ERR_PLAN;
+    const int units = B * (H / (kHeadsPerTile * tiles));
+    const int window_req = (force && force->window) ? force->window : 128;
+    if (window_req % kChunk != 0 || window_req < kChunk || window_req > 2048) return SMD_ERR_PLAN;
+
+    int split = 0;
+    if (force && force->split) {
+        split = force->split;
+        if (!is_split(split)) return SMD_ERR_PLAN;
+    } else {
+        // Smallest split whose per-CTA share fits, then wider while the grid
+        // is under two waves and every CTA still gets >= 32 keys.
+        for (int s = 1; s <= 16; s *= 2) {
+            const int per = ceil_div(W, s);
+            const int win = std::min(window_req, std::max(kChunk, ceil_div(per, kChunk) * kChunk));
+            if (per <= key_cap_limit(tiles, s, win)) {
+                split = s;
+                break;
+            }
+        }
+        if (split == 0) return SMD_ERR_SHAPE;
+        while (split < 16 && units * split < 2 * sm_count && ceil_div(W, split * 2) >= 32) split *= 2;
+    }
+    const int per = ceil_div(std::max(W, 1), split);
+    const int window = std::min(window_req, std::max(kChunk, ceil_div(per, kChunk) * kChunk));
+    const int key_cap = std::max(kChunk, ceil_div(per, kChunk) * kChunk);
+    const MmaLayout L = mma_layout(tiles, split, window, key_cap);
+    if (L.total > kMaxSmemBytes) return (force && (force->split || force->window)) ? SMD_ERR_PLAN
+                                                                                  : SMD_ERR_SHAPE;
+    cfg->tiles = tiles;
+    cfg->wait_budget_ns = (force && force->wait_budget_us > 0)
+                              ? static_cast<uint64_t>(force->wait_budget_us) * 1000ull
+                              : kWaitBudgetNs;
+    cfg->inject_stall = (force && force->inject_stall) ? 1 : 0;
+    cfg->split = split;
+    cfg->window = window;
+    cfg->key_cap = key_cap;
+    cfg->layout = L;
+    out->kernel = SMD_KERNEL_MMA;
+    out->split = split;
+    out->tiles = tiles;
+    out->window = window;
+    out->key_cap = key_cap;
+    out->grid_x = H / (kHeadsPerTile * tiles) * split;
+    out->grid_y = B;
+    out->cluster_x = split;
+    out->threads = kMmaThreads;
+    out->smem_bytes = L.total;
+    return SMD_OK;
+}
+
+int make_plan(int B, int H, int W, const smd_plan_t* force, smd_plan_t* out, MmaConfig* cfg) {
+    if (B < 0 || W < 0 || H <= 0 || H % kHeadsPerTile != 0) return SMD_ERR_SHAPE;
+    static std::once_flag once;
+    static DeviceInfo info;
+    std::call_once(once, [] { info = query_device(); });
+    const int sm_count = info.ok ? info.sm_count : 152;
+    const int kernel = (force && force->kernel) ? force->kernel : SMD_KERNEL_MMA;
+    if (kernel != SMD_KERNEL_MMA) return SMD_ERR_PLAN;
+    return plan_mma(B, H, W, sm_count, force, out, cfg);
+}
+
+float scale_log2_of(float sm, float qs, float ks) {
+    const double v = static_cast<double>(sm) * static_cast<double>(qs) * static_cast<double>(ks);
+    return static_cast<float>(v * 1.4426950408889634073599246810019);
+}
+
+int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* indices, int32_t W,
+           const int32_t* counts, int32_t B, int32_t H, float sm_scale, float q_scale,
+           float k_scale, uint16_t* out, float* lse, int32_t* status, smd_stream_t stream,
+           const smd_plan_t* force) {
+    if (B < 0 || W < 0 || N < 0 || H <= 0 || H % kHeadsPerTile != 0) return SMD_ERR_SHAPE;
+    if (N >= (int64_t(1) << 31)) return SMD_ERR_SHAPE;
+    if (B == 0) return SMD_OK;
+    if (!q || !out || !lse || !counts) return SMD_ERR_NULL;
+    if (W > 0 && (!indices || !kv_pool)) return SMD_ERR_NULL;
+    if (W > 0 && N == 0) return SMD_ERR_SHAPE;
+    if (!aligned(q, 16) || !aligned(out, 16) || (kv_pool && !aligned(kv_pool, 16)))
+        return SMD_ERR_ALIGN;
+    if ((indices && !aligned(indices, 4)) || !aligned(counts, 4) || !aligned(lse, 4) ||
+        (status && !aligned(status, 4)))
+        return SMD_ERR_ALIGN;
+
+    smd_plan_t plan{};
+    MmaConfig cfg{};
+    const int rc = make_plan(B, H, W, force, &plan, &cfg);
+    if (rc != SMD_OK) return rc;
+
+    CallArgs a{};
+    a.q = q;
+    a.kv = kv_pool;
+    a.N = N;
+    a.indices = indices;
+    a.W = W;
+    a.counts = counts;
+    a.B = B;
+    a.H = H;
+    a.scale_log2 = scale_log2_of(sm_scale, q_scale, k_scale);
+    a.k_scale = k_scale;
+    a.out = out;
+    a.lse = lse;
+    a.status = status;
+    return launch_mma(a, cfg, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+}  // namespace smd
+
+extern "C" {
+
+int smd_sparse_mla_decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
+                          const int32_t* indices, int32_t W, const int32_t* counts, int32_t B,
+                          int32_t H, float sm_scale, float q_scale, float k_scale, uint16_t* out,
+                          float* lse, int32_t* status, smd_stream_t stream) {
+    return smd::decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale, out,
+                       lse, status, stream, nullptr);
+}
+
+int smd_sparse_mla_decode_ex(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
+                             const int32_t* indices, int32_t W, const int32_t* counts, int32_t B,
+                             int32_t H, float sm_scale, float q_scale, float k_scale,
+                             uint16_t* out, float* lse, int32_t* status, smd_stream_t stream,
+                             const smd_plan_t* force) {
+    return smd::decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale, out,
+                       lse, status, stream, force);
+}
+
+int smd_plan(int32_t B, int32_t H, int32_t W, smd_plan_t* plan) {
+    if (!plan) return SMD_ERR_NULL;
+    smd::MmaConfig cfg{};
+    smd_plan_t p{};
+    const int rc = smd::make_plan(B, H, W, nullptr, &p, &cfg);
+    if (rc == SMD_OK) *plan = p;
+    return rc;
+}
+
+float smd_scale_log2(float sm_scale, float q_scale, float k_scale) {
+    return smd::scale_log2_of(sm_scale, q_scale, k_scale);
+}
+
+const char* smd_status_str(int status) {
+    switch (status) {
+        case SMD_OK:
+            return "ok";
+        case SMD_ERR_NULL:
+            return "a required pointer is NULL";
+        case SMD_ERR_SHAPE:
+            return "invalid shape (H must be a positive multiple of 16; B, W, N >= 0; N >= 1 "
+                   "when B*W > 0; N < 2^31; the top-k width must fit the plan)";
+        case SMD_ERR_ALIGN:
+            return "misaligned pointer (q, kv_pool, out: 16 bytes; indices, counts, lse, "
+                   "status: 4 bytes)";
+        case SMD_ERR_LAUNCH:
+            return "CUDA launch failed";
+        case SMD_ERR_TIMEOUT:
+            return "a bounded device wait ran out (device status)";
+        case SMD_ERR_PLAN:
+            return "the forced plan is invalid for these shapes";
+        case SMD_ERR_DEVICE:
+            return "no usable CUDA device";
+        default:
+            return "unknown status";
+    }
+}
+
+int smd_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// Internal declarations shared by the C ABI layer and the kernels.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "smd.h"
+
+namespace smd {
+
+constexpr int kRow = 576;        // bytes of a cache / query row
+constexpr int kLatent = 512;     // columns read by PV
+constexpr int kHeadsPerTile = 16;
+constexpr int kRowPitch = 592;   // shared-memory pitch of a 576-byte row (bank spread)
+constexpr int kChunk = 64;       // keys per gather barrier
+constexpr int kMmaThreads = 512; // 16 warps; PV warp w owns latent columns 32w..32w+31
+
+// Everything a kernel needs to know about one call.
+struct CallArgs {
+    const uint8_t* q;
+    const uint8_t* kv;
+    int64_t N;
+    const int32_t* indices;
+    int32_t W;
+    const int32_t* counts;
+    int32_t B, H;
+    float scale_log2;  // fp32(sm * q_s * k_s * log2 e)
+    float k_scale;
+    uint16_t* out;
+    float* lse;
+    int32_t* status;
+};
+
+// Shared-memory carve-up of the warp-MMA kernel (byte offsets).
+struct MmaLayout {
+    int32_t kv, q, logits, probs, idx, inbox, sums, maxima, lsum, rowmax, bars;
+    int32_t logit_pitch;  // floats per logits row
+    int32_t prob_pitch;   // bytes per P8 row
+    int32_t total;
+};
+
+__host__ __device__ inline int32_t align_up(int32_t x, int32_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline MmaLayout mma_layout(int tiles, int split, int window, int key_cap) {
+    MmaLayout L{};
+    const int ch = kHeadsPerTile * tiles;
+    int32_t o = 0;
+    L.kv = o;
+    o += window * kRowPitch;
+    o = align_up(o, 128);
+    L.q = o;
+    o += ch * kRowPitch;
+    o = align_up(o, 16);
+    L.logit_pitch = key_cap + 8;  // rows 8 banks apart for the float2 stores
+    L.logits = o;
+    o += ch * L.logit_pitch * 4;
+    o = align_up(o, 16);
+    L.prob_pitch = window + 16;
+    L.probs = o;
+    o += ch * L.prob_pitch;
+    o = align_up(o, 16);
+    L.idx = o;
+    o += key_cap * 4;
+    o = align_up(o, 16);
+    L.inbox = o;  // [split][ch][512/split] fp32: every CTA's partial of my columns
+    o += ch * kLatent * 4;
+    L.sums = o;   // [split][ch] fp32
+    o += split * ch * 4;
+    L.maxima = o; // [split][ch] fp32
+    o += split * ch * 4;
+    L.lsum = o;   // [ch] running sums of P
+    o += ch * 4;
+    L.rowmax = o; // [ch] the row maximum
+    o += ch * 4;
+    o = align_up(o, 8);
+    L.bars = o;   // window/64 gather barriers, q, maxima, inbound
+    o += 8 * (window / kChunk + 3);
+    L.total = align_up(o, 128);
+    (void)split;
+    return L;
+}
+
+struct MmaConfig {
+    int tiles, split, window, key_cap;
+    MmaLayout layout;
+    uint64_t wait_budget_ns;
+    int inject_stall;
+};
+
+// Launches the warp-MMA kernel; returns an smd_status.
+int launch_mma(const CallArgs& a, const MmaConfig& cfg, cudaStream_t stream);
+
+}  // namespace smd

@@ -1,0 +1,409 @@
+// Sparse MLA decode, warp-level FP8 tensor-core kernel (sm_103a).
+//
+// One CTA takes (query row b, 16*T heads, its share of the row's keys); the
+// S CTAs of a thread-block cluster split the row's keys as the attn_sparse
+// page's SparseDcpDecode does (per = ceil(n / S), CTA s takes keys
+// [s*per, s*per + per) clamped to n: the kernel body's key split), and merge
+// their partials over distributed shared memory in FP32 (the page's merge
+// method: column ownership, sums in CTA order).
+//
+// Precision follows the page's "Precision" paragraph with the P anchor at the
+// maximum over the WHOLE row: the CTAs first compute all their logits (pass
+// A), exchange their maxima across the cluster, and only then form
+// P = 2^(s - m + log2 448) in E4M3 and run PV (pass B). Per head, every
+// reduction runs in a fixed order that depends neither on timing nor on the
+// number of 16-head tiles a CTA takes.
+//
+// Pass A per window of resident keys: each 576-byte cache row is one
+// cp.async.bulk into shared memory (one mbarrier per 64 keys); QK is
+// mma.sync m16n8k32 E4M3 x E4M3 -> FP32 over the 576 columns (a warp job is
+// 16 heads x 8 keys, two accumulation chains over the 18 k-steps); the
+// scaled logits go to shared memory. Pass B per window: P for 64 keys of a
+// head per warp (lane: a key pair, stored as an E4M3 pair), the FP32 sum of
+// the unquantized P by a fixed butterfly, then PV: warp w owns latent columns
+// 32w..32w+31, V read as words and byte-transposed in registers into the MMA's
+// B fragments. Rows past the count up to the 32-key step are zeroed so that a
+// zero P never meets a NaN byte pattern.
+#include <cmath>
+#include <cstdint>
+
+#include "smd_internal.h"
+#include "smd_ptx.cuh"
+
+namespace smd {
+
+namespace {
+
+struct MmaParams {
+    CallArgs a;
+    int32_t split, window, key_cap;
+    MmaLayout L;
+    float log2_448;
+    uint64_t budget_ns;  // bound of every wait
+    int32_t inject_stall;
+};
+
+// Issues the gathers of keys [w0, w0 + wn) of this CTA into the window
+// buffer: `bytes` of each row (576 for QK+PV, 512 when only V is needed).
+// Rows [wn, roundup32(wn)) are zeroed.
+__device__ __forceinline__ void gather_window(const MmaParams& p, uint32_t kv_s,
+                                              const int32_t* idx_s, uint32_t bars, int w0,
+                                              int wn, uint32_t bytes, uint64_t policy) {
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        for (int c = 0; c * kChunk < wn; ++c) {
+            const int cnt = min(kChunk, wn - c * kChunk);
+            mbar_arrive_expect_tx(bars + 8 * c, cnt * bytes);
+        }
+    }
+    for (int i = tid; i < wn; i += kMmaThreads) {
+        const int64_t j = idx_s[w0 + i];
+        const uint8_t* src = p.a.kv + j * kRow;
+        bulk_g2s_stream(kv_s + i * kRowPitch, src, bytes, bars + 8 * (i / kChunk), policy);
+    }
+    const int span = (wn + 31) & ~31;
+    for (int e = wn * (kRow / 16) + tid; e < span * (kRow / 16); e += kMmaThreads) {
+        const int r = e / (kRow / 16), c16 = e % (kRow / 16);
+        sts_zero16(kv_s + r * kRowPitch + 16 * c16);
+    }
+}
+
+template <int T>
+__global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int CH = kHeadsPerTile * T;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, qd = lane & 3;
+    const int S = p.split;
+    const int split = static_cast<int>(cluster_ctarank());
+    const int tile_group = blockIdx.x / S;
+    const int b = blockIdx.y;
+    const int head0 = tile_group * CH;
+
+    const uint32_t base = smem_addr(smem);
+    const uint32_t kv_s = base + p.L.kv;
+    const uint32_t q_s = base + p.L.q;
+    const uint32_t prob_s = base + p.L.probs;
+    float* logits = reinterpret_cast<float*>(smem + p.L.logits);
+    int32_t* idx_s = reinterpret_cast<int32_t*>(smem + p.L.idx);
+    float* inbox = reinterpret_cast<float*>(smem + p.L.inbox);
+    float* sums = reinterpret_cast<float*>(smem + p.L.sums);
+    float* maxima = reinterpret_cast<float*>(smem + p.L.maxima);
+    float* lsum = reinterpret_cast<float*>(smem + p.L.lsum);
+    float* rowmax = reinterpret_cast<float*>(smem + p.L.rowmax);
+    const int nchunk_bars = p.window / kChunk;
+    const uint32_t bars = base + p.L.bars;
+    const uint32_t q_bar = bars + 8 * nchunk_bars;
+    const uint32_t max_bar = q_bar + 8;
+    const uint32_t in_bar = q_bar + 16;
+    const int LP = p.L.logit_pitch, PP = p.L.prob_pitch;
+    const int CW = kLatent / S;  // latent columns this CTA merges
+
+    bool ok = true;
+    int32_t* status = p.a.status;
+
+    if (tid == 0) {
+        for (int c = 0; c < nchunk_bars; ++c) mbar_init(bars + 8 * c, 1);
+        mbar_init(q_bar, 1);
+        mbar_init(max_bar, 1);
+        mbar_init(in_bar, 1);
+        fence_mbar_init();
+        // Bytes the peers will push into this CTA: their maxima, and their
+        // partials of this CTA's columns plus their sums.
+        mbar_arrive_expect_tx(max_bar, (S - 1) * CH * 4);
+        mbar_arrive_expect_tx(in_bar, (S - 1) * (CH * CW * 4 + CH * 4));
+    }
+    for (int h = tid; h < CH; h += kMmaThreads) lsum[h] = 0.f;
+    __syncthreads();
+    // Every CTA's barriers are armed before any peer pushes (waited below).
+    cluster_arrive_relaxed();
+
+    // ---- this CTA's keys: [first, first + mine) of the row ------------------
+    const int W = p.a.W;
+    int n = p.a.counts[b];
+    n = max(min(n, W), 0);
+    const int per = (n + S - 1) / S;
+    const int first = min(n, split * per);
+    const int mine = min(n - first, per);
+    const int32_t* row_idx = p.a.indices + static_cast<int64_t>(b) * W + first;
+    for (int i = tid; i < mine; i += kMmaThreads) idx_s[i] = row_idx[i];
+
+    // (inject_stall: the barrier also expects 16 bytes nobody sends, so the
+    // bounded wait below runs out; a test hook for the timeout path.)
+    if (tid == 0) mbar_arrive_expect_tx(q_bar, CH * kRow + (p.inject_stall ? 16 : 0));
+    if (tid < CH) {
+        const uint8_t* src = p.a.q + (static_cast<int64_t>(b) * p.a.H + head0 + tid) * kRow;
+        bulk_g2s(q_s + tid * kRowPitch, src, kRow, q_bar);
+    }
+    __syncthreads();
+
+    const uint64_t policy = policy_evict_normal();
+    const float neg_inf = -INFINITY;
+    const float lam = p.a.scale_log2;
+    const int nwin = (mine + p.window - 1) / p.window;
+    // Parity of the next completion of each gather barrier (bit c: barrier c).
+    uint32_t phase_bits = 0;
+
+    // ldmatrix lane addressing: A (16 rows x 32 B), B (8 keys x 64 B).
+    const int a_row = (lane & 7) + 8 * ((lane >> 3) & 1);
+    const int a_col = 16 * (lane >> 4);
+
+    mbar_wait(q_bar, 0, ok, status, p.budget_ns);
+
+    // ================================ pass A: logits =========================
+    for (int wi = 0; wi < nwin; ++wi) {
+        const int w0 = wi * p.window;
+        const int wn = min(p.window, mine - w0);
+        if (!__syncthreads_and(ok)) break;  // a failed CTA issues no more copies
+        gather_window(p, kv_s, idx_s, bars, w0, wn, kRow, policy);
+        __syncthreads();  // zeroed tail rows
+        for (int c = 0; c * kChunk < wn; ++c) {
+            const int cnt = min(kChunk, wn - c * kChunk);
+            mbar_wait(bars + 8 * c, (phase_bits >> c) & 1u, ok, status, p.budget_ns);
+            phase_bits ^= 1u << c;
+            for (int job = warp; job < 8 * T; job += kMmaThreads / 32) {
+                const int t = job >> 3, kg = job & 7;
+                if (8 * kg >= cnt) continue;
+                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint32_t kaddr =
+                    kv_s + (c * kChunk + 8 * kg + (lane & 7)) * kRowPitch + 16 * (lane >> 3);
+                const uint32_t qaddr = q_s + (16 * t + a_row) * kRowPitch + a_col;
+#pragma unroll
+                for (int kp = 0; kp < kRow / 64; ++kp) {
+                    uint32_t kb[4], qa[4], qb[4];
+                    ldsm_x4(kaddr + 64 * kp, kb);
+                    ldsm_x4(qaddr + 64 * kp, qa);
+                    ldsm_x4(qaddr + 64 * kp + 32, qb);
+                    mma_e4m3(c0, qa, kb[0], kb[1]);
+                    mma_e4m3(c1, qb, kb[2], kb[3]);
+                }
+                const int key = c * kChunk + 8 * kg + 2 * qd;  // within the window
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float s0 = (key < wn) ? lam * (c0[2 * r] + c1[2 * r]) : neg_inf;
+                    const float s1 = (key + 1 < wn) ? lam * (c0[2 * r + 1] + c1[2 * r + 1]) : neg_inf;
+                    float2* dst = reinterpret_cast<float2*>(
+                        logits + (16 * t + g + 8 * r) * LP + w0 + key);
+                    *dst = make_float2(s0, s1);
+                }
+            }
+        }
+        __syncthreads();  // the window buffer is free again
+        fence_proxy_async();  // ... also for the bulk copies that refill it
+    }
+
+    // ---- the row maximum over the cluster ------------------------------------
+    for (int h = warp; h < CH; h += kMmaThreads / 32) {
+        float mx = neg_inf;
+        for (int k = lane; k < mine; k += 32) mx = fmaxf(mx, logits[h * LP + k]);
+        mx = warp_max(mx);
+        if (lane == 0) maxima[split * CH + h] = mx;
+    }
+    __syncthreads();
+    cluster_wait();  // peers' barriers are initialised
+    if (tid < CH) {
+        const uint32_t v = __float_as_uint(maxima[split * CH + tid]);
+        const uint32_t slot = smem_addr(maxima + split * CH + tid);
+        for (int pr = 0; pr < S; ++pr)
+            if (pr != split) st_async_b32(mapa(slot, pr), v, mapa(max_bar, pr));
+    }
+    mbar_wait(max_bar, 0, ok, status, p.budget_ns, /*always=*/true);
+    for (int h = tid; h < CH; h += kMmaThreads) {
+        float m = neg_inf;
+        for (int pr = 0; pr < S; ++pr) m = fmaxf(m, maxima[pr * CH + h]);
+        rowmax[h] = m;
+    }
+    __syncthreads();
+
+    // ================================ pass B: P and PV =======================
+    float acc[T][4][4];
+#pragma unroll
+    for (int t = 0; t < T; ++t)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[t][j][e] = 0.f;
+
+    // Windows in reverse: the last window of pass A is still resident. Every
+    // chunk's P and PV terms are added in descending chunk order.
+    for (int wi = nwin - 1; wi >= 0; --wi) {
+        const int w0 = wi * p.window;
+        const int wn = min(p.window, mine - w0);
+        const bool regather = (wi != nwin - 1);
+        if (!__syncthreads_and(ok)) break;
+        if (regather) {
+            gather_window(p, kv_s, idx_s, bars, w0, wn, kLatent, policy);
+            __syncthreads();
+        }
+        // Chunks in descending order too: the row's chunks are then summed in
+        // one global order whatever the window size.
+        for (int c = (wn - 1) / kChunk; c >= 0; --c) {
+            const int cnt = min(kChunk, wn - c * kChunk);
+            if (regather) {
+                mbar_wait(bars + 8 * c, (phase_bits >> c) & 1u, ok, status, p.budget_ns);
+                phase_bits ^= 1u << c;
+            }
+            // P of 64 keys x this warp's heads; lane: keys 2*lane, 2*lane + 1.
+#pragma unroll
+            for (int i = 0; i < T; ++i) {
+                const int h = warp + 16 * i;
+                const float bias = rowmax[h] - p.log2_448;
+                const int k = c * kChunk + 2 * lane;
+                const float2 sv = *reinterpret_cast<const float2*>(logits + h * LP + w0 + k);
+                const float p0 = (k < wn) ? ex2_approx(sv.x - bias) : 0.f;
+                const float p1 = (k + 1 < wn) ? ex2_approx(sv.y - bias) : 0.f;
+                sts_u16(prob_s + h * PP + k, e4m3x2(p0, p1));
+                const float tot = warp_sum(p0 + p1);
+                if (lane == 0) lsum[h] += tot;
+            }
+            __syncthreads();
+            // PV: latent columns 32*warp + 4*g + (0..3), every tile.
+            const int span = (cnt + 31) & ~31;
+#pragma unroll
+            for (int ks = 0; ks < kChunk / 32; ++ks) {
+                if (32 * ks >= span) break;
+                uint32_t vb[2][4];
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int key = c * kChunk + 32 * ks + 16 * hf + 4 * qd + i;
+                        w[i] = lds_u32(kv_s + key * kRowPitch + 32 * warp + 4 * g);
+                    }
+                    byte_transpose4(w[0], w[1], w[2], w[3], vb[hf]);
+                }
+#pragma unroll
+                for (int t = 0; t < T; ++t) {
+                    uint32_t pa[4];
+                    ldsm_x4(prob_s + (16 * t + a_row) * PP + c * kChunk + 32 * ks + a_col, pa);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) mma_e4m3(acc[t][j], pa, vb[0][j], vb[1][j]);
+                }
+            }
+        }
+        __syncthreads();  // window buffer and P free for the next window
+        fence_proxy_async();
+    }
+
+    // ---- partials to the column owners (FP32 bits over DSMEM) ----------------
+    // acc[t][j][e]: head 16t + g + 8(e>>1), column 32*warp + 8*qd + 4*(e&1) + j.
+    {
+        const int owner = (32 * warp) / CW;
+        const uint32_t inbox_s = smem_addr(inbox);
+#pragma unroll
+        for (int t = 0; t < T; ++t) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int h = 16 * t + g + 8 * (e >> 1);
+                const int col = 32 * warp + 8 * qd + 4 * (e & 1);
+                const float4 v = make_float4(acc[t][0][e], acc[t][1][e], acc[t][2][e], acc[t][3][e]);
+                const uint32_t dst = inbox_s + ((split * CH + h) * CW + (col - owner * CW)) * 4;
+                if (owner == split)
+                    sts_v4(dst, v);
+                else
+                    st_async_v4(mapa(dst, owner), v, mapa(in_bar, owner));
+            }
+        }
+        if (tid < CH) {
+            const float l = lsum[tid];
+            sums[split * CH + tid] = l;
+            const uint32_t slot = smem_addr(sums + split * CH + tid);
+            for (int pr = 0; pr < S; ++pr)
+                if (pr != split) st_async_b32(mapa(slot, pr), __float_as_uint(l), mapa(in_bar, pr));
+        }
+    }
+    mbar_wait(in_bar, 0, ok, status, p.budget_ns, /*always=*/true);
+    __syncthreads();  // this CTA's own partial (plain stores)
+
+    // ---- merge in CTA order; BF16(sum * k_scale / total) ---------------------
+    if (ok) {
+        const int per_row = CW / 4;
+        for (int it = tid; it < CH * per_row; it += kMmaThreads) {
+            const int h = it / per_row, c4 = it % per_row;
+            float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+            float total = 0.f;
+            for (int src = 0; src < S; ++src) {
+                const float4 v = *reinterpret_cast<const float4*>(inbox + (src * CH + h) * CW + 4 * c4);
+                m.x += v.x;
+                m.y += v.y;
+                m.z += v.z;
+                m.w += v.w;
+                total += sums[src * CH + h];
+            }
+            const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
+            uint2 packed;
+            packed.x = bf16x2(m.x * inv, m.y * inv);
+            packed.y = bf16x2(m.z * inv, m.w * inv);
+            uint16_t* dst = p.a.out + (static_cast<int64_t>(b) * p.a.H + head0 + h) * kLatent +
+                            split * CW + 4 * c4;
+            *reinterpret_cast<uint2*>(dst) = packed;
+        }
+        if (split == 0) {
+            for (int h = tid; h < CH; h += kMmaThreads) {
+                float total = 0.f;
+                for (int src = 0; src < S; ++src) total += sums[src * CH + h];
+                const float lse2 =
+                    total > 0.f ? rowmax[h] - p.log2_448 + log2f(total) : neg_inf;
+                p.a.lse[static_cast<int64_t>(b) * p.a.H + head0 + h] =
+                    total > 0.f ? lse2 * 0.69314718055994530942f : neg_inf;
+            }
+        }
+    }
+}
+
+template <int T>
+int launch_t(const MmaParams& prm, const MmaConfig& cfg, const CallArgs& a, cudaStream_t stream) {
+    auto kern = mma_decode_kernel<T>;
+    cudaError_t err =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.layout.total);
+    if (err != cudaSuccess) return SMD_ERR_LAUNCH;
+    if (cfg.split > 8) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (err != cudaSuccess) return SMD_ERR_LAUNCH;
+    }
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(static_cast<unsigned>(a.H / (kHeadsPerTile * T) * cfg.split),
+                      static_cast<unsigned>(a.B), 1);
+    lc.blockDim = dim3(kMmaThreads, 1, 1);
+    lc.dynamicSmemBytes = static_cast<size_t>(cfg.layout.total);
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cfg.split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    err = cudaLaunchKernelEx(&lc, kern, prm);
+    if (err != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SMD_ERR_LAUNCH;
+    }
+    return SMD_OK;
+}
+
+}  // namespace
+
+int launch_mma(const CallArgs& a, const MmaConfig& cfg, cudaStream_t stream) {
+    MmaParams prm{};
+    prm.a = a;
+    prm.split = cfg.split;
+    prm.window = cfg.window;
+    prm.key_cap = cfg.key_cap;
+    prm.L = cfg.layout;
+    prm.log2_448 = static_cast<float>(std::log2(448.0));
+    prm.budget_ns = cfg.wait_budget_ns;
+    prm.inject_stall = cfg.inject_stall;
+    switch (cfg.tiles) {
+        case 1:
+            return launch_t<1>(prm, cfg, a, stream);
+        case 2:
+            return launch_t<2>(prm, cfg, a, stream);
+        default:
+            return SMD_ERR_PLAN;
+    }
+}
+
+}  // namespace smd

@@ -1,0 +1,249 @@
+// Inline-PTX building blocks for the sparse MLA decode kernels (sm_103a).
+//
+// mbarrier transaction barriers, bulk global->shared copies, cluster
+// barriers and distributed-shared-memory stores, warp-level FP8 MMA and the
+// E4M3 / BF16 conversions. Every wait on another agent (a bulk copy, a peer
+// CTA) is bounded by a %globaltimer budget and reports a status word instead
+// of spinning forever.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace smd {
+
+// Longest a CTA waits for a copy or a peer before it gives up (ns).
+constexpr uint64_t kWaitBudgetNs = 200ull * 1000ull * 1000ull;
+constexpr int32_t kStatusTimeout = -5;  // SMD_ERR_TIMEOUT
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ---------------------------------------------------------------- mbarrier --
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Makes barrier initialisation visible to the cluster (and the async proxy).
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits for phase `parity` of the barrier to complete, at most `budget_ns`.
+// On expiry records SMD_ERR_TIMEOUT in *status (first writer wins), clears
+// `ok` and returns. Later waits of a failed CTA return at once unless
+// `always` is set: exchange barriers that peers fill unconditionally are still
+// waited for, so that no peer store is in flight into a CTA that has exited.
+__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, bool& ok,
+                                          int32_t* status, uint64_t budget_ns,
+                                          bool always = false) {
+    if (!ok && !always) return;
+    if (mbar_test(bar, parity)) return;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_test(bar, parity)) {
+        if (globaltimer() - t0 > budget_ns) {
+            if (status != nullptr) atomicCAS(status, 0, kStatusTimeout);
+            ok = false;
+            return;
+        }
+    }
+}
+
+// ------------------------------------------------------------- bulk copies --
+
+// One contiguous global -> shared copy (both addresses 16-byte aligned, size a
+// multiple of 16) completing on `bar` with its byte count.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// As bulk_g2s, with an L2 evict-first policy (data read once).
+__device__ __forceinline__ void bulk_g2s_stream(uint32_t dst, const void* src, uint32_t bytes,
+                                                uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- clusters --
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Remote stores into a peer CTA's shared memory, counted on its barrier.
+__device__ __forceinline__ void st_async_b32(uint32_t raddr, uint32_t v, uint32_t rbar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(raddr),
+        "r"(v), "r"(rbar)
+        : "memory");
+}
+
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float4 v, uint32_t rbar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(raddr),
+        "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+        "r"(__float_as_uint(v.w)), "r"(rbar)
+        : "memory");
+}
+
+// ------------------------------------------------------------ shared memory --
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts_v4(uint32_t addr, float4 v) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ void sts_zero16(uint32_t addr) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
+}
+
+// Four 8x8 b16 tiles (8 rows x 16 bytes each); lanes 8i..8i+7 address tile i.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// ------------------------------------------------------------------ math --
+
+// D(16x8, f32) += A(16x32, e4m3, row) * B(32x8, e4m3, col).
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 2^x on the SFU (the fast-math exp2 the method uses).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Two floats -> two E4M3 bytes (round to nearest even, saturating to +-448):
+// `lo` in the low byte, `hi` in the high byte.
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two floats -> packed bf16x2 (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Byte transpose of a 4x4 block held in four words: word j of the result
+// holds byte j of w0, w1, w2, w3 (in that order, lowest byte first).
+__device__ __forceinline__ void byte_transpose4(uint32_t w0, uint32_t w1, uint32_t w2,
+                                                uint32_t w3, uint32_t (&out)[4]) {
+    // Interleave bytes of (w0, w1) and (w2, w3), then interleave halves.
+    const uint32_t a = __byte_perm(w0, w1, 0x5140);  // w0.0 w1.0 w0.1 w1.1
+    const uint32_t c = __byte_perm(w0, w1, 0x7362);  // w0.2 w1.2 w0.3 w1.3
+    const uint32_t e = __byte_perm(w2, w3, 0x5140);  // w2.0 w3.0 w2.1 w3.1
+    const uint32_t f = __byte_perm(w2, w3, 0x7362);  // w2.2 w3.2 w2.3 w3.3
+    out[0] = __byte_perm(a, e, 0x5410);
+    out[1] = __byte_perm(a, e, 0x7632);
+    out[2] = __byte_perm(c, f, 0x5410);
+    out[3] = __byte_perm(c, f, 0x7632);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace smd

@@ -1,0 +1,134 @@
+"""Host-side checks of the C-ABI library: it builds for sm_103a, loads, exports
+every entry point include/smd.h declares, and rejects bad arguments before
+any launch. Nothing here launches a kernel or touches device memory."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from sparse_mla_decode_gb300 import binding as smd
+from sparse_mla_decode_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions() -> list[str]:
+    text = open(os.path.join(ROOT, "include", "smd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(smd_\w+)\s*\(", text)))
+
+
+def test_library_builds_and_exports_every_declared_symbol():
+    path = build.build()
+    assert os.path.exists(path)
+    lib = ctypes.CDLL(path)
+    names = declared_functions()
+    assert "smd_sparse_mla_decode" in names and "smd_plan" in names
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_library_is_built_for_sm_103a_only():
+    assert "arch=compute_103a,code=sm_103a" in " ".join(build.ARCH)
+
+
+def test_scale_log2_is_the_rounded_double_product():
+    import oracle
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        sm, qs, ks = (float(np.float32(x)) for x in rng.uniform(1e-4, 2.0, 3))
+        assert smd.smd_scale_log2(sm, qs, ks) == oracle.scale_log2(sm, qs, ks)
+
+
+def test_status_strings():
+    for code in range(-7, 1):
+        s = smd.smd_status_str(code)
+        assert s and s != "unknown status"
+    assert smd.smd_status_str(-99) == "unknown status"
+    assert smd.smd_version() >= 100
+
+
+# Fake but well-aligned addresses: every call below must be rejected on the
+# host before anything is launched.
+A = 1 << 20
+
+
+def call(q=A, kv=A, N=100, idx=A, W=8, counts=A, B=2, H=16, out=A, lse=A, status=0,
+         force=None):
+    if force is None:
+        return smd.smd_sparse_mla_decode(q, kv, N, idx, W, counts, B, H, 0.1, 0.1, 0.1,
+                                         out, lse, status, 0)
+    return smd.smd_sparse_mla_decode_ex(q, kv, N, idx, W, counts, B, H, 0.1, 0.1, 0.1,
+                                        out, lse, status, 0, force)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=0), smd.SMD_ERR_SHAPE),
+    (dict(H=17), smd.SMD_ERR_SHAPE),
+    (dict(H=-16), smd.SMD_ERR_SHAPE),
+    (dict(B=-1), smd.SMD_ERR_SHAPE),
+    (dict(W=-1), smd.SMD_ERR_SHAPE),
+    (dict(N=-1), smd.SMD_ERR_SHAPE),
+    (dict(N=0), smd.SMD_ERR_SHAPE),
+    (dict(N=1 << 31), smd.SMD_ERR_SHAPE),
+    (dict(q=0), smd.SMD_ERR_NULL),
+    (dict(kv=0), smd.SMD_ERR_NULL),
+    (dict(idx=0), smd.SMD_ERR_NULL),
+    (dict(counts=0), smd.SMD_ERR_NULL),
+    (dict(out=0), smd.SMD_ERR_NULL),
+    (dict(lse=0), smd.SMD_ERR_NULL),
+    (dict(q=A + 8), smd.SMD_ERR_ALIGN),
+    (dict(kv=A + 4), smd.SMD_ERR_ALIGN),
+    (dict(out=A + 2), smd.SMD_ERR_ALIGN),
+    (dict(idx=A + 2), smd.SMD_ERR_ALIGN),
+    (dict(counts=A + 1), smd.SMD_ERR_ALIGN),
+    (dict(lse=A + 2), smd.SMD_ERR_ALIGN),
+    (dict(status=A + 2), smd.SMD_ERR_ALIGN),
+    (dict(B=0, q=0, out=0, lse=0, counts=0, idx=0, kv=0), smd.SMD_OK),
+])
+def test_argument_checks(kw, code):
+    assert call(**kw) == code
+
+
+@pytest.mark.parametrize("force", [
+    dict(split=3), dict(split=32), dict(tiles=3), dict(tiles=4), dict(window=65),
+    dict(window=4096), dict(kernel=9),
+])
+def test_invalid_forced_plans_are_rejected(force):
+    p = smd.SmdPlan()
+    for k, v in force.items():
+        setattr(p, k, v)
+    assert call(force=p) == smd.SMD_ERR_PLAN
+
+
+@pytest.mark.parametrize("B,H,W", [(2, 16, 64), (5, 64, 256), (64, 128, 2048), (256, 128, 2048),
+                                   (128, 16, 8192), (1, 16, 0), (3, 48, 100), (7, 32, 1),
+                                   (1, 256, 4096), (4, 16, 16384)])
+def test_plan_invariants(B, H, W):
+    p = smd.smd_plan(B, H, W).as_dict()
+    assert p["kernel"] == smd.SMD_KERNEL_MMA
+    assert p["split"] in (1, 2, 4, 8, 16) and p["cluster_x"] == p["split"]
+    assert p["tiles"] in (1, 2) and H % (16 * p["tiles"]) == 0
+    assert p["grid_x"] == H // (16 * p["tiles"]) * p["split"] and p["grid_y"] == B
+    assert p["key_cap"] >= -(-W // p["split"]) and p["key_cap"] % 64 == 0
+    assert p["window"] % 64 == 0 and 64 <= p["window"] <= p["key_cap"]
+    assert p["smem_bytes"] <= 227 * 1024 and p["threads"] == 512
+
+
+def test_plan_rejects_widths_beyond_the_limit():
+    with pytest.raises(smd.SmdError) as e:
+        smd.smd_plan(1, 16, 1 << 20)
+    assert e.value.status == smd.SMD_ERR_SHAPE
+
+
+def test_cpu_tensors_are_refused():
+    import torch
+    q = torch.zeros((1, 16, 576), dtype=torch.uint8)
+    kv = torch.zeros((8, 576), dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA"):
+        smd.sparse_mla_decode(q, kv, torch.zeros((1, 4), dtype=torch.int32),
+                              torch.zeros(1, dtype=torch.int32), 0.1, 0.1, 0.1)
