@@ -17,6 +17,7 @@ namespace smd {
 namespace {
 
 constexpr int kMaxSmemBytes = 227 * 1024;  // dynamic shared memory per CTA on sm_103
+constexpr int kSpecIdxMaxW = 2048;        // widest row whose index list is loaded up front
 
 struct DeviceInfo {
     int sm_count = 0;
@@ -44,14 +45,16 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 bool is_split(int s) { return s == 1 || s == 2 || s == 4 || s == 8 || s == 16; }
 
-// Most keys one CTA can hold logits for with `tiles` 16-head tiles and a
-// `window`-key buffer, under the shared-memory limit.
-int key_cap_limit(int tiles, int split, int window) {
+// Most keys one CTA can hold logits for with `tiles` 16-head tiles, a
+// `window`-key buffer and `idx_cap` staged indices, under the shared-memory
+// limit.
+int key_cap_limit(int tiles, int split, int window, int idx_cap) {
     // The layout grows by (16*tiles + 1) * 4 bytes per key of capacity.
-    const int base = mma_layout(tiles, split, window, 0).total;
+    const int base = mma_layout(tiles, split, window, 0, idx_cap).total;
     const int per_key = (kHeadsPerTile * tiles + 1) * 4;
     int cap = std::max(0, (kMaxSmemBytes - base) / per_key) / kChunk * kChunk;
-    while (cap > 0 && mma_layout(tiles, split, window, cap).total > kMaxSmemBytes) cap -= kChunk;
+    while (cap > 0 && mma_layout(tiles, split, window, cap, idx_cap).total > kMaxSmemBytes)
+        cap -= kChunk;
     return cap;
 }
 
@@ -66,6 +69,8 @@ int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
     const int units = B * (H / (kHeadsPerTile * tiles));
     const int window_req = (force && force->window) ? force->window : 128;
     if (window_req % kChunk != 0 || window_req < kChunk || window_req > 2048) return SMD_ERR_PLAN;
+    // Rows up to kSpecIdxMaxW wide have their whole index list staged.
+    const int spec = (W <= kSpecIdxMaxW) ? W : 0;
 
     int split = 0;
     if (force && force->split) {
@@ -77,7 +82,7 @@ int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
         for (int s = 1; s <= 16; s *= 2) {
             const int per = ceil_div(W, s);
             const int win = std::min(window_req, std::max(kChunk, ceil_div(per, kChunk) * kChunk));
-            if (per <= key_cap_limit(tiles, s, win)) {
+            if (per <= key_cap_limit(tiles, s, win, spec)) {
                 split = s;
                 break;
             }
@@ -88,7 +93,7 @@ int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
     const int per = ceil_div(std::max(W, 1), split);
     const int window = std::min(window_req, std::max(kChunk, ceil_div(per, kChunk) * kChunk));
     const int key_cap = std::max(kChunk, ceil_div(per, kChunk) * kChunk);
-    const MmaLayout L = mma_layout(tiles, split, window, key_cap);
+    const MmaLayout L = mma_layout(tiles, split, window, key_cap, spec);
     if (L.total > kMaxSmemBytes) return (force && (force->split || force->window)) ? SMD_ERR_PLAN
                                                                                   : SMD_ERR_SHAPE;
     cfg->tiles = tiles;
@@ -96,6 +101,7 @@ int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
                               ? static_cast<uint64_t>(force->wait_budget_us) * 1000ull
                               : kWaitBudgetNs;
     cfg->inject_stall = (force && force->inject_stall) ? 1 : 0;
+    cfg->spec_idx = spec > 0 ? 1 : 0;
     cfg->split = split;
     cfg->window = window;
     cfg->key_cap = key_cap;

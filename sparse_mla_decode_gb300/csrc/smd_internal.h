@@ -42,7 +42,10 @@ struct MmaLayout {
 
 __host__ __device__ inline int32_t align_up(int32_t x, int32_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline MmaLayout mma_layout(int tiles, int split, int window, int key_cap) {
+// idx_cap: int32 entries of the index staging area (the CTA's keys, or the
+// row's whole list when it is loaded speculatively).
+__host__ __device__ inline MmaLayout mma_layout(int tiles, int split, int window, int key_cap,
+                                                int idx_cap) {
     MmaLayout L{};
     const int ch = kHeadsPerTile * tiles;
     int32_t o = 0;
@@ -61,7 +64,7 @@ __host__ __device__ inline MmaLayout mma_layout(int tiles, int split, int window
     o += ch * L.prob_pitch;
     o = align_up(o, 16);
     L.idx = o;
-    o += key_cap * 4;
+    o += (idx_cap > key_cap ? idx_cap : key_cap) * 4;
     o = align_up(o, 16);
     L.inbox = o;  // [split][ch][512/split] fp32: every CTA's partial of my columns
     o += ch * kLatent * 4;
@@ -86,6 +89,7 @@ struct MmaConfig {
     MmaLayout layout;
     uint64_t wait_budget_ns;
     int inject_stall;
+    int spec_idx;
 };
 
 // Launches the warp-MMA kernel; returns an smd_status.

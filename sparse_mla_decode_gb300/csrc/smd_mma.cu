@@ -24,6 +24,7 @@
 // 32w..32w+31, V read as words and byte-transposed in registers into the MMA's
 // B fragments. Rows past the count up to the 32-key step are zeroed so that a
 // zero P never meets a NaN byte pattern.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -34,6 +35,8 @@ namespace smd {
 
 namespace {
 
+constexpr int kMaxDevices = 64;
+
 struct MmaParams {
     CallArgs a;
     int32_t split, window, key_cap;
@@ -41,6 +44,7 @@ struct MmaParams {
     float log2_448;
     uint64_t budget_ns;  // bound of every wait
     int32_t inject_stall;
+    int32_t spec_idx;    // 1: load the row's whole index list with the count
 };
 
 // Issues the gathers of keys [w0, w0 + wn) of this CTA into the window
@@ -49,6 +53,7 @@ struct MmaParams {
 __device__ __forceinline__ void gather_window(const MmaParams& p, uint32_t kv_s,
                                               const int32_t* idx_s, uint32_t bars, int w0,
                                               int wn, uint32_t bytes, uint64_t policy) {
+    // idx_s points at this CTA's first key.
     const int tid = threadIdx.x;
     if (tid == 0) {
         for (int c = 0; c * kChunk < wn; ++c) {
@@ -113,29 +118,37 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         // partials of this CTA's columns plus their sums.
         mbar_arrive_expect_tx(max_bar, (S - 1) * CH * 4);
         mbar_arrive_expect_tx(in_bar, (S - 1) * (CH * CW * 4 + CH * 4));
+        // (inject_stall: the barrier also expects 16 bytes nobody sends, so
+        // the bounded wait below runs out; a test hook for the timeout path.)
+        mbar_arrive_expect_tx(q_bar, CH * kRow + (p.inject_stall ? 16 : 0));
     }
     for (int h = tid; h < CH; h += kMmaThreads) lsum[h] = 0.f;
     __syncthreads();
     // Every CTA's barriers are armed before any peer pushes (waited below).
-    cluster_arrive_relaxed();
+    if (S > 1) cluster_arrive_relaxed();
 
-    // ---- this CTA's keys: [first, first + mine) of the row ------------------
-    const int W = p.a.W;
-    int n = p.a.counts[b];
-    n = max(min(n, W), 0);
-    const int per = (n + S - 1) / S;
-    const int first = min(n, split * per);
-    const int mine = min(n - first, per);
-    const int32_t* row_idx = p.a.indices + static_cast<int64_t>(b) * W + first;
-    for (int i = tid; i < mine; i += kMmaThreads) idx_s[i] = row_idx[i];
-
-    // (inject_stall: the barrier also expects 16 bytes nobody sends, so the
-    // bounded wait below runs out; a test hook for the timeout path.)
-    if (tid == 0) mbar_arrive_expect_tx(q_bar, CH * kRow + (p.inject_stall ? 16 : 0));
+    // The query rows depend on nothing: their copies go first.
     if (tid < CH) {
         const uint8_t* src = p.a.q + (static_cast<int64_t>(b) * p.a.H + head0 + tid) * kRow;
         bulk_g2s(q_s + tid * kRowPitch, src, kRow, q_bar);
     }
+
+    // ---- this CTA's keys: [first, first + mine) of the row ------------------
+    // With spec_idx the row's whole index list is loaded in the same round
+    // trip as its count (the loads do not depend on each other), so the
+    // gathers wait for one DRAM latency instead of two.
+    const int W = p.a.W;
+    const int32_t* row_idx = p.a.indices + static_cast<int64_t>(b) * W;
+    int n = p.a.counts[b];
+    if (p.spec_idx)
+        for (int i = tid; i < W; i += kMmaThreads) idx_s[i] = row_idx[i];
+    n = max(min(n, W), 0);
+    const int per = (n + S - 1) / S;
+    const int first = min(n, split * per);
+    const int mine = min(n - first, per);
+    if (!p.spec_idx)
+        for (int i = tid; i < mine; i += kMmaThreads) idx_s[i] = row_idx[first + i];
+    const int32_t* my_idx = idx_s + (p.spec_idx ? first : 0);
     __syncthreads();
 
     const uint64_t policy = policy_evict_normal();
@@ -156,7 +169,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         const int w0 = wi * p.window;
         const int wn = min(p.window, mine - w0);
         if (!__syncthreads_and(ok)) break;  // a failed CTA issues no more copies
-        gather_window(p, kv_s, idx_s, bars, w0, wn, kRow, policy);
+        gather_window(p, kv_s, my_idx, bars, w0, wn, kRow, policy);
         __syncthreads();  // zeroed tail rows
         for (int c = 0; c * kChunk < wn; ++c) {
             const int cnt = min(kChunk, wn - c * kChunk);
@@ -201,14 +214,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         if (lane == 0) maxima[split * CH + h] = mx;
     }
     __syncthreads();
-    cluster_wait();  // peers' barriers are initialised
-    if (tid < CH) {
-        const uint32_t v = __float_as_uint(maxima[split * CH + tid]);
-        const uint32_t slot = smem_addr(maxima + split * CH + tid);
-        for (int pr = 0; pr < S; ++pr)
-            if (pr != split) st_async_b32(mapa(slot, pr), v, mapa(max_bar, pr));
+    if (S > 1) {
+        cluster_wait();  // peers' barriers are initialised
+        if (tid < CH) {
+            const uint32_t v = __float_as_uint(maxima[split * CH + tid]);
+            const uint32_t slot = smem_addr(maxima + split * CH + tid);
+            for (int pr = 0; pr < S; ++pr)
+                if (pr != split) st_async_b32(mapa(slot, pr), v, mapa(max_bar, pr));
+        }
+        mbar_wait(max_bar, 0, ok, status, p.budget_ns, /*always=*/true);
     }
-    mbar_wait(max_bar, 0, ok, status, p.budget_ns, /*always=*/true);
     for (int h = tid; h < CH; h += kMmaThreads) {
         float m = neg_inf;
         for (int pr = 0; pr < S; ++pr) m = fmaxf(m, maxima[pr * CH + h]);
@@ -233,7 +248,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         const bool regather = (wi != nwin - 1);
         if (!__syncthreads_and(ok)) break;
         if (regather) {
-            gather_window(p, kv_s, idx_s, bars, w0, wn, kLatent, policy);
+            gather_window(p, kv_s, my_idx, bars, w0, wn, kLatent, policy);
             __syncthreads();
         }
         // Chunks in descending order too: the row's chunks are then summed in
@@ -285,6 +300,36 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         }
         __syncthreads();  // window buffer and P free for the next window
         fence_proxy_async();
+    }
+
+    if (S == 1) {
+        // No peers: BF16(acc * k_scale / total) straight from the registers
+        // (the same operations as the merge below with one partial).
+        if (ok) {
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int h = 16 * t + g + 8 * (e >> 1);
+                    const int col = 32 * warp + 8 * qd + 4 * (e & 1);
+                    const float total = 0.f + lsum[h];
+                    const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
+                    uint2 packed;
+                    packed.x = bf16x2((0.f + acc[t][0][e]) * inv, (0.f + acc[t][1][e]) * inv);
+                    packed.y = bf16x2((0.f + acc[t][2][e]) * inv, (0.f + acc[t][3][e]) * inv);
+                    uint16_t* dst =
+                        p.a.out + (static_cast<int64_t>(b) * p.a.H + head0 + h) * kLatent + col;
+                    *reinterpret_cast<uint2*>(dst) = packed;
+                }
+            }
+            for (int h = tid; h < CH; h += kMmaThreads) {
+                const float total = 0.f + lsum[h];
+                p.a.lse[static_cast<int64_t>(b) * p.a.H + head0 + h] =
+                    total > 0.f ? (rowmax[h] - p.log2_448 + log2f(total)) * 0.69314718055994530942f
+                                : -INFINITY;
+            }
+        }
+        return;
     }
 
     // ---- partials to the column owners (FP32 bits over DSMEM) ----------------
@@ -353,16 +398,36 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     }
 }
 
+// Function attributes are set once per device and kernel (and again only when
+// a launch needs more shared memory than was granted before).
+template <int T>
+int ensure_attributes(int smem_bytes, bool nonportable) {
+    static std::atomic<int> smem_set[kMaxDevices];
+    static std::atomic<int> np_set[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SMD_ERR_DEVICE;
+    auto kern = mma_decode_kernel<T>;
+    if (smem_bytes > smem_set[dev].load()) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
+            cudaSuccess)
+            return SMD_ERR_LAUNCH;
+        smem_set[dev].store(smem_bytes);
+    }
+    if (nonportable && !np_set[dev].load()) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+            cudaSuccess)
+            return SMD_ERR_LAUNCH;
+        np_set[dev].store(1);
+    }
+    return SMD_OK;
+}
+
 template <int T>
 int launch_t(const MmaParams& prm, const MmaConfig& cfg, const CallArgs& a, cudaStream_t stream) {
     auto kern = mma_decode_kernel<T>;
-    cudaError_t err =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.layout.total);
-    if (err != cudaSuccess) return SMD_ERR_LAUNCH;
-    if (cfg.split > 8) {
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-        if (err != cudaSuccess) return SMD_ERR_LAUNCH;
-    }
+    const int rc = ensure_attributes<T>(cfg.layout.total, cfg.split > 8);
+    if (rc != SMD_OK) return rc;
+    cudaError_t err;
     cudaLaunchConfig_t lc{};
     lc.gridDim = dim3(static_cast<unsigned>(a.H / (kHeadsPerTile * T) * cfg.split),
                       static_cast<unsigned>(a.B), 1);
@@ -396,6 +461,7 @@ int launch_mma(const CallArgs& a, const MmaConfig& cfg, cudaStream_t stream) {
     prm.log2_448 = static_cast<float>(std::log2(448.0));
     prm.budget_ns = cfg.wait_budget_ns;
     prm.inject_stall = cfg.inject_stall;
+    prm.spec_idx = cfg.spec_idx;
     switch (cfg.tiles) {
         case 1:
             return launch_t<1>(prm, cfg, a, stream);
