@@ -62,7 +62,9 @@ typedef enum {
 /* Kernel families. */
 enum {
     SMD_KERNEL_AUTO = 0,
-    SMD_KERNEL_MMA = 1   /* warp-level FP8 MMA, 16-head tiles */
+    SMD_KERNEL_MMA = 1,  /* warp-level FP8 MMA (mma.sync), 16-head tiles       */
+    SMD_KERNEL_TC = 2    /* tcgen05 + TMEM, 128 heads per CTA, TMA gather4;
+                            needs H % 128 == 0 and 1 <= W <= 2048             */
 };
 
 /* A launch plan: how the work is laid out. `split` decides which keys each
@@ -70,9 +72,11 @@ enum {
  * decide layout, and plans that differ only in them give identical bits. */
 typedef struct {
     int32_t kernel;      /* SMD_KERNEL_* */
-    int32_t split;       /* CTAs per cluster sharing one row: 1, 2, 4, 8, 16 */
-    int32_t tiles;       /* 16-head tiles per CTA (1 or 2)                   */
-    int32_t window;      /* keys resident in shared memory per pass (64k)    */
+    int32_t split;       /* CTAs per cluster sharing one row: 1, 2, 4, 8, 16
+                            (SMD_KERNEL_TC: 1, 2, 4)                         */
+    int32_t tiles;       /* 16-head tiles per CTA (1 or 2; TC: 8, fixed)     */
+    int32_t window;      /* keys resident in shared memory per pass (64k;
+                            TC: 128-key chunks, fixed)                       */
     /* testing hooks (0 = off); only smd_sparse_mla_decode_ex reads them:    */
     int32_t wait_budget_us; /* bound of every device wait (default 200 ms)   */
     int32_t inject_stall;   /* 1: the query barrier expects 16 bytes that no

@@ -22,6 +22,7 @@ SMD_ERR_DEVICE = -7
 
 SMD_KERNEL_AUTO = 0
 SMD_KERNEL_MMA = 1
+SMD_KERNEL_TC = 2
 
 
 class SmdPlan(ctypes.Structure):

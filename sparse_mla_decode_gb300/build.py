@@ -69,7 +69,7 @@ def build(force: bool = False, verbose: bool = False, extra: list[str] | None = 
     with concurrent.futures.ThreadPoolExecutor(max_workers=max(1, len(sources()))) as ex:
         objs = list(ex.map(compile_one, sources()))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcuda"]
+    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -62,7 +62,9 @@ int key_cap_limit(int tiles, int split, int window, int idx_cap) {
 // automatic choice. Returns an smd_status.
 int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_plan_t* out,
              MmaConfig* cfg) {
-    int tiles = (H % 32 == 0) ? 2 : 1;
+    // One 16-head tile per CTA by default: on GB300 the second tile's KV reuse
+    // is worth less than the extra cluster exchange and registers it costs.
+    int tiles = 1;
     if (force && force->tiles) tiles = force->tiles;
     if (tiles != 1 && tiles != 2) return SMD_ERR_PLAN;
     if (H % (kHeadsPerTile * tiles) != 0) return SMD_ERR_PLAN;
@@ -77,8 +79,10 @@ int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
         split = force->split;
         if (!is_split(split)) return SMD_ERR_PLAN;
     } else {
-        // Smallest split whose per-CTA share fits, then wider while the grid
-        // is under two waves and every CTA still gets >= 32 keys.
+        // Smallest split whose per-CTA share fits; then wider while the grid is
+        // under one wave and every CTA still gets >= 64 keys. A wider split
+        // shortens each CTA's gather but adds a cluster exchange of FP32
+        // partials, which is slow on this part (tens of GB/s per SM).
         for (int s = 1; s <= 16; s *= 2) {
             const int per = ceil_div(W, s);
             const int win = std::min(window_req, std::max(kChunk, ceil_div(per, kChunk) * kChunk));
@@ -88,7 +92,7 @@ int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
             }
         }
         if (split == 0) return SMD_ERR_SHAPE;
-        while (split < 16 && units * split < 2 * sm_count && ceil_div(W, split * 2) >= 32) split *= 2;
+        while (split < 16 && units * split < sm_count && ceil_div(W, split * 2) >= 64) split *= 2;
     }
     const int per = ceil_div(std::max(W, 1), split);
     const int window = std::min(window_req, std::max(kChunk, ceil_div(per, kChunk) * kChunk));
@@ -119,15 +123,60 @@ int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
     return SMD_OK;
 }
 
-int make_plan(int B, int H, int W, const smd_plan_t* force, smd_plan_t* out, MmaConfig* cfg) {
+bool tc_fits(int H, int W) {
+    return H % kTcHeads == 0 && W >= 1 && W <= kTcMaxSplit * kTcMaxKeys;
+}
+
+// The tcgen05 kernel's plan: the smallest cluster whose CTAs hold at most
+// kTcMaxKeys keys each (all of them resident in TMEM as logits).
+int plan_tc(int B, int H, int W, const smd_plan_t* force, smd_plan_t* out, TcConfig* cfg) {
+    if (!tc_fits(H, W)) return SMD_ERR_PLAN;
+    if (force && ((force->tiles && force->tiles != kTcHeads / kHeadsPerTile) ||
+                  (force->window && force->window != kTcChunk)))
+        return SMD_ERR_PLAN;
+    int split = 1;
+    while (ceil_div(W, split) > kTcMaxKeys) split *= 2;
+    if (force && force->split) {
+        if (force->split != 1 && force->split != 2 && force->split != 4) return SMD_ERR_PLAN;
+        if (ceil_div(W, force->split) > kTcMaxKeys) return SMD_ERR_PLAN;
+        split = force->split;
+    }
+    cfg->split = split;
+    cfg->wait_budget_ns = (force && force->wait_budget_us > 0)
+                              ? static_cast<uint64_t>(force->wait_budget_us) * 1000ull
+                              : kWaitBudgetNs;
+    cfg->inject_stall = (force && force->inject_stall) ? 1 : 0;
+    out->kernel = SMD_KERNEL_TC;
+    out->split = split;
+    out->tiles = kTcHeads / kHeadsPerTile;
+    out->window = kTcChunk;
+    out->key_cap = kTcMaxKeys;
+    out->grid_x = H / kTcHeads * split;
+    out->grid_y = B;
+    out->cluster_x = split;
+    out->threads = kTcThreads;
+    out->smem_bytes = tc_smem_bytes();
+    return SMD_OK;
+}
+
+struct AnyConfig {
+    int kernel;
+    MmaConfig mma;
+    TcConfig tc;
+};
+
+int make_plan(int B, int H, int W, const smd_plan_t* force, smd_plan_t* out, AnyConfig* cfg) {
     if (B < 0 || W < 0 || H <= 0 || H % kHeadsPerTile != 0) return SMD_ERR_SHAPE;
     static std::once_flag once;
     static DeviceInfo info;
     std::call_once(once, [] { info = query_device(); });
     const int sm_count = info.ok ? info.sm_count : 152;
-    const int kernel = (force && force->kernel) ? force->kernel : SMD_KERNEL_MMA;
-    if (kernel != SMD_KERNEL_MMA) return SMD_ERR_PLAN;
-    return plan_mma(B, H, W, sm_count, force, out, cfg);
+    int kernel = (force && force->kernel) ? force->kernel : SMD_KERNEL_AUTO;
+    if (kernel == SMD_KERNEL_AUTO) kernel = tc_fits(H, W) ? SMD_KERNEL_TC : SMD_KERNEL_MMA;
+    cfg->kernel = kernel;
+    if (kernel == SMD_KERNEL_MMA) return plan_mma(B, H, W, sm_count, force, out, &cfg->mma);
+    if (kernel == SMD_KERNEL_TC) return plan_tc(B, H, W, force, out, &cfg->tc);
+    return SMD_ERR_PLAN;
 }
 
 float scale_log2_of(float sm, float qs, float ks) {
@@ -152,7 +201,7 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
         return SMD_ERR_ALIGN;
 
     smd_plan_t plan{};
-    MmaConfig cfg{};
+    AnyConfig cfg{};
     const int rc = make_plan(B, H, W, force, &plan, &cfg);
     if (rc != SMD_OK) return rc;
 
@@ -170,7 +219,8 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
     a.out = out;
     a.lse = lse;
     a.status = status;
-    return launch_mma(a, cfg, reinterpret_cast<cudaStream_t>(stream));
+    if (cfg.kernel == SMD_KERNEL_TC) return launch_tc(a, cfg.tc, reinterpret_cast<cudaStream_t>(stream));
+    return launch_mma(a, cfg.mma, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -197,7 +247,7 @@ int smd_sparse_mla_decode_ex(const uint8_t* q, const uint8_t* kv_pool, int64_t N
 
 int smd_plan(int32_t B, int32_t H, int32_t W, smd_plan_t* plan) {
     if (!plan) return SMD_ERR_NULL;
-    smd::MmaConfig cfg{};
+    smd::AnyConfig cfg{};
     smd_plan_t p{};
     const int rc = smd::make_plan(B, H, W, nullptr, &p, &cfg);
     if (rc == SMD_OK) *plan = p;

@@ -95,4 +95,24 @@ struct MmaConfig {
 // Launches the warp-MMA kernel; returns an smd_status.
 int launch_mma(const CallArgs& a, const MmaConfig& cfg, cudaStream_t stream);
 
+// tcgen05 kernel: a CTA holds all heads of a 128-head group and at most
+// kTcMaxKeys keys of a row (their logits fill the 512 TMEM columns).
+constexpr int kTcHeads = 128;
+constexpr int kTcChunk = 128;    // keys per gathered chunk
+constexpr int kTcMaxKeys = 512;  // keys per CTA
+constexpr int kTcMaxSplit = 4;   // CTAs per cluster (the merge inbox must fit)
+constexpr int kTcThreads = 256;
+
+struct TcConfig {
+    int split;
+    uint64_t wait_budget_ns;
+    int inject_stall;
+};
+
+// Dynamic shared memory of the tcgen05 kernel (bytes).
+int tc_smem_bytes();
+
+// Launches the tcgen05 kernel; returns an smd_status.
+int launch_tc(const CallArgs& a, const TcConfig& cfg, cudaStream_t stream);
+
 }  // namespace smd

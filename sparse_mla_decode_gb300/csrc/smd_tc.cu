@@ -1,0 +1,593 @@
+// Sparse MLA decode on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// One CTA takes (query row b, a group of 128 heads, its share of the row's
+// keys: at most 512); the S CTAs of a cluster (S <= 4) split the row's keys
+// as the attn_sparse page's SparseDcpDecode does (per = ceil(n / S), CTA s
+// takes [s*per, s*per + per) clamped to n), and merge their FP32 partials in
+// CTA order (the page's merge method). The P anchor is the maximum over the
+// whole row: every CTA first computes the logits of all its keys, the CTAs
+// exchange their maxima, and only then is P formed (P = 2^(s - m + log2 448),
+// E4M3, FP32 sums of the unquantized P) and multiplied with V.
+//
+// All 128 heads of the group live in one CTA, so every gathered cache row is
+// read into shared memory once and used by all heads (M = 128 MMAs).
+//
+// Warp roles (256 threads):
+//   warp 0     producer: the row's count and key range, the query tile (2D
+//              TMA, 128-byte swizzle + 64-byte-swizzle tail) and 128-key
+//              chunks of cache rows (TMA tile::gather4, same swizzles) into
+//              a two-slot ring; in pass B it gathers again the V columns of
+//              chunks no longer resident.
+//   warp 1     MMA issuer: per chunk S = Q K^T (18 x M128 N128 K32 E4M3 MMAs)
+//              into TMEM columns 128c..128c+127; after P is ready, O = P V
+//              (M128 N256 K32 MMAs, V read MN-major from the same gathered
+//              tile) into TMEM columns 0..511, which the logits no longer need.
+//   warps 4-7  softmax and epilogue, thread h = head h = TMEM lane h: the
+//              row maximum (cluster exchange over DSMEM), P written straight
+//              into the K-major swizzled operand layout (over the dead query
+//              tile), then the partials of O go to their column owners over
+//              DSMEM and are merged in CTA order into BF16 out and the LSE.
+// Every wait on a copy, the tensor core or a peer is bounded.
+#include <cuda.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "smd_internal.h"
+#include "smd_ptx.cuh"
+
+namespace smd {
+namespace {
+
+constexpr int kBlock = 16384;       // one 128-byte-wide column block of 128 rows (SW128)
+constexpr int kTail = 8192;         // the 64-byte tail block of 128 rows (SW64)
+constexpr int kTile = 4 * kBlock + kTail;  // 576 columns x 128 rows
+constexpr int kOffQP = 0;           // query tile, later the P tiles (4 x 16 KB)
+constexpr int kOffRing = kTile;     // two chunk slots
+constexpr int kOffMax = 3 * kTile;  // [S][128] maxima
+constexpr int kOffSums = kOffMax + 4 * 128 * 4;  // [S][128] sums
+constexpr int kOffBars = kOffSums + 4 * 128 * 4;
+constexpr int kNumBars = 16;
+constexpr int kOffTmem = kOffBars + 8 * kNumBars;
+constexpr int kSmemUsed = kOffTmem + 16;
+constexpr int kSmemBytes = kSmemUsed + 1024;  // + alignment of the dynamic base to 1 KB
+
+// barrier indices. A slot's "free" signals of pass A (after QK) and of pass B
+// (after PV) use separate barriers, so that no barrier can complete twice
+// before the thread that waits on it has seen the first completion.
+constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = 3, kBarS = 5, kBarP = 9, kBarO = 10,
+              kBarMax = 11, kBarRdy = 12, kBarIn = 13, kBarFreeB = 14;
+
+struct TcMaps {
+    CUtensorMap q, q_tail, kv, kv_tail;
+};
+
+struct TcParams {
+    CallArgs a;
+    int32_t split;
+    float log2_448;
+    uint64_t budget_ns;
+    int32_t inject_stall;
+};
+
+struct Range {
+    int n, first, mine, nch;
+};
+
+__device__ __forceinline__ Range key_range(const TcParams& p, int b, int split) {
+    Range r;
+    int n = p.a.counts[b];
+    n = max(min(n, p.a.W), 0);
+    const int per = (n + p.split - 1) / p.split;
+    r.n = n;
+    r.first = min(n, split * per);
+    r.mine = min(n - r.first, per);
+    r.nch = (r.mine + kTcChunk - 1) / kTcChunk;
+    return r;
+}
+
+// Waits for the next completion of a barrier whose completions this thread
+// counts in `seen`.
+__device__ __forceinline__ void wait_next(uint32_t bar, uint32_t& seen, bool& ok, int32_t* status,
+                                          uint64_t budget) {
+    mbar_wait(bar, seen & 1u, ok, status, budget);
+    ++seen;
+}
+
+// ---- warp 0: TMA producer ----------------------------------------------------
+__device__ __forceinline__ void producer(const TcMaps& maps, const TcParams& p, uint32_t base,
+                                         uint32_t bars, int b, int group, int split, bool& ok) {
+    const int lane = threadIdx.x & 31;
+    const Range r = key_range(p, b, split);
+    if (lane == 0) {
+        const int y = b * p.a.H + group * kTcHeads;
+        for (int j = 0; j < 4; ++j)
+            tma_load_2d(base + kOffQP + j * kBlock, &maps.q, 128 * j, y, bars + 8 * kBarQ);
+        tma_load_2d(base + kOffQP + 4 * kBlock, &maps.q_tail, 512, y, bars + 8 * kBarQ);
+    }
+    // Lane l gathers rows 4l..4l+3 of every chunk; entries past the CTA's
+    // keys gather pool row 0 (a real row: finite bytes; its P is zero).
+    int rows[4][4];
+    const int32_t* idx = p.a.indices + static_cast<int64_t>(b) * p.a.W + r.first;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int pos = kTcChunk * c + 4 * lane + j;
+            rows[c][j] = (pos < r.mine) ? idx[pos] : 0;
+        }
+    // Completions of the pass-A "slot free" barriers (after QK of the slot's
+    // chunks, ascending) and of the pass-B ones (after PV, descending) seen.
+    uint32_t seen[2] = {0u, 0u};
+    uint32_t seen_b[2] = {0u, 0u};
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (c >= r.nch || !ok) break;
+        const int s = c & 1;
+        const uint32_t need = static_cast<uint32_t>(c >> 1);  // QK(c - 2) done: completion need-1
+        while (seen[s] < need) wait_next(bars + 8 * (kBarEmpty + s), seen[s], ok, p.a.status, p.budget_ns);
+        if (!ok) break;
+        const uint32_t slot = base + kOffRing + s * kTile;
+        if (lane == 0) mbar_arrive_expect_tx(bars + 8 * (kBarFull + s), kTile);
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            tma_gather4(slot + j * kBlock + 4 * lane * 128, &maps.kv, 128 * j, rows[c][0], rows[c][1],
+                        rows[c][2], rows[c][3], bars + 8 * (kBarFull + s));
+        tma_gather4(slot + 4 * kBlock + 4 * lane * 64, &maps.kv_tail, 512, rows[c][0], rows[c][1],
+                    rows[c][2], rows[c][3], bars + 8 * (kBarFull + s));
+    }
+    // Pass B visits chunks in descending order; the last two are resident, the
+    // others come back (V columns only) into their slot once PV of the chunk
+    // two above has released it.
+#pragma unroll
+    for (int c = 1; c >= 0; --c) {
+        if (c > r.nch - 3 || !ok) continue;
+        const int s = c & 1;
+        int later = 0;  // pass-B completions on slot s before PV(c + 2)
+        for (int c2 = r.nch - 1; c2 > c + 2; --c2) later += ((c2 & 1) == s);
+        const uint32_t need = static_cast<uint32_t>(later + 1);
+        while (seen_b[s] < need)
+            wait_next(bars + 8 * (kBarFreeB + s), seen_b[s], ok, p.a.status, p.budget_ns);
+        if (!ok) break;
+        const uint32_t slot = base + kOffRing + s * kTile;
+        if (lane == 0) mbar_arrive_expect_tx(bars + 8 * (kBarFull + s), 4 * kBlock);
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            tma_gather4(slot + j * kBlock + 4 * lane * 128, &maps.kv, 128 * j, rows[c][0], rows[c][1],
+                        rows[c][2], rows[c][3], bars + 8 * (kBarFull + s));
+    }
+}
+
+// ---- warp 1, one lane: MMA issuer ---------------------------------------------
+__device__ __forceinline__ void mma_issuer(const TcParams& p, uint32_t base, uint32_t bars,
+                                           uint32_t tmem, int b, int split, bool& ok) {
+    const Range r = key_range(p, b, split);
+    mbar_wait(bars + 8 * kBarQ, 0, ok, p.a.status, p.budget_ns);
+    tc_fence_after();
+    uint32_t full_seen[2] = {0u, 0u};
+    constexpr uint32_t kIdQK = umma_idesc_e4m3(128, kTcChunk, 0);
+    constexpr uint32_t kIdPV = umma_idesc_e4m3(128, 256, 1);
+    const uint32_t q_s = base + kOffQP;
+    // ---- pass A: S_c = Q K_c^T into TMEM columns 128c .. 128c + 127
+    for (int c = 0; c < r.nch && ok; ++c) {
+        const int s = c & 1;
+        wait_next(bars + 8 * (kBarFull + s), full_seen[s], ok, p.a.status, p.budget_ns);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t slot = base + kOffRing + s * kTile;
+        const uint32_t d = tmem + kTcChunk * c;
+        uint32_t acc = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                umma_e4m3(d, umma_desc(q_s + j * kBlock + 32 * kk, 16, 1024, 2),
+                          umma_desc(slot + j * kBlock + 32 * kk, 16, 1024, 2), kIdQK, acc);
+                acc = 1;
+            }
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+            umma_e4m3(d, umma_desc(q_s + 4 * kBlock + 32 * kk, 16, 512, 4),
+                      umma_desc(slot + 4 * kBlock + 32 * kk, 16, 512, 4), kIdQK, 1);
+        umma_commit(bars + 8 * (kBarS + c));
+        umma_commit(bars + 8 * (kBarEmpty + s));
+    }
+    // ---- P is in shared memory and every logit has been read out of TMEM.
+    mbar_wait(bars + 8 * kBarP, 0, ok, p.a.status, p.budget_ns);
+    tc_fence_after();
+    // ---- pass B: O = sum_c P_c V_c, chunks in descending order, O in TMEM
+    // columns 0..511 (two N = 256 halves). V is the MN-major operand: 128-byte
+    // latent chunks one column block (16 KB) apart, 8-key groups 1 KB apart.
+    for (int c = r.nch - 1; c >= 0 && ok; --c) {
+        const int s = c & 1;
+        if (c <= r.nch - 3) {
+            wait_next(bars + 8 * (kBarFull + s), full_seen[s], ok, p.a.status, p.budget_ns);
+            if (!ok) break;
+            tc_fence_after();
+        }
+        const uint32_t slot = base + kOffRing + s * kTile;
+        const uint32_t p_tile = base + kOffQP + c * kBlock;
+        const int cnt = min(kTcChunk, r.mine - kTcChunk * c);
+        const int ksteps = (cnt + 31) / 32;
+        for (int ks = 0; ks < ksteps; ++ks) {
+            const uint32_t acc = (c == r.nch - 1 && ks == 0) ? 0u : 1u;
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                umma_e4m3(tmem + 256 * h, umma_desc(p_tile + 32 * ks, 16, 1024, 2),
+                          umma_desc(slot + 2 * h * kBlock + ks * 4096, kBlock, 1024, 2), kIdPV, acc);
+        }
+        umma_commit(bars + 8 * (kBarFreeB + s));
+    }
+    umma_commit(bars + 8 * kBarO);
+}
+
+// ---- warps 4-7: softmax and epilogue (thread h = head h = TMEM lane h) ------------
+__device__ __forceinline__ void zero32(float (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+}
+
+// BF16(v * inv) of 32 columns -> 64 bytes at dst (16-byte aligned).
+__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32], float inv) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = bf16x2(v[2 * i] * inv, v[2 * i + 1] * inv);
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+__device__ __forceinline__ void epilogue(const TcParams& p, uint8_t* smem, uint32_t base,
+                                         uint32_t bars, uint32_t tmem, int b, int group, int split,
+                                         bool& ok) {
+    const int h = threadIdx.x - 128;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * ((threadIdx.x >> 5) & 3)) << 16);
+    const Range r = key_range(p, b, split);
+    const int S = p.split;
+    const float lam = p.a.scale_log2;
+    float* maxima = reinterpret_cast<float*>(smem + kOffMax);
+    float* sums = reinterpret_cast<float*>(smem + kOffSums);
+    int32_t* status = p.a.status;
+
+    // ---- the maximum of this CTA's scaled logits, chunk by chunk as QK lands
+    float m = -INFINITY;
+    for (int c = 0; c < r.nch; ++c) {
+        mbar_wait(bars + 8 * (kBarS + c), 0, ok, status, p.budget_ns);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const int cnt = min(kTcChunk, r.mine - kTcChunk * c);
+        for (int q = 0; 32 * q < cnt; ++q) {
+            float v[32];
+            tmem_ld32(lane_base + kTcChunk * c + 32 * q, v);
+            const int lim = cnt - 32 * q;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < lim) m = fmaxf(m, lam * v[j]);
+        }
+    }
+    // ---- the row maximum over the cluster
+    if (S > 1) {
+        cluster_wait();  // every peer's barriers are initialised
+        maxima[split * 128 + h] = m;
+        const uint32_t slot = smem_addr(maxima + split * 128 + h);
+        for (int pr = 0; pr < S; ++pr)
+            if (pr != split) st_async_b32(mapa(slot, pr), __float_as_uint(m), mapa(bars + 8 * kBarMax, pr));
+        mbar_wait(bars + 8 * kBarMax, 0, ok, status, p.budget_ns, /*always=*/true);
+        ok = __all_sync(0xffffffffu, ok);
+        for (int pr = 0; pr < S; ++pr) m = fmaxf(m, maxima[pr * 128 + h]);
+    }
+
+    // ---- P = 2^(s - m + log2 448) in E4M3 into the K-major 128-byte-swizzled
+    // A operand (row h, 16-byte chunk k stored at chunk k ^ (h & 7)); FP32 sum
+    // of the unquantized P in key order.
+    const float bias = m - p.log2_448;
+    float l = 0.f;
+    for (int c = 0; c < r.nch && ok; ++c) {
+        const int cnt = min(kTcChunk, r.mine - kTcChunk * c);
+        uint8_t* row = smem + kOffQP + c * kBlock + (h >> 3) * 1024 + (h & 7) * 128;
+        for (int q = 0; 32 * q < cnt; ++q) {
+            float v[32];
+            tmem_ld32(lane_base + kTcChunk * c + 32 * q, v);
+            const int lim = cnt - 32 * q;
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float pr[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = 4 * i + e;
+                    pr[e] = (j < lim) ? ex2_approx(lam * v[j] - bias) : 0.f;
+                    l += pr[e];
+                }
+                w[i] = static_cast<uint32_t>(e4m3x2(pr[0], pr[1])) |
+                       (static_cast<uint32_t>(e4m3x2(pr[2], pr[3])) << 16);
+            }
+            *reinterpret_cast<uint4*>(row + (((2 * q) ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(row + (((2 * q + 1) ^ (h & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+    }
+    fence_proxy_async();  // P (generic stores) -> the tensor core's reads
+    tc_fence_before();    // every logit read is complete
+    mbar_arrive_local(bars + 8 * kBarP);
+
+    mbar_wait(bars + 8 * kBarO, 0, ok, status, p.budget_ns);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    const bool have_o = ok && r.mine > 0;  // O in TMEM is defined only if PV ran
+    uint16_t* orow = p.a.out + (static_cast<int64_t>(b) * p.a.H + group * kTcHeads + h) * kLatent;
+    float* lse = p.a.lse + static_cast<int64_t>(b) * p.a.H + group * kTcHeads + h;
+
+    if (S == 1) {
+        if (ok) {
+            const float total = 0.f + l;
+            const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
+            for (int q = 0; q < kLatent / 32; ++q) {
+                float v[32];
+                if (have_o)
+                    tmem_ld32(lane_base + 32 * q, v);
+                else
+                    zero32(v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f + v[j];
+                store_bf16x32(orow + 32 * q, v, inv);
+            }
+            *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f : -INFINITY;
+        }
+        return;
+    }
+
+    // ---- partials of O to their column owners. Their inbox lies over this
+    // CTA's tiles, so a CTA accepts pushes only after its own PV is done.
+    const int CW = kLatent / S;
+    const int pitch = CW + 4;  // floats per inbox row: rows 4 banks apart
+    float* inbox = reinterpret_cast<float*>(smem);
+    if (h == 0)
+        for (int pr = 0; pr < S; ++pr)
+            if (pr != split) mbar_arrive_remote(mapa(bars + 8 * kBarRdy, pr));
+    mbar_wait(bars + 8 * kBarRdy, 0, ok, status, p.budget_ns, /*always=*/true);
+    ok = __all_sync(0xffffffffu, ok);
+    sums[split * 128 + h] = l;
+    const uint32_t sum_slot = smem_addr(sums + split * 128 + h);
+    for (int pr = 0; pr < S; ++pr) {
+        if (pr == split) continue;
+        const uint32_t rin = mapa(bars + 8 * kBarIn, pr);
+        st_async_b32(mapa(sum_slot, pr), __float_as_uint(l), rin);
+        const int src_slot = (split + S - pr - 1) % S;  // this CTA's slot among pr's sources
+        const uint32_t dst = smem_addr(inbox + (src_slot * 128 + h) * pitch);
+        for (int q = 0; q < CW / 32; ++q) {
+            float v[32];
+            if (have_o)
+                tmem_ld32(lane_base + pr * CW + 32 * q, v);
+            else
+                zero32(v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                st_async_v4(mapa(dst + (32 * q + 4 * i) * 4, pr),
+                            make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]), rin);
+        }
+    }
+    mbar_wait(bars + 8 * kBarIn, 0, ok, status, p.budget_ns, /*always=*/true);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return;
+
+    // ---- merge this CTA's columns in CTA order: BF16(sum * k_scale / total)
+    float total = 0.f;
+    for (int rk = 0; rk < S; ++rk) total += sums[rk * 128 + h];
+    const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
+    for (int q = 0; q < CW / 32; ++q) {
+        float own[32], acc[32];
+        if (have_o)
+            tmem_ld32(lane_base + split * CW + 32 * q, own);
+        else
+            zero32(own);
+        zero32(acc);
+        for (int rk = 0; rk < S; ++rk) {
+            if (rk == split) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc[j] += own[j];
+            } else {
+                const int src_slot = (rk + S - split - 1) % S;
+                const float4* src =
+                    reinterpret_cast<const float4*>(inbox + (src_slot * 128 + h) * pitch + 32 * q);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 x = src[i];
+                    acc[4 * i] += x.x;
+                    acc[4 * i + 1] += x.y;
+                    acc[4 * i + 2] += x.z;
+                    acc[4 * i + 3] += x.w;
+                }
+            }
+        }
+        store_bf16x32(orow + split * CW + 32 * q, acc, inv);
+    }
+    if (split == 0)
+        *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f : -INFINITY;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_decode_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const uint32_t base = smem_addr(smem);
+    const uint32_t bars = base + kOffBars;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = p.split;
+    const int split = static_cast<int>(cluster_ctarank());
+    const int group = blockIdx.x / S;
+    const int b = blockIdx.y;
+    bool ok = true;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bars + 8 * kBarQ, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bars + 8 * (kBarFull + i), 1);
+            mbar_init(bars + 8 * (kBarEmpty + i), 1);
+            mbar_init(bars + 8 * (kBarFreeB + i), 1);
+        }
+        for (int c = 0; c < 4; ++c) mbar_init(bars + 8 * (kBarS + c), 1);
+        mbar_init(bars + 8 * kBarP, 128);
+        mbar_init(bars + 8 * kBarO, 1);
+        mbar_init(bars + 8 * kBarMax, 1);
+        mbar_init(bars + 8 * kBarRdy, S > 1 ? S - 1 : 1);
+        mbar_init(bars + 8 * kBarIn, 1);
+        fence_mbar_init();
+        const int CW = kLatent / S;
+        // (inject_stall: the query barrier also expects 16 bytes nobody sends,
+        // so its bounded wait runs out; a test hook for the timeout path.)
+        mbar_arrive_expect_tx(bars + 8 * kBarQ, kTile + (p.inject_stall ? 16 : 0));
+        mbar_arrive_expect_tx(bars + 8 * kBarMax, (S - 1) * 128 * 4);
+        mbar_arrive_expect_tx(bars + 8 * kBarIn, (S - 1) * (128 * CW * 4 + 128 * 4));
+    }
+    if (warp == 1) tmem_alloc(base + kOffTmem, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmem);
+    if (S > 1) cluster_arrive_relaxed();
+
+    if (warp == 0) {
+        producer(maps, p, base, bars, b, group, split, ok);
+    } else if (warp == 1) {
+        if (lane == 0) mma_issuer(p, base, bars, tmem, b, split, ok);
+        __syncwarp();
+    } else if (warp >= 4) {
+        epilogue(p, smem, base, bars, tmem, b, group, split, ok);
+    }
+    if (S > 1 && warp < 4) cluster_wait();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_free(tmem, 512);
+    }
+}
+
+// ---- host ------------------------------------------------------------------------
+
+// A few encoded tensor maps, keyed by (tensor base, rows, box): encoding is a
+// host call of about a microsecond, and the cache pool / query buffers of a
+// decode loop do not move.
+struct MapEntry {
+    const void* ptr;
+    uint64_t rows;
+    uint32_t box_cols, box_rows;
+    CUtensorMap map;
+};
+
+std::mutex g_map_mu;
+MapEntry g_maps[16];
+int g_map_n = 0, g_map_next = 0;
+
+// cuTensorMapEncodeTiled, looked up through the runtime (the library does not
+// link the driver library, so it loads on machines without one).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+bool encode_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint32_t box_cols,
+                uint32_t box_rows) {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    for (int i = 0; i < g_map_n; ++i) {
+        const MapEntry& e = g_maps[i];
+        if (e.ptr == ptr && e.rows == rows && e.box_cols == box_cols && e.box_rows == box_rows) {
+            *out = e.map;
+            return true;
+        }
+    }
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRow), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRow)};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapSwizzle swz =
+        box_cols == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    EncodeTiledFn encode = encode_fn();
+    if (encode == nullptr) return false;
+    CUtensorMap m;
+    const CUresult r = encode(
+        &m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    MapEntry& e = g_maps[g_map_next];
+    e.ptr = ptr;
+    e.rows = rows;
+    e.box_cols = box_cols;
+    e.box_rows = box_rows;
+    e.map = m;
+    g_map_next = (g_map_next + 1) % 16;
+    if (g_map_n < 16) ++g_map_n;
+    *out = m;
+    return true;
+}
+
+constexpr int kMaxDevices = 64;
+
+}  // namespace
+
+int tc_smem_bytes() { return kSmemBytes; }
+
+int launch_tc(const CallArgs& a, const TcConfig& cfg, cudaStream_t stream) {
+    TcMaps maps;
+    const uint64_t qrows = static_cast<uint64_t>(a.B) * static_cast<uint64_t>(a.H);
+    if (!encode_map(&maps.q, a.q, qrows, 128, kTcHeads) ||
+        !encode_map(&maps.q_tail, a.q, qrows, 64, kTcHeads) ||
+        !encode_map(&maps.kv, a.kv, static_cast<uint64_t>(a.N), 128, 1) ||
+        !encode_map(&maps.kv_tail, a.kv, static_cast<uint64_t>(a.N), 64, 1))
+        return SMD_ERR_LAUNCH;
+    TcParams prm{};
+    prm.a = a;
+    prm.split = cfg.split;
+    prm.log2_448 = static_cast<float>(std::log2(448.0));
+    prm.budget_ns = cfg.wait_budget_ns;
+    prm.inject_stall = cfg.inject_stall;
+
+    static std::atomic<int> attr_set[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SMD_ERR_DEVICE;
+    if (!attr_set[dev].load()) {
+        if (cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemBytes) != cudaSuccess)
+            return SMD_ERR_LAUNCH;
+        attr_set[dev].store(1);
+    }
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(static_cast<unsigned>(a.H / kTcHeads * cfg.split), static_cast<unsigned>(a.B), 1);
+    lc.blockDim = dim3(kTcThreads, 1, 1);
+    lc.dynamicSmemBytes = static_cast<size_t>(kSmemBytes);
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cfg.split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lc, tc_decode_kernel, maps, prm) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SMD_ERR_LAUNCH;
+    }
+    return SMD_OK;
+}
+
+}  // namespace smd

@@ -97,6 +97,7 @@ def test_argument_checks(kw, code):
 @pytest.mark.parametrize("force", [
     dict(split=3), dict(split=32), dict(tiles=3), dict(tiles=4), dict(window=65),
     dict(window=4096), dict(kernel=9),
+    dict(kernel=2),                 # the tcgen05 kernel needs H % 128 == 0 (H = 16 here)
 ])
 def test_invalid_forced_plans_are_rejected(force):
     p = smd.SmdPlan()
@@ -107,9 +108,18 @@ def test_invalid_forced_plans_are_rejected(force):
 
 @pytest.mark.parametrize("B,H,W", [(2, 16, 64), (5, 64, 256), (64, 128, 2048), (256, 128, 2048),
                                    (128, 16, 8192), (1, 16, 0), (3, 48, 100), (7, 32, 1),
-                                   (1, 256, 4096), (4, 16, 16384)])
+                                   (1, 256, 4096), (4, 16, 16384), (3, 128, 100), (2, 256, 513),
+                                   (1, 128, 0), (2, 128, 2049)])
 def test_plan_invariants(B, H, W):
     p = smd.smd_plan(B, H, W).as_dict()
+    if H % 128 == 0 and 1 <= W <= 2048:
+        # tcgen05 kernel: 128 heads per CTA, <= 512 keys per CTA, cluster <= 4
+        assert p["kernel"] == smd.SMD_KERNEL_TC
+        assert p["split"] in (1, 2, 4) and -(-W // p["split"]) <= 512
+        assert p["split"] == 1 or -(-W // (p["split"] // 2)) > 512  # the smallest such split
+        assert p["grid_x"] == H // 128 * p["split"] and p["grid_y"] == B
+        assert p["threads"] == 256 and p["smem_bytes"] <= 227 * 1024
+        return
     assert p["kernel"] == smd.SMD_KERNEL_MMA
     assert p["split"] in (1, 2, 4, 8, 16) and p["cluster_x"] == p["split"]
     assert p["tiles"] in (1, 2) and H % (16 * p["tiles"]) == 0
@@ -132,3 +142,16 @@ def test_cpu_tensors_are_refused():
     with pytest.raises(ValueError, match="CUDA"):
         smd.sparse_mla_decode(q, kv, torch.zeros((1, 4), dtype=torch.int32),
                               torch.zeros(1, dtype=torch.int32), 0.1, 0.1, 0.1)
+
+
+@pytest.mark.parametrize("H,W,force", [
+    (128, 8, dict(kernel=2, split=8)),     # tcgen05 clusters hold at most 4 CTAs
+    (128, 2049, dict(kernel=2)),           # more than 4 x 512 keys
+    (128, 2048, dict(kernel=2, split=2)),  # 1024 keys per CTA do not fit in TMEM
+    (128, 64, dict(kernel=2, tiles=2)),    # the tcgen05 kernel's layout is fixed
+])
+def test_invalid_tc_plans_are_rejected(H, W, force):
+    p = smd.SmdPlan()
+    for k, v in force.items():
+        setattr(p, k, v)
+    assert call(H=H, W=W, force=p) == smd.SMD_ERR_PLAN
