@@ -101,7 +101,7 @@ constexpr int kTcHeads = 128;
 constexpr int kTcChunk = 128;    // keys per gathered chunk
 constexpr int kTcMaxKeys = 512;  // keys per CTA
 constexpr int kTcMaxSplit = 4;   // CTAs per cluster (the merge inbox must fit)
-constexpr int kTcThreads = 256;
+constexpr int kTcThreads = 512;
 
 struct TcConfig {
     int split;

@@ -12,21 +12,22 @@
 // All 128 heads of the group live in one CTA, so every gathered cache row is
 // read into shared memory once and used by all heads (M = 128 MMAs).
 //
-// Warp roles (256 threads):
-//   warp 0     producer: the row's count and key range, the query tile (2D
-//              TMA, 128-byte swizzle + 64-byte-swizzle tail) and 128-key
-//              chunks of cache rows (TMA tile::gather4, same swizzles) into
-//              a two-slot ring; in pass B it gathers again the V columns of
-//              chunks no longer resident.
-//   warp 1     MMA issuer: per chunk S = Q K^T (18 x M128 N128 K32 E4M3 MMAs)
-//              into TMEM columns 128c..128c+127; after P is ready, O = P V
-//              (M128 N256 K32 MMAs, V read MN-major from the same gathered
-//              tile) into TMEM columns 0..511, which the logits no longer need.
-//   warps 4-7  softmax and epilogue, thread h = head h = TMEM lane h: the
-//              row maximum (cluster exchange over DSMEM), P written straight
-//              into the K-major swizzled operand layout (over the dead query
-//              tile), then the partials of O go to their column owners over
-//              DSMEM and are merged in CTA order into BF16 out and the LSE.
+// Warp roles (512 threads):
+//   warps 0-7   producers: the row's count and key range, the query tile (2D
+//               TMA, 128-byte swizzle + 64-byte-swizzle tail) and 128-key
+//               chunks of cache rows (TMA tile::gather4, same swizzles, one
+//               issue per thread) into a two-slot ring; in pass B they gather
+//               again the V columns of chunks no longer resident.
+//   warp 8      MMA issuer: per chunk S = Q K^T (18 x M128 N128 K32 E4M3 MMAs)
+//               into TMEM columns 128c..128c+127; after P is ready, O = P V
+//               (M128 N256 K32 MMAs, V read MN-major from the same gathered
+//               tile) into TMEM columns 0..511, which the logits no longer need.
+//   warps 12-15 softmax, thread h = head h = TMEM lane h: the row maximum
+//               (cluster exchange over DSMEM), P written straight into the
+//               K-major swizzled operand layout over the dead query tile.
+//   all warps   once O is complete: the partials of O go to their column
+//               owners over DSMEM and are merged in CTA order into BF16 out
+//               and the LSE (four warps per TMEM lane quarter).
 // Every wait on a copy, the tensor core or a peer is bounded.
 #include <cuda.h>
 
@@ -49,7 +50,9 @@ constexpr int kOffQP = 0;           // query tile, later the P tiles (4 x 16 KB)
 constexpr int kOffRing = kTile;     // two chunk slots
 constexpr int kOffMax = 3 * kTile;  // [S][128] maxima
 constexpr int kOffSums = kOffMax + 4 * 128 * 4;  // [S][128] sums
-constexpr int kOffBars = kOffSums + 4 * 128 * 4;
+constexpr int kOffRowMax = kOffSums + 4 * 128 * 4;  // [128] the row maxima
+constexpr int kOffIdx = kOffRowMax + 128 * 4;        // [512] this CTA's key indices
+constexpr int kOffBars = kOffIdx + kTcMaxKeys * 4;
 constexpr int kNumBars = 16;
 constexpr int kOffTmem = kOffBars + 8 * kNumBars;
 constexpr int kSmemUsed = kOffTmem + 16;
@@ -97,53 +100,55 @@ __device__ __forceinline__ void wait_next(uint32_t bar, uint32_t& seen, bool& ok
     ++seen;
 }
 
-// ---- warp 0: TMA producer ----------------------------------------------------
-__device__ __forceinline__ void producer(const TcMaps& maps, const TcParams& p, uint32_t base,
-                                         uint32_t bars, int b, int group, int split, bool& ok) {
-    const int lane = threadIdx.x & 31;
+// ---- warps 0-7: TMA producers -------------------------------------------------
+// One TMA issue per thread per chunk: a single warp issuing all of a chunk's
+// 160 gathers is limited by the issue rate (well below HBM bandwidth).
+constexpr int kProducerThreads = 256;
+
+__device__ __forceinline__ void producer(const TcMaps& maps, const TcParams& p, uint8_t* smem,
+                                         uint32_t base, uint32_t bars, int b, int group, int split,
+                                         bool& ok) {
+    const int t = threadIdx.x;
     const Range r = key_range(p, b, split);
-    if (lane == 0) {
+    if (t == 0) {
         const int y = b * p.a.H + group * kTcHeads;
         for (int j = 0; j < 4; ++j)
             tma_load_2d(base + kOffQP + j * kBlock, &maps.q, 128 * j, y, bars + 8 * kBarQ);
         tma_load_2d(base + kOffQP + 4 * kBlock, &maps.q_tail, 512, y, bars + 8 * kBarQ);
     }
-    // Lane l gathers rows 4l..4l+3 of every chunk; entries past the CTA's
-    // keys gather pool row 0 (a real row: finite bytes; its P is zero).
-    int rows[4][4];
+    // This CTA's key indices; entries past its keys name pool row 0 (a real
+    // row: finite bytes; its P is zero).
+    int32_t* idx_s = reinterpret_cast<int32_t*>(smem + kOffIdx);
     const int32_t* idx = p.a.indices + static_cast<int64_t>(b) * p.a.W + r.first;
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int pos = kTcChunk * c + 4 * lane + j;
-            rows[c][j] = (pos < r.mine) ? idx[pos] : 0;
-        }
+    for (int i = t; i < kTcMaxKeys; i += kProducerThreads) idx_s[i] = (i < r.mine) ? idx[i] : 0;
+    asm volatile("bar.sync 1, %0;" ::"r"(kProducerThreads) : "memory");
+
     // Completions of the pass-A "slot free" barriers (after QK of the slot's
     // chunks, ascending) and of the pass-B ones (after PV, descending) seen.
     uint32_t seen[2] = {0u, 0u};
     uint32_t seen_b[2] = {0u, 0u};
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        if (c >= r.nch || !ok) break;
+    // Pass A: chunk c: thread t < 160 issues piece t % 5 (four 128-byte column
+    // blocks and the 64-byte tail) of rows 4g..4g+3, g = t / 5.
+    for (int c = 0; c < r.nch && ok; ++c) {
         const int s = c & 1;
-        const uint32_t need = static_cast<uint32_t>(c >> 1);  // QK(c - 2) done: completion need-1
+        const uint32_t need = static_cast<uint32_t>(c >> 1);  // QK(c - 2) has released the slot
         while (seen[s] < need) wait_next(bars + 8 * (kBarEmpty + s), seen[s], ok, p.a.status, p.budget_ns);
         if (!ok) break;
         const uint32_t slot = base + kOffRing + s * kTile;
-        if (lane == 0) mbar_arrive_expect_tx(bars + 8 * (kBarFull + s), kTile);
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            tma_gather4(slot + j * kBlock + 4 * lane * 128, &maps.kv, 128 * j, rows[c][0], rows[c][1],
-                        rows[c][2], rows[c][3], bars + 8 * (kBarFull + s));
-        tma_gather4(slot + 4 * kBlock + 4 * lane * 64, &maps.kv_tail, 512, rows[c][0], rows[c][1],
-                    rows[c][2], rows[c][3], bars + 8 * (kBarFull + s));
+        const uint32_t full = bars + 8 * (kBarFull + s);
+        if (t == 0) mbar_arrive_expect_tx(full, kTile);
+        if (t < 160) {
+            const int g = t / 5, j = t % 5;
+            const int32_t* rw = idx_s + kTcChunk * c + 4 * g;
+            if (j < 4)
+                tma_gather4(slot + j * kBlock + 4 * g * 128, &maps.kv, 128 * j, rw[0], rw[1], rw[2], rw[3], full);
+            else
+                tma_gather4(slot + 4 * kBlock + 4 * g * 64, &maps.kv_tail, 512, rw[0], rw[1], rw[2], rw[3], full);
+        }
     }
     // Pass B visits chunks in descending order; the last two are resident, the
     // others come back (V columns only) into their slot once PV of the chunk
     // two above has released it.
-#pragma unroll
     for (int c = 1; c >= 0; --c) {
         if (c > r.nch - 3 || !ok) continue;
         const int s = c & 1;
@@ -154,12 +159,13 @@ __device__ __forceinline__ void producer(const TcMaps& maps, const TcParams& p, 
             wait_next(bars + 8 * (kBarFreeB + s), seen_b[s], ok, p.a.status, p.budget_ns);
         if (!ok) break;
         const uint32_t slot = base + kOffRing + s * kTile;
-        if (lane == 0) mbar_arrive_expect_tx(bars + 8 * (kBarFull + s), 4 * kBlock);
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            tma_gather4(slot + j * kBlock + 4 * lane * 128, &maps.kv, 128 * j, rows[c][0], rows[c][1],
-                        rows[c][2], rows[c][3], bars + 8 * (kBarFull + s));
+        const uint32_t full = bars + 8 * (kBarFull + s);
+        if (t == 0) mbar_arrive_expect_tx(full, 4 * kBlock);
+        if (t < 128) {
+            const int g = t / 4, j = t % 4;
+            const int32_t* rw = idx_s + kTcChunk * c + 4 * g;
+            tma_gather4(slot + j * kBlock + 4 * g * 128, &maps.kv, 128 * j, rw[0], rw[1], rw[2], rw[3], full);
+        }
     }
 }
 
@@ -242,19 +248,23 @@ __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32
     for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
-__device__ __forceinline__ void epilogue(const TcParams& p, uint8_t* smem, uint32_t base,
-                                         uint32_t bars, uint32_t tmem, int b, int group, int split,
-                                         bool& ok) {
-    const int h = threadIdx.x - 128;
+// ---- warps 12-15: softmax (thread h = head h = TMEM lane h) ----------------------
+// The row maximum (cluster exchange over DSMEM), then P in E4M3 into the K-major
+// 128-byte-swizzled A operand (row h, 16-byte chunk k stored at chunk
+// k ^ (h & 7)) and the FP32 sum of the unquantized P in key order. Leaves the
+// row maximum and the sum in shared memory for the finish.
+__device__ __forceinline__ void softmax(const TcParams& p, uint8_t* smem, uint32_t bars,
+                                        uint32_t tmem, int b, int split, bool& ok) {
+    const int h = threadIdx.x & 127;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * ((threadIdx.x >> 5) & 3)) << 16);
     const Range r = key_range(p, b, split);
     const int S = p.split;
     const float lam = p.a.scale_log2;
     float* maxima = reinterpret_cast<float*>(smem + kOffMax);
     float* sums = reinterpret_cast<float*>(smem + kOffSums);
+    float* rowmax = reinterpret_cast<float*>(smem + kOffRowMax);
     int32_t* status = p.a.status;
 
-    // ---- the maximum of this CTA's scaled logits, chunk by chunk as QK lands
     float m = -INFINITY;
     for (int c = 0; c < r.nch; ++c) {
         mbar_wait(bars + 8 * (kBarS + c), 0, ok, status, p.budget_ns);
@@ -271,7 +281,6 @@ __device__ __forceinline__ void epilogue(const TcParams& p, uint8_t* smem, uint3
                 if (j < lim) m = fmaxf(m, lam * v[j]);
         }
     }
-    // ---- the row maximum over the cluster
     if (S > 1) {
         cluster_wait();  // every peer's barriers are initialised
         maxima[split * 128 + h] = m;
@@ -282,10 +291,8 @@ __device__ __forceinline__ void epilogue(const TcParams& p, uint8_t* smem, uint3
         ok = __all_sync(0xffffffffu, ok);
         for (int pr = 0; pr < S; ++pr) m = fmaxf(m, maxima[pr * 128 + h]);
     }
+    rowmax[h] = m;
 
-    // ---- P = 2^(s - m + log2 448) in E4M3 into the K-major 128-byte-swizzled
-    // A operand (row h, 16-byte chunk k stored at chunk k ^ (h & 7)); FP32 sum
-    // of the unquantized P in key order.
     const float bias = m - p.log2_448;
     float l = 0.f;
     for (int c = 0; c < r.nch && ok; ++c) {
@@ -312,13 +319,27 @@ __device__ __forceinline__ void epilogue(const TcParams& p, uint8_t* smem, uint3
             *reinterpret_cast<uint4*>(row + (((2 * q + 1) ^ (h & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
         }
     }
+    sums[split * 128 + h] = l;
     fence_proxy_async();  // P (generic stores) -> the tensor core's reads
     tc_fence_before();    // every logit read is complete
     mbar_arrive_local(bars + 8 * kBarP);
+}
 
-    mbar_wait(bars + 8 * kBarO, 0, ok, status, p.budget_ns);
-    ok = __all_sync(0xffffffffu, ok);
-    tc_fence_after();
+// ---- all 16 warps: partial exchange, merge and output -----------------------------
+// Warp w serves TMEM lane quarter w % 4 (heads 32(w % 4) .. +31) and column
+// group w / 4 of every column range it handles.
+__device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_t bars,
+                                       uint32_t tmem, int b, int group, int split, bool& ok) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = 32 * (warp & 3) + lane;
+    const int cg = warp >> 2;  // column group 0..3
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    const Range r = key_range(p, b, split);
+    const int S = p.split;
+    float* sums = reinterpret_cast<float*>(smem + kOffSums);
+    const float m = reinterpret_cast<const float*>(smem + kOffRowMax)[h];
+    const float l = sums[split * 128 + h];
+    int32_t* status = p.a.status;
     const bool have_o = ok && r.mine > 0;  // O in TMEM is defined only if PV ran
     uint16_t* orow = p.a.out + (static_cast<int64_t>(b) * p.a.H + group * kTcHeads + h) * kLatent;
     float* lse = p.a.lse + static_cast<int64_t>(b) * p.a.H + group * kTcHeads + h;
@@ -327,43 +348,46 @@ __device__ __forceinline__ void epilogue(const TcParams& p, uint8_t* smem, uint3
         if (ok) {
             const float total = 0.f + l;
             const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
-            for (int q = 0; q < kLatent / 32; ++q) {
+            for (int q = 0; q < kLatent / 128; ++q) {
+                const int col = cg * (kLatent / 4) + 32 * q;
                 float v[32];
                 if (have_o)
-                    tmem_ld32(lane_base + 32 * q, v);
+                    tmem_ld32(lane_base + col, v);
                 else
                     zero32(v);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.f + v[j];
-                store_bf16x32(orow + 32 * q, v, inv);
+                store_bf16x32(orow + col, v, inv);
             }
-            *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f : -INFINITY;
+            if (cg == 0)
+                *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f
+                                   : -INFINITY;
         }
         return;
     }
 
-    // ---- partials of O to their column owners. Their inbox lies over this
-    // CTA's tiles, so a CTA accepts pushes only after its own PV is done.
-    const int CW = kLatent / S;
-    const int pitch = CW + 4;  // floats per inbox row: rows 4 banks apart
+    // Partials of O go to their column owners; the inbox lies over this CTA's
+    // tiles, so a CTA accepts pushes only after its own PV is done.
+    const int CW = kLatent / S;       // columns per owner
+    const int GW = CW / 4;            // columns per column group
+    const int pitch = CW + 4;         // floats per inbox row: rows 4 banks apart
     float* inbox = reinterpret_cast<float*>(smem);
-    if (h == 0)
+    if (threadIdx.x == 0)
         for (int pr = 0; pr < S; ++pr)
             if (pr != split) mbar_arrive_remote(mapa(bars + 8 * kBarRdy, pr));
     mbar_wait(bars + 8 * kBarRdy, 0, ok, status, p.budget_ns, /*always=*/true);
     ok = __all_sync(0xffffffffu, ok);
-    sums[split * 128 + h] = l;
     const uint32_t sum_slot = smem_addr(sums + split * 128 + h);
     for (int pr = 0; pr < S; ++pr) {
         if (pr == split) continue;
         const uint32_t rin = mapa(bars + 8 * kBarIn, pr);
-        st_async_b32(mapa(sum_slot, pr), __float_as_uint(l), rin);
+        if (cg == 0) st_async_b32(mapa(sum_slot, pr), __float_as_uint(l), rin);
         const int src_slot = (split + S - pr - 1) % S;  // this CTA's slot among pr's sources
-        const uint32_t dst = smem_addr(inbox + (src_slot * 128 + h) * pitch);
-        for (int q = 0; q < CW / 32; ++q) {
+        const uint32_t dst = smem_addr(inbox + (src_slot * 128 + h) * pitch + cg * GW);
+        for (int q = 0; q < GW / 32; ++q) {
             float v[32];
             if (have_o)
-                tmem_ld32(lane_base + pr * CW + 32 * q, v);
+                tmem_ld32(lane_base + pr * CW + cg * GW + 32 * q, v);
             else
                 zero32(v);
 #pragma unroll
@@ -376,14 +400,15 @@ __device__ __forceinline__ void epilogue(const TcParams& p, uint8_t* smem, uint3
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) return;
 
-    // ---- merge this CTA's columns in CTA order: BF16(sum * k_scale / total)
+    // Merge this CTA's columns in CTA order: BF16(sum * k_scale / total).
     float total = 0.f;
     for (int rk = 0; rk < S; ++rk) total += sums[rk * 128 + h];
     const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
-    for (int q = 0; q < CW / 32; ++q) {
+    for (int q = 0; q < GW / 32; ++q) {
+        const int col = split * CW + cg * GW + 32 * q;
         float own[32], acc[32];
         if (have_o)
-            tmem_ld32(lane_base + split * CW + 32 * q, own);
+            tmem_ld32(lane_base + col, own);
         else
             zero32(own);
         zero32(acc);
@@ -393,8 +418,8 @@ __device__ __forceinline__ void epilogue(const TcParams& p, uint8_t* smem, uint3
                 for (int j = 0; j < 32; ++j) acc[j] += own[j];
             } else {
                 const int src_slot = (rk + S - split - 1) % S;
-                const float4* src =
-                    reinterpret_cast<const float4*>(inbox + (src_slot * 128 + h) * pitch + 32 * q);
+                const float4* src = reinterpret_cast<const float4*>(
+                    inbox + (src_slot * 128 + h) * pitch + cg * GW + 32 * q);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float4 x = src[i];
@@ -405,9 +430,9 @@ __device__ __forceinline__ void epilogue(const TcParams& p, uint8_t* smem, uint3
                 }
             }
         }
-        store_bf16x32(orow + split * CW + 32 * q, acc, inv);
+        store_bf16x32(orow + col, acc, inv);
     }
-    if (split == 0)
+    if (split == 0 && cg == 0)
         *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f : -INFINITY;
 }
 
@@ -445,25 +470,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_arrive_expect_tx(bars + 8 * kBarMax, (S - 1) * 128 * 4);
         mbar_arrive_expect_tx(bars + 8 * kBarIn, (S - 1) * (128 * CW * 4 + 128 * 4));
     }
-    if (warp == 1) tmem_alloc(base + kOffTmem, 512);
+    if (warp == 8) tmem_alloc(base + kOffTmem, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmem);
     if (S > 1) cluster_arrive_relaxed();
 
-    if (warp == 0) {
-        producer(maps, p, base, bars, b, group, split, ok);
-    } else if (warp == 1) {
+    if (warp < 8) {
+        producer(maps, p, smem, base, bars, b, group, split, ok);
+    } else if (warp == 8) {
         if (lane == 0) mma_issuer(p, base, bars, tmem, b, split, ok);
         __syncwarp();
-    } else if (warp >= 4) {
-        epilogue(p, smem, base, bars, tmem, b, group, split, ok);
+    } else if (warp >= 12) {
+        softmax(p, smem, bars, tmem, b, split, ok);
     }
-    if (S > 1 && warp < 4) cluster_wait();
+    // Every warp: O is complete in TMEM; then the exchange and the merge.
+    mbar_wait(bars + 8 * kBarO, 0, ok, p.a.status, p.budget_ns);
+    tc_fence_after();
+    if (S > 1 && warp < 12) cluster_wait();  // the softmax warps waited before their max exchange
+    ok = __syncthreads_and(ok) != 0;         // the sums and row maxima are visible; one verdict
+    finish(p, smem, bars, tmem, b, group, split, ok);
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == 8) {
         tc_fence_after();
         tmem_free(tmem, 512);
     }

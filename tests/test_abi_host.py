@@ -118,7 +118,7 @@ def test_plan_invariants(B, H, W):
         assert p["split"] in (1, 2, 4) and -(-W // p["split"]) <= 512
         assert p["split"] == 1 or -(-W // (p["split"] // 2)) > 512  # the smallest such split
         assert p["grid_x"] == H // 128 * p["split"] and p["grid_y"] == B
-        assert p["threads"] == 256 and p["smem_bytes"] <= 227 * 1024
+        assert p["threads"] == 512 and p["smem_bytes"] <= 227 * 1024
         return
     assert p["kernel"] == smd.SMD_KERNEL_MMA
     assert p["split"] in (1, 2, 4, 8, 16) and p["cluster_x"] == p["split"]
