@@ -56,7 +56,10 @@ typedef enum {
     SMD_ERR_LAUNCH = -4,  /* the CUDA launch failed (cudaGetLastError)        */
     SMD_ERR_TIMEOUT = -5, /* device status: a bounded wait ran out            */
     SMD_ERR_PLAN = -6,    /* a forced plan is invalid for these shapes        */
-    SMD_ERR_DEVICE = -7   /* no usable sm_103 device / attribute query failed */
+    SMD_ERR_DEVICE = -7,  /* no usable sm_103 device / attribute query failed;
+                             device status: an SM id beyond the workspace    */
+    SMD_ERR_WORKSPACE = -8 /* workspace given but smaller than
+                             smd_workspace_bytes() or not 16-byte aligned    */
 } smd_status;
 
 /* Kernel families. */
@@ -118,14 +121,38 @@ int smd_sparse_mla_decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
  * device. Host only; touches no device memory. */
 int smd_plan(int32_t B, int32_t H, int32_t W, smd_plan_t* plan);
 
-/* As smd_sparse_mla_decode, with the plan fields kernel/split/tiles/window
- * taken from `force` (0 = the automatic choice for that field). Used by the
- * tests to run every layout variant; `force` may be NULL. */
+/* Bytes of workspace smd_sparse_mla_decode_ws can use for (B, H, W): 0 when
+ * the plan merges its split partials on chip only (then a workspace is not
+ * needed), else the size of the L2 exchange workspace (one slot of FP32
+ * partials per SM id; about 48 MiB). Host only. */
+int64_t smd_workspace_bytes(int32_t B, int32_t H, int32_t W);
+
+/* As smd_sparse_mla_decode, with a caller-owned device workspace. When the
+ * plan splits rows over a cluster of tcgen05 CTAs, their FP32 partials are
+ * exchanged through this workspace (L2) instead of distributed shared
+ * memory, which is faster on GB300. workspace may be NULL (the on-chip
+ * exchange is used); otherwise it must be 16-byte aligned and at least
+ * smd_workspace_bytes(B, H, W) long (else SMD_ERR_WORKSPACE). Its contents
+ * need no initialisation and are scratch; calls that overlap on the GPU
+ * must not share one workspace. */
+int smd_sparse_mla_decode_ws(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
+                             const int32_t* indices, int32_t W, const int32_t* counts,
+                             int32_t B, int32_t H,
+                             float sm_scale, float q_scale, float k_scale,
+                             uint16_t* out, float* lse, int32_t* status,
+                             void* workspace, int64_t workspace_bytes,
+                             smd_stream_t stream);
+
+/* As smd_sparse_mla_decode_ws, with the plan fields kernel/split/tiles/window
+ * (and the testing hooks) taken from `force` (0 = the automatic choice for
+ * that field). Used by the tests to run every variant; `force` and
+ * `workspace` may be NULL. */
 int smd_sparse_mla_decode_ex(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
                              const int32_t* indices, int32_t W, const int32_t* counts,
                              int32_t B, int32_t H,
                              float sm_scale, float q_scale, float k_scale,
                              uint16_t* out, float* lse, int32_t* status,
+                             void* workspace, int64_t workspace_bytes,
                              smd_stream_t stream, const smd_plan_t* force);
 
 /* The base-2 logit scale the kernels use: fp32(sm*q_s*k_s*log2 e),

@@ -19,6 +19,7 @@ SMD_ERR_LAUNCH = -4
 SMD_ERR_TIMEOUT = -5
 SMD_ERR_PLAN = -6
 SMD_ERR_DEVICE = -7
+SMD_ERR_WORKSPACE = -8
 
 SMD_KERNEL_AUTO = 0
 SMD_KERNEL_MMA = 1
@@ -64,8 +65,13 @@ def lib() -> ctypes.CDLL:
             so = ctypes.CDLL(path)
             so.smd_sparse_mla_decode.restype = ctypes.c_int
             so.smd_sparse_mla_decode.argtypes = _DECODE_ARGS
+            ws_args = _DECODE_ARGS[:-1] + [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+            so.smd_sparse_mla_decode_ws.restype = ctypes.c_int
+            so.smd_sparse_mla_decode_ws.argtypes = ws_args
             so.smd_sparse_mla_decode_ex.restype = ctypes.c_int
-            so.smd_sparse_mla_decode_ex.argtypes = _DECODE_ARGS + [ctypes.POINTER(SmdPlan)]
+            so.smd_sparse_mla_decode_ex.argtypes = ws_args + [ctypes.POINTER(SmdPlan)]
+            so.smd_workspace_bytes.restype = ctypes.c_int64
+            so.smd_workspace_bytes.argtypes = [ctypes.c_int32] * 3
             so.smd_plan.restype = ctypes.c_int
             so.smd_plan.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                     ctypes.POINTER(SmdPlan)]
@@ -91,11 +97,24 @@ def smd_sparse_mla_decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_s
                                        q_scale, k_scale, out, lse, status, stream)
 
 
+def smd_sparse_mla_decode_ws(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale,
+                             out, lse, status, workspace, workspace_bytes, stream) -> int:
+    return lib().smd_sparse_mla_decode_ws(q, kv_pool, N, indices, W, counts, B, H, sm_scale,
+                                          q_scale, k_scale, out, lse, status, workspace,
+                                          workspace_bytes, stream)
+
+
 def smd_sparse_mla_decode_ex(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale,
-                             out, lse, status, stream, force: SmdPlan | None) -> int:
+                             out, lse, status, workspace, workspace_bytes, stream,
+                             force: SmdPlan | None) -> int:
     ref = ctypes.byref(force) if force is not None else None
     return lib().smd_sparse_mla_decode_ex(q, kv_pool, N, indices, W, counts, B, H, sm_scale,
-                                          q_scale, k_scale, out, lse, status, stream, ref)
+                                          q_scale, k_scale, out, lse, status, workspace,
+                                          workspace_bytes, stream, ref)
+
+
+def smd_workspace_bytes(B: int, H: int, W: int) -> int:
+    return int(lib().smd_workspace_bytes(B, H, W))
 
 
 def smd_plan(B: int, H: int, W: int) -> SmdPlan:
@@ -135,12 +154,14 @@ def _bytes_view(t, name: str):
 
 def sparse_mla_decode(q, kv_pool, indices, counts, sm_scale: float, q_scale: float,
                       k_scale: float, out=None, lse=None, status=None, stream=None,
-                      plan: SmdPlan | dict | None = None):
+                      plan: SmdPlan | dict | None = None, workspace=None):
     """Decode on the GPU. q [B,H,576] and kv_pool [N,576] E4M3 (uint8 or
     float8_e4m3fn), indices [B,W] int32, counts [B] int32, all CUDA tensors.
     Returns (out [B,H,512] bfloat16, lse [B,H] float32). ``plan`` forces
     plan fields (smd_sparse_mla_decode_ex); ``status`` is an optional int32
-    CUDA tensor that receives device-side errors."""
+    CUDA tensor that receives device-side errors; ``workspace`` an optional
+    CUDA tensor of at least smd_workspace_bytes(B, H, W) bytes for the L2
+    exchange of split partials."""
     import torch
 
     q = _bytes_view(q, "q")
@@ -167,17 +188,21 @@ def sparse_mla_decode(q, kv_pool, indices, counts, sm_scale: float, q_scale: flo
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
     args = (_ptr(q), _ptr(kv_pool), int(kv_pool.shape[0]), _ptr(indices), W, _ptr(counts), B, H,
-            float(sm_scale), float(q_scale), float(k_scale), _ptr(out), _ptr(lse), _ptr(status),
-            int(stream))
-    if plan is None:
-        rc = smd_sparse_mla_decode(*args)
+            float(sm_scale), float(q_scale), float(k_scale), _ptr(out), _ptr(lse), _ptr(status))
+    ws = (_ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size())
+    if workspace is not None and not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    if plan is None and workspace is None:
+        rc = smd_sparse_mla_decode(*args, int(stream))
+    elif plan is None:
+        rc = smd_sparse_mla_decode_ws(*args, *ws, int(stream))
     else:
         if isinstance(plan, dict):
             p = SmdPlan()
             for k, v in plan.items():
                 setattr(p, k, int(v))
             plan = p
-        rc = smd_sparse_mla_decode_ex(*args, plan)
+        rc = smd_sparse_mla_decode_ex(*args, *ws, int(stream), plan)
     if rc != SMD_OK:
         raise SmdError(rc, "smd_sparse_mla_decode")
     return out, lse

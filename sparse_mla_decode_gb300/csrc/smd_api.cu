@@ -184,10 +184,14 @@ float scale_log2_of(float sm, float qs, float ks) {
     return static_cast<float>(v * 1.4426950408889634073599246810019);
 }
 
+int64_t workspace_for(const AnyConfig& cfg) {
+    return (cfg.kernel == SMD_KERNEL_TC && cfg.tc.split > 1) ? kTcWsBytes : 0;
+}
+
 int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* indices, int32_t W,
            const int32_t* counts, int32_t B, int32_t H, float sm_scale, float q_scale,
-           float k_scale, uint16_t* out, float* lse, int32_t* status, smd_stream_t stream,
-           const smd_plan_t* force) {
+           float k_scale, uint16_t* out, float* lse, int32_t* status, void* workspace,
+           int64_t workspace_bytes, smd_stream_t stream, const smd_plan_t* force) {
     if (B < 0 || W < 0 || N < 0 || H <= 0 || H % kHeadsPerTile != 0) return SMD_ERR_SHAPE;
     if (N >= (int64_t(1) << 31)) return SMD_ERR_SHAPE;
     if (B == 0) return SMD_OK;
@@ -204,6 +208,10 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
     AnyConfig cfg{};
     const int rc = make_plan(B, H, W, force, &plan, &cfg);
     if (rc != SMD_OK) return rc;
+    if (workspace != nullptr) {
+        if (!aligned(workspace, 16) || workspace_bytes < workspace_for(cfg)) return SMD_ERR_WORKSPACE;
+        if (workspace_for(cfg) > 0) cfg.tc.ws = static_cast<float*>(workspace);
+    }
 
     CallArgs a{};
     a.q = q;
@@ -233,16 +241,33 @@ int smd_sparse_mla_decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
                           int32_t H, float sm_scale, float q_scale, float k_scale, uint16_t* out,
                           float* lse, int32_t* status, smd_stream_t stream) {
     return smd::decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale, out,
-                       lse, status, stream, nullptr);
+                       lse, status, nullptr, 0, stream, nullptr);
+}
+
+int smd_sparse_mla_decode_ws(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
+                             const int32_t* indices, int32_t W, const int32_t* counts, int32_t B,
+                             int32_t H, float sm_scale, float q_scale, float k_scale,
+                             uint16_t* out, float* lse, int32_t* status, void* workspace,
+                             int64_t workspace_bytes, smd_stream_t stream) {
+    return smd::decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale, out,
+                       lse, status, workspace, workspace_bytes, stream, nullptr);
 }
 
 int smd_sparse_mla_decode_ex(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
                              const int32_t* indices, int32_t W, const int32_t* counts, int32_t B,
                              int32_t H, float sm_scale, float q_scale, float k_scale,
-                             uint16_t* out, float* lse, int32_t* status, smd_stream_t stream,
+                             uint16_t* out, float* lse, int32_t* status, void* workspace,
+                             int64_t workspace_bytes, smd_stream_t stream,
                              const smd_plan_t* force) {
     return smd::decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale, out,
-                       lse, status, stream, force);
+                       lse, status, workspace, workspace_bytes, stream, force);
+}
+
+int64_t smd_workspace_bytes(int32_t B, int32_t H, int32_t W) {
+    smd::AnyConfig cfg{};
+    smd_plan_t p{};
+    if (smd::make_plan(B, H, W, nullptr, &p, &cfg) != SMD_OK) return 0;
+    return smd::workspace_for(cfg);
 }
 
 int smd_plan(int32_t B, int32_t H, int32_t W, smd_plan_t* plan) {
@@ -277,7 +302,9 @@ const char* smd_status_str(int status) {
         case SMD_ERR_PLAN:
             return "the forced plan is invalid for these shapes";
         case SMD_ERR_DEVICE:
-            return "no usable CUDA device";
+            return "no usable CUDA device (or an SM id beyond the exchange workspace)";
+        case SMD_ERR_WORKSPACE:
+            return "workspace smaller than smd_workspace_bytes() or not 16-byte aligned";
         default:
             return "unknown status";
     }

@@ -103,10 +103,18 @@ constexpr int kTcMaxKeys = 512;  // keys per CTA
 constexpr int kTcMaxSplit = 4;   // CTAs per cluster (the merge inbox must fit)
 constexpr int kTcThreads = 512;
 
+// L2 exchange workspace of the tcgen05 kernel: one slot per SM id (%smid <
+// kTcWsSlots), each holding a CTA's FP32 partials of the other owners'
+// columns: (split - 1) x 128 heads x (512 / split) floats, at most 3 x 128 x 128.
+constexpr int kTcWsSlots = 256;
+constexpr int kTcWsSlotFloats = 3 * 128 * 128;
+constexpr int64_t kTcWsBytes = static_cast<int64_t>(kTcWsSlots) * kTcWsSlotFloats * 4;
+
 struct TcConfig {
     int split;
     uint64_t wait_budget_ns;
     int inject_stall;
+    float* ws;  // caller's workspace (>= kTcWsBytes) or null
 };
 
 // Dynamic shared memory of the tcgen05 kernel (bytes).

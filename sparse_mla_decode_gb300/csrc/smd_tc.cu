@@ -37,6 +37,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "smd.h"
 #include "smd_internal.h"
 #include "smd_ptx.cuh"
 
@@ -51,9 +52,10 @@ constexpr int kOffRing = kTile;     // two chunk slots
 constexpr int kOffMax = 3 * kTile;  // [S][128] maxima
 constexpr int kOffSums = kOffMax + 4 * 128 * 4;  // [S][128] sums
 constexpr int kOffRowMax = kOffSums + 4 * 128 * 4;  // [128] the row maxima
-constexpr int kOffIdx = kOffRowMax + 128 * 4;        // [512] this CTA's key indices
+constexpr int kOffSmid = kOffRowMax + 128 * 4;       // [4] SM ids of the cluster's CTAs
+constexpr int kOffIdx = kOffSmid + 16;               // [512] this CTA's key indices
 constexpr int kOffBars = kOffIdx + kTcMaxKeys * 4;
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 18;
 constexpr int kOffTmem = kOffBars + 8 * kNumBars;
 constexpr int kSmemUsed = kOffTmem + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // + alignment of the dynamic base to 1 KB
@@ -62,7 +64,8 @@ constexpr int kSmemBytes = kSmemUsed + 1024;  // + alignment of the dynamic base
 // (after PV) use separate barriers, so that no barrier can complete twice
 // before the thread that waits on it has seen the first completion.
 constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = 3, kBarS = 5, kBarP = 9, kBarO = 10,
-              kBarMax = 11, kBarRdy = 12, kBarIn = 13, kBarFreeB = 14;
+              kBarMax = 11, kBarRdy = 12, kBarIn = 13, kBarFreeB = 14, kBarDataReady = 16,
+              kBarReadersDone = 17;
 
 struct TcMaps {
     CUtensorMap q, q_tail, kv, kv_tail;
@@ -74,7 +77,28 @@ struct TcParams {
     float log2_448;
     uint64_t budget_ns;
     int32_t inject_stall;
+    float* ws;          // L2 exchange workspace (kTcWsSlots SM slots), or null: DSMEM exchange
 };
+
+__device__ __forceinline__ uint32_t sm_id() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ float4 ld_global_cg(const float* p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_global_v4(float* p, float4 v) {
+    asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
 
 struct Range {
     int n, first, mine, nch;
@@ -287,6 +311,13 @@ __device__ __forceinline__ void softmax(const TcParams& p, uint8_t* smem, uint32
         const uint32_t slot = smem_addr(maxima + split * 128 + h);
         for (int pr = 0; pr < S; ++pr)
             if (pr != split) st_async_b32(mapa(slot, pr), __float_as_uint(m), mapa(bars + 8 * kBarMax, pr));
+        if (h == 0) {  // this CTA's SM id, for the L2 exchange workspace
+            uint32_t* smids = reinterpret_cast<uint32_t*>(smem + kOffSmid);
+            const uint32_t me = sm_id();
+            smids[split] = me;
+            for (int pr = 0; pr < S; ++pr)
+                if (pr != split) st_async_b32(mapa(smem_addr(smids + split), pr), me, mapa(bars + 8 * kBarMax, pr));
+        }
         mbar_wait(bars + 8 * kBarMax, 0, ok, status, p.budget_ns, /*always=*/true);
         ok = __all_sync(0xffffffffu, ok);
         for (int pr = 0; pr < S; ++pr) m = fmaxf(m, maxima[pr * 128 + h]);
@@ -366,10 +397,94 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
         return;
     }
 
-    // Partials of O go to their column owners; the inbox lies over this CTA's
-    // tiles, so a CTA accepts pushes only after its own PV is done.
     const int CW = kLatent / S;       // columns per owner
     const int GW = CW / 4;            // columns per column group
+    if (p.ws != nullptr) {
+        // ---- L2 exchange: every CTA writes its partials of the other owners'
+        // columns into its SM's workspace slot; each owner reads the peers'
+        // slots (bypassing L1) and merges in CTA order. A slot stays valid
+        // until the peers have read it (the readers-done handshake), so the
+        // next CTA on the same SM cannot overwrite it early.
+        const uint32_t* smids = reinterpret_cast<const uint32_t*>(smem + kOffSmid);
+        bool slots_ok = true;
+        for (int rk = 0; rk < S; ++rk) slots_ok = slots_ok && smids[rk] < static_cast<uint32_t>(kTcWsSlots);
+        if (!slots_ok && threadIdx.x == 0 && status != nullptr) atomicCAS(status, 0, SMD_ERR_DEVICE);
+        const bool write = ok && slots_ok;
+        float* mine_ws = p.ws + static_cast<size_t>(slots_ok ? smids[split] : 0) * kTcWsSlotFloats;
+        const uint32_t sum_slot = smem_addr(sums + split * 128 + h);
+        for (int k = 1; k < S; ++k) {
+            const int pr = split ^ k;
+            if (cg == 0) st_async_b32(mapa(sum_slot, pr), __float_as_uint(l), mapa(bars + 8 * kBarIn, pr));
+            if (!write) continue;
+            const int blk = (split + S - pr - 1) % S;  // this CTA's block for owner pr
+            float* dst = mine_ws + (static_cast<size_t>(blk) * 128 + h) * CW + cg * GW;
+            for (int q = 0; q < GW / 32; ++q) {
+                float v[32];
+                if (have_o)
+                    tmem_ld32(lane_base + pr * CW + cg * GW + 32 * q, v);
+                else
+                    zero32(v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    st_global_v4(dst + 32 * q + 4 * i,
+                                 make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+            }
+        }
+        asm volatile("fence.acq_rel.cluster;" ::: "memory");
+        __syncthreads();
+        if (threadIdx.x == 0)
+            for (int pr = 0; pr < S; ++pr)
+                if (pr != split) mbar_arrive_remote(mapa(bars + 8 * kBarDataReady, pr));
+        mbar_wait(bars + 8 * kBarDataReady, 0, ok, status, p.budget_ns, /*always=*/true);
+        mbar_wait(bars + 8 * kBarIn, 0, ok, status, p.budget_ns, /*always=*/true);
+        const bool go = __syncthreads_and(ok && slots_ok) != 0;
+        if (go) {
+            float total = 0.f;
+            for (int rk = 0; rk < S; ++rk) total += sums[rk * 128 + h];
+            const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
+            for (int q = 0; q < GW / 32; ++q) {
+                const int col = split * CW + cg * GW + 32 * q;
+                float own[32], acc[32];
+                if (have_o)
+                    tmem_ld32(lane_base + col, own);
+                else
+                    zero32(own);
+                zero32(acc);
+                for (int rk = 0; rk < S; ++rk) {
+                    if (rk == split) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) acc[j] += own[j];
+                    } else {
+                        const int blk = (rk + S - split - 1) % S;  // rk's block for this owner
+                        const float* src = p.ws + static_cast<size_t>(smids[rk]) * kTcWsSlotFloats +
+                                           (static_cast<size_t>(blk) * 128 + h) * CW + cg * GW + 32 * q;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 x = ld_global_cg(src + 4 * i);
+                            acc[4 * i] += x.x;
+                            acc[4 * i + 1] += x.y;
+                            acc[4 * i + 2] += x.z;
+                            acc[4 * i + 3] += x.w;
+                        }
+                    }
+                }
+                store_bf16x32(orow + col, acc, inv);
+            }
+            if (split == 0 && cg == 0)
+                *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f
+                                   : -INFINITY;
+        }
+        __syncthreads();  // every read of the peers' slots is done
+        if (threadIdx.x == 0)
+            for (int pr = 0; pr < S; ++pr)
+                if (pr != split) mbar_arrive_remote(mapa(bars + 8 * kBarReadersDone, pr));
+        mbar_wait(bars + 8 * kBarReadersDone, 0, ok, status, p.budget_ns, /*always=*/true);
+        return;
+    }
+
+    // ---- DSMEM exchange: partials of O go to their column owners; the inbox
+    // lies over this CTA's tiles, so a CTA accepts pushes only after its own
+    // PV is done.
     const int pitch = CW + 4;         // floats per inbox row: rows 4 banks apart
     float* inbox = reinterpret_cast<float*>(smem);
     if (threadIdx.x == 0)
@@ -378,8 +493,10 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
     mbar_wait(bars + 8 * kBarRdy, 0, ok, status, p.budget_ns, /*always=*/true);
     ok = __all_sync(0xffffffffu, ok);
     const uint32_t sum_slot = smem_addr(sums + split * 128 + h);
-    for (int pr = 0; pr < S; ++pr) {
-        if (pr == split) continue;
+    // Partner k of this CTA is split ^ k: every CTA sends to a different peer
+    // at the same time instead of all of them to rank 0 first.
+    for (int k = 1; k < S; ++k) {
+        const int pr = split ^ k;
         const uint32_t rin = mapa(bars + 8 * kBarIn, pr);
         if (cg == 0) st_async_b32(mapa(sum_slot, pr), __float_as_uint(l), rin);
         const int src_slot = (split + S - pr - 1) % S;  // this CTA's slot among pr's sources
@@ -462,13 +579,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(bars + 8 * kBarMax, 1);
         mbar_init(bars + 8 * kBarRdy, S > 1 ? S - 1 : 1);
         mbar_init(bars + 8 * kBarIn, 1);
+        mbar_init(bars + 8 * kBarDataReady, S > 1 ? S - 1 : 1);
+        mbar_init(bars + 8 * kBarReadersDone, S > 1 ? S - 1 : 1);
         fence_mbar_init();
         const int CW = kLatent / S;
         // (inject_stall: the query barrier also expects 16 bytes nobody sends,
         // so its bounded wait runs out; a test hook for the timeout path.)
         mbar_arrive_expect_tx(bars + 8 * kBarQ, kTile + (p.inject_stall ? 16 : 0));
-        mbar_arrive_expect_tx(bars + 8 * kBarMax, (S - 1) * 128 * 4);
-        mbar_arrive_expect_tx(bars + 8 * kBarIn, (S - 1) * (128 * CW * 4 + 128 * 4));
+        mbar_arrive_expect_tx(bars + 8 * kBarMax, (S - 1) * (128 * 4 + 4));
+        // DSMEM exchange: the peers' partials and sums; L2 exchange: the sums only.
+        mbar_arrive_expect_tx(bars + 8 * kBarIn,
+                              (S - 1) * ((p.ws ? 0 : 128 * CW * 4) + 128 * 4));
     }
     if (warp == 8) tmem_alloc(base + kOffTmem, 512);
     tc_fence_before();
@@ -591,6 +712,7 @@ int launch_tc(const CallArgs& a, const TcConfig& cfg, cudaStream_t stream) {
     prm.log2_448 = static_cast<float>(std::log2(448.0));
     prm.budget_ns = cfg.wait_budget_ns;
     prm.inject_stall = cfg.inject_stall;
+    prm.ws = cfg.split > 1 ? cfg.ws : nullptr;
 
     static std::atomic<int> attr_set[kMaxDevices];
     int dev = 0;

@@ -45,7 +45,7 @@ def test_scale_log2_is_the_rounded_double_product():
 
 
 def test_status_strings():
-    for code in range(-7, 1):
+    for code in range(-8, 1):
         s = smd.smd_status_str(code)
         assert s and s != "unknown status"
     assert smd.smd_status_str(-99) == "unknown status"
@@ -63,7 +63,7 @@ def call(q=A, kv=A, N=100, idx=A, W=8, counts=A, B=2, H=16, out=A, lse=A, status
         return smd.smd_sparse_mla_decode(q, kv, N, idx, W, counts, B, H, 0.1, 0.1, 0.1,
                                          out, lse, status, 0)
     return smd.smd_sparse_mla_decode_ex(q, kv, N, idx, W, counts, B, H, 0.1, 0.1, 0.1,
-                                        out, lse, status, 0, force)
+                                        out, lse, status, 0, 0, 0, force)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -155,3 +155,14 @@ def test_invalid_tc_plans_are_rejected(H, W, force):
     for k, v in force.items():
         setattr(p, k, v)
     assert call(H=H, W=W, force=p) == smd.SMD_ERR_PLAN
+
+
+def test_workspace_size_and_checks():
+    # tcgen05 plans with a split use the L2 exchange workspace; others need none
+    assert smd.smd_workspace_bytes(256, 128, 2048) >= 3 * 128 * 128 * 4 * 152
+    assert smd.smd_workspace_bytes(5, 128, 300) == 0       # split 1: no exchange
+    assert smd.smd_workspace_bytes(5, 64, 256) == 0        # warp-MMA kernel: on-chip merge
+    need = smd.smd_workspace_bytes(2, 128, 2048)
+    args = (A, A, 100, A, 2048, A, 2, 128, 0.1, 0.1, 0.1, A, A, 0)
+    assert smd.smd_sparse_mla_decode_ws(*args, A, need - 16, 0) == smd.SMD_ERR_WORKSPACE
+    assert smd.smd_sparse_mla_decode_ws(*args, A + 8, need, 0) == smd.SMD_ERR_WORKSPACE

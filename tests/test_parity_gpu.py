@@ -28,13 +28,14 @@ def to_dev(case, dev):
             torch.from_numpy(case.indices).to(dev), torch.from_numpy(case.counts).to(dev))
 
 
-def gpu_decode(case, dev, plan=None, tensors=None):
+def gpu_decode(case, dev, plan=None, tensors=None, workspace=None):
     import torch
     from sparse_mla_decode_gb300 import binding
     q, kv, idx, cnt = tensors if tensors is not None else to_dev(case, dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     out, lse = binding.sparse_mla_decode(q, kv, idx, cnt, case.sm_scale, case.q_scale,
-                                         case.k_scale, status=status, plan=plan)
+                                         case.k_scale, status=status, plan=plan,
+                                         workspace=workspace)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, binding.smd_status_str(int(status.item()))
     return out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy()

@@ -25,22 +25,51 @@ SHAPES = [
 ]
 
 
+@pytest.fixture(scope="module")
+def workspace(cuda):
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    nbytes = binding.smd_workspace_bytes(256, 128, 2048)
+    return torch.empty(nbytes // 4, dtype=torch.float32, device=cuda)
+
+
 @pytest.mark.parametrize("shape", SHAPES, ids=[f"B{s[0]}H{s[1]}W{s[2]}" for s in SHAPES])
-def test_tc_random_shapes(cuda, shape):
+def test_tc_random_shapes(cuda, shape, workspace):
+    """Both exchanges of the split partials (DSMEM, and L2 through the
+    workspace) match the oracle and give identical bits (same sum order)."""
     B, H, W, N, counts = shape
     case = inputs.random_case(300 + W, B=B, H=H, W=W, N=N, counts=counts, heavy_frac=0.02)
-    out_g, lse_g = gpu_decode(case, cuda, dict(kernel=TC))
+    t = to_dev(case, cuda)
+    out_g, lse_g = gpu_decode(case, cuda, dict(kernel=TC), tensors=t)
     out_o, lse_o = oracle_decode(case)
     check(out_g, lse_g, out_o, lse_o, f"tc {shape}")
+    out_w, lse_w = gpu_decode(case, cuda, dict(kernel=TC), tensors=t, workspace=workspace)
+    check(out_w, lse_w, out_o, lse_o, f"tc l2 {shape}")
+    assert np.array_equal(out_w, out_g)
+    assert np.array_equal(lse_w.view(np.uint32), lse_g.view(np.uint32))
+
+
+def test_tc_l2_exchange_over_many_waves(cuda, workspace):
+    """800 CTAs on 152 SMs: workspace slots are reused wave after wave."""
+    case = inputs.random_case(320, B=200, H=128, W=2048, N=50000, heavy_frac=0.01)
+    t = to_dev(case, cuda)
+    out_w, lse_w = gpu_decode(case, cuda, tensors=t, workspace=workspace)
+    out_g, lse_g = gpu_decode(case, cuda, tensors=t)
+    assert np.array_equal(out_w, out_g)
+    assert np.array_equal(lse_w.view(np.uint32), lse_g.view(np.uint32))
+    rows = [0, 57, 199]
+    out_o, lse_o = oracle_decode(case, rows)
+    check(out_w[rows], lse_w[rows], out_o, lse_o, "tc l2 waves")
 
 
 @pytest.mark.parametrize("split", [1, 2, 4])
-def test_tc_every_split(cuda, split):
+def test_tc_every_split(cuda, split, workspace):
     case = inputs.random_case(310, B=3, H=128, W=512, N=6000, counts=[512, 300, 0],
                               heavy_frac=0.02)
-    out_g, lse_g = gpu_decode(case, cuda, dict(kernel=TC, split=split))
-    out_o, lse_o = oracle_decode(case)
-    check(out_g, lse_g, out_o, lse_o, f"tc split {split}")
+    for ws in (None, workspace):
+        out_g, lse_g = gpu_decode(case, cuda, dict(kernel=TC, split=split), workspace=ws)
+        out_o, lse_o = oracle_decode(case)
+        check(out_g, lse_g, out_o, lse_o, f"tc split {split} ws {ws is not None}")
 
 
 def test_tc_and_mma_kernels_agree(cuda):
