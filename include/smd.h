@@ -155,6 +155,38 @@ int smd_sparse_mla_decode_ex(const uint8_t* q, const uint8_t* kv_pool, int64_t N
                              void* workspace, int64_t workspace_bytes,
                              smd_stream_t stream, const smd_plan_t* force);
 
+/* As smd_sparse_mla_decode, for callers that cannot allocate device memory:
+ * a plug-in living inside a host framework that owns every device buffer
+ * and hands it only its inputs and outputs, or a serving loop whose memory
+ * is reserved up front so that no call can fail for lack of it or stall in
+ * the allocator. The attn_sparse page has no counterpart of this call.
+ *
+ * It allocates nothing (no cudaMalloc, no cudaFree, no allocating library
+ * routine). When the plan splits rows over a cluster of tcgen05 CTAs, their
+ * FP32 partials go through scratch that the library itself holds: a
+ * file-scope device array of 160 SM slots of 192 KiB (30 MiB), which every
+ * GPU that loads the library keeps until the process exits. Other plans need
+ * no scratch and run as smd_sparse_mla_decode does.
+ *
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture on the device.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's contents; nothing in it needs to start at zero (each call writes
+ *     every value it reads). Calls whose kernels overlap on the GPU race on
+ *     it: queue them on one stream or order them by events.
+ *   - A device with more than 160 SMs is rejected (SMD_ERR_WORKSPACE); a CTA
+ *     on an SM id beyond the array writes SMD_ERR_DEVICE to `status` and
+ *     leaves the array untouched.
+ * Arguments, layouts, ownership and the other errors are those of
+ * smd_sparse_mla_decode. */
+int smd_sparse_mla_decode_noalloc(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
+                                  const int32_t* indices, int32_t W, const int32_t* counts,
+                                  int32_t B, int32_t H,
+                                  float sm_scale, float q_scale, float k_scale,
+                                  uint16_t* out, float* lse, int32_t* status,
+                                  smd_stream_t stream);
+
 /* The base-2 logit scale the kernels use: fp32(sm*q_s*k_s*log2 e),
  * evaluated in double and rounded once. */
 float smd_scale_log2(float sm_scale, float q_scale, float k_scale);

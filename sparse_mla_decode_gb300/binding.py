@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
             so.smd_sparse_mla_decode_ws.argtypes = ws_args
             so.smd_sparse_mla_decode_ex.restype = ctypes.c_int
             so.smd_sparse_mla_decode_ex.argtypes = ws_args + [ctypes.POINTER(SmdPlan)]
+            so.smd_sparse_mla_decode_noalloc.restype = ctypes.c_int
+            so.smd_sparse_mla_decode_noalloc.argtypes = _DECODE_ARGS
             so.smd_workspace_bytes.restype = ctypes.c_int64
             so.smd_workspace_bytes.argtypes = [ctypes.c_int32] * 3
             so.smd_plan.restype = ctypes.c_int
@@ -111,6 +113,14 @@ def smd_sparse_mla_decode_ex(q, kv_pool, N, indices, W, counts, B, H, sm_scale, 
     return lib().smd_sparse_mla_decode_ex(q, kv_pool, N, indices, W, counts, B, H, sm_scale,
                                           q_scale, k_scale, out, lse, status, workspace,
                                           workspace_bytes, stream, ref)
+
+
+def smd_sparse_mla_decode_noalloc(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale,
+                                  k_scale, out, lse, status, stream) -> int:
+    """The decode for callers that cannot allocate device memory: split
+    partials go through the library's own static scratch (see smd.h)."""
+    return lib().smd_sparse_mla_decode_noalloc(q, kv_pool, N, indices, W, counts, B, H, sm_scale,
+                                               q_scale, k_scale, out, lse, status, stream)
 
 
 def smd_workspace_bytes(B: int, H: int, W: int) -> int:

@@ -191,7 +191,8 @@ int64_t workspace_for(const AnyConfig& cfg) {
 int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* indices, int32_t W,
            const int32_t* counts, int32_t B, int32_t H, float sm_scale, float q_scale,
            float k_scale, uint16_t* out, float* lse, int32_t* status, void* workspace,
-           int64_t workspace_bytes, smd_stream_t stream, const smd_plan_t* force) {
+           int64_t workspace_bytes, smd_stream_t stream, const smd_plan_t* force,
+           bool library_scratch = false) {
     if (B < 0 || W < 0 || N < 0 || H <= 0 || H % kHeadsPerTile != 0) return SMD_ERR_SHAPE;
     if (N >= (int64_t(1) << 31)) return SMD_ERR_SHAPE;
     if (B == 0) return SMD_OK;
@@ -211,6 +212,18 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
     if (workspace != nullptr) {
         if (!aligned(workspace, 16) || workspace_bytes < workspace_for(cfg)) return SMD_ERR_WORKSPACE;
         if (workspace_for(cfg) > 0) cfg.tc.ws = static_cast<float*>(workspace);
+    } else if (library_scratch && workspace_for(cfg) > 0) {
+        // The library's own static scratch: one slot per SM id.
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SMD_ERR_DEVICE;
+        if (sms > kStaticScratchSlots) return SMD_ERR_WORKSPACE;
+        int src = SMD_OK;
+        float* scratch = static_scratch(&src);
+        if (src != SMD_OK) return src;
+        cfg.tc.ws = scratch;
+        cfg.tc.ws_slots = kStaticScratchSlots;
     }
 
     CallArgs a{};
@@ -261,6 +274,15 @@ int smd_sparse_mla_decode_ex(const uint8_t* q, const uint8_t* kv_pool, int64_t N
                              const smd_plan_t* force) {
     return smd::decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale, out,
                        lse, status, workspace, workspace_bytes, stream, force);
+}
+
+int smd_sparse_mla_decode_noalloc(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
+                                  const int32_t* indices, int32_t W, const int32_t* counts,
+                                  int32_t B, int32_t H, float sm_scale, float q_scale,
+                                  float k_scale, uint16_t* out, float* lse, int32_t* status,
+                                  smd_stream_t stream) {
+    return smd::decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale, out,
+                       lse, status, nullptr, 0, stream, nullptr, /*library_scratch=*/true);
 }
 
 int64_t smd_workspace_bytes(int32_t B, int32_t H, int32_t W) {

@@ -114,8 +114,16 @@ struct TcConfig {
     int split;
     uint64_t wait_budget_ns;
     int inject_stall;
-    float* ws;  // caller's workspace (>= kTcWsBytes) or null
+    float* ws;     // exchange workspace or null (on-chip exchange)
+    int ws_slots;  // SM-id slots in ws (0: kTcWsSlots)
 };
+
+// SM-id slots of the library's own static exchange scratch (GB300: 152 SMs).
+constexpr int kStaticScratchSlots = 160;
+
+// Device address of the static exchange scratch on the current device (looked
+// up once per device); null with *rc set on failure.
+float* static_scratch(int* rc);
 
 // Dynamic shared memory of the tcgen05 kernel (bytes).
 int tc_smem_bytes();

@@ -77,7 +77,8 @@ struct TcParams {
     float log2_448;
     uint64_t budget_ns;
     int32_t inject_stall;
-    float* ws;          // L2 exchange workspace (kTcWsSlots SM slots), or null: DSMEM exchange
+    float* ws;          // L2 exchange workspace (ws_slots SM slots), or null: DSMEM exchange
+    int32_t ws_slots;   // SM-id slots the workspace holds
 };
 
 __device__ __forceinline__ uint32_t sm_id() {
@@ -407,7 +408,7 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
         // next CTA on the same SM cannot overwrite it early.
         const uint32_t* smids = reinterpret_cast<const uint32_t*>(smem + kOffSmid);
         bool slots_ok = true;
-        for (int rk = 0; rk < S; ++rk) slots_ok = slots_ok && smids[rk] < static_cast<uint32_t>(kTcWsSlots);
+        for (int rk = 0; rk < S; ++rk) slots_ok = slots_ok && smids[rk] < static_cast<uint32_t>(p.ws_slots);
         if (!slots_ok && threadIdx.x == 0 && status != nullptr) atomicCAS(status, 0, SMD_ERR_DEVICE);
         const bool write = ok && slots_ok;
         float* mine_ws = p.ws + static_cast<size_t>(slots_ok ? smids[split] : 0) * kTcWsSlotFloats;
@@ -698,6 +699,37 @@ constexpr int kMaxDevices = 64;
 
 int tc_smem_bytes() { return kSmemBytes; }
 
+// ---- the exchange scratch of smd_sparse_mla_decode_noalloc --------------------------
+// A file-scope device array: every GPU that loads the library holds these
+// kStaticScratchSlots x 192 KiB (30 MiB) until the process exits. Host code
+// must not pass the symbol itself to a kernel (in host code it names a host-
+// side stand-in); static_scratch() looks up its device address once per
+// device, with that device current.
+static __device__ __align__(256) float g_exchange_scratch[static_cast<size_t>(kStaticScratchSlots) *
+                                                           kTcWsSlotFloats];
+
+float* static_scratch(int* rc) {
+    static std::mutex mu;
+    static float* addr[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        *rc = SMD_ERR_DEVICE;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_exchange_scratch) != cudaSuccess || ptr == nullptr) {
+            (void)cudaGetLastError();
+            *rc = SMD_ERR_DEVICE;
+            return nullptr;
+        }
+        addr[dev] = static_cast<float*>(ptr);
+    }
+    *rc = SMD_OK;
+    return addr[dev];
+}
+
 int launch_tc(const CallArgs& a, const TcConfig& cfg, cudaStream_t stream) {
     TcMaps maps;
     const uint64_t qrows = static_cast<uint64_t>(a.B) * static_cast<uint64_t>(a.H);
@@ -713,6 +745,7 @@ int launch_tc(const CallArgs& a, const TcConfig& cfg, cudaStream_t stream) {
     prm.budget_ns = cfg.wait_budget_ns;
     prm.inject_stall = cfg.inject_stall;
     prm.ws = cfg.split > 1 ? cfg.ws : nullptr;
+    prm.ws_slots = cfg.ws_slots > 0 ? cfg.ws_slots : kTcWsSlots;
 
     static std::atomic<int> attr_set[kMaxDevices];
     int dev = 0;
