@@ -156,6 +156,14 @@ def reduce_max(value: float, world: int, device) -> float:
     return float(t.item())
 
 
+def aggregate(bytes_per_rank: int, ms_local: float, world: int, device) -> tuple[float, float]:
+    """Replicas: every rank moved bytes_per_rank in its own time; the job time
+    is the slowest rank's and the job throughput all ranks' bytes over it.
+    Returns (ms of the slowest rank, GB/s of the whole job)."""
+    ms = reduce_max(ms_local, world, device)
+    return ms, world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def workload_stats(case) -> dict:
     from sparse_mla_decode_gb300 import inputs
     return inputs.algorithmic_bytes(case)
@@ -224,7 +232,7 @@ def run_gpu(args, world, rank, local) -> dict | None:
         raise RuntimeError(f"device status {int(status.item())}")
     times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_local = float(np.mean(times_ms))
-    ms = reduce_max(ms_local, world, dev)
+    ms, value = aggregate(stats["kv_gathered"], ms_local, world, dev)
 
     # ---- end to end through the public call: host buffers in, host buffers out.
     hq = torch.from_numpy(case.q8).pin_memory()
@@ -268,14 +276,13 @@ def run_gpu(args, world, rank, local) -> dict | None:
 
     pk = peaks()
     gathered = stats["kv_gathered"]
-    value = world * gathered / (ms * 1e-3) / 1e9
     e2e_value = world * gathered / (e2e_ms * 1e-3) / 1e9
     achieved = stats["total"] / (ms * 1e-3) / 1e9
     fp8_peak_tflops = 2.0 * pk["bf16_tflops"]
     t_hbm = stats["total"] / (pk["hbm_gbs"] * 1e9)
     t_tc = stats["flops"] / (fp8_peak_tflops * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
-    traffic = load_traffic(args.config)
+    traffic = load_traffic(args.config, plan["kernel"])
     roofline = {
         "bound": bound,
         "achieved": round(achieved, 2) if bound == "hbm" else round(
@@ -283,7 +290,7 @@ def run_gpu(args, world, rank, local) -> dict | None:
         "peak": pk["hbm_gbs"] if bound == "hbm" else fp8_peak_tflops,
         "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
         "traffic": traffic,
-        "kernel": "mma_decode_kernel",
+        "kernel": KERNEL_FILES[plan["kernel"]][0],
         "algorithmic_bytes": stats["total"],
         "algorithmic_flops": stats["flops"],
         "t_roof_us": round(max(t_hbm, t_tc) * 1e6, 4),
@@ -329,12 +336,16 @@ def run_gpu(args, world, rank, local) -> dict | None:
     return line
 
 
-def load_traffic(config: str):
+KERNEL_FILES = {1: ("mma_decode_kernel", "smd_mma.cu"), 2: ("tc_decode_kernel", "smd_tc.cu")}
+
+
+def load_traffic(config: str, kernel: int = 1):
     """dram bytes per launch from the committed ncu summary of this kernel and
     workload; None unless it was taken on the current kernel source."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", f"mma_decode_kernel_{config}.json")
-    src = os.path.join(ROOT, "sparse_mla_decode_gb300", "csrc", "smd_mma.cu")
+    name, source = KERNEL_FILES[kernel]
+    path = os.path.join(ROOT, "profiles", f"{name}_{config}.json")
+    src = os.path.join(ROOT, "sparse_mla_decode_gb300", "csrc", source)
     try:
         with open(path) as f:
             d = json.load(f)
