@@ -55,7 +55,7 @@ constexpr int kOffRowMax = kOffSums + 4 * 128 * 4;  // [128] the row maxima
 constexpr int kOffSmid = kOffRowMax + 128 * 4;       // [4] SM ids of the cluster's CTAs
 constexpr int kOffIdx = kOffSmid + 16;               // [512] this CTA's key indices
 constexpr int kOffBars = kOffIdx + kTcMaxKeys * 4;
-constexpr int kNumBars = 18;
+constexpr int kNumBars = 24;
 constexpr int kOffTmem = kOffBars + 8 * kNumBars;
 constexpr int kSmemUsed = kOffTmem + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // + alignment of the dynamic base to 1 KB
@@ -64,8 +64,10 @@ constexpr int kSmemBytes = kSmemUsed + 1024;  // + alignment of the dynamic base
 // (after PV) use separate barriers, so that no barrier can complete twice
 // before the thread that waits on it has seen the first completion.
 constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = 3, kBarS = 5, kBarP = 9, kBarO = 10,
-              kBarMax = 11, kBarRdy = 12, kBarIn = 13, kBarFreeB = 14, kBarDataReady = 16,
-              kBarReadersDone = 17;
+              kBarMax = 11, kBarIn = 13, kBarFreeB = 14, kBarDataReady = 16,
+              kBarReadersDone = 17,
+              kBarRoundFree = 18,  // [3]: round k's partner may push into this CTA's inbox
+              kBarRoundFull = 21;  // [3]: round k's partner's partial has landed
 
 struct TcMaps {
     CUtensorMap q, q_tail, kv, kv_tail;
@@ -357,6 +359,77 @@ __device__ __forceinline__ void softmax(const TcParams& p, uint8_t* smem, uint32
     mbar_arrive_local(bars + 8 * kBarP);
 }
 
+// Pairwise-round exchange and merge of one CTA's columns; NP = 32-column
+// pieces per thread (2 for a 2-way split, 1 for a 4-way split).
+template <int NP>
+__device__ __forceinline__ void exchange_rounds(const TcParams& p, uint8_t* smem, uint32_t bars,
+                                                uint32_t lane_base, uint16_t* orow, float* lse,
+                                                float m, int h, int cg, int split, bool have_o,
+                                                bool& ok) {
+    const int S = p.split;
+    const int CW = kLatent / S, GW = CW / 4, pitch = CW + 4;
+    float* inbox = reinterpret_cast<float*>(smem);
+    const float* sums = reinterpret_cast<const float*>(smem + kOffSums);
+    int32_t* status = p.a.status;
+    float acc[NP][32];
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+        float own[32];
+        if (have_o)
+            tmem_ld32(lane_base + split * CW + cg * GW + 32 * q, own);
+        else
+            zero32(own);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[q][j] = 0.f + own[j];
+    }
+    for (int k = 1; k < S; ++k) {
+        const int pr = split ^ k;
+        // The partner's inbox is free for this round.
+        mbar_wait(bars + 8 * (kBarRoundFree + k - 1), 0, ok, status, p.budget_ns, /*always=*/true);
+        const uint32_t rfull = mapa(bars + 8 * (kBarRoundFull + k - 1), pr);
+        const uint32_t dst = smem_addr(inbox + h * pitch + cg * GW);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            float v[32];
+            if (have_o)
+                tmem_ld32(lane_base + pr * CW + cg * GW + 32 * q, v);
+            else
+                zero32(v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                st_async_v4(mapa(dst + (32 * q + 4 * i) * 4, pr),
+                            make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]), rfull);
+        }
+        // The partner's partial of this CTA's columns has landed.
+        mbar_wait(bars + 8 * (kBarRoundFull + k - 1), 0, ok, status, p.budget_ns, /*always=*/true);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) {
+            const float4* src = reinterpret_cast<const float4*>(inbox + h * pitch + cg * GW + 32 * q);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 x = src[i];
+                acc[q][4 * i] += x.x;
+                acc[q][4 * i + 1] += x.y;
+                acc[q][4 * i + 2] += x.z;
+                acc[q][4 * i + 3] += x.w;
+            }
+        }
+        __syncthreads();  // the inbox is consumed
+        if (threadIdx.x == 0 && k + 1 < S)
+            mbar_arrive_remote(mapa(bars + 8 * (kBarRoundFree + k), split ^ (k + 1)));
+    }
+    mbar_wait(bars + 8 * kBarIn, 0, ok, status, p.budget_ns, /*always=*/true);
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok) return;
+    float total = 0.f + sums[split * 128 + h];
+    for (int k = 1; k < S; ++k) total += sums[(split ^ k) * 128 + h];
+    const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
+#pragma unroll
+    for (int q = 0; q < NP; ++q) store_bf16x32(orow + split * CW + cg * GW + 32 * q, acc[q], inv);
+    if (split == 0 && cg == 0)
+        *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f : -INFINITY;
+}
+
 // ---- all 16 warps: partial exchange, merge and output -----------------------------
 // Warp w serves TMEM lane quarter w % 4 (heads 32(w % 4) .. +31) and column
 // group w / 4 of every column range it handles.
@@ -440,8 +513,10 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
         mbar_wait(bars + 8 * kBarIn, 0, ok, status, p.budget_ns, /*always=*/true);
         const bool go = __syncthreads_and(ok && slots_ok) != 0;
         if (go) {
-            float total = 0.f;
-            for (int rk = 0; rk < S; ++rk) total += sums[rk * 128 + h];
+            // Merge order (both exchange paths): this CTA's partial, then its
+            // partners split ^ 1, split ^ 2, split ^ 3.
+            float total = 0.f + sums[split * 128 + h];
+            for (int k = 1; k < S; ++k) total += sums[(split ^ k) * 128 + h];
             const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
             for (int q = 0; q < GW / 32; ++q) {
                 const int col = split * CW + cg * GW + 32 * q;
@@ -451,11 +526,11 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
                 else
                     zero32(own);
                 zero32(acc);
-                for (int rk = 0; rk < S; ++rk) {
-                    if (rk == split) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) acc[j] += own[j];
-                    } else {
+                for (int j = 0; j < 32; ++j) acc[j] += own[j];
+                for (int k = 1; k < S; ++k) {
+                    const int rk = split ^ k;
+                    {
                         const int blk = (rk + S - split - 1) % S;  // rk's block for this owner
                         const float* src = p.ws + static_cast<size_t>(smids[rk]) * kTcWsSlotFloats +
                                            (static_cast<size_t>(blk) * 128 + h) * CW + cg * GW + 32 * q;
@@ -483,75 +558,22 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
         return;
     }
 
-    // ---- DSMEM exchange: partials of O go to their column owners; the inbox
-    // lies over this CTA's tiles, so a CTA accepts pushes only after its own
-    // PV is done.
-    const int pitch = CW + 4;         // floats per inbox row: rows 4 banks apart
-    float* inbox = reinterpret_cast<float*>(smem);
-    if (threadIdx.x == 0)
-        for (int pr = 0; pr < S; ++pr)
-            if (pr != split) mbar_arrive_remote(mapa(bars + 8 * kBarRdy, pr));
-    mbar_wait(bars + 8 * kBarRdy, 0, ok, status, p.budget_ns, /*always=*/true);
-    ok = __all_sync(0xffffffffu, ok);
-    const uint32_t sum_slot = smem_addr(sums + split * 128 + h);
-    // Partner k of this CTA is split ^ k: every CTA sends to a different peer
-    // at the same time instead of all of them to rank 0 first.
-    for (int k = 1; k < S; ++k) {
-        const int pr = split ^ k;
-        const uint32_t rin = mapa(bars + 8 * kBarIn, pr);
-        if (cg == 0) st_async_b32(mapa(sum_slot, pr), __float_as_uint(l), rin);
-        const int src_slot = (split + S - pr - 1) % S;  // this CTA's slot among pr's sources
-        const uint32_t dst = smem_addr(inbox + (src_slot * 128 + h) * pitch + cg * GW);
-        for (int q = 0; q < GW / 32; ++q) {
-            float v[32];
-            if (have_o)
-                tmem_ld32(lane_base + pr * CW + cg * GW + 32 * q, v);
-            else
-                zero32(v);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                st_async_v4(mapa(dst + (32 * q + 4 * i) * 4, pr),
-                            make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]), rin);
+    // ---- DSMEM exchange in pairwise rounds: in round k this CTA and its
+    // partner split ^ k swap their partials of each other's columns (pairwise
+    // traffic sustains about twice the all-to-all rate on this part). One
+    // inbox lies over this CTA's tiles: round 1 may start once the partner's
+    // PV is done, round k + 1 once the partner has consumed round k.
+    if (cg == 0)
+        for (int k = 1; k < S; ++k) {
+            const int pr = split ^ k;
+            st_async_b32(mapa(smem_addr(sums + split * 128 + h), pr), __float_as_uint(l),
+                         mapa(bars + 8 * kBarIn, pr));
         }
-    }
-    mbar_wait(bars + 8 * kBarIn, 0, ok, status, p.budget_ns, /*always=*/true);
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) return;
-
-    // Merge this CTA's columns in CTA order: BF16(sum * k_scale / total).
-    float total = 0.f;
-    for (int rk = 0; rk < S; ++rk) total += sums[rk * 128 + h];
-    const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
-    for (int q = 0; q < GW / 32; ++q) {
-        const int col = split * CW + cg * GW + 32 * q;
-        float own[32], acc[32];
-        if (have_o)
-            tmem_ld32(lane_base + col, own);
-        else
-            zero32(own);
-        zero32(acc);
-        for (int rk = 0; rk < S; ++rk) {
-            if (rk == split) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) acc[j] += own[j];
-            } else {
-                const int src_slot = (rk + S - split - 1) % S;
-                const float4* src = reinterpret_cast<const float4*>(
-                    inbox + (src_slot * 128 + h) * pitch + cg * GW + 32 * q);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float4 x = src[i];
-                    acc[4 * i] += x.x;
-                    acc[4 * i + 1] += x.y;
-                    acc[4 * i + 2] += x.z;
-                    acc[4 * i + 3] += x.w;
-                }
-            }
-        }
-        store_bf16x32(orow + col, acc, inv);
-    }
-    if (split == 0 && cg == 0)
-        *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f : -INFINITY;
+    if (threadIdx.x == 0) mbar_arrive_remote(mapa(bars + 8 * kBarRoundFree, split ^ 1));
+    if (S == 2)
+        exchange_rounds<2>(p, smem, bars, lane_base, orow, lse, m, h, cg, split, have_o, ok);
+    else
+        exchange_rounds<1>(p, smem, bars, lane_base, orow, lse, m, h, cg, split, have_o, ok);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -578,8 +600,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(bars + 8 * kBarP, 128);
         mbar_init(bars + 8 * kBarO, 1);
         mbar_init(bars + 8 * kBarMax, 1);
-        mbar_init(bars + 8 * kBarRdy, S > 1 ? S - 1 : 1);
         mbar_init(bars + 8 * kBarIn, 1);
+        for (int k = 0; k < 3; ++k) {
+            mbar_init(bars + 8 * (kBarRoundFree + k), 1);
+            mbar_init(bars + 8 * (kBarRoundFull + k), 1);
+        }
         mbar_init(bars + 8 * kBarDataReady, S > 1 ? S - 1 : 1);
         mbar_init(bars + 8 * kBarReadersDone, S > 1 ? S - 1 : 1);
         fence_mbar_init();
@@ -588,9 +613,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // so its bounded wait runs out; a test hook for the timeout path.)
         mbar_arrive_expect_tx(bars + 8 * kBarQ, kTile + (p.inject_stall ? 16 : 0));
         mbar_arrive_expect_tx(bars + 8 * kBarMax, (S - 1) * (128 * 4 + 4));
-        // DSMEM exchange: the peers' partials and sums; L2 exchange: the sums only.
-        mbar_arrive_expect_tx(bars + 8 * kBarIn,
-                              (S - 1) * ((p.ws ? 0 : 128 * CW * 4) + 128 * 4));
+        // The peers' sums; on the DSMEM path, round k's partial of this CTA's columns.
+        mbar_arrive_expect_tx(bars + 8 * kBarIn, (S - 1) * 128 * 4);
+        if (p.ws == nullptr)
+            for (int k = 1; k < S; ++k)
+                mbar_arrive_expect_tx(bars + 8 * (kBarRoundFull + k - 1), 128 * CW * 4);
     }
     if (warp == 8) tmem_alloc(base + kOffTmem, 512);
     tc_fence_before();
