@@ -22,10 +22,12 @@
 //               into TMEM columns 128c..128c+127; after P is ready, O = P V
 //               (M128 N256 K32 MMAs, V read MN-major from the same gathered
 //               tile) into TMEM columns 0..511, which the logits no longer need.
-//   warps 12-15 softmax, thread h = head h = TMEM lane h: the row maximum
-//               (cluster exchange over DSMEM), P written straight into the
-//               K-major swizzled operand layout over the dead query tile.
-//   all warps   once O is complete: the partials of O go to their column
+//   warps 12-15 row maximum, thread h = head h = TMEM lane h, as the QK
+//               chunks complete (cluster exchange over DSMEM).
+//   all warps   then P, written straight into the K-major swizzled operand
+//               layout over the dead query tile (four warps per TMEM lane
+//               quarter, 32 keys of every chunk each);
+//               once O is complete: the partials of O go to their column
 //               owners over DSMEM and are merged in CTA order into BF16 out
 //               and the LSE (four warps per TMEM lane quarter).
 // Every wait on a copy, the tensor core or a peer is bounded.
@@ -54,7 +56,8 @@ constexpr int kOffSums = kOffMax + 4 * 128 * 4;  // [S][128] sums
 constexpr int kOffRowMax = kOffSums + 4 * 128 * 4;  // [128] the row maxima
 constexpr int kOffSmid = kOffRowMax + 128 * 4;       // [4] SM ids of the cluster's CTAs
 constexpr int kOffIdx = kOffSmid + 16;               // [512] this CTA's key indices
-constexpr int kOffBars = kOffIdx + kTcMaxKeys * 4;
+constexpr int kOffLsum = kOffIdx + kTcMaxKeys * 4;   // [4][128] sums of P per 32-key group
+constexpr int kOffBars = kOffLsum + 4 * 128 * 4;
 constexpr int kNumBars = 24;
 constexpr int kOffTmem = kOffBars + 8 * kNumBars;
 constexpr int kSmemUsed = kOffTmem + 16;
@@ -132,9 +135,9 @@ __device__ __forceinline__ void wait_next(uint32_t bar, uint32_t& seen, bool& ok
 // 160 gathers is limited by the issue rate (well below HBM bandwidth).
 constexpr int kProducerThreads = 256;
 
-__device__ __forceinline__ void producer(const TcMaps& maps, const TcParams& p, uint8_t* smem,
-                                         uint32_t base, uint32_t bars, int b, int group, int split,
-                                         bool& ok) {
+__device__ __forceinline__ void producer_a(const TcMaps& maps, const TcParams& p, uint8_t* smem,
+                                           uint32_t base, uint32_t bars, int b, int group, int split,
+                                           bool& ok) {
     const int t = threadIdx.x;
     const Range r = key_range(p, b, split);
     if (t == 0) {
@@ -151,9 +154,8 @@ __device__ __forceinline__ void producer(const TcMaps& maps, const TcParams& p, 
     asm volatile("bar.sync 1, %0;" ::"r"(kProducerThreads) : "memory");
 
     // Completions of the pass-A "slot free" barriers (after QK of the slot's
-    // chunks, ascending) and of the pass-B ones (after PV, descending) seen.
+    // chunks, ascending) seen.
     uint32_t seen[2] = {0u, 0u};
-    uint32_t seen_b[2] = {0u, 0u};
     // Pass A: chunk c: thread t < 160 issues piece t % 5 (four 128-byte column
     // blocks and the 64-byte tail) of rows 4g..4g+3, g = t / 5.
     for (int c = 0; c < r.nch && ok; ++c) {
@@ -173,9 +175,18 @@ __device__ __forceinline__ void producer(const TcMaps& maps, const TcParams& p, 
                 tma_gather4(slot + 4 * kBlock + 4 * g * 64, &maps.kv_tail, 512, rw[0], rw[1], rw[2], rw[3], full);
         }
     }
-    // Pass B visits chunks in descending order; the last two are resident, the
-    // others come back (V columns only) into their slot once PV of the chunk
-    // two above has released it.
+}
+
+// Pass B visits chunks in descending order; the last two are resident, the
+// others come back (V columns only) into their slot once PV of the chunk two
+// above has released it.
+__device__ __forceinline__ void producer_b(const TcMaps& maps, const TcParams& p, uint8_t* smem,
+                                           uint32_t base, uint32_t bars, int b, int split,
+                                           bool& ok) {
+    const int t = threadIdx.x;
+    const Range r = key_range(p, b, split);
+    const int32_t* idx_s = reinterpret_cast<const int32_t*>(smem + kOffIdx);
+    uint32_t seen_b[2] = {0u, 0u};  // completions of the pass-B "slot free" barriers seen
     for (int c = 1; c >= 0; --c) {
         if (c > r.nch - 3 || !ok) continue;
         const int s = c & 1;
@@ -196,15 +207,16 @@ __device__ __forceinline__ void producer(const TcMaps& maps, const TcParams& p, 
     }
 }
 
-// ---- warp 1, one lane: MMA issuer ---------------------------------------------
-__device__ __forceinline__ void mma_issuer(const TcParams& p, uint32_t base, uint32_t bars,
-                                           uint32_t tmem, int b, int split, bool& ok) {
+// ---- warp 8, one lane: MMA issuer -----------------------------------------------
+// full_seen counts the completions of the two slots' "full" barriers this
+// thread has waited for; pass B continues from pass A's counts.
+__device__ __forceinline__ void mma_pass_a(const TcParams& p, uint32_t base, uint32_t bars,
+                                           uint32_t tmem, int b, int split, uint32_t (&full_seen)[2],
+                                           bool& ok) {
     const Range r = key_range(p, b, split);
     mbar_wait(bars + 8 * kBarQ, 0, ok, p.a.status, p.budget_ns);
     tc_fence_after();
-    uint32_t full_seen[2] = {0u, 0u};
     constexpr uint32_t kIdQK = umma_idesc_e4m3(128, kTcChunk, 0);
-    constexpr uint32_t kIdPV = umma_idesc_e4m3(128, 256, 1);
     const uint32_t q_s = base + kOffQP;
     // ---- pass A: S_c = Q K_c^T into TMEM columns 128c .. 128c + 127
     for (int c = 0; c < r.nch && ok; ++c) {
@@ -230,6 +242,13 @@ __device__ __forceinline__ void mma_issuer(const TcParams& p, uint32_t base, uin
         umma_commit(bars + 8 * (kBarS + c));
         umma_commit(bars + 8 * (kBarEmpty + s));
     }
+}
+
+__device__ __forceinline__ void mma_pass_b(const TcParams& p, uint32_t base, uint32_t bars,
+                                           uint32_t tmem, int b, int split, uint32_t (&full_seen)[2],
+                                           bool& ok) {
+    const Range r = key_range(p, b, split);
+    constexpr uint32_t kIdPV = umma_idesc_e4m3(128, 256, 1);
     // ---- P is in shared memory and every logit has been read out of TMEM.
     mbar_wait(bars + 8 * kBarP, 0, ok, p.a.status, p.budget_ns);
     tc_fence_after();
@@ -275,12 +294,10 @@ __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32
     for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
-// ---- warps 12-15: softmax (thread h = head h = TMEM lane h) ----------------------
-// The row maximum (cluster exchange over DSMEM), then P in E4M3 into the K-major
-// 128-byte-swizzled A operand (row h, 16-byte chunk k stored at chunk
-// k ^ (h & 7)) and the FP32 sum of the unquantized P in key order. Leaves the
-// row maximum and the sum in shared memory for the finish.
-__device__ __forceinline__ void softmax(const TcParams& p, uint8_t* smem, uint32_t bars,
+// ---- warps 12-15: row maximum (thread h = head h = TMEM lane h) ------------------
+// The maximum of the CTA's logits as the QK chunks complete, then the maximum
+// over the row (cluster exchange over DSMEM), left in shared memory.
+__device__ __forceinline__ void row_max(const TcParams& p, uint8_t* smem, uint32_t bars,
                                         uint32_t tmem, int b, int split, bool& ok) {
     const int h = threadIdx.x & 127;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * ((threadIdx.x >> 5) & 3)) << 16);
@@ -288,7 +305,6 @@ __device__ __forceinline__ void softmax(const TcParams& p, uint8_t* smem, uint32
     const int S = p.split;
     const float lam = p.a.scale_log2;
     float* maxima = reinterpret_cast<float*>(smem + kOffMax);
-    float* sums = reinterpret_cast<float*>(smem + kOffSums);
     float* rowmax = reinterpret_cast<float*>(smem + kOffRowMax);
     int32_t* status = p.a.status;
 
@@ -326,34 +342,48 @@ __device__ __forceinline__ void softmax(const TcParams& p, uint8_t* smem, uint32
         for (int pr = 0; pr < S; ++pr) m = fmaxf(m, maxima[pr * 128 + h]);
     }
     rowmax[h] = m;
+}
 
-    const float bias = m - p.log2_448;
+// ---- all 16 warps: P ---------------------------------------------------------------
+// Warp w takes TMEM lane quarter w % 4 (thread = head h) and keys 32j..32j+31,
+// j = w / 4, of every chunk: P = 2^(s - m + log2 448) in E4M3 into the K-major
+// 128-byte-swizzled A operand (row h, 16-byte chunk k stored at chunk
+// k ^ (h & 7)), and the FP32 sum of the unquantized P of its keys, chunks in
+// ascending order, into lsum[j][h]. The exp2 unit bounds this phase, so it
+// runs on every warp.
+__device__ __forceinline__ void p_phase(const TcParams& p, uint8_t* smem, uint32_t bars,
+                                        uint32_t tmem, int b, int split, bool ok) {
+    const int warp = threadIdx.x >> 5;
+    const int h = 32 * (warp & 3) + (threadIdx.x & 31);
+    const int j = warp >> 2;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    const Range r = key_range(p, b, split);
+    const float lam = p.a.scale_log2;
+    const float bias = reinterpret_cast<const float*>(smem + kOffRowMax)[h] - p.log2_448;
     float l = 0.f;
     for (int c = 0; c < r.nch && ok; ++c) {
-        const int cnt = min(kTcChunk, r.mine - kTcChunk * c);
+        const int lim = min(kTcChunk, r.mine - kTcChunk * c) - 32 * j;
+        if (lim <= 0) continue;  // warp-uniform
         uint8_t* row = smem + kOffQP + c * kBlock + (h >> 3) * 1024 + (h & 7) * 128;
-        for (int q = 0; 32 * q < cnt; ++q) {
-            float v[32];
-            tmem_ld32(lane_base + kTcChunk * c + 32 * q, v);
-            const int lim = cnt - 32 * q;
-            uint32_t w[8];
+        float v[32];
+        tmem_ld32(lane_base + kTcChunk * c + 32 * j, v);
+        uint32_t w[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float pr[4];
+        for (int i = 0; i < 8; ++i) {
+            float pr[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j = 4 * i + e;
-                    pr[e] = (j < lim) ? ex2_approx(lam * v[j] - bias) : 0.f;
-                    l += pr[e];
-                }
-                w[i] = static_cast<uint32_t>(e4m3x2(pr[0], pr[1])) |
-                       (static_cast<uint32_t>(e4m3x2(pr[2], pr[3])) << 16);
+            for (int e = 0; e < 4; ++e) {
+                const int k = 4 * i + e;
+                pr[e] = (k < lim) ? ex2_approx(lam * v[k] - bias) : 0.f;
+                l += pr[e];
             }
-            *reinterpret_cast<uint4*>(row + (((2 * q) ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<uint4*>(row + (((2 * q + 1) ^ (h & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+            w[i] = static_cast<uint32_t>(e4m3x2(pr[0], pr[1])) |
+                   (static_cast<uint32_t>(e4m3x2(pr[2], pr[3])) << 16);
         }
+        *reinterpret_cast<uint4*>(row + (((2 * j) ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(row + (((2 * j + 1) ^ (h & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
     }
-    sums[split * 128 + h] = l;
+    reinterpret_cast<float*>(smem + kOffLsum)[j * 128 + h] = l;
     fence_proxy_async();  // P (generic stores) -> the tensor core's reads
     tc_fence_before();    // every logit read is complete
     mbar_arrive_local(bars + 8 * kBarP);
@@ -443,7 +473,10 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
     const int S = p.split;
     float* sums = reinterpret_cast<float*>(smem + kOffSums);
     const float m = reinterpret_cast<const float*>(smem + kOffRowMax)[h];
-    const float l = sums[split * 128 + h];
+    // This CTA's sum of P: its four key groups in a fixed order.
+    const float* lsum = reinterpret_cast<const float*>(smem + kOffLsum);
+    const float l = ((lsum[h] + lsum[128 + h]) + lsum[256 + h]) + lsum[384 + h];
+    if (cg == 0) sums[split * 128 + h] = l;  // read after the barriers below
     int32_t* status = p.a.status;
     const bool have_o = ok && r.mine > 0;  // O in TMEM is defined only if PV ran
     uint16_t* orow = p.a.out + (static_cast<int64_t>(b) * p.a.H + group * kTcHeads + h) * kLatent;
@@ -597,7 +630,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(bars + 8 * (kBarFreeB + i), 1);
         }
         for (int c = 0; c < 4; ++c) mbar_init(bars + 8 * (kBarS + c), 1);
-        mbar_init(bars + 8 * kBarP, 128);
+        mbar_init(bars + 8 * kBarP, kTcThreads);
         mbar_init(bars + 8 * kBarO, 1);
         mbar_init(bars + 8 * kBarMax, 1);
         mbar_init(bars + 8 * kBarIn, 1);
@@ -626,19 +659,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmem);
     if (S > 1) cluster_arrive_relaxed();
 
+    uint32_t full_seen[2] = {0u, 0u};
     if (warp < 8) {
-        producer(maps, p, smem, base, bars, b, group, split, ok);
+        producer_a(maps, p, smem, base, bars, b, group, split, ok);
     } else if (warp == 8) {
-        if (lane == 0) mma_issuer(p, base, bars, tmem, b, split, ok);
+        if (lane == 0) mma_pass_a(p, base, bars, tmem, b, split, full_seen, ok);
         __syncwarp();
     } else if (warp >= 12) {
-        softmax(p, smem, bars, tmem, b, split, ok);
+        row_max(p, smem, bars, tmem, b, split, ok);
+    }
+    if (S > 1 && warp < 12) cluster_wait();  // the max warps waited before their exchange
+    // Every QK is complete and the row maxima are in shared memory; one verdict.
+    ok = __syncthreads_and(ok) != 0;
+    tc_fence_after();
+    p_phase(p, smem, bars, tmem, b, split, ok);
+    if (warp < 8) {
+        producer_b(maps, p, smem, base, bars, b, split, ok);
+    } else if (warp == 8) {
+        if (lane == 0) mma_pass_b(p, base, bars, tmem, b, split, full_seen, ok);
+        __syncwarp();
     }
     // Every warp: O is complete in TMEM; then the exchange and the merge.
     mbar_wait(bars + 8 * kBarO, 0, ok, p.a.status, p.budget_ns);
     tc_fence_after();
-    if (S > 1 && warp < 12) cluster_wait();  // the softmax warps waited before their max exchange
-    ok = __syncthreads_and(ok) != 0;         // the sums and row maxima are visible; one verdict
+    ok = __syncthreads_and(ok) != 0;  // the partial sums of P are visible; one verdict
     finish(p, smem, bars, tmem, b, group, split, ok);
     tc_fence_before();
     __syncthreads();
