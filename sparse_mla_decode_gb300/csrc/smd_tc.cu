@@ -397,8 +397,11 @@ __device__ __forceinline__ void exchange_rounds(const TcParams& p, uint8_t* smem
                                                 float m, int h, int cg, int split, bool have_o,
                                                 bool& ok) {
     const int S = p.split;
-    const int CW = kLatent / S, GW = CW / 4, pitch = CW + 4;
-    float* inbox = reinterpret_cast<float*>(smem);
+    const int CW = kLatent / S, GW = CW / 4;
+    // Inbox of 128 x CW floats in 16-byte units: unit u of head h's columns in
+    // column group cg at (cg * GW / 4 + u) * 128 + h, so that one warp-wide
+    // 16-byte store (32 heads) covers 512 contiguous bytes.
+    float4* inbox = reinterpret_cast<float4*>(smem);
     const float* sums = reinterpret_cast<const float*>(smem + kOffSums);
     int32_t* status = p.a.status;
     float acc[NP][32];
@@ -417,7 +420,7 @@ __device__ __forceinline__ void exchange_rounds(const TcParams& p, uint8_t* smem
         // The partner's inbox is free for this round.
         mbar_wait(bars + 8 * (kBarRoundFree + k - 1), 0, ok, status, p.budget_ns, /*always=*/true);
         const uint32_t rfull = mapa(bars + 8 * (kBarRoundFull + k - 1), pr);
-        const uint32_t dst = smem_addr(inbox + h * pitch + cg * GW);
+        const uint32_t dst = mapa(smem_addr(inbox + cg * (GW / 4) * 128 + h), pr);
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
             float v[32];
@@ -427,17 +430,17 @@ __device__ __forceinline__ void exchange_rounds(const TcParams& p, uint8_t* smem
                 zero32(v);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                st_async_v4(mapa(dst + (32 * q + 4 * i) * 4, pr),
+                st_async_v4(dst + (8 * q + i) * 128 * 16,
                             make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]), rfull);
         }
         // The partner's partial of this CTA's columns has landed.
         mbar_wait(bars + 8 * (kBarRoundFull + k - 1), 0, ok, status, p.budget_ns, /*always=*/true);
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
-            const float4* src = reinterpret_cast<const float4*>(inbox + h * pitch + cg * GW + 32 * q);
+            const float4* src = inbox + (cg * (GW / 4) + 8 * q) * 128 + h;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const float4 x = src[i];
+                const float4 x = src[i * 128];
                 acc[q][4 * i] += x.x;
                 acc[q][4 * i + 1] += x.y;
                 acc[q][4 * i + 2] += x.z;
@@ -524,7 +527,8 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
             if (cg == 0) st_async_b32(mapa(sum_slot, pr), __float_as_uint(l), mapa(bars + 8 * kBarIn, pr));
             if (!write) continue;
             const int blk = (split + S - pr - 1) % S;  // this CTA's block for owner pr
-            float* dst = mine_ws + (static_cast<size_t>(blk) * 128 + h) * CW + cg * GW;
+            // 16-byte unit u of head h's columns in group cg at (cg * GW / 4 + u) * 128 + h
+            float* dst = mine_ws + static_cast<size_t>(blk) * 128 * CW + (cg * (GW / 4) * 128 + h) * 4;
             for (int q = 0; q < GW / 32; ++q) {
                 float v[32];
                 if (have_o)
@@ -533,7 +537,7 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
                     zero32(v);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                    st_global_v4(dst + 32 * q + 4 * i,
+                    st_global_v4(dst + (8 * q + i) * 128 * 4,
                                  make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
             }
         }
@@ -566,10 +570,11 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
                     {
                         const int blk = (rk + S - split - 1) % S;  // rk's block for this owner
                         const float* src = p.ws + static_cast<size_t>(smids[rk]) * kTcWsSlotFloats +
-                                           (static_cast<size_t>(blk) * 128 + h) * CW + cg * GW + 32 * q;
+                                           static_cast<size_t>(blk) * 128 * CW +
+                                           ((cg * (GW / 4) + 8 * q) * 128 + h) * 4;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
-                            const float4 x = ld_global_cg(src + 4 * i);
+                            const float4 x = ld_global_cg(src + i * 128 * 4);
                             acc[4 * i] += x.x;
                             acc[4 * i + 1] += x.y;
                             acc[4 * i + 2] += x.z;
