@@ -57,7 +57,8 @@ constexpr int kOffRowMax = kOffSums + 4 * 128 * 4;  // [128] the row maxima
 constexpr int kOffSmid = kOffRowMax + 128 * 4;       // [4] SM ids of the cluster's CTAs
 constexpr int kOffIdx = kOffSmid + 16;               // [512] this CTA's key indices
 constexpr int kOffLsum = kOffIdx + kTcMaxKeys * 4;   // [4][128] sums of P per 32-key group
-constexpr int kOffBars = kOffLsum + 4 * 128 * 4;
+constexpr int kOffFlags = kOffLsum + 4 * 128 * 4;    // [4] words the partners' "free" signals write
+constexpr int kOffBars = kOffFlags + 16;
 constexpr int kNumBars = 24;
 constexpr int kOffTmem = kOffBars + 8 * kNumBars;
 constexpr int kSmemUsed = kOffTmem + 16;
@@ -69,8 +70,8 @@ constexpr int kSmemBytes = kSmemUsed + 1024;  // + alignment of the dynamic base
 constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = 3, kBarS = 5, kBarP = 9, kBarO = 10,
               kBarMax = 11, kBarIn = 13, kBarFreeB = 14, kBarDataReady = 16,
               kBarReadersDone = 17,
-              kBarRoundFree = 18,  // [3]: round k's partner may push into this CTA's inbox
-              kBarRoundFull = 21;  // [3]: round k's partner's partial has landed
+              kBarRoundFree = 18,  // [3]: k - 1: partner split ^ k's inbox is free
+              kBarRoundFull = 21;  // [3]: k - 1: partner split ^ k's partial has landed here
 
 struct TcMaps {
     CUtensorMap q, q_tail, kv, kv_tail;
@@ -278,20 +279,9 @@ __device__ __forceinline__ void mma_pass_b(const TcParams& p, uint32_t base, uin
     umma_commit(bars + 8 * kBarO);
 }
 
-// ---- warps 4-7: softmax and epilogue (thread h = head h = TMEM lane h) ------------
 __device__ __forceinline__ void zero32(float (&v)[32]) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = 0.f;
-}
-
-// BF16(v * inv) of 32 columns -> 64 bytes at dst (16-byte aligned).
-__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float (&v)[32], float inv) {
-    uint32_t w[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) w[i] = bf16x2(v[2 * i] * inv, v[2 * i + 1] * inv);
-    uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
 // ---- warps 12-15: row maximum (thread h = head h = TMEM lane h) ------------------
@@ -389,38 +379,58 @@ __device__ __forceinline__ void p_phase(const TcParams& p, uint8_t* smem, uint32
     mbar_arrive_local(bars + 8 * kBarP);
 }
 
-// Pairwise-round exchange and merge of one CTA's columns; NP = 32-column
-// pieces per thread (2 for a 2-way split, 1 for a 4-way split).
+// BF16(v * inv) of 32 columns of head h, starting at column `col` of the
+// staging tile (128 rows of row_bytes; 16-byte chunk c of row h is stored at
+// chunk c ^ (h & 7), so that 32 heads' stores spread over the banks).
+__device__ __forceinline__ void stage_bf16x32(uint8_t* stage, int row_bytes, int h, int col,
+                                              const float (&v)[32], float inv) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = bf16x2(v[2 * i] * inv, v[2 * i + 1] * inv);
+    uint8_t* row = stage + h * row_bytes;
+    const int c0 = col >> 3;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<uint4*>(row + (((c0 + i) ^ (h & 7)) << 4)) =
+            make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+// The staged 128-head tile to out (dst = head 0's first column; rows kLatent
+// BF16 apart), every warp-wide store covering whole rows of the tile. The
+// caller makes the staged tile visible to all threads first.
+__device__ __forceinline__ void flush_tile(const uint8_t* stage, int row_bytes, uint16_t* dst) {
+    const int chunks = row_bytes >> 4;
+    for (int e = threadIdx.x; e < 128 * chunks; e += kTcThreads) {
+        const int r = e / chunks, c = e - r * chunks;
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + r * row_bytes + ((c ^ (r & 7)) << 4));
+        *reinterpret_cast<uint4*>(dst + static_cast<int64_t>(r) * kLatent + c * 8) = v;
+    }
+}
+
+// DSMEM exchange and merge of one CTA's columns; NP = 32-column pieces per
+// thread (2 for a 2-way split, 1 for a 4-way split). This CTA holds one inbox
+// per partner: inbox k - 1 receives partner split ^ k's partial of this CTA's
+// columns (128 x CW floats in 16-byte units: unit u of head h's columns in
+// column group cg at (cg * GW / 4 + u) * 128 + h, so that one warp-wide
+// 16-byte store of 32 heads covers 512 contiguous bytes). The pushes go out
+// back to back, partner split ^ 1 first, each once that partner's tiles are
+// dead; the merge adds this CTA's partial, then split ^ 1, ^ 2, ^ 3.
 template <int NP>
-__device__ __forceinline__ void exchange_rounds(const TcParams& p, uint8_t* smem, uint32_t bars,
-                                                uint32_t lane_base, uint16_t* orow, float* lse,
-                                                float m, int h, int cg, int split, bool have_o,
-                                                bool& ok) {
+__device__ __forceinline__ void exchange_dsmem(const TcParams& p, uint8_t* smem, uint32_t bars,
+                                               uint32_t lane_base, uint16_t* oblock, float* lse,
+                                               float m, int h, int cg, int split, bool have_o,
+                                               bool& ok) {
     const int S = p.split;
     const int CW = kLatent / S, GW = CW / 4;
-    // Inbox of 128 x CW floats in 16-byte units: unit u of head h's columns in
-    // column group cg at (cg * GW / 4 + u) * 128 + h, so that one warp-wide
-    // 16-byte store (32 heads) covers 512 contiguous bytes.
+    const int units = 128 * CW / 4;  // 16-byte units per inbox
     float4* inbox = reinterpret_cast<float4*>(smem);
     const float* sums = reinterpret_cast<const float*>(smem + kOffSums);
     int32_t* status = p.a.status;
-    float acc[NP][32];
-#pragma unroll
-    for (int q = 0; q < NP; ++q) {
-        float own[32];
-        if (have_o)
-            tmem_ld32(lane_base + split * CW + cg * GW + 32 * q, own);
-        else
-            zero32(own);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) acc[q][j] = 0.f + own[j];
-    }
     for (int k = 1; k < S; ++k) {
         const int pr = split ^ k;
-        // The partner's inbox is free for this round.
         mbar_wait(bars + 8 * (kBarRoundFree + k - 1), 0, ok, status, p.budget_ns, /*always=*/true);
         const uint32_t rfull = mapa(bars + 8 * (kBarRoundFull + k - 1), pr);
-        const uint32_t dst = mapa(smem_addr(inbox + cg * (GW / 4) * 128 + h), pr);
+        const uint32_t dst = mapa(smem_addr(inbox + (k - 1) * units + cg * (GW / 4) * 128 + h), pr);
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
             float v[32];
@@ -433,11 +443,23 @@ __device__ __forceinline__ void exchange_rounds(const TcParams& p, uint8_t* smem
                 st_async_v4(dst + (8 * q + i) * 128 * 16,
                             make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]), rfull);
         }
-        // The partner's partial of this CTA's columns has landed.
+    }
+    float acc[NP][32];
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+        float own[32];
+        if (have_o)
+            tmem_ld32(lane_base + split * CW + cg * GW + 32 * q, own);
+        else
+            zero32(own);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[q][j] = 0.f + own[j];
+    }
+    for (int k = 1; k < S; ++k) {
         mbar_wait(bars + 8 * (kBarRoundFull + k - 1), 0, ok, status, p.budget_ns, /*always=*/true);
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
-            const float4* src = inbox + (cg * (GW / 4) + 8 * q) * 128 + h;
+            const float4* src = inbox + (k - 1) * units + (cg * (GW / 4) + 8 * q) * 128 + h;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const float4 x = src[i * 128];
@@ -447,20 +469,19 @@ __device__ __forceinline__ void exchange_rounds(const TcParams& p, uint8_t* smem
                 acc[q][4 * i + 3] += x.w;
             }
         }
-        __syncthreads();  // the inbox is consumed
-        if (threadIdx.x == 0 && k + 1 < S)
-            mbar_arrive_remote(mapa(bars + 8 * (kBarRoundFree + k), split ^ (k + 1)));
     }
     mbar_wait(bars + 8 * kBarIn, 0, ok, status, p.budget_ns, /*always=*/true);
-    ok = __syncthreads_and(ok) != 0;
+    ok = __syncthreads_and(ok) != 0;  // also: every inbox is consumed
     if (!ok) return;
     float total = 0.f + sums[split * 128 + h];
     for (int k = 1; k < S; ++k) total += sums[(split ^ k) * 128 + h];
     const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
 #pragma unroll
-    for (int q = 0; q < NP; ++q) store_bf16x32(orow + split * CW + cg * GW + 32 * q, acc[q], inv);
+    for (int q = 0; q < NP; ++q) stage_bf16x32(smem, CW * 2, h, cg * GW + 32 * q, acc[q], inv);
     if (split == 0 && cg == 0)
         *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f : -INFINITY;
+    __syncthreads();
+    flush_tile(smem, CW * 2, oblock);
 }
 
 // ---- all 16 warps: partial exchange, merge and output -----------------------------
@@ -482,11 +503,12 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
     if (cg == 0) sums[split * 128 + h] = l;  // read after the barriers below
     int32_t* status = p.a.status;
     const bool have_o = ok && r.mine > 0;  // O in TMEM is defined only if PV ran
-    uint16_t* orow = p.a.out + (static_cast<int64_t>(b) * p.a.H + group * kTcHeads + h) * kLatent;
+    // Head 0 of the group; this CTA writes columns [split * CW, split * CW + CW).
+    uint16_t* oblock = p.a.out + (static_cast<int64_t>(b) * p.a.H + group * kTcHeads) * kLatent;
     float* lse = p.a.lse + static_cast<int64_t>(b) * p.a.H + group * kTcHeads + h;
 
     if (S == 1) {
-        if (ok) {
+        if (ok) {  // uniform: set by the barrier before the finish
             const float total = 0.f + l;
             const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
             for (int q = 0; q < kLatent / 128; ++q) {
@@ -498,11 +520,13 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
                     zero32(v);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.f + v[j];
-                store_bf16x32(orow + col, v, inv);
+                stage_bf16x32(smem, kLatent * 2, h, col, v, inv);
             }
             if (cg == 0)
                 *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f
                                    : -INFINITY;
+            __syncthreads();
+            flush_tile(smem, kLatent * 2, oblock);
         }
         return;
     }
@@ -582,11 +606,13 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
                         }
                     }
                 }
-                store_bf16x32(orow + col, acc, inv);
+                stage_bf16x32(smem, CW * 2, h, col - split * CW, acc, inv);
             }
             if (split == 0 && cg == 0)
                 *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f
                                    : -INFINITY;
+            __syncthreads();
+            flush_tile(smem, CW * 2, oblock + split * CW);
         }
         __syncthreads();  // every read of the peers' slots is done
         if (threadIdx.x == 0)
@@ -596,22 +622,27 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
         return;
     }
 
-    // ---- DSMEM exchange in pairwise rounds: in round k this CTA and its
-    // partner split ^ k swap their partials of each other's columns (pairwise
-    // traffic sustains about twice the all-to-all rate on this part). One
-    // inbox lies over this CTA's tiles: round 1 may start once the partner's
-    // PV is done, round k + 1 once the partner has consumed round k.
+    // ---- DSMEM exchange: one inbox per partner over this CTA's dead tiles
+    // (P and the ring); partner split ^ k pushes into inbox k - 1.
     if (cg == 0)
         for (int k = 1; k < S; ++k) {
             const int pr = split ^ k;
             st_async_b32(mapa(smem_addr(sums + split * 128 + h), pr), __float_as_uint(l),
                          mapa(bars + 8 * kBarIn, pr));
         }
-    if (threadIdx.x == 0) mbar_arrive_remote(mapa(bars + 8 * kBarRoundFree, split ^ 1));
+    // This CTA's tiles are dead: every partner may push into its inbox here.
+    // The signal is a 4-byte st.async completing on the partner's barrier (a
+    // cluster-scope release arrive costs about 3 us here).
+    if (threadIdx.x == 0)
+        for (int k = 1; k < S; ++k) {
+            const int pr = split ^ k;
+            st_async_b32(mapa(smem_addr(smem + kOffFlags + 4 * k), pr), 1u,
+                         mapa(bars + 8 * (kBarRoundFree + k - 1), pr));
+        }
     if (S == 2)
-        exchange_rounds<2>(p, smem, bars, lane_base, orow, lse, m, h, cg, split, have_o, ok);
+        exchange_dsmem<2>(p, smem, bars, lane_base, oblock + split * CW, lse, m, h, cg, split, have_o, ok);
     else
-        exchange_rounds<1>(p, smem, bars, lane_base, orow, lse, m, h, cg, split, have_o, ok);
+        exchange_dsmem<1>(p, smem, bars, lane_base, oblock + split * CW, lse, m, h, cg, split, have_o, ok);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -654,8 +685,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // The peers' sums; on the DSMEM path, round k's partial of this CTA's columns.
         mbar_arrive_expect_tx(bars + 8 * kBarIn, (S - 1) * 128 * 4);
         if (p.ws == nullptr)
-            for (int k = 1; k < S; ++k)
+            for (int k = 1; k < S; ++k) {
+                mbar_arrive_expect_tx(bars + 8 * (kBarRoundFree + k - 1), 4);
                 mbar_arrive_expect_tx(bars + 8 * (kBarRoundFull + k - 1), 128 * CW * 4);
+            }
     }
     if (warp == 8) tmem_alloc(base + kOffTmem, 512);
     tc_fence_before();
