@@ -334,17 +334,21 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
 
     // ---- partials to the column owners (FP32 bits over DSMEM) ----------------
     // acc[t][j][e]: head 16t + g + 8(e>>1), column 32*warp + 8*qd + 4*(e&1) + j.
+    // The inbox holds 16-byte units (columns j = 0..3 of one (t, e, lane)):
+    // unit ((((src * WPO + wl) * T + t) * 4 + e) * 32 + lane) for the partial
+    // of CTA src from warp wl of the owner's WPO = CW / 32 column warps, so one
+    // warp-wide store covers 512 contiguous bytes.
+    const int WPO = CW / 32;
     {
-        const int owner = (32 * warp) / CW;
+        const int owner = warp / WPO;
+        const int wl = warp - owner * WPO;
         const uint32_t inbox_s = smem_addr(inbox);
 #pragma unroll
         for (int t = 0; t < T; ++t) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int h = 16 * t + g + 8 * (e >> 1);
-                const int col = 32 * warp + 8 * qd + 4 * (e & 1);
                 const float4 v = make_float4(acc[t][0][e], acc[t][1][e], acc[t][2][e], acc[t][3][e]);
-                const uint32_t dst = inbox_s + ((split * CH + h) * CW + (col - owner * CW)) * 4;
+                const uint32_t dst = inbox_s + (((((split * WPO + wl) * T + t) * 4 + e) * 32) + lane) * 16;
                 if (owner == split)
                     sts_v4(dst, v);
                 else
@@ -364,13 +368,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
 
     // ---- merge in CTA order; BF16(sum * k_scale / total) ---------------------
     if (ok) {
-        const int per_row = CW / 4;
-        for (int it = tid; it < CH * per_row; it += kMmaThreads) {
-            const int h = it / per_row, c4 = it % per_row;
+        const int units = WPO * T * 128;  // 16-byte units of one CTA's partial of my columns
+        const float4* in4 = reinterpret_cast<const float4*>(inbox);
+        for (int u = tid; u < units; u += kMmaThreads) {
+            const int ln = u & 31, e = (u >> 5) & 3, t = (u >> 7) % T, wl = (u >> 7) / T;
+            const int h = 16 * t + (ln >> 2) + 8 * (e >> 1);
+            const int c = 32 * wl + 8 * (ln & 3) + 4 * (e & 1);
             float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
             float total = 0.f;
             for (int src = 0; src < S; ++src) {
-                const float4 v = *reinterpret_cast<const float4*>(inbox + (src * CH + h) * CW + 4 * c4);
+                const float4 v = in4[src * units + u];
                 m.x += v.x;
                 m.y += v.y;
                 m.z += v.z;
@@ -382,7 +389,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
             packed.x = bf16x2(m.x * inv, m.y * inv);
             packed.y = bf16x2(m.z * inv, m.w * inv);
             uint16_t* dst = p.a.out + (static_cast<int64_t>(b) * p.a.H + head0 + h) * kLatent +
-                            split * CW + 4 * c4;
+                            split * CW + c;
             *reinterpret_cast<uint2*>(dst) = packed;
         }
         if (split == 0) {
