@@ -9,7 +9,9 @@ top-k 256, counts U[200,256] with one empty row, a 65536-row E4M3 pool).
 
 Timing: W untimed warm-up steps, then K timed steps between a barrier and
 torch.cuda.synchronize() on both sides. L2 is flushed before every step by
-reading a buffer twice the L2 size; each decode call is bracketed by CUDA
+writing a buffer twice the L2 size and then reading another one (no dirty
+line is left to be written back during the decode); each decode call is
+bracketed by CUDA
 events on the stream it is launched on, so ``ms_per_step`` is decode time only.
 ``value`` is the gathered-KV throughput (576 bytes per (row, key)) of all
 ranks; ``e2e`` is the same metric through the public call with the step's
@@ -186,6 +188,10 @@ def run_gpu(args, world, rank, local) -> dict | None:
     out = torch.empty((case.B, case.H, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((case.B, case.H), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    # L2 flush: write a buffer twice the L2 size, then read another one of that
+    # size, so that no dirty line of the write is left to be written back
+    # inside the timed region.
+    flush_w = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     flush_out = torch.empty((), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -204,6 +210,7 @@ def run_gpu(args, world, rank, local) -> dict | None:
             raise binding.SmdError(rc, "decode")
 
     def l2_flush():
+        flush_w.zero_()
         torch.sum(flush, dim=0, out=flush_out)
 
     # Warm-up (also JIT/module load).
@@ -319,7 +326,7 @@ def run_gpu(args, world, rank, local) -> dict | None:
             "name": args.config,
             "B": case.B, "H": case.H, "top_k": case.W, "pool_rows": case.N,
             "gathered_keys": case.gathered_rows(), "unique_rows": case.unique_rows(),
-            "l2": "flushed before every timed step (read of a 2x-L2 buffer, outside the events)",
+            "l2": "flushed before every timed step (write of a 2x-L2 buffer, then read of another, outside the events)",
             "plan": plan,
             "workspace_bytes": int(ws_bytes),
             "parallelism": f"replicas x{world}",

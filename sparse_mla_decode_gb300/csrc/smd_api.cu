@@ -17,7 +17,6 @@ namespace smd {
 namespace {
 
 constexpr int kMaxSmemBytes = 227 * 1024;  // dynamic shared memory per CTA on sm_103
-constexpr int kSpecIdxMaxW = 2048;        // widest row whose index list is loaded up front
 
 struct DeviceInfo {
     int sm_count = 0;

@@ -14,6 +14,7 @@ constexpr int kLatent = 512;     // columns read by PV
 constexpr int kHeadsPerTile = 16;
 constexpr int kRowPitch = 592;   // shared-memory pitch of a 576-byte row (bank spread)
 constexpr int kChunk = 64;       // keys per gather barrier
+constexpr int kSpecIdxMaxW = 2048;  // widest row whose index list the warp-MMA kernel loads up front
 constexpr int kMmaThreads = 512; // 16 warps; PV warp w owns latent columns 32w..32w+31
 
 // Everything a kernel needs to know about one call.

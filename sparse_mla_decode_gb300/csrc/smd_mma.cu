@@ -14,8 +14,9 @@
 // reduction runs in a fixed order that depends neither on timing nor on the
 // number of 16-head tiles a CTA takes.
 //
-// Pass A per window of resident keys: each 576-byte cache row is one
-// cp.async.bulk into shared memory (one mbarrier per 64 keys); QK is
+// Pass A per window of resident keys: the 576-byte cache rows come into
+// shared memory as 16-byte cp.async copies spread over all threads (one
+// mbarrier per 64 keys, one arrival per thread); QK is
 // mma.sync m16n8k32 E4M3 x E4M3 -> FP32 over the 576 columns (a warp job is
 // 16 heads x 8 keys, two accumulation chains over the 18 k-steps); the
 // scaled logits go to shared memory. Pass B per window: P for 64 keys of a
@@ -48,23 +49,24 @@ struct MmaParams {
 };
 
 // Issues the gathers of keys [w0, w0 + wn) of this CTA into the window
-// buffer: `bytes` of each row (576 for QK+PV, 512 when only V is needed).
-// Rows [wn, roundup32(wn)) are zeroed.
+// buffer: `bytes` of each row (576 for QK+PV, 512 when only V is needed), as
+// 16-byte copies spread over all threads (consecutive threads, consecutive
+// pieces of a row). Every thread arrives on the barrier of each 64-key chunk
+// once its copies of the chunk have landed. Rows [wn, roundup32(wn)) are zeroed.
 __device__ __forceinline__ void gather_window(const MmaParams& p, uint32_t kv_s,
                                               const int32_t* idx_s, uint32_t bars, int w0,
-                                              int wn, uint32_t bytes, uint64_t policy) {
+                                              int wn, uint32_t bytes) {
     // idx_s points at this CTA's first key.
     const int tid = threadIdx.x;
-    if (tid == 0) {
-        for (int c = 0; c * kChunk < wn; ++c) {
-            const int cnt = min(kChunk, wn - c * kChunk);
-            mbar_arrive_expect_tx(bars + 8 * c, cnt * bytes);
+    const int per_row = static_cast<int>(bytes) / 16;
+    for (int c = 0; c * kChunk < wn; ++c) {
+        const int r0 = c * kChunk, cnt = min(kChunk, wn - r0);
+        for (int e = tid; e < cnt * per_row; e += kMmaThreads) {
+            const int r = e / per_row, c16 = e - r * per_row;
+            const int64_t j = idx_s[w0 + r0 + r];
+            cp_async16(kv_s + (r0 + r) * kRowPitch + 16 * c16, p.a.kv + j * kRow + 16 * c16);
         }
-    }
-    for (int i = tid; i < wn; i += kMmaThreads) {
-        const int64_t j = idx_s[w0 + i];
-        const uint8_t* src = p.a.kv + j * kRow;
-        bulk_g2s_stream(kv_s + i * kRowPitch, src, bytes, bars + 8 * (i / kChunk), policy);
+        cp_async_arrive(bars + 8 * c);
     }
     const int span = (wn + 31) & ~31;
     for (int e = wn * (kRow / 16) + tid; e < span * (kRow / 16); e += kMmaThreads) {
@@ -108,8 +110,22 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     bool ok = true;
     int32_t* status = p.a.status;
 
+    // The row's count and (when the row is at most kSpecIdxMaxW wide) its whole
+    // index list are loaded first, in one round trip that the setup below
+    // overlaps; the loads do not depend on each other.
+    const int W = p.a.W;
+    const int32_t* row_idx = p.a.indices + static_cast<int64_t>(b) * W;
+    int n = p.a.counts[b];
+    constexpr int kSpecPerThread = kSpecIdxMaxW / kMmaThreads;
+    int32_t spec[kSpecPerThread];
+#pragma unroll
+    for (int k = 0; k < kSpecPerThread; ++k) {
+        const int i = tid + k * kMmaThreads;
+        spec[k] = (p.spec_idx && i < W) ? row_idx[i] : 0;
+    }
+
     if (tid == 0) {
-        for (int c = 0; c < nchunk_bars; ++c) mbar_init(bars + 8 * c, 1);
+        for (int c = 0; c < nchunk_bars; ++c) mbar_init(bars + 8 * c, kMmaThreads);
         mbar_init(q_bar, 1);
         mbar_init(max_bar, 1);
         mbar_init(in_bar, 1);
@@ -134,14 +150,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     }
 
     // ---- this CTA's keys: [first, first + mine) of the row ------------------
-    // With spec_idx the row's whole index list is loaded in the same round
-    // trip as its count (the loads do not depend on each other), so the
-    // gathers wait for one DRAM latency instead of two.
-    const int W = p.a.W;
-    const int32_t* row_idx = p.a.indices + static_cast<int64_t>(b) * W;
-    int n = p.a.counts[b];
-    if (p.spec_idx)
-        for (int i = tid; i < W; i += kMmaThreads) idx_s[i] = row_idx[i];
+    // With spec_idx the index list came with the count, so the gathers wait
+    // for one DRAM latency instead of two.
+    if (p.spec_idx) {
+#pragma unroll
+        for (int k = 0; k < kSpecPerThread; ++k) {
+            const int i = tid + k * kMmaThreads;
+            if (i < W) idx_s[i] = spec[k];
+        }
+    }
     n = max(min(n, W), 0);
     const int per = (n + S - 1) / S;
     const int first = min(n, split * per);
@@ -151,7 +168,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     const int32_t* my_idx = idx_s + (p.spec_idx ? first : 0);
     __syncthreads();
 
-    const uint64_t policy = policy_evict_normal();
     const float neg_inf = -INFINITY;
     const float lam = p.a.scale_log2;
     const int nwin = (mine + p.window - 1) / p.window;
@@ -169,7 +185,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         const int w0 = wi * p.window;
         const int wn = min(p.window, mine - w0);
         if (!__syncthreads_and(ok)) break;  // a failed CTA issues no more copies
-        gather_window(p, kv_s, my_idx, bars, w0, wn, kRow, policy);
+        gather_window(p, kv_s, my_idx, bars, w0, wn, kRow);
         __syncthreads();  // zeroed tail rows
         for (int c = 0; c * kChunk < wn; ++c) {
             const int cnt = min(kChunk, wn - c * kChunk);
@@ -203,7 +219,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
             }
         }
         __syncthreads();  // the window buffer is free again
-        fence_proxy_async();  // ... also for the bulk copies that refill it
     }
 
     // ---- the row maximum over the cluster ------------------------------------
@@ -248,7 +263,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         const bool regather = (wi != nwin - 1);
         if (!__syncthreads_and(ok)) break;
         if (regather) {
-            gather_window(p, kv_s, my_idx, bars, w0, wn, kLatent, policy);
+            gather_window(p, kv_s, my_idx, bars, w0, wn, kLatent);
             __syncthreads();
         }
         // Chunks in descending order too: the row's chunks are then summed in
@@ -299,7 +314,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
             }
         }
         __syncthreads();  // window buffer and P free for the next window
-        fence_proxy_async();
     }
 
     if (S == 1) {
@@ -329,6 +343,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
                                 : -INFINITY;
             }
         }
+        cp_async_wait_all();  // after a failed wait, no copy may land once the CTA is gone
         return;
     }
 
@@ -403,6 +418,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
             }
         }
     }
+    cp_async_wait_all();
 }
 
 // Function attributes are set once per device and kernel (and again only when

@@ -88,6 +88,23 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
+// One 16-byte global -> shared copy through the load/store unit, bypassing L1
+// (both addresses 16-byte aligned).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// This thread's arrival on `bar`, made once every cp.async it has issued so
+// far has landed (the barrier counts one arrival per participating thread).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Waits until every cp.async this thread has issued has landed.
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // As bulk_g2s, with an L2 evict-first policy (data read once).
 __device__ __forceinline__ void bulk_g2s_stream(uint32_t dst, const void* src, uint32_t bytes,
                                                 uint32_t bar, uint64_t policy) {
