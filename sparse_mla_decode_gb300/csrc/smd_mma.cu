@@ -14,12 +14,13 @@
 // reduction runs in a fixed order that depends neither on timing nor on the
 // number of 16-head tiles a CTA takes.
 //
-// Pass A per window of resident keys: the 576-byte cache rows come into
-// shared memory as 16-byte cp.async copies spread over all threads (one
-// mbarrier per 64 keys, one arrival per thread); QK is
-// mma.sync m16n8k32 E4M3 x E4M3 -> FP32 over the 576 columns (a warp job is
-// 16 heads x 8 keys, two accumulation chains over the 18 k-steps); the
-// scaled logits go to shared memory. Pass B per window: P for 64 keys of a
+// The keys pass through a ring of 64-key slots. Pass A per chunk: the
+// 576-byte cache rows come into shared memory as 16-byte cp.async copies
+// spread over all threads (one mbarrier per slot, one arrival per thread),
+// issued a ring's length ahead of their use; QK is mma.sync m16n8k32 E4M3 x
+// E4M3 -> FP32 over the 576 columns (a warp job is 16 heads x 16 keys, two
+// accumulation chains per 8 keys over the 18 k-steps); the scaled logits go
+// to shared memory. Pass B per chunk, descending: P for 64 keys of a
 // head per warp (lane: a key pair, stored as an E4M3 pair), the FP32 sum of
 // the unquantized P by a fixed butterfly, then PV: warp w owns latent columns
 // 32w..32w+31, V read as words and byte-transposed in registers into the MMA's
@@ -48,30 +49,29 @@ struct MmaParams {
     int32_t spec_idx;    // 1: load the row's whole index list with the count
 };
 
-// Issues the gathers of keys [w0, w0 + wn) of this CTA into the window
-// buffer: `bytes` of each row (576 for QK+PV, 512 when only V is needed), as
-// 16-byte copies spread over all threads (consecutive threads, consecutive
-// pieces of a row). Every thread arrives on the barrier of each 64-key chunk
-// once its copies of the chunk have landed. Rows [wn, roundup32(wn)) are zeroed.
-__device__ __forceinline__ void gather_window(const MmaParams& p, uint32_t kv_s,
-                                              const int32_t* idx_s, uint32_t bars, int w0,
-                                              int wn, uint32_t bytes) {
-    // idx_s points at this CTA's first key.
-    const int tid = threadIdx.x;
+// Issues the gathers of one chunk of `cnt` <= 64 keys (`keys`: their pool
+// rows) into a ring slot: `bytes` of each row (576 for QK + PV, 512 when only
+// V is needed), as 16-byte copies spread over all threads. Every thread
+// arrives on the slot's barrier once its copies have landed. Rows
+// [cnt, roundup32(cnt)) are zeroed.
+__device__ __forceinline__ void gather_chunk(const MmaParams& p, uint32_t slot_s,
+                                             const int32_t* keys, uint32_t bar, int cnt,
+                                             uint32_t bytes) {
+    // Warp w copies rows w, w + 16, ...; lane l the row's 16-byte pieces l
+    // and l + 32 (36 pieces per 576-byte row, 32 per 512-byte V row).
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int per_row = static_cast<int>(bytes) / 16;
-    for (int c = 0; c * kChunk < wn; ++c) {
-        const int r0 = c * kChunk, cnt = min(kChunk, wn - r0);
-        for (int e = tid; e < cnt * per_row; e += kMmaThreads) {
-            const int r = e / per_row, c16 = e - r * per_row;
-            const int64_t j = idx_s[w0 + r0 + r];
-            cp_async16(kv_s + (r0 + r) * kRowPitch + 16 * c16, p.a.kv + j * kRow + 16 * c16);
-        }
-        cp_async_arrive(bars + 8 * c);
+    for (int r = warp; r < cnt; r += kMmaThreads / 32) {
+        const uint8_t* src = p.a.kv + static_cast<int64_t>(keys[r]) * kRow;
+        const uint32_t dst = slot_s + r * kRowPitch;
+        cp_async16(dst + 16 * lane, src + 16 * lane);
+        if (lane + 32 < per_row) cp_async16(dst + 16 * (lane + 32), src + 16 * (lane + 32));
     }
-    const int span = (wn + 31) & ~31;
-    for (int e = wn * (kRow / 16) + tid; e < span * (kRow / 16); e += kMmaThreads) {
+    cp_async_arrive(bar);
+    const int span = (cnt + 31) & ~31;
+    for (int e = cnt * (kRow / 16) + threadIdx.x; e < span * (kRow / 16); e += kMmaThreads) {
         const int r = e / (kRow / 16), c16 = e % (kRow / 16);
-        sts_zero16(kv_s + r * kRowPitch + 16 * c16);
+        sts_zero16(slot_s + r * kRowPitch + 16 * c16);
     }
 }
 
@@ -170,8 +170,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
 
     const float neg_inf = -INFINITY;
     const float lam = p.a.scale_log2;
-    const int nwin = (mine + p.window - 1) / p.window;
-    // Parity of the next completion of each gather barrier (bit c: barrier c).
+    // The KV buffer is a ring of NS slots of 64 keys; chunk c (keys
+    // 64c .. 64c + 63 of this CTA) goes to slot c % NS.
+    const int NS = p.window / kChunk;
+    const int nch = (mine + kChunk - 1) / kChunk;
+    // Parity of the next completion of each slot's barrier (bit s: slot s).
     uint32_t phase_bits = 0;
 
     // ldmatrix lane addressing: A (16 rows x 32 B), B (8 keys x 64 B).
@@ -181,44 +184,58 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     mbar_wait(q_bar, 0, ok, status, p.budget_ns);
 
     // ================================ pass A: logits =========================
-    for (int wi = 0; wi < nwin; ++wi) {
-        const int w0 = wi * p.window;
-        const int wn = min(p.window, mine - w0);
-        if (!__syncthreads_and(ok)) break;  // a failed CTA issues no more copies
-        gather_window(p, kv_s, my_idx, bars, w0, wn, kRow);
-        __syncthreads();  // zeroed tail rows
-        for (int c = 0; c * kChunk < wn; ++c) {
-            const int cnt = min(kChunk, wn - c * kChunk);
-            mbar_wait(bars + 8 * c, (phase_bits >> c) & 1u, ok, status, p.budget_ns);
-            phase_bits ^= 1u << c;
-            for (int job = warp; job < 8 * T; job += kMmaThreads / 32) {
-                const int t = job >> 3, kg = job & 7;
-                if (8 * kg >= cnt) continue;
-                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-                const uint32_t kaddr =
-                    kv_s + (c * kChunk + 8 * kg + (lane & 7)) * kRowPitch + 16 * (lane >> 3);
-                const uint32_t qaddr = q_s + (16 * t + a_row) * kRowPitch + a_col;
+    // The gather of chunk c + NS is issued as soon as QK of chunk c has left
+    // its slot, so copies and QK overlap.
+    for (int c = 0; c < min(NS, nch); ++c)
+        gather_chunk(p, kv_s + c * kChunk * kRowPitch, my_idx + c * kChunk, bars + 8 * c,
+                     min(kChunk, mine - c * kChunk), kRow);
+    for (int c = 0; c < nch; ++c) {
+        const int s = c % NS;
+        const int cnt = min(kChunk, mine - c * kChunk);
+        const uint32_t slot_s = kv_s + s * kChunk * kRowPitch;
+        mbar_wait(bars + 8 * s, (phase_bits >> s) & 1u, ok, status, p.budget_ns);
+        phase_bits ^= 1u << s;
+        // Warp job: 16 heads (tile t) x 16 keys (two 8-key n-tiles), so each
+        // query fragment read from shared memory serves two MMAs; per n-tile
+        // two accumulation chains (the two 32-byte halves of every 64-byte
+        // k-step), added once at the end.
+        for (int job = warp; job < 4 * T; job += kMmaThreads / 32) {
+            const int t = job >> 2, kg = job & 3;
+            if (16 * kg >= cnt) continue;
+            float c0[2][4] = {}, c1[2][4] = {};
+            const uint32_t kaddr = slot_s + (16 * kg + (lane & 7)) * kRowPitch + 16 * (lane >> 3);
+            const uint32_t qaddr = q_s + (16 * t + a_row) * kRowPitch + a_col;
 #pragma unroll
-                for (int kp = 0; kp < kRow / 64; ++kp) {
-                    uint32_t kb[4], qa[4], qb[4];
-                    ldsm_x4(kaddr + 64 * kp, kb);
-                    ldsm_x4(qaddr + 64 * kp, qa);
-                    ldsm_x4(qaddr + 64 * kp + 32, qb);
-                    mma_e4m3(c0, qa, kb[0], kb[1]);
-                    mma_e4m3(c1, qb, kb[2], kb[3]);
-                }
-                const int key = c * kChunk + 8 * kg + 2 * qd;  // within the window
+            for (int kp = 0; kp < kRow / 64; ++kp) {
+                uint32_t kb0[4], kb1[4], qa[4], qb[4];
+                ldsm_x4(qaddr + 64 * kp, qa);
+                ldsm_x4(qaddr + 64 * kp + 32, qb);
+                ldsm_x4(kaddr + 64 * kp, kb0);
+                ldsm_x4(kaddr + 8 * kRowPitch + 64 * kp, kb1);
+                mma_e4m3(c0[0], qa, kb0[0], kb0[1]);
+                mma_e4m3(c1[0], qb, kb0[2], kb0[3]);
+                mma_e4m3(c0[1], qa, kb1[0], kb1[1]);
+                mma_e4m3(c1[1], qb, kb1[2], kb1[3]);
+            }
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                const int kk = 16 * kg + 8 * n + 2 * qd;  // within the chunk
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const float s0 = (key < wn) ? lam * (c0[2 * r] + c1[2 * r]) : neg_inf;
-                    const float s1 = (key + 1 < wn) ? lam * (c0[2 * r + 1] + c1[2 * r + 1]) : neg_inf;
+                    const float s0 = (kk < cnt) ? lam * (c0[n][2 * r] + c1[n][2 * r]) : neg_inf;
+                    const float s1 =
+                        (kk + 1 < cnt) ? lam * (c0[n][2 * r + 1] + c1[n][2 * r + 1]) : neg_inf;
                     float2* dst = reinterpret_cast<float2*>(
-                        logits + (16 * t + g + 8 * r) * LP + w0 + key);
+                        logits + (16 * t + g + 8 * r) * LP + c * kChunk + kk);
                     *dst = make_float2(s0, s1);
                 }
             }
         }
-        __syncthreads();  // the window buffer is free again
+        // The slot is free; a failed CTA issues no more copies.
+        if (!__syncthreads_and(ok)) break;
+        if (c + NS < nch)
+            gather_chunk(p, slot_s, my_idx + (c + NS) * kChunk, bars + 8 * s,
+                         min(kChunk, mine - (c + NS) * kChunk), kRow);
     }
 
     // ---- the row maximum over the cluster ------------------------------------
@@ -255,65 +272,60 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[t][j][e] = 0.f;
 
-    // Windows in reverse: the last window of pass A is still resident. Every
-    // chunk's P and PV terms are added in descending chunk order.
-    for (int wi = nwin - 1; wi >= 0; --wi) {
-        const int w0 = wi * p.window;
-        const int wn = min(p.window, mine - w0);
-        const bool regather = (wi != nwin - 1);
+    // Chunks in descending order, so every row's chunks are summed in one
+    // global order whatever the ring size: the last NS chunks are still
+    // resident; chunk c - NS comes back (V columns only) into the slot of
+    // chunk c once PV of chunk c has left it.
+    for (int c = nch - 1; c >= 0; --c) {
+        const int s = c % NS;
+        const int cnt = min(kChunk, mine - c * kChunk);
+        const uint32_t slot_s = kv_s + s * kChunk * kRowPitch;
+        if (c < nch - NS) {
+            mbar_wait(bars + 8 * s, (phase_bits >> s) & 1u, ok, status, p.budget_ns);
+            phase_bits ^= 1u << s;
+        }
+        // P of 64 keys x this warp's heads; lane: keys 2*lane, 2*lane + 1.
+#pragma unroll
+        for (int i = 0; i < T; ++i) {
+            const int h = warp + 16 * i;
+            const float bias = rowmax[h] - p.log2_448;
+            const int kk = 2 * lane;
+            const float2 sv = *reinterpret_cast<const float2*>(logits + h * LP + c * kChunk + kk);
+            const float p0 = (kk < cnt) ? ex2_approx(sv.x - bias) : 0.f;
+            const float p1 = (kk + 1 < cnt) ? ex2_approx(sv.y - bias) : 0.f;
+            sts_u16(prob_s + h * PP + kk, e4m3x2(p0, p1));
+            const float tot = warp_sum(p0 + p1);
+            if (lane == 0) lsum[h] += tot;
+        }
+        __syncthreads();
+        // PV: latent columns 32*warp + 4*g + (0..3), every tile.
+        const int span = (cnt + 31) & ~31;
+#pragma unroll
+        for (int ks = 0; ks < kChunk / 32; ++ks) {
+            if (32 * ks >= span) break;
+            uint32_t vb[2][4];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int key = 32 * ks + 16 * hf + 4 * qd + i;
+                    w[i] = lds_u32(slot_s + key * kRowPitch + 32 * warp + 4 * g);
+                }
+                byte_transpose4(w[0], w[1], w[2], w[3], vb[hf]);
+            }
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+                uint32_t pa[4];
+                ldsm_x4(prob_s + (16 * t + a_row) * PP + 32 * ks + a_col, pa);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) mma_e4m3(acc[t][j], pa, vb[0][j], vb[1][j]);
+            }
+        }
+        // The slot and P are free; a failed CTA issues no more copies.
         if (!__syncthreads_and(ok)) break;
-        if (regather) {
-            gather_window(p, kv_s, my_idx, bars, w0, wn, kLatent);
-            __syncthreads();
-        }
-        // Chunks in descending order too: the row's chunks are then summed in
-        // one global order whatever the window size.
-        for (int c = (wn - 1) / kChunk; c >= 0; --c) {
-            const int cnt = min(kChunk, wn - c * kChunk);
-            if (regather) {
-                mbar_wait(bars + 8 * c, (phase_bits >> c) & 1u, ok, status, p.budget_ns);
-                phase_bits ^= 1u << c;
-            }
-            // P of 64 keys x this warp's heads; lane: keys 2*lane, 2*lane + 1.
-#pragma unroll
-            for (int i = 0; i < T; ++i) {
-                const int h = warp + 16 * i;
-                const float bias = rowmax[h] - p.log2_448;
-                const int k = c * kChunk + 2 * lane;
-                const float2 sv = *reinterpret_cast<const float2*>(logits + h * LP + w0 + k);
-                const float p0 = (k < wn) ? ex2_approx(sv.x - bias) : 0.f;
-                const float p1 = (k + 1 < wn) ? ex2_approx(sv.y - bias) : 0.f;
-                sts_u16(prob_s + h * PP + k, e4m3x2(p0, p1));
-                const float tot = warp_sum(p0 + p1);
-                if (lane == 0) lsum[h] += tot;
-            }
-            __syncthreads();
-            // PV: latent columns 32*warp + 4*g + (0..3), every tile.
-            const int span = (cnt + 31) & ~31;
-#pragma unroll
-            for (int ks = 0; ks < kChunk / 32; ++ks) {
-                if (32 * ks >= span) break;
-                uint32_t vb[2][4];
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int key = c * kChunk + 32 * ks + 16 * hf + 4 * qd + i;
-                        w[i] = lds_u32(kv_s + key * kRowPitch + 32 * warp + 4 * g);
-                    }
-                    byte_transpose4(w[0], w[1], w[2], w[3], vb[hf]);
-                }
-#pragma unroll
-                for (int t = 0; t < T; ++t) {
-                    uint32_t pa[4];
-                    ldsm_x4(prob_s + (16 * t + a_row) * PP + c * kChunk + 32 * ks + a_col, pa);
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) mma_e4m3(acc[t][j], pa, vb[0][j], vb[1][j]);
-                }
-            }
-        }
-        __syncthreads();  // window buffer and P free for the next window
+        if (c - NS >= 0)
+            gather_chunk(p, slot_s, my_idx + (c - NS) * kChunk, bars + 8 * s, kChunk, kLatent);
     }
 
     if (S == 1) {

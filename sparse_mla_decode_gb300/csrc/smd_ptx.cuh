@@ -204,10 +204,11 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
 
 // ------------------------------------------------------------------ math --
 
-// D(16x8, f32) += A(16x32, e4m3, row) * B(32x8, e4m3, col).
+// D(16x8, f32) += A(16x32, e4m3, row) * B(32x8, e4m3, col). Registers only,
+// so not volatile: the compiler may schedule it around independent loads.
 __device__ __forceinline__ void mma_e4m3(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
         "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
