@@ -122,15 +122,18 @@ int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
     return SMD_OK;
 }
 
+// The tcgen05 kernel takes 128 heads per CTA, or all H < 128 heads of a row
+// (the remaining TMEM lanes are padding that is computed and not stored).
 bool tc_fits(int H, int W) {
-    return H % kTcHeads == 0 && W >= 1 && W <= kTcMaxSplit * kTcMaxKeys;
+    return (H % kTcHeads == 0 || H < kTcHeads) && W >= 1 && W <= kTcMaxSplit * kTcMaxKeys;
 }
 
 // The tcgen05 kernel's plan: the smallest cluster whose CTAs hold at most
 // kTcMaxKeys keys each (all of them resident in TMEM as logits).
 int plan_tc(int B, int H, int W, const smd_plan_t* force, smd_plan_t* out, TcConfig* cfg) {
     if (!tc_fits(H, W)) return SMD_ERR_PLAN;
-    if (force && ((force->tiles && force->tiles != kTcHeads / kHeadsPerTile) ||
+    const int lanes = std::min(H, kTcHeads);
+    if (force && ((force->tiles && force->tiles != lanes / kHeadsPerTile) ||
                   (force->window && force->window != kTcChunk)))
         return SMD_ERR_PLAN;
     int split = 1;
@@ -147,10 +150,10 @@ int plan_tc(int B, int H, int W, const smd_plan_t* force, smd_plan_t* out, TcCon
     cfg->inject_stall = (force && force->inject_stall) ? 1 : 0;
     out->kernel = SMD_KERNEL_TC;
     out->split = split;
-    out->tiles = kTcHeads / kHeadsPerTile;
+    out->tiles = lanes / kHeadsPerTile;
     out->window = kTcChunk;
     out->key_cap = kTcMaxKeys;
-    out->grid_x = H / kTcHeads * split;
+    out->grid_x = ceil_div(H, kTcHeads) * split;
     out->grid_y = B;
     out->cluster_x = split;
     out->threads = kTcThreads;
@@ -171,7 +174,8 @@ int make_plan(int B, int H, int W, const smd_plan_t* force, smd_plan_t* out, Any
     std::call_once(once, [] { info = query_device(); });
     const int sm_count = info.ok ? info.sm_count : 152;
     int kernel = (force && force->kernel) ? force->kernel : SMD_KERNEL_AUTO;
-    if (kernel == SMD_KERNEL_AUTO) kernel = tc_fits(H, W) ? SMD_KERNEL_TC : SMD_KERNEL_MMA;
+    if (kernel == SMD_KERNEL_AUTO)
+        kernel = (H % kTcHeads == 0 && tc_fits(H, W)) ? SMD_KERNEL_TC : SMD_KERNEL_MMA;
     cfg->kernel = kernel;
     if (kernel == SMD_KERNEL_MMA) return plan_mma(B, H, W, sm_count, force, out, &cfg->mma);
     if (kernel == SMD_KERNEL_TC) return plan_tc(B, H, W, force, out, &cfg->tc);

@@ -85,6 +85,7 @@ struct TcParams {
     int32_t inject_stall;
     float* ws;          // L2 exchange workspace (ws_slots SM slots), or null: DSMEM exchange
     int32_t ws_slots;   // SM-id slots the workspace holds
+    int32_t lanes;      // heads a CTA computes (min(H, 128)); the other TMEM lanes are padding
 };
 
 __device__ __forceinline__ uint32_t sm_id() {
@@ -395,12 +396,13 @@ __device__ __forceinline__ void stage_bf16x32(uint8_t* stage, int row_bytes, int
             make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
 }
 
-// The staged 128-head tile to out (dst = head 0's first column; rows kLatent
-// BF16 apart), every warp-wide store covering whole rows of the tile. The
-// caller makes the staged tile visible to all threads first.
-__device__ __forceinline__ void flush_tile(const uint8_t* stage, int row_bytes, uint16_t* dst) {
+// The first `rows` heads of the staged tile to out (dst = head 0's first
+// column; rows kLatent BF16 apart), every warp-wide store covering whole rows
+// of the tile. The caller makes the staged tile visible to all threads first.
+__device__ __forceinline__ void flush_tile(const uint8_t* stage, int row_bytes, int rows,
+                                           uint16_t* dst) {
     const int chunks = row_bytes >> 4;
-    for (int e = threadIdx.x; e < 128 * chunks; e += kTcThreads) {
+    for (int e = threadIdx.x; e < rows * chunks; e += kTcThreads) {
         const int r = e / chunks, c = e - r * chunks;
         const uint4 v = *reinterpret_cast<const uint4*>(stage + r * row_bytes + ((c ^ (r & 7)) << 4));
         *reinterpret_cast<uint4*>(dst + static_cast<int64_t>(r) * kLatent + c * 8) = v;
@@ -478,10 +480,10 @@ __device__ __forceinline__ void exchange_dsmem(const TcParams& p, uint8_t* smem,
     const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
 #pragma unroll
     for (int q = 0; q < NP; ++q) stage_bf16x32(smem, CW * 2, h, cg * GW + 32 * q, acc[q], inv);
-    if (split == 0 && cg == 0)
+    if (split == 0 && cg == 0 && h < p.lanes)
         *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f : -INFINITY;
     __syncthreads();
-    flush_tile(smem, CW * 2, oblock);
+    flush_tile(smem, CW * 2, p.lanes, oblock);
 }
 
 // ---- all 16 warps: partial exchange, merge and output -----------------------------
@@ -522,11 +524,11 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
                 for (int j = 0; j < 32; ++j) v[j] = 0.f + v[j];
                 stage_bf16x32(smem, kLatent * 2, h, col, v, inv);
             }
-            if (cg == 0)
+            if (cg == 0 && h < p.lanes)
                 *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f
                                    : -INFINITY;
             __syncthreads();
-            flush_tile(smem, kLatent * 2, oblock);
+            flush_tile(smem, kLatent * 2, p.lanes, oblock);
         }
         return;
     }
@@ -608,11 +610,11 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
                 }
                 stage_bf16x32(smem, CW * 2, h, col - split * CW, acc, inv);
             }
-            if (split == 0 && cg == 0)
+            if (split == 0 && cg == 0 && h < p.lanes)
                 *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f
                                    : -INFINITY;
             __syncthreads();
-            flush_tile(smem, CW * 2, oblock + split * CW);
+            flush_tile(smem, CW * 2, p.lanes, oblock + split * CW);
         }
         __syncthreads();  // every read of the peers' slots is done
         if (threadIdx.x == 0)
@@ -855,6 +857,7 @@ int launch_tc(const CallArgs& a, const TcConfig& cfg, cudaStream_t stream) {
     prm.inject_stall = cfg.inject_stall;
     prm.ws = cfg.split > 1 ? cfg.ws : nullptr;
     prm.ws_slots = cfg.ws_slots > 0 ? cfg.ws_slots : kTcWsSlots;
+    prm.lanes = a.H < kTcHeads ? a.H : kTcHeads;
 
     static std::atomic<int> attr_set[kMaxDevices];
     int dev = 0;
@@ -866,7 +869,8 @@ int launch_tc(const CallArgs& a, const TcConfig& cfg, cudaStream_t stream) {
         attr_set[dev].store(1);
     }
     cudaLaunchConfig_t lc{};
-    lc.gridDim = dim3(static_cast<unsigned>(a.H / kTcHeads * cfg.split), static_cast<unsigned>(a.B), 1);
+    lc.gridDim = dim3(static_cast<unsigned>((a.H + kTcHeads - 1) / kTcHeads * cfg.split),
+                      static_cast<unsigned>(a.B), 1);
     lc.blockDim = dim3(kTcThreads, 1, 1);
     lc.dynamicSmemBytes = static_cast<size_t>(kSmemBytes);
     lc.stream = stream;

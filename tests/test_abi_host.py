@@ -97,7 +97,7 @@ def test_argument_checks(kw, code):
 @pytest.mark.parametrize("force", [
     dict(split=3), dict(split=32), dict(tiles=3), dict(tiles=4), dict(window=65),
     dict(window=4096), dict(kernel=9),
-    dict(kernel=2),                 # the tcgen05 kernel needs H % 128 == 0 (H = 16 here)
+    dict(kernel=2, tiles=2),        # the tcgen05 kernel takes all 16 heads of the row here
 ])
 def test_invalid_forced_plans_are_rejected(force):
     p = smd.SmdPlan()
@@ -149,6 +149,7 @@ def test_cpu_tensors_are_refused():
     (128, 2049, dict(kernel=2)),           # more than 4 x 512 keys
     (128, 2048, dict(kernel=2, split=2)),  # 1024 keys per CTA do not fit in TMEM
     (128, 64, dict(kernel=2, tiles=2)),    # the tcgen05 kernel's layout is fixed
+    (144, 64, dict(kernel=2)),             # above 128 heads only whole groups of 128
 ])
 def test_invalid_tc_plans_are_rejected(H, W, force):
     p = smd.SmdPlan()

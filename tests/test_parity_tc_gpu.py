@@ -1,5 +1,6 @@
 """GPU parity of the tcgen05 kernel (128 heads per CTA, TMA gather4, TMEM
-accumulators) against the CPU oracle, at chunk and split boundaries."""
+accumulators) against the CPU oracle, at chunk and split boundaries, and
+with fewer than 128 heads (the remaining TMEM lanes are padding)."""
 from __future__ import annotations
 
 import numpy as np
@@ -102,3 +103,32 @@ def test_tc_timeout_reports_status(cuda):
     out_g, lse_g = gpu_decode(case, cuda, dict(kernel=TC), tensors=(q, kv, idx, cnt))
     out_o, lse_o = oracle_decode(case)
     check(out_g, lse_g, out_o, lse_o, "tc after timeout")
+
+
+FEW_HEADS = [
+    # (B, H, W, N, counts, split): H < 128 fills part of the 128 TMEM lanes; the
+    # query tile then reaches into the next row's heads (or past the tensor).
+    (5, 64, 256, 65536, [256, 200, 0, 231, 17], 1),
+    (3, 16, 64, 4096, [64, 37, 1], 1),
+    (4, 48, 600, 7000, [600, 513, 129, 0], 2),
+    (2, 112, 1100, 9000, [1100, 64], 4),
+]
+
+
+@pytest.mark.parametrize("shape", FEW_HEADS, ids=[f"B{s[0]}H{s[1]}W{s[2]}S{s[5]}" for s in FEW_HEADS])
+def test_tc_fewer_than_128_heads(cuda, shape, workspace):
+    """The padding lanes' results are never stored; the real ones match the
+    oracle, and the warp-MMA kernel, for both exchanges."""
+    B, H, W, N, counts, split = shape
+    case = inputs.random_case(330 + H, B=B, H=H, W=W, N=N, counts=counts, heavy_frac=0.02)
+    t = to_dev(case, cuda)
+    out_o, lse_o = oracle_decode(case)
+    out_g, lse_g = gpu_decode(case, cuda, dict(kernel=TC, split=split), tensors=t)
+    check(out_g, lse_g, out_o, lse_o, f"tc few heads {shape}")
+    if split > 1:
+        out_w, lse_w = gpu_decode(case, cuda, dict(kernel=TC, split=split), tensors=t,
+                                  workspace=workspace)
+        assert np.array_equal(out_w, out_g)
+        assert np.array_equal(lse_w.view(np.uint32), lse_g.view(np.uint32))
+    out_m, lse_m = gpu_decode(case, cuda, dict(kernel=MMA), tensors=t)
+    check(out_g, lse_g, out_m, lse_m, f"tc vs mma few heads {shape}")
