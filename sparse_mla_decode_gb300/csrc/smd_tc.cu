@@ -137,22 +137,24 @@ __device__ __forceinline__ void wait_next(uint32_t bar, uint32_t& seen, bool& ok
 // 160 gathers is limited by the issue rate (well below HBM bandwidth).
 constexpr int kProducerThreads = 256;
 
+// Entries of the row's index list each producer thread loads at kernel entry.
+constexpr int kSpecPer = kTcMaxSplit * kTcMaxKeys / kProducerThreads;
+
 __device__ __forceinline__ void producer_a(const TcMaps& maps, const TcParams& p, uint8_t* smem,
-                                           uint32_t base, uint32_t bars, int b, int group, int split,
-                                           bool& ok) {
+                                           uint32_t base, uint32_t bars, int b, int split,
+                                           const int32_t (&spec)[kSpecPer], bool& ok) {
     const int t = threadIdx.x;
     const Range r = key_range(p, b, split);
-    if (t == 0) {
-        const int y = b * p.a.H + group * kTcHeads;
-        for (int j = 0; j < 4; ++j)
-            tma_load_2d(base + kOffQP + j * kBlock, &maps.q, 128 * j, y, bars + 8 * kBarQ);
-        tma_load_2d(base + kOffQP + 4 * kBlock, &maps.q_tail, 512, y, bars + 8 * kBarQ);
-    }
-    // This CTA's key indices; entries past its keys name pool row 0 (a real
-    // row: finite bytes; its P is zero).
+    // This CTA's key indices (from the row's list, loaded at kernel entry);
+    // entries past its keys name pool row 0 (a real row: finite bytes; its P
+    // is zero).
     int32_t* idx_s = reinterpret_cast<int32_t*>(smem + kOffIdx);
-    const int32_t* idx = p.a.indices + static_cast<int64_t>(b) * p.a.W + r.first;
-    for (int i = t; i < kTcMaxKeys; i += kProducerThreads) idx_s[i] = (i < r.mine) ? idx[i] : 0;
+#pragma unroll
+    for (int k = 0; k < kSpecPer; ++k) {
+        const int i = t + k * kProducerThreads - r.first;
+        if (i >= 0 && i < r.mine) idx_s[i] = spec[k];
+    }
+    for (int i = r.mine + t; i < kTcMaxKeys; i += kProducerThreads) idx_s[i] = 0;
     asm volatile("bar.sync 1, %0;" ::"r"(kProducerThreads) : "memory");
 
     // Completions of the pass-A "slot free" barriers (after QK of the slot's
@@ -660,6 +662,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int b = blockIdx.y;
     bool ok = true;
 
+    // The row's count (read again later from L1) and whole index list
+    // (W <= 2048) are loaded first: their round trip overlaps the setup.
+    int32_t spec[kSpecPer];
+    {
+        const int n_early = p.a.counts[b];
+        const int32_t* row_idx = p.a.indices + static_cast<int64_t>(b) * p.a.W;
+        const int lim = min(p.a.W, max(n_early, 0));
+#pragma unroll
+        for (int k = 0; k < kSpecPer; ++k) {
+            const int i = threadIdx.x + k * kProducerThreads;
+            spec[k] = (warp < 8 && i < lim) ? row_idx[i] : 0;
+        }
+    }
+
     if (threadIdx.x == 0) {
         mbar_init(bars + 8 * kBarQ, 1);
         for (int i = 0; i < 2; ++i) {
@@ -683,6 +699,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // (inject_stall: the query barrier also expects 16 bytes nobody sends,
         // so its bounded wait runs out; a test hook for the timeout path.)
         mbar_arrive_expect_tx(bars + 8 * kBarQ, kTile + (p.inject_stall ? 16 : 0));
+        // The query tile depends on nothing: it goes before the rest of the setup.
+        const int y = b * p.a.H + group * kTcHeads;
+        for (int j = 0; j < 4; ++j)
+            tma_load_2d(base + kOffQP + j * kBlock, &maps.q, 128 * j, y, bars + 8 * kBarQ);
+        tma_load_2d(base + kOffQP + 4 * kBlock, &maps.q_tail, 512, y, bars + 8 * kBarQ);
         mbar_arrive_expect_tx(bars + 8 * kBarMax, (S - 1) * (128 * 4 + 4));
         // The peers' sums; on the DSMEM path, round k's partial of this CTA's columns.
         mbar_arrive_expect_tx(bars + 8 * kBarIn, (S - 1) * 128 * 4);
@@ -701,7 +722,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     uint32_t full_seen[2] = {0u, 0u};
     if (warp < 8) {
-        producer_a(maps, p, smem, base, bars, b, group, split, ok);
+        producer_a(maps, p, smem, base, bars, b, split, spec, ok);
     } else if (warp == 8) {
         if (lane == 0) mma_pass_a(p, base, bars, tmem, b, split, full_seen, ok);
         __syncwarp();
