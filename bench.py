@@ -179,7 +179,10 @@ def run_gpu(args, world, rank, local) -> dict | None:
     torch.cuda.set_device(dev)
     case = inputs.config(args.config)
     stats = workload_stats(case)
-    plan = binding.smd_plan(case.B, case.H, case.W).as_dict()
+    # Rows that come in groups sharing one index list (the dense-as-sparse
+    # workload's four causal rows per request) go through the grouped call.
+    group = ROW_GROUP.get(args.config, 1)
+    plan = binding.smd_plan_grouped(case.B, case.H, case.W, group).as_dict()
 
     q = torch.from_numpy(case.q8).to(dev)
     kv = torch.from_numpy(case.kv8).to(dev)
@@ -204,8 +207,13 @@ def run_gpu(args, world, rank, local) -> dict | None:
             case.B, case.H, case.sm_scale, case.q_scale, case.k_scale, out.data_ptr(),
             lse.data_ptr(), status.data_ptr(), sptr)
 
+    gptrs = ptrs[:8] + (group,) + ptrs[8:]
+
     def decode():
-        rc = binding.smd_sparse_mla_decode(*ptrs)
+        if group > 1:
+            rc = binding.smd_sparse_mla_decode_grouped(*gptrs)
+        else:
+            rc = binding.smd_sparse_mla_decode(*ptrs)
         if rc != 0:
             raise binding.SmdError(rc, "decode")
 
@@ -254,7 +262,7 @@ def run_gpu(args, world, rank, local) -> dict | None:
         didx.copy_(hidx, non_blocking=True)
         dcnt.copy_(hcnt, non_blocking=True)
         binding.sparse_mla_decode(dq, kv, didx, dcnt, case.sm_scale, case.q_scale, case.k_scale,
-                                  out=out, lse=lse, status=status)
+                                  out=out, lse=lse, status=status, row_group=group)
         hout.copy_(out, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
 
@@ -328,6 +336,7 @@ def run_gpu(args, world, rank, local) -> dict | None:
             "gathered_keys": case.gathered_rows(), "unique_rows": case.unique_rows(),
             "l2": "flushed before every timed step (write of a 2x-L2 buffer, then read of another, outside the events)",
             "plan": plan,
+            "row_group": group,
             "workspace_bytes": int(ws_bytes),
             "parallelism": f"replicas x{world}",
         },
@@ -343,7 +352,10 @@ def run_gpu(args, world, rank, local) -> dict | None:
     return line
 
 
-KERNEL_FILES = {1: ("mma_decode_kernel", "smd_mma.cu"), 2: ("tc_decode_kernel", "smd_tc.cu")}
+KERNEL_FILES = {1: ("mma_decode_kernel", "smd_mma.cu"), 2: ("tc_decode_kernel", "smd_tc.cu"),
+                3: ("group_decode_kernel", "smd_group.cu")}
+# Workloads whose rows come in groups sharing one index list (rows per group).
+ROW_GROUP = {"dense": 4}
 
 
 def load_traffic(config: str, kernel: int = 1):

@@ -58,16 +58,20 @@ typedef enum {
     SMD_ERR_PLAN = -6,    /* a forced plan is invalid for these shapes        */
     SMD_ERR_DEVICE = -7,  /* no usable sm_103 device / attribute query failed;
                              device status: an SM id beyond the workspace    */
-    SMD_ERR_WORKSPACE = -8 /* workspace given but smaller than
+    SMD_ERR_WORKSPACE = -8, /* workspace given but smaller than
                              smd_workspace_bytes() or not 16-byte aligned    */
+    SMD_ERR_GROUP = -9    /* device status: rows of a group do not share their
+                             index list (smd_sparse_mla_decode_grouped)      */
 } smd_status;
 
 /* Kernel families. */
 enum {
     SMD_KERNEL_AUTO = 0,
     SMD_KERNEL_MMA = 1,  /* warp-level FP8 MMA (mma.sync), 16-head tiles       */
-    SMD_KERNEL_TC = 2    /* tcgen05 + TMEM, 128 heads per CTA, TMA gather4;
-                            needs H % 128 == 0 and 1 <= W <= 2048             */
+    SMD_KERNEL_TC = 2,   /* tcgen05 + TMEM, 128 heads per CTA (or all H < 128
+                            heads of a row), TMA gather4; 1 <= W <= 2048     */
+    SMD_KERNEL_GROUP = 3 /* warp-level FP8 MMA over groups of rows sharing one
+                            index list (smd_sparse_mla_decode_grouped)       */
 };
 
 /* A launch plan: how the work is laid out. `split` decides which keys each
@@ -130,7 +134,7 @@ int64_t smd_workspace_bytes(int32_t B, int32_t H, int32_t W);
 /* As smd_sparse_mla_decode, with a caller-owned device workspace. When the
  * plan splits rows over a cluster of tcgen05 CTAs, their FP32 partials are
  * exchanged through this workspace (L2) instead of distributed shared
- * memory, which is faster on GB300. workspace may be NULL (the on-chip
+ * memory (about as fast on GB300). workspace may be NULL (the on-chip
  * exchange is used); otherwise it must be 16-byte aligned and at least
  * smd_workspace_bytes(B, H, W) long (else SMD_ERR_WORKSPACE). Its contents
  * need no initialisation and are scratch; calls that overlap on the GPU
@@ -186,6 +190,43 @@ int smd_sparse_mla_decode_noalloc(const uint8_t* q, const uint8_t* kv_pool, int6
                                   float sm_scale, float q_scale, float k_scale,
                                   uint16_t* out, float* lse, int32_t* status,
                                   smd_stream_t stream);
+
+/* The decode for rows that come in groups sharing one index list: the
+ * verify rows of a multi-token decode step, where row i of a request sees the
+ * first L - G + 1 + i tokens of its cache (the attn_sparse page's verify rows;
+ * the dense-as-sparse workload). The result is that of smd_sparse_mla_decode
+ * on the same arguments, up to FP32 summation order (the keys are split over
+ * a cluster by the group's longest list instead of by each row's own); the
+ * cache rows a group reads are gathered once for all its rows.
+ *   row_group  G: 1 (same as smd_sparse_mla_decode), 2 or 4; B % G == 0.
+ *              Rows g*G .. g*G + G - 1 form group g.
+ * Contract: within a group, let r* be the row with the largest clamped count
+ * (the first such); every row r of the group reads a prefix of r*'s list:
+ * indices[r][i] == indices[r*][i] for i < clamp(counts[r], 0, W). The kernel
+ * checks this for the keys it reads and writes SMD_ERR_GROUP to `status` on
+ * a mismatch (the outputs of that group are then unspecified).
+ * The other arguments, layouts, ownership and errors are those of
+ * smd_sparse_mla_decode; B % G != 0 or another G is SMD_ERR_SHAPE. */
+int smd_sparse_mla_decode_grouped(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
+                                  const int32_t* indices, int32_t W, const int32_t* counts,
+                                  int32_t B, int32_t H, int32_t row_group,
+                                  float sm_scale, float q_scale, float k_scale,
+                                  uint16_t* out, float* lse, int32_t* status,
+                                  smd_stream_t stream);
+
+/* The plan smd_sparse_mla_decode_grouped would use (G > 1: kernel
+ * SMD_KERNEL_GROUP, tiles = G, window = keys of the ring of 64-key slots).
+ * Host only. */
+int smd_plan_grouped(int32_t B, int32_t H, int32_t W, int32_t row_group, smd_plan_t* plan);
+
+/* As smd_sparse_mla_decode_grouped, with split, window and the testing hooks
+ * taken from `force` (0 = automatic; may be NULL). For the tests. */
+int smd_sparse_mla_decode_grouped_ex(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
+                                     const int32_t* indices, int32_t W, const int32_t* counts,
+                                     int32_t B, int32_t H, int32_t row_group,
+                                     float sm_scale, float q_scale, float k_scale,
+                                     uint16_t* out, float* lse, int32_t* status,
+                                     smd_stream_t stream, const smd_plan_t* force);
 
 /* The base-2 logit scale the kernels use: fp32(sm*q_s*k_s*log2 e),
  * evaluated in double and rounded once. */

@@ -20,10 +20,12 @@ SMD_ERR_TIMEOUT = -5
 SMD_ERR_PLAN = -6
 SMD_ERR_DEVICE = -7
 SMD_ERR_WORKSPACE = -8
+SMD_ERR_GROUP = -9
 
 SMD_KERNEL_AUTO = 0
 SMD_KERNEL_MMA = 1
 SMD_KERNEL_TC = 2
+SMD_KERNEL_GROUP = 3
 
 
 class SmdPlan(ctypes.Structure):
@@ -72,6 +74,13 @@ def lib() -> ctypes.CDLL:
             so.smd_sparse_mla_decode_ex.argtypes = ws_args + [ctypes.POINTER(SmdPlan)]
             so.smd_sparse_mla_decode_noalloc.restype = ctypes.c_int
             so.smd_sparse_mla_decode_noalloc.argtypes = _DECODE_ARGS
+            grp_args = _DECODE_ARGS[:8] + [ctypes.c_int32] + _DECODE_ARGS[8:]
+            so.smd_sparse_mla_decode_grouped.restype = ctypes.c_int
+            so.smd_sparse_mla_decode_grouped.argtypes = grp_args
+            so.smd_sparse_mla_decode_grouped_ex.restype = ctypes.c_int
+            so.smd_sparse_mla_decode_grouped_ex.argtypes = grp_args + [ctypes.POINTER(SmdPlan)]
+            so.smd_plan_grouped.restype = ctypes.c_int
+            so.smd_plan_grouped.argtypes = [ctypes.c_int32] * 4 + [ctypes.POINTER(SmdPlan)]
             so.smd_workspace_bytes.restype = ctypes.c_int64
             so.smd_workspace_bytes.argtypes = [ctypes.c_int32] * 3
             so.smd_plan.restype = ctypes.c_int
@@ -123,6 +132,30 @@ def smd_sparse_mla_decode_noalloc(q, kv_pool, N, indices, W, counts, B, H, sm_sc
                                                q_scale, k_scale, out, lse, status, stream)
 
 
+def smd_sparse_mla_decode_grouped(q, kv_pool, N, indices, W, counts, B, H, row_group, sm_scale,
+                                  q_scale, k_scale, out, lse, status, stream) -> int:
+    return lib().smd_sparse_mla_decode_grouped(q, kv_pool, N, indices, W, counts, B, H,
+                                               row_group, sm_scale, q_scale, k_scale, out, lse,
+                                               status, stream)
+
+
+def smd_sparse_mla_decode_grouped_ex(q, kv_pool, N, indices, W, counts, B, H, row_group,
+                                     sm_scale, q_scale, k_scale, out, lse, status, stream,
+                                     force: SmdPlan | None) -> int:
+    ref = ctypes.byref(force) if force is not None else None
+    return lib().smd_sparse_mla_decode_grouped_ex(q, kv_pool, N, indices, W, counts, B, H,
+                                                  row_group, sm_scale, q_scale, k_scale, out,
+                                                  lse, status, stream, ref)
+
+
+def smd_plan_grouped(B: int, H: int, W: int, row_group: int) -> SmdPlan:
+    p = SmdPlan()
+    rc = lib().smd_plan_grouped(B, H, W, row_group, ctypes.byref(p))
+    if rc != SMD_OK:
+        raise SmdError(rc, "smd_plan_grouped")
+    return p
+
+
 def smd_workspace_bytes(B: int, H: int, W: int) -> int:
     return int(lib().smd_workspace_bytes(B, H, W))
 
@@ -164,14 +197,15 @@ def _bytes_view(t, name: str):
 
 def sparse_mla_decode(q, kv_pool, indices, counts, sm_scale: float, q_scale: float,
                       k_scale: float, out=None, lse=None, status=None, stream=None,
-                      plan: SmdPlan | dict | None = None, workspace=None):
+                      plan: SmdPlan | dict | None = None, workspace=None, row_group: int = 1):
     """Decode on the GPU. q [B,H,576] and kv_pool [N,576] E4M3 (uint8 or
     float8_e4m3fn), indices [B,W] int32, counts [B] int32, all CUDA tensors.
     Returns (out [B,H,512] bfloat16, lse [B,H] float32). ``plan`` forces
     plan fields (smd_sparse_mla_decode_ex); ``status`` is an optional int32
     CUDA tensor that receives device-side errors; ``workspace`` an optional
     CUDA tensor of at least smd_workspace_bytes(B, H, W) bytes for the L2
-    exchange of split partials."""
+    exchange of split partials; ``row_group`` > 1 calls
+    smd_sparse_mla_decode_grouped (rows in groups sharing one index list)."""
     import torch
 
     q = _bytes_view(q, "q")
@@ -202,16 +236,27 @@ def sparse_mla_decode(q, kv_pool, indices, counts, sm_scale: float, q_scale: flo
     ws = (_ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size())
     if workspace is not None and not workspace.is_cuda:
         raise ValueError("workspace must be a CUDA tensor")
+    if isinstance(plan, dict):
+        p = SmdPlan()
+        for k, v in plan.items():
+            setattr(p, k, int(v))
+        plan = p
+    if row_group != 1:
+        if workspace is not None:
+            raise ValueError("the grouped decode takes no workspace")
+        g_args = args[:8] + (int(row_group),) + args[8:]
+        if plan is None:
+            rc = smd_sparse_mla_decode_grouped(*g_args, int(stream))
+        else:
+            rc = smd_sparse_mla_decode_grouped_ex(*g_args, int(stream), plan)
+        if rc != SMD_OK:
+            raise SmdError(rc, "smd_sparse_mla_decode_grouped")
+        return out, lse
     if plan is None and workspace is None:
         rc = smd_sparse_mla_decode(*args, int(stream))
     elif plan is None:
         rc = smd_sparse_mla_decode_ws(*args, *ws, int(stream))
     else:
-        if isinstance(plan, dict):
-            p = SmdPlan()
-            for k, v in plan.items():
-                setattr(p, k, int(v))
-            plan = p
         rc = smd_sparse_mla_decode_ex(*args, *ws, int(stream), plan)
     if rc != SMD_OK:
         raise SmdError(rc, "smd_sparse_mla_decode")

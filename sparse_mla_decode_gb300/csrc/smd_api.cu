@@ -161,6 +161,56 @@ int plan_tc(int B, int H, int W, const smd_plan_t* force, smd_plan_t* out, TcCon
     return SMD_OK;
 }
 
+// The row-group kernel's plan: the smallest cluster whose CTAs stage at most
+// kGroupMaxKeys indices each, then wider while the grid is under one wave and
+// every CTA keeps >= 64 keys; a ring of two 64-key slots unless forced.
+int plan_group(int B, int H, int W, int G, int sm_count, const smd_plan_t* force, smd_plan_t* out,
+               GroupConfig* cfg) {
+    if ((G != 2 && G != 4) || B % G != 0) return SMD_ERR_SHAPE;
+    if (force && force->tiles && force->tiles != G) return SMD_ERR_PLAN;
+    if (force && force->kernel && force->kernel != SMD_KERNEL_GROUP) return SMD_ERR_PLAN;
+    const int units = B / G * (H / kHeadsPerTile);
+    int split = 1;
+    while (split < kGroupMaxSplit && ceil_div(W, split) > kGroupMaxKeys) split *= 2;
+    if (ceil_div(W, split) > kGroupMaxKeys) return SMD_ERR_SHAPE;
+    if (force && force->split) {
+        if (!is_split(force->split) || ceil_div(W, force->split) > kGroupMaxKeys) return SMD_ERR_PLAN;
+        split = force->split;
+    } else {
+        while (split < kGroupMaxSplit && units * split < sm_count && ceil_div(W, split * 2) >= 64)
+            split *= 2;
+    }
+    int nslots = 2;
+    if (force && force->window) {
+        if (force->window % kChunk != 0 || force->window < kChunk || force->window > 8 * kChunk)
+            return SMD_ERR_PLAN;
+        nslots = force->window / kChunk;
+    }
+    const int key_cap = std::max(kChunk, ceil_div(ceil_div(std::max(W, 1), split), kChunk) * kChunk);
+    const GroupLayout L = group_layout(G, split, nslots, key_cap);
+    if (L.total > kMaxSmemBytes) return SMD_ERR_PLAN;
+    cfg->G = G;
+    cfg->split = split;
+    cfg->nslots = nslots;
+    cfg->key_cap = key_cap;
+    cfg->layout = L;
+    cfg->wait_budget_ns = (force && force->wait_budget_us > 0)
+                              ? static_cast<uint64_t>(force->wait_budget_us) * 1000ull
+                              : kWaitBudgetNs;
+    cfg->inject_stall = (force && force->inject_stall) ? 1 : 0;
+    out->kernel = SMD_KERNEL_GROUP;
+    out->split = split;
+    out->tiles = G;
+    out->window = nslots * kChunk;
+    out->key_cap = key_cap;
+    out->grid_x = H / kHeadsPerTile * split;
+    out->grid_y = B / G;
+    out->cluster_x = split;
+    out->threads = kMmaThreads;
+    out->smem_bytes = L.total;
+    return SMD_OK;
+}
+
 struct AnyConfig {
     int kernel;
     MmaConfig mma;
@@ -191,12 +241,21 @@ int64_t workspace_for(const AnyConfig& cfg) {
     return (cfg.kernel == SMD_KERNEL_TC && cfg.tc.split > 1) ? kTcWsBytes : 0;
 }
 
+int sm_count_of_device() {
+    static std::once_flag once;
+    static DeviceInfo info;
+    std::call_once(once, [] { info = query_device(); });
+    return info.ok ? info.sm_count : 152;
+}
+
 int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* indices, int32_t W,
            const int32_t* counts, int32_t B, int32_t H, float sm_scale, float q_scale,
            float k_scale, uint16_t* out, float* lse, int32_t* status, void* workspace,
            int64_t workspace_bytes, smd_stream_t stream, const smd_plan_t* force,
-           bool library_scratch = false) {
+           bool library_scratch = false, int row_group = 1) {
     if (B < 0 || W < 0 || N < 0 || H <= 0 || H % kHeadsPerTile != 0) return SMD_ERR_SHAPE;
+    if (row_group != 1 && ((row_group != 2 && row_group != 4) || B % row_group != 0))
+        return SMD_ERR_SHAPE;
     if (N >= (int64_t(1) << 31)) return SMD_ERR_SHAPE;
     if (B == 0) return SMD_OK;
     if (!q || !out || !lse || !counts) return SMD_ERR_NULL;
@@ -207,6 +266,28 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
     if ((indices && !aligned(indices, 4)) || !aligned(counts, 4) || !aligned(lse, 4) ||
         (status && !aligned(status, 4)))
         return SMD_ERR_ALIGN;
+
+    if (row_group > 1) {
+        smd_plan_t plan{};
+        GroupConfig gcfg{};
+        const int rc = plan_group(B, H, W, row_group, sm_count_of_device(), force, &plan, &gcfg);
+        if (rc != SMD_OK) return rc;
+        CallArgs a{};
+        a.q = q;
+        a.kv = kv_pool;
+        a.N = N;
+        a.indices = indices;
+        a.W = W;
+        a.counts = counts;
+        a.B = B;
+        a.H = H;
+        a.scale_log2 = scale_log2_of(sm_scale, q_scale, k_scale);
+        a.k_scale = k_scale;
+        a.out = out;
+        a.lse = lse;
+        a.status = status;
+        return launch_group(a, gcfg, reinterpret_cast<cudaStream_t>(stream));
+    }
 
     smd_plan_t plan{};
     AnyConfig cfg{};
@@ -304,6 +385,36 @@ int smd_plan(int32_t B, int32_t H, int32_t W, smd_plan_t* plan) {
     return rc;
 }
 
+int smd_sparse_mla_decode_grouped(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
+                                  const int32_t* indices, int32_t W, const int32_t* counts,
+                                  int32_t B, int32_t H, int32_t row_group, float sm_scale,
+                                  float q_scale, float k_scale, uint16_t* out, float* lse,
+                                  int32_t* status, smd_stream_t stream) {
+    return smd::decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale, out,
+                       lse, status, nullptr, 0, stream, nullptr, false, row_group);
+}
+
+int smd_sparse_mla_decode_grouped_ex(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
+                                     const int32_t* indices, int32_t W, const int32_t* counts,
+                                     int32_t B, int32_t H, int32_t row_group, float sm_scale,
+                                     float q_scale, float k_scale, uint16_t* out, float* lse,
+                                     int32_t* status, smd_stream_t stream,
+                                     const smd_plan_t* force) {
+    return smd::decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale, out,
+                       lse, status, nullptr, 0, stream, force, false, row_group);
+}
+
+int smd_plan_grouped(int32_t B, int32_t H, int32_t W, int32_t row_group, smd_plan_t* plan) {
+    if (!plan) return SMD_ERR_NULL;
+    if (row_group == 1) return smd_plan(B, H, W, plan);
+    if (B < 0 || W < 0 || H <= 0 || H % smd::kHeadsPerTile != 0) return SMD_ERR_SHAPE;
+    smd::GroupConfig cfg{};
+    smd_plan_t p{};
+    const int rc = smd::plan_group(B, H, W, row_group, smd::sm_count_of_device(), nullptr, &p, &cfg);
+    if (rc == SMD_OK) *plan = p;
+    return rc;
+}
+
 float smd_scale_log2(float sm_scale, float q_scale, float k_scale) {
     return smd::scale_log2_of(sm_scale, q_scale, k_scale);
 }
@@ -330,6 +441,8 @@ const char* smd_status_str(int status) {
             return "no usable CUDA device (or an SM id beyond the exchange workspace)";
         case SMD_ERR_WORKSPACE:
             return "workspace smaller than smd_workspace_bytes() or not 16-byte aligned";
+        case SMD_ERR_GROUP:
+            return "rows of a group do not share their index list (device status)";
         default:
             return "unknown status";
     }

@@ -119,6 +119,68 @@ struct TcConfig {
     int ws_slots;  // SM-id slots in ws (0: kTcWsSlots)
 };
 
+// Row-group warp-MMA kernel: G consecutive rows that share one index list
+// (each reads a prefix of it) go through one gather; a CTA takes 16 heads of
+// each of the G rows (G tiles) and its share of the group's longest list.
+constexpr int kGroupMaxSplit = 16;
+constexpr int kGroupMaxKeys = 2048;  // keys per CTA (index staging)
+
+struct GroupLayout {
+    int32_t ring, q, lg, probs, overlay_end;  // inbox of the partials overlays [0, overlay_end)
+    int32_t idx, sums, maxima, wmax, lsum, rowmax, nrow, flags, bars;
+    int32_t total;
+};
+
+// lg: logits of the current chunk, [16 G][72] fp32; probs: its E4M3 P, [16 G][80].
+__host__ __device__ inline GroupLayout group_layout(int G, int split, int nslots, int key_cap) {
+    GroupLayout L{};
+    const int ch = kHeadsPerTile * G;
+    int32_t o = 0;
+    L.ring = o;
+    o += nslots * kChunk * kRowPitch;
+    L.q = o;
+    o += ch * kRowPitch;
+    L.lg = o;
+    o += ch * (kChunk + 8) * 4;
+    L.probs = o;
+    o += ch * (kChunk + 16);
+    o = align_up(o, 16);
+    const int32_t inbox = ch * kLatent * 4;  // split x ch x (512 / split) fp32
+    L.overlay_end = o > inbox ? o : inbox;
+    o = L.overlay_end;
+    L.idx = o;
+    o += key_cap * 4;
+    L.sums = o;    // [split][ch]
+    o += split * ch * 4;
+    L.maxima = o;  // [split][ch]
+    o += split * ch * 4;
+    L.wmax = o;    // [4 key groups][ch]
+    o += 4 * ch * 4;
+    L.lsum = o;
+    o += ch * 4;
+    L.rowmax = o;
+    o += ch * 4;
+    L.nrow = o;    // [G] clamped counts
+    o += 16;
+    L.flags = o;   // words the peers' "free" signals write
+    o += 16;
+    o = align_up(o, 8);
+    L.bars = o;    // ring slots, q, maxima, inbound, peers free
+    o += 8 * (nslots + 4);
+    L.total = align_up(o, 128);
+    return L;
+}
+
+struct GroupConfig {
+    int G, split, nslots, key_cap;
+    GroupLayout layout;
+    uint64_t wait_budget_ns;
+    int inject_stall;
+};
+
+// Launches the row-group kernel; returns an smd_status.
+int launch_group(const CallArgs& a, const GroupConfig& cfg, cudaStream_t stream);
+
 // SM-id slots of the library's own static exchange scratch (GB300: 152 SMs).
 constexpr int kStaticScratchSlots = 160;
 

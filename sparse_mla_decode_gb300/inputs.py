@@ -302,6 +302,29 @@ def random_case(seed: int, B: int, H: int, W: int, N: int, counts=None,
     return Case(f"random{seed}", q8, kv8, idx.astype(np.int32), counts, sm, qs, ks)
 
 
+def grouped_case(seed: int, R: int, G: int, H: int, W: int, N: int, counts=None) -> Case:
+    """R requests of G query rows that share one index list (the causal rows
+    of a multi-token decode step). Every row of a request holds the request's
+    whole list of W unique pool rows, of which it reads its first counts[b];
+    by default row i of a request reads L - G + 1 + i, L ~ U[G, W]. ``counts``
+    (R*G values, any order within a group, clamped by the call) overrides."""
+    ss = np.random.SeedSequence(5000 + seed)
+    rng = np.random.Generator(np.random.PCG64(ss.spawn(1)[0]))
+    B = R * G
+    q8, qs = make_query(rng, B, H)
+    kv8, ks = make_pool(ss.spawn(1)[0], N, rng=rng)
+    if counts is None:
+        L = rng.integers(G, W + 1, size=R)
+        counts = np.array([L[r] - G + 1 + i for r in range(R) for i in range(G)])
+    counts = np.asarray(counts, np.int64).astype(np.int32)
+    idx = np.zeros((B, W), np.int64)
+    for r in range(R):
+        lst = rng.choice(N, size=W, replace=False) if W <= N else rng.integers(0, N, size=W)
+        idx[r * G:(r + 1) * G] = lst
+    _fill_tail(rng, idx, counts, N)
+    return Case(f"grouped{seed}", q8, kv8, idx.astype(np.int32), counts, _f32(192 ** -0.5), qs, ks)
+
+
 def algorithmic_bytes(case: Case) -> dict:
     """Bytes a decode must move at least once: the distinct cache rows read,
     the query, the BF16 output and the FP32 LSE (index/count reads excluded)."""

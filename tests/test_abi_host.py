@@ -45,7 +45,7 @@ def test_scale_log2_is_the_rounded_double_product():
 
 
 def test_status_strings():
-    for code in range(-8, 1):
+    for code in range(-9, 1):
         s = smd.smd_status_str(code)
         assert s and s != "unknown status"
     assert smd.smd_status_str(-99) == "unknown status"
@@ -167,3 +167,53 @@ def test_workspace_size_and_checks():
     args = (A, A, 100, A, 2048, A, 2, 128, 0.1, 0.1, 0.1, A, A, 0)
     assert smd.smd_sparse_mla_decode_ws(*args, A, need - 16, 0) == smd.SMD_ERR_WORKSPACE
     assert smd.smd_sparse_mla_decode_ws(*args, A + 8, need, 0) == smd.SMD_ERR_WORKSPACE
+
+
+def call_grouped(G, B=8, H=16, W=64, q=A, counts=A, force=None):
+    if force is None:
+        return smd.smd_sparse_mla_decode_grouped(q, A, 100, A, W, counts, B, H, G, 0.1, 0.1, 0.1,
+                                                 A, A, 0, 0)
+    return smd.smd_sparse_mla_decode_grouped_ex(q, A, 100, A, W, counts, B, H, G, 0.1, 0.1, 0.1,
+                                                A, A, 0, 0, force)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(G=3), smd.SMD_ERR_SHAPE),
+    (dict(G=8), smd.SMD_ERR_SHAPE),
+    (dict(G=0), smd.SMD_ERR_SHAPE),
+    (dict(G=4, B=6), smd.SMD_ERR_SHAPE),
+    (dict(G=2, H=24), smd.SMD_ERR_SHAPE),
+    (dict(G=4, q=0), smd.SMD_ERR_NULL),
+    (dict(G=4, q=A + 8), smd.SMD_ERR_ALIGN),
+    (dict(G=4, B=0, q=0, counts=0), smd.SMD_OK),
+])
+def test_grouped_argument_checks(kw, code):
+    assert call_grouped(**kw) == code
+
+
+@pytest.mark.parametrize("force", [dict(split=3), dict(split=32), dict(tiles=2), dict(window=65),
+                                   dict(window=1024), dict(kernel=1)])
+def test_invalid_grouped_plans_are_rejected(force):
+    p = smd.SmdPlan()
+    for k, v in force.items():
+        setattr(p, k, v)
+    assert call_grouped(4, force=p) == smd.SMD_ERR_PLAN
+
+
+@pytest.mark.parametrize("B,H,W,G", [(128, 16, 8192, 4), (8, 16, 300, 2), (4, 64, 2048, 4),
+                                     (2, 16, 1, 2), (64, 32, 700, 4), (4, 16, 32768, 4)])
+def test_grouped_plan_invariants(B, H, W, G):
+    p = smd.smd_plan_grouped(B, H, W, G).as_dict()
+    assert p["kernel"] == smd.SMD_KERNEL_GROUP and p["tiles"] == G
+    assert p["split"] in (1, 2, 4, 8, 16) and p["cluster_x"] == p["split"]
+    assert -(-W // p["split"]) <= 2048 and p["key_cap"] >= -(-W // p["split"])
+    assert p["grid_x"] == H // 16 * p["split"] and p["grid_y"] == B // G
+    assert p["window"] % 64 == 0 and p["threads"] == 512 and p["smem_bytes"] <= 227 * 1024
+    if W <= 16384:  # a group of one is the per-row plan (which takes up to 16 x 1024 keys)
+        assert smd.smd_plan_grouped(B, H, W, 1).as_dict() == smd.smd_plan(B, H, W).as_dict()
+
+
+def test_grouped_plan_rejects_lists_beyond_the_cluster():
+    with pytest.raises(smd.SmdError) as e:
+        smd.smd_plan_grouped(4, 16, 16 * 2048 + 1, 4)
+    assert e.value.status == smd.SMD_ERR_SHAPE

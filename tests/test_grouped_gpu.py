@@ -1,0 +1,114 @@
+"""GPU parity of the grouped decode (smd_sparse_mla_decode_grouped): rows in
+groups of 2 or 4 that share one index list, gathered once per group. Each
+row's result is checked against the CPU oracle (which knows nothing about
+groups), against the per-row decode, across ring sizes (identical bits) and
+splits, and the contract check and the timeout path are exercised."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+from sparse_mla_decode_gb300 import inputs
+from test_parity_gpu import check, oracle_decode, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def grouped(case, dev, G, plan=None, tensors=None, expect_status=0):
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    q, kv, idx, cnt = tensors if tensors is not None else to_dev(case, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out, lse = binding.sparse_mla_decode(q, kv, idx, cnt, case.sm_scale, case.q_scale,
+                                         case.k_scale, status=status, plan=plan, row_group=G)
+    torch.cuda.synchronize()
+    assert int(status.item()) == expect_status, binding.smd_status_str(int(status.item()))
+    return out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy()
+
+
+SHAPES = [
+    # (R, G, H, W, N, counts): ragged chunk and split boundaries; empty rows;
+    # the longest list in any row of the group, not only the last.
+    (3, 4, 16, 700, 9000, None),
+    (2, 4, 16, 129, 3000, [1, 64, 65, 129, 0, 0, 0, 0]),
+    (2, 4, 32, 300, 5000, [300, 12, 299, 5, 64, 63, 62, 61]),
+    (4, 2, 16, 2048, 20000, None),
+    (3, 2, 48, 97, 2000, [97, 96, 0, 33, 1, 2]),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"R{s[0]}G{s[1]}H{s[2]}W{s[3]}" for s in SHAPES])
+def test_grouped_matches_the_oracle_and_the_per_row_decode(cuda, shape):
+    R, G, H, W, N, counts = shape
+    case = inputs.grouped_case(10 * R + G + W, R, G, H, W, N, counts)
+    t = to_dev(case, cuda)
+    out_g, lse_g = grouped(case, cuda, G, tensors=t)
+    out_o, lse_o = oracle_decode(case)
+    check(out_g, lse_g, out_o, lse_o, f"grouped {shape}")
+    from test_parity_gpu import gpu_decode
+    out_r, lse_r = gpu_decode(case, cuda, tensors=t)
+    check(out_g, lse_g, out_r, lse_r, f"grouped vs per-row {shape}")
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8, 16])
+def test_grouped_every_split(cuda, split):
+    case = inputs.grouped_case(41, 2, 4, 16, 1100, 12000, [1100, 1099, 700, 2, 0, 300, 301, 64])
+    t = to_dev(case, cuda)
+    out_o, lse_o = oracle_decode(case)
+    out_g, lse_g = grouped(case, cuda, 4, plan=dict(split=split), tensors=t)
+    check(out_g, lse_g, out_o, lse_o, f"grouped split {split}")
+
+
+def test_grouped_ring_size_changes_no_bits(cuda):
+    """The ring size (64-key slots) only lays work out: identical bits."""
+    case = inputs.grouped_case(42, 3, 4, 16, 900, 10000)
+    t = to_dev(case, cuda)
+    ref = grouped(case, cuda, 4, plan=dict(split=4, window=64), tensors=t)
+    for window in (128, 192, 256):
+        out, lse = grouped(case, cuda, 4, plan=dict(split=4, window=window), tensors=t)
+        assert np.array_equal(out, ref[0]), window
+        assert np.array_equal(lse.view(np.uint32), ref[1].view(np.uint32)), window
+
+
+def test_group_of_one_is_the_per_row_decode(cuda):
+    case = inputs.grouped_case(43, 2, 4, 16, 200, 3000)
+    t = to_dev(case, cuda)
+    from test_parity_gpu import gpu_decode
+    out_1, lse_1 = grouped(case, cuda, 1, tensors=t)
+    out_r, lse_r = gpu_decode(case, cuda, tensors=t)
+    assert np.array_equal(out_1, out_r)
+    assert np.array_equal(lse_1.view(np.uint32), lse_r.view(np.uint32))
+
+
+def test_rows_that_do_not_share_their_list_are_reported(cuda):
+    """One row of the second group reads a key its group's longest list does
+    not hold: the call reports SMD_ERR_GROUP; the first group is unaffected."""
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.grouped_case(44, 2, 4, 16, 256, 4000, [256, 255, 254, 253, 200, 256, 100, 7])
+    case.indices[6, 50] = (case.indices[5, 50] + 1) % case.N
+    t = to_dev(case, cuda)
+    out_g, lse_g = grouped(case, cuda, 4, tensors=t, expect_status=binding.SMD_ERR_GROUP)
+    out_o, lse_o = oracle_decode(case, rows=[0, 1, 2, 3])
+    check(out_g[:4], lse_g[:4], out_o, lse_o, "grouped, the group that keeps the contract")
+
+
+def test_grouped_timeout_is_reported_and_the_context_survives(cuda):
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.grouped_case(45, 2, 4, 16, 300, 4000)
+    t = to_dev(case, cuda)
+    grouped(case, cuda, 4, plan=dict(inject_stall=1, wait_budget_us=2000, split=2), tensors=t,
+            expect_status=binding.SMD_ERR_TIMEOUT)
+    out_g, lse_g = grouped(case, cuda, 4, tensors=t)
+    out_o, lse_o = oracle_decode(case)
+    check(out_g, lse_g, out_o, lse_o, "grouped after a timeout")
+
+
+def test_dense_as_sparse_full_size_sampled_rows(cuda):
+    """The dense-as-sparse workload at full size through the grouped call,
+    in the plan bench.py times; sampled requests against the oracle."""
+    case = inputs.config("dense")
+    t = to_dev(case, cuda)
+    out_g, lse_g = grouped(case, cuda, 4, tensors=t)
+    rows = [0, 1, 2, 3, 60, 61, 62, 63, 124, 125, 126, 127]
+    out_o, lse_o = oracle_decode(case, rows)
+    check(out_g[rows], lse_g[rows], out_o, lse_o, "dense grouped sampled")
