@@ -70,8 +70,10 @@ enum {
     SMD_KERNEL_MMA = 1,  /* warp-level FP8 MMA (mma.sync), 16-head tiles       */
     SMD_KERNEL_TC = 2,   /* tcgen05 + TMEM, 128 heads per CTA (or all H < 128
                             heads of a row), TMA gather4; 1 <= W <= 2048     */
-    SMD_KERNEL_GROUP = 3 /* warp-level FP8 MMA over groups of rows sharing one
-                            index list (smd_sparse_mla_decode_grouped)       */
+    SMD_KERNEL_GROUP = 3,   /* warp-level FP8 MMA over groups of rows sharing
+                               one index list (smd_sparse_mla_decode_grouped) */
+    SMD_KERNEL_TC_GROUP = 4 /* tcgen05 over such groups: G * H = 32 or 64 TMEM
+                               lanes, W <= 16 * 512, clusters of up to 16     */
 };
 
 /* A launch plan: how the work is laid out. `split` decides which keys each
@@ -215,12 +217,14 @@ int smd_sparse_mla_decode_grouped(const uint8_t* q, const uint8_t* kv_pool, int6
                                   smd_stream_t stream);
 
 /* The plan smd_sparse_mla_decode_grouped would use (G > 1: kernel
- * SMD_KERNEL_GROUP, tiles = G, window = keys of the ring of 64-key slots).
- * Host only. */
+ * SMD_KERNEL_TC_GROUP when G * H is 32 or 64 and W <= 8192, else
+ * SMD_KERNEL_GROUP with tiles = G and window = keys of its ring of 64-key
+ * slots). Host only. */
 int smd_plan_grouped(int32_t B, int32_t H, int32_t W, int32_t row_group, smd_plan_t* plan);
 
-/* As smd_sparse_mla_decode_grouped, with split, window and the testing hooks
- * taken from `force` (0 = automatic; may be NULL). For the tests. */
+/* As smd_sparse_mla_decode_grouped, with kernel (SMD_KERNEL_GROUP or
+ * SMD_KERNEL_TC_GROUP), split, window and the testing hooks taken from
+ * `force` (0 = automatic; may be NULL). For the tests. */
 int smd_sparse_mla_decode_grouped_ex(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
                                      const int32_t* indices, int32_t W, const int32_t* counts,
                                      int32_t B, int32_t H, int32_t row_group,

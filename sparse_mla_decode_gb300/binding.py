@@ -26,6 +26,7 @@ SMD_KERNEL_AUTO = 0
 SMD_KERNEL_MMA = 1
 SMD_KERNEL_TC = 2
 SMD_KERNEL_GROUP = 3
+SMD_KERNEL_TC_GROUP = 4
 
 
 class SmdPlan(ctypes.Structure):

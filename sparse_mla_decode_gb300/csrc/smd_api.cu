@@ -164,6 +164,43 @@ int plan_tc(int B, int H, int W, const smd_plan_t* force, smd_plan_t* out, TcCon
 // The row-group kernel's plan: the smallest cluster whose CTAs stage at most
 // kGroupMaxKeys indices each, then wider while the grid is under one wave and
 // every CTA keeps >= 64 keys; a ring of two 64-key slots unless forced.
+bool tcg_fits(int H, int W, int G) {
+    const int lanes = G * H;
+    return (lanes == 32 || lanes == 64) && W >= 1 && W <= kTcgMaxSplit * kTcMaxKeys;
+}
+
+// The tcgen05 row-group plan: the smallest cluster whose CTAs hold at most
+// kTcMaxKeys keys of the group's longest list each.
+int plan_tcg(int B, int H, int W, int G, const smd_plan_t* force, smd_plan_t* out, TcgConfig* cfg) {
+    if (!tcg_fits(H, W, G)) return SMD_ERR_PLAN;
+    if ((force && force->tiles && force->tiles != G * H / kHeadsPerTile) ||
+        (force && force->window && force->window != kTcChunk))
+        return SMD_ERR_PLAN;
+    int split = 1;
+    while (ceil_div(W, split) > kTcMaxKeys) split *= 2;
+    if (force && force->split) {
+        if (!is_split(force->split) || ceil_div(W, force->split) > kTcMaxKeys) return SMD_ERR_PLAN;
+        split = force->split;
+    }
+    cfg->G = G;
+    cfg->split = split;
+    cfg->wait_budget_ns = (force && force->wait_budget_us > 0)
+                              ? static_cast<uint64_t>(force->wait_budget_us) * 1000ull
+                              : kWaitBudgetNs;
+    cfg->inject_stall = (force && force->inject_stall) ? 1 : 0;
+    out->kernel = SMD_KERNEL_TC_GROUP;
+    out->split = split;
+    out->tiles = G * H / kHeadsPerTile;
+    out->window = kTcChunk;
+    out->key_cap = kTcMaxKeys;
+    out->grid_x = split;
+    out->grid_y = B / G;
+    out->cluster_x = split;
+    out->threads = kTcThreads;
+    out->smem_bytes = 0;  // filled by the caller
+    return SMD_OK;
+}
+
 int plan_group(int B, int H, int W, int G, int sm_count, const smd_plan_t* force, smd_plan_t* out,
                GroupConfig* cfg) {
     if ((G != 2 && G != 4) || B % G != 0) return SMD_ERR_SHAPE;
@@ -268,9 +305,16 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
         return SMD_ERR_ALIGN;
 
     if (row_group > 1) {
+        if (B % row_group != 0) return SMD_ERR_SHAPE;
+        const int want = (force && force->kernel) ? force->kernel
+                         : tcg_fits(H, W, row_group) ? SMD_KERNEL_TC_GROUP
+                                                     : SMD_KERNEL_GROUP;
         smd_plan_t plan{};
         GroupConfig gcfg{};
-        const int rc = plan_group(B, H, W, row_group, sm_count_of_device(), force, &plan, &gcfg);
+        TcgConfig tcfg{};
+        const int rc = want == SMD_KERNEL_TC_GROUP
+                           ? plan_tcg(B, H, W, row_group, force, &plan, &tcfg)
+                           : plan_group(B, H, W, row_group, sm_count_of_device(), force, &plan, &gcfg);
         if (rc != SMD_OK) return rc;
         CallArgs a{};
         a.q = q;
@@ -286,6 +330,7 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
         a.out = out;
         a.lse = lse;
         a.status = status;
+        if (want == SMD_KERNEL_TC_GROUP) return launch_tcg(a, tcfg, reinterpret_cast<cudaStream_t>(stream));
         return launch_group(a, gcfg, reinterpret_cast<cudaStream_t>(stream));
     }
 
@@ -408,9 +453,17 @@ int smd_plan_grouped(int32_t B, int32_t H, int32_t W, int32_t row_group, smd_pla
     if (!plan) return SMD_ERR_NULL;
     if (row_group == 1) return smd_plan(B, H, W, plan);
     if (B < 0 || W < 0 || H <= 0 || H % smd::kHeadsPerTile != 0) return SMD_ERR_SHAPE;
-    smd::GroupConfig cfg{};
+    if ((row_group != 2 && row_group != 4) || B % row_group != 0) return SMD_ERR_SHAPE;
     smd_plan_t p{};
-    const int rc = smd::plan_group(B, H, W, row_group, smd::sm_count_of_device(), nullptr, &p, &cfg);
+    int rc;
+    if (smd::tcg_fits(H, W, row_group)) {
+        smd::TcgConfig cfg{};
+        rc = smd::plan_tcg(B, H, W, row_group, nullptr, &p, &cfg);
+        p.smem_bytes = smd::tcg_smem_bytes();
+    } else {
+        smd::GroupConfig cfg{};
+        rc = smd::plan_group(B, H, W, row_group, smd::sm_count_of_device(), nullptr, &p, &cfg);
+    }
     if (rc == SMD_OK) *plan = p;
     return rc;
 }

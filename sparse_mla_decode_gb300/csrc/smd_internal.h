@@ -3,6 +3,7 @@
 
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "smd.h"
@@ -181,6 +182,22 @@ struct GroupConfig {
 // Launches the row-group kernel; returns an smd_status.
 int launch_group(const CallArgs& a, const GroupConfig& cfg, cudaStream_t stream);
 
+// Row groups on the tcgen05 kernel: a CTA takes all H heads of the G rows
+// (G * H = 32 or 64 TMEM lanes) and at most 512 keys of the group's longest
+// list; clusters of up to 16 CTAs.
+constexpr int kTcgMaxSplit = 16;
+
+struct TcgConfig {
+    int G, split;
+    uint64_t wait_budget_ns;
+    int inject_stall;
+};
+
+int launch_tcg(const CallArgs& a, const TcgConfig& cfg, cudaStream_t stream);
+
+// Dynamic shared memory of the tcgen05 row-group kernel (bytes).
+int tcg_smem_bytes();
+
 // SM-id slots of the library's own static exchange scratch (GB300: 152 SMs).
 constexpr int kStaticScratchSlots = 160;
 
@@ -190,6 +207,12 @@ float* static_scratch(int* rc);
 
 // Dynamic shared memory of the tcgen05 kernel (bytes).
 int tc_smem_bytes();
+
+// A 2D tensor map over rows of 576 bytes (query or cache rows) with a box of
+// box_cols x box_rows (128 columns: 128-byte swizzle; 64: 64-byte swizzle),
+// from a small cache keyed by (ptr, rows, box). False if encoding failed.
+bool encode_row_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint32_t box_cols,
+                    uint32_t box_rows);
 
 // Launches the tcgen05 kernel; returns an smd_status.
 int launch_tc(const CallArgs& a, const TcConfig& cfg, cudaStream_t stream);

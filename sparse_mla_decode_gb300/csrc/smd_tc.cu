@@ -831,6 +831,11 @@ constexpr int kMaxDevices = 64;
 
 int tc_smem_bytes() { return kSmemBytes; }
 
+bool encode_row_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint32_t box_cols,
+                    uint32_t box_rows) {
+    return encode_map(out, ptr, rows, box_cols, box_rows);
+}
+
 // ---- the exchange scratch of smd_sparse_mla_decode_noalloc --------------------------
 // A file-scope device array: every GPU that loads the library holds these
 // kStaticScratchSlots x 192 KiB (30 MiB) until the process exits. Host code

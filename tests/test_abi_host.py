@@ -192,7 +192,8 @@ def test_grouped_argument_checks(kw, code):
 
 
 @pytest.mark.parametrize("force", [dict(split=3), dict(split=32), dict(tiles=2), dict(window=65),
-                                   dict(window=1024), dict(kernel=1)])
+                                   dict(window=1024), dict(kernel=1), dict(kernel=4, split=32),
+                                   dict(kernel=4, window=64), dict(kernel=3, split=3)])
 def test_invalid_grouped_plans_are_rejected(force):
     p = smd.SmdPlan()
     for k, v in force.items():
@@ -201,14 +202,22 @@ def test_invalid_grouped_plans_are_rejected(force):
 
 
 @pytest.mark.parametrize("B,H,W,G", [(128, 16, 8192, 4), (8, 16, 300, 2), (4, 64, 2048, 4),
-                                     (2, 16, 1, 2), (64, 32, 700, 4), (4, 16, 32768, 4)])
+                                     (2, 16, 1, 2), (64, 32, 700, 4), (4, 16, 32768, 4),
+                                     (6, 32, 9000, 2), (8, 16, 8193, 4)])
 def test_grouped_plan_invariants(B, H, W, G):
     p = smd.smd_plan_grouped(B, H, W, G).as_dict()
-    assert p["kernel"] == smd.SMD_KERNEL_GROUP and p["tiles"] == G
     assert p["split"] in (1, 2, 4, 8, 16) and p["cluster_x"] == p["split"]
-    assert -(-W // p["split"]) <= 2048 and p["key_cap"] >= -(-W // p["split"])
-    assert p["grid_x"] == H // 16 * p["split"] and p["grid_y"] == B // G
-    assert p["window"] % 64 == 0 and p["threads"] == 512 and p["smem_bytes"] <= 227 * 1024
+    assert p["threads"] == 512 and 0 < p["smem_bytes"] <= 227 * 1024
+    if G * H in (32, 64) and W <= 8192:
+        # tcgen05 groups: all G x H lanes in one CTA, <= 512 keys per CTA, smallest split
+        assert p["kernel"] == smd.SMD_KERNEL_TC_GROUP and p["tiles"] == G * H // 16
+        assert -(-W // p["split"]) <= 512 and (p["split"] == 1 or -(-W // (p["split"] // 2)) > 512)
+        assert p["grid_x"] == p["split"] and p["grid_y"] == B // G
+    else:
+        assert p["kernel"] == smd.SMD_KERNEL_GROUP and p["tiles"] == G
+        assert -(-W // p["split"]) <= 2048 and p["key_cap"] >= -(-W // p["split"])
+        assert p["grid_x"] == H // 16 * p["split"] and p["grid_y"] == B // G
+        assert p["window"] % 64 == 0
     if W <= 16384:  # a group of one is the per-row plan (which takes up to 16 x 1024 keys)
         assert smd.smd_plan_grouped(B, H, W, 1).as_dict() == smd.smd_plan(B, H, W).as_dict()
 

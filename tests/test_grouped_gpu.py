@@ -1,5 +1,6 @@
 """GPU parity of the grouped decode (smd_sparse_mla_decode_grouped): rows in
-groups of 2 or 4 that share one index list, gathered once per group. Each
+groups of 2 or 4 that share one index list, gathered once per group, on both
+group kernels (tcgen05 where G x H is 32 or 64 lanes, warp MMA always). Each
 row's result is checked against the CPU oracle (which knows nothing about
 groups), against the per-row decode, across ring sizes (identical bits) and
 splits, and the contract check and the timeout path are exercised."""
@@ -12,6 +13,14 @@ from sparse_mla_decode_gb300 import inputs
 from test_parity_gpu import check, oracle_decode, to_dev
 
 pytestmark = pytest.mark.gpu
+
+MMA_GROUP = 3
+TC_GROUP = 4
+
+
+def kernels(G, H, W):
+    """The group kernels that take these shapes."""
+    return [MMA_GROUP, TC_GROUP] if G * H in (32, 64) and W <= 8192 else [MMA_GROUP]
 
 
 def grouped(case, dev, G, plan=None, tensors=None, expect_status=0):
@@ -42,30 +51,43 @@ def test_grouped_matches_the_oracle_and_the_per_row_decode(cuda, shape):
     R, G, H, W, N, counts = shape
     case = inputs.grouped_case(10 * R + G + W, R, G, H, W, N, counts)
     t = to_dev(case, cuda)
-    out_g, lse_g = grouped(case, cuda, G, tensors=t)
     out_o, lse_o = oracle_decode(case)
-    check(out_g, lse_g, out_o, lse_o, f"grouped {shape}")
     from test_parity_gpu import gpu_decode
     out_r, lse_r = gpu_decode(case, cuda, tensors=t)
-    check(out_g, lse_g, out_r, lse_r, f"grouped vs per-row {shape}")
+    for kern in kernels(G, H, W):
+        out_g, lse_g = grouped(case, cuda, G, plan=dict(kernel=kern), tensors=t)
+        check(out_g, lse_g, out_o, lse_o, f"grouped kernel {kern} {shape}")
+        check(out_g, lse_g, out_r, lse_r, f"grouped kernel {kern} vs per-row {shape}")
 
 
-@pytest.mark.parametrize("split", [1, 2, 4, 8, 16])
-def test_grouped_every_split(cuda, split):
+@pytest.mark.parametrize("kern,split", [(MMA_GROUP, s) for s in (1, 2, 4, 8, 16)] +
+                         [(TC_GROUP, s) for s in (4, 8, 16)])
+def test_grouped_every_split(cuda, kern, split):
     case = inputs.grouped_case(41, 2, 4, 16, 1100, 12000, [1100, 1099, 700, 2, 0, 300, 301, 64])
     t = to_dev(case, cuda)
     out_o, lse_o = oracle_decode(case)
-    out_g, lse_g = grouped(case, cuda, 4, plan=dict(split=split), tensors=t)
-    check(out_g, lse_g, out_o, lse_o, f"grouped split {split}")
+    out_g, lse_g = grouped(case, cuda, 4, plan=dict(kernel=kern, split=split), tensors=t)
+    check(out_g, lse_g, out_o, lse_o, f"grouped kernel {kern} split {split}")
+
+
+def test_tc_groups_up_to_8192_keys(cuda):
+    """Sixteen CTAs per cluster, 512 keys each, ragged last CTAs."""
+    case = inputs.grouped_case(46, 2, 4, 16, 8192, 40000, [8192, 8191, 8190, 8189, 5000, 5001, 4999, 0])
+    t = to_dev(case, cuda)
+    out_g, lse_g = grouped(case, cuda, 4, plan=dict(kernel=TC_GROUP), tensors=t)
+    out_o, lse_o = oracle_decode(case)
+    check(out_g, lse_g, out_o, lse_o, "tc groups 8192")
 
 
 def test_grouped_ring_size_changes_no_bits(cuda):
-    """The ring size (64-key slots) only lays work out: identical bits."""
+    """The warp-MMA group kernel's ring size (64-key slots) only lays work
+    out: identical bits."""
     case = inputs.grouped_case(42, 3, 4, 16, 900, 10000)
     t = to_dev(case, cuda)
-    ref = grouped(case, cuda, 4, plan=dict(split=4, window=64), tensors=t)
+    ref = grouped(case, cuda, 4, plan=dict(kernel=MMA_GROUP, split=4, window=64), tensors=t)
     for window in (128, 192, 256):
-        out, lse = grouped(case, cuda, 4, plan=dict(split=4, window=window), tensors=t)
+        out, lse = grouped(case, cuda, 4, plan=dict(kernel=MMA_GROUP, split=4, window=window),
+                           tensors=t)
         assert np.array_equal(out, ref[0]), window
         assert np.array_equal(lse.view(np.uint32), ref[1].view(np.uint32)), window
 
@@ -80,35 +102,40 @@ def test_group_of_one_is_the_per_row_decode(cuda):
     assert np.array_equal(lse_1.view(np.uint32), lse_r.view(np.uint32))
 
 
-def test_rows_that_do_not_share_their_list_are_reported(cuda):
+@pytest.mark.parametrize("kern", [MMA_GROUP, TC_GROUP])
+def test_rows_that_do_not_share_their_list_are_reported(cuda, kern):
     """One row of the second group reads a key its group's longest list does
     not hold: the call reports SMD_ERR_GROUP; the first group is unaffected."""
     from sparse_mla_decode_gb300 import binding
     case = inputs.grouped_case(44, 2, 4, 16, 256, 4000, [256, 255, 254, 253, 200, 256, 100, 7])
     case.indices[6, 50] = (case.indices[5, 50] + 1) % case.N
     t = to_dev(case, cuda)
-    out_g, lse_g = grouped(case, cuda, 4, tensors=t, expect_status=binding.SMD_ERR_GROUP)
+    out_g, lse_g = grouped(case, cuda, 4, plan=dict(kernel=kern), tensors=t,
+                           expect_status=binding.SMD_ERR_GROUP)
     out_o, lse_o = oracle_decode(case, rows=[0, 1, 2, 3])
-    check(out_g[:4], lse_g[:4], out_o, lse_o, "grouped, the group that keeps the contract")
+    check(out_g[:4], lse_g[:4], out_o, lse_o, f"grouped kernel {kern}, the group that keeps the contract")
 
 
-def test_grouped_timeout_is_reported_and_the_context_survives(cuda):
+@pytest.mark.parametrize("kern", [MMA_GROUP, TC_GROUP])
+def test_grouped_timeout_is_reported_and_the_context_survives(cuda, kern):
     from sparse_mla_decode_gb300 import binding
-    case = inputs.grouped_case(45, 2, 4, 16, 300, 4000)
+    case = inputs.grouped_case(45, 2, 4, 16, 600, 4000)
     t = to_dev(case, cuda)
-    grouped(case, cuda, 4, plan=dict(inject_stall=1, wait_budget_us=2000, split=2), tensors=t,
-            expect_status=binding.SMD_ERR_TIMEOUT)
-    out_g, lse_g = grouped(case, cuda, 4, tensors=t)
+    grouped(case, cuda, 4, plan=dict(kernel=kern, inject_stall=1, wait_budget_us=2000, split=2),
+            tensors=t, expect_status=binding.SMD_ERR_TIMEOUT)
+    out_g, lse_g = grouped(case, cuda, 4, plan=dict(kernel=kern), tensors=t)
     out_o, lse_o = oracle_decode(case)
-    check(out_g, lse_g, out_o, lse_o, "grouped after a timeout")
+    check(out_g, lse_g, out_o, lse_o, f"grouped kernel {kern} after a timeout")
 
 
 def test_dense_as_sparse_full_size_sampled_rows(cuda):
-    """The dense-as-sparse workload at full size through the grouped call,
-    in the plan bench.py times; sampled requests against the oracle."""
+    """The dense-as-sparse workload at full size through the grouped call, in
+    the plan bench.py times and on the other group kernel; sampled requests
+    against the oracle."""
     case = inputs.config("dense")
     t = to_dev(case, cuda)
-    out_g, lse_g = grouped(case, cuda, 4, tensors=t)
     rows = [0, 1, 2, 3, 60, 61, 62, 63, 124, 125, 126, 127]
     out_o, lse_o = oracle_decode(case, rows)
-    check(out_g[rows], lse_g[rows], out_o, lse_o, "dense grouped sampled")
+    for plan in (None, dict(kernel=MMA_GROUP)):
+        out_g, lse_g = grouped(case, cuda, 4, plan=plan, tensors=t)
+        check(out_g[rows], lse_g[rows], out_o, lse_o, f"dense grouped sampled {plan}")
