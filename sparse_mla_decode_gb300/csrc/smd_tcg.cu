@@ -89,10 +89,39 @@ __device__ __forceinline__ void wait_next(uint32_t bar, uint32_t& seen, bool& ok
     ++seen;
 }
 
+// The contract, on the keys this CTA reads: every other row of the group
+// agrees with the staged list on its first count entries (warps 0-7, once the
+// first chunks' gathers are in flight; a mismatch only sets the status).
+__device__ __forceinline__ void check_contract(const TcgParams& p, const uint8_t* smem, int b0,
+                                               int ref, const Keys& k) {
+    const int t = threadIdx.x;
+    const int32_t* idx_s = reinterpret_cast<const int32_t*>(smem + kOffIdx);
+    const int32_t* nrow = reinterpret_cast<const int32_t*>(smem + kOffNrow);
+    bool bad = false;
+    for (int r = 0; r < p.G; ++r) {
+        if (r == ref) continue;
+        const int32_t* row_idx = p.a.indices + static_cast<int64_t>(b0 + r) * p.a.W + k.first;
+        const int lim = min(k.mine, nrow[r] - k.first);
+        int v[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = t + u * kProducerThreads;
+            v[u] = (i < lim) ? row_idx[i] : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = t + u * kProducerThreads;
+            if (i < lim && v[u] != idx_s[i]) bad = true;
+        }
+    }
+    if (bad && p.a.status != nullptr) atomicCAS(p.a.status, 0, SMD_ERR_GROUP);
+}
+
 // ---- warps 0-7: TMA producers -------------------------------------------------
 // Pass A: the query tile was issued at setup; here the CTA's indices (from the
-// group's longest list) are staged and checked against the other rows' lists,
-// then chunk c goes to slot c & 1 once QK of chunk c - 2 has left it; thread
+// group's longest list) are staged, then chunk c goes to slot c & 1 once QK
+// of chunk c - 2 has left it (the contract is checked after the first chunks
+// are issued); thread
 // t < 160 issues piece t % 5 (four 128-byte column blocks, the 64-byte tail)
 // of rows 4g .. 4g + 3, g = t / 5.
 __device__ __forceinline__ void producer_a(const TcgMaps& maps, const TcgParams& p, uint8_t* smem,
@@ -101,17 +130,8 @@ __device__ __forceinline__ void producer_a(const TcgMaps& maps, const TcgParams&
     const int t = threadIdx.x;
     const int W = p.a.W;
     int32_t* idx_s = reinterpret_cast<int32_t*>(smem + kOffIdx);
-    const int32_t* nrow = reinterpret_cast<const int32_t*>(smem + kOffNrow);
     const int32_t* ref_idx = p.a.indices + static_cast<int64_t>(b0 + ref) * W + k.first;
     for (int i = t; i < kTcMaxKeys; i += kProducerThreads) idx_s[i] = (i < k.mine) ? ref_idx[i] : 0;
-    bool bad = false;
-    for (int r = 0; r < p.G; ++r) {
-        if (r == ref) continue;
-        const int32_t* row_idx = p.a.indices + static_cast<int64_t>(b0 + r) * W + k.first;
-        const int lim = min(k.mine, nrow[r] - k.first);
-        for (int i = t; i < lim; i += kProducerThreads) bad = bad || (row_idx[i] != ref_idx[i]);
-    }
-    if (bad && p.a.status != nullptr) atomicCAS(p.a.status, 0, SMD_ERR_GROUP);
     asm volatile("bar.sync 1, %0;" ::"r"(kProducerThreads) : "memory");
 
     uint32_t seen[2] = {0u, 0u};
@@ -131,7 +151,9 @@ __device__ __forceinline__ void producer_a(const TcgMaps& maps, const TcgParams&
             else
                 tma_gather4(slot + 4 * kBlock + 4 * g * 64, &maps.kv_tail, 512, rw[0], rw[1], rw[2], rw[3], full);
         }
+        if (c == min(k.nch, 2) - 1) check_contract(p, smem, b0, ref, k);  // off the gathers' path
     }
+    if (k.nch == 0) check_contract(p, smem, b0, ref, k);
 }
 
 // Pass B visits chunks in descending order; the last two are resident, the
