@@ -353,7 +353,7 @@ def run_gpu(args, world, rank, local) -> dict | None:
 
 
 KERNEL_FILES = {1: ("mma_decode_kernel", "smd_mma.cu"), 2: ("tc_decode_kernel", "smd_tc.cu"),
-                3: ("group_decode_kernel", "smd_group.cu")}
+                3: ("group_decode_kernel", "smd_group.cu"), 4: ("tcg_decode_kernel", "smd_tcg.cu")}
 # Workloads whose rows come in groups sharing one index list (rows per group).
 ROW_GROUP = {"dense": 4}
 
