@@ -36,7 +36,7 @@ struct CallArgs {
 
 // Shared-memory carve-up of the warp-MMA kernel (byte offsets).
 struct MmaLayout {
-    int32_t kv, q, logits, probs, idx, inbox, sums, maxima, lsum, rowmax, bars;
+    int32_t kv, q, logits, probs, idx, inbox, sums, maxima, wmax, lsum, rowmax, bars;
     int32_t logit_pitch;  // floats per logits row
     int32_t prob_pitch;   // bytes per P8 row
     int32_t total;
@@ -74,6 +74,8 @@ __host__ __device__ inline MmaLayout mma_layout(int tiles, int split, int window
     o += split * ch * 4;
     L.maxima = o; // [split][ch] fp32
     o += split * ch * 4;
+    L.wmax = o;   // [4 key groups][ch] fp32: the QK jobs' maxima
+    o += 4 * ch * 4;
     L.lsum = o;   // [ch] running sums of P
     o += ch * 4;
     L.rowmax = o; // [ch] the row maximum

@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     float* inbox = reinterpret_cast<float*>(smem + p.L.inbox);
     float* sums = reinterpret_cast<float*>(smem + p.L.sums);
     float* maxima = reinterpret_cast<float*>(smem + p.L.maxima);
+    float* wmax = reinterpret_cast<float*>(smem + p.L.wmax);
     float* lsum = reinterpret_cast<float*>(smem + p.L.lsum);
     float* rowmax = reinterpret_cast<float*>(smem + p.L.rowmax);
     const int nchunk_bars = p.window / kChunk;
@@ -183,6 +184,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
 
     mbar_wait(q_bar, 0, ok, status, p.budget_ns);
 
+    // The maximum of each QK job's logits (heads g and g + 8 of its tile over
+    // its keys), kept as the logits are written; warp w has job w (4T <= 16).
+    float jmax[2] = {-INFINITY, -INFINITY};
+
     // ================================ pass A: logits =========================
     // The gather of chunk c + NS is issued as soon as QK of chunk c has left
     // its slot, so copies and QK overlap.
@@ -228,6 +233,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
                     float2* dst = reinterpret_cast<float2*>(
                         logits + (16 * t + g + 8 * r) * LP + c * kChunk + kk);
                     *dst = make_float2(s0, s1);
+                    jmax[r] = fmaxf(jmax[r], fmaxf(s0, s1));
                 }
             }
         }
@@ -239,12 +245,20 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     }
 
     // ---- the row maximum over the cluster ------------------------------------
-    for (int h = warp; h < CH; h += kMmaThreads / 32) {
-        float mx = neg_inf;
-        for (int k = lane; k < mine; k += 32) mx = fmaxf(mx, logits[h * LP + k]);
-        mx = warp_max(mx);
-        if (lane == 0) maxima[split * CH + h] = mx;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        jmax[r] = fmaxf(jmax[r], __shfl_xor_sync(0xffffffffu, jmax[r], 1));
+        jmax[r] = fmaxf(jmax[r], __shfl_xor_sync(0xffffffffu, jmax[r], 2));
     }
+    if (warp < 4 * T && qd == 0) {
+        const int t = warp >> 2, kg = warp & 3;
+        wmax[kg * CH + 16 * t + g] = jmax[0];
+        wmax[kg * CH + 16 * t + g + 8] = jmax[1];
+    }
+    __syncthreads();
+    for (int h = tid; h < CH; h += kMmaThreads)
+        maxima[split * CH + h] =
+            fmaxf(fmaxf(wmax[h], wmax[CH + h]), fmaxf(wmax[2 * CH + h], wmax[3 * CH + h]));
     __syncthreads();
     if (S > 1) {
         cluster_wait();  // peers' barriers are initialised
@@ -284,6 +298,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
             mbar_wait(bars + 8 * s, (phase_bits >> s) & 1u, ok, status, p.budget_ns);
             phase_bits ^= 1u << s;
         }
+        // V of the chunk, byte-transposed into MMA fragments, before P (it
+        // does not depend on P): latent columns 32*warp + 4*g + (0..3).
+        const int span = (cnt + 31) & ~31;
+        uint32_t vb[kChunk / 32][2][4];
+#pragma unroll
+        for (int ks = 0; ks < kChunk / 32; ++ks) {
+            if (32 * ks >= span) break;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int key = 32 * ks + 16 * hf + 4 * qd + i;
+                    w[i] = lds_u32(slot_s + key * kRowPitch + 32 * warp + 4 * g);
+                }
+                byte_transpose4(w[0], w[1], w[2], w[3], vb[ks][hf]);
+            }
+        }
         // P of 64 keys x this warp's heads; lane: keys 2*lane, 2*lane + 1.
 #pragma unroll
         for (int i = 0; i < T; ++i) {
@@ -299,27 +331,15 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         }
         __syncthreads();
         // PV: latent columns 32*warp + 4*g + (0..3), every tile.
-        const int span = (cnt + 31) & ~31;
 #pragma unroll
         for (int ks = 0; ks < kChunk / 32; ++ks) {
             if (32 * ks >= span) break;
-            uint32_t vb[2][4];
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t w[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int key = 32 * ks + 16 * hf + 4 * qd + i;
-                    w[i] = lds_u32(slot_s + key * kRowPitch + 32 * warp + 4 * g);
-                }
-                byte_transpose4(w[0], w[1], w[2], w[3], vb[hf]);
-            }
 #pragma unroll
             for (int t = 0; t < T; ++t) {
                 uint32_t pa[4];
                 ldsm_x4(prob_s + (16 * t + a_row) * PP + 32 * ks + a_col, pa);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) mma_e4m3(acc[t][j], pa, vb[0][j], vb[1][j]);
+                for (int j = 0; j < 4; ++j) mma_e4m3(acc[t][j], pa, vb[ks][0][j], vb[ks][1][j]);
             }
         }
         // The slot and P are free; a failed CTA issues no more copies.
