@@ -33,13 +33,13 @@
 #include "smd.h"
 #include "smd_internal.h"
 #include "smd_ptx.cuh"
+#include "smd_tc_common.cuh"
 
 namespace smd {
 namespace {
 
-constexpr int kBlock = 16384;       // one 128-byte-wide column block of 128 rows (SW128)
-constexpr int kTail = 8192;         // the 64-byte tail block of 128 rows (SW64)
-constexpr int kTile = 4 * kBlock + kTail;  // 576 columns x 128 rows
+using tcc::kBlock;
+using tcc::kTile;
 constexpr int kOffQP = 0;           // query tile, later the P tiles (4 x 16 KB)
 constexpr int kOffRing = kTile;     // two chunk slots
 constexpr int kDead = 3 * kTile;    // [0, kDead): inboxes and the output stage after PV
@@ -83,10 +83,23 @@ __device__ __forceinline__ int inbox_bytes(int lanes, int CW) {
     return (lanes * CW * 4 + lanes * 4 + 15) & ~15;
 }
 
-__device__ __forceinline__ void wait_next(uint32_t bar, uint32_t& seen, bool& ok, int32_t* status,
-                                          uint64_t budget) {
-    mbar_wait(bar, seen & 1u, ok, status, budget);
-    ++seen;
+// The shared-memory addresses and barriers of the chunk pipeline.
+__device__ __forceinline__ tcc::Pipe pipe_of(const TcgParams& p, uint32_t base, uint32_t bars,
+                                             const uint8_t* smem) {
+    tcc::Pipe pp;
+    pp.q = base + kOffQP;
+    pp.ring = base + kOffRing;
+    pp.full = bars + 8 * kBarFull;
+    pp.empty = bars + 8 * kBarEmpty;
+    pp.free_b = bars + 8 * kBarFreeB;
+    pp.s = bars + 8 * kBarS;
+    pp.bar_q = bars + 8 * kBarQ;
+    pp.bar_p = bars + 8 * kBarP;
+    pp.bar_o = bars + 8 * kBarO;
+    pp.idx = reinterpret_cast<const int32_t*>(smem + kOffIdx);
+    pp.status = p.a.status;
+    pp.budget_ns = p.budget_ns;
+    return pp;
 }
 
 // The contract, on the keys this CTA reads: every other row of the group
@@ -119,134 +132,21 @@ __device__ __forceinline__ void check_contract(const TcgParams& p, const uint8_t
 
 // ---- warps 0-7: TMA producers -------------------------------------------------
 // Pass A: the query tile was issued at setup; here the CTA's indices (from the
-// group's longest list) are staged, then chunk c goes to slot c & 1 once QK
-// of chunk c - 2 has left it (the contract is checked after the first chunks
-// are issued); thread
-// t < 160 issues piece t % 5 (four 128-byte column blocks, the 64-byte tail)
-// of rows 4g .. 4g + 3, g = t / 5.
-__device__ __forceinline__ void producer_a(const TcgMaps& maps, const TcgParams& p, uint8_t* smem,
-                                           uint32_t base, uint32_t bars, int b0, int ref,
+// group's longest list) are staged, the first two chunks gathered, the
+// contract checked (off the gathers' path) and the other chunks gathered.
+__device__ __forceinline__ void producer_a(const TcgMaps& maps, const TcgParams& p,
+                                           const tcc::Pipe& pp, uint8_t* smem, int b0, int ref,
                                            const Keys& k, bool& ok) {
     const int t = threadIdx.x;
-    const int W = p.a.W;
     int32_t* idx_s = reinterpret_cast<int32_t*>(smem + kOffIdx);
-    const int32_t* ref_idx = p.a.indices + static_cast<int64_t>(b0 + ref) * W + k.first;
+    const int32_t* ref_idx = p.a.indices + static_cast<int64_t>(b0 + ref) * p.a.W + k.first;
     for (int i = t; i < kTcMaxKeys; i += kProducerThreads) idx_s[i] = (i < k.mine) ? ref_idx[i] : 0;
     asm volatile("bar.sync 1, %0;" ::"r"(kProducerThreads) : "memory");
-
     uint32_t seen[2] = {0u, 0u};
-    for (int c = 0; c < k.nch && ok; ++c) {
-        const int s = c & 1;
-        const uint32_t need = static_cast<uint32_t>(c >> 1);
-        while (seen[s] < need) wait_next(bars + 8 * (kBarEmpty + s), seen[s], ok, p.a.status, p.budget_ns);
-        if (!ok) break;
-        const uint32_t slot = base + kOffRing + s * kTile;
-        const uint32_t full = bars + 8 * (kBarFull + s);
-        if (t == 0) mbar_arrive_expect_tx(full, kTile);
-        if (t < 160) {
-            const int g = t / 5, j = t % 5;
-            const int32_t* rw = idx_s + kTcChunk * c + 4 * g;
-            if (j < 4)
-                tma_gather4(slot + j * kBlock + 4 * g * 128, &maps.kv, 128 * j, rw[0], rw[1], rw[2], rw[3], full);
-            else
-                tma_gather4(slot + 4 * kBlock + 4 * g * 64, &maps.kv_tail, 512, rw[0], rw[1], rw[2], rw[3], full);
-        }
-        if (c == min(k.nch, 2) - 1) check_contract(p, smem, b0, ref, k);  // off the gathers' path
-    }
-    if (k.nch == 0) check_contract(p, smem, b0, ref, k);
-}
-
-// Pass B visits chunks in descending order; the last two are resident, the
-// others come back (V columns only) into their slot once PV of the chunk two
-// above has released it.
-__device__ __forceinline__ void producer_b(const TcgMaps& maps, const TcgParams& p, uint8_t* smem,
-                                           uint32_t base, uint32_t bars, const Keys& k, bool& ok) {
-    const int t = threadIdx.x;
-    const int32_t* idx_s = reinterpret_cast<const int32_t*>(smem + kOffIdx);
-    uint32_t seen_b[2] = {0u, 0u};
-    for (int c = 1; c >= 0; --c) {
-        if (c > k.nch - 3 || !ok) continue;
-        const int s = c & 1;
-        int later = 0;  // pass-B completions on slot s before PV(c + 2)
-        for (int c2 = k.nch - 1; c2 > c + 2; --c2) later += ((c2 & 1) == s);
-        const uint32_t need = static_cast<uint32_t>(later + 1);
-        while (seen_b[s] < need)
-            wait_next(bars + 8 * (kBarFreeB + s), seen_b[s], ok, p.a.status, p.budget_ns);
-        if (!ok) break;
-        const uint32_t slot = base + kOffRing + s * kTile;
-        const uint32_t full = bars + 8 * (kBarFull + s);
-        if (t == 0) mbar_arrive_expect_tx(full, 4 * kBlock);
-        if (t < 128) {
-            const int g = t / 4, j = t % 4;
-            const int32_t* rw = idx_s + kTcChunk * c + 4 * g;
-            tma_gather4(slot + j * kBlock + 4 * g * 128, &maps.kv, 128 * j, rw[0], rw[1], rw[2], rw[3], full);
-        }
-    }
-}
-
-// ---- warp 8, one lane: MMA issuer -----------------------------------------------
-__device__ __forceinline__ void mma_pass_a(const TcgParams& p, uint32_t base, uint32_t bars,
-                                           uint32_t tmem, const Keys& k, uint32_t (&full_seen)[2],
-                                           bool& ok) {
-    mbar_wait(bars + 8 * kBarQ, 0, ok, p.a.status, p.budget_ns);
-    tc_fence_after();
-    constexpr uint32_t kIdQK = umma_idesc_e4m3(128, kTcChunk, 0);
-    const uint32_t q_s = base + kOffQP;
-    // S_c = Q K_c^T into TMEM columns 128c .. 128c + 127.
-    for (int c = 0; c < k.nch && ok; ++c) {
-        const int s = c & 1;
-        wait_next(bars + 8 * (kBarFull + s), full_seen[s], ok, p.a.status, p.budget_ns);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t slot = base + kOffRing + s * kTile;
-        const uint32_t d = tmem + kTcChunk * c;
-        uint32_t acc = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                umma_e4m3(d, umma_desc(q_s + j * kBlock + 32 * kk, 16, 1024, 2),
-                          umma_desc(slot + j * kBlock + 32 * kk, 16, 1024, 2), kIdQK, acc);
-                acc = 1;
-            }
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
-            umma_e4m3(d, umma_desc(q_s + 4 * kBlock + 32 * kk, 16, 512, 4),
-                      umma_desc(slot + 4 * kBlock + 32 * kk, 16, 512, 4), kIdQK, 1);
-        umma_commit(bars + 8 * (kBarS + c));
-        umma_commit(bars + 8 * (kBarEmpty + s));
-    }
-}
-
-// O = sum_c P_c V_c, chunks in descending order, into TMEM columns 0..511 (two
-// N = 256 halves); V is the MN-major operand read from the gathered tile.
-__device__ __forceinline__ void mma_pass_b(const TcgParams& p, uint32_t base, uint32_t bars,
-                                           uint32_t tmem, const Keys& k, uint32_t (&full_seen)[2],
-                                           bool& ok) {
-    constexpr uint32_t kIdPV = umma_idesc_e4m3(128, 256, 1);
-    mbar_wait(bars + 8 * kBarP, 0, ok, p.a.status, p.budget_ns);
-    tc_fence_after();
-    for (int c = k.nch - 1; c >= 0 && ok; --c) {
-        const int s = c & 1;
-        if (c <= k.nch - 3) {
-            wait_next(bars + 8 * (kBarFull + s), full_seen[s], ok, p.a.status, p.budget_ns);
-            if (!ok) break;
-            tc_fence_after();
-        }
-        const uint32_t slot = base + kOffRing + s * kTile;
-        const uint32_t p_tile = base + kOffQP + c * kBlock;
-        const int cnt = min(kTcChunk, k.mine - kTcChunk * c);
-        const int ksteps = (cnt + 31) / 32;
-        for (int ks = 0; ks < ksteps; ++ks) {
-            const uint32_t acc = (c == k.nch - 1 && ks == 0) ? 0u : 1u;
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-                umma_e4m3(tmem + 256 * h, umma_desc(p_tile + 32 * ks, 16, 1024, 2),
-                          umma_desc(slot + 2 * h * kBlock + ks * 4096, kBlock, 1024, 2), kIdPV, acc);
-        }
-        umma_commit(bars + 8 * (kBarFreeB + s));
-    }
-    umma_commit(bars + 8 * kBarO);
+    const int head = min(k.nch, 2);
+    tcc::gather_pass_a(maps.kv, maps.kv_tail, pp, 0, head, seen, ok);
+    check_contract(p, smem, b0, ref, k);
+    tcc::gather_pass_a(maps.kv, maps.kv_tail, pp, head, k.nch, seen, ok);
 }
 
 // ---- warps 12-13: this CTA's maxima (thread = lane = TMEM lane h < L) ----------
@@ -517,11 +417,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     k.mine = min(nmax - k.first, per);
     k.nch = (k.mine + kTcChunk - 1) / kTcChunk;
 
+    const tcc::Pipe pp = pipe_of(p, base, bars, smem);
     uint32_t full_seen[2] = {0u, 0u};
     if (warp < 8) {
-        producer_a(maps, p, smem, base, bars, b0, ref, k, ok);
+        producer_a(maps, p, pp, smem, b0, ref, k, ok);
     } else if (warp == 8) {
-        if (lane == 0) mma_pass_a(p, base, bars, tmem, k, full_seen, ok);
+        if (lane == 0) tcc::mma_qk(pp, tmem, k.nch, full_seen, ok);
         __syncwarp();
     } else if (warp >= 12) {
         local_max(p, smem, bars, tmem, k, ok);
@@ -547,9 +448,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     p_phase(p, smem, bars, tmem, k, ok);
     if (warp < 8) {
-        producer_b(maps, p, smem, base, bars, k, ok);
+        tcc::gather_pass_b(maps.kv, pp, k.nch, ok);
     } else if (warp == 8) {
-        if (lane == 0) mma_pass_b(p, base, bars, tmem, k, full_seen, ok);
+        if (lane == 0) tcc::mma_pv(pp, tmem, k.nch, k.mine, full_seen, ok);
         __syncwarp();
     }
     mbar_wait(bars + 8 * kBarO, 0, ok, p.a.status, p.budget_ns);
