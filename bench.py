@@ -183,6 +183,11 @@ def run_gpu(args, world, rank, local) -> dict | None:
     # workload's four causal rows per request) go through the grouped call.
     group = ROW_GROUP.get(args.config, 1)
     plan = binding.smd_plan_grouped(case.B, case.H, case.W, group).as_dict()
+    # Where the library's workspace plan (the spread kernel) applies, the
+    # workspace entry point is timed with a workspace of the size it asks for.
+    ws_bytes = binding.smd_workspace_bytes(case.B, case.H, case.W) if group == 1 else 0
+    if ws_bytes > 0:
+        plan = binding.smd_plan_ws(case.B, case.H, case.W).as_dict()
 
     q = torch.from_numpy(case.q8).to(dev)
     kv = torch.from_numpy(case.kv8).to(dev)
@@ -200,9 +205,7 @@ def run_gpu(args, world, rank, local) -> dict | None:
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
 
-    # The on-chip (DSMEM) exchange of split partials measured faster than the
-    # L2-workspace exchange on GB300, so the plain entry point is timed.
-    ws_bytes = 0
+    workspace = torch.zeros(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     ptrs = (q.data_ptr(), kv.data_ptr(), case.N, idx.data_ptr(), case.W, cnt.data_ptr(),
             case.B, case.H, case.sm_scale, case.q_scale, case.k_scale, out.data_ptr(),
             lse.data_ptr(), status.data_ptr(), sptr)
@@ -212,6 +215,8 @@ def run_gpu(args, world, rank, local) -> dict | None:
     def decode():
         if group > 1:
             rc = binding.smd_sparse_mla_decode_grouped(*gptrs)
+        elif ws_bytes > 0:
+            rc = binding.smd_sparse_mla_decode_ws(*ptrs[:-1], workspace.data_ptr(), ws_bytes, sptr)
         else:
             rc = binding.smd_sparse_mla_decode(*ptrs)
         if rc != 0:
@@ -262,7 +267,8 @@ def run_gpu(args, world, rank, local) -> dict | None:
         didx.copy_(hidx, non_blocking=True)
         dcnt.copy_(hcnt, non_blocking=True)
         binding.sparse_mla_decode(dq, kv, didx, dcnt, case.sm_scale, case.q_scale, case.k_scale,
-                                  out=out, lse=lse, status=status, row_group=group)
+                                  out=out, lse=lse, status=status, row_group=group,
+                                  workspace=workspace if ws_bytes > 0 else None)
         hout.copy_(out, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
 
@@ -353,7 +359,8 @@ def run_gpu(args, world, rank, local) -> dict | None:
 
 
 KERNEL_FILES = {1: ("mma_decode_kernel", "smd_mma.cu"), 2: ("tc_decode_kernel", "smd_tc.cu"),
-                3: ("group_decode_kernel", "smd_group.cu"), 4: ("tcg_decode_kernel", "smd_tcg.cu")}
+                3: ("group_decode_kernel", "smd_group.cu"), 4: ("tcg_decode_kernel", "smd_tcg.cu"),
+                5: ("tcs_decode_kernel", "smd_tcs.cu")}
 # Workloads whose rows come in groups sharing one index list (rows per group).
 ROW_GROUP = {"dense": 4}
 

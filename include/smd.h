@@ -72,8 +72,14 @@ enum {
                             heads of a row), TMA gather4; 1 <= W <= 2048     */
     SMD_KERNEL_GROUP = 3,   /* warp-level FP8 MMA over groups of rows sharing
                                one index list (smd_sparse_mla_decode_grouped) */
-    SMD_KERNEL_TC_GROUP = 4 /* tcgen05 over such groups: G * H = 32 or 64 TMEM
+    SMD_KERNEL_TC_GROUP = 4, /* tcgen05 over such groups: G * H = 32 or 64 TMEM
                                lanes, W <= 16 * 512, clusters of up to 16     */
+    SMD_KERNEL_TC_SPREAD = 5 /* tcgen05 with a row's keys spread over any CTAs
+                               of a cooperative grid (pieces of <= 512 keys,
+                               as many as the row's count needs); maxima and
+                               FP32 partials through the caller's workspace;
+                               H % 128 == 0 or H < 128, 1 <= W <= 32 * 512,
+                               B * ceil(H / 128) <= 1024                      */
 };
 
 /* A launch plan: how the work is laid out. `split` decides which keys each
@@ -94,6 +100,9 @@ typedef struct {
     /* filled in by smd_plan / smd_sparse_mla_decode_ex:                     */
     int32_t key_cap;     /* most keys one CTA holds logits for               */
     int32_t grid_x, grid_y, cluster_x, threads, smem_bytes;
+                         /* (SMD_KERNEL_TC_SPREAD: a non-zero grid_x in a
+                            forced plan caps the grid; it only lays work out,
+                            so every grid gives identical bits)             */
 } smd_plan_t;
 
 /*
@@ -127,20 +136,36 @@ int smd_sparse_mla_decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
  * device. Host only; touches no device memory. */
 int smd_plan(int32_t B, int32_t H, int32_t W, smd_plan_t* plan);
 
-/* Bytes of workspace smd_sparse_mla_decode_ws can use for (B, H, W): 0 when
- * the plan merges its split partials on chip only (then a workspace is not
- * needed), else the size of the L2 exchange workspace (one slot of FP32
- * partials per SM id; about 48 MiB). Host only. */
+/* Bytes of workspace smd_sparse_mla_decode_ws can use for (B, H, W): the
+ * size SMD_KERNEL_TC_SPREAD wants when smd_plan_ws would choose it (one slot
+ * per possible piece, B * ceil(H / 128) * ceil(W / 512) slots of about
+ * 257 KiB), else 0 (the plan merges on chip: no workspace needed). Host only. */
 int64_t smd_workspace_bytes(int32_t B, int32_t H, int32_t W);
 
-/* As smd_sparse_mla_decode, with a caller-owned device workspace. When the
- * plan splits rows over a cluster of tcgen05 CTAs, their FP32 partials are
- * exchanged through this workspace (L2) instead of distributed shared
- * memory (about as fast on GB300). workspace may be NULL (the on-chip
- * exchange is used); otherwise it must be 16-byte aligned and at least
- * smd_workspace_bytes(B, H, W) long (else SMD_ERR_WORKSPACE). Its contents
- * need no initialisation and are scratch; calls that overlap on the GPU
- * must not share one workspace. */
+/* Bytes of workspace the plan forced by `force` (as smd_sparse_mla_decode_ex
+ * reads it; NULL = automatic) can use: the spread kernel's slots, or a
+ * cluster plan's L2 exchange slots (which smd_sparse_mla_decode_ex uses when
+ * it is given a workspace). Host only. */
+int64_t smd_workspace_bytes_ex(int32_t B, int32_t H, int32_t W, const smd_plan_t* force);
+
+/* The plan smd_sparse_mla_decode_ws uses for (B, H, W) given a workspace:
+ * with H % 128 == 0, B * ceil(H / 128) <= 1024 and W > 512 it is
+ * SMD_KERNEL_TC_SPREAD when the rows are longer than one cluster holds
+ * (W > 2048) or when the at most B * ceil(H / 128) * ceil(W / 512) pieces
+ * fill no more than two waves of the device; otherwise the plan of smd_plan.
+ * Host only. */
+int smd_plan_ws(int32_t B, int32_t H, int32_t W, smd_plan_t* plan);
+
+/* As smd_sparse_mla_decode, with a caller-owned device workspace, in the
+ * plan of smd_plan_ws. SMD_KERNEL_TC_SPREAD exchanges the row maxima and the
+ * FP32 partials of a row's pieces through it. workspace may be NULL (the plan of
+ * smd_plan is used); otherwise it must be 16-byte aligned and at least
+ * smd_workspace_bytes(B, H, W) long (else SMD_ERR_WORKSPACE); plans other
+ * than the spread kernel leave it untouched. Its contents need no initialisation: the
+ * spread kernel's flags hold a per-call 64-bit token and are zeroed as they
+ * are consumed. Calls that overlap on the GPU must not share one workspace;
+ * after a call that reported a device error, zero the workspace before a
+ * CUDA graph replays a captured call on it. */
 int smd_sparse_mla_decode_ws(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
                              const int32_t* indices, int32_t W, const int32_t* counts,
                              int32_t B, int32_t H,
@@ -152,7 +177,9 @@ int smd_sparse_mla_decode_ws(const uint8_t* q, const uint8_t* kv_pool, int64_t N
 /* As smd_sparse_mla_decode_ws, with the plan fields kernel/split/tiles/window
  * (and the testing hooks) taken from `force` (0 = the automatic choice for
  * that field). Used by the tests to run every variant; `force` and
- * `workspace` may be NULL. */
+ * `workspace` may be NULL. Given a workspace (smd_workspace_bytes_ex bytes),
+ * a forced cluster plan of the tcgen05 kernel exchanges its partials through
+ * it (L2) instead of distributed shared memory. */
 int smd_sparse_mla_decode_ex(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
                              const int32_t* indices, int32_t W, const int32_t* counts,
                              int32_t B, int32_t H,

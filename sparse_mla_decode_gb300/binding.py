@@ -27,6 +27,7 @@ SMD_KERNEL_MMA = 1
 SMD_KERNEL_TC = 2
 SMD_KERNEL_GROUP = 3
 SMD_KERNEL_TC_GROUP = 4
+SMD_KERNEL_TC_SPREAD = 5
 
 
 class SmdPlan(ctypes.Structure):
@@ -84,9 +85,14 @@ def lib() -> ctypes.CDLL:
             so.smd_plan_grouped.argtypes = [ctypes.c_int32] * 4 + [ctypes.POINTER(SmdPlan)]
             so.smd_workspace_bytes.restype = ctypes.c_int64
             so.smd_workspace_bytes.argtypes = [ctypes.c_int32] * 3
+            so.smd_workspace_bytes_ex.restype = ctypes.c_int64
+            so.smd_workspace_bytes_ex.argtypes = [ctypes.c_int32] * 3 + [ctypes.POINTER(SmdPlan)]
             so.smd_plan.restype = ctypes.c_int
             so.smd_plan.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                     ctypes.POINTER(SmdPlan)]
+            so.smd_plan_ws.restype = ctypes.c_int
+            so.smd_plan_ws.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.POINTER(SmdPlan)]
             so.smd_scale_log2.restype = ctypes.c_float
             so.smd_scale_log2.argtypes = [ctypes.c_float] * 3
             so.smd_status_str.restype = ctypes.c_char_p
@@ -161,11 +167,29 @@ def smd_workspace_bytes(B: int, H: int, W: int) -> int:
     return int(lib().smd_workspace_bytes(B, H, W))
 
 
+def smd_workspace_bytes_ex(B: int, H: int, W: int, force: SmdPlan | dict | None = None) -> int:
+    if isinstance(force, dict):
+        p = SmdPlan()
+        for k, v in force.items():
+            setattr(p, k, int(v))
+        force = p
+    ref = ctypes.byref(force) if force is not None else None
+    return int(lib().smd_workspace_bytes_ex(B, H, W, ref))
+
+
 def smd_plan(B: int, H: int, W: int) -> SmdPlan:
     p = SmdPlan()
     rc = lib().smd_plan(B, H, W, ctypes.byref(p))
     if rc != SMD_OK:
         raise SmdError(rc, "smd_plan")
+    return p
+
+
+def smd_plan_ws(B: int, H: int, W: int) -> SmdPlan:
+    p = SmdPlan()
+    rc = lib().smd_plan_ws(B, H, W, ctypes.byref(p))
+    if rc != SMD_OK:
+        raise SmdError(rc, "smd_plan_ws")
     return p
 
 
@@ -204,8 +228,9 @@ def sparse_mla_decode(q, kv_pool, indices, counts, sm_scale: float, q_scale: flo
     Returns (out [B,H,512] bfloat16, lse [B,H] float32). ``plan`` forces
     plan fields (smd_sparse_mla_decode_ex); ``status`` is an optional int32
     CUDA tensor that receives device-side errors; ``workspace`` an optional
-    CUDA tensor of at least smd_workspace_bytes(B, H, W) bytes for the L2
-    exchange of split partials; ``row_group`` > 1 calls
+    CUDA tensor for smd_sparse_mla_decode_ws (at least
+    smd_workspace_bytes(B, H, W) bytes: the spread kernel's or the L2
+    exchange of split partials); ``row_group`` > 1 calls
     smd_sparse_mla_decode_grouped (rows in groups sharing one index list)."""
     import torch
 

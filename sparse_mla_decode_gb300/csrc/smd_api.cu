@@ -248,24 +248,97 @@ int plan_group(int B, int H, int W, int G, int sm_count, const smd_plan_t* force
     return SMD_OK;
 }
 
+// The spread kernel: 128 heads per CTA (or all H < 128), pieces of at most
+// kTcMaxKeys keys, at most kTcsMaxPieces pieces per row.
+bool tcs_fits(int B, int H, int W) {
+    return (H % kTcHeads == 0 || H < kTcHeads) && W >= 1 && W <= kTcsMaxPieces * kTcMaxKeys &&
+           static_cast<int64_t>(B) * ceil_div(H, kTcHeads) <= kTcsMaxUnits;
+}
+
+int64_t tcs_items_cap(int B, int H, int W) {
+    return static_cast<int64_t>(B) * ceil_div(H, kTcHeads) * ceil_div(W, kTcMaxKeys);
+}
+
+int64_t tcs_workspace_bytes(int B, int H, int W) {
+    return tcs_workspace(tcs_items_cap(B, H, W)).total;
+}
+
+// The spread kernel's plan: one CTA per resident slot, no more than there can
+// be pieces (a forced grid_x caps it).
+int plan_tcs(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_plan_t* out,
+             TcsConfig* cfg) {
+    if (!tcs_fits(B, H, W)) return SMD_ERR_PLAN;
+    const int lanes = std::min(H, kTcHeads);
+    if (force && ((force->tiles && force->tiles != lanes / kHeadsPerTile) ||
+                  (force->window && force->window != kTcChunk) || force->split))
+        return SMD_ERR_PLAN;
+    // Resident CTAs (one per SM); without a device, planning assumes one per SM.
+    int max_grid = tcs_max_grid();
+    if (max_grid <= 0) max_grid = sm_count;
+    const int64_t items = tcs_items_cap(B, H, W);
+    int grid = static_cast<int>(std::min<int64_t>(max_grid, items));
+    if (force && force->grid_x) {
+        if (force->grid_x < 1 || force->grid_x > max_grid) return SMD_ERR_PLAN;
+        // every piece of a row must find a CTA of its own
+        if (force->grid_x < std::min(kTcsMaxPieces, ceil_div(W, kTcMaxKeys))) return SMD_ERR_PLAN;
+        grid = std::min<int64_t>(force->grid_x, items);
+    }
+    cfg->grid = grid;
+    cfg->items_cap = static_cast<int>(items);
+    cfg->wait_budget_ns = (force && force->wait_budget_us > 0)
+                              ? static_cast<uint64_t>(force->wait_budget_us) * 1000ull
+                              : kWaitBudgetNs;
+    cfg->inject_stall = (force && force->inject_stall) ? 1 : 0;
+    cfg->ws = nullptr;
+    out->kernel = SMD_KERNEL_TC_SPREAD;
+    out->split = ceil_div(W, kTcMaxKeys);  // the most pieces a row can have
+    out->tiles = lanes / kHeadsPerTile;
+    out->window = kTcChunk;
+    out->key_cap = kTcMaxKeys;
+    out->grid_x = grid;
+    out->grid_y = 1;
+    out->cluster_x = 1;
+    out->threads = kTcThreads;
+    out->smem_bytes = tcs_smem_bytes();
+    return SMD_OK;
+}
+
+// With a workspace, the spread kernel takes rows longer than a cluster holds
+// and, for rows longer than one CTA holds, batches whose pieces fill at most
+// two waves (the cluster kernel would leave SMs idle or run a second wave of
+// whole rows).
+bool prefer_spread(int B, int H, int W, int sm_count) {
+    if (H % kTcHeads != 0 || !tcs_fits(B, H, W) || W <= kTcMaxKeys) return false;
+    return W > kTcMaxSplit * kTcMaxKeys || tcs_items_cap(B, H, W) <= 2 * sm_count;
+}
+
 struct AnyConfig {
     int kernel;
     MmaConfig mma;
     TcConfig tc;
+    TcsConfig tcs;
 };
 
-int make_plan(int B, int H, int W, const smd_plan_t* force, smd_plan_t* out, AnyConfig* cfg) {
+// ws_bytes: >= 0 when the caller passes a workspace (its size is checked by
+// the caller of make_plan), -1 when there is none.
+int make_plan(int B, int H, int W, const smd_plan_t* force, smd_plan_t* out, AnyConfig* cfg,
+              int64_t ws_bytes = -1) {
     if (B < 0 || W < 0 || H <= 0 || H % kHeadsPerTile != 0) return SMD_ERR_SHAPE;
     static std::once_flag once;
     static DeviceInfo info;
     std::call_once(once, [] { info = query_device(); });
     const int sm_count = info.ok ? info.sm_count : 152;
     int kernel = (force && force->kernel) ? force->kernel : SMD_KERNEL_AUTO;
-    if (kernel == SMD_KERNEL_AUTO)
-        kernel = (H % kTcHeads == 0 && tc_fits(H, W)) ? SMD_KERNEL_TC : SMD_KERNEL_MMA;
+    if (kernel == SMD_KERNEL_AUTO) {
+        if (ws_bytes >= 0 && prefer_spread(B, H, W, sm_count))
+            kernel = SMD_KERNEL_TC_SPREAD;
+        else
+            kernel = (H % kTcHeads == 0 && tc_fits(H, W)) ? SMD_KERNEL_TC : SMD_KERNEL_MMA;
+    }
     cfg->kernel = kernel;
     if (kernel == SMD_KERNEL_MMA) return plan_mma(B, H, W, sm_count, force, out, &cfg->mma);
     if (kernel == SMD_KERNEL_TC) return plan_tc(B, H, W, force, out, &cfg->tc);
+    if (kernel == SMD_KERNEL_TC_SPREAD) return plan_tcs(B, H, W, sm_count, force, out, &cfg->tcs);
     return SMD_ERR_PLAN;
 }
 
@@ -275,6 +348,7 @@ float scale_log2_of(float sm, float qs, float ks) {
 }
 
 int64_t workspace_for(const AnyConfig& cfg) {
+    if (cfg.kernel == SMD_KERNEL_TC_SPREAD) return tcs_workspace(cfg.tcs.items_cap).total;
     return (cfg.kernel == SMD_KERNEL_TC && cfg.tc.split > 1) ? kTcWsBytes : 0;
 }
 
@@ -336,10 +410,17 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
 
     smd_plan_t plan{};
     AnyConfig cfg{};
-    const int rc = make_plan(B, H, W, force, &plan, &cfg);
+    if (workspace != nullptr && !aligned(workspace, 16)) return SMD_ERR_WORKSPACE;
+    const int rc = make_plan(B, H, W, force, &plan, &cfg, workspace != nullptr ? 0 : -1);
     if (rc != SMD_OK) return rc;
-    if (workspace != nullptr) {
-        if (!aligned(workspace, 16) || workspace_bytes < workspace_for(cfg)) return SMD_ERR_WORKSPACE;
+    if (cfg.kernel == SMD_KERNEL_TC_SPREAD) {
+        if (workspace == nullptr || workspace_bytes < workspace_for(cfg)) return SMD_ERR_WORKSPACE;
+        cfg.tcs.ws = workspace;
+    } else if (workspace != nullptr && force != nullptr) {
+        // A forced plan with a workspace: a cluster plan's partials go through
+        // it (L2). The automatic plan keeps the on-chip exchange, which is the
+        // faster one on GB300.
+        if (workspace_bytes < workspace_for(cfg)) return SMD_ERR_WORKSPACE;
         if (workspace_for(cfg) > 0) cfg.tc.ws = static_cast<float*>(workspace);
     } else if (library_scratch && workspace_for(cfg) > 0) {
         // The library's own static scratch: one slot per SM id.
@@ -370,6 +451,8 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
     a.lse = lse;
     a.status = status;
     if (cfg.kernel == SMD_KERNEL_TC) return launch_tc(a, cfg.tc, reinterpret_cast<cudaStream_t>(stream));
+    if (cfg.kernel == SMD_KERNEL_TC_SPREAD)
+        return launch_tcs(a, cfg.tcs, reinterpret_cast<cudaStream_t>(stream));
     return launch_mma(a, cfg.mma, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -417,8 +500,24 @@ int smd_sparse_mla_decode_noalloc(const uint8_t* q, const uint8_t* kv_pool, int6
 int64_t smd_workspace_bytes(int32_t B, int32_t H, int32_t W) {
     smd::AnyConfig cfg{};
     smd_plan_t p{};
-    if (smd::make_plan(B, H, W, nullptr, &p, &cfg) != SMD_OK) return 0;
+    if (smd::make_plan(B, H, W, nullptr, &p, &cfg, 0) != SMD_OK) return 0;
+    return cfg.kernel == SMD_KERNEL_TC_SPREAD ? smd::workspace_for(cfg) : 0;
+}
+
+int64_t smd_workspace_bytes_ex(int32_t B, int32_t H, int32_t W, const smd_plan_t* force) {
+    smd::AnyConfig cfg{};
+    smd_plan_t p{};
+    if (smd::make_plan(B, H, W, force, &p, &cfg, 0) != SMD_OK) return 0;
     return smd::workspace_for(cfg);
+}
+
+int smd_plan_ws(int32_t B, int32_t H, int32_t W, smd_plan_t* plan) {
+    if (!plan) return SMD_ERR_NULL;
+    smd::AnyConfig cfg{};
+    smd_plan_t p{};
+    const int rc = smd::make_plan(B, H, W, nullptr, &p, &cfg, 0);
+    if (rc == SMD_OK) *plan = p;
+    return rc;
 }
 
 int smd_plan(int32_t B, int32_t H, int32_t W, smd_plan_t* plan) {

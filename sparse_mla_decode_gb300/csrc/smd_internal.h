@@ -200,6 +200,57 @@ int launch_tcg(const CallArgs& a, const TcgConfig& cfg, cudaStream_t stream);
 // Dynamic shared memory of the tcgen05 row-group kernel (bytes).
 int tcg_smem_bytes();
 
+// tcgen05 kernel with a row's keys spread over any CTAs of a cooperative grid:
+// a unit (row, 128-head group) of n keys becomes ceil(n / 512) items; maxima
+// and FP32 partials are exchanged through a global workspace.
+constexpr int kTcsMaxUnits = 1024;  // B * ceil(H / 128)
+constexpr int kTcsMaxPieces = 32;   // items per unit: W <= 32 * 512
+
+// Byte offsets of the workspace parts for `items` item slots.
+struct TcsWorkspace {
+    int64_t flag_max;   // [items] u64: the item's maxima are published
+    int64_t flag_part;  // [items][kTcsMaxPieces] u64: its partial for owner j is written
+    int64_t max;        // [items][128] fp32
+    int64_t sum;        // [items][128] fp32
+    int64_t part;       // [items][128 x 512] fp32 partials, 16-byte units head-innermost
+    int64_t total;
+};
+
+__host__ __device__ inline int64_t align_up64(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline TcsWorkspace tcs_workspace(int64_t items) {
+    TcsWorkspace w{};
+    int64_t o = 0;
+    w.flag_max = o;
+    o = align_up64(o + items * 8, 256);
+    w.flag_part = o;
+    o = align_up64(o + items * kTcsMaxPieces * 8, 256);
+    w.max = o;
+    o = align_up64(o + items * 128 * 4, 256);
+    w.sum = o;
+    o = align_up64(o + items * 128 * 4, 256);
+    w.part = o;
+    o = align_up64(o + items * 128 * kLatent * 4, 256);
+    w.total = o;
+    return w;
+}
+
+struct TcsConfig {
+    int grid;       // CTAs (at most the resident CTAs of the device)
+    int items_cap;  // item slots in the workspace: units * ceil(W / 512)
+    uint64_t wait_budget_ns;
+    int inject_stall;
+    void* ws;
+};
+
+int launch_tcs(const CallArgs& a, const TcsConfig& cfg, cudaStream_t stream);
+
+// Dynamic shared memory of the spread kernel (bytes).
+int tcs_smem_bytes();
+
+// CTAs of the spread kernel the current device holds at once (0 on failure).
+int tcs_max_grid();
+
 // SM-id slots of the library's own static exchange scratch (GB300: 152 SMs).
 constexpr int kStaticScratchSlots = 160;
 

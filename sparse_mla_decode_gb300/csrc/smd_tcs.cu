@@ -1,0 +1,706 @@
+// Sparse MLA decode on the tcgen05 tensor cores with a row's keys spread over
+// any CTAs of the grid (not one cluster): the split-KV pattern of the
+// attn_sparse page's SparseDcpDecode carried across clusters, with the FP32
+// partials and the per-row counter in global memory as the page's P3 split
+// variant does (its "cross-cluster merge through a global workspace").
+//
+// Work items. A unit is (query row b, group of 128 heads); a unit whose row
+// holds n > 0 keys (n = clamp(counts[b], 0, W)) becomes s = ceil(n / 512)
+// items of at most 512 keys each (piece j takes [j * per, j * per + per)
+// clamped to n, per = ceil(n / s); the attn_sparse page's count-balanced
+// partition). Every CTA reads the counts and lays the items out the same way:
+// a prefix sum over units numbers them, and item i runs on CTA i % grid in
+// round i / grid. The grid is launched cooperatively (every CTA resident), so
+// a CTA that waits for a peer item of its unit always waits for a CTA that is
+// running: the peer's earlier rounds never wait on later items.
+//
+// Per item the pipeline is the tcgen05 kernel's (TMA tile::gather4 of 128-key
+// chunks into a two-slot ring, S = Q K^T into TMEM, P in E4M3 straight into
+// the swizzled operand layout, O = P V into TMEM). The row maximum and the
+// partials go through global memory (L2):
+//   1. each item publishes its 128 maxima and raises its "max" flag; it waits
+//      for the unit's other items' flags and takes the maximum over them;
+//   2. after PV it writes its FP32 partials of the other items' columns
+//      (owner j of s owns columns [16 floor(32 j / s), 16 floor(32 (j+1) / s)))
+//      and its sums, and raises one flag per owner;
+//   3. each owner waits for its flags, merges its own partial first and then
+//      the others in item order, and writes BF16 out (and LSE, owner 0).
+// A flag holds the call's 64-bit token, so stale words from earlier calls
+// never pass; the reader of a flag zeroes it once it is consumed.
+// Every wait (copies, tensor core, peer flags) is bounded.
+#include <cuda.h>
+
+#include <atomic>
+#include <chrono>
+#include <cmath>
+#include <cstdint>
+
+#include "smd.h"
+#include "smd_internal.h"
+#include "smd_ptx.cuh"
+#include "smd_tc_common.cuh"
+
+namespace smd {
+namespace {
+
+using tcc::kBlock;
+using tcc::kTile;
+
+constexpr int kOffQP = 0;                                 // query tile, later the P tiles
+constexpr int kOffRing = kTile;                           // two chunk slots; the output stage after PV
+constexpr int kOffPrefix = 3 * kTile;                     // [units + 1] first item of each unit
+constexpr int kOffRowMax = kOffPrefix + (kTcsMaxUnits + 1) * 4 + 12;  // [128]
+constexpr int kOffLsum = kOffRowMax + 128 * 4;            // [4][128] sums of P per 32-key group
+constexpr int kOffIdx = kOffLsum + 4 * 128 * 4;           // [512] this item's key indices
+constexpr int kOffWarpSum = kOffIdx + kTcMaxKeys * 4;     // [16] block scan
+constexpr int kOffBars = kOffWarpSum + 16 * 4;
+constexpr int kNumBars = 13;
+constexpr int kOffTmem = kOffBars + 8 * kNumBars;
+constexpr int kSmemUsed = kOffTmem + 16;
+constexpr int kSmemBytes = kSmemUsed + 1024;  // + alignment of the dynamic base to 1 KB
+static_assert(kOffRowMax % 16 == 0 && kOffBars % 8 == 0, "layout alignment");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+
+constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = 3, kBarFreeB = 5, kBarS = 7, kBarP = 11,
+              kBarO = 12;
+
+constexpr int kProducerThreads = 256;
+
+struct TcsMaps {
+    CUtensorMap q, q_tail, kv, kv_tail;
+};
+
+struct TcsParams {
+    CallArgs a;
+    int32_t HG;      // head groups per row (ceil(H / 128))
+    int32_t lanes;   // heads a CTA computes (min(H, 128)); the other TMEM lanes are padding
+    int32_t units;   // B * HG
+    int32_t grid;    // CTAs
+    float log2_448;
+    uint64_t budget_ns;
+    int32_t inject_stall;
+    uint64_t token;  // this call's flag value (never 0)
+    TcsWorkspace ws;
+    uint8_t* ws_base;
+};
+
+struct Item {
+    int b, g, s, j, item0;  // row, head group, items of the unit, this piece, the unit's first item
+    int first, mine, nch;   // keys of this piece
+};
+
+__device__ __forceinline__ float4 ld_cg_v4(const float* p) {
+    float4 v;
+    asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float ld_cg_f32(const float* p) {
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(float* p, float4 v) {
+    asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits (bounded) until *flag holds the call's token; on expiry the status
+// gets SMD_ERR_TIMEOUT and ok is cleared.
+__device__ __forceinline__ void wait_flag(const uint64_t* flag, uint64_t token, bool& ok,
+                                          int32_t* status, uint64_t budget_ns) {
+    if (ld_acquire_u64(flag) == token) return;
+    const uint64_t t0 = globaltimer();
+    while (ld_acquire_u64(flag) != token) {
+        if (globaltimer() - t0 > budget_ns) {
+            if (status != nullptr) atomicCAS(status, 0, kStatusTimeout);
+            ok = false;
+            return;
+        }
+    }
+}
+
+// First column of owner j's slice when a unit has s items (a multiple of 16).
+__device__ __forceinline__ int slice_begin(int j, int s) { return 16 * ((32 * j) / s); }
+
+__device__ __forceinline__ int clamped_count(const TcsParams& p, int b) {
+    return max(min(p.a.counts[b], p.a.W), 0);
+}
+
+__device__ __forceinline__ int pieces_of(int n) { return (n + kTcMaxKeys - 1) / kTcMaxKeys; }
+
+// The shared-memory addresses and barriers of the chunk pipeline.
+__device__ __forceinline__ tcc::Pipe pipe_of(const TcsParams& p, uint32_t base, uint32_t bars,
+                                             const uint8_t* smem) {
+    tcc::Pipe pp;
+    pp.q = base + kOffQP;
+    pp.ring = base + kOffRing;
+    pp.full = bars + 8 * kBarFull;
+    pp.empty = bars + 8 * kBarEmpty;
+    pp.free_b = bars + 8 * kBarFreeB;
+    pp.s = bars + 8 * kBarS;
+    pp.bar_q = bars + 8 * kBarQ;
+    pp.bar_p = bars + 8 * kBarP;
+    pp.bar_o = bars + 8 * kBarO;
+    pp.idx = reinterpret_cast<const int32_t*>(smem + kOffIdx);
+    pp.status = p.a.status;
+    pp.budget_ns = p.budget_ns;
+    return pp;
+}
+
+// ---- setup: the item layout ----------------------------------------------------------
+// pre[u] = first item of unit u (exclusive prefix sum of the units' item
+// counts), pre[units] = all items. Two units per thread (units <= 1024).
+__device__ __forceinline__ void scan_units(const TcsParams& p, uint8_t* smem) {
+    int32_t* pre = reinterpret_cast<int32_t*>(smem + kOffPrefix);
+    int32_t* wsum = reinterpret_cast<int32_t*>(smem + kOffWarpSum);
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int u0 = 2 * t, u1 = 2 * t + 1;
+    const int s0 = u0 < p.units ? pieces_of(clamped_count(p, u0 / p.HG)) : 0;
+    const int s1 = u1 < p.units ? pieces_of(clamped_count(p, u1 / p.HG)) : 0;
+    const int v = s0 + s1;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < kTcThreads / 32 ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < kTcThreads / 32) wsum[lane] = w;
+    }
+    __syncthreads();
+    const int excl = x - v + (warp > 0 ? wsum[warp - 1] : 0);
+    if (u0 < p.units) pre[u0] = excl;
+    if (u1 < p.units) pre[u1] = excl + s0;
+    if (t == 0) pre[p.units] = wsum[kTcThreads / 32 - 1];
+    __syncthreads();
+}
+
+// Item i (< all items): its unit (binary search over pre) and keys.
+__device__ __forceinline__ Item item_of(const TcsParams& p, const uint8_t* smem, int i) {
+    const int32_t* pre = reinterpret_cast<const int32_t*>(smem + kOffPrefix);
+    int lo = 0, hi = p.units - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pre[mid] <= i)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    Item it;
+    it.b = lo / p.HG;
+    it.g = lo - it.b * p.HG;
+    it.item0 = pre[lo];
+    it.s = pre[lo + 1] - pre[lo];
+    it.j = i - it.item0;
+    const int n = clamped_count(p, it.b);
+    const int per = (n + it.s - 1) / it.s;
+    it.first = min(n, it.j * per);
+    it.mine = min(n - it.first, per);
+    it.nch = (it.mine + kTcChunk - 1) / kTcChunk;
+    return it;
+}
+
+// Units without keys assigned to this CTA (unit u on CTA u % grid): zero
+// output and LSE -inf. Run by `nthreads` threads starting at thread t0.
+__device__ __forceinline__ void zero_empty_units(const TcsParams& p, const uint8_t* smem, int t0,
+                                                 int nthreads) {
+    const int32_t* pre = reinterpret_cast<const int32_t*>(smem + kOffPrefix);
+    const int t = threadIdx.x - t0;
+    for (int u = blockIdx.x; u < p.units; u += p.grid) {
+        if (pre[u + 1] != pre[u]) continue;
+        const int b = u / p.HG, g = u - b * p.HG;
+        const int64_t row0 = static_cast<int64_t>(b) * p.a.H + g * kTcHeads;
+        uint4* dst = reinterpret_cast<uint4*>(p.a.out + row0 * kLatent);
+        for (int e = t; e < p.lanes * (kLatent / 8); e += nthreads) dst[e] = make_uint4(0u, 0u, 0u, 0u);
+        for (int h = t; h < p.lanes; h += nthreads) p.a.lse[row0 + h] = -INFINITY;
+    }
+}
+
+// (Re)initialises the pipeline barriers (thread 0). Before the second and
+// later items every barrier is idle: all copies have landed and every MMA
+// has completed (O is complete).
+__device__ __forceinline__ void init_bars(uint32_t bars, bool again) {
+    if (again)
+        for (int i = 0; i < kNumBars; ++i)
+            asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bars + 8 * i) : "memory");
+    mbar_init(bars + 8 * kBarQ, 1);
+    for (int i = 0; i < 2; ++i) {
+        mbar_init(bars + 8 * (kBarFull + i), 1);
+        mbar_init(bars + 8 * (kBarEmpty + i), 1);
+        mbar_init(bars + 8 * (kBarFreeB + i), 1);
+    }
+    for (int c = 0; c < 4; ++c) mbar_init(bars + 8 * (kBarS + c), 1);
+    mbar_init(bars + 8 * kBarP, kTcThreads);
+    mbar_init(bars + 8 * kBarO, 1);
+    fence_mbar_init();
+}
+
+// ---- warps 0-7: this item's key indices, then pass A's gathers -------------------
+// Entries past its keys name pool row 0 (a real row: finite bytes; its P is 0).
+// This item's key indices, two per producer thread (entries past its keys: 0).
+__device__ __forceinline__ void load_idx(const TcsParams& p, const Item& it, int32_t (&v)[2]) {
+    const int32_t* row_idx = p.a.indices + static_cast<int64_t>(it.b) * p.a.W + it.first;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+        const int i = threadIdx.x + u * kProducerThreads;
+        v[u] = (i < it.mine) ? row_idx[i] : 0;
+    }
+}
+
+// `pre` holds this item's indices when `have` (loaded early for the first item).
+__device__ __forceinline__ void producer_a(const TcsMaps& maps, const TcsParams& p,
+                                           const tcc::Pipe& pp, uint8_t* smem, const Item& it,
+                                           const int32_t (&pre)[2], bool have, bool& ok) {
+    const int t = threadIdx.x;
+    int32_t* idx_s = reinterpret_cast<int32_t*>(smem + kOffIdx);
+    int32_t v[2] = {pre[0], pre[1]};
+    if (!have) load_idx(p, it, v);
+    idx_s[t] = v[0];
+    idx_s[t + kProducerThreads] = v[1];
+    asm volatile("bar.sync 1, %0;" ::"r"(kProducerThreads) : "memory");
+    uint32_t seen[2] = {0u, 0u};
+    tcc::gather_pass_a(maps.kv, maps.kv_tail, pp, 0, it.nch, seen, ok);
+}
+
+// ---- warps 12-15: the row maximum (thread h = head h = TMEM lane h) ---------------
+// This item's maximum as the QK chunks complete; for a unit of several items
+// it is published (global memory + the item's flag) and the maximum over the
+// unit's items is taken once every flag is up.
+__device__ __forceinline__ void row_max(const TcsParams& p, uint8_t* smem, uint32_t bars,
+                                        uint32_t tmem, const Item& it, int item, bool& ok) {
+    const int h = threadIdx.x & 127;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * ((threadIdx.x >> 5) & 3)) << 16);
+    const float lam = p.a.scale_log2;
+    float m = -INFINITY;
+    for (int c = 0; c < it.nch; ++c) {
+        mbar_wait(bars + 8 * (kBarS + c), 0, ok, p.a.status, p.budget_ns);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const int cnt = min(kTcChunk, it.mine - kTcChunk * c);
+        for (int q = 0; 32 * q < cnt; ++q) {
+            float v[32];
+            tmem_ld32(lane_base + kTcChunk * c + 32 * q, v);
+            const int lim = cnt - 32 * q;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (j < lim) m = fmaxf(m, lam * v[j]);
+        }
+    }
+    float* rowmax = reinterpret_cast<float*>(smem + kOffRowMax);
+    if (it.s == 1) {
+        rowmax[h] = m;
+        return;
+    }
+    float* ws_max = reinterpret_cast<float*>(p.ws_base + p.ws.max);
+    uint64_t* flag_max = reinterpret_cast<uint64_t*>(p.ws_base + p.ws.flag_max);
+    ws_max[static_cast<int64_t>(item) * kTcHeads + h] = m;  // published even after a failure
+    __threadfence();
+    asm volatile("bar.sync 2, 128;" ::: "memory");
+    if (h == 0) st_release_u64(flag_max + item, p.token);
+    if (h < it.s) wait_flag(flag_max + it.item0 + h, p.token, ok, p.a.status, p.budget_ns);
+    asm volatile("bar.sync 2, 128;" ::: "memory");
+    float mr = -INFINITY;
+    for (int jj = 0; jj < it.s; ++jj)
+        mr = fmaxf(mr, ld_cg_f32(ws_max + static_cast<int64_t>(it.item0 + jj) * kTcHeads + h));
+    rowmax[h] = mr;
+}
+
+// ---- all 16 warps: P ---------------------------------------------------------------
+// Warp w: TMEM lane quarter w % 4 (thread = head h), keys 32j .. 32j + 31 of
+// every chunk, j = w / 4; P = 2^(s - m + log2 448) in E4M3 into the K-major
+// 128-byte-swizzled A operand, and the FP32 sum of the unquantized P of those
+// keys (chunks ascending) into lsum[j][h].
+__device__ __forceinline__ void p_phase(const TcsParams& p, uint8_t* smem, uint32_t bars,
+                                        uint32_t tmem, const Item& it, bool ok) {
+    const int warp = threadIdx.x >> 5;
+    const int h = 32 * (warp & 3) + (threadIdx.x & 31);
+    const int j = warp >> 2;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    const float lam = p.a.scale_log2;
+    const float bias = reinterpret_cast<const float*>(smem + kOffRowMax)[h] - p.log2_448;
+    float l = 0.f;
+    for (int c = 0; c < it.nch && ok; ++c) {
+        const int lim = min(kTcChunk, it.mine - kTcChunk * c) - 32 * j;
+        if (lim <= 0) continue;  // warp-uniform
+        uint8_t* row = smem + kOffQP + c * kBlock + (h >> 3) * 1024 + (h & 7) * 128;
+        float v[32];
+        tmem_ld32(lane_base + kTcChunk * c + 32 * j, v);
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float pr[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int k = 4 * i + e;
+                pr[e] = (k < lim) ? ex2_approx(lam * v[k] - bias) : 0.f;
+                l += pr[e];
+            }
+            w[i] = static_cast<uint32_t>(e4m3x2(pr[0], pr[1])) |
+                   (static_cast<uint32_t>(e4m3x2(pr[2], pr[3])) << 16);
+        }
+        *reinterpret_cast<uint4*>(row + (((2 * j) ^ (h & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(row + (((2 * j + 1) ^ (h & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    reinterpret_cast<float*>(smem + kOffLsum)[j * 128 + h] = l;
+    fence_proxy_async();  // P (generic stores) -> the tensor core's reads
+    tc_fence_before();    // every logit read is complete
+    mbar_arrive_local(bars + 8 * kBarP);
+}
+
+// BF16(v * inv) of 16 columns of head h at column `col` of the staging tile
+// (rows of row_bytes; 16-byte chunk c of row h at chunk c ^ (h & mask)).
+__device__ __forceinline__ void stage16(uint8_t* stage, int row_bytes, int mask, int h, int col,
+                                        const float (&v)[16], float inv) {
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = bf16x2(v[2 * i] * inv, v[2 * i + 1] * inv);
+    uint8_t* row = stage + h * row_bytes;
+    const int c0 = col >> 3;
+    *reinterpret_cast<uint4*>(row + ((c0 ^ (h & mask)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ (h & mask)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// The first `rows` heads of the staging tile to out (rows kLatent BF16 apart),
+// whole rows per warp-wide store. The caller syncs before.
+__device__ __forceinline__ void flush(const uint8_t* stage, int row_bytes, int mask, int rows,
+                                      uint16_t* dst) {
+    const int chunks = row_bytes >> 4;
+    for (int e = threadIdx.x; e < rows * chunks; e += kTcThreads) {
+        const int r = e / chunks, c = e - r * chunks;
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + r * row_bytes + ((c ^ (r & mask)) << 4));
+        *reinterpret_cast<uint4*>(dst + static_cast<int64_t>(r) * kLatent + c * 8) = v;
+    }
+}
+
+// XOR mask of the staging swizzle for rows of `chunks` 16-byte chunks: the
+// largest power of two (at most 8) that divides chunks, minus one.
+__device__ __forceinline__ int stage_mask(int chunks) { return min(chunks & -chunks, 8) - 1; }
+
+// Partner k (1 <= k < s) of piece j in the merge order: j ^ k when s is a
+// power of two (the order of the cluster kernels), else (j + k) % s.
+__device__ __forceinline__ int partner(int j, int k, int s) {
+    return (s & (s - 1)) == 0 ? (j ^ k) : (j + k) % s;
+}
+
+// ---- all 16 warps: exchange, merge, output ---------------------------------------
+// Warp w serves TMEM lane quarter w % 4 (thread = head h) and column group
+// cg = w / 4.
+__device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32_t tmem,
+                                       const Item& it, int item, bool& ok) {
+    const int warp = threadIdx.x >> 5;
+    const int h = 32 * (warp & 3) + (threadIdx.x & 31);
+    const int cg = warp >> 2;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    const float* lsum = reinterpret_cast<const float*>(smem + kOffLsum);
+    const float l = ((lsum[h] + lsum[128 + h]) + lsum[256 + h]) + lsum[384 + h];
+    const float m = reinterpret_cast<const float*>(smem + kOffRowMax)[h];
+    const bool have_o = ok && it.mine > 0;  // O in TMEM is defined only if PV ran
+    const int64_t row0 = static_cast<int64_t>(it.b) * p.a.H + it.g * kTcHeads;
+    uint16_t* oblock = p.a.out + row0 * kLatent;
+    float* lse = p.a.lse + row0 + h;
+    uint8_t* stage = smem + kOffRing;  // the ring is dead once O is complete
+
+    if (it.s == 1) {
+        if (ok) {  // uniform: set by the barrier before the finish
+            const float total = 0.f + l;
+            const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
+            for (int q = 0; q < 8; ++q) {
+                const int col = cg * 128 + 16 * q;
+                float v[16];
+                if (have_o) {
+                    tmem_ld16(lane_base + col, v);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) v[i] = 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = 0.f + v[i];
+                stage16(stage, kLatent * 2, 7, h, col, v, inv);
+            }
+            if (cg == 0 && h < p.lanes)
+                *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f
+                                   : -INFINITY;
+            __syncthreads();
+            flush(stage, kLatent * 2, 7, p.lanes, oblock);
+        }
+        return;
+    }
+
+    const int s = it.s, j = it.j;
+    const int c0 = slice_begin(j, s), c1 = slice_begin(j + 1, s), CW = c1 - c0;
+    constexpr int64_t kPartFloats = static_cast<int64_t>(kTcHeads) * kLatent;
+    float* part = reinterpret_cast<float*>(p.ws_base + p.ws.part);
+    float* sums = reinterpret_cast<float*>(p.ws_base + p.ws.sum);
+    uint64_t* fpart = reinterpret_cast<uint64_t*>(p.ws_base + p.ws.flag_part);
+    uint64_t* fmax = reinterpret_cast<uint64_t*>(p.ws_base + p.ws.flag_max);
+
+    // 1. This item's partials of the other owners' columns (16-byte unit u of
+    // head h at (u * 128 + h): one warp-wide store covers 512 contiguous bytes),
+    // and its sums; then one flag per owner. (Every SM exchanges at once here,
+    // so the phase is bound by L2 bandwidth; all 16 warps write.)
+    float* mine_part = part + static_cast<int64_t>(item) * kPartFloats;
+    for (int q = 0; q < 8; ++q) {
+        const int col = 128 * cg + 16 * q;
+        if (col >= c0 && col < c1) continue;  // warp-uniform: the own slice
+        float v[16];
+        if (have_o) {
+            tmem_ld16(lane_base + col, v);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        }
+        float* dst = mine_part + ((col >> 2) * kTcHeads + h) * 4;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            st_v4(dst + i * kTcHeads * 4, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+    }
+    if (cg == 0) sums[static_cast<int64_t>(item) * kTcHeads + h] = l;
+    __syncthreads();
+    const int t = threadIdx.x;
+    if (t < s && t != j) {
+        __threadfence();  // after the barrier: orders every thread's stores above
+        st_release_u64(fpart + static_cast<int64_t>(item) * kTcsMaxPieces + t, p.token);
+    }
+
+    // 2. The other items' partials of this slice (each flag is read here only,
+    // so it is zeroed once seen).
+    if (t < s && t != j) {
+        uint64_t* f = fpart + static_cast<int64_t>(it.item0 + t) * kTcsMaxPieces + j;
+        wait_flag(f, p.token, ok, p.a.status, p.budget_ns);
+        *f = 0ull;
+    }
+    ok = __syncthreads_and(ok) != 0;
+    // Every item of the unit has read the maxima (it raised its flags for the
+    // owners after that): this item's max flag is consumed.
+    if (t == 0) fmax[item] = 0ull;
+    if (!ok) return;
+
+    // 3. Merge: this item's partial, then its partners in the fixed order.
+    float total = 0.f + l;
+    for (int k = 1; k < s; ++k)
+        total += ld_cg_f32(sums + static_cast<int64_t>(it.item0 + partner(j, k, s)) * kTcHeads + h);
+    const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
+    const int mask = stage_mask(CW / 8);
+    for (int q = cg; 16 * q < CW; q += 4) {
+        const int col = c0 + 16 * q;
+        float acc[16];
+        if (have_o) {
+            tmem_ld16(lane_base + col, acc);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f + acc[i];
+        for (int k = 1; k < s; ++k) {
+            const float* src = part + static_cast<int64_t>(it.item0 + partner(j, k, s)) * kPartFloats +
+                               ((col >> 2) * kTcHeads + h) * 4;
+            float4 x[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) x[i] = ld_cg_v4(src + i * kTcHeads * 4);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[4 * i] += x[i].x;
+                acc[4 * i + 1] += x[i].y;
+                acc[4 * i + 2] += x[i].z;
+                acc[4 * i + 3] += x[i].w;
+            }
+        }
+        stage16(stage, CW * 2, mask, h, col - c0, acc, inv);
+    }
+    if (j == 0 && cg == 0 && h < p.lanes)
+        *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f : -INFINITY;
+    __syncthreads();
+    flush(stage, CW * 2, mask, p.lanes, oblock + c0);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tcs_decode_kernel(const __grid_constant__ TcsMaps maps, const TcsParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const uint32_t base = smem_addr(smem);
+    const uint32_t bars = base + kOffBars;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    bool ok = true;
+
+    scan_units(p, smem);
+    const int total = reinterpret_cast<const int32_t*>(smem + kOffPrefix)[p.units];
+    // The first item's indices are loaded now: their round trip overlaps the setup.
+    int32_t idx0[2] = {0, 0};
+    if (warp < 8 && static_cast<int>(blockIdx.x) < total)
+        load_idx(p, item_of(p, smem, blockIdx.x), idx0);
+    if (threadIdx.x == 0) init_bars(bars, false);
+    if (warp == 8) tmem_alloc(base + kOffTmem, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + kOffTmem);
+    const tcc::Pipe pp = pipe_of(p, base, bars, smem);
+    // Warps 9-11 have nothing to do until P: the empty units go now.
+    if (warp >= 9 && warp < 12) zero_empty_units(p, smem, 9 * 32, 3 * 32);
+
+    for (int r = 0;; ++r) {
+        const int item = blockIdx.x + r * p.grid;
+        if (item >= total) break;  // uniform
+        const Item it = item_of(p, smem, item);
+        if (r > 0) {
+            if (threadIdx.x == 0) init_bars(bars, true);
+            __syncthreads();
+        }
+        if (threadIdx.x == 0) {
+            // (inject_stall: the query barrier also expects 16 bytes nobody
+            // sends, so its bounded wait runs out; a test hook.)
+            mbar_arrive_expect_tx(bars + 8 * kBarQ, kTile + (p.inject_stall ? 16 : 0));
+            const int y = it.b * p.a.H + it.g * kTcHeads;
+            for (int c = 0; c < 4; ++c)
+                tma_load_2d(base + kOffQP + c * kBlock, &maps.q, 128 * c, y, bars + 8 * kBarQ);
+            tma_load_2d(base + kOffQP + 4 * kBlock, &maps.q_tail, 512, y, bars + 8 * kBarQ);
+        }
+        uint32_t full_seen[2] = {0u, 0u};
+        if (warp < 8) {
+            producer_a(maps, p, pp, smem, it, idx0, r == 0, ok);
+        } else if (warp == 8) {
+            if (lane == 0) tcc::mma_qk(pp, tmem, it.nch, full_seen, ok);
+            __syncwarp();
+        } else if (warp >= 12) {
+            row_max(p, smem, bars, tmem, it, item, ok);
+        }
+        ok = __syncthreads_and(ok) != 0;  // every QK is complete; the row maxima are here
+        tc_fence_after();
+        p_phase(p, smem, bars, tmem, it, ok);
+        if (warp < 8) {
+            tcc::gather_pass_b(maps.kv, pp, it.nch, ok);
+        } else if (warp == 8) {
+            if (lane == 0) tcc::mma_pv(pp, tmem, it.nch, it.mine, full_seen, ok);
+            __syncwarp();
+        }
+        mbar_wait(bars + 8 * kBarO, 0, ok, p.a.status, p.budget_ns);
+        tc_fence_after();
+        ok = __syncthreads_and(ok) != 0;  // the partial sums of P are visible; one verdict
+        finish(p, smem, tmem, it, item, ok);
+        tc_fence_before();  // every TMEM read of this item precedes the next item's MMAs
+        __syncthreads();
+    }
+    if (warp == 8) {
+        tc_fence_after();
+        tmem_free(tmem, 512);
+    }
+}
+
+}  // namespace
+
+// ---- host ------------------------------------------------------------------------
+
+int tcs_smem_bytes() { return kSmemBytes; }
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+// A flag token for each call: a counter run through a 64-bit mixer (splitmix64)
+// from a per-process seed, so that words left by another process or an
+// earlier call that stopped early do not match; never 0.
+uint64_t next_token() {
+    static std::atomic<uint64_t> counter{0};
+    static const uint64_t seed = [] {
+        uint64_t x = reinterpret_cast<uintptr_t>(&counter);
+        x ^= static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count());
+        return x;
+    }();
+    uint64_t z = seed + 0x9E3779B97F4A7C15ull * (counter.fetch_add(1) + 1);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    return z == 0 ? 1 : z;
+}
+
+}  // namespace
+
+int tcs_max_grid() {
+    static std::atomic<int> cached[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    int v = cached[dev].load();
+    if (v > 0) return v;
+    if (cudaFuncSetAttribute(tcs_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tcs_decode_kernel, kTcThreads,
+                                                      kSmemBytes) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    v = per_sm * sms;
+    cached[dev].store(v);
+    return v;
+}
+
+int launch_tcs(const CallArgs& a, const TcsConfig& cfg, cudaStream_t stream) {
+    TcsMaps maps;
+    const uint64_t qrows = static_cast<uint64_t>(a.B) * static_cast<uint64_t>(a.H);
+    if (!encode_row_map(&maps.q, a.q, qrows, 128, kTcHeads) ||
+        !encode_row_map(&maps.q_tail, a.q, qrows, 64, kTcHeads) ||
+        !encode_row_map(&maps.kv, a.kv, static_cast<uint64_t>(a.N), 128, 1) ||
+        !encode_row_map(&maps.kv_tail, a.kv, static_cast<uint64_t>(a.N), 64, 1))
+        return SMD_ERR_LAUNCH;
+    const int max_grid = tcs_max_grid();
+    if (max_grid <= 0 || cfg.grid > max_grid) return SMD_ERR_LAUNCH;
+    TcsParams prm{};
+    prm.a = a;
+    prm.HG = (a.H + kTcHeads - 1) / kTcHeads;
+    prm.lanes = a.H < kTcHeads ? a.H : kTcHeads;
+    prm.units = a.B * prm.HG;
+    prm.grid = cfg.grid;
+    prm.log2_448 = static_cast<float>(std::log2(448.0));
+    prm.budget_ns = cfg.wait_budget_ns;
+    prm.inject_stall = cfg.inject_stall;
+    prm.token = next_token();
+    prm.ws = tcs_workspace(cfg.items_cap);
+    prm.ws_base = static_cast<uint8_t*>(cfg.ws);
+
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(static_cast<unsigned>(cfg.grid), 1, 1);
+    lc.blockDim = dim3(kTcThreads, 1, 1);
+    lc.dynamicSmemBytes = static_cast<size_t>(kSmemBytes);
+    lc.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident: peers' waits end
+    attr[0].val.cooperative = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    if (cudaLaunchKernelEx(&lc, tcs_decode_kernel, maps, prm) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SMD_ERR_LAUNCH;
+    }
+    return SMD_OK;
+}
+
+}  // namespace smd

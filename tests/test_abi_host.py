@@ -159,11 +159,20 @@ def test_invalid_tc_plans_are_rejected(H, W, force):
 
 
 def test_workspace_size_and_checks():
-    # tcgen05 plans with a split use the L2 exchange workspace; others need none
-    assert smd.smd_workspace_bytes(256, 128, 2048) >= 3 * 128 * 128 * 4 * 152
-    assert smd.smd_workspace_bytes(5, 128, 300) == 0       # split 1: no exchange
+    # The automatic plan takes a workspace only for the spread kernel: rows
+    # of several pieces whose pieces fill at most two waves, or rows longer
+    # than a cluster holds; one slot of ~257 KiB per possible piece.
+    assert smd.smd_workspace_bytes(64, 128, 2048) >= 64 * 4 * 128 * 512 * 4
+    assert smd.smd_workspace_bytes(2, 128, 8192) >= 2 * 16 * 128 * 512 * 4
+    assert smd.smd_workspace_bytes(256, 128, 2048) == 0    # four waves: the cluster kernel
+    assert smd.smd_workspace_bytes(5, 128, 300) == 0       # one piece per row: no exchange
     assert smd.smd_workspace_bytes(5, 64, 256) == 0        # warp-MMA kernel: on-chip merge
+    # a forced cluster plan with a split can exchange through L2: one slot per SM id
+    p = smd.SmdPlan()
+    p.kernel = smd.SMD_KERNEL_TC
+    assert smd.smd_workspace_bytes_ex(256, 128, 2048, p) >= 3 * 128 * 128 * 4 * 152
     need = smd.smd_workspace_bytes(2, 128, 2048)
+    assert need > 0
     args = (A, A, 100, A, 2048, A, 2, 128, 0.1, 0.1, 0.1, A, A, 0)
     assert smd.smd_sparse_mla_decode_ws(*args, A, need - 16, 0) == smd.SMD_ERR_WORKSPACE
     assert smd.smd_sparse_mla_decode_ws(*args, A + 8, need, 0) == smd.SMD_ERR_WORKSPACE

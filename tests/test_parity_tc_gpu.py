@@ -30,7 +30,7 @@ SHAPES = [
 def workspace(cuda):
     import torch
     from sparse_mla_decode_gb300 import binding
-    nbytes = binding.smd_workspace_bytes(256, 128, 2048)
+    nbytes = binding.smd_workspace_bytes_ex(256, 128, 2048, dict(kernel=2))
     return torch.empty(nbytes // 4, dtype=torch.float32, device=cuda)
 
 
@@ -54,7 +54,7 @@ def test_tc_l2_exchange_over_many_waves(cuda, workspace):
     """800 CTAs on 152 SMs: workspace slots are reused wave after wave."""
     case = inputs.random_case(320, B=200, H=128, W=2048, N=50000, heavy_frac=0.01)
     t = to_dev(case, cuda)
-    out_w, lse_w = gpu_decode(case, cuda, tensors=t, workspace=workspace)
+    out_w, lse_w = gpu_decode(case, cuda, dict(kernel=TC), tensors=t, workspace=workspace)
     out_g, lse_g = gpu_decode(case, cuda, tensors=t)
     assert np.array_equal(out_w, out_g)
     assert np.array_equal(lse_w.view(np.uint32), lse_g.view(np.uint32))

@@ -1,0 +1,154 @@
+"""GPU parity of the spread tcgen05 kernel (SMD_KERNEL_TC_SPREAD): a row's
+keys in pieces of at most 512 over any CTAs of a cooperative grid, maxima
+and partials through the caller's workspace. Checked against the CPU oracle,
+bit for bit against the cluster kernel where both split a row the same way,
+bit for bit across grid sizes (rounds and units that straddle two rounds),
+on rows longer than a cluster holds, with a workspace full of garbage and
+reused, and through the timeout path."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+from sparse_mla_decode_gb300 import inputs
+from test_parity_gpu import check, oracle_decode, to_dev
+
+pytestmark = pytest.mark.gpu
+
+SPREAD = 5
+TC = 2
+
+
+def workspace_for(case, dev, fill=None):
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    # the spread plan's size, also where the automatic plan would not take it
+    n = binding.smd_workspace_bytes_ex(case.B, case.H, case.W, dict(kernel=SPREAD))
+    assert n > 0
+    if fill is None:
+        return torch.zeros(n, dtype=torch.uint8, device=dev)
+    g = torch.Generator(device=dev).manual_seed(fill)
+    return torch.randint(0, 256, (n,), dtype=torch.uint8, device=dev, generator=g)
+
+
+def spread(case, dev, tensors=None, ws=None, plan=None, expect_status=0):
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    q, kv, idx, cnt = tensors if tensors is not None else to_dev(case, dev)
+    ws = workspace_for(case, dev) if ws is None else ws
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    force = dict(kernel=SPREAD)
+    force.update(plan or {})
+    out, lse = binding.sparse_mla_decode(q, kv, idx, cnt, case.sm_scale, case.q_scale,
+                                         case.k_scale, status=status, plan=force, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == expect_status, binding.smd_status_str(int(status.item()))
+    return out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy()
+
+
+SHAPES = [
+    # (B, H, W, N, counts): one piece, several, ragged piece boundaries, empty
+    # rows, more than a cluster holds (W > 2048), H < 128 and H = 256.
+    (4, 128, 2048, 20000, [2048, 1, 0, 1537]),
+    (3, 128, 1100, 9000, [513, 1024, 1100]),
+    (2, 128, 9000, 40000, [9000, 6001]),
+    (3, 64, 1500, 8000, [1500, 700, 0]),
+    (2, 256, 700, 5000, [700, 512]),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"B{s[0]}H{s[1]}W{s[2]}" for s in SHAPES])
+def test_spread_matches_the_oracle(cuda, shape):
+    B, H, W, N, counts = shape
+    case = inputs.random_case(B * 13 + W, B=B, H=H, W=W, N=N, counts=counts, heavy_frac=0.02)
+    out_g, lse_g = spread(case, cuda)
+    out_o, lse_o = oracle_decode(case)
+    check(out_g, lse_g, out_o, lse_o, f"spread {shape}")
+
+
+@pytest.mark.parametrize("W", [1024, 2048])
+def test_spread_is_the_cluster_kernel_where_they_split_alike(cuda, W):
+    """Full rows: the cluster kernel's split (W / 512) is every row's piece
+    count, so both sum the same keys in the same order: identical bits."""
+    case = inputs.random_case(70 + W, B=5, H=128, W=W, N=30000, counts=[W] * 5)
+    t = to_dev(case, cuda)
+    from test_parity_gpu import gpu_decode
+    out_c, lse_c = gpu_decode(case, cuda, plan=dict(kernel=TC), tensors=t)
+    out_s, lse_s = spread(case, cuda, tensors=t)
+    assert np.array_equal(out_s, out_c)
+    assert np.array_equal(lse_s.view(np.uint32), lse_c.view(np.uint32))
+
+
+def test_spread_grid_changes_no_bits(cuda):
+    """The grid only lays pieces out: with 5 CTAs most rows straddle two
+    rounds; identical bits on every grid."""
+    rng = np.random.default_rng(71)
+    counts = rng.integers(0, 2049, size=24).tolist()
+    counts[3] = 0
+    counts[4] = 2048
+    case = inputs.random_case(71, B=24, H=128, W=2048, N=60000, counts=counts)
+    t = to_dev(case, cuda)
+    ref = spread(case, cuda, tensors=t)
+    for grid in (4, 5, 17, 152):
+        out, lse = spread(case, cuda, tensors=t, plan=dict(grid_x=grid))
+        assert np.array_equal(out, ref[0]), grid
+        assert np.array_equal(lse.view(np.uint32), ref[1].view(np.uint32)), grid
+    rows = [0, 3, 4, 11, 23]
+    out_o, lse_o = oracle_decode(case, rows)
+    check(ref[0][rows], ref[1][rows], out_o, lse_o, "spread grid")
+
+
+def test_spread_longest_rows(cuda):
+    """32 pieces of 512 keys: the longest row the spread kernel takes."""
+    case = inputs.random_case(72, B=1, H=128, W=16384, N=70000, counts=[16384])
+    out_g, lse_g = spread(case, cuda)
+    out_o, lse_o = oracle_decode(case)
+    check(out_g, lse_g, out_o, lse_o, "spread 16384")
+
+
+def test_spread_workspace_garbage_and_reuse(cuda):
+    """The workspace needs no initialisation, and every call leaves its flags
+    consumed: random bytes first, then the same workspace twice more."""
+    case = inputs.random_case(73, B=6, H=128, W=2048, N=30000, counts=[2048, 900, 1, 0, 1600, 513])
+    t = to_dev(case, cuda)
+    ws = workspace_for(case, cuda, fill=5)
+    first = spread(case, cuda, tensors=t, ws=ws)
+    for _ in range(2):
+        again = spread(case, cuda, tensors=t, ws=ws)
+        assert np.array_equal(again[0], first[0])
+        assert np.array_equal(again[1].view(np.uint32), first[1].view(np.uint32))
+    out_o, lse_o = oracle_decode(case)
+    check(first[0], first[1], out_o, lse_o, "spread garbage workspace")
+
+
+def test_spread_timeout_is_reported_and_the_context_survives(cuda):
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.random_case(74, B=3, H=128, W=1500, N=9000, counts=[1500, 600, 1200])
+    t = to_dev(case, cuda)
+    ws = workspace_for(case, cuda)
+    spread(case, cuda, tensors=t, ws=ws, plan=dict(inject_stall=1, wait_budget_us=2000),
+           expect_status=binding.SMD_ERR_TIMEOUT)
+    ws.zero_()
+    out_g, lse_g = spread(case, cuda, tensors=t, ws=ws)
+    out_o, lse_o = oracle_decode(case)
+    check(out_g, lse_g, out_o, lse_o, "spread after a timeout")
+
+
+def test_dsa_config_through_the_workspace_call(cuda):
+    """The DSA workload at full size through smd_sparse_mla_decode_ws, in the
+    plan bench.py times; sampled rows against the oracle."""
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.config("dsa")
+    t = to_dev(case, cuda)
+    nbytes = binding.smd_workspace_bytes(case.B, case.H, case.W)
+    assert binding.smd_plan_ws(case.B, case.H, case.W).kernel == SPREAD
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=cuda)
+    from test_parity_gpu import gpu_decode
+    out_g, lse_g = gpu_decode(case, cuda, tensors=t, workspace=ws)
+    zero = np.where(case.counts == 0)[0][:2].tolist()
+    rows = [0, 1, 17, 33, 63] + zero
+    out_o, lse_o = oracle_decode(case, rows)
+    check(out_g[rows], lse_g[rows], out_o, lse_o, "dsa spread")
+    n = case.clamped_counts()
+    assert np.all(np.isneginf(lse_g[n == 0])) and np.all(np.isfinite(lse_g[n > 0]))
