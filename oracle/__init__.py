@@ -67,6 +67,17 @@ def _load():
                 ctypes.c_int, ctypes.c_int,
                 ctypes.POINTER(ctypes.c_uint16), ctypes.POINTER(ctypes.c_double),
                 ctypes.POINTER(ctypes.c_double)]
+            lib.smo_sparse_mla_decode_bf16q.restype = ctypes.c_int
+            lib.smo_sparse_mla_decode_bf16q.argtypes = [
+                ctypes.POINTER(ctypes.c_uint16), u8p, ctypes.c_int64, i32p, ctypes.c_int32,
+                i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_float, ctypes.c_float,
+                ctypes.c_int, ctypes.c_int,
+                ctypes.POINTER(ctypes.c_uint16), ctypes.POINTER(ctypes.c_double),
+                ctypes.POINTER(ctypes.c_double), i32p]
+            lib.smo_q_split.restype = ctypes.c_int
+            lib.smo_q_split.argtypes = [ctypes.POINTER(ctypes.c_uint16), u8p, u8p]
+            lib.smo_q_split_exponent.restype = ctypes.c_int
+            lib.smo_q_split_exponent.argtypes = [ctypes.c_double]
             lib.smo_row_head_terms.restype = ctypes.c_int32
             lib.smo_row_head_terms.argtypes = [
                 u8p, u8p, ctypes.c_int64, i32p, ctypes.c_int32, i32p,
@@ -135,6 +146,49 @@ def sparse_mla_decode(q8, kv8, indices, counts, sm_scale, q_scale, k_scale,
     if rc != 0:
         raise ValueError("oracle: an index of a valid entry lies outside the pool")
     return out16, out64, lse
+
+
+def sparse_mla_decode_bf16q(q16, kv8, indices, counts, sm_scale, k_scale,
+                            mode: int = MODE_RECIPE, threads: int = 0):
+    """The decode with a BF16 query (q16: bf16 bits, uint16 [B,H,576]), split
+    per (row, head) into E4M3 hi + lo (the mla_attn page's q_split). Returns
+    (out_bf16, out_f64, lse, k [B,H] the split exponents)."""
+    q16 = np.ascontiguousarray(q16, np.uint16)
+    _, kv8, indices, counts = _inputs(np.zeros((q16.shape[0], q16.shape[1], 576), np.uint8),
+                                      kv8, indices, counts)
+    assert q16.ndim == 3 and q16.shape[2] == 576, q16.shape
+    B, H = q16.shape[0], q16.shape[1]
+    W = indices.shape[1]
+    out16 = np.zeros((B, H, 512), np.uint16)
+    out64 = np.zeros((B, H, 512), np.float64)
+    lse = np.zeros((B, H), np.float64)
+    ks = np.zeros((B, H), np.int32)
+    if B * H == 0:
+        return out16, out64, lse, ks
+    rc = _load().smo_sparse_mla_decode_bf16q(
+        _ptr(q16, ctypes.c_uint16), _ptr(kv8, ctypes.c_uint8), kv8.shape[0],
+        _ptr(indices, ctypes.c_int32), W, _ptr(counts, ctypes.c_int32), B, H,
+        sm_scale, k_scale, int(mode), int(threads),
+        _ptr(out16, ctypes.c_uint16), _ptr(out64, ctypes.c_double),
+        _ptr(lse, ctypes.c_double), _ptr(ks, ctypes.c_int32))
+    if rc != 0:
+        raise ValueError("oracle: an index of a valid entry lies outside the pool")
+    return out16, out64, lse, ks
+
+
+def q_split(q_row16) -> tuple[np.ndarray, np.ndarray, int]:
+    """One 576-column bf16 query row -> (hi codes, lo codes, k)."""
+    q_row16 = np.ascontiguousarray(q_row16, np.uint16)
+    assert q_row16.shape == (576,)
+    hi = np.zeros(576, np.uint8)
+    lo = np.zeros(576, np.uint8)
+    k = _load().smo_q_split(_ptr(q_row16, ctypes.c_uint16), _ptr(hi, ctypes.c_uint8),
+                            _ptr(lo, ctypes.c_uint8))
+    return hi, lo, int(k)
+
+
+def q_split_exponent(amax: float) -> int:
+    return int(_load().smo_q_split_exponent(float(amax)))
 
 
 def row_head_terms(q8, kv8, indices, counts, b, h, sm_scale, q_scale, k_scale):

@@ -9,6 +9,8 @@ the format's largest finite value (448).
 
 Layouts (what the C ABI takes):
   q8       uint8 [B, H, 576]   E4M3 query codes
+  q16      uint16 [B, H, 576]  the bf16 query (bits) the codes were quantized
+                               from, for the bf16-query entry point
   kv8      uint8 [N, 576]      E4M3 cache rows (512 latent + 64 more QK columns)
   indices  int32 [B, W]        the first counts[b] entries of row b are its keys
   counts   int32 [B]
@@ -40,6 +42,7 @@ class Case:
     sm_scale: float
     q_scale: float
     k_scale: float
+    q16: np.ndarray | None = None  # uint16 [B, H, 576]: the bf16 query q8 was quantized from
 
     @property
     def B(self) -> int:
@@ -124,10 +127,14 @@ def quantize_per_tensor(x: np.ndarray) -> tuple[np.ndarray, float]:
     return codes, scale
 
 
-def make_query(rng: np.random.Generator, B: int, H: int) -> tuple[np.ndarray, float]:
+def make_query(rng: np.random.Generator, B: int, H: int) -> tuple[np.ndarray, float, np.ndarray]:
+    """The bf16 query N(0,1): its per-tensor E4M3 codes and scale, and its
+    bf16 bits (for the bf16-query entry point)."""
     q = rng.standard_normal((B, H, ROW), dtype=np.float32)
     q = to_bf16_values(q)  # the model's query is bf16
-    return quantize_per_tensor(q)
+    codes, scale = quantize_per_tensor(q)
+    q16 = (np.ascontiguousarray(q, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    return codes, scale, q16
 
 
 def make_pool(seed_seq: np.random.SeedSequence, N: int, heavy_frac: float = 0.0,
@@ -172,14 +179,14 @@ def tiny(seed: int = 0) -> Case:
     ss = np.random.SeedSequence(seed)
     rng = np.random.Generator(np.random.PCG64(ss.spawn(1)[0]))
     B, H, W, N = 2, 16, 64, 4096
-    q8, qs = make_query(rng, B, H)
+    q8, qs, q16 = make_query(rng, B, H)
     kv8, ks = make_pool(ss.spawn(1)[0], N)
     counts = np.array([64, 37], np.int32)
     idx = np.zeros((B, W), np.int64)
     for b in range(B):
         idx[b] = rng.choice(N, size=W, replace=False)
     _fill_tail(rng, idx, counts, N)
-    return Case("tiny", q8, kv8, idx.astype(np.int32), counts, _f32(192 ** -0.5), qs, ks)
+    return Case("tiny", q8, kv8, idx.astype(np.int32), counts, _f32(192 ** -0.5), qs, ks, q16=q16)
 
 
 def latency(seed: int = 1) -> Case:
@@ -188,7 +195,7 @@ def latency(seed: int = 1) -> Case:
     ss = np.random.SeedSequence(seed)
     rng = np.random.Generator(np.random.PCG64(ss.spawn(1)[0]))
     B, H, W, N = 5, 64, 256, 65536
-    q8, qs = make_query(rng, B, H)
+    q8, qs, q16 = make_query(rng, B, H)
     kv8, ks = make_pool(ss.spawn(1)[0], N)
     counts = rng.integers(200, 257, size=B).astype(np.int32)
     counts[rng.integers(0, B)] = 0
@@ -196,7 +203,7 @@ def latency(seed: int = 1) -> Case:
     for b in range(B):
         idx[b] = rng.choice(N, size=W, replace=False)
     _fill_tail(rng, idx, counts, N)
-    return Case("latency", q8, kv8, idx.astype(np.int32), counts, _f32(192 ** -0.5), qs, ks)
+    return Case("latency", q8, kv8, idx.astype(np.int32), counts, _f32(192 ** -0.5), qs, ks, q16=q16)
 
 
 def dsa(seed: int = 2) -> Case:
@@ -205,7 +212,7 @@ def dsa(seed: int = 2) -> Case:
     ss = np.random.SeedSequence(seed)
     rng = np.random.Generator(np.random.PCG64(ss.spawn(1)[0]))
     B, H, W, N, WIN = 64, 128, 2048, 262144, 4096
-    q8, qs = make_query(rng, B, H)
+    q8, qs, q16 = make_query(rng, B, H)
     kv8, ks = make_pool(ss.spawn(1)[0], N)
     counts = rng.integers(1, W + 1, size=B).astype(np.int32)
     counts[rng.choice(B, size=4, replace=False)] = 0
@@ -218,7 +225,7 @@ def dsa(seed: int = 2) -> Case:
         rng.shuffle(row)
         idx[b] = row
     _fill_tail(rng, idx, counts, N)
-    return Case("dsa", q8, kv8, idx.astype(np.int32), counts, _f32(192 ** -0.5), qs, ks)
+    return Case("dsa", q8, kv8, idx.astype(np.int32), counts, _f32(192 ** -0.5), qs, ks, q16=q16)
 
 
 def throughput(seed: int = 3) -> Case:
@@ -227,13 +234,13 @@ def throughput(seed: int = 3) -> Case:
     ss = np.random.SeedSequence(seed)
     rng = np.random.Generator(np.random.PCG64(ss.spawn(1)[0]))
     B, H, W, N = 256, 128, 2048, 1 << 20
-    q8, qs = make_query(rng, B, H)
+    q8, qs, q16 = make_query(rng, B, H)
     kv8, ks = make_pool(ss.spawn(1)[0], N, heavy_frac=0.01, heavy_gain=8.0, rng=rng)
     counts = np.full(B, W, np.int32)
     idx = np.zeros((B, W), np.int64)
     for b in range(B):
         idx[b] = rng.choice(N, size=W, replace=False)
-    return Case("throughput", q8, kv8, idx.astype(np.int32), counts, _f32(192 ** -0.5), qs, ks)
+    return Case("throughput", q8, kv8, idx.astype(np.int32), counts, _f32(192 ** -0.5), qs, ks, q16=q16)
 
 
 def dense(seed: int = 4) -> Case:
@@ -244,7 +251,7 @@ def dense(seed: int = 4) -> Case:
     rng = np.random.Generator(np.random.PCG64(ss.spawn(1)[0]))
     R, QLEN, H, W, N = 32, 4, 16, 8192, 262144
     B = R * QLEN
-    q8, qs = make_query(rng, B, H)
+    q8, qs, q16 = make_query(rng, B, H)
     kv8, ks = make_pool(ss.spawn(1)[0], N)
     perm = rng.permutation(N)
     L = rng.integers(1024, 8193, size=R)
@@ -260,7 +267,7 @@ def dense(seed: int = 4) -> Case:
             counts[b] = n
             idx[b, :n] = tokens[:n]
     _fill_tail(rng, idx, counts, N)
-    return Case("dense", q8, kv8, idx.astype(np.int32), counts, _f32(192 ** -0.5), qs, ks)
+    return Case("dense", q8, kv8, idx.astype(np.int32), counts, _f32(192 ** -0.5), qs, ks, q16=q16)
 
 
 CONFIGS = {
@@ -284,7 +291,7 @@ def random_case(seed: int, B: int, H: int, W: int, N: int, counts=None,
     row's indices with replacement (duplicates allowed)."""
     ss = np.random.SeedSequence(1000 + seed)
     rng = np.random.Generator(np.random.PCG64(ss.spawn(1)[0]))
-    q8, qs = make_query(rng, B, H)
+    q8, qs, q16 = make_query(rng, B, H)
     kv8, ks = make_pool(ss.spawn(1)[0], N, heavy_frac=heavy_frac, rng=rng)
     if counts is None:
         counts = rng.integers(0, W + 1, size=B)
@@ -299,7 +306,7 @@ def random_case(seed: int, B: int, H: int, W: int, N: int, counts=None,
             idx[b] = rng.choice(N, size=W, replace=False)
     _fill_tail(rng, idx, counts, N)
     sm = _f32(192 ** -0.5) if sm_scale is None else _f32(sm_scale)
-    return Case(f"random{seed}", q8, kv8, idx.astype(np.int32), counts, sm, qs, ks)
+    return Case(f"random{seed}", q8, kv8, idx.astype(np.int32), counts, sm, qs, ks, q16=q16)
 
 
 def grouped_case(seed: int, R: int, G: int, H: int, W: int, N: int, counts=None) -> Case:
@@ -311,7 +318,7 @@ def grouped_case(seed: int, R: int, G: int, H: int, W: int, N: int, counts=None)
     ss = np.random.SeedSequence(5000 + seed)
     rng = np.random.Generator(np.random.PCG64(ss.spawn(1)[0]))
     B = R * G
-    q8, qs = make_query(rng, B, H)
+    q8, qs, q16 = make_query(rng, B, H)
     kv8, ks = make_pool(ss.spawn(1)[0], N, rng=rng)
     if counts is None:
         L = rng.integers(G, W + 1, size=R)
@@ -322,7 +329,7 @@ def grouped_case(seed: int, R: int, G: int, H: int, W: int, N: int, counts=None)
         lst = rng.choice(N, size=W, replace=False) if W <= N else rng.integers(0, N, size=W)
         idx[r * G:(r + 1) * G] = lst
     _fill_tail(rng, idx, counts, N)
-    return Case(f"grouped{seed}", q8, kv8, idx.astype(np.int32), counts, _f32(192 ** -0.5), qs, ks)
+    return Case(f"grouped{seed}", q8, kv8, idx.astype(np.int32), counts, _f32(192 ** -0.5), qs, ks, q16=q16)
 
 
 def algorithmic_bytes(case: Case) -> dict:

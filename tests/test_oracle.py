@@ -6,7 +6,10 @@ format's anchor values; exact logits against rational arithmetic; closed forms
 (equal logits -> plain mean of V, one dominant key -> its V row, count 1,
 count 0 -> zeros and -inf); the index-order invariance that the row-max anchor
 gives; the E4M3-P error bound against the unquantized fp64 reference; and a
-brute-force rational re-implementation on tiny inputs.
+brute-force rational re-implementation on tiny inputs. For the bf16-query
+variant: the split exponent's defining inequality, exactness of hi + lo over
+every bf16 value where the residual fits, the reduction to the E4M3 decode,
+and the removal of the query rounding against an unrounded reference.
 
 The method these follow is the "attn_sparse" page (SparseDcpDecode): module
 docstring paragraphs "Per CTA", "Precision" and "Rows of count 0", and the
@@ -361,3 +364,105 @@ def test_golden_fixture_regression():
     want_lse = np.array([(-math.inf if v is None else v) for v in g["lse"]])
     assert np.allclose(lse.reshape(-1), want_lse, rtol=0, atol=1e-12)
     assert np.array_equal(np.isneginf(lse.reshape(-1)), np.isneginf(want_lse))
+
+
+# ------------------------------------------- the bf16 query, split hi + lo ---
+# The mla_attn page: "q_split" (the bf16 Q rows to "E4M3 hi, lo of q 2^k") and
+# "fp8_split4" (x ~ hi + lo). Reading: one power-of-two scale per (row, head).
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 values that are exactly bf16 -> their bits."""
+    x = np.ascontiguousarray(x, np.float32)
+    bits = x.view(np.uint32)
+    assert np.all(bits & 0xFFFF == 0)
+    return (bits >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("amax", [448.0, 448.5, 449.0, 224.0, 1.0, 0.875, 0.8749, 3.9,
+                                  2.0 ** -20, 1e-30, 7e8, 1e30])
+def test_q_split_exponent_is_the_largest_in_range(amax):
+    """amax * 2^k <= 448 < amax * 2^(k+1), in exact arithmetic (clamped to
+    [-32, 32])."""
+    k = oracle.q_split_exponent(amax)
+    a = Fraction(amax)
+    two = Fraction(2)
+    if -32 < k < 32:
+        assert a * two ** k <= 448 < a * two ** (k + 1), (amax, k)
+    else:
+        assert k in (-32, 32)
+        assert (a * two ** k <= 448) if k == 32 else (a * two ** k > 224)
+    assert oracle.q_split_exponent(0.0) == 0
+
+
+def test_q_split_is_exact_where_the_residual_fits():
+    """Every bf16 value x with 2^-2 <= |x| <= 448 is hi + lo exactly (the
+    residual has at most four significant bits on a 2^-9 grid); below that
+    the error is at most half the smallest E4M3 step (2^-10). A row holding
+    448 gets k = 0, so the codes are those of x itself."""
+    e = np.arange(-20, 9)
+    mant = np.arange(128)
+    vals = np.array([(1 + m / 128.0) * 2.0 ** int(x) for x in e for m in mant], np.float64)
+    vals = vals[vals <= 448.0]
+    vals = np.concatenate([vals, -vals]).astype(np.float32)
+    for start in range(0, vals.size, 575):
+        chunk = vals[start:start + 575]
+        row = np.zeros(576, np.float32)
+        row[0] = 448.0
+        row[1:1 + chunk.size] = chunk
+        hi, lo, k = oracle.q_split(_bf16_bits(row))
+        assert k == 0
+        got = dec(hi) + dec(lo)
+        x = row.astype(np.float64)
+        big = np.abs(x) >= 0.25
+        assert np.array_equal(got[big], x[big])
+        assert np.all(np.abs(got[~big] - x[~big]) <= 2.0 ** -10)
+        # hi alone is the plain E4M3 rounding of x (torch's cast)
+        assert np.array_equal(dec(hi), dec(inputs.to_e4m3(row)))
+
+
+@pytest.mark.parametrize("shift", [0, -5, 3])
+def test_bf16_query_that_is_e4m3_reduces_to_the_e4m3_decode(shift):
+    """A bf16 query whose values are E4M3 values times 2^shift, with 448 x
+    2^shift in every (row, head): the split gives lo = 0 and k = -shift, so
+    the decode is the E4M3 decode with q_scale = 2^shift, bit for bit."""
+    case = inputs.random_case(90, B=3, H=16, W=100, N=800, counts=[100, 37, 0])
+    q8 = case.q8.copy()
+    q8[:, :, 5] = 0x7E  # 448
+    qv = (dec(q8) * 2.0 ** shift).astype(np.float32)
+    q16 = _bf16_bits(qv)
+    o16, o64, lse, ks = oracle.sparse_mla_decode_bf16q(q16, case.kv8, case.indices, case.counts,
+                                                       case.sm_scale, case.k_scale)
+    assert np.all(ks == -shift)
+    r16, r64, rlse = oracle.sparse_mla_decode(q8, case.kv8, case.indices, case.counts,
+                                              case.sm_scale, 2.0 ** shift, case.k_scale)
+    assert np.array_equal(o16, r16)
+    assert np.array_equal(lse.view(np.uint64), rlse.view(np.uint64))
+
+
+def test_bf16_query_split_removes_the_query_rounding():
+    """Against a float64 reference that uses the bf16 query unrounded (and P
+    unquantized): the split query's decode (P unquantized too) is within
+    1e-4 of max|out|, and more than 20x closer than the per-tensor E4M3
+    query's decode. A split that dropped lo would be as far off as E4M3."""
+    case = inputs.random_case(91, B=2, H=16, W=300, N=3000, counts=[300, 211])
+    qv = (case.q16.astype(np.uint32) << 16).view(np.float32)  # the bf16 values
+    kvv = dec(case.kv8)
+    lam0 = float(np.float32(case.sm_scale * case.k_scale * 1.4426950408889634))
+    ref = np.zeros((case.B, case.H, 512))
+    for b in range(case.B):
+        n = int(case.counts[b])
+        rows = kvv[case.indices[b, :n]]
+        s = lam0 * (qv[b].astype(np.float64) @ rows.T)       # [H, n], base 2
+        P = np.exp2(s - s.max(axis=1, keepdims=True))
+        ref[b] = case.k_scale * (P @ rows[:, :512]) / P.sum(axis=1, keepdims=True)
+    _, split64, _, _ = oracle.sparse_mla_decode_bf16q(case.q16, case.kv8, case.indices,
+                                                      case.counts, case.sm_scale, case.k_scale,
+                                                      mode=oracle.MODE_UNQUANT)
+    _, e4m3_64, _ = oracle.sparse_mla_decode(case.q8, case.kv8, case.indices, case.counts,
+                                             case.sm_scale, case.q_scale, case.k_scale,
+                                             mode=oracle.MODE_UNQUANT)
+    scale = np.abs(ref).max()
+    err_split = np.abs(split64 - ref).max()
+    err_e4m3 = np.abs(e4m3_64 - ref).max()
+    assert err_split <= 1e-4 * scale, (err_split, scale)
+    assert err_split * 20 < err_e4m3, (err_split, err_e4m3)
