@@ -179,17 +179,25 @@ def run_gpu(args, world, rank, local) -> dict | None:
     torch.cuda.set_device(dev)
     case = inputs.config(args.config)
     stats = workload_stats(case)
+    bf16q = args.query == "bf16"
+    if bf16q:  # the query is read as bf16: twice the bytes
+        stats["total"] += stats["q"]
+        stats["q"] *= 2
     # Rows that come in groups sharing one index list (the dense-as-sparse
-    # workload's four causal rows per request) go through the grouped call.
-    group = ROW_GROUP.get(args.config, 1)
+    # workload's four causal rows per request) go through the grouped call
+    # (the bf16-query call takes rows one by one).
+    group = 1 if bf16q else ROW_GROUP.get(args.config, 1)
     plan = binding.smd_plan_grouped(case.B, case.H, case.W, group).as_dict()
     # Where the library's workspace plan (the spread kernel) applies, the
     # workspace entry point is timed with a workspace of the size it asks for.
-    ws_bytes = binding.smd_workspace_bytes(case.B, case.H, case.W) if group == 1 else 0
+    ws_bytes = binding.smd_workspace_bytes(case.B, case.H, case.W) if group == 1 and not bf16q else 0
     if ws_bytes > 0:
         plan = binding.smd_plan_ws(case.B, case.H, case.W).as_dict()
+    if bf16q:
+        plan = binding.smd_plan_bf16q(case.B, case.H, case.W).as_dict()
 
     q = torch.from_numpy(case.q8).to(dev)
+    q16 = torch.from_numpy(case.q16.view(np.int16)).to(dev).view(torch.bfloat16)
     kv = torch.from_numpy(case.kv8).to(dev)
     idx = torch.from_numpy(case.indices).to(dev)
     cnt = torch.from_numpy(case.counts).to(dev)
@@ -211,9 +219,12 @@ def run_gpu(args, world, rank, local) -> dict | None:
             lse.data_ptr(), status.data_ptr(), sptr)
 
     gptrs = ptrs[:8] + (group,) + ptrs[8:]
+    bptrs = (q16.data_ptr(),) + ptrs[1:8] + (case.sm_scale, case.k_scale) + ptrs[11:]
 
     def decode():
-        if group > 1:
+        if bf16q:
+            rc = binding.smd_sparse_mla_decode_bf16q(*bptrs)
+        elif group > 1:
             rc = binding.smd_sparse_mla_decode_grouped(*gptrs)
         elif ws_bytes > 0:
             rc = binding.smd_sparse_mla_decode_ws(*ptrs[:-1], workspace.data_ptr(), ws_bytes, sptr)
@@ -255,20 +266,26 @@ def run_gpu(args, world, rank, local) -> dict | None:
     ms, value = aggregate(stats["kv_gathered"], ms_local, world, dev)
 
     # ---- end to end through the public call: host buffers in, host buffers out.
-    hq = torch.from_numpy(case.q8).pin_memory()
+    hq = (torch.from_numpy(case.q16.view(np.int16)).view(torch.bfloat16) if bf16q
+          else torch.from_numpy(case.q8)).pin_memory()
     hidx = torch.from_numpy(case.indices).pin_memory()
     hcnt = torch.from_numpy(case.counts).pin_memory()
     hout = torch.empty((case.B, case.H, 512), dtype=torch.bfloat16).pin_memory()
     hlse = torch.empty((case.B, case.H), dtype=torch.float32).pin_memory()
-    dq, didx, dcnt = torch.empty_like(q), torch.empty_like(idx), torch.empty_like(cnt)
+    dq, didx, dcnt = torch.empty_like(q16 if bf16q else q), torch.empty_like(idx), torch.empty_like(cnt)
 
     def e2e_step():
         dq.copy_(hq, non_blocking=True)
         didx.copy_(hidx, non_blocking=True)
         dcnt.copy_(hcnt, non_blocking=True)
-        binding.sparse_mla_decode(dq, kv, didx, dcnt, case.sm_scale, case.q_scale, case.k_scale,
-                                  out=out, lse=lse, status=status, row_group=group,
-                                  workspace=workspace if ws_bytes > 0 else None)
+        if bf16q:
+            binding.sparse_mla_decode_bf16q(dq, kv, didx, dcnt, case.sm_scale, case.k_scale,
+                                            out=out, lse=lse, status=status)
+        else:
+            binding.sparse_mla_decode(dq, kv, didx, dcnt, case.sm_scale, case.q_scale,
+                                      case.k_scale, out=out, lse=lse, status=status,
+                                      row_group=group,
+                                      workspace=workspace if ws_bytes > 0 else None)
         hout.copy_(out, non_blocking=True)
         hlse.copy_(lse, non_blocking=True)
 
@@ -289,7 +306,7 @@ def run_gpu(args, world, rank, local) -> dict | None:
     barrier(world)
     e2e_ms = reduce_max(float(np.mean([s.elapsed_time(e) for s, e in zip(e_starts, e_ends)])),
                         world, dev)
-    h2d = hq.numel() + hidx.numel() * 4 + hcnt.numel() * 4
+    h2d = hq.numel() * hq.element_size() + hidx.numel() * 4 + hcnt.numel() * 4
     d2h = hout.numel() * 2 + hlse.numel() * 4
 
     if rank != 0:
@@ -303,7 +320,7 @@ def run_gpu(args, world, rank, local) -> dict | None:
     t_hbm = stats["total"] / (pk["hbm_gbs"] * 1e9)
     t_tc = stats["flops"] / (fp8_peak_tflops * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
-    traffic = load_traffic(args.config, plan["kernel"])
+    traffic = load_traffic(args.config + ("_bf16q" if bf16q else ""), plan["kernel"])
     roofline = {
         "bound": bound,
         "achieved": round(achieved, 2) if bound == "hbm" else round(
@@ -320,7 +337,8 @@ def run_gpu(args, world, rank, local) -> dict | None:
                                        "; FP8 = 2 x measured BF16 (nominal ratio)"),
     }
     roofline["frac"] = round(roofline["achieved"] / roofline["peak"], 5)
-    cpu = cpu_baseline(case, stats, args.cpu_seconds) if world == 1 or rank == 0 else None
+    cpu = (cpu_baseline(case, stats, args.cpu_seconds, bf16q) if world == 1 or rank == 0
+           else None)
     line = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -333,11 +351,13 @@ def run_gpu(args, world, rank, local) -> dict | None:
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "fp8_e4m3 (fp32 accumulate)",
+        "dtype": ("bf16 query split into E4M3 hi + lo; fp8_e4m3 cache (fp32 accumulate)"
+                  if bf16q else "fp8_e4m3 (fp32 accumulate)"),
         "data": "synthetic (seeded numpy PCG64; E4M3 per-tensor scaled)",
         "config": {
             "workload": WORKLOAD_TEXT[args.config],
             "name": args.config,
+            "query": "bf16 (split)" if bf16q else "e4m3 (per-tensor scale)",
             "B": case.B, "H": case.H, "top_k": case.W, "pool_rows": case.N,
             "gathered_keys": case.gathered_rows(), "unique_rows": case.unique_rows(),
             "l2": "flushed before every timed step (write of a 2x-L2 buffer, then read of another, outside the events)",
@@ -384,7 +404,7 @@ def load_traffic(config: str, kernel: int = 1):
         return None
 
 
-def cpu_baseline(case, stats, seconds: float) -> dict:
+def cpu_baseline(case, stats, seconds: float, bf16q: bool = False) -> dict:
     """The oracle, as it stands, on the host cores: repeats of the whole
     workload (or a row sample of it) for about `seconds`."""
     import oracle
@@ -401,8 +421,12 @@ def cpu_baseline(case, stats, seconds: float) -> dict:
     reps, t_total = 0, 0.0
     while t_total < seconds or reps < 1:
         t0 = time.perf_counter()
-        oracle.sparse_mla_decode(q8, case.kv8, idx, cnt, case.sm_scale, case.q_scale,
-                                 case.k_scale, threads=cores)
+        if bf16q:
+            oracle.sparse_mla_decode_bf16q(case.q16[rows], case.kv8, idx, cnt, case.sm_scale,
+                                           case.k_scale, threads=cores)
+        else:
+            oracle.sparse_mla_decode(q8, case.kv8, idx, cnt, case.sm_scale, case.q_scale,
+                                     case.k_scale, threads=cores)
         t_total += time.perf_counter() - t0
         reps += 1
     per_call = t_total / reps
@@ -420,14 +444,21 @@ def run_reference(args, world, rank) -> dict | None:
     stats = workload_stats(case)
     import oracle
     cores = oracle.max_threads()
+
+    def step():
+        if args.query == "bf16":
+            oracle.sparse_mla_decode_bf16q(case.q16, case.kv8, case.indices, case.counts,
+                                           case.sm_scale, case.k_scale, threads=cores)
+        else:
+            oracle.sparse_mla_decode(case.q8, case.kv8, case.indices, case.counts, case.sm_scale,
+                                     case.q_scale, case.k_scale, threads=cores)
+
     for _ in range(args.warmup):
-        oracle.sparse_mla_decode(case.q8, case.kv8, case.indices, case.counts, case.sm_scale,
-                                 case.q_scale, case.k_scale, threads=cores)
+        step()
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.sparse_mla_decode(case.q8, case.kv8, case.indices, case.counts, case.sm_scale,
-                                 case.q_scale, case.k_scale, threads=cores)
+        step()
         times.append(time.perf_counter() - t0)
     ms = 1e3 * float(np.mean(times))
     value = stats["kv_gathered"] / (ms * 1e-3) / 1e9
@@ -455,6 +486,8 @@ def main(argv=None):
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(WORKLOAD_TEXT))
     ap.add_argument("--impl", default="smd", choices=["smd", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--query", default="e4m3", choices=["e4m3", "bf16"],
+                    help="bf16: the bf16-query call (query split into E4M3 hi + lo)")
     args = ap.parse_args(argv)
     world, rank, local = (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
                           int(os.environ.get("LOCAL_RANK", "0")))

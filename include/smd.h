@@ -220,6 +220,38 @@ int smd_sparse_mla_decode_noalloc(const uint8_t* q, const uint8_t* kv_pool, int6
                                   uint16_t* out, float* lse, int32_t* status,
                                   smd_stream_t stream);
 
+/* The decode with a BF16 query, without its per-tensor E4M3 rounding (the
+ * mla_attn page: "q_split", the bf16 Q rows to "E4M3 hi, lo of q 2^k", and
+ * "fp8_split4", x ~ hi + lo). Each (row, head) query row is scaled by 2^k,
+ * the largest power of two with max|q| 2^k <= 448 (k = 0 for a zero row,
+ * k clamped to [-32, 32]), and split into hi = E4M3(q 2^k) and
+ * lo = E4M3(q 2^k - hi), both round-to-nearest-even and saturating; hi + lo
+ * is q 2^k exactly wherever |q 2^k| >= 2^-2. The logit is
+ *   s_i = fp32(lambda_h * fp32(sum_c (hi_c + lo_c) * kv8[j_i, c])),
+ *   lambda_h = fp32(sm_scale * 2^-k * k_scale * log2 e)
+ * and everything after the logits is as in smd_sparse_mla_decode. QK costs
+ * twice the MMAs. Runs on the warp-MMA kernel (any H multiple of 16).
+ *   q   [B, H, 576] bfloat16 (raw 16-bit storage), row-major, 16-byte
+ *       aligned, finite. There is no q_scale: the split finds its own scale.
+ * The other arguments, layouts, ownership and errors are those of
+ * smd_sparse_mla_decode. */
+int smd_sparse_mla_decode_bf16q(const uint16_t* q, const uint8_t* kv_pool, int64_t N,
+                                const int32_t* indices, int32_t W, const int32_t* counts,
+                                int32_t B, int32_t H, float sm_scale, float k_scale,
+                                uint16_t* out, float* lse, int32_t* status, smd_stream_t stream);
+
+/* As smd_sparse_mla_decode_bf16q with plan fields (kernel SMD_KERNEL_MMA or
+ * 0, split, tiles, window, the testing hooks) taken from `force` (may be
+ * NULL). For the tests. */
+int smd_sparse_mla_decode_bf16q_ex(const uint16_t* q, const uint8_t* kv_pool, int64_t N,
+                                   const int32_t* indices, int32_t W, const int32_t* counts,
+                                   int32_t B, int32_t H, float sm_scale, float k_scale,
+                                   uint16_t* out, float* lse, int32_t* status,
+                                   smd_stream_t stream, const smd_plan_t* force);
+
+/* The plan smd_sparse_mla_decode_bf16q would use. Host only. */
+int smd_plan_bf16q(int32_t B, int32_t H, int32_t W, smd_plan_t* plan);
+
 /* The decode for rows that come in groups sharing one index list: the
  * verify rows of a multi-token decode step, where row i of a request sees the
  * first L - G + 1 + i tokens of its cache (the attn_sparse page's verify rows;

@@ -81,6 +81,16 @@ def lib() -> ctypes.CDLL:
             so.smd_sparse_mla_decode_grouped.argtypes = grp_args
             so.smd_sparse_mla_decode_grouped_ex.restype = ctypes.c_int
             so.smd_sparse_mla_decode_grouped_ex.argtypes = grp_args + [ctypes.POINTER(SmdPlan)]
+            bq_args = ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                        ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                        ctypes.c_float, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                        ctypes.c_void_p, ctypes.c_void_p])
+            so.smd_sparse_mla_decode_bf16q.restype = ctypes.c_int
+            so.smd_sparse_mla_decode_bf16q.argtypes = bq_args
+            so.smd_sparse_mla_decode_bf16q_ex.restype = ctypes.c_int
+            so.smd_sparse_mla_decode_bf16q_ex.argtypes = bq_args + [ctypes.POINTER(SmdPlan)]
+            so.smd_plan_bf16q.restype = ctypes.c_int
+            so.smd_plan_bf16q.argtypes = [ctypes.c_int32] * 3 + [ctypes.POINTER(SmdPlan)]
             so.smd_plan_grouped.restype = ctypes.c_int
             so.smd_plan_grouped.argtypes = [ctypes.c_int32] * 4 + [ctypes.POINTER(SmdPlan)]
             so.smd_workspace_bytes.restype = ctypes.c_int64
@@ -160,6 +170,27 @@ def smd_plan_grouped(B: int, H: int, W: int, row_group: int) -> SmdPlan:
     rc = lib().smd_plan_grouped(B, H, W, row_group, ctypes.byref(p))
     if rc != SMD_OK:
         raise SmdError(rc, "smd_plan_grouped")
+    return p
+
+
+def smd_sparse_mla_decode_bf16q(q, kv_pool, N, indices, W, counts, B, H, sm_scale, k_scale,
+                                out, lse, status, stream) -> int:
+    return lib().smd_sparse_mla_decode_bf16q(q, kv_pool, N, indices, W, counts, B, H, sm_scale,
+                                             k_scale, out, lse, status, stream)
+
+
+def smd_sparse_mla_decode_bf16q_ex(q, kv_pool, N, indices, W, counts, B, H, sm_scale, k_scale,
+                                   out, lse, status, stream, force: SmdPlan | None) -> int:
+    ref = ctypes.byref(force) if force is not None else None
+    return lib().smd_sparse_mla_decode_bf16q_ex(q, kv_pool, N, indices, W, counts, B, H, sm_scale,
+                                                k_scale, out, lse, status, stream, ref)
+
+
+def smd_plan_bf16q(B: int, H: int, W: int) -> SmdPlan:
+    p = SmdPlan()
+    rc = lib().smd_plan_bf16q(B, H, W, ctypes.byref(p))
+    if rc != SMD_OK:
+        raise SmdError(rc, "smd_plan_bf16q")
     return p
 
 
@@ -286,4 +317,51 @@ def sparse_mla_decode(q, kv_pool, indices, counts, sm_scale: float, q_scale: flo
         rc = smd_sparse_mla_decode_ex(*args, *ws, int(stream), plan)
     if rc != SMD_OK:
         raise SmdError(rc, "smd_sparse_mla_decode")
+    return out, lse
+
+
+def sparse_mla_decode_bf16q(q, kv_pool, indices, counts, sm_scale: float, k_scale: float,
+                            out=None, lse=None, status=None, stream=None,
+                            plan: SmdPlan | dict | None = None):
+    """Decode with a bfloat16 query q [B,H,576] (split into E4M3 hi + lo per
+    (row, head) on the GPU: smd_sparse_mla_decode_bf16q). kv_pool [N,576] E4M3,
+    indices [B,W] int32, counts [B] int32, all CUDA tensors. Returns
+    (out [B,H,512] bfloat16, lse [B,H] float32)."""
+    import torch
+
+    kv_pool = _bytes_view(kv_pool, "kv_pool")
+    if q.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"q: expected bfloat16, got {q.dtype}")
+    for name, t in (("q", q), ("kv_pool", kv_pool), ("indices", indices), ("counts", counts)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (the decode has no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if indices.dtype != torch.int32 or counts.dtype != torch.int32:
+        raise TypeError("indices and counts must be int32")
+    if q.dim() != 3 or q.shape[2] != 576 or kv_pool.dim() != 2 or kv_pool.shape[1] != 576:
+        raise ValueError("q must be [B,H,576] and kv_pool [N,576]")
+    B, H = int(q.shape[0]), int(q.shape[1])
+    if indices.dim() != 2 or indices.shape[0] < B or counts.shape[0] < B:
+        raise ValueError("indices must be [>=B, W] and counts [>=B]")
+    W = int(indices.shape[1])
+    if out is None:
+        out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    args = (_ptr(q), _ptr(kv_pool), int(kv_pool.shape[0]), _ptr(indices), W, _ptr(counts), B, H,
+            float(sm_scale), float(k_scale), _ptr(out), _ptr(lse), _ptr(status), int(stream))
+    if isinstance(plan, dict):
+        p = SmdPlan()
+        for k, v in plan.items():
+            setattr(p, k, int(v))
+        plan = p
+    rc = (smd_sparse_mla_decode_bf16q(*args) if plan is None
+          else smd_sparse_mla_decode_bf16q_ex(*args, plan))
+    if rc != SMD_OK:
+        raise SmdError(rc, "smd_sparse_mla_decode_bf16q")
     return out, lse

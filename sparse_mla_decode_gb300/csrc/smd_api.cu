@@ -47,12 +47,12 @@ bool is_split(int s) { return s == 1 || s == 2 || s == 4 || s == 8 || s == 16; }
 // Most keys one CTA can hold logits for with `tiles` 16-head tiles, a
 // `window`-key buffer and `idx_cap` staged indices, under the shared-memory
 // limit.
-int key_cap_limit(int tiles, int split, int window, int idx_cap) {
+int key_cap_limit(int tiles, int split, int window, int idx_cap, bool qsplit) {
     // The layout grows by (16*tiles + 1) * 4 bytes per key of capacity.
-    const int base = mma_layout(tiles, split, window, 0, idx_cap).total;
+    const int base = mma_layout(tiles, split, window, 0, idx_cap, qsplit).total;
     const int per_key = (kHeadsPerTile * tiles + 1) * 4;
     int cap = std::max(0, (kMaxSmemBytes - base) / per_key) / kChunk * kChunk;
-    while (cap > 0 && mma_layout(tiles, split, window, cap, idx_cap).total > kMaxSmemBytes)
+    while (cap > 0 && mma_layout(tiles, split, window, cap, idx_cap, qsplit).total > kMaxSmemBytes)
         cap -= kChunk;
     return cap;
 }
@@ -60,7 +60,7 @@ int key_cap_limit(int tiles, int split, int window, int idx_cap) {
 // Fills the MMA kernel's plan. `force` fields that are non-zero override the
 // automatic choice. Returns an smd_status.
 int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_plan_t* out,
-             MmaConfig* cfg) {
+             MmaConfig* cfg, bool qsplit = false) {
     // One 16-head tile per CTA by default: on GB300 the second tile's KV reuse
     // is worth less than the extra cluster exchange and registers it costs.
     int tiles = 1;
@@ -85,7 +85,7 @@ int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
         for (int s = 1; s <= 16; s *= 2) {
             const int per = ceil_div(W, s);
             const int win = std::min(window_req, std::max(kChunk, ceil_div(per, kChunk) * kChunk));
-            if (per <= key_cap_limit(tiles, s, win, spec)) {
+            if (per <= key_cap_limit(tiles, s, win, spec, qsplit)) {
                 split = s;
                 break;
             }
@@ -96,7 +96,7 @@ int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
     const int per = ceil_div(std::max(W, 1), split);
     const int window = std::min(window_req, std::max(kChunk, ceil_div(per, kChunk) * kChunk));
     const int key_cap = std::max(kChunk, ceil_div(per, kChunk) * kChunk);
-    const MmaLayout L = mma_layout(tiles, split, window, key_cap, spec);
+    const MmaLayout L = mma_layout(tiles, split, window, key_cap, spec, qsplit);
     if (L.total > kMaxSmemBytes) return (force && (force->split || force->window)) ? SMD_ERR_PLAN
                                                                                   : SMD_ERR_SHAPE;
     cfg->tiles = tiles;
@@ -105,6 +105,7 @@ int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
                               : kWaitBudgetNs;
     cfg->inject_stall = (force && force->inject_stall) ? 1 : 0;
     cfg->spec_idx = spec > 0 ? 1 : 0;
+    cfg->qsplit = qsplit ? 1 : 0;
     cfg->split = split;
     cfg->window = window;
     cfg->key_cap = key_cap;
@@ -363,7 +364,7 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
            const int32_t* counts, int32_t B, int32_t H, float sm_scale, float q_scale,
            float k_scale, uint16_t* out, float* lse, int32_t* status, void* workspace,
            int64_t workspace_bytes, smd_stream_t stream, const smd_plan_t* force,
-           bool library_scratch = false, int row_group = 1) {
+           bool library_scratch = false, int row_group = 1, const uint16_t* q16 = nullptr) {
     if (B < 0 || W < 0 || N < 0 || H <= 0 || H % kHeadsPerTile != 0) return SMD_ERR_SHAPE;
     if (row_group != 1 && ((row_group != 2 && row_group != 4) || B % row_group != 0))
         return SMD_ERR_SHAPE;
@@ -406,6 +407,31 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
         a.status = status;
         if (want == SMD_KERNEL_TC_GROUP) return launch_tcg(a, tcfg, reinterpret_cast<cudaStream_t>(stream));
         return launch_group(a, gcfg, reinterpret_cast<cudaStream_t>(stream));
+    }
+
+    if (q16 != nullptr) {
+        // The split query runs on the warp-MMA kernel.
+        if (force && force->kernel && force->kernel != SMD_KERNEL_MMA) return SMD_ERR_PLAN;
+        smd_plan_t plan{};
+        MmaConfig mcfg{};
+        const int rc = plan_mma(B, H, W, sm_count_of_device(), force, &plan, &mcfg, true);
+        if (rc != SMD_OK) return rc;
+        CallArgs a{};
+        a.q = nullptr;
+        a.q16 = q16;
+        a.kv = kv_pool;
+        a.N = N;
+        a.indices = indices;
+        a.W = W;
+        a.counts = counts;
+        a.B = B;
+        a.H = H;
+        a.scale_log2 = scale_log2_of(sm_scale, 1.0f, k_scale);  // 2^-k per head on the GPU
+        a.k_scale = k_scale;
+        a.out = out;
+        a.lse = lse;
+        a.status = status;
+        return launch_mma(a, mcfg, reinterpret_cast<cudaStream_t>(stream));
     }
 
     smd_plan_t plan{};
@@ -486,6 +512,35 @@ int smd_sparse_mla_decode_ex(const uint8_t* q, const uint8_t* kv_pool, int64_t N
                              const smd_plan_t* force) {
     return smd::decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale, out,
                        lse, status, workspace, workspace_bytes, stream, force);
+}
+
+int smd_sparse_mla_decode_bf16q(const uint16_t* q, const uint8_t* kv_pool, int64_t N,
+                                const int32_t* indices, int32_t W, const int32_t* counts,
+                                int32_t B, int32_t H, float sm_scale, float k_scale,
+                                uint16_t* out, float* lse, int32_t* status, smd_stream_t stream) {
+    return smd::decode(reinterpret_cast<const uint8_t*>(q), kv_pool, N, indices, W, counts, B, H,
+                       sm_scale, 1.0f, k_scale, out, lse, status, nullptr, 0, stream, nullptr,
+                       false, 1, q);
+}
+
+int smd_sparse_mla_decode_bf16q_ex(const uint16_t* q, const uint8_t* kv_pool, int64_t N,
+                                   const int32_t* indices, int32_t W, const int32_t* counts,
+                                   int32_t B, int32_t H, float sm_scale, float k_scale,
+                                   uint16_t* out, float* lse, int32_t* status,
+                                   smd_stream_t stream, const smd_plan_t* force) {
+    return smd::decode(reinterpret_cast<const uint8_t*>(q), kv_pool, N, indices, W, counts, B, H,
+                       sm_scale, 1.0f, k_scale, out, lse, status, nullptr, 0, stream, force,
+                       false, 1, q);
+}
+
+int smd_plan_bf16q(int32_t B, int32_t H, int32_t W, smd_plan_t* plan) {
+    if (!plan) return SMD_ERR_NULL;
+    if (B < 0 || W < 0 || H <= 0 || H % smd::kHeadsPerTile != 0) return SMD_ERR_SHAPE;
+    smd_plan_t p{};
+    smd::MmaConfig cfg{};
+    const int rc = smd::plan_mma(B, H, W, smd::sm_count_of_device(), nullptr, &p, &cfg, true);
+    if (rc == SMD_OK) *plan = p;
+    return rc;
 }
 
 int smd_sparse_mla_decode_noalloc(const uint8_t* q, const uint8_t* kv_pool, int64_t N,

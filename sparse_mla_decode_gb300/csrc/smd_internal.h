@@ -32,11 +32,12 @@ struct CallArgs {
     uint16_t* out;
     float* lse;
     int32_t* status;
+    const uint16_t* q16;  // bf16 query [B, H, 576] (the split-query call), else null
 };
 
 // Shared-memory carve-up of the warp-MMA kernel (byte offsets).
 struct MmaLayout {
-    int32_t kv, q, logits, probs, idx, inbox, sums, maxima, wmax, lsum, rowmax, bars;
+    int32_t kv, q, logits, probs, idx, inbox, sums, maxima, wmax, lsum, rowmax, lamh, bars;
     int32_t logit_pitch;  // floats per logits row
     int32_t prob_pitch;   // bytes per P8 row
     int32_t total;
@@ -45,9 +46,10 @@ struct MmaLayout {
 __host__ __device__ inline int32_t align_up(int32_t x, int32_t a) { return (x + a - 1) / a * a; }
 
 // idx_cap: int32 entries of the index staging area (the CTA's keys, or the
-// row's whole list when it is loaded speculatively).
+// row's whole list when it is loaded speculatively). qsplit: the query is
+// held as two E4M3 tiles (hi, then lo) with a logit scale per head.
 __host__ __device__ inline MmaLayout mma_layout(int tiles, int split, int window, int key_cap,
-                                                int idx_cap) {
+                                                int idx_cap, bool qsplit = false) {
     MmaLayout L{};
     const int ch = kHeadsPerTile * tiles;
     int32_t o = 0;
@@ -55,7 +57,7 @@ __host__ __device__ inline MmaLayout mma_layout(int tiles, int split, int window
     o += window * kRowPitch;
     o = align_up(o, 128);
     L.q = o;
-    o += ch * kRowPitch;
+    o += ch * kRowPitch * (qsplit ? 2 : 1);
     o = align_up(o, 16);
     L.logit_pitch = key_cap + 8;  // rows 8 banks apart for the float2 stores
     L.logits = o;
@@ -80,6 +82,8 @@ __host__ __device__ inline MmaLayout mma_layout(int tiles, int split, int window
     o += ch * 4;
     L.rowmax = o; // [ch] the row maximum
     o += ch * 4;
+    L.lamh = o;   // [ch] per-head logit scale (split query)
+    o += ch * 4;
     o = align_up(o, 8);
     L.bars = o;   // window/64 gather barriers, q, maxima, inbound
     o += 8 * (window / kChunk + 3);
@@ -94,6 +98,7 @@ struct MmaConfig {
     uint64_t wait_budget_ns;
     int inject_stall;
     int spec_idx;
+    int qsplit;  // 1: bf16 query (CallArgs::q16), split into E4M3 hi + lo
 };
 
 // Launches the warp-MMA kernel; returns an smd_status.

@@ -30,6 +30,8 @@
 #include <cmath>
 #include <cstdint>
 
+#include <cuda_fp16.h>
+
 #include "smd_internal.h"
 #include "smd_ptx.cuh"
 
@@ -75,7 +77,77 @@ __device__ __forceinline__ void gather_chunk(const MmaParams& p, uint32_t slot_s
     }
 }
 
-template <int T>
+// The E4M3 values of two codes (exact in f16, then f32).
+__device__ __forceinline__ float2 e4m3x2_values(uint16_t codes) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
+    return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
+
+// The split query (the mla_attn page's q_split, "E4M3 hi, lo of q 2^k"): warp w
+// takes heads w, w + 16, ... of the CTA's CH; per head the largest k with
+// amax 2^k <= 448 (k = 0 for a zero row; clamped to [-32, 32]),
+// hi = E4M3(q 2^k) and lo = E4M3(q 2^k - hi) (both round-to-nearest-even,
+// saturating; q 2^k and q 2^k - hi are exact in fp32) into the two query
+// tiles, and the head's logit scale lam0 2^-k.
+template <int CH>
+__device__ __forceinline__ void split_query(const MmaParams& p, int b, int head0, uint8_t* q_hi,
+                                            uint8_t* q_lo, float* lamh) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int kPieces = kRow / 8;  // 16-byte pieces of a bf16 row
+    for (int hh = warp; hh < CH; hh += kMmaThreads / 32) {
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.a.q16 + (static_cast<int64_t>(b) * p.a.H + head0 + hh) * kRow);
+        uint4 v[3];
+        float amax = 0.f;
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+            const int piece = lane + 32 * u;
+            v[u] = piece < kPieces ? __ldg(src + piece) : make_uint4(0u, 0u, 0u, 0u);
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)),
+                                         fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+        }
+        amax = warp_max(amax);
+        int k = 0;
+        if (amax > 0.f) {
+            int e = 0;
+            const float m = frexpf(amax, &e);  // amax = m 2^e, m in [0.5, 1)
+            k = (m <= 0.875f) ? 9 - e : 8 - e;
+            k = max(-32, min(32, k));
+        }
+        const float up = __int_as_float((127 + k) << 23);  // 2^k
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+            const int piece = lane + 32 * u;
+            if (piece >= kPieces) continue;
+            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+            uint32_t hw[2], lw[2];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float x0 = __uint_as_float(w[i] << 16) * up;
+                const float x1 = __uint_as_float(w[i] & 0xFFFF0000u) * up;
+                const uint16_t hc = e4m3x2(x0, x1);
+                const float2 hv = e4m3x2_values(hc);
+                const uint16_t lc = e4m3x2(x0 - hv.x, x1 - hv.y);
+                if (i & 1) {
+                    hw[i >> 1] |= static_cast<uint32_t>(hc) << 16;
+                    lw[i >> 1] |= static_cast<uint32_t>(lc) << 16;
+                } else {
+                    hw[i >> 1] = hc;
+                    lw[i >> 1] = lc;
+                }
+            }
+            *reinterpret_cast<uint2*>(q_hi + hh * kRowPitch + 8 * piece) = make_uint2(hw[0], hw[1]);
+            *reinterpret_cast<uint2*>(q_lo + hh * kRowPitch + 8 * piece) = make_uint2(lw[0], lw[1]);
+        }
+        if (lane == 0) lamh[hh] = p.a.scale_log2 * __int_as_float((127 - k) << 23);
+    }
+}
+
+template <int T, bool QS>
 __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int CH = kHeadsPerTile * T;
@@ -137,7 +209,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         mbar_arrive_expect_tx(in_bar, (S - 1) * (CH * CW * 4 + CH * 4));
         // (inject_stall: the barrier also expects 16 bytes nobody sends, so
         // the bounded wait below runs out; a test hook for the timeout path.)
-        mbar_arrive_expect_tx(q_bar, CH * kRow + (p.inject_stall ? 16 : 0));
+        mbar_arrive_expect_tx(q_bar, (QS ? 0 : CH * kRow) + (p.inject_stall ? 16 : 0));
     }
     for (int h = tid; h < CH; h += kMmaThreads) lsum[h] = 0.f;
     __syncthreads();
@@ -145,7 +217,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     if (S > 1) cluster_arrive_relaxed();
 
     // The query rows depend on nothing: their copies go first.
-    if (tid < CH) {
+    float* lamh = reinterpret_cast<float*>(smem + p.L.lamh);
+    if constexpr (QS) {
+        split_query<CH>(p, b, head0, smem + p.L.q, smem + p.L.q + CH * kRowPitch, lamh);
+    } else if (tid < CH) {
         const uint8_t* src = p.a.q + (static_cast<int64_t>(b) * p.a.H + head0 + tid) * kRow;
         bulk_g2s(q_s + tid * kRowPitch, src, kRow, q_bar);
     }
@@ -221,15 +296,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
                 mma_e4m3(c1[0], qb, kb0[2], kb0[3]);
                 mma_e4m3(c0[1], qa, kb1[0], kb1[1]);
                 mma_e4m3(c1[1], qb, kb1[2], kb1[3]);
+                if constexpr (QS) {  // the lo tile into the same accumulators
+                    ldsm_x4(qaddr + CH * kRowPitch + 64 * kp, qa);
+                    ldsm_x4(qaddr + CH * kRowPitch + 64 * kp + 32, qb);
+                    mma_e4m3(c0[0], qa, kb0[0], kb0[1]);
+                    mma_e4m3(c1[0], qb, kb0[2], kb0[3]);
+                    mma_e4m3(c0[1], qa, kb1[0], kb1[1]);
+                    mma_e4m3(c1[1], qb, kb1[2], kb1[3]);
+                }
             }
 #pragma unroll
             for (int n = 0; n < 2; ++n) {
                 const int kk = 16 * kg + 8 * n + 2 * qd;  // within the chunk
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
-                    const float s0 = (kk < cnt) ? lam * (c0[n][2 * r] + c1[n][2 * r]) : neg_inf;
+                    const float lr = QS ? lamh[16 * t + g + 8 * r] : lam;
+                    const float s0 = (kk < cnt) ? lr * (c0[n][2 * r] + c1[n][2 * r]) : neg_inf;
                     const float s1 =
-                        (kk + 1 < cnt) ? lam * (c0[n][2 * r + 1] + c1[n][2 * r + 1]) : neg_inf;
+                        (kk + 1 < cnt) ? lr * (c0[n][2 * r + 1] + c1[n][2 * r + 1]) : neg_inf;
                     float2* dst = reinterpret_cast<float2*>(
                         logits + (16 * t + g + 8 * r) * LP + c * kChunk + kk);
                     *dst = make_float2(s0, s1);
@@ -455,13 +539,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
 
 // Function attributes are set once per device and kernel (and again only when
 // a launch needs more shared memory than was granted before).
-template <int T>
+template <int T, bool QS>
 int ensure_attributes(int smem_bytes, bool nonportable) {
     static std::atomic<int> smem_set[kMaxDevices];
     static std::atomic<int> np_set[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SMD_ERR_DEVICE;
-    auto kern = mma_decode_kernel<T>;
+    auto kern = mma_decode_kernel<T, QS>;
     if (smem_bytes > smem_set[dev].load()) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
             cudaSuccess)
@@ -477,10 +561,10 @@ int ensure_attributes(int smem_bytes, bool nonportable) {
     return SMD_OK;
 }
 
-template <int T>
+template <int T, bool QS>
 int launch_t(const MmaParams& prm, const MmaConfig& cfg, const CallArgs& a, cudaStream_t stream) {
-    auto kern = mma_decode_kernel<T>;
-    const int rc = ensure_attributes<T>(cfg.layout.total, cfg.split > 8);
+    auto kern = mma_decode_kernel<T, QS>;
+    const int rc = ensure_attributes<T, QS>(cfg.layout.total, cfg.split > 8);
     if (rc != SMD_OK) return rc;
     cudaError_t err;
     cudaLaunchConfig_t lc{};
@@ -517,11 +601,16 @@ int launch_mma(const CallArgs& a, const MmaConfig& cfg, cudaStream_t stream) {
     prm.budget_ns = cfg.wait_budget_ns;
     prm.inject_stall = cfg.inject_stall;
     prm.spec_idx = cfg.spec_idx;
-    switch (cfg.tiles) {
-        case 1:
-            return launch_t<1>(prm, cfg, a, stream);
+    if (cfg.qsplit && a.q16 == nullptr) return SMD_ERR_NULL;
+    switch (cfg.tiles * 2 + (cfg.qsplit ? 1 : 0)) {
         case 2:
-            return launch_t<2>(prm, cfg, a, stream);
+            return launch_t<1, false>(prm, cfg, a, stream);
+        case 3:
+            return launch_t<1, true>(prm, cfg, a, stream);
+        case 4:
+            return launch_t<2, false>(prm, cfg, a, stream);
+        case 5:
+            return launch_t<2, true>(prm, cfg, a, stream);
         default:
             return SMD_ERR_PLAN;
     }

@@ -235,3 +235,45 @@ def test_grouped_plan_rejects_lists_beyond_the_cluster():
     with pytest.raises(smd.SmdError) as e:
         smd.smd_plan_grouped(4, 16, 16 * 2048 + 1, 4)
     assert e.value.status == smd.SMD_ERR_SHAPE
+
+
+def call_bf16q(q=A, kv=A, N=100, idx=A, W=8, counts=A, B=2, H=16, out=A, lse=A, status=0,
+               force=None):
+    if force is None:
+        return smd.smd_sparse_mla_decode_bf16q(q, kv, N, idx, W, counts, B, H, 0.1, 0.1,
+                                               out, lse, status, 0)
+    return smd.smd_sparse_mla_decode_bf16q_ex(q, kv, N, idx, W, counts, B, H, 0.1, 0.1,
+                                              out, lse, status, 0, force)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=17), smd.SMD_ERR_SHAPE),
+    (dict(N=0), smd.SMD_ERR_SHAPE),
+    (dict(q=0), smd.SMD_ERR_NULL),
+    (dict(counts=0), smd.SMD_ERR_NULL),
+    (dict(q=A + 8), smd.SMD_ERR_ALIGN),
+    (dict(out=A + 2), smd.SMD_ERR_ALIGN),
+    (dict(B=0, q=0, out=0, lse=0, counts=0, idx=0, kv=0), smd.SMD_OK),
+])
+def test_bf16q_argument_checks(kw, code):
+    assert call_bf16q(**kw) == code
+
+
+@pytest.mark.parametrize("force", [dict(kernel=2), dict(kernel=5), dict(split=3), dict(tiles=3),
+                                   dict(window=65)])
+def test_bf16q_invalid_forced_plans_are_rejected(force):
+    p = smd.SmdPlan()
+    for k, v in force.items():
+        setattr(p, k, v)
+    assert call_bf16q(force=p) == smd.SMD_ERR_PLAN
+
+
+@pytest.mark.parametrize("B,H,W", [(5, 64, 256), (64, 128, 2048), (2, 16, 8192), (3, 48, 100)])
+def test_bf16q_plan_runs_the_warp_mma_kernel_with_both_query_tiles(B, H, W):
+    p = smd.smd_plan_bf16q(B, H, W)
+    e = smd.smd_plan(B, H, W) if not (H % 128 == 0 and W <= 2048) else None
+    assert p.kernel == smd.SMD_KERNEL_MMA
+    assert p.split * p.key_cap >= W and p.smem_bytes <= 227 * 1024
+    if e is not None and e.split == p.split and e.window == p.window:
+        # the second query tile (16 x tiles rows of 592 bytes) is the only growth
+        assert p.smem_bytes >= e.smem_bytes + 16 * p.tiles * 592 - 128
