@@ -351,3 +351,44 @@ def seeded_permutation(seed: int, n: int) -> np.ndarray:
 __all__ = ["Case", "CONFIGS", "config", "random_case", "algorithmic_bytes",
            "to_e4m3", "to_bf16_values", "ROW", "LATENT", "E4M3_MAX",
            "seeded_permutation"]
+
+
+@dataclasses.dataclass
+class TopkCase:
+    """Inputs of the top-k select: bf16 logits (bits) [B, L] and row lengths."""
+    name: str
+    logits: np.ndarray    # uint16 [B, L] bf16 bits
+    row_ends: np.ndarray  # int32 [B]
+    K: int
+
+    @property
+    def B(self) -> int:
+        return int(self.logits.shape[0])
+
+    @property
+    def L(self) -> int:
+        return int(self.logits.shape[1])
+
+
+def topk_case(seed: int, B: int, L: int, K: int, row_ends=None, scale: float = 1.0,
+              nan_frac: float = 0.0) -> TopkCase:
+    """bf16 logits N(0, scale^2) (a small scale makes many equal values), a
+    fraction of NaNs at random places; row lengths uniform in [K / 2, L]
+    unless given."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((B, L), dtype=np.float32) * np.float32(scale)
+    if nan_frac > 0:
+        x[rng.random((B, L)) < nan_frac] = np.nan
+    bits = (np.ascontiguousarray(to_bf16_values(x), np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    if row_ends is None:
+        ends = rng.integers(max(1, K // 2), L + 1, size=B).astype(np.int32)
+    else:
+        ends = np.asarray(row_ends, np.int32)
+    return TopkCase(f"topk{seed}", bits, ends, int(K))
+
+
+def topk_config() -> TopkCase:
+    """The indexer's select at DSA decode: 64 rows of bf16 logits over up to
+    65536 cached tokens (row lengths uniform in [1024, 65536]), top-k 2048."""
+    return topk_case(7, 64, 65536, 2048, scale=1.0,
+                     row_ends=np.random.default_rng(8).integers(1024, 65537, size=64))
