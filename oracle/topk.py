@@ -14,8 +14,9 @@ read for one GPU, without the exchange's packing):
     key      o_i = the bf16 bits mapped to an unsigned 16-bit key whose order
              is the order of the values: bits | 0x8000 for a positive sign,
              ~bits for a negative one (so -0 sorts just below +0)
-    if at most K logits are valid: all valid i, ascending
-    else     v = the K-th largest key among the valid ones;
+    if fewer than K logits are valid: all valid i, ascending
+    else     v = the K-th largest key among the valid ones (the page finds it
+             whenever the histogram's running count reaches K);
              first every i with o_i > v (ascending i), then the i with o_i == v
              in ascending order until K are taken
   count[r] = min(K, number of valid logits); entries past the count are -1.
@@ -44,7 +45,7 @@ def select_row(bits: np.ndarray, K: int) -> np.ndarray:
     order."""
     key, valid = order_keys(bits)
     idx = np.nonzero(valid)[0]
-    if idx.size <= K:
+    if idx.size < K:
         return idx.astype(np.int32)
     v = np.sort(key[idx])[::-1][K - 1]  # the K-th largest key
     gt = np.nonzero(valid & (key > v))[0]

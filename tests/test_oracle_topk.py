@@ -70,10 +70,17 @@ def test_nan_is_never_selected_and_short_rows_return_every_valid_index():
     assert idx[0].tolist() == [2, 0]
 
 
+def test_exactly_k_valid_takes_the_threshold_order():
+    """K valid logits: the threshold is the smallest, so it goes last."""
+    bits = bits_of([5.0, 1.0, 7.0])
+    idx, cnt = ot.topk_select(bits[None], 3)
+    assert cnt[0] == 3 and idx[0].tolist() == [0, 2, 1]
+
+
 def test_row_end_and_signed_zero_and_infinities():
     bits = bits_of([0.0, -0.0, float("-inf"), float("inf"), 9.0, 8.0])
     idx, cnt = ot.topk_select(np.stack([bits, bits]), 2, row_ends=[4, -3])
     assert idx[0].tolist() == [3, 0]      # +inf, then +0 above -0
     assert cnt[1] == 0 and idx[1].tolist() == [-1, -1]
-    idx, cnt = ot.topk_select(bits[None], 6, row_ends=[99])
-    assert sorted(idx[0].tolist()) == list(range(6))  # every logit (end clamped to L)
+    idx, cnt = ot.topk_select(bits[None], 7, row_ends=[99])
+    assert idx[0].tolist() == [0, 1, 2, 3, 4, 5, -1]  # every logit (end clamped to L)
