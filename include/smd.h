@@ -252,6 +252,32 @@ int smd_sparse_mla_decode_bf16q_ex(const uint16_t* q, const uint8_t* kv_pool, in
 /* The plan smd_sparse_mla_decode_bf16q would use. Host only. */
 int smd_plan_bf16q(int32_t B, int32_t H, int32_t W, smd_plan_t* plan);
 
+/* Top-k select over bf16 logits, producing the decode's index list and
+ * count on the device (the topk_exchange page: the select of
+ * push_local_topk, its radix passes, threshold and tie rule, for one GPU).
+ * For row r, over its first end = clamp(row_ends[r], 0, L) logits (all L when
+ * row_ends is NULL):
+ *   a logit is valid unless it is a NaN; its key is the bf16 bit pattern
+ *   mapped to an unsigned 16-bit number in value order (bits | 0x8000 for a
+ *   positive sign, ~bits for a negative one, so -0 sorts just below +0);
+ *   v = the K-th largest key among the valid logits;
+ *   indices[r] = every position with key > v in ascending order, then the
+ *   positions with key == v in ascending order until K are taken;
+ *   a row with fewer than K valid logits gets all of them in ascending order;
+ *   counts[r] = min(K, valid logits); indices[r][counts[r] .. K) = -1.
+ * One CTA per row: a row of up to 98304 logits is read from HBM once.
+ *   logits     [B, row_stride] bf16 bits, row_stride >= L, 2-byte aligned.
+ *              Read only. With 16-byte aligned rows (logits 16-byte aligned,
+ *              row_stride a multiple of 8) the rows are read in 16-byte
+ *              pieces, up to round_up(L, 8) logits a row.
+ *   row_ends   [B] int32 or NULL.
+ *   indices    [B, K] int32 (row stride K); counts [B] int32. Written.
+ * B >= 0 (0: no-op), L >= 0, K >= 1; otherwise SMD_ERR_SHAPE. All pointers
+ * are caller-owned device memory; asynchronous on `stream`. */
+int smd_topk_select(const uint16_t* logits, int64_t row_stride, const int32_t* row_ends,
+                    int32_t B, int32_t L, int32_t K, int32_t* indices, int32_t* counts,
+                    smd_stream_t stream);
+
 /* The decode for rows that come in groups sharing one index list: the
  * verify rows of a multi-token decode step, where row i of a request sees the
  * first L - G + 1 + i tokens of its cache (the attn_sparse page's verify rows;

@@ -91,6 +91,10 @@ def lib() -> ctypes.CDLL:
             so.smd_sparse_mla_decode_bf16q_ex.argtypes = bq_args + [ctypes.POINTER(SmdPlan)]
             so.smd_plan_bf16q.restype = ctypes.c_int
             so.smd_plan_bf16q.argtypes = [ctypes.c_int32] * 3 + [ctypes.POINTER(SmdPlan)]
+            so.smd_topk_select.restype = ctypes.c_int
+            so.smd_topk_select.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
             so.smd_plan_grouped.restype = ctypes.c_int
             so.smd_plan_grouped.argtypes = [ctypes.c_int32] * 4 + [ctypes.POINTER(SmdPlan)]
             so.smd_workspace_bytes.restype = ctypes.c_int64
@@ -192,6 +196,10 @@ def smd_plan_bf16q(B: int, H: int, W: int) -> SmdPlan:
     if rc != SMD_OK:
         raise SmdError(rc, "smd_plan_bf16q")
     return p
+
+
+def smd_topk_select(logits, row_stride, row_ends, B, L, K, indices, counts, stream) -> int:
+    return lib().smd_topk_select(logits, row_stride, row_ends, B, L, K, indices, counts, stream)
 
 
 def smd_workspace_bytes(B: int, H: int, W: int) -> int:
@@ -365,3 +373,36 @@ def sparse_mla_decode_bf16q(q, kv_pool, indices, counts, sm_scale: float, k_scal
     if rc != SMD_OK:
         raise SmdError(rc, "smd_sparse_mla_decode_bf16q")
     return out, lse
+
+
+def topk_select(logits, K: int, row_ends=None, indices=None, counts=None, stream=None):
+    """Top-k select on the GPU (smd_topk_select). logits: bfloat16 CUDA tensor
+    [B, L] with unit column stride (a column slice of a wider tensor is fine;
+    16-byte aligned rows are read fastest); row_ends: optional
+    int32 [B]. Returns (indices int32 [B, K], counts int32 [B]), ready to be
+    the decode's index list and counts."""
+    import torch
+
+    if logits.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"logits: expected bfloat16, got {logits.dtype}")
+    if not logits.is_cuda:
+        raise ValueError("logits must be a CUDA tensor (the select has no CPU path)")
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be [B, L] with unit column stride")
+    B, L = int(logits.shape[0]), int(logits.shape[1])
+    stride = int(logits.stride(0)) if B > 1 else L
+    if row_ends is not None and (row_ends.dtype != torch.int32 or not row_ends.is_cuda):
+        raise TypeError("row_ends must be an int32 CUDA tensor")
+    if indices is None:
+        indices = torch.empty((B, K), dtype=torch.int32, device=logits.device)
+    if counts is None:
+        counts = torch.empty((B,), dtype=torch.int32, device=logits.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(logits.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = smd_topk_select(_ptr(logits), stride, _ptr(row_ends), B, L, int(K), _ptr(indices),
+                         _ptr(counts), int(stream))
+    if rc != SMD_OK:
+        raise SmdError(rc, "smd_topk_select")
+    return indices, counts

@@ -622,6 +622,19 @@ int smd_plan_grouped(int32_t B, int32_t H, int32_t W, int32_t row_group, smd_pla
     return rc;
 }
 
+int smd_topk_select(const uint16_t* logits, int64_t row_stride, const int32_t* row_ends,
+                    int32_t B, int32_t L, int32_t K, int32_t* indices, int32_t* counts,
+                    smd_stream_t stream) {
+    if (B < 0 || L < 0 || K < 1 || row_stride < L) return SMD_ERR_SHAPE;
+    if (B == 0) return SMD_OK;
+    if (!indices || !counts || (L > 0 && !logits)) return SMD_ERR_NULL;
+    if ((logits && !smd::aligned(logits, 2)) || !smd::aligned(indices, 4) ||
+        !smd::aligned(counts, 4) || (row_ends && !smd::aligned(row_ends, 4)))
+        return SMD_ERR_ALIGN;
+    return smd::launch_topk(logits, row_stride, row_ends, B, L, K, indices, counts,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
 float smd_scale_log2(float sm_scale, float q_scale, float k_scale) {
     return smd::scale_log2_of(sm_scale, q_scale, k_scale);
 }

@@ -381,7 +381,7 @@ def topk_case(seed: int, B: int, L: int, K: int, row_ends=None, scale: float = 1
         x[rng.random((B, L)) < nan_frac] = np.nan
     bits = (np.ascontiguousarray(to_bf16_values(x), np.float32).view(np.uint32) >> 16).astype(np.uint16)
     if row_ends is None:
-        ends = rng.integers(max(1, K // 2), L + 1, size=B).astype(np.int32)
+        ends = rng.integers(max(1, min(K // 2, L)), L + 1, size=B).astype(np.int32)
     else:
         ends = np.asarray(row_ends, np.int32)
     return TopkCase(f"topk{seed}", bits, ends, int(K))

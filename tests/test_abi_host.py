@@ -277,3 +277,23 @@ def test_bf16q_plan_runs_the_warp_mma_kernel_with_both_query_tiles(B, H, W):
     if e is not None and e.split == p.split and e.window == p.window:
         # the second query tile (16 x tiles rows of 592 bytes) is the only growth
         assert p.smem_bytes >= e.smem_bytes + 16 * p.tiles * 592 - 128
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=0), smd.SMD_ERR_SHAPE),
+    (dict(L=-1), smd.SMD_ERR_SHAPE),
+    (dict(B=-1), smd.SMD_ERR_SHAPE),
+    (dict(stride=8, L=16), smd.SMD_ERR_SHAPE),  # shorter than a row
+    (dict(logits=0), smd.SMD_ERR_NULL),
+    (dict(indices=0), smd.SMD_ERR_NULL),
+    (dict(counts=0), smd.SMD_ERR_NULL),
+    (dict(logits=A + 1), smd.SMD_ERR_ALIGN),
+    (dict(indices=A + 2), smd.SMD_ERR_ALIGN),
+    (dict(row_ends=A + 1), smd.SMD_ERR_ALIGN),
+    (dict(B=0, logits=0, indices=0, counts=0), smd.SMD_OK),
+])
+def test_topk_select_argument_checks(kw, code):
+    args = dict(logits=A, stride=64, row_ends=0, B=2, L=64, K=8, indices=A, counts=A)
+    args.update(kw)
+    assert smd.smd_topk_select(args["logits"], args["stride"], args["row_ends"], args["B"],
+                               args["L"], args["K"], args["indices"], args["counts"], 0) == code
