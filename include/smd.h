@@ -265,18 +265,28 @@ int smd_plan_bf16q(int32_t B, int32_t H, int32_t W, smd_plan_t* plan);
  *   positions with key == v in ascending order until K are taken;
  *   a row with fewer than K valid logits gets all of them in ascending order;
  *   counts[r] = min(K, valid logits); indices[r][counts[r] .. K) = -1.
- * One CTA per row: a row of up to 98304 logits is read from HBM once.
+ * A row is split over a cluster of up to 8 CTAs; a part of up to 16384
+ * logits is read from HBM once (longer parts are read again from L2).
  *   logits     [B, row_stride] bf16 bits, row_stride >= L, 2-byte aligned.
  *              Read only. With 16-byte aligned rows (logits 16-byte aligned,
  *              row_stride a multiple of 8) the rows are read in 16-byte
  *              pieces, up to round_up(L, 8) logits a row.
  *   row_ends   [B] int32 or NULL.
  *   indices    [B, K] int32 (row stride K); counts [B] int32. Written.
+ *   status     optional device int32: a bounded wait on a peer CTA that ran
+ *              out writes SMD_ERR_TIMEOUT there.
  * B >= 0 (0: no-op), L >= 0, K >= 1; otherwise SMD_ERR_SHAPE. All pointers
  * are caller-owned device memory; asynchronous on `stream`. */
 int smd_topk_select(const uint16_t* logits, int64_t row_stride, const int32_t* row_ends,
                     int32_t B, int32_t L, int32_t K, int32_t* indices, int32_t* counts,
-                    smd_stream_t stream);
+                    int32_t* status, smd_stream_t stream);
+
+/* As smd_topk_select with the CTAs per row forced (`cluster` 1, 2, 4 or 8;
+ * 0 = automatic; else SMD_ERR_PLAN). The split only lays work out: every
+ * value gives the same indices and counts. For the tests. */
+int smd_topk_select_ex(const uint16_t* logits, int64_t row_stride, const int32_t* row_ends,
+                       int32_t B, int32_t L, int32_t K, int32_t* indices, int32_t* counts,
+                       int32_t* status, smd_stream_t stream, int32_t cluster);
 
 /* The decode for rows that come in groups sharing one index list: the
  * verify rows of a multi-token decode step, where row i of a request sees the

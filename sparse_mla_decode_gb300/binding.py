@@ -92,9 +92,12 @@ def lib() -> ctypes.CDLL:
             so.smd_plan_bf16q.restype = ctypes.c_int
             so.smd_plan_bf16q.argtypes = [ctypes.c_int32] * 3 + [ctypes.POINTER(SmdPlan)]
             so.smd_topk_select.restype = ctypes.c_int
-            so.smd_topk_select.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
-                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                           ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+            tk_args = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32,
+                       ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                       ctypes.c_void_p, ctypes.c_void_p]
+            so.smd_topk_select.argtypes = tk_args
+            so.smd_topk_select_ex.restype = ctypes.c_int
+            so.smd_topk_select_ex.argtypes = tk_args + [ctypes.c_int32]
             so.smd_plan_grouped.restype = ctypes.c_int
             so.smd_plan_grouped.argtypes = [ctypes.c_int32] * 4 + [ctypes.POINTER(SmdPlan)]
             so.smd_workspace_bytes.restype = ctypes.c_int64
@@ -198,8 +201,16 @@ def smd_plan_bf16q(B: int, H: int, W: int) -> SmdPlan:
     return p
 
 
-def smd_topk_select(logits, row_stride, row_ends, B, L, K, indices, counts, stream) -> int:
-    return lib().smd_topk_select(logits, row_stride, row_ends, B, L, K, indices, counts, stream)
+def smd_topk_select(logits, row_stride, row_ends, B, L, K, indices, counts, status,
+                    stream) -> int:
+    return lib().smd_topk_select(logits, row_stride, row_ends, B, L, K, indices, counts, status,
+                                 stream)
+
+
+def smd_topk_select_ex(logits, row_stride, row_ends, B, L, K, indices, counts, status, stream,
+                       cluster) -> int:
+    return lib().smd_topk_select_ex(logits, row_stride, row_ends, B, L, K, indices, counts,
+                                    status, stream, cluster)
 
 
 def smd_workspace_bytes(B: int, H: int, W: int) -> int:
@@ -375,7 +386,8 @@ def sparse_mla_decode_bf16q(q, kv_pool, indices, counts, sm_scale: float, k_scal
     return out, lse
 
 
-def topk_select(logits, K: int, row_ends=None, indices=None, counts=None, stream=None):
+def topk_select(logits, K: int, row_ends=None, indices=None, counts=None, stream=None,
+                status=None, cluster: int = 0):
     """Top-k select on the GPU (smd_topk_select). logits: bfloat16 CUDA tensor
     [B, L] with unit column stride (a column slice of a wider tensor is fine;
     16-byte aligned rows are read fastest); row_ends: optional
@@ -401,8 +413,8 @@ def topk_select(logits, K: int, row_ends=None, indices=None, counts=None, stream
         stream = torch.cuda.current_stream(logits.device).cuda_stream
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
-    rc = smd_topk_select(_ptr(logits), stride, _ptr(row_ends), B, L, int(K), _ptr(indices),
-                         _ptr(counts), int(stream))
+    rc = smd_topk_select_ex(_ptr(logits), stride, _ptr(row_ends), B, L, int(K), _ptr(indices),
+                            _ptr(counts), _ptr(status), int(stream), int(cluster))
     if rc != SMD_OK:
         raise SmdError(rc, "smd_topk_select")
     return indices, counts

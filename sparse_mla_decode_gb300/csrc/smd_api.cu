@@ -622,17 +622,36 @@ int smd_plan_grouped(int32_t B, int32_t H, int32_t W, int32_t row_group, smd_pla
     return rc;
 }
 
-int smd_topk_select(const uint16_t* logits, int64_t row_stride, const int32_t* row_ends,
-                    int32_t B, int32_t L, int32_t K, int32_t* indices, int32_t* counts,
-                    smd_stream_t stream) {
+int smd_topk_select_ex(const uint16_t* logits, int64_t row_stride, const int32_t* row_ends,
+                       int32_t B, int32_t L, int32_t K, int32_t* indices, int32_t* counts,
+                       int32_t* status, smd_stream_t stream, int32_t cluster) {
     if (B < 0 || L < 0 || K < 1 || row_stride < L) return SMD_ERR_SHAPE;
+    if (cluster < 0 || cluster > 8 || (cluster & (cluster - 1)) != 0) return SMD_ERR_PLAN;
     if (B == 0) return SMD_OK;
     if (!indices || !counts || (L > 0 && !logits)) return SMD_ERR_NULL;
     if ((logits && !smd::aligned(logits, 2)) || !smd::aligned(indices, 4) ||
-        !smd::aligned(counts, 4) || (row_ends && !smd::aligned(row_ends, 4)))
+        !smd::aligned(counts, 4) || (row_ends && !smd::aligned(row_ends, 4)) ||
+        (status && !smd::aligned(status, 4)))
         return SMD_ERR_ALIGN;
-    return smd::launch_topk(logits, row_stride, row_ends, B, L, K, indices, counts,
+    int C = cluster;
+    if (C == 0) {
+        // CTAs per row (a power of two, at most 8): parts whose keys stay in
+        // shared memory (16384 logits) while the CTAs fit the device at once
+        // (two per SM), then more while the SMs are not all busy.
+        const int slots = 2 * smd::sm_count_of_device();
+        C = 1;
+        while (C < 8 && (L + C - 1) / C > 16384 && static_cast<int64_t>(B) * C * 2 <= slots) C *= 2;
+        while (C < 8 && static_cast<int64_t>(B) * C * 2 <= slots / 2 && C * 4096 < L) C *= 2;
+    }
+    return smd::launch_topk(logits, row_stride, row_ends, B, L, K, indices, counts, status, C,
                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+int smd_topk_select(const uint16_t* logits, int64_t row_stride, const int32_t* row_ends,
+                    int32_t B, int32_t L, int32_t K, int32_t* indices, int32_t* counts,
+                    int32_t* status, smd_stream_t stream) {
+    return smd_topk_select_ex(logits, row_stride, row_ends, B, L, K, indices, counts, status,
+                              stream, 0);
 }
 
 float smd_scale_log2(float sm_scale, float q_scale, float k_scale) {

@@ -256,9 +256,11 @@ int tcs_smem_bytes();
 // CTAs of the spread kernel the current device holds at once (0 on failure).
 int tcs_max_grid();
 
-// Top-k select over bf16 logits (one CTA per row); returns an smd_status.
+// Top-k select over bf16 logits (a cluster of C CTAs per row, C a power of
+// two <= 8); returns an smd_status.
 int launch_topk(const uint16_t* logits, int64_t stride, const int32_t* row_ends, int32_t B,
-                int32_t L, int32_t K, int32_t* indices, int32_t* counts, cudaStream_t stream);
+                int32_t L, int32_t K, int32_t* indices, int32_t* counts, int32_t* status,
+                int C, cudaStream_t stream);
 
 // SM-id slots of the library's own static exchange scratch (GB300: 152 SMs).
 constexpr int kStaticScratchSlots = 160;

@@ -296,4 +296,10 @@ def test_topk_select_argument_checks(kw, code):
     args = dict(logits=A, stride=64, row_ends=0, B=2, L=64, K=8, indices=A, counts=A)
     args.update(kw)
     assert smd.smd_topk_select(args["logits"], args["stride"], args["row_ends"], args["B"],
-                               args["L"], args["K"], args["indices"], args["counts"], 0) == code
+                               args["L"], args["K"], args["indices"], args["counts"], 0,
+                               0) == code
+
+
+@pytest.mark.parametrize("cluster", [3, 16, -1])
+def test_topk_select_rejects_other_cluster_sizes(cluster):
+    assert smd.smd_topk_select_ex(A, 64, 0, 2, 64, 8, A, A, 0, 0, cluster) == smd.SMD_ERR_PLAN

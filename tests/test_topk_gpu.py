@@ -14,7 +14,7 @@ from sparse_mla_decode_gb300 import inputs
 pytestmark = pytest.mark.gpu
 
 
-def gpu_select(case, dev, stride=None, ends=True):
+def gpu_select(case, dev, stride=None, ends=True, cluster=0):
     import torch
     from sparse_mla_decode_gb300 import binding
     B, L = case.logits.shape
@@ -25,8 +25,10 @@ def gpu_select(case, dev, stride=None, ends=True):
         buf[:, :L] = case.logits
         x = torch.from_numpy(buf.view(np.int16)).to(dev).view(torch.bfloat16)[:, :L]
     re = torch.from_numpy(case.row_ends).to(dev) if ends else None
-    idx, cnt = binding.topk_select(x, case.K, row_ends=re)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    idx, cnt = binding.topk_select(x, case.K, row_ends=re, status=status, cluster=cluster)
     torch.cuda.synchronize()
+    assert int(status.item()) == 0
     return idx.cpu().numpy(), cnt.cpu().numpy()
 
 
@@ -36,7 +38,7 @@ CASES = [
     (2, 3, 5000, 2048, 0.01, 0.0),     # many equal values: the tie rule decides
     (3, 5, 4096, 64, 1.0, 0.3),        # NaNs
     (4, 2, 100, 512, 1.0, 0.0),        # K above the row length
-    (5, 2, 120000, 2048, 0.1, 0.01),   # longer than the shared-memory cache
+    (5, 2, 200000, 2048, 0.1, 0.01),   # parts longer than the shared-memory cache
     (6, 7, 8, 8, 1.0, 0.0),
 ]
 
@@ -52,6 +54,9 @@ def test_select_matches_the_oracle(cuda, case_args):
     idx_o2, cnt_o2 = ot.topk_select(case.logits, K)  # whole rows
     idx_g2, cnt_g2 = gpu_select(case, cuda, ends=False)
     assert np.array_equal(idx_g2, idx_o2) and np.array_equal(cnt_g2, cnt_o2)
+    for cluster in (1, 2, 8):  # the split of a row over CTAs changes nothing
+        idx_c, cnt_c = gpu_select(case, cuda, cluster=cluster)
+        assert np.array_equal(idx_c, idx_o) and np.array_equal(cnt_c, cnt_o), cluster
 
 
 def test_select_with_a_padded_row_stride(cuda):
