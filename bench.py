@@ -57,7 +57,10 @@ WORKLOAD_TEXT = {
                   "1% of rows x8",
     "dense": "dense-as-sparse: 32 requests x 4 causal rows, L U[1024,8192], H=16, pool "
              "262144x576 E4M3 shuffled",
+    "topk": "top-k select (the decode's index producer): 64 rows of bf16 logits, row lengths "
+            "U[1024,65536] of 65536, top-k 2048",
 }
+TOPK_METRIC = "top-k select µs/call and bf16-logit GB/s; % of HBM roofline"
 
 
 def peaks() -> dict:
@@ -436,6 +439,179 @@ def cpu_baseline(case, stats, seconds: float, bf16q: bool = False) -> dict:
             "kind": "oracle", "sample": sample, "us_per_call_sample": round(per_call * 1e6, 1)}
 
 
+def topk_bytes(case) -> dict:
+    """Bytes the select must move at least once: the logits before each row's
+    end, the index list and the counts."""
+    ends = np.minimum(np.maximum(case.row_ends.astype(np.int64), 0), case.L)
+    read = 2 * int(ends.sum())
+    written = 4 * case.B * case.K + 4 * case.B
+    return {"logits": read, "out": written, "total": read + written}
+
+
+def run_topk(args, world, rank, local) -> dict | None:
+    """The select on the GPU: one step = one smd_topk_select call over every row."""
+    import torch
+    from sparse_mla_decode_gb300 import binding, inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    case = inputs.topk_config()
+    stats = topk_bytes(case)
+    x = torch.from_numpy(case.logits.view(np.int16)).to(dev).view(torch.bfloat16)
+    ends = torch.from_numpy(case.row_ends).to(dev)
+    idx = torch.empty((case.B, case.K), dtype=torch.int32, device=dev)
+    cnt = torch.empty((case.B,), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush_w = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.empty((), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ptrs = (x.data_ptr(), case.L, ends.data_ptr(), case.B, case.L, case.K, idx.data_ptr(),
+            cnt.data_ptr(), status.data_ptr(), stream.cuda_stream)
+
+    def select():
+        rc = binding.smd_topk_select(*ptrs)
+        if rc != 0:
+            raise binding.SmdError(rc, "select")
+
+    def l2_flush():
+        flush_w.zero_()
+        torch.sum(flush, dim=0, out=flush_out)
+
+    for _ in range(max(args.warmup, 3)):
+        l2_flush()
+        select()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local).start() if rank == 0 else None
+    time.sleep(0.2 if sampler else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        l2_flush()
+        starts[i].record(stream)
+        select()
+        stops[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop() if sampler else None
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    ms_local = float(np.mean([a.elapsed_time(b) for a, b in zip(starts, stops)]))
+    ms, value = aggregate(stats["logits"], ms_local, world, dev)
+
+    # end to end: logits and row ends from pinned host memory, indices and counts back
+    hx = torch.from_numpy(case.logits.view(np.int16)).pin_memory()
+    he = torch.from_numpy(case.row_ends).pin_memory()
+    hidx = torch.empty((case.B, case.K), dtype=torch.int32).pin_memory()
+    hcnt = torch.empty((case.B,), dtype=torch.int32).pin_memory()
+    dx = torch.empty((case.B, case.L), dtype=torch.int16, device=dev)
+    de = torch.empty_like(ends)
+
+    def e2e_step():
+        dx.copy_(hx, non_blocking=True)
+        de.copy_(he, non_blocking=True)
+        binding.topk_select(dx.view(torch.bfloat16), case.K, row_ends=de, indices=idx,
+                            counts=cnt, status=status)
+        hidx.copy_(idx, non_blocking=True)
+        hcnt.copy_(cnt, non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        l2_flush()
+        e2e_step()
+    torch.cuda.synchronize()
+    e_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        l2_flush()
+        e_starts[i].record(stream)
+        e2e_step()
+        e_stops[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = reduce_max(float(np.mean([a.elapsed_time(b) for a, b in zip(e_starts, e_stops)])),
+                        world, dev)
+    if rank != 0:
+        return None
+    pk = peaks()
+    achieved = stats["total"] / (ms * 1e-3) / 1e9
+    cpu = topk_cpu_baseline(case, stats, args.cpu_seconds)
+    return {
+        "metric": TOPK_METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+        "us_per_call": round(ms * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 keys (u16 integer compares)",
+        "data": "synthetic (seeded numpy PCG64 normal logits, bf16)",
+        "config": {"workload": WORKLOAD_TEXT["topk"], "name": "topk", "B": case.B, "L": case.L,
+                   "top_k": case.K,
+                   "l2": "flushed before every timed step (write of a 2x-L2 buffer, then read of another, outside the events)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": pk["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 5), "traffic": None,
+                     "kernel": "topk_select_kernel", "algorithmic_bytes": stats["total"],
+                     "t_roof_us": round(stats["total"] / (pk["hbm_gbs"] * 1e9) * 1e6, 4),
+                     "peak_source": pk["source"]},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * stats["logits"] / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
+                "us_per_call": round(e2e_ms * 1e3, 3),
+                "h2d_bytes_per_step": int(hx.numel() * 2 + he.numel() * 4),
+                "d2h_bytes_per_step": int(hidx.numel() * 4 + hcnt.numel() * 4),
+                "note": "logits and row ends H2D from pinned memory; indices and counts D2H"},
+        "gpu_launches": args.steps, "clocks": clocks, "wall_s_timed_region": round(wall, 4),
+    }
+
+
+def topk_cpu_baseline(case, stats, seconds: float) -> dict:
+    """The select oracle (numpy, one core) on the whole workload, repeated for
+    about `seconds`."""
+    from oracle import topk as otk
+    reps, t_total = 0, 0.0
+    while t_total < seconds or reps < 1:
+        t0 = time.perf_counter()
+        otk.topk_select(case.logits, case.K, case.row_ends)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    per_call = t_total / reps
+    return {"value": round(stats["logits"] / per_call / 1e9, 6), "unit": UNIT, "cores": 1,
+            "kind": "oracle", "sample": f"whole workload, {reps} repeats",
+            "us_per_call_sample": round(per_call * 1e6, 1)}
+
+
+def run_topk_reference(args, world, rank) -> dict | None:
+    if rank != 0:
+        return None
+    from oracle import topk as otk
+    from sparse_mla_decode_gb300 import inputs
+    case = inputs.topk_config()
+    stats = topk_bytes(case)
+    for _ in range(args.warmup):
+        otk.topk_select(case.logits, case.K, case.row_ends)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        otk.topk_select(case.logits, case.K, case.row_ends)
+        times.append(time.perf_counter() - t0)
+    ms = 1e3 * float(np.mean(times))
+    value = stats["logits"] / (ms * 1e-3) / 1e9
+    return {
+        "impl": "reference", "metric": TOPK_METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "us_per_call": round(ms * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u16 keys (numpy oracle)", "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT["topk"], "name": "topk", "B": case.B, "L": case.L,
+                   "top_k": case.K},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "whole workload per step"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args, world, rank) -> dict | None:
     if rank != 0:
         return None
@@ -494,10 +670,12 @@ def main(argv=None):
     if args.impl == "reference":
         if args.steps > 50 and args.config != "tiny":
             args.steps = 50
-        line = run_reference(args, world, rank)
+        line = (run_topk_reference(args, world, rank) if args.config == "topk"
+                else run_reference(args, world, rank))
     else:
         world, rank, local = dist_setup(args.gpus)
-        line = run_gpu(args, world, rank, local)
+        line = (run_topk(args, world, rank, local) if args.config == "topk"
+                else run_gpu(args, world, rank, local))
     if line is not None:
         print(json.dumps(line), flush=True)
     if args.impl != "reference" and world > 1:
