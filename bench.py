@@ -383,7 +383,7 @@ def run_gpu(args, world, rank, local) -> dict | None:
 
 KERNEL_FILES = {1: ("mma_decode_kernel", "smd_mma.cu"), 2: ("tc_decode_kernel", "smd_tc.cu"),
                 3: ("group_decode_kernel", "smd_group.cu"), 4: ("tcg_decode_kernel", "smd_tcg.cu"),
-                5: ("tcs_decode_kernel", "smd_tcs.cu")}
+                5: ("tcs_decode_kernel", "smd_tcs.cu"), "topk": ("topk_select_kernel", "smd_topk.cu")}
 # Workloads whose rows come in groups sharing one index list (rows per group).
 ROW_GROUP = {"dense": 4}
 
@@ -552,7 +552,8 @@ def run_topk(args, world, rank, local) -> dict | None:
                    "l2": "flushed before every timed step (write of a 2x-L2 buffer, then read of another, outside the events)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": pk["hbm_gbs"],
-                     "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 5), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 5),
+                     "traffic": load_traffic("topk", "topk"),
                      "kernel": "topk_select_kernel", "algorithmic_bytes": stats["total"],
                      "t_roof_us": round(stats["total"] / (pk["hbm_gbs"] * 1e9) * 1e6, 4),
                      "peak_source": pk["source"]},
