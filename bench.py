@@ -193,11 +193,12 @@ def run_gpu(args, world, rank, local) -> dict | None:
     plan = binding.smd_plan_grouped(case.B, case.H, case.W, group).as_dict()
     # Where the library's workspace plan (the spread kernel) applies, the
     # workspace entry point is timed with a workspace of the size it asks for.
-    ws_bytes = binding.smd_workspace_bytes(case.B, case.H, case.W) if group == 1 and not bf16q else 0
+    ws_bytes = binding.smd_workspace_bytes(case.B, case.H, case.W) if group == 1 else 0
     if ws_bytes > 0:
         plan = binding.smd_plan_ws(case.B, case.H, case.W).as_dict()
-    if bf16q:
-        plan = binding.smd_plan_bf16q(case.B, case.H, case.W).as_dict()
+    if bf16q:  # with the workspace it asks for (the spread kernel where it applies)
+        ws_bytes = binding.smd_workspace_bytes_bf16q(case.B, case.H, case.W)
+        plan = binding.smd_plan_bf16q(case.B, case.H, case.W, ws_bytes).as_dict()
 
     q = torch.from_numpy(case.q8).to(dev)
     q16 = torch.from_numpy(case.q16.view(np.int16)).to(dev).view(torch.bfloat16)
@@ -225,7 +226,10 @@ def run_gpu(args, world, rank, local) -> dict | None:
     bptrs = (q16.data_ptr(),) + ptrs[1:8] + (case.sm_scale, case.k_scale) + ptrs[11:]
 
     def decode():
-        if bf16q:
+        if bf16q and ws_bytes > 0:
+            rc = binding.smd_sparse_mla_decode_bf16q_ws(*bptrs[:-1], workspace.data_ptr(), ws_bytes,
+                                                        sptr)
+        elif bf16q:
             rc = binding.smd_sparse_mla_decode_bf16q(*bptrs)
         elif group > 1:
             rc = binding.smd_sparse_mla_decode_grouped(*gptrs)
@@ -283,7 +287,8 @@ def run_gpu(args, world, rank, local) -> dict | None:
         dcnt.copy_(hcnt, non_blocking=True)
         if bf16q:
             binding.sparse_mla_decode_bf16q(dq, kv, didx, dcnt, case.sm_scale, case.k_scale,
-                                            out=out, lse=lse, status=status)
+                                            out=out, lse=lse, status=status,
+                                            workspace=workspace if ws_bytes > 0 else None)
         else:
             binding.sparse_mla_decode(dq, kv, didx, dcnt, case.sm_scale, case.q_scale,
                                       case.k_scale, out=out, lse=lse, status=status,

@@ -230,7 +230,8 @@ int smd_sparse_mla_decode_noalloc(const uint8_t* q, const uint8_t* kv_pool, int6
  *   s_i = fp32(lambda_h * fp32(sum_c (hi_c + lo_c) * kv8[j_i, c])),
  *   lambda_h = fp32(sm_scale * 2^-k * k_scale * log2 e)
  * and everything after the logits is as in smd_sparse_mla_decode. QK costs
- * twice the MMAs. Runs on the warp-MMA kernel (any H multiple of 16).
+ * twice the MMAs. This call runs on the warp-MMA kernel (any H multiple of 16),
+ * which splits the query itself.
  *   q   [B, H, 576] bfloat16 (raw 16-bit storage), row-major, 16-byte
  *       aligned, finite. There is no q_scale: the split finds its own scale.
  * The other arguments, layouts, ownership and errors are those of
@@ -240,17 +241,40 @@ int smd_sparse_mla_decode_bf16q(const uint16_t* q, const uint8_t* kv_pool, int64
                                 int32_t B, int32_t H, float sm_scale, float k_scale,
                                 uint16_t* out, float* lse, int32_t* status, smd_stream_t stream);
 
-/* As smd_sparse_mla_decode_bf16q with plan fields (kernel SMD_KERNEL_MMA or
- * 0, split, tiles, window, the testing hooks) taken from `force` (may be
- * NULL). For the tests. */
+/* As smd_sparse_mla_decode_bf16q with a caller-owned device workspace of at
+ * least smd_workspace_bytes_bf16q(B, H, W) bytes (16-byte aligned; else
+ * SMD_ERR_WORKSPACE): when H % 128 == 0, B * H / 128 <= 1024 and W <= 16384
+ * the query is split by a first kernel into E4M3 hi and lo rows and logit
+ * scales in the workspace, and the decode runs on the spread tcgen05 kernel
+ * (SMD_KERNEL_TC_SPREAD: its query tile holds hi, its second ring slot holds
+ * lo until QK is done, so its gathers run one chunk deep). Other shapes run
+ * as smd_sparse_mla_decode_bf16q. The workspace needs no initialisation
+ * (see smd_sparse_mla_decode_ws). */
+int smd_sparse_mla_decode_bf16q_ws(const uint16_t* q, const uint8_t* kv_pool, int64_t N,
+                                   const int32_t* indices, int32_t W, const int32_t* counts,
+                                   int32_t B, int32_t H, float sm_scale, float k_scale,
+                                   uint16_t* out, float* lse, int32_t* status, void* workspace,
+                                   int64_t workspace_bytes, smd_stream_t stream);
+
+/* Bytes of workspace smd_sparse_mla_decode_bf16q_ws uses for (B, H, W): the
+ * spread kernel's slots and the split query (2 x 576 + 4 bytes per query
+ * row), or 0 where it runs on the warp-MMA kernel. Host only. */
+int64_t smd_workspace_bytes_bf16q(int32_t B, int32_t H, int32_t W);
+
+/* As smd_sparse_mla_decode_bf16q_ws with plan fields (kernel SMD_KERNEL_MMA,
+ * SMD_KERNEL_TC_SPREAD or 0, split, tiles, window, grid_x, the testing hooks)
+ * taken from `force` (may be NULL); workspace may be NULL unless the plan is
+ * the spread kernel. For the tests. */
 int smd_sparse_mla_decode_bf16q_ex(const uint16_t* q, const uint8_t* kv_pool, int64_t N,
                                    const int32_t* indices, int32_t W, const int32_t* counts,
                                    int32_t B, int32_t H, float sm_scale, float k_scale,
-                                   uint16_t* out, float* lse, int32_t* status,
-                                   smd_stream_t stream, const smd_plan_t* force);
+                                   uint16_t* out, float* lse, int32_t* status, void* workspace,
+                                   int64_t workspace_bytes, smd_stream_t stream,
+                                   const smd_plan_t* force);
 
-/* The plan smd_sparse_mla_decode_bf16q would use. Host only. */
-int smd_plan_bf16q(int32_t B, int32_t H, int32_t W, smd_plan_t* plan);
+/* The plan of the bf16-query call with a workspace of workspace_bytes (0:
+ * smd_sparse_mla_decode_bf16q's). Host only. */
+int smd_plan_bf16q(int32_t B, int32_t H, int32_t W, int64_t workspace_bytes, smd_plan_t* plan);
 
 /* Top-k select over bf16 logits, producing the decode's index list and
  * count on the device (the topk_exchange page: the select of

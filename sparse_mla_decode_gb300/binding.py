@@ -87,10 +87,16 @@ def lib() -> ctypes.CDLL:
                         ctypes.c_void_p, ctypes.c_void_p])
             so.smd_sparse_mla_decode_bf16q.restype = ctypes.c_int
             so.smd_sparse_mla_decode_bf16q.argtypes = bq_args
+            bq_ws = bq_args[:-1] + [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+            so.smd_sparse_mla_decode_bf16q_ws.restype = ctypes.c_int
+            so.smd_sparse_mla_decode_bf16q_ws.argtypes = bq_ws
             so.smd_sparse_mla_decode_bf16q_ex.restype = ctypes.c_int
-            so.smd_sparse_mla_decode_bf16q_ex.argtypes = bq_args + [ctypes.POINTER(SmdPlan)]
+            so.smd_sparse_mla_decode_bf16q_ex.argtypes = bq_ws + [ctypes.POINTER(SmdPlan)]
+            so.smd_workspace_bytes_bf16q.restype = ctypes.c_int64
+            so.smd_workspace_bytes_bf16q.argtypes = [ctypes.c_int32] * 3
             so.smd_plan_bf16q.restype = ctypes.c_int
-            so.smd_plan_bf16q.argtypes = [ctypes.c_int32] * 3 + [ctypes.POINTER(SmdPlan)]
+            so.smd_plan_bf16q.argtypes = [ctypes.c_int32] * 3 + [ctypes.c_int64,
+                                                                 ctypes.POINTER(SmdPlan)]
             so.smd_topk_select.restype = ctypes.c_int
             tk_args = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int32,
                        ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
@@ -186,16 +192,29 @@ def smd_sparse_mla_decode_bf16q(q, kv_pool, N, indices, W, counts, B, H, sm_scal
                                              k_scale, out, lse, status, stream)
 
 
+def smd_sparse_mla_decode_bf16q_ws(q, kv_pool, N, indices, W, counts, B, H, sm_scale, k_scale,
+                                   out, lse, status, workspace, workspace_bytes, stream) -> int:
+    return lib().smd_sparse_mla_decode_bf16q_ws(q, kv_pool, N, indices, W, counts, B, H, sm_scale,
+                                                k_scale, out, lse, status, workspace,
+                                                workspace_bytes, stream)
+
+
 def smd_sparse_mla_decode_bf16q_ex(q, kv_pool, N, indices, W, counts, B, H, sm_scale, k_scale,
-                                   out, lse, status, stream, force: SmdPlan | None) -> int:
+                                   out, lse, status, workspace, workspace_bytes, stream,
+                                   force: SmdPlan | None) -> int:
     ref = ctypes.byref(force) if force is not None else None
     return lib().smd_sparse_mla_decode_bf16q_ex(q, kv_pool, N, indices, W, counts, B, H, sm_scale,
-                                                k_scale, out, lse, status, stream, ref)
+                                                k_scale, out, lse, status, workspace,
+                                                workspace_bytes, stream, ref)
 
 
-def smd_plan_bf16q(B: int, H: int, W: int) -> SmdPlan:
+def smd_workspace_bytes_bf16q(B: int, H: int, W: int) -> int:
+    return int(lib().smd_workspace_bytes_bf16q(B, H, W))
+
+
+def smd_plan_bf16q(B: int, H: int, W: int, workspace_bytes: int = 0) -> SmdPlan:
     p = SmdPlan()
-    rc = lib().smd_plan_bf16q(B, H, W, ctypes.byref(p))
+    rc = lib().smd_plan_bf16q(B, H, W, int(workspace_bytes), ctypes.byref(p))
     if rc != SMD_OK:
         raise SmdError(rc, "smd_plan_bf16q")
     return p
@@ -341,7 +360,7 @@ def sparse_mla_decode(q, kv_pool, indices, counts, sm_scale: float, q_scale: flo
 
 def sparse_mla_decode_bf16q(q, kv_pool, indices, counts, sm_scale: float, k_scale: float,
                             out=None, lse=None, status=None, stream=None,
-                            plan: SmdPlan | dict | None = None):
+                            plan: SmdPlan | dict | None = None, workspace=None):
     """Decode with a bfloat16 query q [B,H,576] (split into E4M3 hi + lo per
     (row, head) on the GPU: smd_sparse_mla_decode_bf16q). kv_pool [N,576] E4M3,
     indices [B,W] int32, counts [B] int32, all CUDA tensors. Returns
@@ -373,14 +392,19 @@ def sparse_mla_decode_bf16q(q, kv_pool, indices, counts, sm_scale: float, k_scal
     elif hasattr(stream, "cuda_stream"):
         stream = stream.cuda_stream
     args = (_ptr(q), _ptr(kv_pool), int(kv_pool.shape[0]), _ptr(indices), W, _ptr(counts), B, H,
-            float(sm_scale), float(k_scale), _ptr(out), _ptr(lse), _ptr(status), int(stream))
+            float(sm_scale), float(k_scale), _ptr(out), _ptr(lse), _ptr(status))
+    ws = (_ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size())
     if isinstance(plan, dict):
         p = SmdPlan()
         for k, v in plan.items():
             setattr(p, k, int(v))
         plan = p
-    rc = (smd_sparse_mla_decode_bf16q(*args) if plan is None
-          else smd_sparse_mla_decode_bf16q_ex(*args, plan))
+    if plan is not None:
+        rc = smd_sparse_mla_decode_bf16q_ex(*args, *ws, int(stream), plan)
+    elif workspace is not None:
+        rc = smd_sparse_mla_decode_bf16q_ws(*args, *ws, int(stream))
+    else:
+        rc = smd_sparse_mla_decode_bf16q(*args, int(stream))
     if rc != SMD_OK:
         raise SmdError(rc, "smd_sparse_mla_decode_bf16q")
     return out, lse

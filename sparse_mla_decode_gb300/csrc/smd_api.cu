@@ -260,10 +260,6 @@ int64_t tcs_items_cap(int B, int H, int W) {
     return static_cast<int64_t>(B) * ceil_div(H, kTcHeads) * ceil_div(W, kTcMaxKeys);
 }
 
-int64_t tcs_workspace_bytes(int B, int H, int W) {
-    return tcs_workspace(tcs_items_cap(B, H, W)).total;
-}
-
 // The spread kernel's plan: one CTA per resident slot, no more than there can
 // be pieces (a forced grid_x caps it).
 int plan_tcs(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_plan_t* out,
@@ -311,6 +307,14 @@ int plan_tcs(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
 bool prefer_spread(int B, int H, int W, int sm_count) {
     if (H % kTcHeads != 0 || !tcs_fits(B, H, W) || W <= kTcMaxKeys) return false;
     return W > kTcMaxSplit * kTcMaxKeys || tcs_items_cap(B, H, W) <= 2 * sm_count;
+}
+
+// The split query on the spread kernel: 128-head groups and rows it takes.
+bool bf16q_spread_fits(int B, int H, int W) { return H % kTcHeads == 0 && tcs_fits(B, H, W); }
+
+int64_t bf16q_workspace_bytes(int B, int H, int W) {
+    if (!bf16q_spread_fits(B, H, W)) return 0;
+    return tcs_workspace(tcs_items_cap(B, H, W), static_cast<int64_t>(B) * H).total;
 }
 
 struct AnyConfig {
@@ -410,12 +414,26 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
     }
 
     if (q16 != nullptr) {
-        // The split query runs on the warp-MMA kernel.
-        if (force && force->kernel && force->kernel != SMD_KERNEL_MMA) return SMD_ERR_PLAN;
+        // The split query: on the spread tcgen05 kernel when a workspace is
+        // given and the shapes fit it, else on the warp-MMA kernel.
+        const int fk = (force && force->kernel) ? force->kernel : SMD_KERNEL_AUTO;
+        if (fk != SMD_KERNEL_AUTO && fk != SMD_KERNEL_MMA && fk != SMD_KERNEL_TC_SPREAD)
+            return SMD_ERR_PLAN;
+        if (workspace != nullptr && !aligned(workspace, 16)) return SMD_ERR_WORKSPACE;
+        const bool spread = fk == SMD_KERNEL_TC_SPREAD ||
+                            (fk == SMD_KERNEL_AUTO && workspace != nullptr && bf16q_spread_fits(B, H, W));
         smd_plan_t plan{};
         MmaConfig mcfg{};
-        const int rc = plan_mma(B, H, W, sm_count_of_device(), force, &plan, &mcfg, true);
+        TcsConfig tcfg{};
+        const int rc = spread ? plan_tcs(B, H, W, sm_count_of_device(), force, &plan, &tcfg)
+                              : plan_mma(B, H, W, sm_count_of_device(), force, &plan, &mcfg, true);
         if (rc != SMD_OK) return rc;
+        if (spread) {
+            const int64_t need = tcs_workspace(tcfg.items_cap, static_cast<int64_t>(B) * H).total;
+            if (workspace == nullptr || workspace_bytes < need) return SMD_ERR_WORKSPACE;
+            tcfg.qsplit = 1;
+            tcfg.ws = workspace;
+        }
         CallArgs a{};
         a.q = nullptr;
         a.q16 = q16;
@@ -431,6 +449,7 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
         a.out = out;
         a.lse = lse;
         a.status = status;
+        if (spread) return launch_tcs(a, tcfg, reinterpret_cast<cudaStream_t>(stream));
         return launch_mma(a, mcfg, reinterpret_cast<cudaStream_t>(stream));
     }
 
@@ -523,22 +542,44 @@ int smd_sparse_mla_decode_bf16q(const uint16_t* q, const uint8_t* kv_pool, int64
                        false, 1, q);
 }
 
+int smd_sparse_mla_decode_bf16q_ws(const uint16_t* q, const uint8_t* kv_pool, int64_t N,
+                                   const int32_t* indices, int32_t W, const int32_t* counts,
+                                   int32_t B, int32_t H, float sm_scale, float k_scale,
+                                   uint16_t* out, float* lse, int32_t* status, void* workspace,
+                                   int64_t workspace_bytes, smd_stream_t stream) {
+    return smd::decode(reinterpret_cast<const uint8_t*>(q), kv_pool, N, indices, W, counts, B, H,
+                       sm_scale, 1.0f, k_scale, out, lse, status, workspace, workspace_bytes,
+                       stream, nullptr, false, 1, q);
+}
+
 int smd_sparse_mla_decode_bf16q_ex(const uint16_t* q, const uint8_t* kv_pool, int64_t N,
                                    const int32_t* indices, int32_t W, const int32_t* counts,
                                    int32_t B, int32_t H, float sm_scale, float k_scale,
-                                   uint16_t* out, float* lse, int32_t* status,
-                                   smd_stream_t stream, const smd_plan_t* force) {
+                                   uint16_t* out, float* lse, int32_t* status, void* workspace,
+                                   int64_t workspace_bytes, smd_stream_t stream,
+                                   const smd_plan_t* force) {
     return smd::decode(reinterpret_cast<const uint8_t*>(q), kv_pool, N, indices, W, counts, B, H,
-                       sm_scale, 1.0f, k_scale, out, lse, status, nullptr, 0, stream, force,
-                       false, 1, q);
+                       sm_scale, 1.0f, k_scale, out, lse, status, workspace, workspace_bytes,
+                       stream, force, false, 1, q);
 }
 
-int smd_plan_bf16q(int32_t B, int32_t H, int32_t W, smd_plan_t* plan) {
+int64_t smd_workspace_bytes_bf16q(int32_t B, int32_t H, int32_t W) {
+    if (B < 0 || W < 0 || H <= 0 || H % smd::kHeadsPerTile != 0) return 0;
+    return smd::bf16q_workspace_bytes(B, H, W);
+}
+
+int smd_plan_bf16q(int32_t B, int32_t H, int32_t W, int64_t workspace_bytes, smd_plan_t* plan) {
     if (!plan) return SMD_ERR_NULL;
     if (B < 0 || W < 0 || H <= 0 || H % smd::kHeadsPerTile != 0) return SMD_ERR_SHAPE;
     smd_plan_t p{};
-    smd::MmaConfig cfg{};
-    const int rc = smd::plan_mma(B, H, W, smd::sm_count_of_device(), nullptr, &p, &cfg, true);
+    int rc;
+    if (workspace_bytes > 0 && smd::bf16q_spread_fits(B, H, W)) {
+        smd::TcsConfig cfg{};
+        rc = smd::plan_tcs(B, H, W, smd::sm_count_of_device(), nullptr, &p, &cfg);
+    } else {
+        smd::MmaConfig cfg{};
+        rc = smd::plan_mma(B, H, W, smd::sm_count_of_device(), nullptr, &p, &cfg, true);
+    }
     if (rc == SMD_OK) *plan = p;
     return rc;
 }

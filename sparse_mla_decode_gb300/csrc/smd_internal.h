@@ -218,12 +218,14 @@ struct TcsWorkspace {
     int64_t max;        // [items][128] fp32
     int64_t sum;        // [items][128] fp32
     int64_t part;       // [items][128 x 512] fp32 partials, 16-byte units head-innermost
+    int64_t q_hi, q_lo; // [qrows][576] E4M3: the split bf16 query (qrows = B * H, else 0)
+    int64_t lamh;       // [qrows] fp32: each query row's logit scale
     int64_t total;
 };
 
 __host__ __device__ inline int64_t align_up64(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline TcsWorkspace tcs_workspace(int64_t items) {
+__host__ __device__ inline TcsWorkspace tcs_workspace(int64_t items, int64_t qrows = 0) {
     TcsWorkspace w{};
     int64_t o = 0;
     w.flag_max = o;
@@ -236,6 +238,12 @@ __host__ __device__ inline TcsWorkspace tcs_workspace(int64_t items) {
     o = align_up64(o + items * 128 * 4, 256);
     w.part = o;
     o = align_up64(o + items * 128 * kLatent * 4, 256);
+    w.q_hi = o;
+    o = align_up64(o + qrows * kRow, 256);
+    w.q_lo = o;
+    o = align_up64(o + qrows * kRow, 256);
+    w.lamh = o;
+    o = align_up64(o + qrows * 4, 256);
     w.total = o;
     return w;
 }
@@ -243,6 +251,7 @@ __host__ __device__ inline TcsWorkspace tcs_workspace(int64_t items) {
 struct TcsConfig {
     int grid;       // CTAs (at most the resident CTAs of the device)
     int items_cap;  // item slots in the workspace: units * ceil(W / 512)
+    int qsplit;     // 1: bf16 query (CallArgs::q16), split into the workspace first
     uint64_t wait_budget_ns;
     int inject_stall;
     void* ws;

@@ -30,10 +30,9 @@
 #include <cmath>
 #include <cstdint>
 
-#include <cuda_fp16.h>
-
 #include "smd_internal.h"
 #include "smd_ptx.cuh"
+#include "smd_qsplit.cuh"
 
 namespace smd {
 
@@ -77,73 +76,17 @@ __device__ __forceinline__ void gather_chunk(const MmaParams& p, uint32_t slot_s
     }
 }
 
-// The E4M3 values of two codes (exact in f16, then f32).
-__device__ __forceinline__ float2 e4m3x2_values(uint16_t codes) {
-    uint32_t h2;
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(codes));
-    return __half22float2(*reinterpret_cast<const __half2*>(&h2));
-}
-
-// The split query (the mla_attn page's q_split, "E4M3 hi, lo of q 2^k"): warp w
-// takes heads w, w + 16, ... of the CTA's CH; per head the largest k with
-// amax 2^k <= 448 (k = 0 for a zero row; clamped to [-32, 32]),
-// hi = E4M3(q 2^k) and lo = E4M3(q 2^k - hi) (both round-to-nearest-even,
-// saturating; q 2^k and q 2^k - hi are exact in fp32) into the two query
-// tiles, and the head's logit scale lam0 2^-k.
+// The split query: warp w takes heads w, w + 16, ... of the CTA's CH into the
+// two query tiles (rows kRowPitch apart) and their logit scales.
 template <int CH>
 __device__ __forceinline__ void split_query(const MmaParams& p, int b, int head0, uint8_t* q_hi,
                                             uint8_t* q_lo, float* lamh) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    constexpr int kPieces = kRow / 8;  // 16-byte pieces of a bf16 row
     for (int hh = warp; hh < CH; hh += kMmaThreads / 32) {
-        const uint4* src = reinterpret_cast<const uint4*>(
-            p.a.q16 + (static_cast<int64_t>(b) * p.a.H + head0 + hh) * kRow);
-        uint4 v[3];
-        float amax = 0.f;
-#pragma unroll
-        for (int u = 0; u < 3; ++u) {
-            const int piece = lane + 32 * u;
-            v[u] = piece < kPieces ? __ldg(src + piece) : make_uint4(0u, 0u, 0u, 0u);
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)),
-                                         fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
-        }
-        amax = warp_max(amax);
-        int k = 0;
-        if (amax > 0.f) {
-            int e = 0;
-            const float m = frexpf(amax, &e);  // amax = m 2^e, m in [0.5, 1)
-            k = (m <= 0.875f) ? 9 - e : 8 - e;
-            k = max(-32, min(32, k));
-        }
-        const float up = __int_as_float((127 + k) << 23);  // 2^k
-#pragma unroll
-        for (int u = 0; u < 3; ++u) {
-            const int piece = lane + 32 * u;
-            if (piece >= kPieces) continue;
-            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-            uint32_t hw[2], lw[2];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float x0 = __uint_as_float(w[i] << 16) * up;
-                const float x1 = __uint_as_float(w[i] & 0xFFFF0000u) * up;
-                const uint16_t hc = e4m3x2(x0, x1);
-                const float2 hv = e4m3x2_values(hc);
-                const uint16_t lc = e4m3x2(x0 - hv.x, x1 - hv.y);
-                if (i & 1) {
-                    hw[i >> 1] |= static_cast<uint32_t>(hc) << 16;
-                    lw[i >> 1] |= static_cast<uint32_t>(lc) << 16;
-                } else {
-                    hw[i >> 1] = hc;
-                    lw[i >> 1] = lc;
-                }
-            }
-            *reinterpret_cast<uint2*>(q_hi + hh * kRowPitch + 8 * piece) = make_uint2(hw[0], hw[1]);
-            *reinterpret_cast<uint2*>(q_lo + hh * kRowPitch + 8 * piece) = make_uint2(lw[0], lw[1]);
-        }
-        if (lane == 0) lamh[hh] = p.a.scale_log2 * __int_as_float((127 - k) << 23);
+        const float lam = split_query_row(p.a.q16 + (static_cast<int64_t>(b) * p.a.H + head0 + hh) * kRow,
+                                          q_hi + hh * kRowPitch, q_lo + hh * kRowPitch,
+                                          p.a.scale_log2);
+        if (lane == 0) lamh[hh] = lam;
     }
 }
 

@@ -23,8 +23,16 @@ constexpr int kTail = 8192;                // the 64-byte tail block of 128 rows
 constexpr int kTile = 4 * kBlock + kTail;  // 576 columns x 128 rows
 
 // Shared-memory addresses and barriers of one CTA's pipeline.
+//
+// Split query (q_lo != 0): the query's hi tile is at q and its lo tile fills
+// ring slot 1 until QK is done, so pass A gathers every chunk into slot 0
+// (one chunk in flight) and QK adds the lo products; pass B finds chunk
+// nch - 1 resident in slot 0 and brings the others back into slot
+// (nch - 1 - c) & 1. Otherwise chunk c uses slot c & 1 in both passes and
+// the last two chunks are resident after pass A.
 struct Pipe {
     uint32_t q;       // the query tile, later the P tiles (chunk c at q + c * kBlock)
+    uint32_t q_lo;    // the split query's lo tile (ring slot 1), or 0
     uint32_t ring;    // two chunk slots of kTile bytes
     uint32_t full;    // [2] a slot's gathers have landed
     uint32_t empty;   // [2] pass A: QK has left a slot
@@ -44,16 +52,25 @@ __device__ __forceinline__ void wait_next(uint32_t bar, uint32_t& seen, bool& ok
     ++seen;
 }
 
-// Producer warps, pass A, chunks [c_begin, c_end): chunk c goes to slot c & 1
-// once QK of chunk c - 2 has left it; thread t < 160 issues piece t % 5 of
-// rows 4g .. 4g + 3, g = t / 5. `seen` counts the "empty" completions.
+// Slot of chunk c in pass A and in pass B (see Pipe).
+__device__ __forceinline__ int slot_a(const Pipe& pp, int c) { return pp.q_lo ? 0 : (c & 1); }
+__device__ __forceinline__ int slot_b(const Pipe& pp, int c, int nch) {
+    return pp.q_lo ? ((nch - 1 - c) & 1) : (c & 1);
+}
+// Chunks pass B finds resident (the last ones gathered in pass A).
+__device__ __forceinline__ int resident_b(const Pipe& pp) { return pp.q_lo ? 1 : 2; }
+
+// Producer warps, pass A, chunks [c_begin, c_end): chunk c goes to its slot
+// once QK of the chunk before it in that slot has left; thread t < 160
+// issues piece t % 5 of rows 4g .. 4g + 3, g = t / 5. `seen` counts the
+// "empty" completions.
 __device__ __forceinline__ void gather_pass_a(const CUtensorMap& kv, const CUtensorMap& kv_tail,
                                               const Pipe& pp, int c_begin, int c_end,
                                               uint32_t (&seen)[2], bool& ok) {
     const int t = threadIdx.x;
     for (int c = c_begin; c < c_end && ok; ++c) {
-        const int s = c & 1;
-        const uint32_t need = static_cast<uint32_t>(c >> 1);
+        const int s = slot_a(pp, c);
+        const uint32_t need = static_cast<uint32_t>(pp.q_lo ? c : (c >> 1));
         while (seen[s] < need) wait_next(pp.empty + 8 * s, seen[s], ok, pp.status, pp.budget_ns);
         if (!ok) break;
         const uint32_t slot = pp.ring + s * kTile;
@@ -70,19 +87,18 @@ __device__ __forceinline__ void gather_pass_a(const CUtensorMap& kv, const CUten
     }
 }
 
-// Producer warps, pass B: chunks in descending order; the last two are
-// resident, the others come back (V columns only) into their slot once PV of
-// the chunk two above has released it.
+// Producer warps, pass B: chunks in descending order; the resident ones stay,
+// the others come back (V columns only) into their slot once PV of the chunk
+// two above has released it (a slot that held no chunk is free at once).
 __device__ __forceinline__ void gather_pass_b(const CUtensorMap& kv, const Pipe& pp, int nch,
                                               bool& ok) {
     const int t = threadIdx.x;
     uint32_t seen_b[2] = {0u, 0u};  // completions of the pass-B "slot free" barriers seen
-    for (int c = 1; c >= 0; --c) {
-        if (c > nch - 3 || !ok) continue;
-        const int s = c & 1;
-        int later = 0;  // pass-B completions on slot s before PV(c + 2)
-        for (int c2 = nch - 1; c2 > c + 2; --c2) later += ((c2 & 1) == s);
-        const uint32_t need = static_cast<uint32_t>(later + 1);
+    for (int c = nch - 1 - resident_b(pp); c >= 0 && ok; --c) {
+        const int s = slot_b(pp, c, nch);
+        int freed = 0;  // pass-B completions on slot s up to PV(c + 2), its previous chunk
+        for (int c2 = nch - 1; c2 >= c + 2; --c2) freed += (slot_b(pp, c2, nch) == s);
+        const uint32_t need = static_cast<uint32_t>(freed);
         while (seen_b[s] < need) wait_next(pp.free_b + 8 * s, seen_b[s], ok, pp.status, pp.budget_ns);
         if (!ok) break;
         const uint32_t slot = pp.ring + s * kTile;
@@ -97,33 +113,37 @@ __device__ __forceinline__ void gather_pass_b(const CUtensorMap& kv, const Pipe&
 }
 
 // MMA issuer (one lane), pass A: S_c = Q K_c^T into TMEM columns 128c .. + 127
-// (18 x M128 N128 K32 E4M3 MMAs), committing to "QK done" and "slot empty".
-// `full_seen` counts the slots' "full" completions (pass B continues it).
+// (18 x M128 N128 K32 E4M3 MMAs; 36 with the split query's lo tile),
+// committing to "QK done" and "slot empty". `full_seen` counts the slots'
+// "full" completions (pass B continues it).
 __device__ __forceinline__ void mma_qk(const Pipe& pp, uint32_t tmem, int nch,
                                        uint32_t (&full_seen)[2], bool& ok) {
     mbar_wait(pp.bar_q, 0, ok, pp.status, pp.budget_ns);
     tc_fence_after();
     constexpr uint32_t kIdQK = umma_idesc_e4m3(128, kTcChunk, 0);
     for (int c = 0; c < nch && ok; ++c) {
-        const int s = c & 1;
+        const int s = slot_a(pp, c);
         wait_next(pp.full + 8 * s, full_seen[s], ok, pp.status, pp.budget_ns);
         if (!ok) break;
         tc_fence_after();
         const uint32_t slot = pp.ring + s * kTile;
         const uint32_t d = tmem + kTcChunk * c;
         uint32_t acc = 0;
+        for (int part = 0; part < (pp.q_lo ? 2 : 1); ++part) {  // hi, then the split query's lo
+            const uint32_t qa = part ? pp.q_lo : pp.q;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+            for (int j = 0; j < 4; ++j)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                umma_e4m3(d, umma_desc(pp.q + j * kBlock + 32 * kk, 16, 1024, 2),
-                          umma_desc(slot + j * kBlock + 32 * kk, 16, 1024, 2), kIdQK, acc);
-                acc = 1;
-            }
+                for (int kk = 0; kk < 4; ++kk) {
+                    umma_e4m3(d, umma_desc(qa + j * kBlock + 32 * kk, 16, 1024, 2),
+                              umma_desc(slot + j * kBlock + 32 * kk, 16, 1024, 2), kIdQK, acc);
+                    acc = 1;
+                }
 #pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
-            umma_e4m3(d, umma_desc(pp.q + 4 * kBlock + 32 * kk, 16, 512, 4),
-                      umma_desc(slot + 4 * kBlock + 32 * kk, 16, 512, 4), kIdQK, 1);
+            for (int kk = 0; kk < 2; ++kk)
+                umma_e4m3(d, umma_desc(qa + 4 * kBlock + 32 * kk, 16, 512, 4),
+                          umma_desc(slot + 4 * kBlock + 32 * kk, 16, 512, 4), kIdQK, 1);
+        }
         umma_commit(pp.s + 8 * c);
         umma_commit(pp.empty + 8 * s);
     }
@@ -139,8 +159,8 @@ __device__ __forceinline__ void mma_pv(const Pipe& pp, uint32_t tmem, int nch, i
     mbar_wait(pp.bar_p, 0, ok, pp.status, pp.budget_ns);
     tc_fence_after();
     for (int c = nch - 1; c >= 0 && ok; --c) {
-        const int s = c & 1;
-        if (c <= nch - 3) {
+        const int s = slot_b(pp, c, nch);
+        if (c < nch - resident_b(pp)) {
             wait_next(pp.full + 8 * s, full_seen[s], ok, pp.status, pp.budget_ns);
             if (!ok) break;
             tc_fence_after();

@@ -88,6 +88,7 @@ __device__ __forceinline__ tcc::Pipe pipe_of(const TcgParams& p, uint32_t base, 
                                              const uint8_t* smem) {
     tcc::Pipe pp;
     pp.q = base + kOffQP;
+    pp.q_lo = 0u;  // the query is one E4M3 tile
     pp.ring = base + kOffRing;
     pp.full = bars + 8 * kBarFull;
     pp.empty = bars + 8 * kBarEmpty;

@@ -38,6 +38,7 @@
 #include "smd.h"
 #include "smd_internal.h"
 #include "smd_ptx.cuh"
+#include "smd_qsplit.cuh"
 #include "smd_tc_common.cuh"
 
 namespace smd {
@@ -68,6 +69,7 @@ constexpr int kProducerThreads = 256;
 
 struct TcsMaps {
     CUtensorMap q, q_tail, kv, kv_tail;
+    CUtensorMap q_lo, q_lo_tail;  // the split query's lo rows (unused otherwise)
 };
 
 struct TcsParams {
@@ -82,7 +84,14 @@ struct TcsParams {
     uint64_t token;  // this call's flag value (never 0)
     TcsWorkspace ws;
     uint8_t* ws_base;
+    const float* lamh;  // the split query's per-row logit scales [B * H], or null
 };
+
+// The logit scale of head h (0 .. 127) of the item's group.
+__device__ __forceinline__ float lam_of(const TcsParams& p, int b, int g, int h) {
+    if (p.lamh == nullptr) return p.a.scale_log2;
+    return h < p.lanes ? p.lamh[static_cast<int64_t>(b) * p.a.H + g * kTcHeads + h] : 0.f;
+}
 
 struct Item {
     int b, g, s, j, item0;  // row, head group, items of the unit, this piece, the unit's first item
@@ -148,6 +157,7 @@ __device__ __forceinline__ tcc::Pipe pipe_of(const TcsParams& p, uint32_t base, 
                                              const uint8_t* smem) {
     tcc::Pipe pp;
     pp.q = base + kOffQP;
+    pp.q_lo = p.lamh != nullptr ? base + kOffRing + kTile : 0u;
     pp.ring = base + kOffRing;
     pp.full = bars + 8 * kBarFull;
     pp.empty = bars + 8 * kBarEmpty;
@@ -293,7 +303,7 @@ __device__ __forceinline__ void row_max(const TcsParams& p, uint8_t* smem, uint3
                                         uint32_t tmem, const Item& it, int item, bool& ok) {
     const int h = threadIdx.x & 127;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * ((threadIdx.x >> 5) & 3)) << 16);
-    const float lam = p.a.scale_log2;
+    const float lam = lam_of(p, it.b, it.g, h);
     float m = -INFINITY;
     for (int c = 0; c < it.nch; ++c) {
         mbar_wait(bars + 8 * (kBarS + c), 0, ok, p.a.status, p.budget_ns);
@@ -340,7 +350,7 @@ __device__ __forceinline__ void p_phase(const TcsParams& p, uint8_t* smem, uint3
     const int h = 32 * (warp & 3) + (threadIdx.x & 31);
     const int j = warp >> 2;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    const float lam = p.a.scale_log2;
+    const float lam = lam_of(p, it.b, it.g, h);
     const float bias = reinterpret_cast<const float*>(smem + kOffRowMax)[h] - p.log2_448;
     float l = 0.f;
     for (int c = 0; c < it.nch && ok; ++c) {
@@ -574,11 +584,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (threadIdx.x == 0) {
             // (inject_stall: the query barrier also expects 16 bytes nobody
             // sends, so its bounded wait runs out; a test hook.)
-            mbar_arrive_expect_tx(bars + 8 * kBarQ, kTile + (p.inject_stall ? 16 : 0));
+            const bool split = p.lamh != nullptr;
+            mbar_arrive_expect_tx(bars + 8 * kBarQ, (split ? 2 : 1) * kTile + (p.inject_stall ? 16 : 0));
             const int y = it.b * p.a.H + it.g * kTcHeads;
             for (int c = 0; c < 4; ++c)
                 tma_load_2d(base + kOffQP + c * kBlock, &maps.q, 128 * c, y, bars + 8 * kBarQ);
             tma_load_2d(base + kOffQP + 4 * kBlock, &maps.q_tail, 512, y, bars + 8 * kBarQ);
+            if (split) {  // the lo rows into ring slot 1, free until QK is done
+                const uint32_t lo = base + kOffRing + kTile;
+                for (int c = 0; c < 4; ++c)
+                    tma_load_2d(lo + c * kBlock, &maps.q_lo, 128 * c, y, bars + 8 * kBarQ);
+                tma_load_2d(lo + 4 * kBlock, &maps.q_lo_tail, 512, y, bars + 8 * kBarQ);
+            }
         }
         uint32_t full_seen[2] = {0u, 0u};
         if (warp < 8) {
@@ -609,6 +626,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         tmem_free(tmem, 512);
     }
+}
+
+// The split query into the workspace (smd_qsplit.cuh): one warp per query row.
+__global__ void __launch_bounds__(256) tcs_qsplit_kernel(const uint16_t* q16, int64_t rows,
+                                                         float lam0, uint8_t* q_hi, uint8_t* q_lo,
+                                                         float* lamh) {
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (r >= rows) return;  // warp-uniform
+    const float lam = split_query_row(q16 + r * kRow, q_hi + r * kRow, q_lo + r * kRow, lam0);
+    if ((threadIdx.x & 31) == 0) lamh[r] = lam;
 }
 
 }  // namespace
@@ -664,10 +691,26 @@ int tcs_max_grid() {
 }
 
 int launch_tcs(const CallArgs& a, const TcsConfig& cfg, cudaStream_t stream) {
-    TcsMaps maps;
+    TcsMaps maps{};
     const uint64_t qrows = static_cast<uint64_t>(a.B) * static_cast<uint64_t>(a.H);
-    if (!encode_row_map(&maps.q, a.q, qrows, 128, kTcHeads) ||
-        !encode_row_map(&maps.q_tail, a.q, qrows, 64, kTcHeads) ||
+    const TcsWorkspace ws = tcs_workspace(cfg.items_cap, cfg.qsplit ? static_cast<int64_t>(qrows) : 0);
+    uint8_t* base = static_cast<uint8_t*>(cfg.ws);
+    const uint8_t* q = a.q;
+    if (cfg.qsplit) {
+        // The bf16 rows split into E4M3 hi and lo rows and their logit scales, in the workspace.
+        if (a.q16 == nullptr) return SMD_ERR_NULL;
+        const unsigned blocks = static_cast<unsigned>((qrows + 7) / 8);
+        tcs_qsplit_kernel<<<blocks, 256, 0, stream>>>(a.q16, static_cast<int64_t>(qrows),
+                                                      a.scale_log2, base + ws.q_hi, base + ws.q_lo,
+                                                      reinterpret_cast<float*>(base + ws.lamh));
+        if (cudaGetLastError() != cudaSuccess) return SMD_ERR_LAUNCH;
+        q = base + ws.q_hi;
+        if (!encode_row_map(&maps.q_lo, base + ws.q_lo, qrows, 128, kTcHeads) ||
+            !encode_row_map(&maps.q_lo_tail, base + ws.q_lo, qrows, 64, kTcHeads))
+            return SMD_ERR_LAUNCH;
+    }
+    if (!encode_row_map(&maps.q, q, qrows, 128, kTcHeads) ||
+        !encode_row_map(&maps.q_tail, q, qrows, 64, kTcHeads) ||
         !encode_row_map(&maps.kv, a.kv, static_cast<uint64_t>(a.N), 128, 1) ||
         !encode_row_map(&maps.kv_tail, a.kv, static_cast<uint64_t>(a.N), 64, 1))
         return SMD_ERR_LAUNCH;
@@ -683,8 +726,9 @@ int launch_tcs(const CallArgs& a, const TcsConfig& cfg, cudaStream_t stream) {
     prm.budget_ns = cfg.wait_budget_ns;
     prm.inject_stall = cfg.inject_stall;
     prm.token = next_token();
-    prm.ws = tcs_workspace(cfg.items_cap);
-    prm.ws_base = static_cast<uint8_t*>(cfg.ws);
+    prm.ws = ws;
+    prm.ws_base = base;
+    prm.lamh = cfg.qsplit ? reinterpret_cast<const float*>(base + ws.lamh) : nullptr;
 
     cudaLaunchConfig_t lc{};
     lc.gridDim = dim3(static_cast<unsigned>(cfg.grid), 1, 1);

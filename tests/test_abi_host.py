@@ -243,7 +243,7 @@ def call_bf16q(q=A, kv=A, N=100, idx=A, W=8, counts=A, B=2, H=16, out=A, lse=A, 
         return smd.smd_sparse_mla_decode_bf16q(q, kv, N, idx, W, counts, B, H, 0.1, 0.1,
                                                out, lse, status, 0)
     return smd.smd_sparse_mla_decode_bf16q_ex(q, kv, N, idx, W, counts, B, H, 0.1, 0.1,
-                                              out, lse, status, 0, force)
+                                              out, lse, status, 0, 0, 0, force)
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -259,7 +259,7 @@ def test_bf16q_argument_checks(kw, code):
     assert call_bf16q(**kw) == code
 
 
-@pytest.mark.parametrize("force", [dict(kernel=2), dict(kernel=5), dict(split=3), dict(tiles=3),
+@pytest.mark.parametrize("force", [dict(kernel=2), dict(kernel=4), dict(split=3), dict(tiles=3),
                                    dict(window=65)])
 def test_bf16q_invalid_forced_plans_are_rejected(force):
     p = smd.SmdPlan()
@@ -268,9 +268,23 @@ def test_bf16q_invalid_forced_plans_are_rejected(force):
     assert call_bf16q(force=p) == smd.SMD_ERR_PLAN
 
 
+def test_bf16q_workspace_plan():
+    """With a workspace the 128-head shapes go to the spread kernel, which
+    needs the split query's rows besides its slots; others stay on warp MMA."""
+    nb = smd.smd_workspace_bytes_bf16q(64, 128, 2048)
+    assert nb >= 64 * 4 * 128 * 512 * 4 + 64 * 128 * (2 * 576 + 4)
+    assert smd.smd_plan_bf16q(64, 128, 2048, nb).kernel == smd.SMD_KERNEL_TC_SPREAD
+    assert smd.smd_plan_bf16q(64, 128, 2048, 0).kernel == smd.SMD_KERNEL_MMA
+    assert smd.smd_workspace_bytes_bf16q(5, 64, 256) == 0
+    assert smd.smd_plan_bf16q(5, 64, 256, 1 << 30).kernel == smd.SMD_KERNEL_MMA
+    p = smd.SmdPlan()
+    p.kernel = smd.SMD_KERNEL_TC_SPREAD
+    assert call_bf16q(B=2, H=128, W=64, force=p) == smd.SMD_ERR_WORKSPACE  # no workspace
+
+
 @pytest.mark.parametrize("B,H,W", [(5, 64, 256), (64, 128, 2048), (2, 16, 8192), (3, 48, 100)])
 def test_bf16q_plan_runs_the_warp_mma_kernel_with_both_query_tiles(B, H, W):
-    p = smd.smd_plan_bf16q(B, H, W)
+    p = smd.smd_plan_bf16q(B, H, W, 0)
     e = smd.smd_plan(B, H, W) if not (H % 128 == 0 and W <= 2048) else None
     assert p.kernel == smd.SMD_KERNEL_MMA
     assert p.split * p.key_cap >= W and p.smem_bytes <= 227 * 1024

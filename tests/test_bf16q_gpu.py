@@ -124,3 +124,75 @@ def test_bf16q_timeout_is_reported_and_the_context_survives(cuda):
     out_g, lse_g = bf16q_decode(case, cuda, tensors=t)
     out_o, lse_o = oracle_bf16q(case)
     check(out_g, lse_g, out_o, lse_o, "bf16q after a timeout")
+
+
+# ---- the split query on the spread tcgen05 kernel (smd_sparse_mla_decode_bf16q_ws) ------
+
+SPREAD = 5
+
+
+def bf16q_ws(case, dev, tensors=None, plan=None, expect_status=0):
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    nb = binding.smd_workspace_bytes_bf16q(case.B, case.H, case.W)
+    assert nb > 0
+    ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _, kv, idx, cnt = tensors if tensors is not None else to_dev(case, dev)
+    out, lse = binding.sparse_mla_decode_bf16q(q16_dev(case, dev), kv, idx, cnt, case.sm_scale,
+                                               case.k_scale, status=status, plan=plan,
+                                               workspace=ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == expect_status, binding.smd_status_str(int(status.item()))
+    return out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy()
+
+
+SPREAD_SHAPES = [
+    # (B, H, W, N, counts): one piece (no exchange), several, ragged, empty rows, a long row, H = 256
+    (3, 128, 300, 4000, [300, 0, 129]),
+    (4, 128, 2048, 20000, [2048, 1537, 513, 1]),
+    (2, 128, 9000, 40000, [9000, 4097]),
+    (2, 256, 700, 5000, [700, 512]),
+]
+
+
+@pytest.mark.parametrize("shape", SPREAD_SHAPES, ids=[f"B{s[0]}H{s[1]}W{s[2]}" for s in SPREAD_SHAPES])
+def test_bf16q_on_the_spread_kernel_matches_the_oracle(cuda, shape):
+    from sparse_mla_decode_gb300 import binding
+    B, H, W, N, counts = shape
+    case = inputs.random_case(B * 17 + W, B=B, H=H, W=W, N=N, counts=counts, heavy_frac=0.02)
+    assert binding.smd_plan_bf16q(B, H, W, 1 << 40).kernel == SPREAD
+    out_g, lse_g = bf16q_ws(case, cuda)
+    out_o, lse_o = oracle_bf16q(case)
+    check(out_g, lse_g, out_o, lse_o, f"bf16q spread {shape}")
+
+
+def test_bf16q_spread_grid_changes_no_bits(cuda):
+    case = inputs.random_case(99, B=10, H=128, W=2048, N=30000,
+                              counts=[2048, 5, 0, 1400, 700, 2048, 513, 1, 1999, 900])
+    t = to_dev(case, cuda)
+    ref = bf16q_ws(case, cuda, tensors=t)
+    for grid in (4, 9, 152):
+        out, lse = bf16q_ws(case, cuda, tensors=t, plan=dict(kernel=SPREAD, grid_x=grid))
+        assert np.array_equal(out, ref[0]), grid
+        assert np.array_equal(lse.view(np.uint32), ref[1].view(np.uint32)), grid
+
+
+def test_bf16q_spread_dsa_config_sampled(cuda):
+    case = inputs.config("dsa")
+    out_g, lse_g = bf16q_ws(case, cuda)
+    zero = np.where(case.counts == 0)[0][:1].tolist()
+    rows = [0, 9, 63] + zero
+    out_o, lse_o = oracle_bf16q(case, rows)
+    check(out_g[rows], lse_g[rows], out_o, lse_o, "bf16q spread dsa")
+
+
+def test_bf16q_spread_timeout_is_reported_and_the_context_survives(cuda):
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.random_case(100, B=3, H=128, W=1500, N=9000, counts=[1500, 600, 1200])
+    t = to_dev(case, cuda)
+    bf16q_ws(case, cuda, tensors=t, plan=dict(kernel=SPREAD, inject_stall=1, wait_budget_us=2000),
+             expect_status=binding.SMD_ERR_TIMEOUT)
+    out_g, lse_g = bf16q_ws(case, cuda, tensors=t)
+    out_o, lse_o = oracle_bf16q(case)
+    check(out_g, lse_g, out_o, lse_o, "bf16q spread after a timeout")
