@@ -18,6 +18,10 @@ ranks; ``e2e`` is the same metric through the public call with the step's
 inputs (q, indices, counts) copied from pinned host memory and its outputs
 (out, lse) copied back inside the timed region (the cache pool is resident).
 
+Besides the mean, the line gives the median of the flushed calls and, under
+``graph``, the warm per-call time of 100 back-to-back calls captured in one
+CUDA graph.
+
 ``--impl reference`` times the CPU oracle (the plain C restatement of the
 method) on the host cores, the only reference this method has.
 
@@ -225,18 +229,18 @@ def run_gpu(args, world, rank, local) -> dict | None:
     gptrs = ptrs[:8] + (group,) + ptrs[8:]
     bptrs = (q16.data_ptr(),) + ptrs[1:8] + (case.sm_scale, case.k_scale) + ptrs[11:]
 
-    def decode():
+    def decode(st=sptr):
         if bf16q and ws_bytes > 0:
             rc = binding.smd_sparse_mla_decode_bf16q_ws(*bptrs[:-1], workspace.data_ptr(), ws_bytes,
-                                                        sptr)
+                                                        st)
         elif bf16q:
-            rc = binding.smd_sparse_mla_decode_bf16q(*bptrs)
+            rc = binding.smd_sparse_mla_decode_bf16q(*bptrs[:-1], st)
         elif group > 1:
-            rc = binding.smd_sparse_mla_decode_grouped(*gptrs)
+            rc = binding.smd_sparse_mla_decode_grouped(*gptrs[:-1], st)
         elif ws_bytes > 0:
-            rc = binding.smd_sparse_mla_decode_ws(*ptrs[:-1], workspace.data_ptr(), ws_bytes, sptr)
+            rc = binding.smd_sparse_mla_decode_ws(*ptrs[:-1], workspace.data_ptr(), ws_bytes, st)
         else:
-            rc = binding.smd_sparse_mla_decode(*ptrs)
+            rc = binding.smd_sparse_mla_decode(*ptrs[:-1], st)
         if rc != 0:
             raise binding.SmdError(rc, "decode")
 
@@ -271,6 +275,7 @@ def run_gpu(args, world, rank, local) -> dict | None:
     times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     ms_local = float(np.mean(times_ms))
     ms, value = aggregate(stats["kv_gathered"], ms_local, world, dev)
+    graph = graph_timing(decode, dev)
 
     # ---- end to end through the public call: host buffers in, host buffers out.
     hq = (torch.from_numpy(case.q16.view(np.int16)).view(torch.bfloat16) if bf16q
@@ -382,6 +387,8 @@ def run_gpu(args, world, rank, local) -> dict | None:
         "gpu_launches": args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
+        "us_median": round(float(np.median(times_ms)) * 1e3, 3),
+        "graph": graph,
     }
     return line
 
@@ -444,6 +451,43 @@ def cpu_baseline(case, stats, seconds: float, bf16q: bool = False) -> dict:
             "kind": "oracle", "sample": sample, "us_per_call_sample": round(per_call * 1e6, 1)}
 
 
+def graph_timing(call, dev, calls: int = 100, replays: int = 5):
+    """The secondary timing: `calls` back-to-back calls captured in one CUDA
+    graph (no L2 flush between them: warm), replayed `replays` times; per-call
+    microseconds of the fastest and the median replay. None if the capture
+    fails."""
+    import torch
+    try:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            call(side.cuda_stream)
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cs = torch.cuda.current_stream(dev).cuda_stream
+            for _ in range(calls):
+                call(cs)
+        g.replay()
+        torch.cuda.synchronize()
+        per = []
+        for _ in range(replays):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            per.append(e0.elapsed_time(e1) * 1e3 / calls)
+        return {"calls": calls, "us_per_call_min": round(min(per), 3),
+                "us_per_call_median": round(float(np.median(per)), 3),
+                "note": "warm back-to-back calls in one CUDA graph, no L2 flush"}
+    except Exception as exc:  # a capture this build cannot do is reported, not fatal
+        torch.cuda.synchronize()
+        return {"error": str(exc)[:200]}
+
+
 def topk_bytes(case) -> dict:
     """Bytes the select must move at least once: the logits before each row's
     end, the index list and the counts."""
@@ -474,8 +518,8 @@ def run_topk(args, world, rank, local) -> dict | None:
     ptrs = (x.data_ptr(), case.L, ends.data_ptr(), case.B, case.L, case.K, idx.data_ptr(),
             cnt.data_ptr(), status.data_ptr(), stream.cuda_stream)
 
-    def select():
-        rc = binding.smd_topk_select(*ptrs)
+    def select(st=stream.cuda_stream):
+        rc = binding.smd_topk_select(*ptrs[:-1], st)
         if rc != 0:
             raise binding.SmdError(rc, "select")
 
@@ -505,8 +549,10 @@ def run_topk(args, world, rank, local) -> dict | None:
     clocks = sampler.stop() if sampler else None
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {int(status.item())}")
-    ms_local = float(np.mean([a.elapsed_time(b) for a, b in zip(starts, stops)]))
+    times_ms = [a.elapsed_time(b) for a, b in zip(starts, stops)]
+    ms_local = float(np.mean(times_ms))
     ms, value = aggregate(stats["logits"], ms_local, world, dev)
+    graph = graph_timing(select, dev)
 
     # end to end: logits and row ends from pinned host memory, indices and counts back
     hx = torch.from_numpy(case.logits.view(np.int16)).pin_memory()
@@ -569,6 +615,7 @@ def run_topk(args, world, rank, local) -> dict | None:
                 "d2h_bytes_per_step": int(hidx.numel() * 4 + hcnt.numel() * 4),
                 "note": "logits and row ends H2D from pinned memory; indices and counts D2H"},
         "gpu_launches": args.steps, "clocks": clocks, "wall_s_timed_region": round(wall, 4),
+        "us_median": round(float(np.median(times_ms)) * 1e3, 3), "graph": graph,
     }
 
 

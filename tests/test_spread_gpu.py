@@ -152,3 +152,38 @@ def test_dsa_config_through_the_workspace_call(cuda):
     check(out_g[rows], lse_g[rows], out_o, lse_o, "dsa spread")
     n = case.clamped_counts()
     assert np.all(np.isneginf(lse_g[n == 0])) and np.all(np.isfinite(lse_g[n > 0]))
+
+
+def test_spread_call_replays_in_a_cuda_graph(cuda):
+    """Captured once, replayed three times on one workspace: every replay gives
+    the eager call's bits (each call's flags are zeroed by their readers, so
+    the captured tokens never meet a stale flag)."""
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.random_case(75, B=5, H=128, W=2048, N=30000, counts=[2048, 700, 0, 1537, 2000])
+    q, kv, idx, cnt = to_dev(case, cuda)
+    ws = workspace_for(case, cuda, fill=7)
+    ref = spread(case, cuda, tensors=(q, kv, idx, cnt), ws=ws)
+    out = torch.empty((case.B, case.H, 512), dtype=torch.bfloat16, device=cuda)
+    lse = torch.empty((case.B, case.H), dtype=torch.float32, device=cuda)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    side = torch.cuda.Stream(cuda)
+    side.wait_stream(torch.cuda.current_stream(cuda))
+    with torch.cuda.stream(side):
+        binding.sparse_mla_decode(q, kv, idx, cnt, case.sm_scale, case.q_scale, case.k_scale,
+                                  out=out, lse=lse, status=status, plan=dict(kernel=SPREAD),
+                                  workspace=ws)
+    torch.cuda.current_stream(cuda).wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        binding.sparse_mla_decode(q, kv, idx, cnt, case.sm_scale, case.q_scale, case.k_scale,
+                                  out=out, lse=lse, status=status, plan=dict(kernel=SPREAD),
+                                  workspace=ws)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert np.array_equal(out.view(torch.int16).cpu().numpy().view(np.uint16), ref[0])
+        assert np.array_equal(lse.cpu().numpy().view(np.uint32), ref[1].view(np.uint32))
