@@ -197,9 +197,9 @@ def run_gpu(args, world, rank, local) -> dict | None:
     plan = binding.smd_plan_grouped(case.B, case.H, case.W, group).as_dict()
     # Where the library's workspace plan (the spread kernel) applies, the
     # workspace entry point is timed with a workspace of the size it asks for.
-    ws_bytes = binding.smd_workspace_bytes(case.B, case.H, case.W) if group == 1 else 0
+    ws_bytes = binding.smd_workspace_bytes_grouped(case.B, case.H, case.W, group)
     if ws_bytes > 0:
-        plan = binding.smd_plan_ws(case.B, case.H, case.W).as_dict()
+        plan = binding.smd_plan_grouped(case.B, case.H, case.W, group, ws_bytes).as_dict()
     if bf16q:  # with the workspace it asks for (the spread kernel where it applies)
         ws_bytes = binding.smd_workspace_bytes_bf16q(case.B, case.H, case.W)
         plan = binding.smd_plan_bf16q(case.B, case.H, case.W, ws_bytes).as_dict()
@@ -235,6 +235,9 @@ def run_gpu(args, world, rank, local) -> dict | None:
                                                         st)
         elif bf16q:
             rc = binding.smd_sparse_mla_decode_bf16q(*bptrs[:-1], st)
+        elif group > 1 and ws_bytes > 0:
+            rc = binding.smd_sparse_mla_decode_grouped_ws(*gptrs[:-1], workspace.data_ptr(),
+                                                          ws_bytes, st)
         elif group > 1:
             rc = binding.smd_sparse_mla_decode_grouped(*gptrs[:-1], st)
         elif ws_bytes > 0:

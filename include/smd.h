@@ -335,20 +335,47 @@ int smd_sparse_mla_decode_grouped(const uint8_t* q, const uint8_t* kv_pool, int6
                                   uint16_t* out, float* lse, int32_t* status,
                                   smd_stream_t stream);
 
-/* The plan smd_sparse_mla_decode_grouped would use (G > 1: kernel
- * SMD_KERNEL_TC_GROUP when G * H is 32 or 64 and W <= 8192, else
- * SMD_KERNEL_GROUP with tiles = G and window = keys of its ring of 64-key
- * slots). Host only. */
-int smd_plan_grouped(int32_t B, int32_t H, int32_t W, int32_t row_group, smd_plan_t* plan);
+/* The plan of the grouped call with a workspace of workspace_bytes (0: the
+ * plan of smd_sparse_mla_decode_grouped: G > 1: kernel SMD_KERNEL_TC_GROUP
+ * when G * H is 32 or 64 and W <= 8192, else SMD_KERNEL_GROUP with tiles = G
+ * and window = keys of its ring of 64-key slots; with a workspace the spread
+ * kernel where smd_sparse_mla_decode_grouped_ws takes it). Host only. */
+int smd_plan_grouped(int32_t B, int32_t H, int32_t W, int32_t row_group, int64_t workspace_bytes,
+                     smd_plan_t* plan);
 
-/* As smd_sparse_mla_decode_grouped, with kernel (SMD_KERNEL_GROUP or
- * SMD_KERNEL_TC_GROUP), split, window and the testing hooks taken from
- * `force` (0 = automatic; may be NULL). For the tests. */
+/* As smd_sparse_mla_decode_grouped, with a caller-owned device workspace of
+ * at least smd_workspace_bytes_grouped(B, H, W, row_group) bytes (16-byte
+ * aligned; else SMD_ERR_WORKSPACE). When G * H <= 128, B / G <= 1024 and
+ * W <= 16384 and the row-group tcgen05 kernel does not take the shapes
+ * (W > 8192, or G * H other than 32 and 64) the groups run on the spread
+ * tcgen05 kernel
+ * (SMD_KERNEL_TC_SPREAD): a group (all H heads of its G rows, G * H TMEM
+ * lanes) of n keys (its longest list) becomes ceil(n / 512) pieces over a
+ * cooperative grid, each lane masking the keys past its own row's count, the
+ * contract checked as in smd_sparse_mla_decode_grouped. Other shapes run as
+ * smd_sparse_mla_decode_grouped. The workspace needs no initialisation. */
+int smd_sparse_mla_decode_grouped_ws(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
+                                     const int32_t* indices, int32_t W, const int32_t* counts,
+                                     int32_t B, int32_t H, int32_t row_group,
+                                     float sm_scale, float q_scale, float k_scale,
+                                     uint16_t* out, float* lse, int32_t* status,
+                                     void* workspace, int64_t workspace_bytes,
+                                     smd_stream_t stream);
+
+/* Bytes of workspace smd_sparse_mla_decode_grouped_ws uses (0 where it runs
+ * the cluster kernels; row_group 1: smd_workspace_bytes). Host only. */
+int64_t smd_workspace_bytes_grouped(int32_t B, int32_t H, int32_t W, int32_t row_group);
+
+/* As smd_sparse_mla_decode_grouped_ws, with kernel (SMD_KERNEL_GROUP,
+ * SMD_KERNEL_TC_GROUP or SMD_KERNEL_TC_SPREAD), split, window, grid_x and the
+ * testing hooks taken from `force` (0 = automatic; may be NULL); workspace
+ * may be NULL unless the plan is the spread kernel. For the tests. */
 int smd_sparse_mla_decode_grouped_ex(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
                                      const int32_t* indices, int32_t W, const int32_t* counts,
                                      int32_t B, int32_t H, int32_t row_group,
                                      float sm_scale, float q_scale, float k_scale,
                                      uint16_t* out, float* lse, int32_t* status,
+                                     void* workspace, int64_t workspace_bytes,
                                      smd_stream_t stream, const smd_plan_t* force);
 
 /* The base-2 logit scale the kernels use: fp32(sm*q_s*k_s*log2 e),

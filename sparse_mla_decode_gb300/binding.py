@@ -79,8 +79,13 @@ def lib() -> ctypes.CDLL:
             grp_args = _DECODE_ARGS[:8] + [ctypes.c_int32] + _DECODE_ARGS[8:]
             so.smd_sparse_mla_decode_grouped.restype = ctypes.c_int
             so.smd_sparse_mla_decode_grouped.argtypes = grp_args
+            grp_ws = grp_args[:-1] + [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+            so.smd_sparse_mla_decode_grouped_ws.restype = ctypes.c_int
+            so.smd_sparse_mla_decode_grouped_ws.argtypes = grp_ws
             so.smd_sparse_mla_decode_grouped_ex.restype = ctypes.c_int
-            so.smd_sparse_mla_decode_grouped_ex.argtypes = grp_args + [ctypes.POINTER(SmdPlan)]
+            so.smd_sparse_mla_decode_grouped_ex.argtypes = grp_ws + [ctypes.POINTER(SmdPlan)]
+            so.smd_workspace_bytes_grouped.restype = ctypes.c_int64
+            so.smd_workspace_bytes_grouped.argtypes = [ctypes.c_int32] * 4
             bq_args = ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
                         ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
                         ctypes.c_float, ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
@@ -105,7 +110,8 @@ def lib() -> ctypes.CDLL:
             so.smd_topk_select_ex.restype = ctypes.c_int
             so.smd_topk_select_ex.argtypes = tk_args + [ctypes.c_int32]
             so.smd_plan_grouped.restype = ctypes.c_int
-            so.smd_plan_grouped.argtypes = [ctypes.c_int32] * 4 + [ctypes.POINTER(SmdPlan)]
+            so.smd_plan_grouped.argtypes = [ctypes.c_int32] * 4 + [ctypes.c_int64,
+                                                                   ctypes.POINTER(SmdPlan)]
             so.smd_workspace_bytes.restype = ctypes.c_int64
             so.smd_workspace_bytes.argtypes = [ctypes.c_int32] * 3
             so.smd_workspace_bytes_ex.restype = ctypes.c_int64
@@ -169,18 +175,31 @@ def smd_sparse_mla_decode_grouped(q, kv_pool, N, indices, W, counts, B, H, row_g
                                                status, stream)
 
 
+def smd_sparse_mla_decode_grouped_ws(q, kv_pool, N, indices, W, counts, B, H, row_group,
+                                     sm_scale, q_scale, k_scale, out, lse, status, workspace,
+                                     workspace_bytes, stream) -> int:
+    return lib().smd_sparse_mla_decode_grouped_ws(q, kv_pool, N, indices, W, counts, B, H,
+                                                  row_group, sm_scale, q_scale, k_scale, out,
+                                                  lse, status, workspace, workspace_bytes, stream)
+
+
 def smd_sparse_mla_decode_grouped_ex(q, kv_pool, N, indices, W, counts, B, H, row_group,
-                                     sm_scale, q_scale, k_scale, out, lse, status, stream,
-                                     force: SmdPlan | None) -> int:
+                                     sm_scale, q_scale, k_scale, out, lse, status, workspace,
+                                     workspace_bytes, stream, force: SmdPlan | None) -> int:
     ref = ctypes.byref(force) if force is not None else None
     return lib().smd_sparse_mla_decode_grouped_ex(q, kv_pool, N, indices, W, counts, B, H,
                                                   row_group, sm_scale, q_scale, k_scale, out,
-                                                  lse, status, stream, ref)
+                                                  lse, status, workspace, workspace_bytes,
+                                                  stream, ref)
 
 
-def smd_plan_grouped(B: int, H: int, W: int, row_group: int) -> SmdPlan:
+def smd_workspace_bytes_grouped(B: int, H: int, W: int, row_group: int) -> int:
+    return int(lib().smd_workspace_bytes_grouped(B, H, W, row_group))
+
+
+def smd_plan_grouped(B: int, H: int, W: int, row_group: int, workspace_bytes: int = 0) -> SmdPlan:
     p = SmdPlan()
-    rc = lib().smd_plan_grouped(B, H, W, row_group, ctypes.byref(p))
+    rc = lib().smd_plan_grouped(B, H, W, row_group, int(workspace_bytes), ctypes.byref(p))
     if rc != SMD_OK:
         raise SmdError(rc, "smd_plan_grouped")
     return p
@@ -337,13 +356,13 @@ def sparse_mla_decode(q, kv_pool, indices, counts, sm_scale: float, q_scale: flo
             setattr(p, k, int(v))
         plan = p
     if row_group != 1:
-        if workspace is not None:
-            raise ValueError("the grouped decode takes no workspace")
         g_args = args[:8] + (int(row_group),) + args[8:]
-        if plan is None:
-            rc = smd_sparse_mla_decode_grouped(*g_args, int(stream))
+        if plan is not None:
+            rc = smd_sparse_mla_decode_grouped_ex(*g_args, *ws, int(stream), plan)
+        elif workspace is not None:
+            rc = smd_sparse_mla_decode_grouped_ws(*g_args, *ws, int(stream))
         else:
-            rc = smd_sparse_mla_decode_grouped_ex(*g_args, int(stream), plan)
+            rc = smd_sparse_mla_decode_grouped(*g_args, int(stream))
         if rc != SMD_OK:
             raise SmdError(rc, "smd_sparse_mla_decode_grouped")
         return out, lse

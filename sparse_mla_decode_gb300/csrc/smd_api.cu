@@ -249,30 +249,37 @@ int plan_group(int B, int H, int W, int G, int sm_count, const smd_plan_t* force
     return SMD_OK;
 }
 
-// The spread kernel: 128 heads per CTA (or all H < 128), pieces of at most
-// kTcMaxKeys keys, at most kTcsMaxPieces pieces per row.
-bool tcs_fits(int B, int H, int W) {
-    return (H % kTcHeads == 0 || H < kTcHeads) && W >= 1 && W <= kTcsMaxPieces * kTcMaxKeys &&
-           static_cast<int64_t>(B) * ceil_div(H, kTcHeads) <= kTcsMaxUnits;
+// The spread kernel: 128 heads per CTA (or all H < 128), or all H heads of a
+// group of G rows (G * H <= 128 lanes); pieces of at most kTcMaxKeys keys, at
+// most kTcsMaxPieces pieces per unit.
+int64_t tcs_units(int B, int H, int G) {
+    return G > 1 ? B / G : static_cast<int64_t>(B) * ceil_div(H, kTcHeads);
 }
 
-int64_t tcs_items_cap(int B, int H, int W) {
-    return static_cast<int64_t>(B) * ceil_div(H, kTcHeads) * ceil_div(W, kTcMaxKeys);
+bool tcs_fits(int B, int H, int W, int G = 1) {
+    const bool lanes_ok = G > 1 ? (B % G == 0 && G * H <= kTcHeads)
+                                : (H % kTcHeads == 0 || H < kTcHeads);
+    return lanes_ok && W >= 1 && W <= kTcsMaxPieces * kTcMaxKeys &&
+           tcs_units(B, H, G) <= kTcsMaxUnits;
+}
+
+int64_t tcs_items_cap(int B, int H, int W, int G = 1) {
+    return tcs_units(B, H, G) * ceil_div(W, kTcMaxKeys);
 }
 
 // The spread kernel's plan: one CTA per resident slot, no more than there can
 // be pieces (a forced grid_x caps it).
 int plan_tcs(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_plan_t* out,
-             TcsConfig* cfg) {
-    if (!tcs_fits(B, H, W)) return SMD_ERR_PLAN;
-    const int lanes = std::min(H, kTcHeads);
+             TcsConfig* cfg, int G = 1) {
+    if (!tcs_fits(B, H, W, G)) return SMD_ERR_PLAN;
+    const int lanes = G > 1 ? G * H : std::min(H, kTcHeads);
     if (force && ((force->tiles && force->tiles != lanes / kHeadsPerTile) ||
                   (force->window && force->window != kTcChunk) || force->split))
         return SMD_ERR_PLAN;
     // Resident CTAs (one per SM); without a device, planning assumes one per SM.
     int max_grid = tcs_max_grid();
     if (max_grid <= 0) max_grid = sm_count;
-    const int64_t items = tcs_items_cap(B, H, W);
+    const int64_t items = tcs_items_cap(B, H, W, G);
     int grid = static_cast<int>(std::min<int64_t>(max_grid, items));
     if (force && force->grid_x) {
         if (force->grid_x < 1 || force->grid_x > max_grid) return SMD_ERR_PLAN;
@@ -280,6 +287,7 @@ int plan_tcs(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
         if (force->grid_x < std::min(kTcsMaxPieces, ceil_div(W, kTcMaxKeys))) return SMD_ERR_PLAN;
         grid = std::min<int64_t>(force->grid_x, items);
     }
+    cfg->G = G;
     cfg->grid = grid;
     cfg->items_cap = static_cast<int>(items);
     cfg->wait_budget_ns = (force && force->wait_budget_us > 0)
@@ -298,6 +306,18 @@ int plan_tcs(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
     out->threads = kTcThreads;
     out->smem_bytes = tcs_smem_bytes();
     return SMD_OK;
+}
+
+// Row groups with a workspace run on the spread kernel where the row-group
+// tcgen05 kernel does not take them (longer lists, other lane counts): with
+// up to 16 pieces per group and half the TMEM lanes real, its exchange
+// through L2 costs more than the cluster kernel's on-chip one.
+bool grouped_spread(int B, int H, int W, int G) {
+    return tcs_fits(B, H, W, G) && !tcg_fits(H, W, G);
+}
+
+int64_t grouped_workspace_bytes(int B, int H, int W, int G) {
+    return grouped_spread(B, H, W, G) ? tcs_workspace(tcs_items_cap(B, H, W, G)).total : 0;
 }
 
 // With a workspace, the spread kernel takes rows longer than a cluster holds
@@ -385,9 +405,35 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
 
     if (row_group > 1) {
         if (B % row_group != 0) return SMD_ERR_SHAPE;
+        if (workspace != nullptr && !aligned(workspace, 16)) return SMD_ERR_WORKSPACE;
         const int want = (force && force->kernel) ? force->kernel
+                         : (workspace != nullptr && grouped_spread(B, H, W, row_group)) ? SMD_KERNEL_TC_SPREAD
                          : tcg_fits(H, W, row_group) ? SMD_KERNEL_TC_GROUP
                                                      : SMD_KERNEL_GROUP;
+        if (want == SMD_KERNEL_TC_SPREAD) {
+            smd_plan_t plan{};
+            TcsConfig scfg{};
+            const int rc = plan_tcs(B, H, W, sm_count_of_device(), force, &plan, &scfg, row_group);
+            if (rc != SMD_OK) return rc;
+            if (workspace == nullptr || workspace_bytes < tcs_workspace(scfg.items_cap).total)
+                return SMD_ERR_WORKSPACE;
+            scfg.ws = workspace;
+            CallArgs a{};
+            a.q = q;
+            a.kv = kv_pool;
+            a.N = N;
+            a.indices = indices;
+            a.W = W;
+            a.counts = counts;
+            a.B = B;
+            a.H = H;
+            a.scale_log2 = scale_log2_of(sm_scale, q_scale, k_scale);
+            a.k_scale = k_scale;
+            a.out = out;
+            a.lse = lse;
+            a.status = status;
+            return launch_tcs(a, scfg, reinterpret_cast<cudaStream_t>(stream));
+        }
         smd_plan_t plan{};
         GroupConfig gcfg{};
         TcgConfig tcfg{};
@@ -634,24 +680,46 @@ int smd_sparse_mla_decode_grouped(const uint8_t* q, const uint8_t* kv_pool, int6
                        lse, status, nullptr, 0, stream, nullptr, false, row_group);
 }
 
+int smd_sparse_mla_decode_grouped_ws(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
+                                     const int32_t* indices, int32_t W, const int32_t* counts,
+                                     int32_t B, int32_t H, int32_t row_group, float sm_scale,
+                                     float q_scale, float k_scale, uint16_t* out, float* lse,
+                                     int32_t* status, void* workspace, int64_t workspace_bytes,
+                                     smd_stream_t stream) {
+    return smd::decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale, out,
+                       lse, status, workspace, workspace_bytes, stream, nullptr, false, row_group);
+}
+
 int smd_sparse_mla_decode_grouped_ex(const uint8_t* q, const uint8_t* kv_pool, int64_t N,
                                      const int32_t* indices, int32_t W, const int32_t* counts,
                                      int32_t B, int32_t H, int32_t row_group, float sm_scale,
                                      float q_scale, float k_scale, uint16_t* out, float* lse,
-                                     int32_t* status, smd_stream_t stream,
-                                     const smd_plan_t* force) {
+                                     int32_t* status, void* workspace, int64_t workspace_bytes,
+                                     smd_stream_t stream, const smd_plan_t* force) {
     return smd::decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale, out,
-                       lse, status, nullptr, 0, stream, force, false, row_group);
+                       lse, status, workspace, workspace_bytes, stream, force, false, row_group);
 }
 
-int smd_plan_grouped(int32_t B, int32_t H, int32_t W, int32_t row_group, smd_plan_t* plan) {
+int64_t smd_workspace_bytes_grouped(int32_t B, int32_t H, int32_t W, int32_t row_group) {
+    if (row_group == 1) return smd_workspace_bytes(B, H, W);
+    if (B < 0 || W < 0 || H <= 0 || H % smd::kHeadsPerTile != 0) return 0;
+    if ((row_group != 2 && row_group != 4) || B % row_group != 0) return 0;
+    return smd::grouped_workspace_bytes(B, H, W, row_group);
+}
+
+int smd_plan_grouped(int32_t B, int32_t H, int32_t W, int32_t row_group, int64_t workspace_bytes,
+                     smd_plan_t* plan) {
     if (!plan) return SMD_ERR_NULL;
-    if (row_group == 1) return smd_plan(B, H, W, plan);
+    if (row_group == 1)
+        return workspace_bytes > 0 ? smd_plan_ws(B, H, W, plan) : smd_plan(B, H, W, plan);
     if (B < 0 || W < 0 || H <= 0 || H % smd::kHeadsPerTile != 0) return SMD_ERR_SHAPE;
     if ((row_group != 2 && row_group != 4) || B % row_group != 0) return SMD_ERR_SHAPE;
     smd_plan_t p{};
     int rc;
-    if (smd::tcg_fits(H, W, row_group)) {
+    if (workspace_bytes > 0 && smd::grouped_spread(B, H, W, row_group)) {
+        smd::TcsConfig cfg{};
+        rc = smd::plan_tcs(B, H, W, smd::sm_count_of_device(), nullptr, &p, &cfg, row_group);
+    } else if (smd::tcg_fits(H, W, row_group)) {
         smd::TcgConfig cfg{};
         rc = smd::plan_tcg(B, H, W, row_group, nullptr, &p, &cfg);
         p.smem_bytes = smd::tcg_smem_bytes();

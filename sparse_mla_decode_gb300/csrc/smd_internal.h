@@ -249,6 +249,7 @@ __host__ __device__ inline TcsWorkspace tcs_workspace(int64_t items, int64_t qro
 }
 
 struct TcsConfig {
+    int G;          // rows per unit (row groups sharing one index list; 1 = per row)
     int grid;       // CTAs (at most the resident CTAs of the device)
     int items_cap;  // item slots in the workspace: units * ceil(W / 512)
     int qsplit;     // 1: bf16 query (CallArgs::q16), split into the workspace first

@@ -74,9 +74,10 @@ struct TcsMaps {
 
 struct TcsParams {
     CallArgs a;
-    int32_t HG;      // head groups per row (ceil(H / 128))
-    int32_t lanes;   // heads a CTA computes (min(H, 128)); the other TMEM lanes are padding
-    int32_t units;   // B * HG
+    int32_t HG;      // head groups per row (ceil(H / 128); 1 for row groups)
+    int32_t G;       // rows per unit: 1, or the row group (rows sharing one index list)
+    int32_t lanes;   // query rows a unit computes (min(H, 128), or G * H); the rest is padding
+    int32_t units;   // B / G * HG
     int32_t grid;    // CTAs
     float log2_448;
     uint64_t budget_ns;
@@ -87,16 +88,23 @@ struct TcsParams {
     const float* lamh;  // the split query's per-row logit scales [B * H], or null
 };
 
-// The logit scale of head h (0 .. 127) of the item's group.
-__device__ __forceinline__ float lam_of(const TcsParams& p, int b, int g, int h) {
-    if (p.lamh == nullptr) return p.a.scale_log2;
-    return h < p.lanes ? p.lamh[static_cast<int64_t>(b) * p.a.H + g * kTcHeads + h] : 0.f;
-}
-
+// A unit is G consecutive query rows b0 .. b0 + G - 1 (G = 1: one row) and
+// head group g; its TMEM lane h (h < lanes) is query row (b0 H + g 128 + h) of
+// the [B * H, 576] query, whose own key count is that of row b0 + h / H. Its
+// keys are the list of its row with the most keys (`ref`, the first such);
+// the other rows read prefixes of it (the row-group contract).
 struct Item {
-    int b, g, s, j, item0;  // row, head group, items of the unit, this piece, the unit's first item
-    int first, mine, nch;   // keys of this piece
+    int b0, g, s, j, item0;  // first row, head group, items of the unit, this piece, its first item
+    int ref, n;              // the row (0 .. G - 1) whose list the unit reads, and its count
+    int first, mine, nch;    // keys of this piece
+    int64_t row0;            // the unit's first query row (b0 * H + g * 128)
 };
+
+// The logit scale of lane h of the unit at query row row0.
+__device__ __forceinline__ float lam_of(const TcsParams& p, int64_t row0, int h) {
+    if (p.lamh == nullptr) return p.a.scale_log2;
+    return h < p.lanes ? p.lamh[row0 + h] : 0.f;
+}
 
 __device__ __forceinline__ float4 ld_cg_v4(const float* p) {
     float4 v;
@@ -152,6 +160,26 @@ __device__ __forceinline__ int clamped_count(const TcsParams& p, int b) {
 
 __device__ __forceinline__ int pieces_of(int n) { return (n + kTcMaxKeys - 1) / kTcMaxKeys; }
 
+// The most keys any row of unit u holds, and the first row holding them.
+__device__ __forceinline__ int unit_count(const TcsParams& p, int u, int* ref = nullptr) {
+    const int b0 = (u / p.HG) * p.G;
+    int n = -1, r0 = 0;
+    for (int r = 0; r < p.G; ++r) {
+        const int c = clamped_count(p, b0 + r);
+        if (c > n) {
+            n = c;
+            r0 = r;
+        }
+    }
+    if (ref != nullptr) *ref = r0;
+    return n;
+}
+
+// Keys lane h of the item reads: those of its own row (padding lanes: none).
+__device__ __forceinline__ int lane_count(const TcsParams& p, int b0, int h) {
+    return h < p.lanes ? clamped_count(p, b0 + h / p.a.H) : 0;
+}
+
 // The shared-memory addresses and barriers of the chunk pipeline.
 __device__ __forceinline__ tcc::Pipe pipe_of(const TcsParams& p, uint32_t base, uint32_t bars,
                                              const uint8_t* smem) {
@@ -180,8 +208,8 @@ __device__ __forceinline__ void scan_units(const TcsParams& p, uint8_t* smem) {
     int32_t* wsum = reinterpret_cast<int32_t*>(smem + kOffWarpSum);
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int u0 = 2 * t, u1 = 2 * t + 1;
-    const int s0 = u0 < p.units ? pieces_of(clamped_count(p, u0 / p.HG)) : 0;
-    const int s1 = u1 < p.units ? pieces_of(clamped_count(p, u1 / p.HG)) : 0;
+    const int s0 = u0 < p.units ? pieces_of(unit_count(p, u0)) : 0;
+    const int s1 = u1 < p.units ? pieces_of(unit_count(p, u1)) : 0;
     const int v = s0 + s1;
     int x = v;
 #pragma unroll
@@ -220,12 +248,14 @@ __device__ __forceinline__ Item item_of(const TcsParams& p, const uint8_t* smem,
             hi = mid - 1;
     }
     Item it;
-    it.b = lo / p.HG;
-    it.g = lo - it.b * p.HG;
+    it.b0 = (lo / p.HG) * p.G;
+    it.g = lo % p.HG;
+    it.row0 = static_cast<int64_t>(it.b0) * p.a.H + it.g * kTcHeads;
     it.item0 = pre[lo];
     it.s = pre[lo + 1] - pre[lo];
     it.j = i - it.item0;
-    const int n = clamped_count(p, it.b);
+    const int n = unit_count(p, lo, &it.ref);
+    it.n = n;
     const int per = (n + it.s - 1) / it.s;
     it.first = min(n, it.j * per);
     it.mine = min(n - it.first, per);
@@ -241,8 +271,7 @@ __device__ __forceinline__ void zero_empty_units(const TcsParams& p, const uint8
     const int t = threadIdx.x - t0;
     for (int u = blockIdx.x; u < p.units; u += p.grid) {
         if (pre[u + 1] != pre[u]) continue;
-        const int b = u / p.HG, g = u - b * p.HG;
-        const int64_t row0 = static_cast<int64_t>(b) * p.a.H + g * kTcHeads;
+        const int64_t row0 = static_cast<int64_t>((u / p.HG) * p.G) * p.a.H + (u % p.HG) * kTcHeads;
         uint4* dst = reinterpret_cast<uint4*>(p.a.out + row0 * kLatent);
         for (int e = t; e < p.lanes * (kLatent / 8); e += nthreads) dst[e] = make_uint4(0u, 0u, 0u, 0u);
         for (int h = t; h < p.lanes; h += nthreads) p.a.lse[row0 + h] = -INFINITY;
@@ -272,12 +301,32 @@ __device__ __forceinline__ void init_bars(uint32_t bars, bool again) {
 // Entries past its keys name pool row 0 (a real row: finite bytes; its P is 0).
 // This item's key indices, two per producer thread (entries past its keys: 0).
 __device__ __forceinline__ void load_idx(const TcsParams& p, const Item& it, int32_t (&v)[2]) {
-    const int32_t* row_idx = p.a.indices + static_cast<int64_t>(it.b) * p.a.W + it.first;
+    const int32_t* row_idx = p.a.indices + static_cast<int64_t>(it.b0 + it.ref) * p.a.W + it.first;
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
         const int i = threadIdx.x + u * kProducerThreads;
         v[u] = (i < it.mine) ? row_idx[i] : 0;
     }
+}
+
+// The row-group contract on this piece's keys: every other row of the unit
+// agrees with the staged list on its own first count entries; a mismatch
+// writes SMD_ERR_GROUP to the status (producer threads).
+__device__ __forceinline__ void check_contract(const TcsParams& p, const int32_t* idx_s,
+                                               const Item& it) {
+    const int t = threadIdx.x;
+    bool bad = false;
+    for (int r = 0; r < p.G; ++r) {
+        if (r == it.ref) continue;
+        const int lim = min(it.mine, clamped_count(p, it.b0 + r) - it.first);
+        const int32_t* row_idx = p.a.indices + static_cast<int64_t>(it.b0 + r) * p.a.W + it.first;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int i = t + u * kProducerThreads;
+            if (i < lim && row_idx[i] != idx_s[i]) bad = true;
+        }
+    }
+    if (bad && p.a.status != nullptr) atomicCAS(p.a.status, 0, SMD_ERR_GROUP);
 }
 
 // `pre` holds this item's indices when `have` (loaded early for the first item).
@@ -292,7 +341,16 @@ __device__ __forceinline__ void producer_a(const TcsMaps& maps, const TcsParams&
     idx_s[t + kProducerThreads] = v[1];
     asm volatile("bar.sync 1, %0;" ::"r"(kProducerThreads) : "memory");
     uint32_t seen[2] = {0u, 0u};
-    tcc::gather_pass_a(maps.kv, maps.kv_tail, pp, 0, it.nch, seen, ok);
+    if (p.G == 1) {
+        tcc::gather_pass_a(maps.kv, maps.kv_tail, pp, 0, it.nch, seen, ok);
+        return;
+    }
+    // Row groups: the contract is checked once the first chunks' gathers are
+    // in flight (it changes nothing but the status).
+    const int head = min(it.nch, pp.q_lo ? 1 : 2);
+    tcc::gather_pass_a(maps.kv, maps.kv_tail, pp, 0, head, seen, ok);
+    check_contract(p, idx_s, it);
+    tcc::gather_pass_a(maps.kv, maps.kv_tail, pp, head, it.nch, seen, ok);
 }
 
 // ---- warps 12-15: the row maximum (thread h = head h = TMEM lane h) ---------------
@@ -303,7 +361,8 @@ __device__ __forceinline__ void row_max(const TcsParams& p, uint8_t* smem, uint3
                                         uint32_t tmem, const Item& it, int item, bool& ok) {
     const int h = threadIdx.x & 127;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * ((threadIdx.x >> 5) & 3)) << 16);
-    const float lam = lam_of(p, it.b, it.g, h);
+    const float lam = lam_of(p, it.row0, h);
+    const int lim_row = lane_count(p, it.b0, h) - it.first;  // this lane's keys in the piece
     float m = -INFINITY;
     for (int c = 0; c < it.nch; ++c) {
         mbar_wait(bars + 8 * (kBarS + c), 0, ok, p.a.status, p.budget_ns);
@@ -311,10 +370,10 @@ __device__ __forceinline__ void row_max(const TcsParams& p, uint8_t* smem, uint3
         if (!ok) break;
         tc_fence_after();
         const int cnt = min(kTcChunk, it.mine - kTcChunk * c);
-        for (int q = 0; 32 * q < cnt; ++q) {
+        for (int q = 0; 32 * q < cnt; ++q) {  // warp-uniform; lanes mask their own keys
             float v[32];
             tmem_ld32(lane_base + kTcChunk * c + 32 * q, v);
-            const int lim = cnt - 32 * q;
+            const int lim = min(cnt, lim_row - kTcChunk * c) - 32 * q;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
                 if (j < lim) m = fmaxf(m, lam * v[j]);
@@ -350,12 +409,14 @@ __device__ __forceinline__ void p_phase(const TcsParams& p, uint8_t* smem, uint3
     const int h = 32 * (warp & 3) + (threadIdx.x & 31);
     const int j = warp >> 2;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-    const float lam = lam_of(p, it.b, it.g, h);
+    const float lam = lam_of(p, it.row0, h);
     const float bias = reinterpret_cast<const float*>(smem + kOffRowMax)[h] - p.log2_448;
+    const int lim_row = lane_count(p, it.b0, h) - it.first;  // this lane's keys in the piece
     float l = 0.f;
     for (int c = 0; c < it.nch && ok; ++c) {
-        const int lim = min(kTcChunk, it.mine - kTcChunk * c) - 32 * j;
-        if (lim <= 0) continue;  // warp-uniform
+        const int cnt = min(kTcChunk, it.mine - kTcChunk * c);
+        if (32 * j >= cnt) continue;  // warp-uniform
+        const int lim = min(cnt, lim_row - kTcChunk * c) - 32 * j;  // per lane
         uint8_t* row = smem + kOffQP + c * kBlock + (h >> 3) * 1024 + (h & 7) * 128;
         float v[32];
         tmem_ld32(lane_base + kTcChunk * c + 32 * j, v);
@@ -429,7 +490,7 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
     const float l = ((lsum[h] + lsum[128 + h]) + lsum[256 + h]) + lsum[384 + h];
     const float m = reinterpret_cast<const float*>(smem + kOffRowMax)[h];
     const bool have_o = ok && it.mine > 0;  // O in TMEM is defined only if PV ran
-    const int64_t row0 = static_cast<int64_t>(it.b) * p.a.H + it.g * kTcHeads;
+    const int64_t row0 = it.row0;
     uint16_t* oblock = p.a.out + row0 * kLatent;
     float* lse = p.a.lse + row0 + h;
     uint8_t* stage = smem + kOffRing;  // the ring is dead once O is complete
@@ -483,6 +544,7 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
 #pragma unroll
             for (int i = 0; i < 16; ++i) v[i] = 0.f;
         }
+        if (h >= p.lanes) continue;  // padding lanes are never merged
         float* dst = mine_part + ((col >> 2) * kTcHeads + h) * 4;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -526,7 +588,7 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = 0.f + acc[i];
-        for (int k = 1; k < s; ++k) {
+        for (int k = 1; k < s && h < p.lanes; ++k) {
             const float* src = part + static_cast<int64_t>(it.item0 + partner(j, k, s)) * kPartFloats +
                                ((col >> 2) * kTcHeads + h) * 4;
             float4 x[4];
@@ -586,7 +648,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // sends, so its bounded wait runs out; a test hook.)
             const bool split = p.lamh != nullptr;
             mbar_arrive_expect_tx(bars + 8 * kBarQ, (split ? 2 : 1) * kTile + (p.inject_stall ? 16 : 0));
-            const int y = it.b * p.a.H + it.g * kTcHeads;
+            const int y = static_cast<int>(it.row0);
             for (int c = 0; c < 4; ++c)
                 tma_load_2d(base + kOffQP + c * kBlock, &maps.q, 128 * c, y, bars + 8 * kBarQ);
             tma_load_2d(base + kOffQP + 4 * kBlock, &maps.q_tail, 512, y, bars + 8 * kBarQ);
@@ -718,9 +780,10 @@ int launch_tcs(const CallArgs& a, const TcsConfig& cfg, cudaStream_t stream) {
     if (max_grid <= 0 || cfg.grid > max_grid) return SMD_ERR_LAUNCH;
     TcsParams prm{};
     prm.a = a;
-    prm.HG = (a.H + kTcHeads - 1) / kTcHeads;
-    prm.lanes = a.H < kTcHeads ? a.H : kTcHeads;
-    prm.units = a.B * prm.HG;
+    prm.G = cfg.G > 1 ? cfg.G : 1;
+    prm.HG = prm.G > 1 ? 1 : (a.H + kTcHeads - 1) / kTcHeads;
+    prm.lanes = prm.G > 1 ? prm.G * a.H : (a.H < kTcHeads ? a.H : kTcHeads);
+    prm.units = a.B / prm.G * prm.HG;
     prm.grid = cfg.grid;
     prm.log2_448 = static_cast<float>(std::log2(448.0));
     prm.budget_ns = cfg.wait_budget_ns;

@@ -183,7 +183,7 @@ def call_grouped(G, B=8, H=16, W=64, q=A, counts=A, force=None):
         return smd.smd_sparse_mla_decode_grouped(q, A, 100, A, W, counts, B, H, G, 0.1, 0.1, 0.1,
                                                  A, A, 0, 0)
     return smd.smd_sparse_mla_decode_grouped_ex(q, A, 100, A, W, counts, B, H, G, 0.1, 0.1, 0.1,
-                                                A, A, 0, 0, force)
+                                                A, A, 0, 0, 0, 0, force)
 
 
 @pytest.mark.parametrize("kw,code", [

@@ -139,3 +139,94 @@ def test_dense_as_sparse_full_size_sampled_rows(cuda):
     for plan in (None, dict(kernel=MMA_GROUP)):
         out_g, lse_g = grouped(case, cuda, 4, plan=plan, tensors=t)
         check(out_g[rows], lse_g[rows], out_o, lse_o, f"dense grouped sampled {plan}")
+
+
+# ---- row groups on the spread tcgen05 kernel (smd_sparse_mla_decode_grouped_ws) ----------
+
+SPREAD = 5
+
+
+def grouped_ws(case, dev, G, tensors=None, plan=None, expect_status=0):
+    """The grouped workspace call; the spread kernel unless `plan` says otherwise."""
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    # the spread kernel's size: one unit per group, like B / G rows of 128 heads
+    nb = binding.smd_workspace_bytes_ex(case.B // G, 128, case.W, dict(kernel=SPREAD))
+    assert nb > 0
+    ws = torch.zeros(nb, dtype=torch.uint8, device=dev)
+    plan = dict(kernel=SPREAD) if plan is None else plan
+    q, kv, idx, cnt = tensors if tensors is not None else to_dev(case, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out, lse = binding.sparse_mla_decode(q, kv, idx, cnt, case.sm_scale, case.q_scale,
+                                         case.k_scale, status=status, plan=plan, row_group=G,
+                                         workspace=ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == expect_status, binding.smd_status_str(int(status.item()))
+    return out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy()
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"R{s[0]}G{s[1]}H{s[2]}W{s[3]}" for s in SHAPES])
+def test_groups_on_the_spread_kernel(cuda, shape):
+    R, G, H, W, N, counts = shape
+    case = inputs.grouped_case(10 * R + G + W, R, G, H, W, N, counts)
+    t = to_dev(case, cuda)
+    out_o, lse_o = oracle_decode(case)
+    out_g, lse_g = grouped_ws(case, cuda, G, tensors=t)
+    check(out_g, lse_g, out_o, lse_o, f"grouped spread {shape}")
+    from sparse_mla_decode_gb300 import binding
+    # with a workspace the automatic plan takes the spread kernel only where
+    # the row-group tcgen05 kernel does not fit
+    want = SPREAD if G * H not in (32, 64) or W > 8192 else TC_GROUP
+    assert binding.smd_plan_grouped(case.B, H, W, G, 1 << 40).kernel == want
+
+
+def test_groups_on_the_spread_kernel_grid_changes_no_bits(cuda):
+    case = inputs.grouped_case(47, 6, 4, 16, 5000, 40000,
+                               [5000, 4999, 4000, 12, 0, 0, 0, 0, 700, 701, 702, 703,
+                                2048, 2047, 10, 1, 3000, 3000, 3000, 3000, 513, 1, 0, 512])
+    t = to_dev(case, cuda)
+    ref = grouped_ws(case, cuda, 4, tensors=t)
+    for grid in (10, 31, 152):
+        out, lse = grouped_ws(case, cuda, 4, tensors=t, plan=dict(kernel=SPREAD, grid_x=grid))
+        assert np.array_equal(out, ref[0]), grid
+        assert np.array_equal(lse.view(np.uint32), ref[1].view(np.uint32)), grid
+    out_o, lse_o = oracle_decode(case)
+    check(ref[0], ref[1], out_o, lse_o, "grouped spread grid")
+
+
+def test_groups_on_the_spread_kernel_report_a_broken_contract(cuda):
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.grouped_case(44, 2, 4, 16, 256, 4000, [256, 255, 254, 253, 200, 256, 100, 7])
+    case.indices[6, 50] = (case.indices[5, 50] + 1) % case.N
+    t = to_dev(case, cuda)
+    out_g, lse_g = grouped_ws(case, cuda, 4, tensors=t, expect_status=binding.SMD_ERR_GROUP)
+    out_o, lse_o = oracle_decode(case, rows=[0, 1, 2, 3])
+    check(out_g[:4], lse_g[:4], out_o, lse_o, "grouped spread, the group that keeps the contract")
+
+
+def test_groups_longer_than_the_row_group_kernel_takes(cuda):
+    """Lists of 12000 keys: the workspace call's automatic plan is the spread
+    kernel (the row-group tcgen05 kernel stops at 8192)."""
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.grouped_case(48, 2, 4, 16, 12000, 60000, [12000, 11999, 9000, 3, 500, 0, 0, 0])
+    nb = binding.smd_workspace_bytes_grouped(case.B, case.H, case.W, 4)
+    assert nb > 0 and binding.smd_plan_grouped(case.B, 16, 12000, 4, nb).kernel == SPREAD
+    q, kv, idx, cnt = to_dev(case, cuda)
+    ws = torch.zeros(nb, dtype=torch.uint8, device=cuda)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    out, lse = binding.sparse_mla_decode(q, kv, idx, cnt, case.sm_scale, case.q_scale,
+                                         case.k_scale, status=status, row_group=4, workspace=ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    out_o, lse_o = oracle_decode(case)
+    check(out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy(), out_o, lse_o,
+          "grouped spread 12000")
+
+
+def test_dense_as_sparse_on_the_spread_kernel_sampled(cuda):
+    case = inputs.config("dense")
+    out_g, lse_g = grouped_ws(case, cuda, 4)
+    rows = [0, 1, 2, 3, 60, 61, 62, 63, 124, 125, 126, 127]
+    out_o, lse_o = oracle_decode(case, rows)
+    check(out_g[rows], lse_g[rows], out_o, lse_o, "dense grouped spread")
