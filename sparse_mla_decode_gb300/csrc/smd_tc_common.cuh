@@ -60,14 +60,22 @@ __device__ __forceinline__ int slot_b(const Pipe& pp, int c, int nch) {
 // Chunks pass B finds resident (the last ones gathered in pass A).
 __device__ __forceinline__ int resident_b(const Pipe& pp) { return pp.q_lo ? 1 : 2; }
 
+// The producers are warps 0-7 (256 threads). A warp's TMA issues run one
+// after another, so a chunk's gathers are spread over all eight warps: lanes
+// 0..P-1 of warp w issue ops P w .. P w + P - 1 (P = 20 in pass A, 16 in
+// pass B).
+constexpr int kIssueA = 20;  // 160 gather4 ops per 128-key chunk (32 row quads x 5 pieces)
+constexpr int kIssueB = 16;  // 128 ops per chunk in pass B (32 row quads x 4 V blocks)
+
 // Producer warps, pass A, chunks [c_begin, c_end): chunk c goes to its slot
-// once QK of the chunk before it in that slot has left; thread t < 160
-// issues piece t % 5 of rows 4g .. 4g + 3, g = t / 5. `seen` counts the
-// "empty" completions.
+// once QK of the chunk before it in that slot has left; op o < 160 is
+// piece o % 5 of rows 4g .. 4g + 3, g = o / 5. `seen` counts the "empty"
+// completions.
 __device__ __forceinline__ void gather_pass_a(const CUtensorMap& kv, const CUtensorMap& kv_tail,
                                               const Pipe& pp, int c_begin, int c_end,
                                               uint32_t (&seen)[2], bool& ok) {
     const int t = threadIdx.x;
+    const int lane = t & 31, o = kIssueA * (t >> 5) + lane;
     for (int c = c_begin; c < c_end && ok; ++c) {
         const int s = slot_a(pp, c);
         const uint32_t need = static_cast<uint32_t>(pp.q_lo ? c : (c >> 1));
@@ -76,8 +84,8 @@ __device__ __forceinline__ void gather_pass_a(const CUtensorMap& kv, const CUten
         const uint32_t slot = pp.ring + s * kTile;
         const uint32_t full = pp.full + 8 * s;
         if (t == 0) mbar_arrive_expect_tx(full, kTile);
-        if (t < 160) {
-            const int g = t / 5, j = t % 5;
+        if (lane < kIssueA) {
+            const int g = o / 5, j = o % 5;
             const int32_t* rw = pp.idx + kTcChunk * c + 4 * g;
             if (j < 4)
                 tma_gather4(slot + j * kBlock + 4 * g * 128, &kv, 128 * j, rw[0], rw[1], rw[2], rw[3], full);
@@ -93,6 +101,7 @@ __device__ __forceinline__ void gather_pass_a(const CUtensorMap& kv, const CUten
 __device__ __forceinline__ void gather_pass_b(const CUtensorMap& kv, const Pipe& pp, int nch,
                                               bool& ok) {
     const int t = threadIdx.x;
+    const int lane = t & 31, o = kIssueB * (t >> 5) + lane;
     uint32_t seen_b[2] = {0u, 0u};  // completions of the pass-B "slot free" barriers seen
     for (int c = nch - 1 - resident_b(pp); c >= 0 && ok; --c) {
         const int s = slot_b(pp, c, nch);
@@ -104,8 +113,8 @@ __device__ __forceinline__ void gather_pass_b(const CUtensorMap& kv, const Pipe&
         const uint32_t slot = pp.ring + s * kTile;
         const uint32_t full = pp.full + 8 * s;
         if (t == 0) mbar_arrive_expect_tx(full, 4 * kBlock);
-        if (t < 128) {
-            const int g = t / 4, j = t % 4;
+        if (lane < kIssueB) {
+            const int g = o / 4, j = o % 4;
             const int32_t* rw = pp.idx + kTcChunk * c + 4 * g;
             tma_gather4(slot + j * kBlock + 4 * g * 128, &kv, 128 * j, rw[0], rw[1], rw[2], rw[3], full);
         }
