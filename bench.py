@@ -396,26 +396,43 @@ def run_gpu(args, world, rank, local) -> dict | None:
     return line
 
 
-KERNEL_FILES = {1: ("mma_decode_kernel", "smd_mma.cu"), 2: ("tc_decode_kernel", "smd_tc.cu"),
-                3: ("group_decode_kernel", "smd_group.cu"), 4: ("tcg_decode_kernel", "smd_tcg.cu"),
-                5: ("tcs_decode_kernel", "smd_tcs.cu"), "topk": ("topk_select_kernel", "smd_topk.cu")}
+# Per kernel: its name and the sources compiled into it (the .cu first, then
+# the headers with device code or layout constants); a committed ncu summary
+# counts for the current build only if it hashes the same files.
+_COMMON = ("smd_internal.h", "smd_ptx.cuh")
+KERNEL_FILES = {
+    1: ("mma_decode_kernel", ("smd_mma.cu",) + _COMMON + ("smd_qsplit.cuh",)),
+    2: ("tc_decode_kernel", ("smd_tc.cu",) + _COMMON + ("smd_tc_common.cuh",)),
+    3: ("group_decode_kernel", ("smd_group.cu",) + _COMMON),
+    4: ("tcg_decode_kernel", ("smd_tcg.cu",) + _COMMON + ("smd_tc_common.cuh",)),
+    5: ("tcs_decode_kernel", ("smd_tcs.cu",) + _COMMON + ("smd_qsplit.cuh", "smd_tc_common.cuh")),
+    "topk": ("topk_select_kernel", ("smd_topk.cu",) + _COMMON),
+}
+
+
+def source_digest(sources) -> str:
+    """sha256[:16] over the kernel's source files, concatenated in order."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in sources:
+        with open(os.path.join(ROOT, "sparse_mla_decode_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 # Workloads whose rows come in groups sharing one index list (rows per group).
 ROW_GROUP = {"dense": 4}
 
 
 def load_traffic(config: str, kernel: int = 1):
     """dram bytes per launch from the committed ncu summary of this kernel and
-    workload; None unless it was taken on the current kernel source."""
-    import hashlib
-    name, source = KERNEL_FILES[kernel]
+    workload; None unless it was taken on the current kernel sources."""
+    name, sources = KERNEL_FILES[kernel]
     path = os.path.join(ROOT, "profiles", f"{name}_{config}.json")
-    src = os.path.join(ROOT, "sparse_mla_decode_gb300", "csrc", source)
     try:
         with open(path) as f:
             d = json.load(f)
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()[:16]
-        if d.get("kernel_source_sha256_16") != digest:
+        if d.get("kernel_source_sha256_16") != source_digest(sources):
             return None
         return d.get("dram_bytes_per_launch")
     except Exception:
