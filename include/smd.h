@@ -25,8 +25,11 @@
  * on the order of a row's indices beyond FP32 summation order.
  *
  * Memory: every pointer argument is DEVICE memory owned by the caller
- * (cudaMalloc / torch). The library allocates nothing per call and keeps no
- * per-call state; all calls are asynchronous on `stream`.
+ * (cudaMalloc / torch), except the *_host arguments of
+ * smd_sparse_mla_decode_host. The library allocates nothing per call and
+ * keeps no per-call state (that call keeps two copy streams and a few
+ * events per device, created on its first use); all calls are asynchronous
+ * on `stream`.
  *
  * Errors: argument and launch problems are returned synchronously as a
  * negative smd_status (nothing is launched). Problems only the GPU can see
@@ -377,6 +380,76 @@ int smd_sparse_mla_decode_grouped_ex(const uint8_t* q, const uint8_t* kv_pool, i
                                      uint16_t* out, float* lse, int32_t* status,
                                      void* workspace, int64_t workspace_bytes,
                                      smd_stream_t stream, const smd_plan_t* force);
+
+/* ---- the decode from and to host memory ---------------------------------------
+ *
+ * Options of smd_sparse_mla_decode_host (all zero: E4M3 query, one row per
+ * index list, the library's chunking).
+ *   row_group   0 or 1: every row has its own index list (smd_sparse_mla_decode_ws);
+ *               2 or 4: rows in groups sharing one list (smd_sparse_mla_decode_grouped_ws).
+ *   bf16_query  0: q is [B, H, 576] E4M3 codes; 1: q is [B, H, 576] bfloat16
+ *               (smd_sparse_mla_decode_bf16q_ws; q_scale is not used). Not
+ *               with row_group > 1.
+ *   chunks      0: the library's choice (smd_plan_host); 1..8: the rows are
+ *               cut into that many consecutive chunks (whole row groups).
+ */
+typedef struct {
+    int32_t row_group;
+    int32_t bf16_query;
+    int32_t chunks;
+    int32_t reserved;  /* must be 0 */
+} smd_host_opts_t;
+
+/* The number of row chunks smd_sparse_mla_decode_host pipelines for these
+ * shapes and options (opts may be NULL), written to *chunks. One chunk when
+ * the device call's plan is the spread kernel (a chunk of its rows would leave
+ * SMs idle) or fills fewer than three waves of the device; otherwise up to
+ * four, each still filling at least one and a half waves. Host only.
+ * Returns SMD_OK or SMD_ERR_SHAPE / SMD_ERR_NULL / SMD_ERR_PLAN. */
+int smd_plan_host(int32_t B, int32_t H, int32_t W, const smd_host_opts_t* opts, int32_t* chunks);
+
+/* Bytes of device workspace smd_sparse_mla_decode_host needs (opts may be
+ * NULL): staging for q, indices, counts, out and lse of all B rows, each
+ * 256-byte aligned, plus the device call's own workspace for one chunk.
+ * Negative (an smd_status) for invalid shapes or options. Host only. */
+int64_t smd_workspace_bytes_host(int32_t B, int32_t H, int32_t W, const smd_host_opts_t* opts);
+
+/* The decode with its inputs and outputs in host memory; the cache pool stays
+ * in device memory (kv_pool as in smd_sparse_mla_decode).
+ *   q_host        [B, H, 576] E4M3 codes, or bfloat16 with opts->bf16_query.
+ *   indices_host  [B, W] int32; counts_host [B] int32.
+ *   out_host      [B, H, 512] bfloat16 (raw 16-bit storage); lse_host [B, H] float32.
+ *   workspace     device memory of at least smd_workspace_bytes_host bytes,
+ *                 16-byte aligned (else SMD_ERR_WORKSPACE); no initialisation needed.
+ * The rows are cut into chunks (smd_plan_host); every array moves with one
+ * cudaMemcpyAsync per chunk. One chunk: copies in, decode and copies out are
+ * queued on `stream` in that order. Several: chunk 0 moves in on `stream`,
+ * the later chunks on the library's upload stream after it (while the earlier
+ * chunks are decoded); each chunk is decoded on `stream` once it is in; every
+ * chunk but the last moves out on the library's download stream while the
+ * next one is decoded, the last on `stream`, which then waits for both copy
+ * streams. So the call is ordered on `stream` like a kernel launch (and can be
+ * captured in a CUDA graph from `stream`). The call is asynchronous: host
+ * buffers must stay valid, and the results are in out_host / lse_host once
+ * `stream` has reached this point.
+ * Host buffers should be page-locked (cudaHostAlloc, cudaHostRegister) for the
+ * copies to overlap; pageable memory gives the same results, without overlap.
+ * Each chunk is decoded by the device call for its rows, so chunks = 1 gives
+ * the bits of that call on all B rows, and more chunks give the bits of the
+ * device calls on the chunks' rows (with the workspace when the whole batch's
+ * plan is the spread kernel, else without one: a chunk runs the kernel of the
+ * whole batch). Calls of several chunks from several host threads are
+ * serialised while they queue their work; such a call being captured into a
+ * CUDA graph keeps the device's copy streams in that capture until it ends,
+ * so no other thread may make one for the same device meanwhile. Returns SMD_OK or a
+ * negative smd_status (argument errors before anything is queued). */
+int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64_t N,
+                               const int32_t* indices_host, int32_t W, const int32_t* counts_host,
+                               int32_t B, int32_t H,
+                               float sm_scale, float q_scale, float k_scale,
+                               uint16_t* out_host, float* lse_host, int32_t* status,
+                               void* workspace, int64_t workspace_bytes,
+                               const smd_host_opts_t* opts, smd_stream_t stream);
 
 /* The base-2 logit scale the kernels use: fp32(sm*q_s*k_s*log2 e),
  * evaluated in double and rounded once. */

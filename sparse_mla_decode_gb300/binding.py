@@ -40,6 +40,12 @@ class SmdPlan(ctypes.Structure):
         return {name: int(getattr(self, name)) for name, _ in self._fields_}
 
 
+class SmdHostOpts(ctypes.Structure):
+    """smd_host_opts_t."""
+    _fields_ = [(name, ctypes.c_int32) for name in ("row_group", "bf16_query", "chunks",
+                                                     "reserved")]
+
+
 class SmdError(RuntimeError):
     def __init__(self, status: int, what: str = ""):
         self.status = int(status)
@@ -122,6 +128,15 @@ def lib() -> ctypes.CDLL:
             so.smd_plan_ws.restype = ctypes.c_int
             so.smd_plan_ws.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.POINTER(SmdPlan)]
+            so.smd_plan_host.restype = ctypes.c_int
+            so.smd_plan_host.argtypes = [ctypes.c_int32] * 3 + [ctypes.POINTER(SmdHostOpts),
+                                                                ctypes.POINTER(ctypes.c_int32)]
+            so.smd_workspace_bytes_host.restype = ctypes.c_int64
+            so.smd_workspace_bytes_host.argtypes = [ctypes.c_int32] * 3 + [
+                ctypes.POINTER(SmdHostOpts)]
+            so.smd_sparse_mla_decode_host.restype = ctypes.c_int
+            so.smd_sparse_mla_decode_host.argtypes = _DECODE_ARGS[:-1] + [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.POINTER(SmdHostOpts), ctypes.c_void_p]
             so.smd_scale_log2.restype = ctypes.c_float
             so.smd_scale_log2.argtypes = [ctypes.c_float] * 3
             so.smd_status_str.restype = ctypes.c_char_p
@@ -281,6 +296,36 @@ def smd_plan_ws(B: int, H: int, W: int) -> SmdPlan:
     return p
 
 
+def _host_opts(row_group: int = 1, bf16_query: bool = False, chunks: int = 0) -> SmdHostOpts:
+    return SmdHostOpts(int(row_group), 1 if bf16_query else 0, int(chunks), 0)
+
+
+def smd_plan_host(B: int, H: int, W: int, row_group: int = 1, bf16_query: bool = False,
+                  chunks: int = 0) -> int:
+    """The number of row chunks smd_sparse_mla_decode_host pipelines."""
+    n = ctypes.c_int32(0)
+    o = _host_opts(row_group, bf16_query, chunks)
+    rc = lib().smd_plan_host(B, H, W, ctypes.byref(o), ctypes.byref(n))
+    if rc != SMD_OK:
+        raise SmdError(rc, "smd_plan_host")
+    return int(n.value)
+
+
+def smd_workspace_bytes_host(B: int, H: int, W: int, row_group: int = 1,
+                             bf16_query: bool = False, chunks: int = 0) -> int:
+    o = _host_opts(row_group, bf16_query, chunks)
+    return int(lib().smd_workspace_bytes_host(B, H, W, ctypes.byref(o)))
+
+
+def smd_sparse_mla_decode_host(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale,
+                               k_scale, out, lse, status, workspace, workspace_bytes,
+                               opts: SmdHostOpts | None, stream) -> int:
+    ref = ctypes.byref(opts) if opts is not None else None
+    return lib().smd_sparse_mla_decode_host(q, kv_pool, N, indices, W, counts, B, H, sm_scale,
+                                            q_scale, k_scale, out, lse, status, workspace,
+                                            workspace_bytes, ref, stream)
+
+
 def smd_scale_log2(sm_scale: float, q_scale: float, k_scale: float) -> float:
     return float(lib().smd_scale_log2(sm_scale, q_scale, k_scale))
 
@@ -426,6 +471,68 @@ def sparse_mla_decode_bf16q(q, kv_pool, indices, counts, sm_scale: float, k_scal
         rc = smd_sparse_mla_decode_bf16q(*args, int(stream))
     if rc != SMD_OK:
         raise SmdError(rc, "smd_sparse_mla_decode_bf16q")
+    return out, lse
+
+
+def sparse_mla_decode_host(q, kv_pool, indices, counts, sm_scale: float, q_scale: float,
+                           k_scale: float, out=None, lse=None, status=None, stream=None,
+                           workspace=None, row_group: int = 1, bf16_query: bool = False,
+                           chunks: int = 0):
+    """Decode with q, indices and counts in HOST memory and out / lse returned
+    to host memory (smd_sparse_mla_decode_host); kv_pool stays a CUDA tensor.
+    q [B,H,576] E4M3 (uint8 or float8_e4m3fn), or bfloat16 with bf16_query;
+    indices [B,W] int32; counts [B] int32: contiguous CPU tensors, page-locked
+    (``pin_memory()``) for the copies to overlap. ``workspace``: a CUDA tensor
+    of at least smd_workspace_bytes_host bytes (allocated here if None).
+    Returns (out [B,H,512] bfloat16, lse [B,H] float32) CPU tensors, complete
+    once ``stream`` has reached the end of the call (synchronize before
+    reading them)."""
+    import torch
+
+    if bf16_query:
+        if q.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+            raise TypeError(f"q: expected bfloat16, got {q.dtype}")
+    else:
+        q = _bytes_view(q, "q")
+    kv_pool = _bytes_view(kv_pool, "kv_pool")
+    if not kv_pool.is_cuda:
+        raise ValueError("kv_pool must be a CUDA tensor")
+    for name, t in (("q", q), ("indices", indices), ("counts", counts)):
+        if t.is_cuda:
+            raise ValueError(f"{name} must be a CPU tensor (this call copies it to the GPU)")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if indices.dtype != torch.int32 or counts.dtype != torch.int32:
+        raise TypeError("indices and counts must be int32")
+    if q.dim() != 3 or q.shape[2] != 576 or kv_pool.dim() != 2 or kv_pool.shape[1] != 576:
+        raise ValueError("q must be [B,H,576] and kv_pool [N,576]")
+    B, H = int(q.shape[0]), int(q.shape[1])
+    if indices.dim() != 2 or indices.shape[0] != B or counts.shape[0] != B:
+        raise ValueError("indices must be [B, W] and counts [B]")
+    W = int(indices.shape[1])
+    if out is None:
+        out = torch.empty((B, H, 512), dtype=torch.bfloat16).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32).pin_memory()
+    for name, t in (("out", out), ("lse", lse)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+    opts = _host_opts(row_group, bf16_query, chunks)
+    if workspace is None:
+        nb = smd_workspace_bytes_host(B, H, W, row_group, bf16_query, chunks)
+        if nb < 0:
+            raise SmdError(nb, "smd_workspace_bytes_host")
+        workspace = torch.empty(max(nb, 16), dtype=torch.uint8, device=kv_pool.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(kv_pool.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    rc = smd_sparse_mla_decode_host(
+        _ptr(q), _ptr(kv_pool), int(kv_pool.shape[0]), _ptr(indices), W, _ptr(counts), B, H,
+        float(sm_scale), float(q_scale), float(k_scale), _ptr(out), _ptr(lse), _ptr(status),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), opts, int(stream))
+    if rc != SMD_OK:
+        raise SmdError(rc, "smd_sparse_mla_decode_host")
     return out, lse
 
 

@@ -1,0 +1,317 @@
+// The decode from and to host memory (smd_sparse_mla_decode_host): the rows
+// are cut into chunks whose host-to-device copies, decode and device-to-host
+// copies are pipelined over a few library-owned copy streams and the caller's
+// stream. Host code only; every decode goes through the public device calls.
+#include <algorithm>
+#include <cstdint>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "smd.h"
+
+namespace smd {
+namespace {
+
+constexpr int kMaxChunks = 8;
+constexpr int kAutoChunks = 4;
+constexpr int64_t kStageAlign = 256;
+constexpr int kHostMaxDevices = 64;
+// Events a call takes: chunk 0's uploads done, one per later upload and per
+// decode but the last, and the join.
+constexpr int kEventsPerDevice = 2 + 2 * kMaxChunks;
+
+int64_t round_up(int64_t x) { return (x + kStageAlign - 1) / kStageAlign * kStageAlign; }
+
+bool is_aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+struct Opts {
+    int G = 1;          // rows per group sharing one index list
+    bool bf16 = false;  // the query is bfloat16
+    int chunks = 0;     // 0: automatic
+};
+
+int read_opts(const smd_host_opts_t* o, Opts* out) {
+    Opts r;
+    if (o != nullptr) {
+        if (o->reserved != 0 || (o->bf16_query != 0 && o->bf16_query != 1)) return SMD_ERR_PLAN;
+        r.G = o->row_group == 0 ? 1 : o->row_group;
+        r.bf16 = o->bf16_query != 0;
+        r.chunks = o->chunks;
+    }
+    if (r.G != 1 && r.G != 2 && r.G != 4) return SMD_ERR_SHAPE;
+    if (r.bf16 && r.G != 1) return SMD_ERR_PLAN;
+    if (r.chunks < 0 || r.chunks > kMaxChunks) return SMD_ERR_PLAN;
+    *out = r;
+    return SMD_OK;
+}
+
+int host_sm_count() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+        cudaGetLastError();  // no device here: plan for a GB300
+        return 152;
+    }
+    return sms;
+}
+
+// Workspace bytes the device call wants for B rows (the spread kernel's), 0
+// when its plan needs none.
+int64_t device_ws(int B, int H, int W, const Opts& o) {
+    if (o.bf16) return smd_workspace_bytes_bf16q(B, H, W);
+    if (o.G > 1) return smd_workspace_bytes_grouped(B, H, W, o.G);
+    return smd_workspace_bytes(B, H, W);
+}
+
+// The plan of the device call on all B rows given its workspace.
+int whole_plan(int B, int H, int W, const Opts& o, smd_plan_t* p) {
+    const int64_t ws = device_ws(B, H, W, o);
+    if (o.bf16) return smd_plan_bf16q(B, H, W, ws, p);
+    if (o.G > 1) return smd_plan_grouped(B, H, W, o.G, ws, p);
+    return smd_plan_ws(B, H, W, p);
+}
+
+// Where the staging buffers sit in the workspace, and how the rows are cut.
+struct Layout {
+    int chunks = 1, rows = 0;  // chunks of `rows` rows (the last may be shorter)
+    bool spread = false;       // the whole batch's plan is the spread kernel
+    int64_t q_row = 0;         // bytes of one row of q
+    int64_t off_q = 0, off_idx = 0, off_cnt = 0, off_out = 0, off_lse = 0, off_dws = 0;
+    int64_t dws_bytes = 0, total = 0;
+};
+
+int layout_of(int B, int H, int W, const Opts& o, Layout* L) {
+    if (B < 0 || W < 0 || H <= 0 || H % 16 != 0) return SMD_ERR_SHAPE;
+    if (B % o.G != 0) return SMD_ERR_SHAPE;
+    Layout r;
+    r.q_row = static_cast<int64_t>(H) * 576 * (o.bf16 ? 2 : 1);
+    if (B > 0) {
+        smd_plan_t p{};
+        const int rc = whole_plan(B, H, W, o, &p);
+        if (rc != SMD_OK) return rc;
+        r.spread = p.kernel == SMD_KERNEL_TC_SPREAD;
+        int chunks = o.chunks;
+        if (chunks == 0) {
+            // Chunks pay when each still fills the device: at least three waves
+            // of CTAs in all, at least one and a half per chunk.
+            const int64_t ctas = static_cast<int64_t>(std::max(p.grid_x, 1)) * std::max(p.grid_y, 1);
+            const int64_t sms = host_sm_count();
+            chunks = (r.spread || ctas < 3 * sms)
+                         ? 1
+                         : static_cast<int>(std::min<int64_t>(kAutoChunks, ctas * 2 / (3 * sms)));
+        }
+        const int groups = B / o.G;
+        chunks = std::max(1, std::min(chunks, groups));
+        const int per = (groups + chunks - 1) / chunks;  // groups per chunk
+        r.rows = per * o.G;
+        r.chunks = (groups + per - 1) / per;
+        // A chunk is decoded by the device call the whole batch would use: with
+        // the workspace when that is the spread kernel, else without one.
+        r.dws_bytes = r.spread ? device_ws(r.rows, H, W, o) : 0;
+        if (r.dws_bytes < 0) return SMD_ERR_SHAPE;
+    }
+    int64_t off = 0;
+    r.off_q = off;
+    off += round_up(static_cast<int64_t>(B) * r.q_row);
+    r.off_idx = off;
+    off += round_up(static_cast<int64_t>(B) * W * 4);
+    r.off_cnt = off;
+    off += round_up(static_cast<int64_t>(B) * 4);
+    r.off_out = off;
+    off += round_up(static_cast<int64_t>(B) * H * 512 * 2);
+    r.off_lse = off;
+    off += round_up(static_cast<int64_t>(B) * H * 4);
+    r.off_dws = off;
+    off += round_up(r.dws_bytes);
+    r.total = off;
+    *L = r;
+    return SMD_OK;
+}
+
+// The library's copy streams and events of one device, created on first use
+// (only calls of more than one chunk use them).
+struct CopyEngine {
+    std::once_flag once;
+    std::mutex mu;  // held while a call queues its work
+    bool ok = false;
+    cudaStream_t up = nullptr;    // uploads of chunks 1 ..
+    cudaStream_t down = nullptr;  // downloads of every chunk but the last
+    cudaEvent_t ev[kEventsPerDevice] = {};
+};
+
+CopyEngine g_engines[kHostMaxDevices];
+
+CopyEngine* engine_of_current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kHostMaxDevices) return nullptr;
+    CopyEngine& e = g_engines[dev];
+    std::call_once(e.once, [&e] {
+        bool ok = cudaStreamCreateWithFlags(&e.up, cudaStreamNonBlocking) == cudaSuccess &&
+                  cudaStreamCreateWithFlags(&e.down, cudaStreamNonBlocking) == cudaSuccess;
+        for (auto& v : e.ev) ok = ok && cudaEventCreateWithFlags(&v, cudaEventDisableTiming) == cudaSuccess;
+        e.ok = ok;
+    });
+    return e.ok ? &e : nullptr;
+}
+
+}  // namespace
+}  // namespace smd
+
+extern "C" {
+
+int smd_plan_host(int32_t B, int32_t H, int32_t W, const smd_host_opts_t* opts, int32_t* chunks) {
+    if (chunks == nullptr) return SMD_ERR_NULL;
+    smd::Opts o;
+    int rc = smd::read_opts(opts, &o);
+    if (rc != SMD_OK) return rc;
+    smd::Layout L;
+    rc = smd::layout_of(B, H, W, o, &L);
+    if (rc != SMD_OK) return rc;
+    *chunks = L.chunks;
+    return SMD_OK;
+}
+
+int64_t smd_workspace_bytes_host(int32_t B, int32_t H, int32_t W, const smd_host_opts_t* opts) {
+    smd::Opts o;
+    int rc = smd::read_opts(opts, &o);
+    if (rc != SMD_OK) return rc;
+    smd::Layout L;
+    rc = smd::layout_of(B, H, W, o, &L);
+    return rc != SMD_OK ? rc : L.total;
+}
+
+int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64_t N,
+                               const int32_t* indices_host, int32_t W, const int32_t* counts_host,
+                               int32_t B, int32_t H, float sm_scale, float q_scale, float k_scale,
+                               uint16_t* out_host, float* lse_host, int32_t* status,
+                               void* workspace, int64_t workspace_bytes,
+                               const smd_host_opts_t* opts, smd_stream_t stream) {
+    using namespace smd;
+    Opts o;
+    int rc = read_opts(opts, &o);
+    if (rc != SMD_OK) return rc;
+    Layout L;
+    rc = layout_of(B, H, W, o, &L);
+    if (rc != SMD_OK) return rc;
+    if (N < 0 || N >= (int64_t(1) << 31)) return SMD_ERR_SHAPE;
+    if (B == 0) return SMD_OK;
+    // The argument checks of the device call, before anything is queued.
+    if (!q_host || !counts_host || !out_host || !lse_host || !workspace) return SMD_ERR_NULL;
+    if (W > 0 && (!indices_host || !kv_pool)) return SMD_ERR_NULL;
+    if (W > 0 && N == 0) return SMD_ERR_SHAPE;
+    if ((kv_pool && !is_aligned(kv_pool, 16)) || (status && !is_aligned(status, 4)))
+        return SMD_ERR_ALIGN;
+    if (!is_aligned(workspace, 16) || workspace_bytes < L.total) return SMD_ERR_WORKSPACE;
+    CopyEngine* eng = nullptr;
+    if (L.chunks > 1) {
+        eng = engine_of_current_device();
+        if (eng == nullptr) return SMD_ERR_DEVICE;
+    }
+
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint8_t* dq = ws + L.off_q;
+    int32_t* didx = reinterpret_cast<int32_t*>(ws + L.off_idx);
+    int32_t* dcnt = reinterpret_cast<int32_t*>(ws + L.off_cnt);
+    uint16_t* dout = reinterpret_cast<uint16_t*>(ws + L.off_out);
+    float* dlse = reinterpret_cast<float*>(ws + L.off_lse);
+    void* dws = L.dws_bytes > 0 ? ws + L.off_dws : nullptr;
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const int64_t out_row = static_cast<int64_t>(H) * 512 * 2, lse_row = static_cast<int64_t>(H) * 4;
+
+    std::unique_lock<std::mutex> lock;
+    if (eng != nullptr) lock = std::unique_lock<std::mutex>(eng->mu);
+    int next_ev = 0;
+    auto take = [&]() { return eng->ev[next_ev++]; };
+    bool cuda_ok = true;
+    auto chk = [&](cudaError_t e) { cuda_ok = cuda_ok && e == cudaSuccess; };
+    int result = SMD_OK;
+
+    // Chunk c's copies in / out, queued on s.
+    auto upload = [&](int c, cudaStream_t s) {
+        const int r0 = c * L.rows, nr = std::min(L.rows, B - r0);
+        chk(cudaMemcpyAsync(dq + r0 * L.q_row, static_cast<const uint8_t*>(q_host) + r0 * L.q_row,
+                            nr * L.q_row, cudaMemcpyHostToDevice, s));
+        if (W > 0)
+            chk(cudaMemcpyAsync(didx + static_cast<int64_t>(r0) * W,
+                                indices_host + static_cast<int64_t>(r0) * W,
+                                static_cast<int64_t>(nr) * W * 4, cudaMemcpyHostToDevice, s));
+        chk(cudaMemcpyAsync(dcnt + r0, counts_host + r0, static_cast<int64_t>(nr) * 4,
+                            cudaMemcpyHostToDevice, s));
+    };
+    auto download = [&](int c, cudaStream_t s) {
+        const int r0 = c * L.rows, nr = std::min(L.rows, B - r0);
+        chk(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(out_host) + r0 * out_row,
+                            reinterpret_cast<const uint8_t*>(dout) + r0 * out_row, nr * out_row,
+                            cudaMemcpyDeviceToHost, s));
+        chk(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse_host) + r0 * lse_row,
+                            reinterpret_cast<const uint8_t*>(dlse) + r0 * lse_row, nr * lse_row,
+                            cudaMemcpyDeviceToHost, s));
+    };
+    auto decode = [&](int c) {
+        const int r0 = c * L.rows, nr = std::min(L.rows, B - r0);
+        const int32_t* ci = didx + static_cast<int64_t>(r0) * W;
+        uint16_t* co = dout + static_cast<int64_t>(r0) * H * 512;
+        float* cl = dlse + static_cast<int64_t>(r0) * H;
+        const int64_t dbytes = dws != nullptr ? L.dws_bytes : 0;
+        if (o.bf16)
+            return smd_sparse_mla_decode_bf16q_ws(reinterpret_cast<const uint16_t*>(dq + r0 * L.q_row),
+                                                  kv_pool, N, ci, W, dcnt + r0, nr, H, sm_scale,
+                                                  k_scale, co, cl, status, dws, dbytes, stream);
+        if (o.G > 1)
+            return smd_sparse_mla_decode_grouped_ws(dq + r0 * L.q_row, kv_pool, N, ci, W, dcnt + r0,
+                                                    nr, H, o.G, sm_scale, q_scale, k_scale, co, cl,
+                                                    status, dws, dbytes, stream);
+        return smd_sparse_mla_decode_ws(dq + r0 * L.q_row, kv_pool, N, ci, W, dcnt + r0, nr, H,
+                                        sm_scale, q_scale, k_scale, co, cl, status, dws, dbytes,
+                                        stream);
+    };
+
+    // Chunk 0 moves in on `stream` itself; the later chunks follow it on the
+    // upload stream (one after another: concurrent uploads would share the
+    // bandwidth chunk 0 needs first) while the earlier chunks are decoded.
+    upload(0, cs);
+    if (L.chunks > 1) {
+        const cudaEvent_t up0 = take();
+        chk(cudaEventRecord(up0, cs));
+        chk(cudaStreamWaitEvent(eng->up, up0, 0));
+        chk(cudaStreamWaitEvent(eng->down, up0, 0));
+    }
+    cudaEvent_t up_done[kMaxChunks] = {};
+    for (int c = 1; c < L.chunks && cuda_ok; ++c) {
+        upload(c, eng->up);
+        up_done[c] = take();
+        chk(cudaEventRecord(up_done[c], eng->up));
+    }
+    // Decode chunk c once it is in; every chunk but the last goes back on the
+    // download stream while the next one is decoded, the last on `stream`.
+    for (int c = 0; c < L.chunks && cuda_ok; ++c) {
+        if (c > 0) chk(cudaStreamWaitEvent(cs, up_done[c], 0));
+        if (!cuda_ok) break;
+        rc = decode(c);
+        if (rc != SMD_OK) {
+            result = rc;
+            break;
+        }
+        if (c + 1 < L.chunks) {
+            const cudaEvent_t done = take();
+            chk(cudaEventRecord(done, cs));
+            chk(cudaStreamWaitEvent(eng->down, done, 0));
+            download(c, eng->down);
+        } else {
+            download(c, cs);
+        }
+    }
+    // Join: `stream` continues after the copy streams' last work.
+    if (L.chunks > 1) {
+        const cudaEvent_t up_end = take(), down_end = take();
+        chk(cudaEventRecord(up_end, eng->up));
+        chk(cudaStreamWaitEvent(cs, up_end, 0));
+        chk(cudaEventRecord(down_end, eng->down));
+        chk(cudaStreamWaitEvent(cs, down_end, 0));
+    }
+    if (result == SMD_OK && !cuda_ok) result = SMD_ERR_LAUNCH;
+    return result;
+}
+
+}  // extern "C"

@@ -317,3 +317,71 @@ def test_topk_select_argument_checks(kw, code):
 @pytest.mark.parametrize("cluster", [3, 16, -1])
 def test_topk_select_rejects_other_cluster_sizes(cluster):
     assert smd.smd_topk_select_ex(A, 64, 0, 2, 64, 8, A, A, 0, 0, cluster) == smd.SMD_ERR_PLAN
+
+
+# ---- smd_sparse_mla_decode_host (argument checks before anything is queued) ------
+
+def host_call(q=A, kv=A, N=100, idx=A, W=8, counts=A, B=2, H=16, out=A, lse=A, status=0,
+              ws=A, ws_bytes=1 << 40, opts=None):
+    return smd.smd_sparse_mla_decode_host(q, kv, N, idx, W, counts, B, H, 0.1, 1.0, 1.0, out,
+                                          lse, status, ws, ws_bytes, opts, 0)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(H=15), smd.SMD_ERR_SHAPE),
+    (dict(B=-1), smd.SMD_ERR_SHAPE),
+    (dict(W=-1), smd.SMD_ERR_SHAPE),
+    (dict(N=-1), smd.SMD_ERR_SHAPE),
+    (dict(N=0), smd.SMD_ERR_SHAPE),
+    (dict(q=0), smd.SMD_ERR_NULL),
+    (dict(idx=0), smd.SMD_ERR_NULL),
+    (dict(kv=0), smd.SMD_ERR_NULL),
+    (dict(counts=0), smd.SMD_ERR_NULL),
+    (dict(out=0), smd.SMD_ERR_NULL),
+    (dict(lse=0), smd.SMD_ERR_NULL),
+    (dict(ws=0), smd.SMD_ERR_NULL),
+    (dict(kv=A + 4), smd.SMD_ERR_ALIGN),
+    (dict(status=A + 2), smd.SMD_ERR_ALIGN),
+    (dict(ws=A + 8), smd.SMD_ERR_WORKSPACE),
+    (dict(ws_bytes=1024), smd.SMD_ERR_WORKSPACE),
+    (dict(opts=smd.SmdHostOpts(3, 0, 0, 0)), smd.SMD_ERR_SHAPE),
+    (dict(opts=smd.SmdHostOpts(4, 0, 0, 0), B=6), smd.SMD_ERR_SHAPE),
+    (dict(opts=smd.SmdHostOpts(4, 1, 0, 0), B=4), smd.SMD_ERR_PLAN),
+    (dict(opts=smd.SmdHostOpts(1, 2, 0, 0)), smd.SMD_ERR_PLAN),
+    (dict(opts=smd.SmdHostOpts(1, 0, 9, 0)), smd.SMD_ERR_PLAN),
+    (dict(opts=smd.SmdHostOpts(1, 0, -1, 0)), smd.SMD_ERR_PLAN),
+    (dict(opts=smd.SmdHostOpts(1, 0, 0, 1)), smd.SMD_ERR_PLAN),
+])
+def test_host_call_argument_checks(kw, code):
+    assert host_call(**kw) == code
+
+
+def test_host_call_with_no_rows_is_a_no_op():
+    assert host_call(B=0, q=0, idx=0, counts=0, out=0, lse=0, ws=0, ws_bytes=0) == smd.SMD_OK
+
+
+@pytest.mark.parametrize("B,H,W,G,bf16,chunks", [
+    (2, 16, 64, 1, False, 1),       # tiny: one small launch
+    (5, 64, 256, 1, False, 1),      # latency
+    (64, 128, 2048, 1, False, 1),   # DSA: the spread kernel takes the whole batch
+    (256, 128, 2048, 1, False, 4),  # throughput: 1024 cluster CTAs, four chunks of 64 rows
+    (128, 16, 8192, 4, False, 2),   # dense-as-sparse: 512 CTAs, two chunks of 16 groups
+    (256, 128, 2048, 1, True, 1),   # bf16 query on the spread kernel
+])
+def test_host_plan_chunks_the_rows_only_where_each_chunk_fills_the_device(B, H, W, G, bf16, chunks):
+    # No device here: the plan is made for a 152-SM GB300.
+    assert smd.smd_plan_host(B, H, W, G, bf16) == chunks
+
+
+@pytest.mark.parametrize("B,H,W,G,bf16", [(2, 16, 64, 1, False), (64, 128, 2048, 1, False),
+                                          (256, 128, 2048, 1, False), (128, 16, 8192, 4, False),
+                                          (12, 64, 300, 1, True)])
+def test_host_workspace_holds_the_staging_and_the_chunk_workspace(B, H, W, G, bf16):
+    staging = B * H * 576 * (2 if bf16 else 1) + B * W * 4 + B * 4 + B * H * 1024 + B * H * 4
+    nb = smd.smd_workspace_bytes_host(B, H, W, G, bf16)
+    assert staging <= nb <= staging + 5 * 256 + max(
+        0, smd.smd_workspace_bytes_bf16q(B, H, W) if bf16 else
+        smd.smd_workspace_bytes_grouped(B, H, W, G) if G > 1 else smd.smd_workspace_bytes(B, H, W))
+    for chunks in (1, 2, 3):
+        rows = -(-(B // G) // chunks) * G
+        assert smd.smd_plan_host(B, H, W, G, bf16, chunks) == -(-B // rows)

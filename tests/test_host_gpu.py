@@ -1,0 +1,167 @@
+"""GPU checks of the host-buffer decode (smd_sparse_mla_decode_host): q, the
+index list and the counts come from host memory, out and lse go back to it,
+pipelined with the decode over row chunks. One chunk gives the bits of the
+device call on all rows; several chunks give the bits of the device call on
+each chunk's rows (the workspace call when the whole batch's plan is the
+spread kernel, else the call without a workspace). Also checked against the
+oracle, with pageable host memory, on a side stream, for grouped rows and
+for the bf16 query."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+from sparse_mla_decode_gb300 import inputs
+from test_parity_gpu import check, gpu_decode, oracle_decode, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def host_decode(case, dev, chunks=0, row_group=1, bf16=False, pinned=True, stream=None):
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    kv = torch.from_numpy(case.kv8).to(dev)
+    if bf16:
+        q = torch.from_numpy(case.q16.view(np.int16)).view(torch.bfloat16)
+    else:
+        q = torch.from_numpy(case.q8)
+    idx = torch.from_numpy(case.indices)
+    cnt = torch.from_numpy(case.counts)
+    out = torch.empty((case.B, case.H, 512), dtype=torch.bfloat16)
+    lse = torch.empty((case.B, case.H), dtype=torch.float32)
+    if pinned:
+        q, idx, cnt, out, lse = (t.pin_memory() for t in (q, idx, cnt, out, lse))
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    # Garbage in the staging area: nothing may depend on its contents.
+    nb = binding.smd_workspace_bytes_host(case.B, case.H, case.W, row_group, bf16, chunks)
+    ws = torch.full((max(nb, 16),), 0xA5, dtype=torch.uint8, device=dev)
+    torch.cuda.current_stream(dev).synchronize()  # the fill; the call may go on another stream
+    binding.sparse_mla_decode_host(q, kv, idx, cnt, case.sm_scale, case.q_scale, case.k_scale,
+                                   out=out, lse=lse, status=status, workspace=ws,
+                                   row_group=row_group, bf16_query=bf16, chunks=chunks,
+                                   stream=stream)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, binding.smd_status_str(int(status.item()))
+    return out.view(torch.int16).numpy().view(np.uint16).copy(), lse.numpy().copy()
+
+
+def rows_of(case, r0, r1):
+    return inputs.Case(case.name, case.q8[r0:r1], case.kv8, case.indices[r0:r1],
+                       case.counts[r0:r1], case.sm_scale, case.q_scale, case.k_scale,
+                       q16=case.q16[r0:r1])
+
+
+def device_ws(case, dev, grouped=1, bf16=False):
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    if bf16:
+        nb = binding.smd_workspace_bytes_bf16q(case.B, case.H, case.W)
+    elif grouped > 1:
+        nb = binding.smd_workspace_bytes_grouped(case.B, case.H, case.W, grouped)
+    else:
+        nb = binding.smd_workspace_bytes(case.B, case.H, case.W)
+    return torch.zeros(nb, dtype=torch.uint8, device=dev) if nb > 0 else None
+
+
+def assert_same(a, b, what):
+    assert np.array_equal(a[0], b[0]), what
+    assert np.array_equal(a[1].view(np.uint32), b[1].view(np.uint32)), what
+
+
+def test_one_chunk_is_the_device_call(cuda):
+    case = inputs.config("latency")
+    from sparse_mla_decode_gb300 import binding
+    assert binding.smd_plan_host(case.B, case.H, case.W) == 1
+    ref = gpu_decode(case, cuda, workspace=device_ws(case, cuda))
+    assert_same(host_decode(case, cuda), ref, "latency, one chunk")
+    assert_same(host_decode(case, cuda, pinned=False), ref, "latency, pageable host memory")
+
+
+@pytest.mark.parametrize("chunks", [2, 3, 5])
+def test_chunks_are_the_device_calls_on_their_rows(cuda, chunks):
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.random_case(801 + chunks, B=11, H=32, W=700, N=12000,
+                              counts=[700, 1, 0, 513, 699, 64, 300, 2, 700, 128, 45])
+    got = host_decode(case, cuda, chunks=chunks)
+    n = binding.smd_plan_host(case.B, case.H, case.W, chunks=chunks)
+    rows = -(-case.B // chunks)
+    assert n == -(-case.B // rows)
+    for c in range(n):
+        r0, r1 = c * rows, min(case.B, (c + 1) * rows)
+        part = rows_of(case, r0, r1)
+        ref = gpu_decode(part, cuda)  # the whole batch's plan is not the spread kernel
+        assert_same((got[0][r0:r1], got[1][r0:r1]), ref, f"chunk {c} of {n}")
+    out_o, lse_o = oracle_decode(case)
+    check(got[0], got[1], out_o, lse_o, f"{chunks} chunks vs the oracle")
+
+
+def test_spread_plan_chunks_use_the_workspace_call(cuda):
+    """H = 128 rows longer than a cluster holds: the whole batch runs on the
+    spread kernel, so two forced chunks are two workspace calls."""
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.random_case(811, B=4, H=128, W=2600, N=30000, counts=[2600, 700, 0, 2100])
+    assert binding.smd_plan_ws(case.B, case.H, case.W).kernel == binding.SMD_KERNEL_TC_SPREAD
+    got = host_decode(case, cuda, chunks=2)
+    for r0 in (0, 2):
+        part = rows_of(case, r0, r0 + 2)
+        ref = gpu_decode(part, cuda, workspace=device_ws(part, cuda))
+        assert_same((got[0][r0:r0 + 2], got[1][r0:r0 + 2]), ref, f"rows {r0}..")
+    assert_same(host_decode(case, cuda), gpu_decode(case, cuda, workspace=device_ws(case, cuda)),
+                "one chunk")
+
+
+def test_grouped_rows_in_chunks_of_whole_groups(cuda):
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.grouped_case(821, R=6, G=4, H=16, W=1500, N=20000)
+    got = host_decode(case, cuda, chunks=2, row_group=4)
+    for r0 in (0, 12):
+        part = rows_of(case, r0, r0 + 12)
+        q, kv, idx, cnt = to_dev(part, cuda)
+        status = torch.zeros(1, dtype=torch.int32, device=cuda)
+        out, lse = binding.sparse_mla_decode(q, kv, idx, cnt, case.sm_scale, case.q_scale,
+                                             case.k_scale, status=status, row_group=4)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        ref = (out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy())
+        assert_same((got[0][r0:r0 + 12], got[1][r0:r0 + 12]), ref, f"groups from row {r0}")
+
+
+def test_bf16_query_from_host_memory(cuda):
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.random_case(831, B=5, H=64, W=256, N=20000, counts=[256, 200, 0, 255, 1])
+    got = host_decode(case, cuda, bf16=True)
+    q16 = torch.from_numpy(case.q16.view(np.int16)).to(cuda).view(torch.bfloat16)
+    _, kv, idx, cnt = to_dev(case, cuda)
+    ws = device_ws(case, cuda, bf16=True)
+    out, lse = binding.sparse_mla_decode_bf16q(q16, kv, idx, cnt, case.sm_scale, case.k_scale,
+                                               workspace=ws)
+    torch.cuda.synchronize()
+    ref = (out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy())
+    assert_same(got, ref, "bf16 query")
+
+
+def test_host_call_is_ordered_on_a_side_stream(cuda):
+    """Queued on a side stream behind a long kernel: the results are complete
+    when that stream is synchronized, and match the default-stream call."""
+    import torch
+    case = inputs.random_case(841, B=6, H=16, W=400, N=8000)
+    ref = host_decode(case, cuda)
+    side = torch.cuda.Stream(cuda)
+    with torch.cuda.stream(side):
+        big = torch.ones(1 << 26, device=cuda)
+        for _ in range(4):
+            big.mul_(1.0)  # keeps the side stream busy before the call
+    got = host_decode(case, cuda, stream=side)
+    assert_same(got, ref, "side stream")
+
+
+def test_throughput_config_in_four_chunks_sampled(cuda):
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.config("throughput")
+    assert binding.smd_plan_host(case.B, case.H, case.W) == 4
+    out_g, lse_g = host_decode(case, cuda)
+    rows = [0, 63, 64, 200, 255]
+    out_o, lse_o = oracle_decode(case, rows)
+    check(out_g[rows], lse_g[rows], out_o, lse_o, "throughput via host buffers")
