@@ -382,7 +382,9 @@ def run_gpu(args, world, rank, local) -> dict | None:
                 "call": "smd_sparse_mla_decode_host", "row_chunks": int(host_chunks),
                 "note": ("q, indices, counts H2D from pinned memory and out, lse D2H inside the "
                          "call, pipelined with the decode over row chunks; pool resident")},
-        "gpu_launches": args.steps,
+        # per step: the decode kernel, plus the query-split kernel before the
+        # spread kernel when the query is bf16
+        "gpu_launches": args.steps * (2 if bf16q and plan["kernel"] == 5 else 1),
         "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
         "us_median": round(float(np.median(times_ms)) * 1e3, 3),

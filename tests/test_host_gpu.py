@@ -165,3 +165,56 @@ def test_throughput_config_in_four_chunks_sampled(cuda):
     rows = [0, 63, 64, 200, 255]
     out_o, lse_o = oracle_decode(case, rows)
     check(out_g[rows], lse_g[rows], out_o, lse_o, "throughput via host buffers")
+
+
+def test_host_call_replays_in_a_cuda_graph(cuda):
+    """Captured with three chunks (the copy streams join the capture and are
+    joined back): a replay reads the host inputs as they are at replay time
+    and writes the host outputs; both replays give the eager call's bits."""
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.random_case(851, B=12, H=32, W=600, N=9000)
+    other = inputs.random_case(852, B=12, H=32, W=600, N=9000)
+    other = inputs.Case(other.name, other.q8, case.kv8, other.indices % case.N, other.counts,
+                        case.sm_scale, case.q_scale, case.k_scale, q16=other.q16)
+    ref = host_decode(case, cuda, chunks=3)
+    ref_other = host_decode(other, cuda, chunks=3)
+    kv = torch.from_numpy(case.kv8).to(cuda)
+    q = torch.from_numpy(case.q8.copy()).pin_memory()
+    idx = torch.from_numpy(case.indices.copy()).pin_memory()
+    cnt = torch.from_numpy(case.counts.copy()).pin_memory()
+    out = torch.zeros((case.B, case.H, 512), dtype=torch.bfloat16).pin_memory()
+    lse = torch.zeros((case.B, case.H), dtype=torch.float32).pin_memory()
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    ws = torch.zeros(binding.smd_workspace_bytes_host(case.B, case.H, case.W, chunks=3),
+                     dtype=torch.uint8, device=cuda)
+
+    def call():
+        binding.sparse_mla_decode_host(q, kv, idx, cnt, case.sm_scale, case.q_scale,
+                                       case.k_scale, out=out, lse=lse, status=status,
+                                       workspace=ws, chunks=3)
+
+    side = torch.cuda.Stream(cuda)
+    side.wait_stream(torch.cuda.current_stream(cuda))
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream(cuda).wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    torch.cuda.synchronize()
+
+    def replay():
+        out.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        return out.view(torch.int16).numpy().view(np.uint16).copy(), lse.numpy().copy()
+
+    assert_same(replay(), ref, "first replay")
+    q.copy_(torch.from_numpy(other.q8))
+    idx.copy_(torch.from_numpy(other.indices))
+    cnt.copy_(torch.from_numpy(other.counts))
+    assert_same(replay(), ref_other, "replay after the host inputs changed")
