@@ -392,12 +392,14 @@ int smd_sparse_mla_decode_grouped_ex(const uint8_t* q, const uint8_t* kv_pool, i
  *               with row_group > 1.
  *   chunks      0: the library's choice (smd_plan_host); 1..8: the rows are
  *               cut into that many consecutive chunks (whole row groups).
+ *   copies      0: the library's choice; 1: always copy through the workspace
+ *               (never read or write the host buffers from a kernel).
  */
 typedef struct {
     int32_t row_group;
     int32_t bf16_query;
     int32_t chunks;
-    int32_t reserved;  /* must be 0 */
+    int32_t copies;
 } smd_host_opts_t;
 
 /* The number of row chunks smd_sparse_mla_decode_host pipelines for these
@@ -434,6 +436,13 @@ int64_t smd_workspace_bytes_host(int32_t B, int32_t H, int32_t W, const smd_host
  * `stream` has reached this point.
  * Host buffers should be page-locked (cudaHostAlloc, cudaHostRegister) for the
  * copies to overlap; pageable memory gives the same results, without overlap.
+ * Direct access: with one chunk, a warp-MMA plan (SMD_KERNEL_MMA or
+ * SMD_KERNEL_GROUP), at most 8 MiB of host data, and indices, counts, out and
+ * lse page-locked, mapped into the device's address space
+ * (cudaPointerGetAttributes reports host memory with a device pointer) and
+ * aligned as the device call wants them, only q is copied: the kernel reads
+ * the index list and the counts from host memory and writes out and lse there
+ * itself (copies = 1 turns this off). The results are the same bits.
  * Each chunk is decoded by the device call for its rows, so chunks = 1 gives
  * the bits of that call on all B rows, and more chunks give the bits of the
  * device calls on the chunks' rows (with the workspace when the whole batch's

@@ -43,7 +43,7 @@ class SmdPlan(ctypes.Structure):
 class SmdHostOpts(ctypes.Structure):
     """smd_host_opts_t."""
     _fields_ = [(name, ctypes.c_int32) for name in ("row_group", "bf16_query", "chunks",
-                                                     "reserved")]
+                                                     "copies")]
 
 
 class SmdError(RuntimeError):
@@ -296,8 +296,9 @@ def smd_plan_ws(B: int, H: int, W: int) -> SmdPlan:
     return p
 
 
-def _host_opts(row_group: int = 1, bf16_query: bool = False, chunks: int = 0) -> SmdHostOpts:
-    return SmdHostOpts(int(row_group), 1 if bf16_query else 0, int(chunks), 0)
+def _host_opts(row_group: int = 1, bf16_query: bool = False, chunks: int = 0,
+               copies: int = 0) -> SmdHostOpts:
+    return SmdHostOpts(int(row_group), 1 if bf16_query else 0, int(chunks), int(copies))
 
 
 def smd_plan_host(B: int, H: int, W: int, row_group: int = 1, bf16_query: bool = False,
@@ -477,7 +478,7 @@ def sparse_mla_decode_bf16q(q, kv_pool, indices, counts, sm_scale: float, k_scal
 def sparse_mla_decode_host(q, kv_pool, indices, counts, sm_scale: float, q_scale: float,
                            k_scale: float, out=None, lse=None, status=None, stream=None,
                            workspace=None, row_group: int = 1, bf16_query: bool = False,
-                           chunks: int = 0):
+                           chunks: int = 0, copies: int = 0):
     """Decode with q, indices and counts in HOST memory and out / lse returned
     to host memory (smd_sparse_mla_decode_host); kv_pool stays a CUDA tensor.
     q [B,H,576] E4M3 (uint8 or float8_e4m3fn), or bfloat16 with bf16_query;
@@ -517,7 +518,7 @@ def sparse_mla_decode_host(q, kv_pool, indices, counts, sm_scale: float, q_scale
     for name, t in (("out", out), ("lse", lse)):
         if t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CPU tensor")
-    opts = _host_opts(row_group, bf16_query, chunks)
+    opts = _host_opts(row_group, bf16_query, chunks, copies)
     if workspace is None:
         nb = smd_workspace_bytes_host(B, H, W, row_group, bf16_query, chunks)
         if nb < 0:

@@ -26,18 +26,24 @@ int64_t round_up(int64_t x) { return (x + kStageAlign - 1) / kStageAlign * kStag
 bool is_aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
 struct Opts {
-    int G = 1;          // rows per group sharing one index list
-    bool bf16 = false;  // the query is bfloat16
-    int chunks = 0;     // 0: automatic
+    int G = 1;            // rows per group sharing one index list
+    bool bf16 = false;    // the query is bfloat16
+    int chunks = 0;       // 0: automatic
+    bool copies = false;  // always copy through the workspace
 };
+
+// Host data up to this size may be read and written by the kernel in place.
+constexpr int64_t kDirectMaxBytes = int64_t(8) << 20;
 
 int read_opts(const smd_host_opts_t* o, Opts* out) {
     Opts r;
     if (o != nullptr) {
-        if (o->reserved != 0 || (o->bf16_query != 0 && o->bf16_query != 1)) return SMD_ERR_PLAN;
+        if ((o->bf16_query != 0 && o->bf16_query != 1) || (o->copies != 0 && o->copies != 1))
+            return SMD_ERR_PLAN;
         r.G = o->row_group == 0 ? 1 : o->row_group;
         r.bf16 = o->bf16_query != 0;
         r.chunks = o->chunks;
+        r.copies = o->copies != 0;
     }
     if (r.G != 1 && r.G != 2 && r.G != 4) return SMD_ERR_SHAPE;
     if (r.bf16 && r.G != 1) return SMD_ERR_PLAN;
@@ -75,6 +81,7 @@ int whole_plan(int B, int H, int W, const Opts& o, smd_plan_t* p) {
 // Where the staging buffers sit in the workspace, and how the rows are cut.
 struct Layout {
     int chunks = 1, rows = 0;  // chunks of `rows` rows (the last may be shorter)
+    int kernel = 0;            // the whole batch's plan (SMD_KERNEL_*)
     bool spread = false;       // the whole batch's plan is the spread kernel
     int64_t q_row = 0;         // bytes of one row of q
     int64_t off_q = 0, off_idx = 0, off_cnt = 0, off_out = 0, off_lse = 0, off_dws = 0;
@@ -90,6 +97,7 @@ int layout_of(int B, int H, int W, const Opts& o, Layout* L) {
         smd_plan_t p{};
         const int rc = whole_plan(B, H, W, o, &p);
         if (rc != SMD_OK) return rc;
+        r.kernel = p.kernel;
         r.spread = p.kernel == SMD_KERNEL_TC_SPREAD;
         int chunks = o.chunks;
         if (chunks == 0) {
@@ -127,6 +135,17 @@ int layout_of(int B, int H, int W, const Opts& o, Layout* L) {
     r.total = off;
     *L = r;
     return SMD_OK;
+}
+
+// The device address of a page-locked host buffer mapped into the current
+// device's address space, or null (pageable memory, device memory, unknown).
+const void* mapped_host(const void* p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
 
 // The library's copy streams and events of one device, created on first use
@@ -203,6 +222,43 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
     if ((kv_pool && !is_aligned(kv_pool, 16)) || (status && !is_aligned(status, 4)))
         return SMD_ERR_ALIGN;
     if (!is_aligned(workspace, 16) || workspace_bytes < L.total) return SMD_ERR_WORKSPACE;
+    // Direct access: the warp-MMA kernels read the index list and the counts
+    // with plain loads and write out and lse with plain stores, so mapped
+    // page-locked host buffers can be handed to the device call as they are.
+    // (The query still moves in by one copy: those kernels bring it into
+    // shared memory with bulk copies, which are kept to device memory.)
+    const int64_t host_bytes = static_cast<int64_t>(B) * (L.q_row + static_cast<int64_t>(W) * 4 + 4 +
+                                                          static_cast<int64_t>(H) * (1024 + 4));
+    if (L.chunks == 1 && !o.copies && host_bytes <= kDirectMaxBytes &&
+        (L.kernel == SMD_KERNEL_MMA || L.kernel == SMD_KERNEL_GROUP) && is_aligned(out_host, 16) &&
+        is_aligned(counts_host, 4) && is_aligned(lse_host, 4) &&
+        (W == 0 || is_aligned(indices_host, 4))) {
+        const void* mi = W > 0 ? mapped_host(indices_host) : nullptr;
+        const void* mc = mapped_host(counts_host);
+        const void* mo = mapped_host(out_host);
+        const void* ml = mapped_host(lse_host);
+        if ((mi || W == 0) && mc && mo && ml) {
+            uint8_t* dq = static_cast<uint8_t*>(workspace) + L.off_q;
+            if (cudaMemcpyAsync(dq, q_host, B * L.q_row, cudaMemcpyHostToDevice,
+                                reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+                return SMD_ERR_LAUNCH;
+            const int32_t* di = static_cast<const int32_t*>(mi);
+            const int32_t* dc = static_cast<const int32_t*>(mc);
+            uint16_t* dout = static_cast<uint16_t*>(const_cast<void*>(mo));
+            float* dlse = static_cast<float*>(const_cast<void*>(ml));
+            if (o.bf16)
+                return smd_sparse_mla_decode_bf16q_ws(reinterpret_cast<const uint16_t*>(dq), kv_pool, N,
+                                                      di, W, dc, B, H, sm_scale, k_scale, dout, dlse,
+                                                      status, nullptr, 0, stream);
+            if (o.G > 1)
+                return smd_sparse_mla_decode_grouped_ws(dq, kv_pool, N, di, W, dc, B, H, o.G, sm_scale,
+                                                        q_scale, k_scale, dout, dlse, status, nullptr,
+                                                        0, stream);
+            return smd_sparse_mla_decode_ws(dq, kv_pool, N, di, W, dc, B, H, sm_scale, q_scale,
+                                            k_scale, dout, dlse, status, nullptr, 0, stream);
+        }
+    }
+
     CopyEngine* eng = nullptr;
     if (L.chunks > 1) {
         eng = engine_of_current_device();

@@ -350,7 +350,7 @@ def host_call(q=A, kv=A, N=100, idx=A, W=8, counts=A, B=2, H=16, out=A, lse=A, s
     (dict(opts=smd.SmdHostOpts(1, 2, 0, 0)), smd.SMD_ERR_PLAN),
     (dict(opts=smd.SmdHostOpts(1, 0, 9, 0)), smd.SMD_ERR_PLAN),
     (dict(opts=smd.SmdHostOpts(1, 0, -1, 0)), smd.SMD_ERR_PLAN),
-    (dict(opts=smd.SmdHostOpts(1, 0, 0, 1)), smd.SMD_ERR_PLAN),
+    (dict(opts=smd.SmdHostOpts(1, 0, 0, 2)), smd.SMD_ERR_PLAN),
 ])
 def test_host_call_argument_checks(kw, code):
     assert host_call(**kw) == code

@@ -17,7 +17,8 @@ from test_parity_gpu import check, gpu_decode, oracle_decode, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def host_decode(case, dev, chunks=0, row_group=1, bf16=False, pinned=True, stream=None):
+def host_decode(case, dev, chunks=0, row_group=1, bf16=False, pinned=True, stream=None,
+                copies=0):
     import torch
     from sparse_mla_decode_gb300 import binding
     kv = torch.from_numpy(case.kv8).to(dev)
@@ -39,7 +40,7 @@ def host_decode(case, dev, chunks=0, row_group=1, bf16=False, pinned=True, strea
     binding.sparse_mla_decode_host(q, kv, idx, cnt, case.sm_scale, case.q_scale, case.k_scale,
                                    out=out, lse=lse, status=status, workspace=ws,
                                    row_group=row_group, bf16_query=bf16, chunks=chunks,
-                                   stream=stream)
+                                   stream=stream, copies=copies)
     torch.cuda.synchronize()
     assert int(status.item()) == 0, binding.smd_status_str(int(status.item()))
     return out.view(torch.int16).numpy().view(np.uint16).copy(), lse.numpy().copy()
@@ -218,3 +219,26 @@ def test_host_call_replays_in_a_cuda_graph(cuda):
     idx.copy_(torch.from_numpy(other.indices))
     cnt.copy_(torch.from_numpy(other.counts))
     assert_same(replay(), ref_other, "replay after the host inputs changed")
+
+
+@pytest.mark.parametrize("kind", ["mma", "mma_groups", "bf16q"])
+def test_direct_host_access_gives_the_bits_of_the_copies(cuda, kind):
+    """One chunk on a warp-MMA plan with page-locked buffers: the kernel reads
+    indices and counts and writes out and lse in host memory (only q is
+    copied). Same bits as copying everything (copies = 1) and as the device
+    call."""
+    from sparse_mla_decode_gb300 import binding
+    if kind == "mma_groups":
+        case = inputs.grouped_case(861, R=3, G=2, H=48, W=700, N=9000)
+        G, bf16 = 2, False
+        assert binding.smd_plan_grouped(case.B, case.H, case.W, 2).kernel == binding.SMD_KERNEL_GROUP
+    else:
+        case = inputs.random_case(862, B=5, H=64, W=256, N=20000, counts=[256, 200, 0, 255, 1])
+        G, bf16 = 1, kind == "bf16q"
+    direct = host_decode(case, cuda, row_group=G, bf16=bf16)
+    copied = host_decode(case, cuda, row_group=G, bf16=bf16, copies=1)
+    assert_same(direct, copied, kind)
+    paged = host_decode(case, cuda, row_group=G, bf16=bf16, pinned=False)
+    assert_same(paged, copied, kind + ", pageable memory (copies)")
+    if kind == "mma":
+        assert_same(direct, gpu_decode(case, cuda), "device call")
