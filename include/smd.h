@@ -404,10 +404,11 @@ typedef struct {
 
 /* The number of row chunks smd_sparse_mla_decode_host pipelines for these
  * shapes and options (opts may be NULL), written to *chunks. One chunk when
- * the device call's plan is the spread kernel (a chunk of its rows would leave
- * SMs idle) or fills fewer than three waves of the device; otherwise up to
- * four, each still filling at least one and a half waves. Host only.
- * Returns SMD_OK or SMD_ERR_SHAPE / SMD_ERR_NULL / SMD_ERR_PLAN. */
+ * the call moves at most 16 MiB of host data (q, indices, counts, out, lse),
+ * when the device call's plan is the spread kernel (a chunk of its rows would
+ * leave SMs idle) or when it fills fewer than three waves of the device;
+ * otherwise up to four, each still filling at least one and a half waves.
+ * Host only. Returns SMD_OK or SMD_ERR_SHAPE / SMD_ERR_NULL / SMD_ERR_PLAN. */
 int smd_plan_host(int32_t B, int32_t H, int32_t W, const smd_host_opts_t* opts, int32_t* chunks);
 
 /* Bytes of device workspace smd_sparse_mla_decode_host needs (opts may be
@@ -436,13 +437,13 @@ int64_t smd_workspace_bytes_host(int32_t B, int32_t H, int32_t W, const smd_host
  * `stream` has reached this point.
  * Host buffers should be page-locked (cudaHostAlloc, cudaHostRegister) for the
  * copies to overlap; pageable memory gives the same results, without overlap.
- * Direct access: with one chunk, a warp-MMA plan (SMD_KERNEL_MMA or
- * SMD_KERNEL_GROUP), at most 8 MiB of host data, and indices, counts, out and
- * lse page-locked, mapped into the device's address space
- * (cudaPointerGetAttributes reports host memory with a device pointer) and
- * aligned as the device call wants them, only q is copied: the kernel reads
- * the index list and the counts from host memory and writes out and lse there
- * itself (copies = 1 turns this off). The results are the same bits.
+ * Direct access: with one chunk, and indices, counts, out and lse page-locked,
+ * mapped into the device's address space (cudaPointerGetAttributes reports
+ * host memory with a device pointer) and aligned as the device call wants
+ * them, only q is copied: the kernel reads the index list and the counts from
+ * host memory and writes out and lse there itself (every kernel reads and
+ * writes them with plain loads and stores; copies = 1 turns this off). The
+ * results are the same bits.
  * Each chunk is decoded by the device call for its rows, so chunks = 1 gives
  * the bits of that call on all B rows, and more chunks give the bits of the
  * device calls on the chunks' rows (with the workspace when the whole batch's

@@ -364,11 +364,12 @@ def test_host_call_with_no_rows_is_a_no_op():
     (2, 16, 64, 1, False, 1),       # tiny: one small launch
     (5, 64, 256, 1, False, 1),      # latency
     (64, 128, 2048, 1, False, 1),   # DSA: the spread kernel takes the whole batch
-    (256, 128, 2048, 1, False, 4),  # throughput: 1024 cluster CTAs, four chunks of 64 rows
-    (128, 16, 8192, 4, False, 2),   # dense-as-sparse: 512 CTAs, two chunks of 16 groups
+    (256, 128, 2048, 1, False, 4),  # throughput: 54 MB of host data, 1024 cluster CTAs: 4 x 64 rows
+    (128, 16, 8192, 4, False, 1),   # dense-as-sparse: 512 CTAs, but only 7.4 MB of host data
+    (512, 16, 8192, 4, False, 4),   # four times the requests: 30 MB, 2048 CTAs
     (256, 128, 2048, 1, True, 1),   # bf16 query on the spread kernel
 ])
-def test_host_plan_chunks_the_rows_only_where_each_chunk_fills_the_device(B, H, W, G, bf16, chunks):
+def test_host_plan_chunks_large_host_data_where_each_chunk_fills_the_device(B, H, W, G, bf16, chunks):
     # No device here: the plan is made for a 152-SM GB300.
     assert smd.smd_plan_host(B, H, W, G, bf16) == chunks
 

@@ -221,14 +221,18 @@ def test_host_call_replays_in_a_cuda_graph(cuda):
     assert_same(replay(), ref_other, "replay after the host inputs changed")
 
 
-@pytest.mark.parametrize("kind", ["mma", "mma_groups", "bf16q"])
+@pytest.mark.parametrize("kind", ["mma", "mma_groups", "bf16q", "tc"])
 def test_direct_host_access_gives_the_bits_of_the_copies(cuda, kind):
-    """One chunk on a warp-MMA plan with page-locked buffers: the kernel reads
-    indices and counts and writes out and lse in host memory (only q is
-    copied). Same bits as copying everything (copies = 1) and as the device
-    call."""
+    """One chunk with page-locked buffers: the kernel reads indices and counts
+    and writes out and lse in host memory (only q is copied), on the warp-MMA
+    kernels and on the tcgen05 cluster kernel. Same bits as copying everything
+    (copies = 1) and as the device call."""
     from sparse_mla_decode_gb300 import binding
-    if kind == "mma_groups":
+    if kind == "tc":
+        case = inputs.random_case(863, B=4, H=128, W=400, N=9000, counts=[400, 1, 0, 257])
+        G, bf16 = 1, False
+        assert binding.smd_plan_ws(case.B, case.H, case.W).kernel == binding.SMD_KERNEL_TC
+    elif kind == "mma_groups":
         case = inputs.grouped_case(861, R=3, G=2, H=48, W=700, N=9000)
         G, bf16 = 2, False
         assert binding.smd_plan_grouped(case.B, case.H, case.W, 2).kernel == binding.SMD_KERNEL_GROUP
@@ -240,5 +244,5 @@ def test_direct_host_access_gives_the_bits_of_the_copies(cuda, kind):
     assert_same(direct, copied, kind)
     paged = host_decode(case, cuda, row_group=G, bf16=bf16, pinned=False)
     assert_same(paged, copied, kind + ", pageable memory (copies)")
-    if kind == "mma":
+    if kind in ("mma", "tc"):
         assert_same(direct, gpu_decode(case, cuda), "device call")
