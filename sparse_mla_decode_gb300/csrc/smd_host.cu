@@ -231,9 +231,12 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
     // counts with plain loads and writes out and lse with plain stores (TMA
     // touches only the query and the cache pool), so when those four host
     // buffers are page-locked and mapped into the device's address space they
-    // are handed to the device call as they are, and only q is copied. (With
-    // several chunks the copy engines move the data faster than the kernels'
-    // own host-memory traffic: throughput 325 against 418 us.)
+    // are handed to the device call as they are, and only q is copied. The
+    // warp-MMA kernel (SMD_KERNEL_MMA) loads q with 16-byte cp.async as well,
+    // so there q is read in place too; the others bring it in by TMA or bulk
+    // copies, which are kept to device memory. (With several chunks the copy
+    // engines move the data faster than the kernels' own host-memory traffic:
+    // throughput 325 against 418 us.)
     const int32_t* m_idx = nullptr;
     const int32_t* m_cnt = nullptr;
     uint16_t* m_out = nullptr;
@@ -246,6 +249,9 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
         m_lse = static_cast<float*>(const_cast<void*>(mapped_host(lse_host)));
     }
     const bool direct = (m_idx != nullptr || W == 0) && m_cnt && m_out && m_lse;
+    const uint8_t* m_q = (direct && L.kernel == SMD_KERNEL_MMA && is_aligned(q_host, 16))
+                             ? static_cast<const uint8_t*>(mapped_host(q_host))
+                             : nullptr;
 
     CopyEngine* eng = nullptr;
     if (L.chunks > 1) {
@@ -254,7 +260,7 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
     }
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    uint8_t* dq = ws + L.off_q;
+    uint8_t* dq = m_q != nullptr ? const_cast<uint8_t*>(m_q) : ws + L.off_q;
     const int32_t* didx = direct ? m_idx : reinterpret_cast<const int32_t*>(ws + L.off_idx);
     const int32_t* dcnt = direct ? m_cnt : reinterpret_cast<const int32_t*>(ws + L.off_cnt);
     uint16_t* dout = direct ? m_out : reinterpret_cast<uint16_t*>(ws + L.off_out);
@@ -274,8 +280,9 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
     // Chunk c's copies in / out, queued on s.
     auto upload = [&](int c, cudaStream_t s) {
         const int r0 = c * L.rows, nr = std::min(L.rows, B - r0);
-        chk(cudaMemcpyAsync(dq + r0 * L.q_row, static_cast<const uint8_t*>(q_host) + r0 * L.q_row,
-                            nr * L.q_row, cudaMemcpyHostToDevice, s));
+        if (m_q == nullptr)
+            chk(cudaMemcpyAsync(dq + r0 * L.q_row, static_cast<const uint8_t*>(q_host) + r0 * L.q_row,
+                                nr * L.q_row, cudaMemcpyHostToDevice, s));
         if (direct) return;
         if (W > 0)
             chk(cudaMemcpyAsync(const_cast<int32_t*>(didx) + static_cast<int64_t>(r0) * W,

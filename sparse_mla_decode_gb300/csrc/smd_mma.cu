@@ -142,7 +142,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
 
     if (tid == 0) {
         for (int c = 0; c < nchunk_bars; ++c) mbar_init(bars + 8 * c, kMmaThreads);
-        mbar_init(q_bar, 1);
+        // E4M3 query: every thread's 16-byte copies arrive, and thread 0's
+        // expect-tx below (0 bytes, or the stall hook's 16).
+        mbar_init(q_bar, QS ? 1 : 1 + kMmaThreads);
         mbar_init(max_bar, 1);
         mbar_init(in_bar, 1);
         fence_mbar_init();
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         mbar_arrive_expect_tx(in_bar, (S - 1) * (CH * CW * 4 + CH * 4));
         // (inject_stall: the barrier also expects 16 bytes nobody sends, so
         // the bounded wait below runs out; a test hook for the timeout path.)
-        mbar_arrive_expect_tx(q_bar, (QS ? 0 : CH * kRow) + (p.inject_stall ? 16 : 0));
+        mbar_arrive_expect_tx(q_bar, p.inject_stall ? 16 : 0);
     }
     for (int h = tid; h < CH; h += kMmaThreads) lsum[h] = 0.f;
     __syncthreads();
@@ -163,9 +165,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     float* lamh = reinterpret_cast<float*>(smem + p.L.lamh);
     if constexpr (QS) {
         split_query<CH>(p, b, head0, smem + p.L.q, smem + p.L.q + CH * kRowPitch, lamh);
-    } else if (tid < CH) {
-        const uint8_t* src = p.a.q + (static_cast<int64_t>(b) * p.a.H + head0 + tid) * kRow;
-        bulk_g2s(q_s + tid * kRowPitch, src, kRow, q_bar);
+    } else {
+        // 16-byte copies through the load/store unit (the query may be mapped
+        // host memory), spread over all threads; each thread arrives once its
+        // own have landed.
+        const uint8_t* src = p.a.q + (static_cast<int64_t>(b) * p.a.H + head0) * kRow;
+        for (int e = tid; e < CH * (kRow / 16); e += kMmaThreads) {
+            const int r = e / (kRow / 16), c16 = e - r * (kRow / 16);
+            cp_async16(q_s + r * kRowPitch + 16 * c16, src + r * kRow + 16 * c16);
+        }
+        cp_async_arrive(q_bar);
     }
 
     // ---- this CTA's keys: [first, first + mine) of the row ------------------
