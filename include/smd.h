@@ -463,6 +463,31 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
                                void* workspace, int64_t workspace_bytes,
                                const smd_host_opts_t* opts, smd_stream_t stream);
 
+/* Bytes of device workspace smd_topk_select_host needs when it copies:
+ * staging for the logits (rows padded to a multiple of 8), row ends,
+ * indices and counts, each 256-byte aligned. Negative for invalid shapes.
+ * Host only. */
+int64_t smd_workspace_bytes_topk_host(int32_t B, int32_t L, int32_t K);
+
+/* The top-k select with its inputs and outputs in host memory: logits_host
+ * [B, row_stride] bf16 bits and row_ends_host [B] (or NULL) are read, and
+ * indices_host [B, K] and counts_host [B] written, as by smd_topk_select
+ * (same arguments, same results). When all of them are page-locked and
+ * mapped into the device's address space (and copies == 0), the select reads
+ * and writes them in place (its kernel uses plain loads and stores); the
+ * workspace is then not touched and may be NULL. Otherwise the logits are
+ * copied into the workspace (at least smd_workspace_bytes_topk_host bytes,
+ * 16-byte aligned, else SMD_ERR_WORKSPACE) with rows padded to a multiple of
+ * 8 logits, and the results are copied back, all on `stream` in order.
+ * copies: 0 the library's choice, 1 always copy (other values SMD_ERR_PLAN).
+ * Asynchronous on `stream`; the results are in the host buffers once `stream`
+ * has reached this point. */
+int smd_topk_select_host(const uint16_t* logits_host, int64_t row_stride,
+                         const int32_t* row_ends_host, int32_t B, int32_t L, int32_t K,
+                         int32_t* indices_host, int32_t* counts_host, int32_t* status,
+                         void* workspace, int64_t workspace_bytes, int32_t copies,
+                         smd_stream_t stream);
+
 /* The base-2 logit scale the kernels use: fp32(sm*q_s*k_s*log2 e),
  * evaluated in double and rounded once. */
 float smd_scale_log2(float sm_scale, float q_scale, float k_scale);

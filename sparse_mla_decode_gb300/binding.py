@@ -137,6 +137,11 @@ def lib() -> ctypes.CDLL:
             so.smd_sparse_mla_decode_host.restype = ctypes.c_int
             so.smd_sparse_mla_decode_host.argtypes = _DECODE_ARGS[:-1] + [
                 ctypes.c_void_p, ctypes.c_int64, ctypes.POINTER(SmdHostOpts), ctypes.c_void_p]
+            so.smd_workspace_bytes_topk_host.restype = ctypes.c_int64
+            so.smd_workspace_bytes_topk_host.argtypes = [ctypes.c_int32] * 3
+            so.smd_topk_select_host.restype = ctypes.c_int
+            so.smd_topk_select_host.argtypes = tk_args[:-1] + [ctypes.c_void_p, ctypes.c_int64,
+                                                               ctypes.c_int32, ctypes.c_void_p]
             so.smd_scale_log2.restype = ctypes.c_float
             so.smd_scale_log2.argtypes = [ctypes.c_float] * 3
             so.smd_status_str.restype = ctypes.c_char_p
@@ -325,6 +330,16 @@ def smd_sparse_mla_decode_host(q, kv_pool, N, indices, W, counts, B, H, sm_scale
     return lib().smd_sparse_mla_decode_host(q, kv_pool, N, indices, W, counts, B, H, sm_scale,
                                             q_scale, k_scale, out, lse, status, workspace,
                                             workspace_bytes, ref, stream)
+
+
+def smd_workspace_bytes_topk_host(B: int, L: int, K: int) -> int:
+    return int(lib().smd_workspace_bytes_topk_host(B, L, K))
+
+
+def smd_topk_select_host(logits, row_stride, row_ends, B, L, K, indices, counts, status,
+                         workspace, workspace_bytes, copies, stream) -> int:
+    return lib().smd_topk_select_host(logits, row_stride, row_ends, B, L, K, indices, counts,
+                                      status, workspace, workspace_bytes, copies, stream)
 
 
 def smd_scale_log2(sm_scale: float, q_scale: float, k_scale: float) -> float:
@@ -568,4 +583,49 @@ def topk_select(logits, K: int, row_ends=None, indices=None, counts=None, stream
                             _ptr(counts), _ptr(status), int(stream), int(cluster))
     if rc != SMD_OK:
         raise SmdError(rc, "smd_topk_select")
+    return indices, counts
+
+
+def topk_select_host(logits, K: int, row_ends=None, indices=None, counts=None, stream=None,
+                     status=None, workspace=None, copies: int = 0, device=None):
+    """Top-k select with host buffers (smd_topk_select_host): logits a bfloat16
+    CPU tensor [B, L] with unit column stride, row_ends an optional int32 CPU
+    tensor [B]; page-locked (``pin_memory()``) for the select to read them in
+    place. Returns (indices int32 [B, K], counts int32 [B]) CPU tensors,
+    complete once ``stream`` has reached the end of the call."""
+    import torch
+
+    if logits.dtype not in (torch.bfloat16, torch.int16, torch.uint16):
+        raise TypeError(f"logits: expected bfloat16, got {logits.dtype}")
+    if logits.is_cuda or logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be a CPU tensor [B, L] with unit column stride")
+    B, L = int(logits.shape[0]), int(logits.shape[1])
+    stride = int(logits.stride(0)) if B > 1 else L
+    if row_ends is not None and (row_ends.dtype != torch.int32 or row_ends.is_cuda):
+        raise TypeError("row_ends must be an int32 CPU tensor")
+    if indices is None:
+        indices = torch.empty((B, K), dtype=torch.int32).pin_memory()
+    if counts is None:
+        counts = torch.empty((B,), dtype=torch.int32).pin_memory()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    if workspace is None and copies:
+        workspace = torch.empty(max(smd_workspace_bytes_topk_host(B, L, int(K)), 16),
+                                dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = smd_topk_select_host(_ptr(logits), stride, _ptr(row_ends), B, L, int(K), _ptr(indices),
+                              _ptr(counts), _ptr(status), _ptr(workspace), nbytes, int(copies),
+                              int(stream))
+    if rc == SMD_ERR_WORKSPACE and workspace is None:
+        # the buffers could not be read in place: copy through a workspace
+        workspace = torch.empty(max(smd_workspace_bytes_topk_host(B, L, int(K)), 16),
+                                dtype=torch.uint8, device=dev)
+        rc = smd_topk_select_host(_ptr(logits), stride, _ptr(row_ends), B, L, int(K),
+                                  _ptr(indices), _ptr(counts), _ptr(status), _ptr(workspace),
+                                  workspace.numel(), int(copies), int(stream))
+    if rc != SMD_OK:
+        raise SmdError(rc, "smd_topk_select_host")
     return indices, counts

@@ -1,7 +1,10 @@
-// The decode from and to host memory (smd_sparse_mla_decode_host): the rows
-// are cut into chunks whose host-to-device copies, decode and device-to-host
-// copies are pipelined over a few library-owned copy streams and the caller's
-// stream. Host code only; every decode goes through the public device calls.
+// The decode and the top-k select from and to host memory
+// (smd_sparse_mla_decode_host, smd_topk_select_host): the kernels read and
+// write mapped page-locked host buffers in place where they can; otherwise
+// the data is copied, for the decode in row chunks whose copies in, decode
+// and copies out are pipelined over a few library-owned copy streams and the
+// caller's stream. Host code only; every launch goes through the public
+// device calls.
 #include <algorithm>
 #include <cstdint>
 #include <mutex>
@@ -365,6 +368,75 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
     }
     if (result == SMD_OK && !cuda_ok) result = SMD_ERR_LAUNCH;
     return result;
+}
+
+int64_t smd_workspace_bytes_topk_host(int32_t B, int32_t L, int32_t K) {
+    using namespace smd;
+    if (B < 0 || L < 0 || K < 1) return SMD_ERR_SHAPE;
+    const int64_t pitch = (static_cast<int64_t>(L) + 7) / 8 * 8;  // staged rows: 16-byte pieces
+    return round_up(B * pitch * 2) + round_up(static_cast<int64_t>(B) * 4) +
+           round_up(static_cast<int64_t>(B) * K * 4) + round_up(static_cast<int64_t>(B) * 4);
+}
+
+int smd_topk_select_host(const uint16_t* logits_host, int64_t row_stride,
+                         const int32_t* row_ends_host, int32_t B, int32_t L, int32_t K,
+                         int32_t* indices_host, int32_t* counts_host, int32_t* status,
+                         void* workspace, int64_t workspace_bytes, int32_t copies,
+                         smd_stream_t stream) {
+    using namespace smd;
+    if (B < 0 || L < 0 || K < 1 || row_stride < L) return SMD_ERR_SHAPE;
+    if (copies != 0 && copies != 1) return SMD_ERR_PLAN;
+    if (B == 0) return SMD_OK;
+    if (!indices_host || !counts_host || (L > 0 && !logits_host)) return SMD_ERR_NULL;
+    if ((logits_host && !is_aligned(logits_host, 2)) || !is_aligned(indices_host, 4) ||
+        !is_aligned(counts_host, 4) || (row_ends_host && !is_aligned(row_ends_host, 4)) ||
+        (status && !is_aligned(status, 4)))
+        return SMD_ERR_ALIGN;
+
+    // Direct access: the select reads the logits and the row ends with plain
+    // loads and writes the indices and counts with plain stores, so mapped
+    // page-locked host buffers go to the device call as they are.
+    if (!copies) {
+        const void* ml = L > 0 ? mapped_host(logits_host) : nullptr;
+        const void* me = row_ends_host ? mapped_host(row_ends_host) : nullptr;
+        const void* mi = mapped_host(indices_host);
+        const void* mc = mapped_host(counts_host);
+        if ((ml || L == 0) && (me || !row_ends_host) && mi && mc)
+            return smd_topk_select(static_cast<const uint16_t*>(ml), row_stride,
+                                   static_cast<const int32_t*>(me), B, L, K,
+                                   static_cast<int32_t*>(const_cast<void*>(mi)),
+                                   static_cast<int32_t*>(const_cast<void*>(mc)), status, stream);
+    }
+
+    // Copies: the logits into rows of a multiple of 8 logits (so the select
+    // reads them in 16-byte pieces), the select, the results back; all on
+    // `stream` in order.
+    const int64_t need = smd_workspace_bytes_topk_host(B, L, K);
+    if (!workspace || !is_aligned(workspace, 16) || workspace_bytes < need) return SMD_ERR_WORKSPACE;
+    const int64_t pitch = (static_cast<int64_t>(L) + 7) / 8 * 8;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint16_t* dx = reinterpret_cast<uint16_t*>(ws);
+    int32_t* de = reinterpret_cast<int32_t*>(ws + round_up(B * pitch * 2));
+    int32_t* di = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(de) + round_up(int64_t(B) * 4));
+    int32_t* dc = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(di) +
+                                             round_up(static_cast<int64_t>(B) * K * 4));
+    const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    bool ok = true;
+    if (L > 0)
+        ok = cudaMemcpy2DAsync(dx, pitch * 2, logits_host, row_stride * 2, static_cast<size_t>(L) * 2,
+                               B, cudaMemcpyHostToDevice, cs) == cudaSuccess;
+    if (ok && row_ends_host)
+        ok = cudaMemcpyAsync(de, row_ends_host, static_cast<size_t>(B) * 4, cudaMemcpyHostToDevice,
+                             cs) == cudaSuccess;
+    if (!ok) return SMD_ERR_LAUNCH;
+    const int rc = smd_topk_select(L > 0 ? dx : nullptr, pitch, row_ends_host ? de : nullptr, B, L,
+                                   K, di, dc, status, stream);
+    if (rc != SMD_OK) return rc;
+    ok = cudaMemcpyAsync(indices_host, di, static_cast<size_t>(B) * K * 4, cudaMemcpyDeviceToHost,
+                         cs) == cudaSuccess &&
+         cudaMemcpyAsync(counts_host, dc, static_cast<size_t>(B) * 4, cudaMemcpyDeviceToHost, cs) ==
+             cudaSuccess;
+    return ok ? SMD_OK : SMD_ERR_LAUNCH;
 }
 
 }  // extern "C"

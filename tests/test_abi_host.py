@@ -386,3 +386,35 @@ def test_host_workspace_holds_the_staging_and_the_chunk_workspace(B, H, W, G, bf
     for chunks in (1, 2, 3):
         rows = -(-(B // G) // chunks) * G
         assert smd.smd_plan_host(B, H, W, G, bf16, chunks) == -(-B // rows)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=0), smd.SMD_ERR_SHAPE),
+    (dict(B=-1), smd.SMD_ERR_SHAPE),
+    (dict(stride=99), smd.SMD_ERR_SHAPE),
+    (dict(copies=2), smd.SMD_ERR_PLAN),
+    (dict(idx=0), smd.SMD_ERR_NULL),
+    (dict(counts=0), smd.SMD_ERR_NULL),
+    (dict(logits=0), smd.SMD_ERR_NULL),
+    (dict(logits=A + 1), smd.SMD_ERR_ALIGN),
+    (dict(idx=A + 2), smd.SMD_ERR_ALIGN),
+    (dict(ends=A + 2), smd.SMD_ERR_ALIGN),
+    # no device here, so nothing is mapped: the copies need a workspace
+    (dict(), smd.SMD_ERR_WORKSPACE),
+    (dict(ws=A, ws_bytes=1024), smd.SMD_ERR_WORKSPACE),
+    (dict(ws=A + 8, ws_bytes=1 << 30), smd.SMD_ERR_WORKSPACE),
+])
+def test_topk_host_argument_checks(kw, code):
+    a = dict(logits=A, stride=100, ends=0, B=2, L=100, K=8, idx=A, counts=A, status=0, ws=0,
+             ws_bytes=0, copies=0)
+    a.update(kw)
+    assert smd.smd_topk_select_host(a["logits"], a["stride"], a["ends"], a["B"], a["L"], a["K"],
+                                    a["idx"], a["counts"], a["status"], a["ws"], a["ws_bytes"],
+                                    a["copies"], 0) == code
+
+
+def test_topk_host_workspace_pads_rows_to_16_bytes():
+    assert smd.smd_workspace_bytes_topk_host(3, 13, 5) >= 3 * 16 * 2 + 3 * 4 + 3 * 5 * 4 + 3 * 4
+    assert smd.smd_workspace_bytes_topk_host(0, 13, 5) == 0
+    assert smd.smd_workspace_bytes_topk_host(2, 8, 0) == smd.SMD_ERR_SHAPE
+    assert smd.smd_topk_select_host(0, 0, 0, 0, 0, 1, 0, 0, 0, 0, 0, 0, 0) == smd.SMD_OK

@@ -97,3 +97,49 @@ def test_select_feeds_the_decode(cuda):
     out_o, lse_o = oracle_decode(dec_case)
     check(out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy(), out_o, lse_o,
           "select -> decode")
+
+
+# ---- the select from and to host memory (smd_topk_select_host) ------------------
+
+def host_select(case, dev, stride=None, ends=True, pinned=True, copies=0):
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    B, L = case.logits.shape
+    buf = np.full((B, stride or L), 0x7FC1, np.uint16)  # NaN patterns in any padding
+    buf[:, :L] = case.logits
+    x = torch.from_numpy(buf.view(np.int16)).view(torch.bfloat16)
+    re = torch.from_numpy(case.row_ends.copy()) if ends else None
+    idx = torch.empty((B, case.K), dtype=torch.int32)
+    cnt = torch.empty((B,), dtype=torch.int32)
+    if pinned:
+        x = x.pin_memory()
+        re = re.pin_memory() if re is not None else None
+        idx, cnt = idx.pin_memory(), cnt.pin_memory()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    binding.topk_select_host(x[:, :L], case.K, row_ends=re, indices=idx, counts=cnt,
+                             status=status, copies=copies, device=dev)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return idx.numpy().copy(), cnt.numpy().copy()
+
+
+@pytest.mark.parametrize("stride", [None, 1003, 1024])
+def test_select_from_host_memory(cuda, stride):
+    """In place (page-locked), through copies (copies = 1, and pageable
+    memory): the device call's result, which is the oracle's."""
+    case = inputs.topk_case(11, 5, 1000, 100, scale=0.05)
+    idx_o, cnt_o = ot.topk_select(case.logits, case.K, case.row_ends)
+    for kw in (dict(), dict(copies=1), dict(pinned=False)):
+        idx_g, cnt_g = host_select(case, cuda, stride=stride, **kw)
+        assert np.array_equal(idx_g, idx_o) and np.array_equal(cnt_g, cnt_o), kw
+    idx_g, cnt_g = host_select(case, cuda, stride=stride, ends=False)
+    idx_o2, cnt_o2 = ot.topk_select(case.logits, case.K)
+    assert np.array_equal(idx_g, idx_o2) and np.array_equal(cnt_g, cnt_o2)
+
+
+def test_select_workload_from_host_memory(cuda):
+    case = inputs.topk_config()
+    idx_g, cnt_g = host_select(case, cuda)
+    idx_o, cnt_o = gpu_select(case, cuda)
+    assert np.array_equal(idx_g, idx_o) and np.array_equal(cnt_g, cnt_o)
