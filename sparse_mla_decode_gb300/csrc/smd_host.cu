@@ -235,7 +235,9 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
     // touches only the query and the cache pool), so when those four host
     // buffers are page-locked and mapped into the device's address space they
     // are handed to the device call as they are, and only q is copied. The
-    // warp-MMA kernel (SMD_KERNEL_MMA) loads q with 16-byte cp.async as well,
+    // warp-MMA kernel (SMD_KERNEL_MMA) loads q with 16-byte cp.async, and a
+    // bf16 query is read only by the split into E4M3 halves (plain loads, in
+    // the warp-MMA kernel or in the split kernel before the spread kernel),
     // so there q is read in place too; the others bring it in by TMA or bulk
     // copies, which are kept to device memory. (With several chunks the copy
     // engines move the data faster than the kernels' own host-memory traffic:
@@ -252,7 +254,8 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
         m_lse = static_cast<float*>(const_cast<void*>(mapped_host(lse_host)));
     }
     const bool direct = (m_idx != nullptr || W == 0) && m_cnt && m_out && m_lse;
-    const uint8_t* m_q = (direct && L.kernel == SMD_KERNEL_MMA && is_aligned(q_host, 16))
+    const bool q_by_loads = L.kernel == SMD_KERNEL_MMA || (o.bf16 && L.kernel == SMD_KERNEL_TC_SPREAD);
+    const uint8_t* m_q = (direct && q_by_loads && is_aligned(q_host, 16))
                              ? static_cast<const uint8_t*>(mapped_host(q_host))
                              : nullptr;
 

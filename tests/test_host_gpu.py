@@ -246,3 +246,24 @@ def test_direct_host_access_gives_the_bits_of_the_copies(cuda, kind):
     assert_same(paged, copied, kind + ", pageable memory (copies)")
     if kind in ("mma", "tc"):
         assert_same(direct, gpu_decode(case, cuda), "device call")
+
+
+def test_bf16_query_on_the_spread_plan_read_in_place(cuda):
+    """H = 128 rows longer than a cluster holds with a bf16 query: the split
+    kernel reads the query from host memory, the spread kernel decodes; same
+    bits as copying it (copies = 1) and as the device call with a workspace."""
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.random_case(871, B=3, H=128, W=2600, N=30000, counts=[2600, 0, 1800])
+    assert binding.smd_plan_bf16q(case.B, case.H, case.W, 1).kernel == binding.SMD_KERNEL_TC_SPREAD
+    direct = host_decode(case, cuda, bf16=True)
+    copied = host_decode(case, cuda, bf16=True, copies=1)
+    assert_same(direct, copied, "bf16 query, spread plan")
+    q16 = torch.from_numpy(case.q16.view(np.int16)).to(cuda).view(torch.bfloat16)
+    _, kv, idx, cnt = to_dev(case, cuda)
+    ws = device_ws(case, cuda, bf16=True)
+    out, lse = binding.sparse_mla_decode_bf16q(q16, kv, idx, cnt, case.sm_scale, case.k_scale,
+                                               workspace=ws)
+    torch.cuda.synchronize()
+    assert_same(direct, (out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy()),
+                "device call")
