@@ -445,8 +445,10 @@ int64_t smd_workspace_bytes_host(int32_t B, int32_t H, int32_t W, const smd_host
  * writes them with plain loads and stores; copies = 1 turns this off). On
  * the warp-MMA plan (SMD_KERNEL_MMA), which loads q with 16-byte cp.async,
  * and for a bf16 query on the spread plan (read only by the split into E4M3
- * halves), a mapped q is read in place as well and nothing is copied. The
- * results are the same bits.
+ * halves), a mapped q is read in place as well and nothing is copied; on the
+ * other plans a mapped q is pulled into the workspace by a small copy kernel
+ * (the SMs' loads read host memory faster than one copy-engine transfer).
+ * The results are the same bits.
  * Each chunk is decoded by the device call for its rows, so chunks = 1 gives
  * the bits of that call on all B rows, and more chunks give the bits of the
  * device calls on the chunks' rows (with the workspace when the whole batch's
