@@ -256,21 +256,28 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
     const int32_t* m_cnt = nullptr;
     uint16_t* m_out = nullptr;
     float* m_lse = nullptr;
-    if (L.chunks == 1 && !o.copies && is_aligned(out_host, 16) && is_aligned(counts_host, 4) &&
-        is_aligned(lse_host, 4) && (W == 0 || is_aligned(indices_host, 4))) {
-        m_idx = W > 0 ? static_cast<const int32_t*>(mapped_host(indices_host)) : nullptr;
-        m_cnt = static_cast<const int32_t*>(mapped_host(counts_host));
-        m_out = static_cast<uint16_t*>(const_cast<void*>(mapped_host(out_host)));
-        m_lse = static_cast<float*>(const_cast<void*>(mapped_host(lse_host)));
+    const uint8_t* q_mapped = nullptr;
+    if (!o.copies) {
+        if (W > 0 && is_aligned(indices_host, 4))
+            m_idx = static_cast<const int32_t*>(mapped_host(indices_host));
+        if (is_aligned(counts_host, 4)) m_cnt = static_cast<const int32_t*>(mapped_host(counts_host));
+        if (is_aligned(out_host, 16))
+            m_out = static_cast<uint16_t*>(const_cast<void*>(mapped_host(out_host)));
+        if (is_aligned(lse_host, 4)) m_lse = static_cast<float*>(const_cast<void*>(mapped_host(lse_host)));
+        if (is_aligned(q_host, 16)) q_mapped = static_cast<const uint8_t*>(mapped_host(q_host));
     }
-    const bool direct = (m_idx != nullptr || W == 0) && m_cnt && m_out && m_lse;
+    // One chunk: everything in place when indices, counts, out and lse are.
+    const bool direct = L.chunks == 1 && (m_idx != nullptr || W == 0) && m_cnt && m_out && m_lse;
     const bool q_by_loads = L.kernel == SMD_KERNEL_MMA || (o.bf16 && L.kernel == SMD_KERNEL_TC_SPREAD);
-    const uint8_t* q_mapped = (direct && is_aligned(q_host, 16))
-                                  ? static_cast<const uint8_t*>(mapped_host(q_host))
-                                  : nullptr;
-    const uint8_t* m_q = q_by_loads ? q_mapped : nullptr;
-    // Otherwise a mapped q is pulled into the staging area by the SMs' loads.
-    const uint8_t* q_pull = q_by_loads ? nullptr : q_mapped;
+    const uint8_t* m_q = (direct && q_by_loads) ? q_mapped : nullptr;
+    // Otherwise a mapped q is pulled into the staging area by the SMs' loads:
+    // on one chunk, and for chunk 0 of several (nothing is decoded yet then,
+    // so the copy kernel has the SMs; later chunks' copies overlap decodes and
+    // stay on the copy engine).
+    const uint8_t* q_pull = m_q != nullptr ? nullptr : q_mapped;
+    // Several chunks: the last chunk's out and lse go straight to host memory
+    // when mapped (no download after the last decode).
+    const bool last_in_place = L.chunks > 1 && m_out && m_lse;
 
     CopyEngine* eng = nullptr;
     if (L.chunks > 1) {
@@ -282,11 +289,13 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
     uint8_t* dq = m_q != nullptr ? const_cast<uint8_t*>(m_q) : ws + L.off_q;
     const int32_t* didx = direct ? m_idx : reinterpret_cast<const int32_t*>(ws + L.off_idx);
     const int32_t* dcnt = direct ? m_cnt : reinterpret_cast<const int32_t*>(ws + L.off_cnt);
-    uint16_t* dout = direct ? m_out : reinterpret_cast<uint16_t*>(ws + L.off_out);
-    float* dlse = direct ? m_lse : reinterpret_cast<float*>(ws + L.off_lse);
+    uint16_t* const sout = reinterpret_cast<uint16_t*>(ws + L.off_out);
+    float* const slse = reinterpret_cast<float*>(ws + L.off_lse);
     void* dws = L.dws_bytes > 0 ? ws + L.off_dws : nullptr;
     const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
     const int64_t out_row = static_cast<int64_t>(H) * 512 * 2, lse_row = static_cast<int64_t>(H) * 4;
+    // Where chunk c's out and lse go: host memory (in place) or staging.
+    auto in_place = [&](int c) { return direct || (last_in_place && c == L.chunks - 1); };
 
     std::unique_lock<std::mutex> lock;
     if (eng != nullptr) lock = std::unique_lock<std::mutex>(eng->mu);
@@ -299,7 +308,7 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
     // Chunk c's copies in / out, queued on s.
     auto upload = [&](int c, cudaStream_t s) {
         const int r0 = c * L.rows, nr = std::min(L.rows, B - r0);
-        if (q_pull != nullptr) {
+        if (q_pull != nullptr && c == 0) {
             const int64_t n16 = nr * L.q_row / 16;  // q rows are multiples of 16 bytes
             const int blocks = static_cast<int>(std::min<int64_t>((n16 + 255) / 256, 4 * host_sm_count()));
             host_to_device16<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(q_pull + r0 * L.q_row),
@@ -318,20 +327,20 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
                             static_cast<int64_t>(nr) * 4, cudaMemcpyHostToDevice, s));
     };
     auto download = [&](int c, cudaStream_t s) {
-        if (direct) return;  // the kernel wrote them in host memory
+        if (in_place(c)) return;  // the kernel wrote them in host memory
         const int r0 = c * L.rows, nr = std::min(L.rows, B - r0);
         chk(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(out_host) + r0 * out_row,
-                            reinterpret_cast<const uint8_t*>(dout) + r0 * out_row, nr * out_row,
+                            reinterpret_cast<const uint8_t*>(sout) + r0 * out_row, nr * out_row,
                             cudaMemcpyDeviceToHost, s));
         chk(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse_host) + r0 * lse_row,
-                            reinterpret_cast<const uint8_t*>(dlse) + r0 * lse_row, nr * lse_row,
+                            reinterpret_cast<const uint8_t*>(slse) + r0 * lse_row, nr * lse_row,
                             cudaMemcpyDeviceToHost, s));
     };
     auto decode = [&](int c) {
         const int r0 = c * L.rows, nr = std::min(L.rows, B - r0);
         const int32_t* ci = didx + static_cast<int64_t>(r0) * W;
-        uint16_t* co = dout + static_cast<int64_t>(r0) * H * 512;
-        float* cl = dlse + static_cast<int64_t>(r0) * H;
+        uint16_t* co = (in_place(c) ? m_out : sout) + static_cast<int64_t>(r0) * H * 512;
+        float* cl = (in_place(c) ? m_lse : slse) + static_cast<int64_t>(r0) * H;
         const int64_t dbytes = dws != nullptr ? L.dws_bytes : 0;
         if (o.bf16)
             return smd_sparse_mla_decode_bf16q_ws(reinterpret_cast<const uint16_t*>(dq + r0 * L.q_row),
