@@ -431,7 +431,8 @@ int64_t smd_workspace_bytes_host(int32_t B, int32_t H, int32_t W, const smd_host
  * chunks are decoded); each chunk is decoded on `stream` once it is in; every
  * chunk but the last moves out on the library's download stream while the
  * next one is decoded, the last on `stream`, which then waits for both copy
- * streams. So the call is ordered on `stream` like a kernel launch (and can be
+ * streams. (With mapped host buffers, chunk 0's q is pulled in by a copy
+ * kernel and the last chunk's out and lse are written in place.) So the call is ordered on `stream` like a kernel launch (and can be
  * captured in a CUDA graph from `stream`). The call is asynchronous: host
  * buffers must stay valid, and the results are in out_host / lse_host once
  * `stream` has reached this point.
