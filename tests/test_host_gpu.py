@@ -267,3 +267,34 @@ def test_bf16_query_on_the_spread_plan_read_in_place(cuda):
     torch.cuda.synchronize()
     assert_same(direct, (out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy()),
                 "device call")
+
+
+def test_bf16_query_in_chunks(cuda):
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.random_case(881, B=6, H=64, W=300, N=9000, counts=[300, 0, 17, 299, 150, 1])
+    got = host_decode(case, cuda, bf16=True, chunks=2)
+    for r0 in (0, 3):
+        part = rows_of(case, r0, r0 + 3)
+        q16 = torch.from_numpy(part.q16.view(np.int16)).to(cuda).view(torch.bfloat16)
+        _, kv, idx, cnt = to_dev(part, cuda)
+        out, lse = binding.sparse_mla_decode_bf16q(q16, kv, idx, cnt, case.sm_scale, case.k_scale)
+        torch.cuda.synchronize()
+        ref = (out.view(torch.int16).cpu().numpy().view(np.uint16), lse.cpu().numpy())
+        assert_same((got[0][r0:r0 + 3], got[1][r0:r0 + 3]), ref, f"bf16 rows {r0}..")
+
+
+@pytest.mark.parametrize("copies", [0, 1])
+def test_zero_width_rows_from_host_memory(cuda, copies):
+    """W = 0 (no index array at all): every row is empty, zeros and -inf."""
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    B, H = 3, 32
+    q = torch.from_numpy(inputs.random_case(882, B=B, H=H, W=4, N=100).q8).pin_memory()
+    kv = torch.zeros((16, 576), dtype=torch.uint8, device=cuda)
+    idx = torch.zeros((B, 0), dtype=torch.int32)
+    cnt = torch.tensor([5, 0, -2], dtype=torch.int32).pin_memory()
+    out, lse = binding.sparse_mla_decode_host(q, kv, idx, cnt, 0.1, 1.0, 1.0, copies=copies)
+    torch.cuda.synchronize()
+    assert not torch.any(out.float() != 0)
+    assert torch.all(torch.isneginf(lse))
