@@ -102,6 +102,7 @@ __device__ __forceinline__ void qk_job(uint32_t slot_s, uint32_t q_s, int t, int
 template <int G>
 __global__ void __launch_bounds__(kMmaThreads, 1) group_decode_kernel(const GroupParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
+    pdl_entry();
     constexpr int CH = kHeadsPerTile * G;  // tile t: heads head0 .. head0 + 15 of row b0 + t
     constexpr int kJobs = 4 * G;           // 16-key QK jobs per chunk, one per warp
 
@@ -495,13 +496,17 @@ int launch_g(const GroupParams& prm, const GroupConfig& cfg, const CallArgs& a, 
     lc.blockDim = dim3(kMmaThreads, 1, 1);
     lc.dynamicSmemBytes = static_cast<size_t>(cfg.layout.total);
     lc.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(cfg.split);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
-    lc.numAttrs = 1;
+    // Programmatic dependent launch: this grid may be scheduled while the
+    // kernel before it finishes (pdl_entry waits for that kernel's completion).
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    lc.numAttrs = 2;
     if (cudaLaunchKernelEx(&lc, group_decode_kernel<G>, prm) != cudaSuccess) {
         (void)cudaGetLastError();
         return SMD_ERR_LAUNCH;

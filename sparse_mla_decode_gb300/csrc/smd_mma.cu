@@ -93,6 +93,7 @@ __device__ __forceinline__ void split_query(const MmaParams& p, int b, int head0
 template <int T, bool QS>
 __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
+    pdl_entry();
     constexpr int CH = kHeadsPerTile * T;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -525,13 +526,17 @@ int launch_t(const MmaParams& prm, const MmaConfig& cfg, const CallArgs& a, cuda
     lc.blockDim = dim3(kMmaThreads, 1, 1);
     lc.dynamicSmemBytes = static_cast<size_t>(cfg.layout.total);
     lc.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(cfg.split);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
-    lc.numAttrs = 1;
+    // Programmatic dependent launch: this grid may be scheduled while the
+    // kernel before it finishes (pdl_entry waits for that kernel's completion).
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    lc.numAttrs = 2;
     err = cudaLaunchKernelEx(&lc, kern, prm);
     if (err != cudaSuccess) {
         (void)cudaGetLastError();

@@ -34,6 +34,17 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 
 // Makes barrier initialisation visible to the cluster (and the async proxy).
+// Programmatic dependent launch. Every kernel of this library starts with
+// pdl_entry(): the next kernel on the stream may then be scheduled as soon as
+// all of this grid's CTAs have started (it waits in its own pdl_entry for
+// this grid to complete), and this grid waits here for the kernel before it
+// to complete, with its writes visible, before its first global access. Both
+// are no-ops when the launch did not ask for programmatic serialization.
+__device__ __forceinline__ void pdl_entry() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

@@ -541,6 +541,7 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_decode_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    pdl_entry();
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t base = smem_addr(smem);
     const uint32_t bars = base + kOffBars;
@@ -791,13 +792,17 @@ int launch_tc(const CallArgs& a, const TcConfig& cfg, cudaStream_t stream) {
     lc.blockDim = dim3(kTcThreads, 1, 1);
     lc.dynamicSmemBytes = static_cast<size_t>(kSmemBytes);
     lc.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(cfg.split);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
-    lc.numAttrs = 1;
+    // Programmatic dependent launch: this grid may be scheduled while the
+    // kernel before it finishes (pdl_entry waits for that kernel's completion).
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    lc.numAttrs = 2;
     if (cudaLaunchKernelEx(&lc, tc_decode_kernel, maps, prm) != cudaSuccess) {
         (void)cudaGetLastError();
         return SMD_ERR_LAUNCH;

@@ -159,6 +159,7 @@ __device__ __forceinline__ int cluster_bins(const int* local, const int* inbox, 
 
 __global__ void __launch_bounds__(kTkThreads, 2) topk_select_kernel(const TopkParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
+    pdl_entry();
     uint4* cache = reinterpret_cast<uint4*>(smem + kOffCache);
     int* hist = reinterpret_cast<int*>(smem + kOffHist);
     int* wtot = reinterpret_cast<int*>(smem + kOffWarp);
@@ -423,13 +424,17 @@ int launch_topk(const uint16_t* logits, int64_t stride, const int32_t* row_ends,
     lc.blockDim = dim3(kTkThreads, 1, 1);
     lc.dynamicSmemBytes = static_cast<size_t>(kTkSmemBytes);
     lc.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(C);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     lc.attrs = attr;
-    lc.numAttrs = 1;
+    // Programmatic dependent launch: this grid may be scheduled while the
+    // kernel before it finishes (pdl_entry waits for that kernel's completion).
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    lc.numAttrs = 2;
     if (cudaLaunchKernelEx(&lc, topk_select_kernel, p) != cudaSuccess) {
         (void)cudaGetLastError();
         return SMD_ERR_LAUNCH;
