@@ -196,3 +196,18 @@ def test_bf16q_spread_timeout_is_reported_and_the_context_survives(cuda):
     out_g, lse_g = bf16q_ws(case, cuda, tensors=t)
     out_o, lse_o = oracle_bf16q(case)
     check(out_g, lse_g, out_o, lse_o, "bf16q spread after a timeout")
+
+
+def test_bf16q_spread_throughput_config_sampled(cuda):
+    """256 rows of 2048 keys: 1024 pieces in seven rounds over the cooperative
+    grid, four pieces a unit exchanging partials; sampled rows of every round
+    and piece position against the oracle."""
+    from sparse_mla_decode_gb300 import binding
+    case = inputs.config("throughput")
+    assert binding.smd_plan_bf16q(case.B, case.H, case.W,
+                                  binding.smd_workspace_bytes_bf16q(case.B, case.H, case.W)
+                                  ).kernel == binding.SMD_KERNEL_TC_SPREAD
+    out_g, lse_g = bf16q_ws(case, cuda)
+    rows = [0, 37, 38, 151, 152, 255]
+    out_o, lse_o = oracle_bf16q(case, rows)
+    check(out_g[rows], lse_g[rows], out_o, lse_o, "bf16q spread throughput")
