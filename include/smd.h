@@ -213,7 +213,9 @@ int smd_sparse_mla_decode_ex(const uint8_t* q, const uint8_t* kv_pool, int64_t N
  *     it: queue them on one stream or order them by events.
  *   - A device with more than 160 SMs is rejected (SMD_ERR_WORKSPACE); a CTA
  *     on an SM id beyond the array writes SMD_ERR_DEVICE to `status` and
- *     leaves the array untouched.
+ *     leaves the array untouched. That row's out and lse are then not
+ *     written although the call returned SMD_OK: pass a `status` word and
+ *     read it after the call, as for any device-side error.
  * Arguments, layouts, ownership and the other errors are those of
  * smd_sparse_mla_decode. */
 int smd_sparse_mla_decode_noalloc(const uint8_t* q, const uint8_t* kv_pool, int64_t N,

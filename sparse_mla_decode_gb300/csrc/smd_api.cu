@@ -12,6 +12,7 @@
 #include "smd.h"
 #include "smd_internal.h"
 #include "smd_ptx.cuh"
+#include "smd_tree.cuh"
 
 namespace smd {
 namespace {
@@ -73,17 +74,19 @@ int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
     // Rows up to kSpecIdxMaxW wide have their whole index list staged.
     const int spec = (W <= kSpecIdxMaxW) ? W : 0;
 
+    // A CTA takes an aligned block of the row's leaves (smd_tree.cuh); the
+    // CTA holding the most holds mma_cta_keys(W, split) keys.
     int split = 0;
     if (force && force->split) {
         split = force->split;
         if (!is_split(split)) return SMD_ERR_PLAN;
     } else {
         // Smallest split whose per-CTA share fits; then wider while the grid is
-        // under one wave and every CTA still gets >= 64 keys. A wider split
-        // shortens each CTA's gather but adds a cluster exchange of FP32
-        // partials, which is slow on this part (tens of GB/s per SM).
+        // under one wave and every CTA still gets a leaf of the widest row. A
+        // wider split shortens each CTA's gather but adds a cluster exchange of
+        // FP32 partials, which is slow on this part (tens of GB/s per SM).
         for (int s = 1; s <= 16; s *= 2) {
-            const int per = ceil_div(W, s);
+            const int per = mma_cta_keys(std::max(W, 1), s);
             const int win = std::min(window_req, std::max(kChunk, ceil_div(per, kChunk) * kChunk));
             if (per <= key_cap_limit(tiles, s, win, spec, qsplit)) {
                 split = s;
@@ -91,9 +94,9 @@ int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
             }
         }
         if (split == 0) return SMD_ERR_SHAPE;
-        while (split < 16 && units * split < sm_count && ceil_div(W, split * 2) >= 64) split *= 2;
+        while (split < 16 && units * split < sm_count && split * 2 <= mma_leaves(W)) split *= 2;
     }
-    const int per = ceil_div(std::max(W, 1), split);
+    const int per = mma_cta_keys(std::max(W, 1), split);
     const int window = std::min(window_req, std::max(kChunk, ceil_div(per, kChunk) * kChunk));
     const int key_cap = std::max(kChunk, ceil_div(per, kChunk) * kChunk);
     const MmaLayout L = mma_layout(tiles, split, window, key_cap, spec, qsplit);
@@ -106,6 +109,9 @@ int plan_mma(int B, int H, int W, int sm_count, const smd_plan_t* force, smd_pla
     cfg->inject_stall = (force && force->inject_stall) ? 1 : 0;
     cfg->spec_idx = spec > 0 ? 1 : 0;
     cfg->qsplit = qsplit ? 1 : 0;
+    // Some row of at most W keys has more leaves than CTAs: its CTAs keep a
+    // subtree stack (the widest rows have min(16, ceil(W / 64)) leaves).
+    cfg->tree_tmem = std::min(kMmaMaxLeaves, ceil_div(W, kChunk)) > split ? 1 : 0;
     cfg->split = split;
     cfg->window = window;
     cfg->key_cap = key_cap;
@@ -208,14 +214,23 @@ int plan_group(int B, int H, int W, int G, int sm_count, const smd_plan_t* force
     if (force && force->tiles && force->tiles != G) return SMD_ERR_PLAN;
     if (force && force->kernel && force->kernel != SMD_KERNEL_GROUP) return SMD_ERR_PLAN;
     const int units = B / G * (H / kHeadsPerTile);
+    // A CTA takes an aligned block of leaves of the group's longest list
+    // (smd_tree.cuh): at most kGroupMaxKeys staged indices, and at most as
+    // many leaves as the TMEM subtree stack holds levels for (128 columns a
+    // warp, 16 G a level: 2^(128 / (16 G)) leaves).
+    const int max_lpc = 1 << (128 / (kHeadsPerTile * G));
+    auto fits = [&](int s) {
+        return mma_cta_keys(std::max(W, 1), s) <= kGroupMaxKeys &&
+               mma_leaves_per_cta(std::max(W, 1), s) <= max_lpc;
+    };
     int split = 1;
-    while (split < kGroupMaxSplit && ceil_div(W, split) > kGroupMaxKeys) split *= 2;
-    if (ceil_div(W, split) > kGroupMaxKeys) return SMD_ERR_SHAPE;
+    while (split < kGroupMaxSplit && !fits(split)) split *= 2;
+    if (!fits(split)) return SMD_ERR_SHAPE;
     if (force && force->split) {
-        if (!is_split(force->split) || ceil_div(W, force->split) > kGroupMaxKeys) return SMD_ERR_PLAN;
+        if (!is_split(force->split) || !fits(force->split)) return SMD_ERR_PLAN;
         split = force->split;
     } else {
-        while (split < kGroupMaxSplit && units * split < sm_count && ceil_div(W, split * 2) >= 64)
+        while (split < kGroupMaxSplit && units * split < sm_count && split * 2 <= mma_leaves(W))
             split *= 2;
     }
     int nslots = 2;
@@ -224,9 +239,11 @@ int plan_group(int B, int H, int W, int G, int sm_count, const smd_plan_t* force
             return SMD_ERR_PLAN;
         nslots = force->window / kChunk;
     }
-    const int key_cap = std::max(kChunk, ceil_div(ceil_div(std::max(W, 1), split), kChunk) * kChunk);
+    const int key_cap =
+        std::max(kChunk, ceil_div(mma_cta_keys(std::max(W, 1), split), kChunk) * kChunk);
     const GroupLayout L = group_layout(G, split, nslots, key_cap);
     if (L.total > kMaxSmemBytes) return SMD_ERR_PLAN;
+    cfg->tree_tmem = std::min(kMmaMaxLeaves, ceil_div(W, kChunk)) > split ? 1 : 0;
     cfg->G = G;
     cfg->split = split;
     cfg->nslots = nslots;

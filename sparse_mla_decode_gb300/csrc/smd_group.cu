@@ -8,13 +8,17 @@
 // point of this kernel. A CTA takes 16 heads of each of the G rows of a group
 // (G tiles of 16 heads) and its share of the group's longest list; the S CTAs
 // of a cluster split that list as the page's SparseDcpDecode splits a row's
-// keys, and tile t masks the keys past its own row's count.
+// keys, at the leaf boundaries of smd_tree.cuh (leaves of 64 * ceil(n / 1024)
+// keys of the group's longest list, at most 16; CTA s takes an aligned block of a
+// power of two of them), and tile t masks the keys past its own row's count.
 //
 // The arithmetic per (row, head) is the warp-MMA kernel's: logits by
 // mma.sync m16n8k32 E4M3 (two accumulation chains per 8 keys), the P anchor at
 // the maximum over the whole row (cluster exchange of the CTAs' maxima),
-// P = 2^(s - m + log2 448) in E4M3, FP32 sums of the unquantized P, PV, and
-// the FP32 merge of the split partials in CTA order. Two things differ so that
+// P = 2^(s - m + log2 448) in E4M3, FP32 sums of the unquantized P, PV (each
+// leaf from zero, the subtrees of a CTA's finished leaves waiting in TMEM),
+// and the FP32 merge of the split partials by the leaf tree, so that the bits
+// do not depend on the split. Two things differ so that
 // G = 4 tiles fit in shared memory: the logits are not kept between the two
 // passes (pass A only tracks the maximum; pass B gathers each chunk again and
 // recomputes its logits, which the same MMA sequence reproduces bit for bit),
@@ -32,6 +36,7 @@
 
 #include "smd_internal.h"
 #include "smd_ptx.cuh"
+#include "smd_tree.cuh"
 
 namespace smd {
 
@@ -48,7 +53,19 @@ struct GroupParams {
     float log2_448;
     uint64_t budget_ns;
     int32_t inject_stall;
+    int32_t tree_tmem;  // 1: a CTA may hold several leaves (TMEM subtree stack)
 };
+
+// Frees the subtree stack's TMEM once every thread is past its last use
+// (warp 0 allocated it).
+__device__ __forceinline__ void release_tmem(int tree_tmem, uint32_t tbase) {
+    tc_fence_before();
+    __syncthreads();
+    if (tree_tmem && (threadIdx.x >> 5) == 0) {
+        tc_fence_after();
+        tmem_free(tbase, 512);
+    }
+}
 
 // The gathers of one chunk of `cnt` <= 64 keys (`keys`: their pool rows) into
 // a ring slot, all 576 bytes of each row, as 16-byte cp.async copies: warp w
@@ -126,6 +143,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) group_decode_kernel(const Grou
     float* lsum = reinterpret_cast<float*>(smem + p.L.lsum);
     float* rowmax = reinterpret_cast<float*>(smem + p.L.rowmax);
     int32_t* nrow = reinterpret_cast<int32_t*>(smem + p.L.nrow);
+    float* lstk = reinterpret_cast<float*>(smem + p.L.lstk);
     const int NS = p.nslots;
     const uint32_t bars = base + p.L.bars;
     const uint32_t q_bar = bars + 8 * NS;
@@ -156,7 +174,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) group_decode_kernel(const Grou
     }
     for (int h = tid; h < CH; h += kMmaThreads) lsum[h] = 0.f;
     if (tid < G) nrow[tid] = max(min(cnt_raw, W), 0);
+    if (p.tree_tmem && warp == 0) tmem_alloc(base + p.L.tslot, 512);
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = p.tree_tmem ? *reinterpret_cast<volatile uint32_t*>(smem + p.L.tslot) : 0u;
     // Every CTA's barriers are armed before any peer pushes (waited below).
     if (S > 1) cluster_arrive_relaxed();
 
@@ -178,9 +200,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) group_decode_kernel(const Grou
             ref = t;
         }
     }
-    const int per = (nmax + S - 1) / S;
-    const int first = min(nmax, split * per);
-    const int mine = min(nmax - first, per);
+    const int leaf = mma_leaf(nmax);
+    const int lpc = mma_leaves_per_cta(nmax, S);
+    const int first = min(nmax, split * lpc * leaf);
+    const int mine = min(nmax - first, lpc * leaf);
     const int32_t* ref_idx = p.a.indices + static_cast<int64_t>(b0 + ref) * W + first;
     for (int i = tid; i < mine; i += kMmaThreads) idx_s[i] = ref_idx[i];
     // The contract: the other rows' lists agree with it on the keys they read.
@@ -283,6 +306,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1) group_decode_kernel(const Grou
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[t][j][e] = 0.f;
 
+    // Leaves (as in the warp-MMA kernel): slot l of this CTA is chunks
+    // [l cpl, l cpl + cpl), walked downwards; each leaf is summed from zero and
+    // pushed into the subtree stack at its end (acc: TMEM levels of 16 G
+    // floats; the sums of P: lstk).
+    const int cpl = leaf / kChunk;
+    int tcnt = nch > 0 ? lpc - 1 - (nch - 1) / cpl : lpc;  // leaves pushed: the absent slots
+    uint32_t tpres = 0u;  // bit d: stack level d holds a subtree
+    const uint32_t tcol = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 128u * (warp >> 2);
     for (int c = nch - 1; c >= 0; --c) {
         const int s = c % NS;
         const int cnt = min(kChunk, mine - c * kChunk);
@@ -346,6 +377,39 @@ __global__ void __launch_bounds__(kMmaThreads, 1) group_decode_kernel(const Grou
                 for (int j = 0; j < 4; ++j) mma_e4m3(acc[t][j], pa, vb[0][j], vb[1][j]);
             }
         }
+        if (c % cpl == 0) {  // leaf c / cpl is complete (uniform)
+            int d = 0;
+            while ((tcnt >> d) & 1) {
+                if ((tpres >> d) & 1u) {
+                    stash_add<G>(tcol + 16u * G * d, acc);
+                    if (lane == 0)
+#pragma unroll
+                        for (int t = 0; t < G; ++t) {
+                            const int h = 16 * t + warp;
+                            lsum[h] = lstk[d * CH + h] + lsum[h];
+                        }
+                }
+                ++d;
+            }
+            tpres &= ~((1u << d) - 1u);
+            if (++tcnt < lpc) {  // not the root: keep the subtree, start the next leaf at zero
+                stash_store<G>(tcol + 16u * G * d, acc);
+                if (lane == 0)
+#pragma unroll
+                    for (int t = 0; t < G; ++t) {
+                        const int h = 16 * t + warp;
+                        lstk[d * CH + h] = lsum[h];
+                        lsum[h] = 0.f;
+                    }
+                tpres |= 1u << d;
+#pragma unroll
+                for (int t = 0; t < G; ++t)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[t][j][e] = 0.f;
+            }
+        }
         // The slot, the logits and P are free; a failed CTA issues no more copies.
         if (!__syncthreads_and(ok)) break;
         if (c - NS >= 0) gather_rows(p, slot_s, idx_s + (c - NS) * kChunk, bars + 8 * s, kChunk);
@@ -362,23 +426,24 @@ __global__ void __launch_bounds__(kMmaThreads, 1) group_decode_kernel(const Grou
                 for (int e = 0; e < 4; ++e) {
                     const int hh = g + 8 * (e >> 1);
                     const int col = 32 * warp + 8 * qd + 4 * (e & 1);
-                    const float total = 0.f + lsum[16 * t + hh];
+                    const float total = lsum[16 * t + hh];
                     const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
                     uint2 packed;
-                    packed.x = bf16x2((0.f + acc[t][0][e]) * inv, (0.f + acc[t][1][e]) * inv);
-                    packed.y = bf16x2((0.f + acc[t][2][e]) * inv, (0.f + acc[t][3][e]) * inv);
+                    packed.x = bf16x2(acc[t][0][e] * inv, acc[t][1][e] * inv);
+                    packed.y = bf16x2(acc[t][2][e] * inv, acc[t][3][e] * inv);
                     uint16_t* dst =
                         p.a.out + (static_cast<int64_t>(b0 + t) * H + head0 + hh) * kLatent + col;
                     *reinterpret_cast<uint2*>(dst) = packed;
                 }
             }
             for (int h = tid; h < CH; h += kMmaThreads) {
-                const float total = 0.f + lsum[h];
+                const float total = lsum[h];
                 p.a.lse[static_cast<int64_t>(b0 + h / kHeadsPerTile) * H + head0 + h % kHeadsPerTile] =
                     total > 0.f ? (rowmax[h] - p.log2_448 + log2f(total)) * 0.69314718055994530942f
                                 : -INFINITY;
             }
         }
+        release_tmem(p.tree_tmem, tbase);
         return;
     }
 
@@ -423,43 +488,53 @@ __global__ void __launch_bounds__(kMmaThreads, 1) group_decode_kernel(const Grou
     mbar_wait(in_bar, 0, ok, status, p.budget_ns, /*always=*/true);
     __syncthreads();  // this CTA's own partial (plain stores)
 
-    // ---- merge in CTA order; BF16(sum * k_scale / total) ---------------------
+    // ---- merge by the leaf tree; BF16(sum * k_scale / total) -----------------
+    // CTA src holds the subtree of leaves [src lpc, src lpc + lpc) of the
+    // group's list: absent if they lie past its longest count.
     if (ok) {
         const int units = WPO * G * 128;  // 16-byte units of one CTA's partial of my columns
         const float4* in4 = reinterpret_cast<const float4*>(smem);
+        const int nl = mma_leaves(nmax);
         for (int u = tid; u < units; u += kMmaThreads) {
             const int ln = u & 31, e = (u >> 5) & 3, t = (u >> 7) % G, wl = (u >> 7) / G;
             const int hh = (ln >> 2) + 8 * (e >> 1);
             const int h = 16 * t + hh;
             const int c = 32 * wl + 8 * (ln & 3) + 4 * (e & 1);
-            float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
-            float total = 0.f;
+            PairSum<4, 4> ps;
+            PairSum<4, 1> ts;
             for (int src = 0; src < S; ++src) {
+                const bool pr = src * lpc < nl;
                 const float4 v = in4[src * units + u];
-                m.x += v.x;
-                m.y += v.y;
-                m.z += v.z;
-                m.w += v.w;
-                total += sums[src * CH + h];
+                const float x[4] = {v.x, v.y, v.z, v.w};
+                ps.push(x, pr);
+                ts.push1(sums[src * CH + h], pr);
             }
+            float m[4], tt[1];
+            ps.root(m);
+            ts.root(tt);
+            const float total = tt[0];
             const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
             uint2 packed;
-            packed.x = bf16x2(m.x * inv, m.y * inv);
-            packed.y = bf16x2(m.z * inv, m.w * inv);
+            packed.x = bf16x2(m[0] * inv, m[1] * inv);
+            packed.y = bf16x2(m[2] * inv, m[3] * inv);
             uint16_t* dst = p.a.out + (static_cast<int64_t>(b0 + t) * H + head0 + hh) * kLatent +
                             split * CW + c;
             *reinterpret_cast<uint2*>(dst) = packed;
         }
         if (split == 0) {
             for (int h = tid; h < CH; h += kMmaThreads) {
-                float total = 0.f;
-                for (int src = 0; src < S; ++src) total += sums[src * CH + h];
+                PairSum<4, 1> ts;
+                for (int src = 0; src < S; ++src) ts.push1(sums[src * CH + h], src * lpc < nl);
+                float tt[1];
+                ts.root(tt);
+                const float total = tt[0];
                 p.a.lse[static_cast<int64_t>(b0 + h / kHeadsPerTile) * H + head0 + h % kHeadsPerTile] =
                     total > 0.f ? (rowmax[h] - p.log2_448 + log2f(total)) * 0.69314718055994530942f
                                 : -INFINITY;
             }
         }
     }
+    release_tmem(p.tree_tmem, tbase);
 }
 
 // Shared-memory size and (for clusters above 8) the non-portable cluster
@@ -526,6 +601,7 @@ int launch_group(const CallArgs& a, const GroupConfig& cfg, cudaStream_t stream)
     prm.log2_448 = static_cast<float>(std::log2(448.0));
     prm.budget_ns = cfg.wait_budget_ns;
     prm.inject_stall = cfg.inject_stall;
+    prm.tree_tmem = cfg.tree_tmem;
     switch (cfg.G) {
         case 2:
             return launch_g<2>(prm, cfg, a, stream);

@@ -37,7 +37,8 @@ struct CallArgs {
 
 // Shared-memory carve-up of the warp-MMA kernel (byte offsets).
 struct MmaLayout {
-    int32_t kv, q, logits, probs, idx, inbox, sums, maxima, wmax, lsum, rowmax, lamh, bars;
+    int32_t kv, q, logits, probs, idx, inbox, sums, maxima, wmax, lsum, rowmax, lamh, lstk, tslot,
+        bars;
     int32_t logit_pitch;  // floats per logits row
     int32_t prob_pitch;   // bytes per P8 row
     int32_t total;
@@ -84,6 +85,10 @@ __host__ __device__ inline MmaLayout mma_layout(int tiles, int split, int window
     o += ch * 4;
     L.lamh = o;   // [ch] per-head logit scale (split query)
     o += ch * 4;
+    L.lstk = o;   // [4 levels][ch] the sums' subtree stack (the leaf tree)
+    o += 4 * ch * 4;
+    L.tslot = o;  // the TMEM address of the partials' subtree stack
+    o += 16;
     o = align_up(o, 8);
     L.bars = o;   // window/64 gather barriers, q, maxima, inbound
     o += 8 * (window / kChunk + 3);
@@ -98,7 +103,8 @@ struct MmaConfig {
     uint64_t wait_budget_ns;
     int inject_stall;
     int spec_idx;
-    int qsplit;  // 1: bf16 query (CallArgs::q16), split into E4M3 hi + lo
+    int qsplit;     // 1: bf16 query (CallArgs::q16), split into E4M3 hi + lo
+    int tree_tmem;  // 1: some CTA holds several leaves (the subtree stack lives in TMEM)
 };
 
 // Launches the warp-MMA kernel; returns an smd_status.
@@ -135,7 +141,7 @@ constexpr int kGroupMaxKeys = 2048;  // keys per CTA (index staging)
 
 struct GroupLayout {
     int32_t ring, q, lg, probs, overlay_end;  // inbox of the partials overlays [0, overlay_end)
-    int32_t idx, sums, maxima, wmax, lsum, rowmax, nrow, flags, bars;
+    int32_t idx, sums, maxima, wmax, lsum, rowmax, nrow, flags, lstk, tslot, bars;
     int32_t total;
 };
 
@@ -172,6 +178,10 @@ __host__ __device__ inline GroupLayout group_layout(int G, int split, int nslots
     o += 16;
     L.flags = o;   // words the peers' "free" signals write
     o += 16;
+    L.lstk = o;    // [4 levels][ch] the sums' subtree stack (the leaf tree)
+    o += 4 * ch * 4;
+    L.tslot = o;   // the TMEM address of the partials' subtree stack
+    o += 16;
     o = align_up(o, 8);
     L.bars = o;    // ring slots, q, maxima, inbound, peers free
     o += 8 * (nslots + 4);
@@ -184,6 +194,7 @@ struct GroupConfig {
     GroupLayout layout;
     uint64_t wait_budget_ns;
     int inject_stall;
+    int tree_tmem;  // 1: some CTA holds several leaves (the subtree stack lives in TMEM)
 };
 
 // Launches the row-group kernel; returns an smd_status.

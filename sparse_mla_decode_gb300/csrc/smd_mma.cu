@@ -2,10 +2,15 @@
 //
 // One CTA takes (query row b, 16*T heads, its share of the row's keys); the
 // S CTAs of a thread-block cluster split the row's keys as the attn_sparse
-// page's SparseDcpDecode does (per = ceil(n / S), CTA s takes keys
-// [s*per, s*per + per) clamped to n: the kernel body's key split), and merge
-// their partials over distributed shared memory in FP32 (the page's merge
-// method: column ownership, sums in CTA order).
+// page's SparseDcpDecode does, with the split points at leaf boundaries: the
+// row's keys form leaves of 64 * ceil(n / 1024) keys (at most 16) and CTA s takes
+// an aligned block of a power of two of them (smd_tree.cuh). The partials
+// merge over distributed shared memory in FP32 (the page's merge method:
+// column ownership), by the fixed pairwise tree over the leaves, so that the
+// bits do not depend on S: each leaf's P V and sums of P are formed from
+// zero, the subtrees of the leaves a CTA has done wait in TMEM (which this
+// kernel does not otherwise use), and the owner adds the CTAs' subtrees by
+// the same tree.
 //
 // Precision follows the page's "Precision" paragraph with the P anchor at the
 // maximum over the WHOLE row: the CTAs first compute all their logits (pass
@@ -33,6 +38,7 @@
 #include "smd_internal.h"
 #include "smd_ptx.cuh"
 #include "smd_qsplit.cuh"
+#include "smd_tree.cuh"
 
 namespace smd {
 
@@ -48,6 +54,7 @@ struct MmaParams {
     uint64_t budget_ns;  // bound of every wait
     int32_t inject_stall;
     int32_t spec_idx;    // 1: load the row's whole index list with the count
+    int32_t tree_tmem;   // 1: a CTA may hold several leaves (TMEM subtree stack)
 };
 
 // Issues the gathers of one chunk of `cnt` <= 64 keys (`keys`: their pool
@@ -90,6 +97,17 @@ __device__ __forceinline__ void split_query(const MmaParams& p, int b, int head0
     }
 }
 
+// Frees the subtree stack's TMEM once every thread is past its last use
+// (warp 0 allocated it).
+__device__ __forceinline__ void release_tmem(int tree_tmem, uint32_t tbase) {
+    tc_fence_before();
+    __syncthreads();
+    if (tree_tmem && (threadIdx.x >> 5) == 0) {
+        tc_fence_after();
+        tmem_free(tbase, 512);
+    }
+}
+
 template <int T, bool QS>
 __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -116,6 +134,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     float* wmax = reinterpret_cast<float*>(smem + p.L.wmax);
     float* lsum = reinterpret_cast<float*>(smem + p.L.lsum);
     float* rowmax = reinterpret_cast<float*>(smem + p.L.rowmax);
+    float* lstk = reinterpret_cast<float*>(smem + p.L.lstk);
     const int nchunk_bars = p.window / kChunk;
     const uint32_t bars = base + p.L.bars;
     const uint32_t q_bar = bars + 8 * nchunk_bars;
@@ -158,7 +177,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         mbar_arrive_expect_tx(q_bar, p.inject_stall ? 16 : 0);
     }
     for (int h = tid; h < CH; h += kMmaThreads) lsum[h] = 0.f;
+    if (p.tree_tmem && warp == 0) tmem_alloc(base + p.L.tslot, 512);
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = p.tree_tmem ? *reinterpret_cast<volatile uint32_t*>(smem + p.L.tslot) : 0u;
     // Every CTA's barriers are armed before any peer pushes (waited below).
     if (S > 1) cluster_arrive_relaxed();
 
@@ -189,9 +212,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         }
     }
     n = max(min(n, W), 0);
-    const int per = (n + S - 1) / S;
-    const int first = min(n, split * per);
-    const int mine = min(n - first, per);
+    const int leaf = mma_leaf(n);
+    const int lpc = mma_leaves_per_cta(n, S);
+    const int first = min(n, split * lpc * leaf);
+    const int mine = min(n - first, lpc * leaf);
     if (!p.spec_idx)
         for (int i = tid; i < mine; i += kMmaThreads) idx_s[i] = row_idx[first + i];
     const int32_t* my_idx = idx_s + (p.spec_idx ? first : 0);
@@ -327,6 +351,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     // global order whatever the ring size: the last NS chunks are still
     // resident; chunk c - NS comes back (V columns only) into the slot of
     // chunk c once PV of chunk c has left it.
+    //
+    // Leaves: slot l of this CTA is chunks [l cpl, l cpl + cpl) of its keys,
+    // walked downwards (the mirror of the tree, same bits). A leaf's P V is
+    // summed from zero in acc and its sums of P in lsum; at its end it is
+    // pushed: the stored subtrees along the binary counter's carry are added
+    // (TMEM levels for acc, lstk for the sums), and the result is stored at the
+    // first free level unless it is this CTA's root, which stays in acc / lsum.
+    const int cpl = leaf / kChunk;
+    int tcnt = nch > 0 ? lpc - 1 - (nch - 1) / cpl : lpc;  // leaves pushed: the absent slots
+    uint32_t tpres = 0u;  // bit d: stack level d holds a subtree
+    const uint32_t tcol = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + 128u * (warp >> 2);
     for (int c = nch - 1; c >= 0; --c) {
         const int s = c % NS;
         const int cnt = min(kChunk, mine - c * kChunk);
@@ -379,6 +414,39 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
                 for (int j = 0; j < 4; ++j) mma_e4m3(acc[t][j], pa, vb[ks][0][j], vb[ks][1][j]);
             }
         }
+        if (c % cpl == 0) {  // leaf c / cpl is complete (uniform)
+            int d = 0;
+            while ((tcnt >> d) & 1) {
+                if ((tpres >> d) & 1u) {
+                    stash_add<T>(tcol + 16u * T * d, acc);
+                    if (lane == 0)
+#pragma unroll
+                        for (int i = 0; i < T; ++i) {
+                            const int h = warp + 16 * i;
+                            lsum[h] = lstk[d * CH + h] + lsum[h];
+                        }
+                }
+                ++d;
+            }
+            tpres &= ~((1u << d) - 1u);
+            if (++tcnt < lpc) {  // not the root: keep the subtree, start the next leaf at zero
+                stash_store<T>(tcol + 16u * T * d, acc);
+                if (lane == 0)
+#pragma unroll
+                    for (int i = 0; i < T; ++i) {
+                        const int h = warp + 16 * i;
+                        lstk[d * CH + h] = lsum[h];
+                        lsum[h] = 0.f;
+                    }
+                tpres |= 1u << d;
+#pragma unroll
+                for (int t = 0; t < T; ++t)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[t][j][e] = 0.f;
+            }
+        }
         // The slot and P are free; a failed CTA issues no more copies.
         if (!__syncthreads_and(ok)) break;
         if (c - NS >= 0)
@@ -395,24 +463,25 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
                 for (int e = 0; e < 4; ++e) {
                     const int h = 16 * t + g + 8 * (e >> 1);
                     const int col = 32 * warp + 8 * qd + 4 * (e & 1);
-                    const float total = 0.f + lsum[h];
+                    const float total = lsum[h];
                     const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
                     uint2 packed;
-                    packed.x = bf16x2((0.f + acc[t][0][e]) * inv, (0.f + acc[t][1][e]) * inv);
-                    packed.y = bf16x2((0.f + acc[t][2][e]) * inv, (0.f + acc[t][3][e]) * inv);
+                    packed.x = bf16x2(acc[t][0][e] * inv, acc[t][1][e] * inv);
+                    packed.y = bf16x2(acc[t][2][e] * inv, acc[t][3][e] * inv);
                     uint16_t* dst =
                         p.a.out + (static_cast<int64_t>(b) * p.a.H + head0 + h) * kLatent + col;
                     *reinterpret_cast<uint2*>(dst) = packed;
                 }
             }
             for (int h = tid; h < CH; h += kMmaThreads) {
-                const float total = 0.f + lsum[h];
+                const float total = lsum[h];
                 p.a.lse[static_cast<int64_t>(b) * p.a.H + head0 + h] =
                     total > 0.f ? (rowmax[h] - p.log2_448 + log2f(total)) * 0.69314718055994530942f
                                 : -INFINITY;
             }
         }
         cp_async_wait_all();  // after a failed wait, no copy may land once the CTA is gone
+        release_tmem(p.tree_tmem, tbase);
         return;
     }
 
@@ -450,36 +519,45 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     mbar_wait(in_bar, 0, ok, status, p.budget_ns, /*always=*/true);
     __syncthreads();  // this CTA's own partial (plain stores)
 
-    // ---- merge in CTA order; BF16(sum * k_scale / total) ---------------------
+    // ---- merge by the leaf tree; BF16(sum * k_scale / total) -----------------
+    // CTA src holds the subtree of leaves [src lpc, src lpc + lpc): absent if
+    // they lie past the row's count.
     if (ok) {
         const int units = WPO * T * 128;  // 16-byte units of one CTA's partial of my columns
         const float4* in4 = reinterpret_cast<const float4*>(inbox);
+        const int nl = mma_leaves(n);
         for (int u = tid; u < units; u += kMmaThreads) {
             const int ln = u & 31, e = (u >> 5) & 3, t = (u >> 7) % T, wl = (u >> 7) / T;
             const int h = 16 * t + (ln >> 2) + 8 * (e >> 1);
             const int c = 32 * wl + 8 * (ln & 3) + 4 * (e & 1);
-            float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
-            float total = 0.f;
+            PairSum<4, 4> ps;
+            PairSum<4, 1> ts;
             for (int src = 0; src < S; ++src) {
+                const bool pr = src * lpc < nl;
                 const float4 v = in4[src * units + u];
-                m.x += v.x;
-                m.y += v.y;
-                m.z += v.z;
-                m.w += v.w;
-                total += sums[src * CH + h];
+                const float x[4] = {v.x, v.y, v.z, v.w};
+                ps.push(x, pr);
+                ts.push1(sums[src * CH + h], pr);
             }
+            float m[4], tt[1];
+            ps.root(m);
+            ts.root(tt);
+            const float total = tt[0];
             const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
             uint2 packed;
-            packed.x = bf16x2(m.x * inv, m.y * inv);
-            packed.y = bf16x2(m.z * inv, m.w * inv);
+            packed.x = bf16x2(m[0] * inv, m[1] * inv);
+            packed.y = bf16x2(m[2] * inv, m[3] * inv);
             uint16_t* dst = p.a.out + (static_cast<int64_t>(b) * p.a.H + head0 + h) * kLatent +
                             split * CW + c;
             *reinterpret_cast<uint2*>(dst) = packed;
         }
         if (split == 0) {
             for (int h = tid; h < CH; h += kMmaThreads) {
-                float total = 0.f;
-                for (int src = 0; src < S; ++src) total += sums[src * CH + h];
+                PairSum<4, 1> ts;
+                for (int src = 0; src < S; ++src) ts.push1(sums[src * CH + h], src * lpc < nl);
+                float tt[1];
+                ts.root(tt);
+                const float total = tt[0];
                 const float lse2 =
                     total > 0.f ? rowmax[h] - p.log2_448 + log2f(total) : neg_inf;
                 p.a.lse[static_cast<int64_t>(b) * p.a.H + head0 + h] =
@@ -488,6 +566,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         }
     }
     cp_async_wait_all();
+    release_tmem(p.tree_tmem, tbase);
 }
 
 // Function attributes are set once per device and kernel (and again only when
@@ -558,6 +637,7 @@ int launch_mma(const CallArgs& a, const MmaConfig& cfg, cudaStream_t stream) {
     prm.budget_ns = cfg.wait_budget_ns;
     prm.inject_stall = cfg.inject_stall;
     prm.spec_idx = cfg.spec_idx;
+    prm.tree_tmem = cfg.tree_tmem;
     if (cfg.qsplit && a.q16 == nullptr) return SMD_ERR_NULL;
     switch (cfg.tiles * 2 + (cfg.qsplit ? 1 : 0)) {
         case 2:

@@ -1,10 +1,12 @@
 // Sparse MLA decode on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
-// One CTA takes (query row b, a group of 128 heads, its share of the row's
-// keys: at most 512); the S CTAs of a cluster (S <= 4) split the row's keys
-// as the attn_sparse page's SparseDcpDecode does (per = ceil(n / S), CTA s
-// takes [s*per, s*per + per) clamped to n), and merge their FP32 partials in
-// CTA order (the page's merge method). The P anchor is the maximum over the
+// One CTA takes (query row b, a group of 128 heads, one 512-key leaf of the
+// row's keys); the S CTAs of a cluster (S <= 4) split the row's keys as the
+// attn_sparse page's SparseDcpDecode does, with the split points fixed at
+// multiples of 512 (CTA s takes keys [512 s, 512 s + 512) clamped to n), and
+// merge their FP32 partials by the fixed pairwise tree of smd_tree.cuh (the
+// page's merge method, column ownership and FP32 sums, in an order that does
+// not depend on S). The P anchor is the maximum over the
 // whole row: every CTA first computes the logits of all its keys, the CTAs
 // exchange their maxima, and only then is P formed (P = 2^(s - m + log2 448),
 // E4M3, FP32 sums of the unquantized P) and multiplied with V.
@@ -43,6 +45,7 @@
 #include "smd_internal.h"
 #include "smd_ptx.cuh"
 #include "smd_tc_common.cuh"
+#include "smd_tree.cuh"
 
 namespace smd {
 namespace {
@@ -112,17 +115,21 @@ struct Range {
     int n, first, mine, nch;
 };
 
+// CTA `split` holds leaf `split`: keys [512 split, 512 split + 512) of the row
+// (the plan's S * 512 >= W).
 __device__ __forceinline__ Range key_range(const TcParams& p, int b, int split) {
     Range r;
     int n = p.a.counts[b];
     n = max(min(n, p.a.W), 0);
-    const int per = (n + p.split - 1) / p.split;
     r.n = n;
-    r.first = min(n, split * per);
-    r.mine = min(n - r.first, per);
+    r.first = min(n, split * kTcLeaf);
+    r.mine = min(n - r.first, kTcLeaf);
     r.nch = (r.mine + kTcChunk - 1) / kTcChunk;
     return r;
 }
+
+// Leaf `rank` of a row of n keys holds at least one key.
+__device__ __forceinline__ bool leaf_present(int rank, int n) { return rank * kTcLeaf < n; }
 
 // The shared-memory addresses and barriers of the chunk pipeline.
 __device__ __forceinline__ tcc::Pipe pipe_of(const TcParams& p, uint32_t base, uint32_t bars,
@@ -300,6 +307,26 @@ __device__ __forceinline__ void flush_tile(const uint8_t* stage, int row_bytes, 
     }
 }
 
+// a (+) b of 32 floats, either operand possibly absent.
+__device__ __forceinline__ void tree_add32(float (&a)[32], bool pa, const float (&b)[32], bool pb) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) a[j] = tree_add(a[j], pa, b[j], pb);
+}
+
+// The four 8-float4 pieces of a partial in an inbox or workspace block (unit
+// i of 32 columns at src[i * stride]).
+template <typename LD>
+__device__ __forceinline__ void load32(LD ld, float (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 x = ld(i);
+        v[4 * i] = x.x;
+        v[4 * i + 1] = x.y;
+        v[4 * i + 2] = x.z;
+        v[4 * i + 3] = x.w;
+    }
+}
+
 // DSMEM exchange and merge of one CTA's columns; NP = 32-column pieces per
 // thread (2 for a 2-way split, 1 for a 4-way split). This CTA holds one inbox
 // per partner: inbox k - 1 receives partner split ^ k's partial of this CTA's
@@ -307,12 +334,13 @@ __device__ __forceinline__ void flush_tile(const uint8_t* stage, int row_bytes, 
 // column group cg at (cg * GW / 4 + u) * 128 + h, so that one warp-wide
 // 16-byte store of 32 heads covers 512 contiguous bytes). The pushes go out
 // back to back, partner split ^ 1 first, each once that partner's tiles are
-// dead; the merge adds this CTA's partial, then split ^ 1, ^ 2, ^ 3.
+// dead. The merge is the pairwise tree in the order own, split ^ 1, split ^ 2,
+// split ^ 3: (own + x1) as soon as round 1 has landed, then + (x2 + x3).
 template <int NP>
 __device__ __forceinline__ void exchange_dsmem(const TcParams& p, uint8_t* smem, uint32_t bars,
                                                uint32_t lane_base, uint16_t* oblock, float* lse,
-                                               float m, int h, int cg, int split, bool have_o,
-                                               bool& ok) {
+                                               float m, int h, int cg, int split, int n,
+                                               bool have_o, bool& ok) {
     const int S = p.split;
     const int CW = kLatent / S, GW = CW / 4;
     const int units = 128 * CW / 4;  // 16-byte units per inbox
@@ -337,40 +365,59 @@ __device__ __forceinline__ void exchange_dsmem(const TcParams& p, uint8_t* smem,
                             make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]), rfull);
         }
     }
+    const bool p0 = leaf_present(split, n), p1 = leaf_present(split ^ 1, n);
     float acc[NP][32];
 #pragma unroll
     for (int q = 0; q < NP; ++q) {
-        float own[32];
         if (have_o)
-            tmem_ld32(lane_base + split * CW + cg * GW + 32 * q, own);
+            tmem_ld32(lane_base + split * CW + cg * GW + 32 * q, acc[q]);
         else
-            zero32(own);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) acc[q][j] = 0.f + own[j];
+            zero32(acc[q]);
     }
-    for (int k = 1; k < S; ++k) {
-        mbar_wait(bars + 8 * (kBarRoundFull + k - 1), 0, ok, status, p.budget_ns, /*always=*/true);
+    auto inbox_ld = [&](int k, int q) {
+        const float4* src = inbox + (k - 1) * units + (cg * (GW / 4) + 8 * q) * 128 + h;
+        return [src](int i) { return src[i * 128]; };
+    };
+    mbar_wait(bars + 8 * kBarRoundFull, 0, ok, status, p.budget_ns, /*always=*/true);
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+        float x[32];
+        load32(inbox_ld(1, q), x);
+        tree_add32(acc[q], p0, x, p1);
+    }
+    bool pa = p0 || p1;
+    if (S == 4) {
+        const bool p2 = leaf_present(split ^ 2, n), p3 = leaf_present(split ^ 3, n);
+        mbar_wait(bars + 8 * (kBarRoundFull + 1), 0, ok, status, p.budget_ns, /*always=*/true);
+        mbar_wait(bars + 8 * (kBarRoundFull + 2), 0, ok, status, p.budget_ns, /*always=*/true);
 #pragma unroll
         for (int q = 0; q < NP; ++q) {
-            const float4* src = inbox + (k - 1) * units + (cg * (GW / 4) + 8 * q) * 128 + h;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 x = src[i * 128];
-                acc[q][4 * i] += x.x;
-                acc[q][4 * i + 1] += x.y;
-                acc[q][4 * i + 2] += x.z;
-                acc[q][4 * i + 3] += x.w;
-            }
+            float x[32], y[32];
+            load32(inbox_ld(2, q), x);
+            load32(inbox_ld(3, q), y);
+            tree_add32(x, p2, y, p3);
+            tree_add32(acc[q], pa, x, p2 || p3);
         }
+        pa = pa || p2 || p3;
     }
     mbar_wait(bars + 8 * kBarIn, 0, ok, status, p.budget_ns, /*always=*/true);
     ok = __syncthreads_and(ok) != 0;  // also: every inbox is consumed
     if (!ok) return;
-    float total = 0.f + sums[split * 128 + h];
-    for (int k = 1; k < S; ++k) total += sums[(split ^ k) * 128 + h];
+    // The sums by the same tree.
+    float total = tree_add(sums[split * 128 + h], p0, sums[(split ^ 1) * 128 + h], p1);
+    if (S == 4) {
+        const bool p2 = leaf_present(split ^ 2, n), p3 = leaf_present(split ^ 3, n);
+        total = tree_add(total, p0 || p1,
+                         tree_add(sums[(split ^ 2) * 128 + h], p2, sums[(split ^ 3) * 128 + h], p3),
+                         p2 || p3);
+    }
+    if (!pa) total = 0.f;
     const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
 #pragma unroll
-    for (int q = 0; q < NP; ++q) stage_bf16x32(smem, CW * 2, h, cg * GW + 32 * q, acc[q], inv);
+    for (int q = 0; q < NP; ++q) {
+        if (!pa) zero32(acc[q]);
+        stage_bf16x32(smem, CW * 2, h, cg * GW + 32 * q, acc[q], inv);
+    }
     if (split == 0 && cg == 0 && h < p.lanes)
         *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f : -INFINITY;
     __syncthreads();
@@ -402,7 +449,7 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
 
     if (S == 1) {
         if (ok) {  // uniform: set by the barrier before the finish
-            const float total = 0.f + l;
+            const float total = l;
             const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
             for (int q = 0; q < kLatent / 128; ++q) {
                 const int col = cg * (kLatent / 4) + 32 * q;
@@ -411,8 +458,6 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
                     tmem_ld32(lane_base + col, v);
                 else
                     zero32(v);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0.f + v[j];
                 stage_bf16x32(smem, kLatent * 2, h, col, v, inv);
             }
             if (cg == 0 && h < p.lanes)
@@ -429,7 +474,7 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
     if (p.ws != nullptr) {
         // ---- L2 exchange: every CTA writes its partials of the other owners'
         // columns into its SM's workspace slot; each owner reads the peers'
-        // slots (bypassing L1) and merges in CTA order. A slot stays valid
+        // slots (bypassing L1) and merges them by the tree. A slot stays valid
         // until the peers have read it (the readers-done handshake), so the
         // next CTA on the same SM cannot overwrite it early.
         const uint32_t* smids = reinterpret_cast<const uint32_t*>(smem + kOffSmid);
@@ -467,38 +512,46 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
         mbar_wait(bars + 8 * kBarIn, 0, ok, status, p.budget_ns, /*always=*/true);
         const bool go = __syncthreads_and(ok && slots_ok) != 0;
         if (go) {
-            // Merge order (both exchange paths): this CTA's partial, then its
-            // partners split ^ 1, split ^ 2, split ^ 3.
-            float total = 0.f + sums[split * 128 + h];
-            for (int k = 1; k < S; ++k) total += sums[(split ^ k) * 128 + h];
+            // The pairwise tree in the order own, split ^ 1, split ^ 2, split ^ 3
+            // (the DSMEM path's sums, bit for bit).
+            auto present = [&](int k) { return leaf_present(split ^ k, r.n); };
+            auto ws_ld = [&](int k, int q) {
+                const int rk = split ^ k;
+                const int blk = (rk + S - split - 1) % S;  // rk's block for this owner
+                const float* src = p.ws + static_cast<size_t>(smids[rk]) * kTcWsSlotFloats +
+                                   static_cast<size_t>(blk) * 128 * CW +
+                                   ((cg * (GW / 4) + 8 * q) * 128 + h) * 4;
+                return [src](int i) { return ld_global_cg(src + i * 128 * 4); };
+            };
+            float total = tree_add(sums[split * 128 + h], present(0), sums[(split ^ 1) * 128 + h],
+                                   present(1));
+            bool pa = present(0) || present(1);
+            if (S == 4) {
+                total = tree_add(total, pa,
+                                 tree_add(sums[(split ^ 2) * 128 + h], present(2),
+                                          sums[(split ^ 3) * 128 + h], present(3)),
+                                 present(2) || present(3));
+                pa = pa || present(2) || present(3);
+            }
+            if (!pa) total = 0.f;
             const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
             for (int q = 0; q < GW / 32; ++q) {
                 const int col = split * CW + cg * GW + 32 * q;
-                float own[32], acc[32];
+                float acc[32], x[32];
                 if (have_o)
-                    tmem_ld32(lane_base + col, own);
+                    tmem_ld32(lane_base + col, acc);
                 else
-                    zero32(own);
-                zero32(acc);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) acc[j] += own[j];
-                for (int k = 1; k < S; ++k) {
-                    const int rk = split ^ k;
-                    {
-                        const int blk = (rk + S - split - 1) % S;  // rk's block for this owner
-                        const float* src = p.ws + static_cast<size_t>(smids[rk]) * kTcWsSlotFloats +
-                                           static_cast<size_t>(blk) * 128 * CW +
-                                           ((cg * (GW / 4) + 8 * q) * 128 + h) * 4;
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float4 x = ld_global_cg(src + i * 128 * 4);
-                            acc[4 * i] += x.x;
-                            acc[4 * i + 1] += x.y;
-                            acc[4 * i + 2] += x.z;
-                            acc[4 * i + 3] += x.w;
-                        }
-                    }
+                    zero32(acc);
+                load32(ws_ld(1, q), x);
+                tree_add32(acc, present(0), x, present(1));
+                if (S == 4) {
+                    float y[32];
+                    load32(ws_ld(2, q), x);
+                    load32(ws_ld(3, q), y);
+                    tree_add32(x, present(2), y, present(3));
+                    tree_add32(acc, present(0) || present(1), x, present(2) || present(3));
                 }
+                if (!pa) zero32(acc);
                 stage_bf16x32(smem, CW * 2, h, col - split * CW, acc, inv);
             }
             if (split == 0 && cg == 0 && h < p.lanes)
@@ -533,9 +586,11 @@ __device__ __forceinline__ void finish(const TcParams& p, uint8_t* smem, uint32_
                          mapa(bars + 8 * (kBarRoundFree + k - 1), pr));
         }
     if (S == 2)
-        exchange_dsmem<2>(p, smem, bars, lane_base, oblock + split * CW, lse, m, h, cg, split, have_o, ok);
+        exchange_dsmem<2>(p, smem, bars, lane_base, oblock + split * CW, lse, m, h, cg, split, r.n,
+                          have_o, ok);
     else
-        exchange_dsmem<1>(p, smem, bars, lane_base, oblock + split * CW, lse, m, h, cg, split, have_o, ok);
+        exchange_dsmem<1>(p, smem, bars, lane_base, oblock + split * CW, lse, m, h, cg, split, r.n,
+                          have_o, ok);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)

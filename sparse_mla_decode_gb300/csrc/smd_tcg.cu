@@ -8,7 +8,9 @@
 // are never stored - and each cache row is gathered once for the whole group.
 // The S CTAs of a cluster (S <= 16, so rows of up to 16 x 512 keys) split the
 // group's longest list as the attn_sparse page's SparseDcpDecode splits a
-// row's keys; lane l masks the keys past its own row's count.
+// row's keys, at the 512-key leaf boundaries of smd_tree.cuh (CTA s takes
+// keys [512 s, 512 s + 512)); lane l masks the keys past its own row's count,
+// so each row sees exactly its own leaves.
 //
 // Per CTA the pipeline is the tcgen05 kernel's (TMA tile::gather4 of 128-key
 // chunks into a two-slot ring, S = Q K^T into TMEM, the row maximum, P in E4M3
@@ -18,8 +20,8 @@
 // shared memory and reads its peers' after a cluster barrier, and after a
 // second cluster barrier (every peer's tiles are then dead) each CTA pushes
 // its FP32 partials of the other owners' columns, with its sums, into their
-// inboxes over the dead tiles; the merge adds this CTA's partial, then
-// split ^ 1, split ^ 2, ... in that order.
+// inboxes over the dead tiles; the merge is the pairwise tree in the order
+// own, split ^ 1, split ^ 2, ..., a CTA past a lane's own count absent for it.
 //
 // Contract (checked): every row of a group reads a prefix of the list of the
 // group's row with the largest clamped count (the first such); a CTA that
@@ -34,6 +36,7 @@
 #include "smd_internal.h"
 #include "smd_ptx.cuh"
 #include "smd_tc_common.cuh"
+#include "smd_tree.cuh"
 
 namespace smd {
 namespace {
@@ -269,7 +272,7 @@ __device__ __forceinline__ void finish(const TcgParams& p, uint8_t* smem, uint32
 
     if (S == 1) {
         if (ok) {  // uniform: set by the barrier before the finish
-            const float total = 0.f + l;
+            const float total = l;
             const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
             if (real) {
                 for (int q = 0; q < GW / 8; ++q) {
@@ -280,8 +283,6 @@ __device__ __forceinline__ void finish(const TcgParams& p, uint8_t* smem, uint32
                     else
 #pragma unroll
                         for (int i = 0; i < 8; ++i) v[i] = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) v[i] = 0.f + v[i];
                     stage8(smem, CW * 2, mask, h, col, v, inv);
                 }
                 if (cg == 0)
@@ -323,32 +324,49 @@ __device__ __forceinline__ void finish(const TcgParams& p, uint8_t* smem, uint32
     if (!ok) return;
     uint8_t* stage = smem + (S - 1) * ib;  // after the inboxes
     if (real) {
-        float total = 0.f + l;
-        for (int kk = 1; kk < S; ++kk)
-            total += *reinterpret_cast<const float*>(smem + (kk - 1) * ib + L * CW * 4 + h * 4);
+        // The pairwise tree in the order own, split ^ 1, split ^ 2, ...; CTA
+        // src is absent for lane h when its leaf lies past h's own count.
+        const int n_lane = reinterpret_cast<const int32_t*>(smem + kOffNrow)[h / p.a.H];
+        auto present = [&](int kk) { return (split ^ kk) * kTcLeaf < n_lane; };
+        float total;
+        {
+            PairSum<4, 1> ts;
+            for (int kk = 0; kk < S; ++kk)
+                ts.push1(kk == 0 ? l
+                                 : *reinterpret_cast<const float*>(smem + (kk - 1) * ib + L * CW * 4 + h * 4),
+                         present(kk));
+            float r[1];
+            ts.root(r);
+            total = r[0];
+        }
         const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
         for (int q = 0; q < GW / 8; ++q) {
-            float acc[8];
-            if (have_o)
-                tmem_ld8(lane_base + split * CW + cg * GW + 8 * q, acc);
-            else
-#pragma unroll
-                for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.f + acc[i];
             const int u = cg * (GW / 4) + 2 * q;
-            for (int kk = 1; kk < S; ++kk) {
-                const float4* src = reinterpret_cast<const float4*>(smem + (kk - 1) * ib);
-                const float4 x = src[u * L + h], y = src[(u + 1) * L + h];
-                acc[0] += x.x;
-                acc[1] += x.y;
-                acc[2] += x.z;
-                acc[3] += x.w;
-                acc[4] += y.x;
-                acc[5] += y.y;
-                acc[6] += y.z;
-                acc[7] += y.w;
+            PairSum<4, 8> ps;
+            for (int kk = 0; kk < S; ++kk) {
+                float x[8];
+                if (kk == 0) {
+                    if (have_o)
+                        tmem_ld8(lane_base + split * CW + cg * GW + 8 * q, x);
+                    else
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) x[i] = 0.f;
+                } else {
+                    const float4* src = reinterpret_cast<const float4*>(smem + (kk - 1) * ib);
+                    const float4 a = src[u * L + h], b = src[(u + 1) * L + h];
+                    x[0] = a.x;
+                    x[1] = a.y;
+                    x[2] = a.z;
+                    x[3] = a.w;
+                    x[4] = b.x;
+                    x[5] = b.y;
+                    x[6] = b.z;
+                    x[7] = b.w;
+                }
+                ps.push(x, present(kk));
             }
+            float acc[8];
+            ps.root(acc);
             stage8(stage, CW * 2, mask, h, cg * GW + 8 * q, acc, inv);
         }
         if (split == 0 && cg == 0)
@@ -414,9 +432,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ref = r;
         }
     Keys k;
-    const int per = (nmax + S - 1) / S;
-    k.first = min(nmax, split * per);
-    k.mine = min(nmax - k.first, per);
+    k.first = min(nmax, split * kTcLeaf);
+    k.mine = min(nmax - k.first, kTcLeaf);
     k.nch = (k.mine + kTcChunk - 1) / kTcChunk;
 
     const tcc::Pipe pp = pipe_of(p, base, bars, smem);

@@ -6,9 +6,10 @@
 //
 // Work items. A unit is (query row b, group of 128 heads); a unit whose row
 // holds n > 0 keys (n = clamp(counts[b], 0, W)) becomes s = ceil(n / 512)
-// items of at most 512 keys each (piece j takes [j * per, j * per + per)
-// clamped to n, per = ceil(n / s); the attn_sparse page's count-balanced
-// partition). Every CTA reads the counts and lays the items out the same way:
+// items of at most 512 keys each: piece j takes the 512-key leaf
+// [512 j, 512 j + 512) clamped to n, the split points of the cluster kernel,
+// so that both evaluate the same summation tree (smd_tree.cuh). Every CTA
+// reads the counts and lays the items out the same way:
 // a prefix sum over units numbers them, and item i runs on CTA i % grid in
 // round i / grid. The grid is launched cooperatively (every CTA resident), so
 // a CTA that waits for a peer item of its unit always waits for a CTA that is
@@ -23,8 +24,9 @@
 //   2. after PV it writes its FP32 partials of the other items' columns
 //      (owner j of s owns columns [16 floor(32 j / s), 16 floor(32 (j+1) / s)))
 //      and its sums, and raises one flag per owner;
-//   3. each owner waits for its flags, merges its own partial first and then
-//      the others in item order, and writes BF16 out (and LSE, owner 0).
+//   3. each owner waits for its flags, merges the pieces by the pairwise tree
+//      (its own partial first, then pieces j ^ 1, j ^ 2, ...), and writes BF16
+//      out (and LSE, owner 0).
 // A flag holds the call's 64-bit token, so stale words from earlier calls
 // never pass; the reader of a flag zeroes it once it is consumed.
 // Every wait (copies, tensor core, peer flags) is bounded.
@@ -40,6 +42,7 @@
 #include "smd_ptx.cuh"
 #include "smd_qsplit.cuh"
 #include "smd_tc_common.cuh"
+#include "smd_tree.cuh"
 
 namespace smd {
 namespace {
@@ -256,9 +259,8 @@ __device__ __forceinline__ Item item_of(const TcsParams& p, const uint8_t* smem,
     it.j = i - it.item0;
     const int n = unit_count(p, lo, &it.ref);
     it.n = n;
-    const int per = (n + it.s - 1) / it.s;
-    it.first = min(n, it.j * per);
-    it.mine = min(n - it.first, per);
+    it.first = min(n, it.j * kTcLeaf);
+    it.mine = min(n - it.first, kTcLeaf);
     it.nch = (it.mine + kTcChunk - 1) / kTcChunk;
     return it;
 }
@@ -471,10 +473,47 @@ __device__ __forceinline__ void flush(const uint8_t* stage, int row_bytes, int m
 // largest power of two (at most 8) that divides chunks, minus one.
 __device__ __forceinline__ int stage_mask(int chunks) { return min(chunks & -chunks, 8) - 1; }
 
-// Partner k (1 <= k < s) of piece j in the merge order: j ^ k when s is a
-// power of two (the order of the cluster kernels), else (j + k) % s.
-__device__ __forceinline__ int partner(int j, int k, int s) {
-    return (s & (s - 1)) == 0 ? (j ^ k) : (j + k) % s;
+// One owner's 16 columns at `col` of a unit of s pieces: the pairwise tree
+// over positions k = 0 .. P - 1 (piece j ^ k; P = s rounded up to a power of
+// two = 2^D, absent pieces past s), NV columns at a time. Lane h's own row
+// holds n_lane keys: pieces past them are absent for it (row groups).
+template <int D, int NV>
+__device__ __forceinline__ void merge_cols(const float* part, int64_t item0, int j, int s,
+                                           int n_lane, int h, int col, const float (&own)[16],
+                                           float (&out)[16]) {
+    constexpr int64_t kPartFloats = static_cast<int64_t>(kTcHeads) * kLatent;
+    const int P = 1 << D;
+#pragma unroll
+    for (int c0 = 0; c0 < 16; c0 += NV) {
+        PairSum<D, NV> ps;
+        for (int k = 0; k < P; ++k) {
+            const int src = j ^ k;
+            const bool pres = src < s && src * kTcLeaf < n_lane;
+            float x[NV];
+            if (k == 0) {
+#pragma unroll
+                for (int e = 0; e < NV; ++e) x[e] = own[c0 + e];
+            } else if (pres) {
+                const float* p4 = part + (item0 + src) * kPartFloats + (((col + c0) >> 2) * kTcHeads + h) * 4;
+#pragma unroll
+                for (int i = 0; i < NV / 4; ++i) {
+                    const float4 v = ld_cg_v4(p4 + i * kTcHeads * 4);
+                    x[4 * i] = v.x;
+                    x[4 * i + 1] = v.y;
+                    x[4 * i + 2] = v.z;
+                    x[4 * i + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < NV; ++e) x[e] = 0.f;
+            }
+            ps.push(x, pres);
+        }
+        float r[NV];
+        ps.root(r);
+#pragma unroll
+        for (int e = 0; e < NV; ++e) out[c0 + e] = r[e];
+    }
 }
 
 // ---- all 16 warps: exchange, merge, output ---------------------------------------
@@ -497,7 +536,7 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
 
     if (it.s == 1) {
         if (ok) {  // uniform: set by the barrier before the finish
-            const float total = 0.f + l;
+            const float total = l;
             const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
             for (int q = 0; q < 8; ++q) {
                 const int col = cg * 128 + 16 * q;
@@ -508,8 +547,6 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] = 0.f;
                 }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = 0.f + v[i];
                 stage16(stage, kLatent * 2, 7, h, col, v, inv);
             }
             if (cg == 0 && h < p.lanes)
@@ -571,36 +608,46 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
     if (t == 0) fmax[item] = 0ull;
     if (!ok) return;
 
-    // 3. Merge: this item's partial, then its partners in the fixed order.
-    float total = 0.f + l;
-    for (int k = 1; k < s; ++k)
-        total += ld_cg_f32(sums + static_cast<int64_t>(it.item0 + partner(j, k, s)) * kTcHeads + h);
+    // 3. Merge: the pairwise tree over the unit's pieces in the order j ^ k.
+    const int n_lane = lane_count(p, it.b0, h);
+    const int D = log2_exact(s);
+    float total;
+    {
+        PairSum<5, 1> ts;
+        for (int k = 0; k < (1 << D); ++k) {
+            const int src = j ^ k;
+            const bool pres = src < s && src * kTcLeaf < n_lane;
+            const float v = k == 0 ? l
+                            : pres ? ld_cg_f32(sums + static_cast<int64_t>(it.item0 + src) * kTcHeads + h)
+                                   : 0.f;
+            ts.push1(v, pres);
+        }
+        float r[1];
+        ts.root(r);
+        total = r[0];
+    }
     const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
     const int mask = stage_mask(CW / 8);
     for (int q = cg; 16 * q < CW; q += 4) {
         const int col = c0 + 16 * q;
-        float acc[16];
+        float own[16], acc[16];
         if (have_o) {
-            tmem_ld16(lane_base + col, acc);
+            tmem_ld16(lane_base + col, own);
         } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+            for (int i = 0; i < 16; ++i) own[i] = 0.f;
         }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.f + acc[i];
-        for (int k = 1; k < s && h < p.lanes; ++k) {
-            const float* src = part + static_cast<int64_t>(it.item0 + partner(j, k, s)) * kPartFloats +
-                               ((col >> 2) * kTcHeads + h) * 4;
-            float4 x[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) x[i] = ld_cg_v4(src + i * kTcHeads * 4);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                acc[4 * i] += x[i].x;
-                acc[4 * i + 1] += x[i].y;
-                acc[4 * i + 2] += x[i].z;
-                acc[4 * i + 3] += x[i].w;
+        if (h < p.lanes) {
+            switch (D) {
+                case 1: merge_cols<1, 16>(part, it.item0, j, s, n_lane, h, col, own, acc); break;
+                case 2: merge_cols<2, 8>(part, it.item0, j, s, n_lane, h, col, own, acc); break;
+                case 3: merge_cols<3, 4>(part, it.item0, j, s, n_lane, h, col, own, acc); break;
+                case 4: merge_cols<4, 4>(part, it.item0, j, s, n_lane, h, col, own, acc); break;
+                default: merge_cols<5, 4>(part, it.item0, j, s, n_lane, h, col, own, acc); break;
             }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.f;  // padding lanes are never stored
         }
         stage16(stage, CW * 2, mask, h, col - c0, acc, inv);
     }

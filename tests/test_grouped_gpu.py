@@ -63,8 +63,17 @@ def test_grouped_matches_the_oracle_and_the_per_row_decode(cuda, shape):
 @pytest.mark.parametrize("kern,split", [(MMA_GROUP, s) for s in (1, 2, 4, 8, 16)] +
                          [(TC_GROUP, s) for s in (4, 8, 16)])
 def test_grouped_every_split(cuda, kern, split):
+    """1100 keys are 9 leaves of 128: the warp-MMA group kernel with groups of
+    4 keeps at most 4 leaves a CTA (two TMEM stack levels of 64 floats), so
+    splits 1 and 2 are refused as a plan, not computed."""
+    from sparse_mla_decode_gb300 import binding
     case = inputs.grouped_case(41, 2, 4, 16, 1100, 12000, [1100, 1099, 700, 2, 0, 300, 301, 64])
     t = to_dev(case, cuda)
+    if kern == MMA_GROUP and split < 4:
+        with pytest.raises(binding.SmdError) as e:
+            grouped(case, cuda, 4, plan=dict(kernel=kern, split=split), tensors=t)
+        assert e.value.status == binding.SMD_ERR_PLAN
+        return
     out_o, lse_o = oracle_decode(case)
     out_g, lse_g = grouped(case, cuda, 4, plan=dict(kernel=kern, split=split), tensors=t)
     check(out_g, lse_g, out_o, lse_o, f"grouped kernel {kern} split {split}")
@@ -121,7 +130,7 @@ def test_grouped_timeout_is_reported_and_the_context_survives(cuda, kern):
     from sparse_mla_decode_gb300 import binding
     case = inputs.grouped_case(45, 2, 4, 16, 600, 4000)
     t = to_dev(case, cuda)
-    grouped(case, cuda, 4, plan=dict(kernel=kern, inject_stall=1, wait_budget_us=2000, split=2),
+    grouped(case, cuda, 4, plan=dict(kernel=kern, inject_stall=1, wait_budget_us=2000, split=4),
             tensors=t, expect_status=binding.SMD_ERR_TIMEOUT)
     out_g, lse_g = grouped(case, cuda, 4, plan=dict(kernel=kern), tensors=t)
     out_o, lse_o = oracle_decode(case)
@@ -134,7 +143,7 @@ def test_dense_as_sparse_full_size_sampled_rows(cuda):
     against the oracle."""
     case = inputs.config("dense")
     t = to_dev(case, cuda)
-    rows = [0, 1, 2, 3, 60, 61, 62, 63, 124, 125, 126, 127]
+    rows = np.concatenate([4 * r + np.arange(4) for r in range(0, 32, 4)])  # 8 requests, 32 rows
     out_o, lse_o = oracle_decode(case, rows)
     for plan in (None, dict(kernel=MMA_GROUP)):
         out_g, lse_g = grouped(case, cuda, 4, plan=plan, tensors=t)
@@ -227,6 +236,6 @@ def test_groups_longer_than_the_row_group_kernel_takes(cuda):
 def test_dense_as_sparse_on_the_spread_kernel_sampled(cuda):
     case = inputs.config("dense")
     out_g, lse_g = grouped_ws(case, cuda, 4)
-    rows = [0, 1, 2, 3, 60, 61, 62, 63, 124, 125, 126, 127]
+    rows = np.concatenate([4 * r + np.arange(4) for r in range(2, 32, 4)])  # 8 other requests
     out_o, lse_o = oracle_decode(case, rows)
     check(out_g[rows], lse_g[rows], out_o, lse_o, "dense grouped spread")
