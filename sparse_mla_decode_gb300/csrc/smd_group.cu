@@ -494,40 +494,26 @@ __global__ void __launch_bounds__(kMmaThreads, 1) group_decode_kernel(const Grou
     if (ok) {
         const int units = WPO * G * 128;  // 16-byte units of one CTA's partial of my columns
         const float4* in4 = reinterpret_cast<const float4*>(smem);
-        const int nl = mma_leaves(nmax);
+        const int np = (mma_leaves(nmax) + lpc - 1) / lpc;  // CTAs 0 .. np - 1 hold keys
         for (int u = tid; u < units; u += kMmaThreads) {
             const int ln = u & 31, e = (u >> 5) & 3, t = (u >> 7) % G, wl = (u >> 7) / G;
             const int hh = (ln >> 2) + 8 * (e >> 1);
             const int h = 16 * t + hh;
             const int c = 32 * wl + 8 * (ln & 3) + 4 * (e & 1);
-            PairSum<4, 4> ps;
-            PairSum<4, 1> ts;
-            for (int src = 0; src < S; ++src) {
-                const bool pr = src * lpc < nl;
-                const float4 v = in4[src * units + u];
-                const float x[4] = {v.x, v.y, v.z, v.w};
-                ps.push(x, pr);
-                ts.push1(sums[src * CH + h], pr);
-            }
-            float m[4], tt[1];
-            ps.root(m);
-            ts.root(tt);
-            const float total = tt[0];
+            const float4 m = tree_xor_n<float4>(S, [&](int k) { return in4[k * units + u]; }, 0, np);
+            const float total = tree_xor_n<float>(S, [&](int k) { return sums[k * CH + h]; }, 0, np);
             const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
             uint2 packed;
-            packed.x = bf16x2(m[0] * inv, m[1] * inv);
-            packed.y = bf16x2(m[2] * inv, m[3] * inv);
+            packed.x = bf16x2(m.x * inv, m.y * inv);
+            packed.y = bf16x2(m.z * inv, m.w * inv);
             uint16_t* dst = p.a.out + (static_cast<int64_t>(b0 + t) * H + head0 + hh) * kLatent +
                             split * CW + c;
             *reinterpret_cast<uint2*>(dst) = packed;
         }
         if (split == 0) {
             for (int h = tid; h < CH; h += kMmaThreads) {
-                PairSum<4, 1> ts;
-                for (int src = 0; src < S; ++src) ts.push1(sums[src * CH + h], src * lpc < nl);
-                float tt[1];
-                ts.root(tt);
-                const float total = tt[0];
+                const float total =
+                    tree_xor_n<float>(S, [&](int k) { return sums[k * CH + h]; }, 0, np);
                 p.a.lse[static_cast<int64_t>(b0 + h / kHeadsPerTile) * H + head0 + h % kHeadsPerTile] =
                     total > 0.f ? (rowmax[h] - p.log2_448 + log2f(total)) * 0.69314718055994530942f
                                 : -INFINITY;

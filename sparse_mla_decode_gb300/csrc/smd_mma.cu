@@ -99,16 +99,19 @@ __device__ __forceinline__ void split_query(const MmaParams& p, int b, int head0
 
 // Frees the subtree stack's TMEM once every thread is past its last use
 // (warp 0 allocated it).
-__device__ __forceinline__ void release_tmem(int tree_tmem, uint32_t tbase) {
+__device__ __forceinline__ void release_tmem(uint32_t tbase) {
     tc_fence_before();
     __syncthreads();
-    if (tree_tmem && (threadIdx.x >> 5) == 0) {
+    if ((threadIdx.x >> 5) == 0) {
         tc_fence_after();
         tmem_free(tbase, 512);
     }
 }
 
-template <int T, bool QS>
+// TR: some CTA of the plan holds several leaves (p.tree_tmem), so the kernel
+// keeps a subtree stack in TMEM; without it every CTA's keys form one leaf and
+// no TMEM is touched.
+template <int T, bool QS, bool TR>
 __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_entry();
@@ -177,11 +180,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         mbar_arrive_expect_tx(q_bar, p.inject_stall ? 16 : 0);
     }
     for (int h = tid; h < CH; h += kMmaThreads) lsum[h] = 0.f;
-    if (p.tree_tmem && warp == 0) tmem_alloc(base + p.L.tslot, 512);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tbase = p.tree_tmem ? *reinterpret_cast<volatile uint32_t*>(smem + p.L.tslot) : 0u;
+    uint32_t tbase = 0u;
+    if constexpr (TR) {
+        if (warp == 0) tmem_alloc(base + p.L.tslot, 512);
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        tbase = *reinterpret_cast<volatile uint32_t*>(smem + p.L.tslot);
+    } else {
+        __syncthreads();
+    }
     // Every CTA's barriers are armed before any peer pushes (waited below).
     if (S > 1) cluster_arrive_relaxed();
 
@@ -414,7 +422,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
                 for (int j = 0; j < 4; ++j) mma_e4m3(acc[t][j], pa, vb[ks][0][j], vb[ks][1][j]);
             }
         }
-        if (c % cpl == 0) {  // leaf c / cpl is complete (uniform)
+        if (TR && c % cpl == 0) {  // leaf c / cpl is complete (uniform)
             int d = 0;
             while ((tcnt >> d) & 1) {
                 if ((tpres >> d) & 1u) {
@@ -481,7 +489,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
             }
         }
         cp_async_wait_all();  // after a failed wait, no copy may land once the CTA is gone
-        release_tmem(p.tree_tmem, tbase);
+        if constexpr (TR) release_tmem(tbase);
         return;
     }
 
@@ -525,39 +533,25 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     if (ok) {
         const int units = WPO * T * 128;  // 16-byte units of one CTA's partial of my columns
         const float4* in4 = reinterpret_cast<const float4*>(inbox);
-        const int nl = mma_leaves(n);
+        const int np = (mma_leaves(n) + lpc - 1) / lpc;  // CTAs 0 .. np - 1 hold keys
         for (int u = tid; u < units; u += kMmaThreads) {
             const int ln = u & 31, e = (u >> 5) & 3, t = (u >> 7) % T, wl = (u >> 7) / T;
             const int h = 16 * t + (ln >> 2) + 8 * (e >> 1);
             const int c = 32 * wl + 8 * (ln & 3) + 4 * (e & 1);
-            PairSum<4, 4> ps;
-            PairSum<4, 1> ts;
-            for (int src = 0; src < S; ++src) {
-                const bool pr = src * lpc < nl;
-                const float4 v = in4[src * units + u];
-                const float x[4] = {v.x, v.y, v.z, v.w};
-                ps.push(x, pr);
-                ts.push1(sums[src * CH + h], pr);
-            }
-            float m[4], tt[1];
-            ps.root(m);
-            ts.root(tt);
-            const float total = tt[0];
+            const float4 m = tree_xor_n<float4>(S, [&](int k) { return in4[k * units + u]; }, 0, np);
+            const float total = tree_xor_n<float>(S, [&](int k) { return sums[k * CH + h]; }, 0, np);
             const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
             uint2 packed;
-            packed.x = bf16x2(m[0] * inv, m[1] * inv);
-            packed.y = bf16x2(m[2] * inv, m[3] * inv);
+            packed.x = bf16x2(m.x * inv, m.y * inv);
+            packed.y = bf16x2(m.z * inv, m.w * inv);
             uint16_t* dst = p.a.out + (static_cast<int64_t>(b) * p.a.H + head0 + h) * kLatent +
                             split * CW + c;
             *reinterpret_cast<uint2*>(dst) = packed;
         }
         if (split == 0) {
             for (int h = tid; h < CH; h += kMmaThreads) {
-                PairSum<4, 1> ts;
-                for (int src = 0; src < S; ++src) ts.push1(sums[src * CH + h], src * lpc < nl);
-                float tt[1];
-                ts.root(tt);
-                const float total = tt[0];
+                const float total =
+                    tree_xor_n<float>(S, [&](int k) { return sums[k * CH + h]; }, 0, np);
                 const float lse2 =
                     total > 0.f ? rowmax[h] - p.log2_448 + log2f(total) : neg_inf;
                 p.a.lse[static_cast<int64_t>(b) * p.a.H + head0 + h] =
@@ -566,18 +560,18 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         }
     }
     cp_async_wait_all();
-    release_tmem(p.tree_tmem, tbase);
+    if constexpr (TR) release_tmem(tbase);
 }
 
 // Function attributes are set once per device and kernel (and again only when
 // a launch needs more shared memory than was granted before).
-template <int T, bool QS>
+template <int T, bool QS, bool TR>
 int ensure_attributes(int smem_bytes, bool nonportable) {
     static std::atomic<int> smem_set[kMaxDevices];
     static std::atomic<int> np_set[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SMD_ERR_DEVICE;
-    auto kern = mma_decode_kernel<T, QS>;
+    auto kern = mma_decode_kernel<T, QS, TR>;
     if (smem_bytes > smem_set[dev].load()) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
             cudaSuccess)
@@ -593,10 +587,10 @@ int ensure_attributes(int smem_bytes, bool nonportable) {
     return SMD_OK;
 }
 
-template <int T, bool QS>
+template <int T, bool QS, bool TR>
 int launch_t(const MmaParams& prm, const MmaConfig& cfg, const CallArgs& a, cudaStream_t stream) {
-    auto kern = mma_decode_kernel<T, QS>;
-    const int rc = ensure_attributes<T, QS>(cfg.layout.total, cfg.split > 8);
+    auto kern = mma_decode_kernel<T, QS, TR>;
+    const int rc = ensure_attributes<T, QS, TR>(cfg.layout.total, cfg.split > 8);
     if (rc != SMD_OK) return rc;
     cudaError_t err;
     cudaLaunchConfig_t lc{};
@@ -639,15 +633,23 @@ int launch_mma(const CallArgs& a, const MmaConfig& cfg, cudaStream_t stream) {
     prm.spec_idx = cfg.spec_idx;
     prm.tree_tmem = cfg.tree_tmem;
     if (cfg.qsplit && a.q16 == nullptr) return SMD_ERR_NULL;
-    switch (cfg.tiles * 2 + (cfg.qsplit ? 1 : 0)) {
-        case 2:
-            return launch_t<1, false>(prm, cfg, a, stream);
-        case 3:
-            return launch_t<1, true>(prm, cfg, a, stream);
+    switch (cfg.tiles * 4 + (cfg.qsplit ? 2 : 0) + (cfg.tree_tmem ? 1 : 0)) {
         case 4:
-            return launch_t<2, false>(prm, cfg, a, stream);
+            return launch_t<1, false, false>(prm, cfg, a, stream);
         case 5:
-            return launch_t<2, true>(prm, cfg, a, stream);
+            return launch_t<1, false, true>(prm, cfg, a, stream);
+        case 6:
+            return launch_t<1, true, false>(prm, cfg, a, stream);
+        case 7:
+            return launch_t<1, true, true>(prm, cfg, a, stream);
+        case 8:
+            return launch_t<2, false, false>(prm, cfg, a, stream);
+        case 9:
+            return launch_t<2, false, true>(prm, cfg, a, stream);
+        case 10:
+            return launch_t<2, true, false>(prm, cfg, a, stream);
+        case 11:
+            return launch_t<2, true, true>(prm, cfg, a, stream);
         default:
             return SMD_ERR_PLAN;
     }

@@ -327,46 +327,33 @@ __device__ __forceinline__ void finish(const TcgParams& p, uint8_t* smem, uint32
         // The pairwise tree in the order own, split ^ 1, split ^ 2, ...; CTA
         // src is absent for lane h when its leaf lies past h's own count.
         const int n_lane = reinterpret_cast<const int32_t*>(smem + kOffNrow)[h / p.a.H];
-        auto present = [&](int kk) { return (split ^ kk) * kTcLeaf < n_lane; };
-        float total;
-        {
-            PairSum<4, 1> ts;
-            for (int kk = 0; kk < S; ++kk)
-                ts.push1(kk == 0 ? l
-                                 : *reinterpret_cast<const float*>(smem + (kk - 1) * ib + L * CW * 4 + h * 4),
-                         present(kk));
-            float r[1];
-            ts.root(r);
-            total = r[0];
-        }
+        const int np = (n_lane + kTcLeaf - 1) / kTcLeaf;  // CTAs 0 .. np - 1 hold keys of h's row
+        const float total = tree_xor_n<float>(S, [&](int kk) {
+            return kk == 0 ? l : *reinterpret_cast<const float*>(smem + (kk - 1) * ib + L * CW * 4 + h * 4);
+        }, split, np);
         const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
         for (int q = 0; q < GW / 8; ++q) {
             const int u = cg * (GW / 4) + 2 * q;
-            PairSum<4, 8> ps;
-            for (int kk = 0; kk < S; ++kk) {
-                float x[8];
-                if (kk == 0) {
-                    if (have_o)
-                        tmem_ld8(lane_base + split * CW + cg * GW + 8 * q, x);
-                    else
+            float own[8];
+            if (have_o)
+                tmem_ld8(lane_base + split * CW + cg * GW + 8 * q, own);
+            else
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) x[i] = 0.f;
-                } else {
-                    const float4* src = reinterpret_cast<const float4*>(smem + (kk - 1) * ib);
-                    const float4 a = src[u * L + h], b = src[(u + 1) * L + h];
-                    x[0] = a.x;
-                    x[1] = a.y;
-                    x[2] = a.z;
-                    x[3] = a.w;
-                    x[4] = b.x;
-                    x[5] = b.y;
-                    x[6] = b.z;
-                    x[7] = b.w;
-                }
-                ps.push(x, present(kk));
-            }
+                for (int i = 0; i < 8; ++i) own[i] = 0.f;
             float acc[8];
-            ps.root(acc);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const float4 r = tree_xor_n<float4>(S, [&](int kk) {
+                    if (kk == 0)
+                        return make_float4(own[4 * half], own[4 * half + 1], own[4 * half + 2],
+                                           own[4 * half + 3]);
+                    return reinterpret_cast<const float4*>(smem + (kk - 1) * ib)[(u + half) * L + h];
+                }, split, np);
+                acc[4 * half] = r.x;
+                acc[4 * half + 1] = r.y;
+                acc[4 * half + 2] = r.z;
+                acc[4 * half + 3] = r.w;
+            }
             stage8(stage, CW * 2, mask, h, cg * GW + 8 * q, acc, inv);
         }
         if (split == 0 && cg == 0)

@@ -473,46 +473,24 @@ __device__ __forceinline__ void flush(const uint8_t* stage, int row_bytes, int m
 // largest power of two (at most 8) that divides chunks, minus one.
 __device__ __forceinline__ int stage_mask(int chunks) { return min(chunks & -chunks, 8) - 1; }
 
-// One owner's 16 columns at `col` of a unit of s pieces: the pairwise tree
-// over positions k = 0 .. P - 1 (piece j ^ k; P = s rounded up to a power of
-// two = 2^D, absent pieces past s), NV columns at a time. Lane h's own row
-// holds n_lane keys: pieces past them are absent for it (row groups).
-template <int D, int NV>
-__device__ __forceinline__ void merge_cols(const float* part, int64_t item0, int j, int s,
-                                           int n_lane, int h, int col, const float (&own)[16],
+// One owner's 16 columns at `col` of a unit: the pairwise tree over positions
+// k = 0 .. P - 1 (piece j ^ k; P = the unit's pieces rounded up to a power of
+// two), pieces src >= np absent (np: the pieces holding keys of lane h's own
+// row; all of the unit's pieces unless row groups), 4 columns at a time.
+__device__ __forceinline__ void merge_cols(const float* part, int64_t item0, int j, int P, int np,
+                                           int h, int col, const float (&own)[16],
                                            float (&out)[16]) {
     constexpr int64_t kPartFloats = static_cast<int64_t>(kTcHeads) * kLatent;
-    const int P = 1 << D;
 #pragma unroll
-    for (int c0 = 0; c0 < 16; c0 += NV) {
-        PairSum<D, NV> ps;
-        for (int k = 0; k < P; ++k) {
-            const int src = j ^ k;
-            const bool pres = src < s && src * kTcLeaf < n_lane;
-            float x[NV];
-            if (k == 0) {
-#pragma unroll
-                for (int e = 0; e < NV; ++e) x[e] = own[c0 + e];
-            } else if (pres) {
-                const float* p4 = part + (item0 + src) * kPartFloats + (((col + c0) >> 2) * kTcHeads + h) * 4;
-#pragma unroll
-                for (int i = 0; i < NV / 4; ++i) {
-                    const float4 v = ld_cg_v4(p4 + i * kTcHeads * 4);
-                    x[4 * i] = v.x;
-                    x[4 * i + 1] = v.y;
-                    x[4 * i + 2] = v.z;
-                    x[4 * i + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < NV; ++e) x[e] = 0.f;
-            }
-            ps.push(x, pres);
-        }
-        float r[NV];
-        ps.root(r);
-#pragma unroll
-        for (int e = 0; e < NV; ++e) out[c0 + e] = r[e];
+    for (int c0 = 0; c0 < 16; c0 += 4) {
+        const float4 r = tree_xor_n<float4>(P, [&](int k) {
+            if (k == 0) return make_float4(own[c0], own[c0 + 1], own[c0 + 2], own[c0 + 3]);
+            return ld_cg_v4(part + (item0 + (j ^ k)) * kPartFloats + (((col + c0) >> 2) * kTcHeads + h) * 4);
+        }, j, np);
+        out[c0] = r.x;
+        out[c0 + 1] = r.y;
+        out[c0 + 2] = r.z;
+        out[c0 + 3] = r.w;
     }
 }
 
@@ -610,22 +588,11 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
 
     // 3. Merge: the pairwise tree over the unit's pieces in the order j ^ k.
     const int n_lane = lane_count(p, it.b0, h);
-    const int D = log2_exact(s);
-    float total;
-    {
-        PairSum<5, 1> ts;
-        for (int k = 0; k < (1 << D); ++k) {
-            const int src = j ^ k;
-            const bool pres = src < s && src * kTcLeaf < n_lane;
-            const float v = k == 0 ? l
-                            : pres ? ld_cg_f32(sums + static_cast<int64_t>(it.item0 + src) * kTcHeads + h)
-                                   : 0.f;
-            ts.push1(v, pres);
-        }
-        float r[1];
-        ts.root(r);
-        total = r[0];
-    }
+    const int P = pow2_ceil(s);
+    const int np = min(s, (n_lane + kTcLeaf - 1) / kTcLeaf);  // pieces holding keys of h's row
+    const float total = tree_xor_n<float>(P, [&](int k) {
+        return k == 0 ? l : ld_cg_f32(sums + static_cast<int64_t>(it.item0 + (j ^ k)) * kTcHeads + h);
+    }, j, np);
     const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
     const int mask = stage_mask(CW / 8);
     for (int q = cg; 16 * q < CW; q += 4) {
@@ -638,13 +605,7 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
             for (int i = 0; i < 16; ++i) own[i] = 0.f;
         }
         if (h < p.lanes) {
-            switch (D) {
-                case 1: merge_cols<1, 16>(part, it.item0, j, s, n_lane, h, col, own, acc); break;
-                case 2: merge_cols<2, 8>(part, it.item0, j, s, n_lane, h, col, own, acc); break;
-                case 3: merge_cols<3, 4>(part, it.item0, j, s, n_lane, h, col, own, acc); break;
-                case 4: merge_cols<4, 4>(part, it.item0, j, s, n_lane, h, col, own, acc); break;
-                default: merge_cols<5, 4>(part, it.item0, j, s, n_lane, h, col, own, acc); break;
-            }
+            merge_cols(part, it.item0, j, P, np, h, col, own, acc);
         } else {
 #pragma unroll
             for (int i = 0; i < 16; ++i) acc[i] = 0.f;  // padding lanes are never stored

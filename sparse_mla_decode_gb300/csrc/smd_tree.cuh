@@ -72,73 +72,59 @@ __device__ __forceinline__ float tree_add(float x, bool px, float y, bool py) {
     return px ? (py ? x + y : x) : y;
 }
 
-// A binary counter over at most 2^D leaves of NV floats pushed in tree
-// position order: level d holds the subtree of the 2^d leaves that bit d of
-// the push count stands for, so at most D + 1 subtrees are live.
-template <int D, int NV>
-struct PairSum {
-    float lvl[D + 1][NV];
-    uint32_t pres;  // bit d: level d's subtree has a present leaf
-    int n;          // leaves pushed
+__device__ __forceinline__ float tree_plus(float a, float b) { return a + b; }
+__device__ __forceinline__ float4 tree_plus(float4 a, float4 b) {
+    return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
 
-    __device__ __forceinline__ PairSum() : pres(0u), n(0) {
-#pragma unroll
-        for (int d = 0; d <= D; ++d)
-#pragma unroll
-            for (int e = 0; e < NV; ++e) lvl[d][e] = 0.f;
+// The tree over positions [OFF + LO, OFF + LO + N) of a unit whose position k
+// holds leaf j ^ k (j: the evaluating owner; j = 0 gives list order), leaf
+// src present iff src < np; `load(k)` gives position k's value and is called
+// for present leaves only. Evaluated depth first, so at most log2 N + 1
+// partial sums are live; N is a compile-time power of two, so the tree
+// unrolls. *pres: some leaf below is present (else 0 is returned).
+template <int LO, int N, typename T, typename F>
+__device__ __forceinline__ T tree_xor(F&& load, int j, int np, int off, bool* pres) {
+    if constexpr (N == 1) {
+        *pres = (j ^ (off + LO)) < np;
+        return *pres ? load(off + LO) : T{};
+    } else {
+        bool pa, pb;
+        const T a = tree_xor<LO, N / 2, T>(load, j, np, off, &pa);
+        const T b = tree_xor<LO + N / 2, N / 2, T>(load, j, np, off, &pb);
+        *pres = pa || pb;
+        return pa ? (pb ? tree_plus(a, b) : a) : b;
     }
+}
 
-    __device__ __forceinline__ void push(const float (&x)[NV], bool px) {
-        float cur[NV];
-#pragma unroll
-        for (int e = 0; e < NV; ++e) cur[e] = x[e];
-        bool pc = px, done = false;
-#pragma unroll
-        for (int d = 0; d <= D; ++d) {
-            if (done) continue;
-            if (d < D && ((n >> d) & 1)) {
-                const bool pl = (pres >> d) & 1u;
-#pragma unroll
-                for (int e = 0; e < NV; ++e) cur[e] = tree_add(lvl[d][e], pl, cur[e], pc);
-                pc = pc || pl;
-            } else {
-#pragma unroll
-                for (int e = 0; e < NV; ++e) lvl[d][e] = cur[e];
-                pres = pc ? (pres | (1u << d)) : (pres & ~(1u << d));
-                done = true;
-            }
-        }
-        ++n;
+// tree_xor over positions 0 .. n - 1, n a power of two (at most 32) chosen at
+// run time. Units of 16 or 32 positions are taken as blocks of 8 (subtrees of
+// the same tree) whose results are then combined, which keeps the unrolled
+// code and its registers small.
+template <typename T, typename F>
+__device__ __forceinline__ T tree_xor_n(int n, F&& load, int j, int np) {
+    bool p;
+    switch (n) {
+        case 1: return tree_xor<0, 1, T>(load, j, np, 0, &p);
+        case 2: return tree_xor<0, 2, T>(load, j, np, 0, &p);
+        case 4: return tree_xor<0, 4, T>(load, j, np, 0, &p);
+        case 8: return tree_xor<0, 8, T>(load, j, np, 0, &p);
+        default: break;
     }
-
-    __device__ __forceinline__ void push1(float x, bool px) {
-        float v[NV];
-        v[0] = x;
-        push(v, px);
+    T blk[4];
+    bool pb[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        pb[b] = false;
+        blk[b] = T{};
+        if (8 * b < n) blk[b] = tree_xor<0, 8, T>(load, j, np, 8 * b, &pb[b]);
     }
-
-    // The root over the leaves pushed (absent leaves fill up to a power of
-    // two); false, with out = 0, if no leaf was present.
-    __device__ __forceinline__ bool root(float (&out)[NV]) const {
-        bool po = false;
-#pragma unroll
-        for (int e = 0; e < NV; ++e) out[e] = 0.f;
-#pragma unroll
-        for (int d = 0; d <= D; ++d) {
-            if ((n >> d) & 1) {
-                const bool pl = (pres >> d) & 1u;
-#pragma unroll
-                for (int e = 0; e < NV; ++e) out[e] = tree_add(lvl[d][e], pl, out[e], po);
-                po = po || pl;
-            }
-        }
-        if (!po) {
-#pragma unroll
-            for (int e = 0; e < NV; ++e) out[e] = 0.f;
-        }
-        return po;
-    }
-};
+    const T lo = pb[0] ? (pb[1] ? tree_plus(blk[0], blk[1]) : blk[0]) : blk[1];
+    if (n == 16) return lo;
+    const bool plo = pb[0] || pb[1];
+    const T hi = pb[2] ? (pb[3] ? tree_plus(blk[2], blk[3]) : blk[2]) : blk[3];
+    return plo ? ((pb[2] || pb[3]) ? tree_plus(lo, hi) : lo) : hi;
+}
 
 // ---- the subtree stack of the warp-MMA kernels ---------------------------------
 // Those kernels hold a leaf's P V partial in registers (acc[T][4][4]: 16 T
