@@ -329,7 +329,7 @@ def run_gpu(args, world, rank, local) -> dict | None:
     gathered = stats["kv_gathered"]
     e2e_value = world * gathered / (e2e_ms * 1e-3) / 1e9
     achieved = stats["total"] / (ms * 1e-3) / 1e9
-    fp8_peak_tflops = 2.0 * pk["bf16_tflops"]
+    fp8_peak_tflops, fp8_source = fp8_peak(pk)
     t_hbm = stats["total"] / (pk["hbm_gbs"] * 1e9)
     t_tc = stats["flops"] / (fp8_peak_tflops * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
@@ -346,8 +346,10 @@ def run_gpu(args, world, rank, local) -> dict | None:
         "algorithmic_flops": stats["flops"],
         "t_roof_us": round(max(t_hbm, t_tc) * 1e6, 4),
         "frac_of_roofline_time": round(max(t_hbm, t_tc) / (ms * 1e-3), 5),
-        "peak_source": pk["source"] + ("" if bound == "hbm" else
-                                       "; FP8 = 2 x measured BF16 (nominal ratio)"),
+        "peak_source": pk["source"] + ("" if bound == "hbm" else "; " + fp8_source),
+        "tensor_peak_tflops": round(fp8_peak_tflops, 1),
+        "tensor_frac": round(stats["flops"] / (ms * 1e-3) / 1e12 / fp8_peak_tflops, 5),
+        "tensor_peak_source": fp8_source,
     }
     roofline["frac"] = round(roofline["achieved"] / roofline["peak"], 5)
     cpu = (cpu_baseline(case, stats, args.cpu_seconds, bf16q) if world == 1 or rank == 0
@@ -515,6 +517,60 @@ def graph_timing(call, dev, calls: int = 100, replays: int = 5):
     except Exception as exc:  # a capture this build cannot do is reported, not fatal
         torch.cuda.synchronize()
         return {"error": str(exc)[:200]}
+
+
+FP8_PEAK_FILE = os.path.join(ROOT, "profiles", "tcgen05_fp8_mma_peak.json")
+
+
+def fp8_peak(pk: dict) -> tuple[float, str]:
+    """The FP8 tensor peak (TFLOP/s) for the roofline: the committed
+    measurement of the tcgen05 kind::f8f6f4 rate probe (bench.py
+    --measure-fp8-peak on this part), else 2 x the measured BF16 peak."""
+    try:
+        with open(FP8_PEAK_FILE) as f:
+            d = json.load(f)
+        return float(d["tflops_median"]), ("builder-measured tcgen05 kind::f8f6f4 rate "
+                                           "(profiles/tcgen05_fp8_mma_peak.json)")
+    except Exception:
+        return 2.0 * pk["bf16_tflops"], "FP8 = 2 x measured BF16 (nominal ratio)"
+
+
+def measure_fp8_peak(args) -> dict:
+    """The FP8 tensor-pipe rate probe (smd_fp8_mma_probe): one CTA per SM
+    issuing M128 N256 K32 E4M3 MMAs back to back; CUDA events around each
+    launch, clocks sampled meanwhile."""
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    iters = 20000
+    for _ in range(max(args.warmup, 3)):
+        ctas = binding.smd_fp8_mma_probe(iters, status.data_ptr(), stream.cuda_stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0).start()
+    time.sleep(0.2)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for a, b in ev:
+        a.record(stream)
+        binding.smd_fp8_mma_probe(iters, status.data_ptr(), stream.cuda_stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    ms = [a.elapsed_time(b) for a, b in ev]
+    flops = ctas * iters * 2 * 128 * 256 * 32
+    return {"what": "tcgen05.mma.cta_group::1.kind::f8f6f4 E4M3 x E4M3 -> FP32, M128 N256 K32, "
+                    "K-major SW128 operands, one issuing thread per SM, back to back",
+            "ctas": ctas, "mma_per_cta": iters, "flops_per_launch": flops,
+            "launches": args.steps, "ms_median": round(float(np.median(ms)), 4),
+            "ms_min": round(float(np.min(ms)), 4),
+            "tflops_median": round(flops / (float(np.median(ms)) * 1e-3) / 1e12, 1),
+            "tflops_max": round(flops / (float(np.min(ms)) * 1e-3) / 1e12, 1),
+            "clocks": clocks}
 
 
 def topk_bytes(case) -> dict:
@@ -751,7 +807,12 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--query", default="e4m3", choices=["e4m3", "bf16"],
                     help="bf16: the bf16-query call (query split into E4M3 hi + lo)")
+    ap.add_argument("--measure-fp8-peak", action="store_true",
+                    help="time the FP8 tensor-pipe rate probe instead (one JSON line)")
     args = ap.parse_args(argv)
+    if args.measure_fp8_peak:
+        print(json.dumps(measure_fp8_peak(args)), flush=True)
+        return
     world, rank, local = (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
                           int(os.environ.get("LOCAL_RANK", "0")))
     if args.impl == "reference":

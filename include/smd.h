@@ -35,7 +35,8 @@
  * negative smd_status (nothing is launched). Problems only the GPU can see
  * (a bounded wait that ran out) are written to the optional device word
  * `status` (left untouched on success; the caller zeroes it beforehand).
- * Indices of valid entries must lie in [0, N); they are not checked.
+ * Indices of valid entries must lie in [0, N); the decode does not check
+ * them (smd_validate_indices does, as a separate call).
  */
 #ifndef SMD_H
 #define SMD_H
@@ -63,8 +64,10 @@ typedef enum {
                              device status: an SM id beyond the workspace    */
     SMD_ERR_WORKSPACE = -8, /* workspace given but smaller than
                              smd_workspace_bytes() or not 16-byte aligned    */
-    SMD_ERR_GROUP = -9    /* device status: rows of a group do not share their
+    SMD_ERR_GROUP = -9,   /* device status: rows of a group do not share their
                              index list (smd_sparse_mla_decode_grouped)      */
+    SMD_ERR_INDEX = -10   /* device status: a valid entry of the index list
+                             lies outside [0, N) (smd_validate_indices)      */
 } smd_status;
 
 /* Kernel families. */
@@ -497,6 +500,42 @@ int smd_topk_select_host(const uint16_t* logits_host, int64_t row_stride,
 /* The base-2 logit scale the kernels use: fp32(sm*q_s*k_s*log2 e),
  * evaluated in double and rounded once. */
 float smd_scale_log2(float sm_scale, float q_scale, float k_scale);
+
+/* Range check of an index list before a decode: for every row b < B and
+ * entry i < n_b = clamp(counts[b], 0, W), indices[b, i] must lie in [0, N).
+ * The attn_sparse page's kernel gathers the rows an index list names without
+ * such a check (SparseDcpDecode.kernel, the gather loop), and so do the
+ * decode calls here, where an out-of-range entry reads outside the cache
+ * pool; a caller that cannot vouch for its lists runs this first, reads
+ * `status`, and decodes only if it is still SMD_OK.
+ *   indices  [B, W] int32 device memory (4-byte aligned); entries past a
+ *            row's count are not read.
+ *   counts   [B] int32 device memory (4-byte aligned).
+ *   N        rows of the cache pool the lists index.
+ *   status   device int32 (4-byte aligned), required; the caller zeroes it
+ *            beforehand. SMD_ERR_INDEX is written there (first writer wins)
+ *            if any valid entry lies outside [0, N); it is left untouched
+ *            otherwise.
+ * Reads the counts and the valid entries only; no entry is used as an
+ * address. Asynchronous on `stream`. Returns SMD_OK, or SMD_ERR_SHAPE (B, W
+ * or N negative), SMD_ERR_NULL, SMD_ERR_ALIGN, SMD_ERR_DEVICE,
+ * SMD_ERR_LAUNCH with nothing launched. B == 0 is a no-op. */
+int smd_validate_indices(const int32_t* indices, int32_t W, const int32_t* counts, int32_t B,
+                         int64_t N, int32_t* status, smd_stream_t stream);
+
+/* Measurement aid, not part of the decode: the rate probe of the FP8 tensor
+ * pipe that gives the tensor side of the decode's roofline its denominator
+ * (the pages state no tensor peak for this part). Launches one CTA per SM,
+ * each issuing `iters` tcgen05.mma.kind::f8f6f4 instructions (E4M3 x E4M3 ->
+ * FP32, M = 128, N = 256, K = 32, both operands K-major in the 128-byte
+ * swizzle: the decode's PV shape) back to back into one TMEM accumulator;
+ * every instruction is 2 * 128 * 256 * 32 FLOPs. The caller times the
+ * launch on `stream` (CUDA events) and divides. *ctas (optional, host
+ * memory) receives the number of CTAs launched; `status` (optional device
+ * int32) receives SMD_ERR_TIMEOUT if the completion wait (2 s) runs out.
+ * Returns SMD_OK, SMD_ERR_SHAPE (iters < 1), SMD_ERR_ALIGN, SMD_ERR_DEVICE
+ * or SMD_ERR_LAUNCH. */
+int smd_fp8_mma_probe(int32_t iters, int32_t* status, smd_stream_t stream, int32_t* ctas);
 
 /* Static text for a status code. */
 const char* smd_status_str(int status);

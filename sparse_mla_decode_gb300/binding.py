@@ -21,6 +21,7 @@ SMD_ERR_PLAN = -6
 SMD_ERR_DEVICE = -7
 SMD_ERR_WORKSPACE = -8
 SMD_ERR_GROUP = -9
+SMD_ERR_INDEX = -10
 
 SMD_KERNEL_AUTO = 0
 SMD_KERNEL_MMA = 1
@@ -142,6 +143,13 @@ def lib() -> ctypes.CDLL:
             so.smd_topk_select_host.restype = ctypes.c_int
             so.smd_topk_select_host.argtypes = tk_args[:-1] + [ctypes.c_void_p, ctypes.c_int64,
                                                                ctypes.c_int32, ctypes.c_void_p]
+            so.smd_validate_indices.restype = ctypes.c_int
+            so.smd_validate_indices.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                                ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p,
+                                                ctypes.c_void_p]
+            so.smd_fp8_mma_probe.restype = ctypes.c_int
+            so.smd_fp8_mma_probe.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
+                                             ctypes.POINTER(ctypes.c_int32)]
             so.smd_scale_log2.restype = ctypes.c_float
             so.smd_scale_log2.argtypes = [ctypes.c_float] * 3
             so.smd_status_str.restype = ctypes.c_char_p
@@ -340,6 +348,19 @@ def smd_topk_select_host(logits, row_stride, row_ends, B, L, K, indices, counts,
                          workspace, workspace_bytes, copies, stream) -> int:
     return lib().smd_topk_select_host(logits, row_stride, row_ends, B, L, K, indices, counts,
                                       status, workspace, workspace_bytes, copies, stream)
+
+
+def smd_validate_indices(indices, W, counts, B, N, status, stream) -> int:
+    return lib().smd_validate_indices(indices, W, counts, B, N, status, stream)
+
+
+def smd_fp8_mma_probe(iters: int, status, stream) -> int:
+    """Launches the FP8 tensor-pipe rate probe; returns the CTAs launched."""
+    n = ctypes.c_int32(0)
+    rc = lib().smd_fp8_mma_probe(iters, status, stream, ctypes.byref(n))
+    if rc != SMD_OK:
+        raise SmdError(rc, "smd_fp8_mma_probe")
+    return n.value
 
 
 def smd_scale_log2(sm_scale: float, q_scale: float, k_scale: float) -> float:
@@ -584,6 +605,28 @@ def topk_select(logits, K: int, row_ends=None, indices=None, counts=None, stream
     if rc != SMD_OK:
         raise SmdError(rc, "smd_topk_select")
     return indices, counts
+
+
+def validate_indices(indices, counts, N: int, status=None, stream=None):
+    """Range check of an index list on the GPU (smd_validate_indices): every
+    valid entry (i < clamp(counts[b], 0, W)) of the int32 CUDA tensor
+    indices [B, W] must lie in [0, N). Returns the int32 status tensor (one
+    element, zeroed here unless given), which holds SMD_ERR_INDEX after the
+    stream reaches the check if an entry lies outside."""
+    import torch
+    if indices.dim() != 2 or indices.dtype != torch.int32 or counts.dtype != torch.int32:
+        raise ValueError("indices [B, W] and counts [B] must be int32")
+    if not (indices.is_cuda and counts.is_cuda) or not indices.is_contiguous():
+        raise ValueError("indices and counts must be contiguous CUDA tensors")
+    B, W = indices.shape
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=indices.device)
+    stream = torch.cuda.current_stream(indices.device) if stream is None else stream
+    rc = smd_validate_indices(_ptr(indices), W, _ptr(counts), B, int(N), _ptr(status),
+                              int(stream.cuda_stream))
+    if rc != SMD_OK:
+        raise SmdError(rc, "smd_validate_indices")
+    return status
 
 
 def topk_select_host(logits, K: int, row_ends=None, indices=None, counts=None, stream=None,

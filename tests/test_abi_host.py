@@ -45,7 +45,7 @@ def test_scale_log2_is_the_rounded_double_product():
 
 
 def test_status_strings():
-    for code in range(-9, 1):
+    for code in range(-10, 1):
         s = smd.smd_status_str(code)
         assert s and s != "unknown status"
     assert smd.smd_status_str(-99) == "unknown status"
@@ -366,7 +366,7 @@ def test_host_call_with_no_rows_is_a_no_op():
     (64, 128, 2048, 1, False, 1),   # DSA: the spread kernel takes the whole batch
     (256, 128, 2048, 1, False, 4),  # throughput: 54 MB of host data, 1024 cluster CTAs: 4 x 64 rows
     (128, 16, 8192, 4, False, 1),   # dense-as-sparse: 512 CTAs, but only 7.4 MB of host data
-    (512, 16, 8192, 4, False, 4),   # four times the requests: 30 MB, 2048 CTAs
+    (512, 16, 8192, 4, False, 1),   # four times the requests: the spread kernel takes the batch
     (256, 128, 2048, 1, True, 1),   # bf16 query on the spread kernel
 ])
 def test_host_plan_chunks_large_host_data_where_each_chunk_fills_the_device(B, H, W, G, bf16, chunks):
@@ -418,3 +418,24 @@ def test_topk_host_workspace_pads_rows_to_16_bytes():
     assert smd.smd_workspace_bytes_topk_host(0, 13, 5) == 0
     assert smd.smd_workspace_bytes_topk_host(2, 8, 0) == smd.SMD_ERR_SHAPE
     assert smd.smd_topk_select_host(0, 0, 0, 0, 0, 1, 0, 0, 0, 0, 0, 0, 0) == smd.SMD_OK
+
+
+# ---- smd_validate_indices: argument checks on the host (nothing launched) ----
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=-1), smd.SMD_ERR_SHAPE),
+    (dict(W=-1), smd.SMD_ERR_SHAPE),
+    (dict(N=-1), smd.SMD_ERR_SHAPE),
+    (dict(status=0), smd.SMD_ERR_NULL),
+    (dict(counts=0), smd.SMD_ERR_NULL),
+    (dict(idx=0), smd.SMD_ERR_NULL),
+    (dict(idx=A + 2), smd.SMD_ERR_ALIGN),
+    (dict(counts=A + 1), smd.SMD_ERR_ALIGN),
+    (dict(status=A + 2), smd.SMD_ERR_ALIGN),
+    (dict(B=0, idx=0, counts=0), smd.SMD_OK),
+])
+def test_validate_indices_argument_checks(kw, code):
+    a = dict(idx=A, W=8, counts=A, B=2, N=100, status=A)
+    a.update(kw)
+    assert smd.smd_validate_indices(a["idx"], a["W"], a["counts"], a["B"], a["N"], a["status"],
+                                    None) == code

@@ -183,10 +183,9 @@ def test_groups_on_the_spread_kernel(cuda, shape):
     out_g, lse_g = grouped_ws(case, cuda, G, tensors=t)
     check(out_g, lse_g, out_o, lse_o, f"grouped spread {shape}")
     from sparse_mla_decode_gb300 import binding
-    # with a workspace the automatic plan takes the spread kernel only where
-    # the row-group tcgen05 kernel does not fit
-    want = SPREAD if G * H not in (32, 64) or W > 8192 else TC_GROUP
-    assert binding.smd_plan_grouped(case.B, H, W, G, 1 << 40).kernel == want
+    # with a workspace the automatic plan takes the spread kernel wherever it
+    # fits (G x H <= 128 lanes, lists of at most 16384 keys)
+    assert binding.smd_plan_grouped(case.B, H, W, G, 1 << 40).kernel == SPREAD
 
 
 def test_groups_on_the_spread_kernel_grid_changes_no_bits(cuda):
