@@ -527,8 +527,8 @@ int smd_validate_indices(const int32_t* indices, int32_t W, const int32_t* count
  * pipe that gives the tensor side of the decode's roofline its denominator
  * (the pages state no tensor peak for this part). Launches one CTA per SM,
  * each issuing `iters` tcgen05.mma.kind::f8f6f4 instructions (E4M3 x E4M3 ->
- * FP32, M = 128, N = 256, K = 32, both operands K-major in the 128-byte
- * swizzle: the decode's PV shape) back to back into one TMEM accumulator;
+ * FP32, M = 128, N = 256, K = 32 as in the decode's PV; both operands K-major
+ * in the 128-byte swizzle) back to back into one TMEM accumulator;
  * every instruction is 2 * 128 * 256 * 32 FLOPs. The caller times the
  * launch on `stream` (CUDA events) and divides. *ctas (optional, host
  * memory) receives the number of CTAs launched; `status` (optional device

@@ -3,10 +3,9 @@
 //
 // One CTA per SM; one thread issues `iters` tcgen05.mma.cta_group::1
 // .kind::f8f6f4 instructions back to back (E4M3 x E4M3 -> FP32, M = 128,
-// N = 256, K = 32: the shape and operand layouts of the decode's PV
-// products, both operands K-major in the 128-byte swizzle) from two zeroed
-// shared-memory tiles into one TMEM accumulator, commits them to an mbarrier
-// and waits for it (bounded). Each instruction is 2 * 128 * 256 * 32 FLOPs;
+// N = 256, K = 32 as in the decode's PV products; both operands K-major in
+// the 128-byte swizzle) from two zeroed shared-memory tiles into one TMEM
+// accumulator, commits them to an mbarrier and waits for it (bounded). Each instruction is 2 * 128 * 256 * 32 FLOPs;
 // the caller times the launch with CUDA events.
 #include <cstdint>
 
