@@ -757,7 +757,7 @@ bool encode_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint32_t box_c
     CUtensorMap m;
     const CUresult r = encode(
         &m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+        CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return false;
     MapEntry& e = g_maps[g_map_next];
