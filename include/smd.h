@@ -386,6 +386,68 @@ int smd_sparse_mla_decode_grouped_ex(const uint8_t* q, const uint8_t* kv_pool, i
                                      void* workspace, int64_t workspace_bytes,
                                      smd_stream_t stream, const smd_plan_t* force);
 
+/* ---- one call for every device-memory variant ------------------------------------
+ *
+ * smd_decode runs the decode of smd_sparse_mla_decode with the variant an
+ * options struct names; options == NULL (or all fields zero) is
+ * smd_sparse_mla_decode itself. Each specialised entry point above equals
+ * smd_decode with these options, bit for bit (they stay for existing callers):
+ *   _ws                    workspace, workspace_bytes
+ *   _ex                    workspace, workspace_bytes, force
+ *   _bf16q / _bf16q_ws / _bf16q_ex   query_type = SMD_QUERY_BF16 (+ as above)
+ *   _grouped / _grouped_ws / _grouped_ex   row_group = 2 or 4 (+ as above)
+ *   _noalloc               library_scratch = 1
+ * The fields:
+ *   row_group        0 or 1: every row has its own index list; 2 or 4: rows
+ *                    in consecutive groups sharing one list (the grouped calls).
+ *   query_type       SMD_QUERY_E4M3: q is [B, H, 576] E4M3 codes with q_scale;
+ *                    SMD_QUERY_BF16: q is [B, H, 576] bfloat16 and q_scale is
+ *                    not used (the bf16q calls).
+ *   library_scratch  nonzero: a split plan exchanges its partials through the
+ *                    library's static scratch (smd_sparse_mla_decode_noalloc,
+ *                    with its restrictions).
+ *   reserved         must be 0.
+ *   workspace, workspace_bytes   caller device workspace or NULL (its size
+ *                    from smd_decode_workspace_bytes).
+ *   status           optional device status word, as in smd_sparse_mla_decode.
+ *   force            NULL: the automatic plan; else a forced plan (for tests).
+ * Invalid combinations return, with nothing launched: SMD_ERR_SHAPE for a
+ * nonzero `reserved`, an unknown query_type or a row_group other than
+ * 0, 1, 2, 4; SMD_ERR_PLAN for a bf16 query with row groups, or
+ * library_scratch with a workspace, row groups or a bf16 query. Otherwise
+ * the return codes, ownership and ordering are those of the call the options
+ * name. */
+typedef enum { SMD_QUERY_E4M3 = 0, SMD_QUERY_BF16 = 1 } smd_query_type;
+
+typedef struct {
+    int32_t row_group;
+    int32_t query_type;
+    int32_t library_scratch;
+    int32_t reserved;
+    void* workspace;
+    int64_t workspace_bytes;
+    int32_t* status;
+    const smd_plan_t* force;
+} smd_options_t;
+
+int smd_decode(const void* q, const uint8_t* kv_pool, int64_t N, const int32_t* indices,
+               int32_t W, const int32_t* counts, int32_t B, int32_t H, float sm_scale,
+               float q_scale, float k_scale, uint16_t* out, float* lse,
+               const smd_options_t* options, smd_stream_t stream);
+
+/* Bytes of workspace the workspace plan of these options wants (0 when that
+ * plan needs none, or for invalid shapes or options): smd_workspace_bytes,
+ * _ex (with force), _bf16q or _grouped. Host only. */
+int64_t smd_decode_workspace_bytes(int32_t B, int32_t H, int32_t W, const smd_options_t* options);
+
+/* The plan smd_decode would run for these shapes and options, written to
+ * *plan (a workspace counts as given when options->workspace is non-NULL or
+ * workspace_bytes > 0; its size is not checked here). Host only; pointers
+ * are not needed. Returns SMD_OK or the status smd_decode would return for
+ * the shapes and options. */
+int smd_decode_plan(int32_t B, int32_t H, int32_t W, const smd_options_t* options,
+                    smd_plan_t* plan);
+
 /* ---- the decode from and to host memory ---------------------------------------
  *
  * Options of smd_sparse_mla_decode_host (all zero: E4M3 query, one row per

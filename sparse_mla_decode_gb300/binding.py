@@ -30,6 +30,9 @@ SMD_KERNEL_GROUP = 3
 SMD_KERNEL_TC_GROUP = 4
 SMD_KERNEL_TC_SPREAD = 5
 
+SMD_QUERY_E4M3 = 0
+SMD_QUERY_BF16 = 1
+
 
 class SmdPlan(ctypes.Structure):
     """smd_plan_t."""
@@ -45,6 +48,14 @@ class SmdHostOpts(ctypes.Structure):
     """smd_host_opts_t."""
     _fields_ = [(name, ctypes.c_int32) for name in ("row_group", "bf16_query", "chunks",
                                                      "copies")]
+
+
+class SmdOptions(ctypes.Structure):
+    """smd_options_t."""
+    _fields_ = [("row_group", ctypes.c_int32), ("query_type", ctypes.c_int32),
+                ("library_scratch", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_int64),
+                ("status", ctypes.c_void_p), ("force", ctypes.POINTER(SmdPlan))]
 
 
 class SmdError(RuntimeError):
@@ -153,6 +164,15 @@ def lib() -> ctypes.CDLL:
             so.smd_scale_log2.restype = ctypes.c_float
             so.smd_scale_log2.argtypes = [ctypes.c_float] * 3
             so.smd_status_str.restype = ctypes.c_char_p
+            so.smd_decode.argtypes = _DECODE_ARGS[:-2] + [ctypes.POINTER(SmdOptions),
+                                                           ctypes.c_void_p]
+            so.smd_decode.restype = ctypes.c_int
+            so.smd_decode_plan.argtypes = [ctypes.c_int32] * 3 + [ctypes.POINTER(SmdOptions),
+                                                                  ctypes.POINTER(SmdPlan)]
+            so.smd_decode_plan.restype = ctypes.c_int
+            so.smd_decode_workspace_bytes.argtypes = [ctypes.c_int32] * 3 + [
+                ctypes.POINTER(SmdOptions)]
+            so.smd_decode_workspace_bytes.restype = ctypes.c_int64
             so.smd_status_str.argtypes = [ctypes.c_int]
             so.smd_version.restype = ctypes.c_int
             so.smd_version.argtypes = []
@@ -363,6 +383,54 @@ def smd_fp8_mma_probe(iters: int, status, stream) -> int:
     return n.value
 
 
+def _as_plan(force):
+    if isinstance(force, dict):
+        p = SmdPlan()
+        for k, v in force.items():
+            setattr(p, k, int(v))
+        return p
+    return force
+
+
+def smd_options(row_group: int = 1, query_type: int = SMD_QUERY_E4M3, library_scratch: bool = False,
+                workspace: int = 0, workspace_bytes: int = 0, status: int = 0,
+                force: SmdPlan | dict | None = None, reserved: int = 0) -> SmdOptions:
+    """An smd_options_t (pointers as integers). The forced plan, if any, is
+    kept alive by the returned struct."""
+    o = SmdOptions()
+    o.row_group, o.query_type, o.library_scratch, o.reserved = (int(row_group), int(query_type),
+                                                                int(bool(library_scratch)),
+                                                                int(reserved))
+    o.workspace, o.workspace_bytes, o.status = int(workspace) or None, int(workspace_bytes), \
+        int(status) or None
+    force = _as_plan(force)
+    if force is not None:
+        o._force = force
+        o.force = ctypes.pointer(force)
+    return o
+
+
+def smd_decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale, out, lse,
+               options: SmdOptions | None, stream) -> int:
+    ref = ctypes.byref(options) if options is not None else None
+    return int(lib().smd_decode(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale,
+                                out, lse, ref, stream))
+
+
+def smd_decode_plan(B: int, H: int, W: int, options: SmdOptions | None = None) -> SmdPlan:
+    p = SmdPlan()
+    ref = ctypes.byref(options) if options is not None else None
+    rc = lib().smd_decode_plan(B, H, W, ref, ctypes.byref(p))
+    if rc != SMD_OK:
+        raise SmdError(rc, "smd_decode_plan")
+    return p
+
+
+def smd_decode_workspace_bytes(B: int, H: int, W: int, options: SmdOptions | None = None) -> int:
+    ref = ctypes.byref(options) if options is not None else None
+    return int(lib().smd_decode_workspace_bytes(B, H, W, ref))
+
+
 def smd_scale_log2(sm_scale: float, q_scale: float, k_scale: float) -> float:
     return float(lib().smd_scale_log2(sm_scale, q_scale, k_scale))
 
@@ -456,6 +524,58 @@ def sparse_mla_decode(q, kv_pool, indices, counts, sm_scale: float, q_scale: flo
         rc = smd_sparse_mla_decode_ex(*args, *ws, int(stream), plan)
     if rc != SMD_OK:
         raise SmdError(rc, "smd_sparse_mla_decode")
+    return out, lse
+
+
+def decode(q, kv_pool, indices, counts, sm_scale: float, q_scale: float, k_scale: float,
+           out=None, lse=None, status=None, stream=None, plan: SmdPlan | dict | None = None,
+           workspace=None, row_group: int = 1, library_scratch: bool = False):
+    """Decode on the GPU through smd_decode (one call for every variant).
+    q [B,H,576]: E4M3 (uint8 or float8_e4m3fn, with q_scale) or bfloat16 (the
+    split query; q_scale is not used); kv_pool [N,576] E4M3, indices [B,W]
+    int32, counts [B] int32, all CUDA tensors. ``row_group`` 2 or 4: rows in
+    groups sharing one index list; ``workspace``, ``plan``, ``status`` as in
+    sparse_mla_decode; ``library_scratch``: the no-alloc exchange. Returns
+    (out [B,H,512] bfloat16, lse [B,H] float32)."""
+    import torch
+
+    bf16 = q.dtype == torch.bfloat16
+    if not bf16:
+        q = _bytes_view(q, "q")
+    kv_pool = _bytes_view(kv_pool, "kv_pool")
+    for name, t in (("q", q), ("kv_pool", kv_pool), ("indices", indices), ("counts", counts)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor (the decode has no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if indices.dtype != torch.int32 or counts.dtype != torch.int32:
+        raise TypeError("indices and counts must be int32")
+    if q.dim() != 3 or q.shape[2] != 576 or kv_pool.dim() != 2 or kv_pool.shape[1] != 576:
+        raise ValueError("q must be [B,H,576] and kv_pool [N,576]")
+    B, H = int(q.shape[0]), int(q.shape[1])
+    if indices.dim() != 2 or indices.shape[0] < B or counts.shape[0] < B:
+        raise ValueError("indices must be [>=B, W] and counts [>=B]")
+    W = int(indices.shape[1])
+    if workspace is not None and not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    if out is None:
+        out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif hasattr(stream, "cuda_stream"):
+        stream = stream.cuda_stream
+    opts = smd_options(row_group=row_group, query_type=SMD_QUERY_BF16 if bf16 else SMD_QUERY_E4M3,
+                       library_scratch=library_scratch, workspace=_ptr(workspace),
+                       workspace_bytes=0 if workspace is None
+                       else workspace.numel() * workspace.element_size(),
+                       status=_ptr(status), force=plan)
+    rc = smd_decode(_ptr(q), _ptr(kv_pool), int(kv_pool.shape[0]), _ptr(indices), W, _ptr(counts),
+                    B, H, float(sm_scale), float(q_scale), float(k_scale), _ptr(out), _ptr(lse),
+                    opts, int(stream))
+    if rc != SMD_OK:
+        raise SmdError(rc, "smd_decode")
     return out, lse
 
 

@@ -404,20 +404,25 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
            const int32_t* counts, int32_t B, int32_t H, float sm_scale, float q_scale,
            float k_scale, uint16_t* out, float* lse, int32_t* status, void* workspace,
            int64_t workspace_bytes, smd_stream_t stream, const smd_plan_t* force,
-           bool library_scratch = false, int row_group = 1, const uint16_t* q16 = nullptr) {
+           bool library_scratch = false, int row_group = 1, const uint16_t* q16 = nullptr,
+           smd_plan_t* dry = nullptr) {
+    // dry != nullptr: no launch and no pointer checks; the plan the call would
+    // run is written to *dry (a workspace of any size counts as given).
     if (B < 0 || W < 0 || N < 0 || H <= 0 || H % kHeadsPerTile != 0) return SMD_ERR_SHAPE;
     if (row_group != 1 && ((row_group != 2 && row_group != 4) || B % row_group != 0))
         return SMD_ERR_SHAPE;
     if (N >= (int64_t(1) << 31)) return SMD_ERR_SHAPE;
-    if (B == 0) return SMD_OK;
-    if (!q || !out || !lse || !counts) return SMD_ERR_NULL;
-    if (W > 0 && (!indices || !kv_pool)) return SMD_ERR_NULL;
-    if (W > 0 && N == 0) return SMD_ERR_SHAPE;
-    if (!aligned(q, 16) || !aligned(out, 16) || (kv_pool && !aligned(kv_pool, 16)))
-        return SMD_ERR_ALIGN;
-    if ((indices && !aligned(indices, 4)) || !aligned(counts, 4) || !aligned(lse, 4) ||
-        (status && !aligned(status, 4)))
-        return SMD_ERR_ALIGN;
+    if (dry == nullptr) {
+        if (B == 0) return SMD_OK;
+        if (!q || !out || !lse || !counts) return SMD_ERR_NULL;
+        if (W > 0 && (!indices || !kv_pool)) return SMD_ERR_NULL;
+        if (W > 0 && N == 0) return SMD_ERR_SHAPE;
+        if (!aligned(q, 16) || !aligned(out, 16) || (kv_pool && !aligned(kv_pool, 16)))
+            return SMD_ERR_ALIGN;
+        if ((indices && !aligned(indices, 4)) || !aligned(counts, 4) || !aligned(lse, 4) ||
+            (status && !aligned(status, 4)))
+            return SMD_ERR_ALIGN;
+    }
 
     if (row_group > 1) {
         if (B % row_group != 0) return SMD_ERR_SHAPE;
@@ -431,6 +436,10 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
             TcsConfig scfg{};
             const int rc = plan_tcs(B, H, W, sm_count_of_device(), force, &plan, &scfg, row_group);
             if (rc != SMD_OK) return rc;
+            if (dry != nullptr) {
+                *dry = plan;
+                return SMD_OK;
+            }
             if (workspace == nullptr || workspace_bytes < tcs_workspace(scfg.items_cap).total)
                 return SMD_ERR_WORKSPACE;
             scfg.ws = workspace;
@@ -457,6 +466,11 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
                            ? plan_tcg(B, H, W, row_group, force, &plan, &tcfg)
                            : plan_group(B, H, W, row_group, sm_count_of_device(), force, &plan, &gcfg);
         if (rc != SMD_OK) return rc;
+        if (dry != nullptr) {
+            if (want == SMD_KERNEL_TC_GROUP) plan.smem_bytes = tcg_smem_bytes();
+            *dry = plan;
+            return SMD_OK;
+        }
         CallArgs a{};
         a.q = q;
         a.kv = kv_pool;
@@ -490,6 +504,10 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
         const int rc = spread ? plan_tcs(B, H, W, sm_count_of_device(), force, &plan, &tcfg)
                               : plan_mma(B, H, W, sm_count_of_device(), force, &plan, &mcfg, true);
         if (rc != SMD_OK) return rc;
+        if (dry != nullptr) {
+            *dry = plan;
+            return SMD_OK;
+        }
         if (spread) {
             const int64_t need = tcs_workspace(tcfg.items_cap, static_cast<int64_t>(B) * H).total;
             if (workspace == nullptr || workspace_bytes < need) return SMD_ERR_WORKSPACE;
@@ -520,6 +538,10 @@ int decode(const uint8_t* q, const uint8_t* kv_pool, int64_t N, const int32_t* i
     if (workspace != nullptr && !aligned(workspace, 16)) return SMD_ERR_WORKSPACE;
     const int rc = make_plan(B, H, W, force, &plan, &cfg, workspace != nullptr ? 0 : -1);
     if (rc != SMD_OK) return rc;
+    if (dry != nullptr) {
+        *dry = plan;
+        return SMD_OK;
+    }
     if (cfg.kernel == SMD_KERNEL_TC_SPREAD) {
         if (workspace == nullptr || workspace_bytes < workspace_for(cfg)) return SMD_ERR_WORKSPACE;
         cfg.tcs.ws = workspace;
@@ -623,6 +645,80 @@ int smd_sparse_mla_decode_bf16q_ex(const uint16_t* q, const uint8_t* kv_pool, in
     return smd::decode(reinterpret_cast<const uint8_t*>(q), kv_pool, N, indices, W, counts, B, H,
                        sm_scale, 1.0f, k_scale, out, lse, status, workspace, workspace_bytes,
                        stream, force, false, 1, q);
+}
+
+}  // extern "C"
+
+namespace smd {
+namespace {
+
+// The variant an options struct names (NULL: the defaults); SMD_OK or the
+// status of an invalid combination.
+int check_options(const smd_options_t* opt) {
+    if (opt == nullptr) return SMD_OK;
+    if (opt->reserved != 0) return SMD_ERR_SHAPE;
+    if (opt->query_type != SMD_QUERY_E4M3 && opt->query_type != SMD_QUERY_BF16) return SMD_ERR_SHAPE;
+    const int G = opt->row_group == 0 ? 1 : opt->row_group;
+    if (G != 1 && G != 2 && G != 4) return SMD_ERR_SHAPE;
+    if (opt->query_type == SMD_QUERY_BF16 && G != 1) return SMD_ERR_PLAN;
+    if (opt->library_scratch &&
+        (opt->workspace != nullptr || G != 1 || opt->query_type == SMD_QUERY_BF16))
+        return SMD_ERR_PLAN;
+    return SMD_OK;
+}
+
+int decode_opts(const void* q, const uint8_t* kv_pool, int64_t N, const int32_t* indices,
+                int32_t W, const int32_t* counts, int32_t B, int32_t H, float sm_scale,
+                float q_scale, float k_scale, uint16_t* out, float* lse,
+                const smd_options_t* opt, smd_stream_t stream, smd_plan_t* dry) {
+    const int rc = check_options(opt);
+    if (rc != SMD_OK) return rc;
+    const smd_options_t o = opt ? *opt : smd_options_t{};
+    const int G = o.row_group == 0 ? 1 : o.row_group;
+    const bool bf16 = o.query_type == SMD_QUERY_BF16;
+    void* ws = o.workspace;
+    int64_t ws_bytes = o.workspace_bytes;
+    // A plan query passes no pointers: a stand-in marks "a workspace is
+    // given" and "the query is bf16" (neither is read).
+    alignas(16) static unsigned char token[16];
+    if (dry != nullptr && ws == nullptr && ws_bytes > 0) ws = token;
+    if (dry != nullptr && q == nullptr) q = token;
+    const uint8_t* q8 = static_cast<const uint8_t*>(q);
+    return decode(q8, kv_pool, N, indices, W, counts, B, H, sm_scale, bf16 ? 1.0f : q_scale, k_scale,
+                  out, lse, o.status, ws, ws_bytes, stream, o.force, o.library_scratch != 0, G,
+                  bf16 ? static_cast<const uint16_t*>(q) : nullptr, dry);
+}
+
+}  // namespace
+}  // namespace smd
+
+extern "C" {
+
+int smd_decode(const void* q, const uint8_t* kv_pool, int64_t N, const int32_t* indices, int32_t W,
+               const int32_t* counts, int32_t B, int32_t H, float sm_scale, float q_scale,
+               float k_scale, uint16_t* out, float* lse, const smd_options_t* options,
+               smd_stream_t stream) {
+    return smd::decode_opts(q, kv_pool, N, indices, W, counts, B, H, sm_scale, q_scale, k_scale, out,
+                            lse, options, stream, nullptr);
+}
+
+int smd_decode_plan(int32_t B, int32_t H, int32_t W, const smd_options_t* options,
+                    smd_plan_t* plan) {
+    if (!plan) return SMD_ERR_NULL;
+    smd_plan_t p{};
+    const int rc = smd::decode_opts(nullptr, nullptr, 1, nullptr, W, nullptr, B, H, 1.f, 1.f, 1.f,
+                                    nullptr, nullptr, options, nullptr, &p);
+    if (rc == SMD_OK) *plan = p;
+    return rc;
+}
+
+int64_t smd_decode_workspace_bytes(int32_t B, int32_t H, int32_t W, const smd_options_t* options) {
+    if (smd::check_options(options) != SMD_OK) return 0;
+    const int G = options && options->row_group ? options->row_group : 1;
+    if (options && options->query_type == SMD_QUERY_BF16) return smd_workspace_bytes_bf16q(B, H, W);
+    if (G > 1) return smd_workspace_bytes_grouped(B, H, W, G);
+    if (options && options->force) return smd_workspace_bytes_ex(B, H, W, options->force);
+    return smd_workspace_bytes(B, H, W);
 }
 
 int64_t smd_workspace_bytes_bf16q(int32_t B, int32_t H, int32_t W) {
