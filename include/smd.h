@@ -474,7 +474,13 @@ typedef struct {
  * the call moves at most 16 MiB of host data (q, indices, counts, out, lse),
  * when the device call's plan is the spread kernel (a chunk of its rows would
  * leave SMs idle) or when it fills fewer than three waves of the device;
- * otherwise up to four, each still filling at least one and a half waves.
+ * otherwise up to four, each still filling at least one and a half waves,
+ * except on the tcgen05 cluster plan: there the rows are cut where the
+ * kernel's waves end (rows per wave = the clusters the device holds at once
+ * over the clusters a row takes; with no device, one cluster per `split`
+ * SMs): one wave, then chunks of two waves (more when eight chunks would
+ * not hold them), then the rows of the partial wave, if any; at most eight.
+ * An explicit opts->chunks cuts the row groups evenly instead.
  * Host only. Returns SMD_OK or SMD_ERR_SHAPE / SMD_ERR_NULL / SMD_ERR_PLAN. */
 int smd_plan_host(int32_t B, int32_t H, int32_t W, const smd_host_opts_t* opts, int32_t* chunks);
 

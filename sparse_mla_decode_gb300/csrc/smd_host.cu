@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "smd.h"
+#include "smd_internal.h"
 
 namespace smd {
 namespace {
@@ -85,13 +86,47 @@ int whole_plan(int B, int H, int W, const Opts& o, smd_plan_t* p) {
 
 // Where the staging buffers sit in the workspace, and how the rows are cut.
 struct Layout {
-    int chunks = 1, rows = 0;  // chunks of `rows` rows (the last may be shorter)
+    int chunks = 1, rows = 0;  // chunk c holds rows r0[c] .. r0[c + 1] - 1; rows: the most in one
+    int r0[kMaxChunks + 1] = {};
     int kernel = 0;            // the whole batch's plan (SMD_KERNEL_*)
     bool spread = false;       // the whole batch's plan is the spread kernel
     int64_t q_row = 0;         // bytes of one row of q
     int64_t off_q = 0, off_idx = 0, off_cnt = 0, off_out = 0, off_lse = 0, off_dws = 0;
     int64_t dws_bytes = 0, total = 0;
 };
+
+// Chunks cut at whole waves of the cluster kernel (rows per wave: the clusters
+// the device holds at once over the clusters a row takes): a one-wave chunk
+// first (its upload is short, so the first decode starts early), then
+// chunks of two waves, then the rows of the last, partial wave (its output
+// is small, so little is left to move out after the last decode). A chunk
+// that ended inside a wave would cost that wave's whole duration again.
+// Unchanged when fewer than three waves.
+void wave_chunks(int B, int G, const smd_plan_t& p, Layout* r) {
+    const int split = std::max(p.split, 1);
+    int clusters = tc_resident_clusters(split);
+    if (clusters <= 0) clusters = host_sm_count() / split;  // no device: every SM
+    const int per_row = std::max(p.grid_x / split, 1);     // clusters a row takes
+    const int rpw = clusters / per_row / G * G;              // rows per wave
+    if (rpw <= 0) return;
+    const int full = B / rpw, rem = B - full * rpw;
+    if (full < 3) return;
+    int w[kMaxChunks];  // waves per chunk (the partial wave apart)
+    int n = 0;
+    w[n++] = 1;
+    const int slots = kMaxChunks - 1 - (rem > 0 ? 1 : 0);  // chunks left for the middle waves
+    const int middle = full - 1;
+    const int per_chunk = std::max(2, (middle + slots - 1) / slots);
+    for (int left = middle; left > 0; left -= per_chunk) w[n++] = std::min(per_chunk, left);
+    int row = 0;
+    for (int c = 0; c < n; ++c) {
+        r->r0[c] = row;
+        row += w[c] * rpw;
+    }
+    r->chunks = n;
+    if (rem > 0) r->r0[r->chunks++] = row;
+    r->r0[r->chunks] = B;
+}
 
 int layout_of(int B, int H, int W, const Opts& o, Layout* L) {
     if (B < 0 || W < 0 || H <= 0 || H % 16 != 0) return SMD_ERR_SHAPE;
@@ -120,8 +155,11 @@ int layout_of(int B, int H, int W, const Opts& o, Layout* L) {
         const int groups = B / o.G;
         chunks = std::max(1, std::min(chunks, groups));
         const int per = (groups + chunks - 1) / chunks;  // groups per chunk
-        r.rows = per * o.G;
         r.chunks = (groups + per - 1) / per;
+        for (int c = 0; c <= r.chunks; ++c) r.r0[c] = std::min(B, c * per * o.G);
+        if (o.chunks == 0 && r.chunks > 1 && p.kernel == SMD_KERNEL_TC)
+            wave_chunks(B, o.G, p, &r);
+        for (int c = 0; c < r.chunks; ++c) r.rows = std::max(r.rows, r.r0[c + 1] - r.r0[c]);
         // A chunk is decoded by the device call the whole batch would use: with
         // the workspace when that is the spread kernel, else without one.
         r.dws_bytes = r.spread ? device_ws(r.rows, H, W, o) : 0;
@@ -305,9 +343,11 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
     auto chk = [&](cudaError_t e) { cuda_ok = cuda_ok && e == cudaSuccess; };
     int result = SMD_OK;
 
-    // Chunk c's copies in / out, queued on s.
+    // Chunk c's copies in / out, queued on s. The counts of all rows go in
+    // with chunk 0 and the LSE of the staged chunks comes back in one copy at
+    // the end (both are small): fewer calls for the host to issue.
     auto upload = [&](int c, cudaStream_t s) {
-        const int r0 = c * L.rows, nr = std::min(L.rows, B - r0);
+        const int r0 = L.r0[c], nr = L.r0[c + 1] - r0;
         if (q_pull != nullptr && c == 0) {
             const int64_t n16 = nr * L.q_row / 16;  // q rows are multiples of 16 bytes
             const int blocks = static_cast<int>(std::min<int64_t>((n16 + 255) / 256, 4 * host_sm_count()));
@@ -323,21 +363,27 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
             chk(cudaMemcpyAsync(const_cast<int32_t*>(didx) + static_cast<int64_t>(r0) * W,
                                 indices_host + static_cast<int64_t>(r0) * W,
                                 static_cast<int64_t>(nr) * W * 4, cudaMemcpyHostToDevice, s));
-        chk(cudaMemcpyAsync(const_cast<int32_t*>(dcnt) + r0, counts_host + r0,
-                            static_cast<int64_t>(nr) * 4, cudaMemcpyHostToDevice, s));
+        if (c == 0)
+            chk(cudaMemcpyAsync(const_cast<int32_t*>(dcnt), counts_host, static_cast<int64_t>(B) * 4,
+                                cudaMemcpyHostToDevice, s));
     };
     auto download = [&](int c, cudaStream_t s) {
         if (in_place(c)) return;  // the kernel wrote them in host memory
-        const int r0 = c * L.rows, nr = std::min(L.rows, B - r0);
+        const int r0 = L.r0[c], nr = L.r0[c + 1] - r0;
         chk(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(out_host) + r0 * out_row,
                             reinterpret_cast<const uint8_t*>(sout) + r0 * out_row, nr * out_row,
                             cudaMemcpyDeviceToHost, s));
-        chk(cudaMemcpyAsync(reinterpret_cast<uint8_t*>(lse_host) + r0 * lse_row,
-                            reinterpret_cast<const uint8_t*>(slse) + r0 * lse_row, nr * lse_row,
-                            cudaMemcpyDeviceToHost, s));
+    };
+    // The LSE of every staged chunk, once they are all decoded (on `stream`).
+    auto download_lse = [&]() {
+        int staged = 0;  // chunks 0 .. staged - 1 are staged (only the last can be in place)
+        while (staged < L.chunks && !in_place(staged)) ++staged;
+        const int nr = L.r0[staged];
+        if (nr > 0)
+            chk(cudaMemcpyAsync(lse_host, slse, nr * lse_row, cudaMemcpyDeviceToHost, cs));
     };
     auto decode = [&](int c) {
-        const int r0 = c * L.rows, nr = std::min(L.rows, B - r0);
+        const int r0 = L.r0[c], nr = L.r0[c + 1] - r0;
         const int32_t* ci = didx + static_cast<int64_t>(r0) * W;
         uint16_t* co = (in_place(c) ? m_out : sout) + static_cast<int64_t>(r0) * H * 512;
         float* cl = (in_place(c) ? m_lse : slse) + static_cast<int64_t>(r0) * H;
@@ -355,9 +401,14 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
                                         stream);
     };
 
-    // Chunk 0 moves in on `stream` itself; the later chunks follow it on the
-    // upload stream (one after another: concurrent uploads would share the
-    // bandwidth chunk 0 needs first) while the earlier chunks are decoded.
+    // Chunk 0 moves in on `stream` itself and is decoded there at once; each
+    // later chunk moves in on the upload stream (one after another, after
+    // chunk 0: concurrent uploads would share the bandwidth chunk 0 needs
+    // first) and is decoded on `stream` once it is in; every chunk but the
+    // last goes back on the download stream while the next one is decoded,
+    // the last on `stream`. The calls are issued in the order the device
+    // needs them (decode c before upload c + 1), so that the device never
+    // waits for the host to issue the next decode.
     upload(0, cs);
     if (L.chunks > 1) {
         const cudaEvent_t up0 = take();
@@ -365,16 +416,9 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
         chk(cudaStreamWaitEvent(eng->up, up0, 0));
         chk(cudaStreamWaitEvent(eng->down, up0, 0));
     }
-    cudaEvent_t up_done[kMaxChunks] = {};
-    for (int c = 1; c < L.chunks && cuda_ok; ++c) {
-        upload(c, eng->up);
-        up_done[c] = take();
-        chk(cudaEventRecord(up_done[c], eng->up));
-    }
-    // Decode chunk c once it is in; every chunk but the last goes back on the
-    // download stream while the next one is decoded, the last on `stream`.
+    cudaEvent_t up_done = nullptr;
     for (int c = 0; c < L.chunks && cuda_ok; ++c) {
-        if (c > 0) chk(cudaStreamWaitEvent(cs, up_done[c], 0));
+        if (c > 0) chk(cudaStreamWaitEvent(cs, up_done, 0));
         if (!cuda_ok) break;
         rc = decode(c);
         if (rc != SMD_OK) {
@@ -382,6 +426,9 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
             break;
         }
         if (c + 1 < L.chunks) {
+            upload(c + 1, eng->up);
+            up_done = take();
+            chk(cudaEventRecord(up_done, eng->up));
             const cudaEvent_t done = take();
             chk(cudaEventRecord(done, cs));
             chk(cudaStreamWaitEvent(eng->down, done, 0));
@@ -390,11 +437,11 @@ int smd_sparse_mla_decode_host(const void* q_host, const uint8_t* kv_pool, int64
             download(c, cs);
         }
     }
-    // Join: `stream` continues after the copy streams' last work.
+    if (result == SMD_OK && cuda_ok && !direct) download_lse();
+    // Join: `stream` continues after the download stream's last copy (every
+    // upload was waited for before its chunk's decode on `stream`).
     if (L.chunks > 1) {
-        const cudaEvent_t up_end = take(), down_end = take();
-        chk(cudaEventRecord(up_end, eng->up));
-        chk(cudaStreamWaitEvent(cs, up_end, 0));
+        const cudaEvent_t down_end = take();
         chk(cudaEventRecord(down_end, eng->down));
         chk(cudaStreamWaitEvent(cs, down_end, 0));
     }

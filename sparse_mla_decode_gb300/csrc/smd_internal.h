@@ -292,6 +292,9 @@ float* static_scratch(int* rc);
 
 // Dynamic shared memory of the tcgen05 kernel (bytes).
 int tc_smem_bytes();
+// Clusters of `split` tcgen05 CTAs (one per SM) the current device holds at
+// once; 0 when the query fails (no device).
+int tc_resident_clusters(int split);
 
 // A 2D tensor map over rows of 576 bytes (query or cache rows) with a box of
 // box_cols x box_rows (128 columns: 128-byte swizzle; 64: 64-byte swizzle),

@@ -778,6 +778,41 @@ constexpr int kMaxDevices = 64;
 
 int tc_smem_bytes() { return kSmemBytes; }
 
+int tc_resident_clusters(int split) {
+    static std::atomic<int> cached[kMaxDevices][kTcMaxSplit + 1];
+    int dev = 0;
+    if (split < 1 || split > kTcMaxSplit || cudaGetDevice(&dev) != cudaSuccess || dev < 0 ||
+        dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    int v = cached[dev][split].load();
+    if (v > 0) return v;
+    if (cudaFuncSetAttribute(tc_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(static_cast<unsigned>(split), 1, 1);
+    lc.blockDim = dim3(kTcThreads, 1, 1);
+    lc.dynamicSmemBytes = static_cast<size_t>(kSmemBytes);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_decode_kernel, &lc) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    cached[dev][split].store(n);
+    return n;
+}
+
 bool encode_row_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint32_t box_cols,
                     uint32_t box_rows) {
     return encode_map(out, ptr, rows, box_cols, box_rows);

@@ -364,7 +364,9 @@ def test_host_call_with_no_rows_is_a_no_op():
     (2, 16, 64, 1, False, 1),       # tiny: one small launch
     (5, 64, 256, 1, False, 1),      # latency
     (64, 128, 2048, 1, False, 1),   # DSA: the spread kernel takes the whole batch
-    (256, 128, 2048, 1, False, 4),  # throughput: 54 MB of host data, 1024 cluster CTAs: 4 x 64 rows
+    # throughput: 54 MB of host data over 1024 cluster CTAs, cut at whole waves
+    # (here, with no device, a wave is 152 / 4 = 38 rows): 38, 76, 76, 38, then 28
+    (256, 128, 2048, 1, False, 5),
     (128, 16, 8192, 4, False, 1),   # dense-as-sparse: 512 CTAs, but only 7.4 MB of host data
     (512, 16, 8192, 4, False, 1),   # four times the requests: the spread kernel takes the batch
     (256, 128, 2048, 1, True, 1),   # bf16 query on the spread kernel

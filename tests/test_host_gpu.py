@@ -158,10 +158,12 @@ def test_host_call_is_ordered_on_a_side_stream(cuda):
     assert_same(got, ref, "side stream")
 
 
-def test_throughput_config_in_four_chunks_sampled(cuda):
+def test_throughput_config_in_wave_chunks_sampled(cuda):
+    """The automatic plan cuts the 256 rows at whole waves of the cluster
+    kernel (a one-wave chunk, two-wave chunks, the partial wave's rows)."""
     from sparse_mla_decode_gb300 import binding
     case = inputs.config("throughput")
-    assert binding.smd_plan_host(case.B, case.H, case.W) == 4
+    assert 4 <= binding.smd_plan_host(case.B, case.H, case.W) <= 8
     out_g, lse_g = host_decode(case, cuda)
     rows = [0, 63, 64, 200, 255]
     out_o, lse_o = oracle_decode(case, rows)
