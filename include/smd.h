@@ -605,6 +605,25 @@ int smd_validate_indices(const int32_t* indices, int32_t W, const int32_t* count
  * or SMD_ERR_LAUNCH. */
 int smd_fp8_mma_probe(int32_t iters, int32_t* status, smd_stream_t stream, int32_t* ctas);
 
+/* Diagnostics of a tracing build (the library built with -DSMD_TRACE:
+ * sparse_mla_decode_gb300.build.build(trace=True), loaded by the binding when
+ * SMD_TRACE_BUILD=1; `python -m sparse_mla_decode_gb300.phases` prints the
+ * timeline). Each traced kernel (SMD_KERNEL_MMA, SMD_KERNEL_TC,
+ * SMD_KERNEL_TC_SPREAD) keeps a table of 8192 rows x 32 uint64 %globaltimer
+ * readings (ns) in device memory: row = CTA (blockIdx.y * gridDim.x +
+ * blockIdx.x; for the spread kernel 4 * blockIdx.x + round, rounds 0..3),
+ * slot = the phase that just ended (the phase list is in the kernel's
+ * source). A launch overwrites the stamps of the rows it runs.
+ *   smd_trace_enabled  1 in a tracing build, else 0.
+ *   smd_trace_read     copies the first n (<= 8192 * 32) stamps of `kernel`'s
+ *                      table to host memory; synchronous.
+ *   smd_trace_clear    zeroes the table; synchronous.
+ * Both return SMD_OK, SMD_ERR_PLAN (not a tracing build, or a kernel without
+ * a table), SMD_ERR_NULL, SMD_ERR_SHAPE or SMD_ERR_LAUNCH. */
+int smd_trace_enabled(void);
+int smd_trace_read(int32_t kernel, uint64_t* host, int32_t n);
+int smd_trace_clear(int32_t kernel);
+
 /* Static text for a status code. */
 const char* smd_status_str(int status);
 

@@ -7,6 +7,7 @@ the import of a decode function raises.
 from __future__ import annotations
 
 import ctypes
+import os
 import threading
 
 from . import build as _build
@@ -79,11 +80,13 @@ _DECODE_ARGS = [
 
 
 def lib() -> ctypes.CDLL:
-    """The loaded library (built in-tree on first use if missing or stale)."""
+    """The loaded library (built in-tree on first use if missing or stale):
+    libsmd.so, or its tracing variant when SMD_TRACE_BUILD=1 (per-phase
+    timestamps of the kernels; same results)."""
     global _lib
     with _lock:
         if _lib is None:
-            path = _build.build()
+            path = _build.build(trace=os.environ.get("SMD_TRACE_BUILD") == "1")
             so = ctypes.CDLL(path)
             so.smd_sparse_mla_decode.restype = ctypes.c_int
             so.smd_sparse_mla_decode.argtypes = _DECODE_ARGS
@@ -173,6 +176,12 @@ def lib() -> ctypes.CDLL:
             so.smd_decode_workspace_bytes.argtypes = [ctypes.c_int32] * 3 + [
                 ctypes.POINTER(SmdOptions)]
             so.smd_decode_workspace_bytes.restype = ctypes.c_int64
+            so.smd_trace_enabled.argtypes = []
+            so.smd_trace_enabled.restype = ctypes.c_int
+            so.smd_trace_read.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_int32]
+            so.smd_trace_read.restype = ctypes.c_int
+            so.smd_trace_clear.argtypes = [ctypes.c_int32]
+            so.smd_trace_clear.restype = ctypes.c_int
             so.smd_status_str.argtypes = [ctypes.c_int]
             so.smd_version.restype = ctypes.c_int
             so.smd_version.argtypes = []
@@ -181,7 +190,7 @@ def lib() -> ctypes.CDLL:
 
 
 def library_path() -> str:
-    return _build.LIB
+    return _build.TRACE_LIB if os.environ.get("SMD_TRACE_BUILD") == "1" else _build.LIB
 
 
 # ---- raw C-ABI calls (pointers as integers) -----------------------------------
@@ -429,6 +438,18 @@ def smd_decode_plan(B: int, H: int, W: int, options: SmdOptions | None = None) -
 def smd_decode_workspace_bytes(B: int, H: int, W: int, options: SmdOptions | None = None) -> int:
     ref = ctypes.byref(options) if options is not None else None
     return int(lib().smd_decode_workspace_bytes(B, H, W, ref))
+
+
+def smd_trace_enabled() -> int:
+    return int(lib().smd_trace_enabled())
+
+
+def smd_trace_read(kernel: int, host, n: int) -> int:
+    return int(lib().smd_trace_read(kernel, host, n))
+
+
+def smd_trace_clear(kernel: int) -> int:
+    return int(lib().smd_trace_clear(kernel))
 
 
 def smd_scale_log2(sm_scale: float, q_scale: float, k_scale: float) -> float:

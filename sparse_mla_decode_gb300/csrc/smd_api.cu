@@ -11,6 +11,7 @@
 
 #include "smd.h"
 #include "smd_internal.h"
+#include "smd_trace.cuh"
 #include "smd_ptx.cuh"
 #include "smd_tree.cuh"
 
@@ -911,5 +912,28 @@ const char* smd_status_str(int status) {
 }
 
 int smd_version(void) { return 100; }
+
+int smd_trace_enabled(void) {
+#ifdef SMD_TRACE
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+static int trace_copy(int32_t kernel, uint64_t* host, int32_t n, bool clear) {
+    if (!clear && host == nullptr) return SMD_ERR_NULL;
+    if (!clear && (n < 0 || n > smd::kTraceRows * smd::kTraceSlots)) return SMD_ERR_SHAPE;
+    switch (kernel) {
+        case SMD_KERNEL_MMA: return smd::mma_trace_copy(host, n, clear);
+        case SMD_KERNEL_TC: return smd::tc_trace_copy(host, n, clear);
+        case SMD_KERNEL_TC_SPREAD: return smd::tcs_trace_copy(host, n, clear);
+        default: return SMD_ERR_PLAN;
+    }
+}
+
+int smd_trace_read(int32_t kernel, uint64_t* host, int32_t n) { return trace_copy(kernel, host, n, false); }
+
+int smd_trace_clear(int32_t kernel) { return trace_copy(kernel, nullptr, 0, true); }
 
 }  // extern "C"

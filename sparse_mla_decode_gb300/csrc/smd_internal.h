@@ -292,6 +292,11 @@ float* static_scratch(int* rc);
 
 // Dynamic shared memory of the tcgen05 kernel (bytes).
 int tc_smem_bytes();
+// Copies (or zeroes, `clear`) a kernel's phase-stamp table of a tracing build
+// (smd_trace.cuh); SMD_ERR_PLAN in the normal build.
+int mma_trace_copy(uint64_t* host, int n, bool clear);
+int tc_trace_copy(uint64_t* host, int n, bool clear);
+int tcs_trace_copy(uint64_t* host, int n, bool clear);
 // Clusters of `split` tcgen05 CTAs (one per SM) the current device holds at
 // once; 0 when the query fails (no device).
 int tc_resident_clusters(int split);

@@ -38,6 +38,7 @@
 #include "smd_internal.h"
 #include "smd_ptx.cuh"
 #include "smd_qsplit.cuh"
+#include "smd_trace.cuh"
 #include "smd_tree.cuh"
 
 namespace smd {
@@ -108,6 +109,8 @@ __device__ __forceinline__ void release_tmem(uint32_t tbase) {
     }
 }
 
+SMD_TRACE_TABLE(g_trace_mma);
+
 // TR: some CTA of the plan holds several leaves (p.tree_tmem), so the kernel
 // keeps a subtree stack in TMEM; without it every CTA's keys form one leaf and
 // no TMEM is touched.
@@ -115,6 +118,10 @@ template <int T, bool QS, bool TR>
 __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     pdl_entry();
+    // Tracing build: phase ends of CTA `trow` (stamps 0 entry, 1 keys staged,
+    // 2 query landed, 3 logits, 4 row maximum, 5 PV, 6 partials in, 7 end).
+    const int trow = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x);
+    if (threadIdx.x == 0) SMD_STAMP(g_trace_mma, trow, 0);
     constexpr int CH = kHeadsPerTile * T;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -228,6 +235,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         for (int i = tid; i < mine; i += kMmaThreads) idx_s[i] = row_idx[first + i];
     const int32_t* my_idx = idx_s + (p.spec_idx ? first : 0);
     __syncthreads();
+    if (tid == 0) SMD_STAMP(g_trace_mma, trow, 1);
 
     const float neg_inf = -INFINITY;
     const float lam = p.a.scale_log2;
@@ -243,6 +251,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     const int a_col = 16 * (lane >> 4);
 
     mbar_wait(q_bar, 0, ok, status, p.budget_ns);
+    if (tid == 0) SMD_STAMP(g_trace_mma, trow, 2);
 
     // The maximum of each QK job's logits (heads g and g + 8 of its tile over
     // its keys), kept as the logits are written; warp w has job w (4T <= 16).
@@ -314,6 +323,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     }
 
     // ---- the row maximum over the cluster ------------------------------------
+    if (tid == 0) SMD_STAMP(g_trace_mma, trow, 3);
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         jmax[r] = fmaxf(jmax[r], __shfl_xor_sync(0xffffffffu, jmax[r], 1));
@@ -339,6 +349,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         }
         mbar_wait(max_bar, 0, ok, status, p.budget_ns, /*always=*/true);
     }
+    if (tid == 0) SMD_STAMP(g_trace_mma, trow, 4);
     for (int h = tid; h < CH; h += kMmaThreads) {
         float m = neg_inf;
         for (int pr = 0; pr < S; ++pr) m = fmaxf(m, maxima[pr * CH + h]);
@@ -461,6 +472,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
             gather_chunk(p, slot_s, my_idx + (c - NS) * kChunk, bars + 8 * s, kChunk, kLatent);
     }
 
+    if (tid == 0) SMD_STAMP(g_trace_mma, trow, 5);
     if (S == 1) {
         // No peers: BF16(acc * k_scale / total) straight from the registers
         // (the same operations as the merge below with one partial).
@@ -490,6 +502,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
         }
         cp_async_wait_all();  // after a failed wait, no copy may land once the CTA is gone
         if constexpr (TR) release_tmem(tbase);
+        if (tid == 0) SMD_STAMP(g_trace_mma, trow, 7);
         return;
     }
 
@@ -526,6 +539,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     }
     mbar_wait(in_bar, 0, ok, status, p.budget_ns, /*always=*/true);
     __syncthreads();  // this CTA's own partial (plain stores)
+    if (tid == 0) SMD_STAMP(g_trace_mma, trow, 6);
 
     // ---- merge by the leaf tree; BF16(sum * k_scale / total) -----------------
     // CTA src holds the subtree of leaves [src lpc, src lpc + lpc): absent if
@@ -561,6 +575,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     }
     cp_async_wait_all();
     if constexpr (TR) release_tmem(tbase);
+    if (tid == 0) SMD_STAMP(g_trace_mma, trow, 7);
 }
 
 // Function attributes are set once per device and kernel (and again only when
@@ -619,6 +634,8 @@ int launch_t(const MmaParams& prm, const MmaConfig& cfg, const CallArgs& a, cuda
 }
 
 }  // namespace
+
+SMD_TRACE_COPY_FN(mma_trace_copy, g_trace_mma)
 
 int launch_mma(const CallArgs& a, const MmaConfig& cfg, cudaStream_t stream) {
     MmaParams prm{};

@@ -45,6 +45,7 @@
 #include "smd_internal.h"
 #include "smd_ptx.cuh"
 #include "smd_tc_common.cuh"
+#include "smd_trace.cuh"
 #include "smd_tree.cuh"
 
 namespace smd {
@@ -79,6 +80,13 @@ constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = 3, kBarS = 5, kBarP = 9, kBar
 struct TcMaps {
     CUtensorMap q, q_tail, kv, kv_tail;
 };
+
+// Tracing build: phase ends of CTA blockIdx.y * gridDim.x + blockIdx.x
+// (stamps 0 entry, 1 keys staged, 2 own maximum, 3 row maximum, 4 P, 5 O,
+// 6 partials pushed, 7 partials in, 8 merged, 9 end).
+SMD_TRACE_TABLE(g_trace_tc);
+
+__device__ __forceinline__ int trace_row() { return static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x); }
 
 struct TcParams {
     CallArgs a;
@@ -174,6 +182,7 @@ __device__ __forceinline__ void producer_a(const TcMaps& maps, const tcc::Pipe& 
     }
     for (int i = r.mine + t; i < kTcMaxKeys; i += kProducerThreads) idx_s[i] = 0;
     asm volatile("bar.sync 1, %0;" ::"r"(kProducerThreads) : "memory");
+    if (t == 0) SMD_STAMP(g_trace_tc, trace_row(), 1);
     uint32_t seen[2] = {0u, 0u};
     tcc::gather_pass_a(maps.kv, maps.kv_tail, pp, 0, r.nch, seen, ok);
 }
@@ -213,6 +222,7 @@ __device__ __forceinline__ void row_max(const TcParams& p, uint8_t* smem, uint32
                 if (j < lim) m = fmaxf(m, lam * v[j]);
         }
     }
+    if (h == 0) SMD_STAMP(g_trace_tc, trace_row(), 2);
     if (S > 1) {
         cluster_wait();  // every peer's barriers are initialised
         maxima[split * 128 + h] = m;
@@ -231,6 +241,7 @@ __device__ __forceinline__ void row_max(const TcParams& p, uint8_t* smem, uint32
         for (int pr = 0; pr < S; ++pr) m = fmaxf(m, maxima[pr * 128 + h]);
     }
     rowmax[h] = m;
+    if (h == 0) SMD_STAMP(g_trace_tc, trace_row(), 3);
 }
 
 // ---- all 16 warps: P ---------------------------------------------------------------
@@ -365,6 +376,7 @@ __device__ __forceinline__ void exchange_dsmem(const TcParams& p, uint8_t* smem,
                             make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]), rfull);
         }
     }
+    if (threadIdx.x == 0) SMD_STAMP(g_trace_tc, trace_row(), 6);
     const bool p0 = leaf_present(split, n), p1 = leaf_present(split ^ 1, n);
     float acc[NP][32];
 #pragma unroll
@@ -400,9 +412,11 @@ __device__ __forceinline__ void exchange_dsmem(const TcParams& p, uint8_t* smem,
         }
         pa = pa || p2 || p3;
     }
+    if (threadIdx.x == 0) SMD_STAMP(g_trace_tc, trace_row(), 7);
     mbar_wait(bars + 8 * kBarIn, 0, ok, status, p.budget_ns, /*always=*/true);
     ok = __syncthreads_and(ok) != 0;  // also: every inbox is consumed
     if (!ok) return;
+    if (threadIdx.x == 0) SMD_STAMP(g_trace_tc, trace_row(), 8);
     // The sums by the same tree.
     float total = tree_add(sums[split * 128 + h], p0, sums[(split ^ 1) * 128 + h], p1);
     if (S == 4) {
@@ -597,6 +611,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_decode_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     pdl_entry();
+    if (threadIdx.x == 0) SMD_STAMP(g_trace_tc, trace_row(), 0);
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t base = smem_addr(smem);
     const uint32_t bars = base + kOffBars;
@@ -681,6 +696,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     ok = __syncthreads_and(ok) != 0;
     tc_fence_after();
     p_phase(p, smem, bars, tmem, b, split, ok);
+    if (threadIdx.x == 0) SMD_STAMP(g_trace_tc, trace_row(), 4);
     if (warp < 8) {
         tcc::gather_pass_b(maps.kv, pp, r.nch, ok);
     } else if (warp == 8) {
@@ -691,9 +707,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_wait(bars + 8 * kBarO, 0, ok, p.a.status, p.budget_ns);
     tc_fence_after();
     ok = __syncthreads_and(ok) != 0;  // the partial sums of P are visible; one verdict
+    if (threadIdx.x == 0) SMD_STAMP(g_trace_tc, trace_row(), 5);
     finish(p, smem, bars, tmem, b, group, split, ok);
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) SMD_STAMP(g_trace_tc, trace_row(), 9);
     if (warp == 8) {
         tc_fence_after();
         tmem_free(tmem, 512);
@@ -775,6 +793,8 @@ bool encode_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint32_t box_c
 constexpr int kMaxDevices = 64;
 
 }  // namespace
+
+SMD_TRACE_COPY_FN(tc_trace_copy, g_trace_tc)
 
 int tc_smem_bytes() { return kSmemBytes; }
 

@@ -42,6 +42,7 @@
 #include "smd_ptx.cuh"
 #include "smd_qsplit.cuh"
 #include "smd_tc_common.cuh"
+#include "smd_trace.cuh"
 #include "smd_tree.cuh"
 
 namespace smd {
@@ -69,6 +70,17 @@ constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = 3, kBarFreeB = 5, kBarS = 7, 
               kBarO = 12;
 
 constexpr int kProducerThreads = 256;
+
+// Tracing build: phase ends of round r < 4 of CTA blockIdx.x, row 4 blockIdx.x
+// + r (stamps 0 item start, 1 keys staged, 2 own maximum, 3 row maximum over
+// the unit's pieces, 4 P, 5 O, 6 partials written, 7 partials in, 8 end; and
+// within the merge, 9 sums merged, 10 columns merged, 11 output staged).
+SMD_TRACE_TABLE(g_trace_tcs);
+
+__device__ __forceinline__ int trace_row(int item, int grid) {
+    const int r = item / grid;
+    return r < 4 ? static_cast<int>(blockIdx.x) * 4 + r : -1;
+}
 
 struct TcsMaps {
     CUtensorMap q, q_tail, kv, kv_tail;
@@ -108,6 +120,7 @@ __device__ __forceinline__ float lam_of(const TcsParams& p, int64_t row0, int h)
     if (p.lamh == nullptr) return p.a.scale_log2;
     return h < p.lanes ? p.lamh[row0 + h] : 0.f;
 }
+
 
 __device__ __forceinline__ float4 ld_cg_v4(const float* p) {
     float4 v;
@@ -342,6 +355,7 @@ __device__ __forceinline__ void producer_a(const TcsMaps& maps, const TcsParams&
     idx_s[t] = v[0];
     idx_s[t + kProducerThreads] = v[1];
     asm volatile("bar.sync 1, %0;" ::"r"(kProducerThreads) : "memory");
+    if (t == 0) SMD_STAMP(g_trace_tcs, trace_row(it.item0 + it.j, p.grid), 1);
     uint32_t seen[2] = {0u, 0u};
     if (p.G == 1) {
         tcc::gather_pass_a(maps.kv, maps.kv_tail, pp, 0, it.nch, seen, ok);
@@ -382,8 +396,10 @@ __device__ __forceinline__ void row_max(const TcsParams& p, uint8_t* smem, uint3
         }
     }
     float* rowmax = reinterpret_cast<float*>(smem + kOffRowMax);
+    if (h == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 2);
     if (it.s == 1) {
         rowmax[h] = m;
+        if (h == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 3);
         return;
     }
     float* ws_max = reinterpret_cast<float*>(p.ws_base + p.ws.max);
@@ -398,6 +414,7 @@ __device__ __forceinline__ void row_max(const TcsParams& p, uint8_t* smem, uint3
     for (int jj = 0; jj < it.s; ++jj)
         mr = fmaxf(mr, ld_cg_f32(ws_max + static_cast<int64_t>(it.item0 + jj) * kTcHeads + h));
     rowmax[h] = mr;
+    if (h == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 3);
 }
 
 // ---- all 16 warps: P ---------------------------------------------------------------
@@ -494,6 +511,27 @@ __device__ __forceinline__ void merge_cols(const float* part, int64_t item0, int
     }
 }
 
+// Groups of cp.async copies (16-byte global -> shared, through the load/store
+// unit): close the group this thread has issued since the last commit; wait
+// until at most N of its groups are still in flight.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// 4 consecutive TMEM columns of this thread's lane (warp-wide).
+__device__ __forceinline__ float4 tmem_ld4(uint32_t taddr) {
+    uint32_t r[4];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    return make_float4(__uint_as_float(r[0]), __uint_as_float(r[1]), __uint_as_float(r[2]),
+                       __uint_as_float(r[3]));
+}
+
 // ---- all 16 warps: exchange, merge, output ---------------------------------------
 // Warp w serves TMEM lane quarter w % 4 (thread = head h) and column group
 // cg = w / 4.
@@ -572,6 +610,7 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
         __threadfence();  // after the barrier: orders every thread's stores above
         st_release_u64(fpart + static_cast<int64_t>(item) * kTcsMaxPieces + t, p.token);
     }
+    if (t == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 6);
 
     // 2. The other items' partials of this slice (each flag is read here only,
     // so it is zeroed once seen).
@@ -581,6 +620,7 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
         *f = 0ull;
     }
     ok = __syncthreads_and(ok) != 0;
+    if (t == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 7);
     // Every item of the unit has read the maxima (it raised its flags for the
     // owners after that): this item's max flag is consumed.
     if (t == 0) fmax[item] = 0ull;
@@ -594,28 +634,94 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
         return k == 0 ? l : ld_cg_f32(sums + static_cast<int64_t>(it.item0 + (j ^ k)) * kTcHeads + h);
     }, j, np);
     const float inv = total > 0.f ? p.a.k_scale / total : 0.f;
-    const int mask = stage_mask(CW / 8);
-    for (int q = cg; 16 * q < CW; q += 4) {
-        const int col = c0 + 16 * q;
-        float own[16], acc[16];
-        if (have_o) {
-            tmem_ld16(lane_base + col, own);
-        } else {
+    if (t == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 9);
+    if (s <= 4) {
+        // Up to four pieces: each thread's 16-column pieces, the peers' values
+        // loaded into registers (at most three loads per four columns), the
+        // BF16 tile staged in the dead ring and stored by whole rows.
+        uint8_t* stage = smem + kOffRing;
+        const int mask = stage_mask(CW / 8);
+        for (int q = cg; 16 * q < CW; q += 4) {
+            const int col = c0 + 16 * q;
+            float own[16], acc[16];
+            if (have_o) {
+                tmem_ld16(lane_base + col, own);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) own[i] = 0.f;
-        }
-        if (h < p.lanes) {
-            merge_cols(part, it.item0, j, P, np, h, col, own, acc);
-        } else {
+                for (int i = 0; i < 16; ++i) own[i] = 0.f;
+            }
+            if (h < p.lanes) {
+                merge_cols(part, it.item0, j, P, np, h, col, own, acc);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = 0.f;  // padding lanes are never stored
+                for (int i = 0; i < 16; ++i) acc[i] = 0.f;  // padding lanes are never stored
+            }
+            stage16(stage, CW * 2, mask, h, col - c0, acc, inv);
         }
-        stage16(stage, CW * 2, mask, h, col - c0, acc, inv);
+        if (t == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 10);
+        if (j == 0 && cg == 0 && h < p.lanes)
+            *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f : -INFINITY;
+        __syncthreads();
+        if (t == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 11);
+        flush(stage, CW * 2, mask, p.lanes, oblock + c0);
+        return;
     }
+    // More pieces (narrow slices, many loads per column): the peers' slices
+    // come into shared memory first (cp.async, which holds no register while
+    // in flight), in batches of BC columns over two buffers that cover the
+    // dead query, P tiles and ring, so that a whole batch is in flight at
+    // once; the tree then reads them from there, and the BF16 output goes
+    // straight to global memory (8 bytes per lane and 4 columns).
+    constexpr int kLandBytes = 3 * kTile / 2 / 16 * 16;  // one of the two buffers
+    const int peers = s - 1;
+    int BC = (kLandBytes / (peers * kTcHeads * 16)) * 4;  // columns per batch (multiple of 4)
+    BC = min(BC, CW);
+    const int nbatch = (CW + BC - 1) / BC;
+    const uint32_t land0 = smem_addr(smem);
+    auto issue = [&](int bt) {
+        const int cb = bt * BC, g4 = min(BC, CW - cb) / 4;  // 4-column units of the batch
+        const int units = peers * g4 * kTcHeads;
+        const uint32_t dst0 = land0 + (bt & 1) * kLandBytes;
+        for (int e = t; e < units; e += kTcThreads) {
+            const int slot = e / (g4 * kTcHeads), rem = e - slot * g4 * kTcHeads;
+            const int g = rem / kTcHeads, hh = rem - g * kTcHeads;
+            const int src = slot < j ? slot : slot + 1;
+            const float* from = part + (it.item0 + src) * kPartFloats +
+                                ((((c0 + cb) >> 2) + g) * kTcHeads + hh) * 4;
+            cp_async16(dst0 + ((slot * g4 + g) * kTcHeads + hh) * 16, from);
+        }
+        cp_async_commit();
+    };
+    issue(0);
+    if (nbatch > 1) issue(1);
+    uint16_t* orow = p.a.out + (it.row0 + h) * kLatent;
+    for (int bt = 0; bt < nbatch; ++bt) {
+        if (bt + 1 < nbatch)
+            cp_async_wait_group<1>();
+        else
+            cp_async_wait_group<0>();
+        __syncthreads();  // batch bt has landed for every thread
+        const int cb = bt * BC, g4 = min(BC, CW - cb) / 4;
+        const float4* land = reinterpret_cast<const float4*>(smem + (bt & 1) * kLandBytes);
+        for (int g = cg; g < g4; g += 4) {  // warp-uniform
+            const int col = c0 + cb + 4 * g;
+            const float4 own = have_o ? tmem_ld4(lane_base + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if (h >= p.lanes) continue;  // padding lanes are never stored
+            const float4 acc = tree_xor_n<float4>(P, [&](int k) {
+                if (k == 0) return own;
+                const int src = j ^ k;
+                return land[((src < j ? src : src - 1) * g4 + g) * kTcHeads + h];
+            }, j, np);
+            *reinterpret_cast<uint2*>(orow + col) =
+                make_uint2(bf16x2(acc.x * inv, acc.y * inv), bf16x2(acc.z * inv, acc.w * inv));
+        }
+        __syncthreads();  // buffer bt & 1 is free
+        if (bt + 2 < nbatch) issue(bt + 2);
+    }
+    if (t == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 10);
     if (j == 0 && cg == 0 && h < p.lanes)
         *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f : -INFINITY;
-    __syncthreads();
-    flush(stage, CW * 2, mask, p.lanes, oblock + c0);
+    if (t == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 11);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -651,6 +757,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (threadIdx.x == 0) init_bars(bars, true);
             __syncthreads();
         }
+        if (threadIdx.x == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 0);
         if (threadIdx.x == 0) {
             // (inject_stall: the query barrier also expects 16 bytes nobody
             // sends, so its bounded wait runs out; a test hook.)
@@ -679,6 +786,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ok = __syncthreads_and(ok) != 0;  // every QK is complete; the row maxima are here
         tc_fence_after();
         p_phase(p, smem, bars, tmem, it, ok);
+        if (threadIdx.x == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 4);
         if (warp < 8) {
             tcc::gather_pass_b(maps.kv, pp, it.nch, ok);
         } else if (warp == 8) {
@@ -688,9 +796,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_wait(bars + 8 * kBarO, 0, ok, p.a.status, p.budget_ns);
         tc_fence_after();
         ok = __syncthreads_and(ok) != 0;  // the partial sums of P are visible; one verdict
+        if (threadIdx.x == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 5);
         finish(p, smem, tmem, it, item, ok);
         tc_fence_before();  // every TMEM read of this item precedes the next item's MMAs
         __syncthreads();
+        if (threadIdx.x == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 8);
     }
     if (warp == 8) {
         tc_fence_after();
@@ -711,6 +821,8 @@ __global__ void __launch_bounds__(256) tcs_qsplit_kernel(const uint16_t* q16, in
 }  // namespace
 
 // ---- host ------------------------------------------------------------------------
+
+SMD_TRACE_COPY_FN(tcs_trace_copy, g_trace_tcs)
 
 int tcs_smem_bytes() { return kSmemBytes; }
 

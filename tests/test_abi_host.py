@@ -441,3 +441,17 @@ def test_validate_indices_argument_checks(kw, code):
     a.update(kw)
     assert smd.smd_validate_indices(a["idx"], a["W"], a["counts"], a["B"], a["N"], a["status"],
                                     None) == code
+
+
+def test_trace_calls_in_the_normal_build_report_no_tables():
+    """The phase stamps exist only in the tracing build (-DSMD_TRACE); the
+    normal library answers every trace call without touching a device."""
+    import numpy as np
+    assert smd.smd_trace_enabled() == 0
+    buf = np.zeros(64, np.uint64)
+    for kernel in (smd.SMD_KERNEL_MMA, smd.SMD_KERNEL_TC, smd.SMD_KERNEL_TC_SPREAD,
+                   smd.SMD_KERNEL_GROUP, smd.SMD_KERNEL_TC_GROUP):
+        assert smd.smd_trace_clear(kernel) == smd.SMD_ERR_PLAN
+        assert smd.smd_trace_read(kernel, buf.ctypes.data, buf.size) == smd.SMD_ERR_PLAN
+    assert smd.smd_trace_read(smd.SMD_KERNEL_TC, None, 4) == smd.SMD_ERR_NULL
+    assert smd.smd_trace_read(smd.SMD_KERNEL_TC, buf.ctypes.data, 8192 * 32 + 1) == smd.SMD_ERR_SHAPE
