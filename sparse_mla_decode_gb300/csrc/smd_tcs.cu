@@ -639,7 +639,6 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
         // Up to four pieces: each thread's 16-column pieces, the peers' values
         // loaded into registers (at most three loads per four columns), the
         // BF16 tile staged in the dead ring and stored by whole rows.
-        uint8_t* stage = smem + kOffRing;
         const int mask = stage_mask(CW / 8);
         for (int q = cg; 16 * q < CW; q += 4) {
             const int col = c0 + 16 * q;
@@ -668,11 +667,14 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
     }
     // More pieces (narrow slices, many loads per column): the peers' slices
     // come into shared memory first (cp.async, which holds no register while
-    // in flight), in batches of BC columns over two buffers that cover the
-    // dead query, P tiles and ring, so that a whole batch is in flight at
-    // once; the tree then reads them from there, and the BF16 output goes
-    // straight to global memory (8 bytes per lane and 4 columns).
-    constexpr int kLandBytes = 3 * kTile / 2 / 16 * 16;  // one of the two buffers
+    // in flight), in batches of BC columns over two buffers in the dead
+    // query, P tiles and ring, so that a whole batch is in flight at once;
+    // the tree then reads them from there. The BF16 tile is staged behind
+    // the buffers and stored by whole rows (out may be mapped host memory).
+    constexpr int kStageMax = kTcHeads * 112 * 2;  // the widest slice of 5 or more pieces
+    constexpr int kLandBytes = (3 * kTile - kStageMax) / 2 / 16 * 16;  // one of the two buffers
+    uint8_t* tile = smem + 2 * kLandBytes;
+    const int mask = stage_mask(CW / 8);
     const int peers = s - 1;
     int BC = (kLandBytes / (peers * kTcHeads * 16)) * 4;  // columns per batch (multiple of 4)
     BC = min(BC, CW);
@@ -694,7 +696,6 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
     };
     issue(0);
     if (nbatch > 1) issue(1);
-    uint16_t* orow = p.a.out + (it.row0 + h) * kLatent;
     for (int bt = 0; bt < nbatch; ++bt) {
         if (bt + 1 < nbatch)
             cp_async_wait_group<1>();
@@ -712,16 +713,19 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
                 const int src = j ^ k;
                 return land[((src < j ? src : src - 1) * g4 + g) * kTcHeads + h];
             }, j, np);
-            *reinterpret_cast<uint2*>(orow + col) =
+            const int cs = col - c0;  // column in the slice: half (cs >> 2) & 1 of chunk cs >> 3
+            *reinterpret_cast<uint2*>(tile + h * (CW * 2) + ((((cs >> 3) ^ (h & mask))) << 4) +
+                                      ((cs >> 2) & 1) * 8) =
                 make_uint2(bf16x2(acc.x * inv, acc.y * inv), bf16x2(acc.z * inv, acc.w * inv));
         }
-        __syncthreads();  // buffer bt & 1 is free
+        __syncthreads();  // buffer bt & 1 is free (after the last batch: the tile is staged)
         if (bt + 2 < nbatch) issue(bt + 2);
     }
     if (t == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 10);
     if (j == 0 && cg == 0 && h < p.lanes)
         *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f : -INFINITY;
     if (t == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 11);
+    flush(tile, CW * 2, mask, p.lanes, oblock + c0);
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
