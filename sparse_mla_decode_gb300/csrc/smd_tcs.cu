@@ -680,13 +680,16 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
     BC = min(BC, CW);
     const int nbatch = (CW + BC - 1) / BC;
     const uint32_t land0 = smem_addr(smem);
+    // Only the lanes of real query rows are copied (the peers never write the
+    // padding lanes' partials, so those lines are not in L2).
+    const int lanes = p.lanes;
     auto issue = [&](int bt) {
         const int cb = bt * BC, g4 = min(BC, CW - cb) / 4;  // 4-column units of the batch
-        const int units = peers * g4 * kTcHeads;
+        const int units = peers * g4 * lanes;
         const uint32_t dst0 = land0 + (bt & 1) * kLandBytes;
         for (int e = t; e < units; e += kTcThreads) {
-            const int slot = e / (g4 * kTcHeads), rem = e - slot * g4 * kTcHeads;
-            const int g = rem / kTcHeads, hh = rem - g * kTcHeads;
+            const int slot = e / (g4 * lanes), rem = e - slot * g4 * lanes;
+            const int g = rem / lanes, hh = rem - g * lanes;
             const int src = slot < j ? slot : slot + 1;
             const float* from = part + (it.item0 + src) * kPartFloats +
                                 ((((c0 + cb) >> 2) + g) * kTcHeads + hh) * 4;
