@@ -224,9 +224,8 @@ constexpr int kTcsMaxPieces = 32;   // items per unit: W <= 32 * 512
 
 // Byte offsets of the workspace parts for `items` item slots.
 struct TcsWorkspace {
-    int64_t flag_max;   // [items] u64: the item's maxima are published
     int64_t flag_part;  // [items][kTcsMaxPieces] u64: its partial for owner j is written
-    int64_t max;        // [items][128] fp32
+    int64_t max;        // [items][128] u64: the call's tag (high half) and an fp32 maximum (low)
     int64_t sum;        // [items][128] fp32
     int64_t part;       // [items][128 x 512] fp32 partials, 16-byte units head-innermost
     int64_t q_hi, q_lo; // [qrows][576] E4M3: the split bf16 query (qrows = B * H, else 0)
@@ -239,12 +238,10 @@ __host__ __device__ inline int64_t align_up64(int64_t x, int64_t a) { return (x 
 __host__ __device__ inline TcsWorkspace tcs_workspace(int64_t items, int64_t qrows = 0) {
     TcsWorkspace w{};
     int64_t o = 0;
-    w.flag_max = o;
-    o = align_up64(o + items * 8, 256);
     w.flag_part = o;
     o = align_up64(o + items * kTcsMaxPieces * 8, 256);
     w.max = o;
-    o = align_up64(o + items * 128 * 4, 256);
+    o = align_up64(o + items * 128 * 8, 256);
     w.sum = o;
     o = align_up64(o + items * 128 * 4, 256);
     w.part = o;

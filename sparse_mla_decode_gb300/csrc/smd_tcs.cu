@@ -19,16 +19,18 @@
 // chunks into a two-slot ring, S = Q K^T into TMEM, P in E4M3 straight into
 // the swizzled operand layout, O = P V into TMEM). The row maximum and the
 // partials go through global memory (L2):
-//   1. each item publishes its 128 maxima and raises its "max" flag; it waits
-//      for the unit's other items' flags and takes the maximum over them;
+//   1. each item publishes its 128 maxima, each as a 64-bit word tagged with
+//      the call (so the value and its readiness arrive in one load), and
+//      takes the maximum over the unit's items as their tags appear;
 //   2. after PV it writes its FP32 partials of the other items' columns
 //      (owner j of s owns columns [16 floor(32 j / s), 16 floor(32 (j+1) / s)))
 //      and its sums, and raises one flag per owner;
 //   3. each owner waits for its flags, merges the pieces by the pairwise tree
 //      (its own partial first, then pieces j ^ 1, j ^ 2, ...), and writes BF16
 //      out (and LSE, owner 0).
-// A flag holds the call's 64-bit token, so stale words from earlier calls
-// never pass; the reader of a flag zeroes it once it is consumed.
+// A flag holds the call's 64-bit token (a maximum's word its low half), so
+// stale words from earlier calls never pass; the reader of a flag zeroes it
+// once it is consumed, an item its maxima once every peer has read them.
 // Every wait (copies, tensor core, peer flags) is bounded.
 #include <cuda.h>
 
@@ -145,6 +147,20 @@ __device__ __forceinline__ void st_v4(float* p, float4 v) {
 __device__ __forceinline__ void st_release_u64(uint64_t* p, uint64_t v) {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// The tag a maximum's word carries: the low half of the call's token, never 0
+// (a consumed word is zeroed).
+__device__ __forceinline__ uint32_t max_tag(uint64_t token) { return static_cast<uint32_t>(token) | 1u; }
 
 __device__ __forceinline__ uint64_t ld_acquire_u64(const uint64_t* p) {
     uint64_t v;
@@ -402,17 +418,31 @@ __device__ __forceinline__ void row_max(const TcsParams& p, uint8_t* smem, uint3
         if (h == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 3);
         return;
     }
-    float* ws_max = reinterpret_cast<float*>(p.ws_base + p.ws.max);
-    uint64_t* flag_max = reinterpret_cast<uint64_t*>(p.ws_base + p.ws.flag_max);
-    ws_max[static_cast<int64_t>(item) * kTcHeads + h] = m;  // published even after a failure
-    __threadfence();
-    asm volatile("bar.sync 2, 128;" ::: "memory");
-    if (h == 0) st_release_u64(flag_max + item, p.token);
-    if (h < it.s) wait_flag(flag_max + it.item0 + h, p.token, ok, p.a.status, p.budget_ns);
-    asm volatile("bar.sync 2, 128;" ::: "memory");
-    float mr = -INFINITY;
-    for (int jj = 0; jj < it.s; ++jj)
-        mr = fmaxf(mr, ld_cg_f32(ws_max + static_cast<int64_t>(it.item0 + jj) * kTcHeads + h));
+    // Head h's maximum as one 64-bit word: the tag and the value's bits, so a
+    // reader that sees the tag sees the value (one single-copy-atomic store,
+    // no fence, no separate flag); published even after a failure. Then
+    // every other item's word for head h, taken as its tag appears (bounded).
+    uint64_t* ws_max = reinterpret_cast<uint64_t*>(p.ws_base + p.ws.max);
+    const uint32_t tag = max_tag(p.token);
+    st_relaxed_u64(ws_max + static_cast<int64_t>(item) * kTcHeads + h,
+                   (static_cast<uint64_t>(tag) << 32) | __float_as_uint(m));
+    float mr = m;
+    uint32_t pending = (it.s >= 32 ? 0xffffffffu : ((1u << it.s) - 1u)) & ~(1u << it.j);
+    const uint64_t t0 = globaltimer();
+    while (pending != 0u && ok) {
+        for (uint32_t rest = pending; rest != 0u; rest &= rest - 1u) {
+            const int jj = __ffs(rest) - 1;
+            const uint64_t w = ld_relaxed_u64(ws_max + static_cast<int64_t>(it.item0 + jj) * kTcHeads + h);
+            if (static_cast<uint32_t>(w >> 32) == tag) {
+                mr = fmaxf(mr, __uint_as_float(static_cast<uint32_t>(w)));
+                pending &= ~(1u << jj);
+            }
+        }
+        if (pending != 0u && globaltimer() - t0 > p.budget_ns) {
+            if (p.a.status != nullptr) atomicCAS(p.a.status, 0, kStatusTimeout);
+            ok = false;
+        }
+    }
     rowmax[h] = mr;
     if (h == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 3);
 }
@@ -580,7 +610,7 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
     float* part = reinterpret_cast<float*>(p.ws_base + p.ws.part);
     float* sums = reinterpret_cast<float*>(p.ws_base + p.ws.sum);
     uint64_t* fpart = reinterpret_cast<uint64_t*>(p.ws_base + p.ws.flag_part);
-    uint64_t* fmax = reinterpret_cast<uint64_t*>(p.ws_base + p.ws.flag_max);
+    uint64_t* ws_max = reinterpret_cast<uint64_t*>(p.ws_base + p.ws.max);
 
     // 1. This item's partials of the other owners' columns (16-byte unit u of
     // head h at (u * 128 + h): one warp-wide store covers 512 contiguous bytes),
@@ -622,8 +652,8 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
     ok = __syncthreads_and(ok) != 0;
     if (t == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 7);
     // Every item of the unit has read the maxima (it raised its flags for the
-    // owners after that): this item's max flag is consumed.
-    if (t == 0) fmax[item] = 0ull;
+    // owners after that): this item's maxima are consumed.
+    if (t < kTcHeads) ws_max[static_cast<int64_t>(item) * kTcHeads + t] = 0ull;
     if (!ok) return;
 
     // 3. Merge: the pairwise tree over the unit's pieces in the order j ^ k.
