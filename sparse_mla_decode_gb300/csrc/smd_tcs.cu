@@ -706,13 +706,15 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
     uint8_t* tile = smem + 2 * kLandBytes;
     const int mask = stage_mask(CW / 8);
     const int peers = s - 1;
-    int BC = (kLandBytes / (peers * kTcHeads * 16)) * 4;  // columns per batch (multiple of 4)
-    BC = min(BC, CW);
-    const int nbatch = (CW + BC - 1) / BC;
-    const uint32_t land0 = smem_addr(smem);
     // Only the lanes of real query rows are copied (the peers never write the
-    // padding lanes' partials, so those lines are not in L2).
+    // padding lanes' partials, so those lines are not in L2) and landed, so
+    // a batch holds 128 / lanes times the columns of a full tile. The
+    // batches are of equal width (a multiple of 4 columns).
     const int lanes = p.lanes;
+    const int bc_max = (kLandBytes / (peers * lanes * 16)) * 4;  // columns a buffer holds
+    const int nbatch = (CW + bc_max - 1) / bc_max;
+    const int BC = (CW + 4 * nbatch - 1) / (4 * nbatch) * 4;
+    const uint32_t land0 = smem_addr(smem);
     auto issue = [&](int bt) {
         const int cb = bt * BC, g4 = min(BC, CW - cb) / 4;  // 4-column units of the batch
         const int units = peers * g4 * lanes;
@@ -723,7 +725,7 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
             const int src = slot < j ? slot : slot + 1;
             const float* from = part + (it.item0 + src) * kPartFloats +
                                 ((((c0 + cb) >> 2) + g) * kTcHeads + hh) * 4;
-            cp_async16(dst0 + ((slot * g4 + g) * kTcHeads + hh) * 16, from);
+            cp_async16(dst0 + ((slot * g4 + g) * lanes + hh) * 16, from);
         }
         cp_async_commit();
     };
@@ -744,7 +746,7 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
             const float4 acc = tree_xor_n<float4>(P, [&](int k) {
                 if (k == 0) return own;
                 const int src = j ^ k;
-                return land[((src < j ? src : src - 1) * g4 + g) * kTcHeads + h];
+                return land[((src < j ? src : src - 1) * g4 + g) * lanes + h];
             }, j, np);
             const int cs = col - c0;  // column in the slice: half (cs >> 2) & 1 of chunk cs >> 3
             *reinterpret_cast<uint2*>(tile + h * (CW * 2) + ((((cs >> 3) ^ (h & mask))) << 4) +
