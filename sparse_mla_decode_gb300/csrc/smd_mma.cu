@@ -121,7 +121,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) mma_decode_kernel(const MmaPar
     // Tracing build: phase ends of CTA `trow` (stamps 0 entry, 1 keys staged,
     // 2 query landed, 3 logits, 4 row maximum, 5 PV, 6 partials in, 7 end).
     const int trow = static_cast<int>(blockIdx.y * gridDim.x + blockIdx.x);
-    if (threadIdx.x == 0) SMD_STAMP(g_trace_mma, trow, 0);
+    if (threadIdx.x == 0) {
+        SMD_STAMP(g_trace_mma, trow, 0);
+        SMD_TRACE_SM(g_trace_mma, trow);
+    }
     constexpr int CH = kHeadsPerTile * T;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

@@ -611,7 +611,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_decode_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     pdl_entry();
-    if (threadIdx.x == 0) SMD_STAMP(g_trace_tc, trace_row(), 0);
+    if (threadIdx.x == 0) {
+        SMD_STAMP(g_trace_tc, trace_row(), 0);
+        SMD_TRACE_SM(g_trace_tc, trace_row());
+    }
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t base = smem_addr(smem);
     const uint32_t bars = base + kOffBars;

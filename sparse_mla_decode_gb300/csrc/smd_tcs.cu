@@ -715,17 +715,24 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
     const int nbatch = (CW + bc_max - 1) / bc_max;
     const int BC = (CW + 4 * nbatch - 1) / (4 * nbatch) * 4;
     const uint32_t land0 = smem_addr(smem);
+    // Thread t copies lane hh of the (peer slot, 4-column group) pairs
+    // q = q0, q0 + R, ...: lanes rounded up to a power of two threads per
+    // pair, R pairs at once (the pair is stepped, not divided out per copy).
+    int lanes_p2 = 16;
+    while (lanes_p2 < lanes) lanes_p2 <<= 1;
+    const int R = kTcThreads / lanes_p2, hh = t & (lanes_p2 - 1), q0 = t / lanes_p2;
     auto issue = [&](int bt) {
         const int cb = bt * BC, g4 = min(BC, CW - cb) / 4;  // 4-column units of the batch
-        const int units = peers * g4 * lanes;
         const uint32_t dst0 = land0 + (bt & 1) * kLandBytes;
-        for (int e = t; e < units; e += kTcThreads) {
-            const int slot = e / (g4 * lanes), rem = e - slot * g4 * lanes;
-            const int g = rem / lanes, hh = rem - g * lanes;
-            const int src = slot < j ? slot : slot + 1;
-            const float* from = part + (it.item0 + src) * kPartFloats +
-                                ((((c0 + cb) >> 2) + g) * kTcHeads + hh) * 4;
-            cp_async16(dst0 + ((slot * g4 + g) * lanes + hh) * 16, from);
+        if (hh < lanes) {
+            int slot = q0 / g4, g = q0 - slot * g4;
+            for (int q = q0; q < peers * g4; q += R) {
+                const int src = slot < j ? slot : slot + 1;
+                const float* from = part + (it.item0 + src) * kPartFloats +
+                                    ((((c0 + cb) >> 2) + g) * kTcHeads + hh) * 4;
+                cp_async16(dst0 + (q * lanes + hh) * 16, from);
+                for (g += R; g >= g4; g -= g4) ++slot;
+            }
         }
         cp_async_commit();
     };
@@ -796,7 +803,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (threadIdx.x == 0) init_bars(bars, true);
             __syncthreads();
         }
-        if (threadIdx.x == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 0);
+        if (threadIdx.x == 0) {
+            SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 0);
+            SMD_TRACE_SM(g_trace_tcs, trace_row(item, p.grid));
+        }
         if (threadIdx.x == 0) {
             // (inject_stall: the query barrier also expects 16 bytes nobody
             // sends, so its bounded wait runs out; a test hook.)

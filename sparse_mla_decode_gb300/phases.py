@@ -8,9 +8,13 @@ resident on the device, the workspace the call asks for, the L2 flushed
 before every call), and prints, for the last call, the median and 90th
 percentile over the kernel's CTAs (the spread kernel: over its items, per
 round) of the time from the CTA's first stamp to the end of each phase, plus
-the span of the launch. The stamps are %globaltimer readings taken by one
-thread at the end of each phase (smd_trace.cuh); the tracing build computes
-the same results as the normal one.
+the span of the launch, then how the SMs were used: the SMs that ran rows,
+the share of the span an SM was running one, the gaps between consecutive
+rows on one SM (a CTA's exit to the next CTA's first stamp there; the spread
+kernel: one item's end to the next one's start) and the idle time after an
+SM's last row. The stamps are %globaltimer readings taken by one thread at
+the end of each phase, and %smid at entry (smd_trace.cuh); the tracing build
+computes the same results as the normal one.
 """
 from __future__ import annotations
 
@@ -101,7 +105,35 @@ def main(argv=None) -> int:
                 continue
             d = (v[okm] - start[okm]) / 1e3
             print(f"| {name} | {np.median(d):.2f} | {np.percentile(d, 90):.2f} |")
+    occupancy(t, names.index("end"))
     return 0
+
+
+def occupancy(t: np.ndarray, end_col: int) -> None:
+    """Per-SM use over the launch: rows with both stamps, grouped by the SM
+    id in the last slot."""
+    t = t[(t[:, 0] != 0) & (t[:, end_col] != 0)]
+    if len(t) == 0:
+        return
+    t0, t1 = t[:, 0].min(), t[:, end_col].max()
+    span = (t1 - t0) / 1e3
+    sm = t[:, -1]
+    busy, gaps, tail = [], [], []
+    for s in np.unique(sm):
+        rows = t[sm == s]
+        rows = rows[np.argsort(rows[:, 0])]
+        ent, end = rows[:, 0], rows[:, end_col]
+        busy.append((end - ent).sum() / 1e3)
+        gaps.extend(((ent[1:] - end[:-1]) / 1e3).tolist())
+        tail.append((t1 - end[-1]) / 1e3)
+    busy = np.array(busy)
+    print(f"\nSMs that ran rows: {len(busy)}; an SM ran a row {100 * busy.mean() / span:.1f} % of the "
+          f"span on average (busy {busy.mean():.1f} of {span:.1f} us)")
+    if gaps:
+        g = np.array(gaps)
+        print(f"gaps between consecutive rows on one SM: {len(g)}, median {np.median(g):.2f} us, "
+              f"mean {g.mean():.2f} us, {g.sum() / len(busy):.1f} us per SM")
+    print(f"idle after an SM's last row: median {np.median(tail):.1f} us, mean {np.mean(tail):.1f} us")
 
 
 if __name__ == "__main__":

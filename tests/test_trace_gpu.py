@@ -68,6 +68,10 @@ def test_tracing_build_bits_and_phase_order(cuda, tmp_path, name, G):
     seq = rows[:, cols]
     assert (seq > 0).all(), f"{name}: a phase without a stamp"
     assert (np.diff(seq, axis=1) >= 0).all(), f"{name}: phases out of order"
+    # The last slot holds the SM each row ran on.
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert ((rows[:, 31] >= 0) & (rows[:, 31] < sms)).all(), f"{name}: SM ids"
 
 
 def test_phases_tool_prints_the_timeline(cuda):
@@ -76,3 +80,4 @@ def test_phases_tool_prints_the_timeline(cuda):
                         "--reps", "3"], cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stderr[-3000:]
     assert "mma_decode_kernel" in r.stdout and "| end |" in r.stdout
+    assert "SMs that ran rows" in r.stdout
