@@ -144,6 +144,12 @@ __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders global data this thread has acquired from other threads' generic
+// stores before its later async-proxy (bulk copy) reads of it.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- clusters --
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

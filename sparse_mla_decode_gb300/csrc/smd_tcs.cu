@@ -61,7 +61,7 @@ constexpr int kOffLsum = kOffRowMax + 128 * 4;            // [4][128] sums of P 
 constexpr int kOffIdx = kOffLsum + 4 * 128 * 4;           // [512] this item's key indices
 constexpr int kOffWarpSum = kOffIdx + kTcMaxKeys * 4;     // [16] block scan
 constexpr int kOffBars = kOffWarpSum + 16 * 4;
-constexpr int kNumBars = 13;
+constexpr int kNumBars = 14;
 constexpr int kOffTmem = kOffBars + 8 * kNumBars;
 constexpr int kSmemUsed = kOffTmem + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // + alignment of the dynamic base to 1 KB
@@ -69,7 +69,7 @@ static_assert(kOffRowMax % 16 == 0 && kOffBars % 8 == 0, "layout alignment");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = 3, kBarFreeB = 5, kBarS = 7, kBarP = 11,
-              kBarO = 12;
+              kBarO = 12, kBarLand = 13;  // the staged merge's bulk copies
 
 constexpr int kProducerThreads = 256;
 
@@ -325,6 +325,7 @@ __device__ __forceinline__ void init_bars(uint32_t bars, bool again) {
     for (int c = 0; c < 4; ++c) mbar_init(bars + 8 * (kBarS + c), 1);
     mbar_init(bars + 8 * kBarP, kTcThreads);
     mbar_init(bars + 8 * kBarO, 1);
+    mbar_init(bars + 8 * kBarLand, 1);
     fence_mbar_init();
 }
 
@@ -523,16 +524,17 @@ __device__ __forceinline__ int stage_mask(int chunks) { return min(chunks & -chu
 // One owner's 16 columns at `col` of a unit: the pairwise tree over positions
 // k = 0 .. P - 1 (piece j ^ k; P = the unit's pieces rounded up to a power of
 // two), pieces src >= np absent (np: the pieces holding keys of lane h's own
-// row; all of the unit's pieces unless row groups), 4 columns at a time.
+// row; all of the unit's pieces unless row groups), 4 columns at a time; L:
+// the unit's lanes (the partials' row stride).
 __device__ __forceinline__ void merge_cols(const float* part, int64_t item0, int j, int P, int np,
-                                           int h, int col, const float (&own)[16],
+                                           int L, int h, int col, const float (&own)[16],
                                            float (&out)[16]) {
     constexpr int64_t kPartFloats = static_cast<int64_t>(kTcHeads) * kLatent;
 #pragma unroll
     for (int c0 = 0; c0 < 16; c0 += 4) {
         const float4 r = tree_xor_n<float4>(P, [&](int k) {
             if (k == 0) return make_float4(own[c0], own[c0 + 1], own[c0 + 2], own[c0 + 3]);
-            return ld_cg_v4(part + (item0 + (j ^ k)) * kPartFloats + (((col + c0) >> 2) * kTcHeads + h) * 4);
+            return ld_cg_v4(part + (item0 + (j ^ k)) * kPartFloats + (((col + c0) >> 2) * L + h) * 4);
         }, j, np);
         out[c0] = r.x;
         out[c0 + 1] = r.y;
@@ -613,8 +615,9 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
     uint64_t* ws_max = reinterpret_cast<uint64_t*>(p.ws_base + p.ws.max);
 
     // 1. This item's partials of the other owners' columns (16-byte unit u of
-    // head h at (u * 128 + h): one warp-wide store covers 512 contiguous bytes),
-    // and its sums; then one flag per owner. (Every SM exchanges at once here,
+    // lane h at (u * lanes + h): one warp-wide store covers 512 contiguous
+    // bytes, and an owner's slice is contiguous), and its sums; then one flag
+    // per owner. (Every SM exchanges at once here,
     // so the phase is bound by L2 bandwidth; all 16 warps write.)
     float* mine_part = part + static_cast<int64_t>(item) * kPartFloats;
     for (int q = 0; q < 8; ++q) {
@@ -628,10 +631,10 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
             for (int i = 0; i < 16; ++i) v[i] = 0.f;
         }
         if (h >= p.lanes) continue;  // padding lanes are never merged
-        float* dst = mine_part + ((col >> 2) * kTcHeads + h) * 4;
+        float* dst = mine_part + ((col >> 2) * p.lanes + h) * 4;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            st_v4(dst + i * kTcHeads * 4, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+            st_v4(dst + i * p.lanes * 4, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
     }
     if (cg == 0) sums[static_cast<int64_t>(item) * kTcHeads + h] = l;
     __syncthreads();
@@ -680,7 +683,7 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
                 for (int i = 0; i < 16; ++i) own[i] = 0.f;
             }
             if (h < p.lanes) {
-                merge_cols(part, it.item0, j, P, np, h, col, own, acc);
+                merge_cols(part, it.item0, j, P, np, p.lanes, h, col, own, acc);
             } else {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) acc[i] = 0.f;  // padding lanes are never stored
@@ -696,11 +699,13 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
         return;
     }
     // More pieces (narrow slices, many loads per column): the peers' slices
-    // come into shared memory first (cp.async, which holds no register while
-    // in flight), in batches of BC columns over two buffers in the dead
-    // query, P tiles and ring, so that a whole batch is in flight at once;
-    // the tree then reads them from there. The BF16 tile is staged behind
-    // the buffers and stored by whole rows (out may be mapped host memory).
+    // come into shared memory first, into the dead query, P tiles and ring,
+    // and the tree reads them from there. Where every peer's slice fits at
+    // once (units of at most 64 lanes), each comes by one bulk copy (it is
+    // contiguous in the workspace); otherwise in batches of BC columns over
+    // two buffers by cp.async (which holds no register while in flight), a
+    // whole batch in flight at once. The BF16 tile is staged behind the
+    // buffers and stored by whole rows (out may be mapped host memory).
     constexpr int kStageMax = kTcHeads * 112 * 2;  // the widest slice of 5 or more pieces
     constexpr int kLandBytes = (3 * kTile - kStageMax) / 2 / 16 * 16;  // one of the two buffers
     uint8_t* tile = smem + 2 * kLandBytes;
@@ -729,13 +734,53 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
             for (int q = q0; q < peers * g4; q += R) {
                 const int src = slot < j ? slot : slot + 1;
                 const float* from = part + (it.item0 + src) * kPartFloats +
-                                    ((((c0 + cb) >> 2) + g) * kTcHeads + hh) * 4;
+                                    ((((c0 + cb) >> 2) + g) * lanes + hh) * 4;
                 cp_async16(dst0 + (q * lanes + hh) * 16, from);
                 for (g += R; g >= g4; g -= g4) ++slot;
             }
         }
         cp_async_commit();
     };
+    const int units = CW / 4;  // 4-column groups of the slice
+    const uint32_t slice_bytes = static_cast<uint32_t>(units * lanes * 16);
+    if (static_cast<int64_t>(peers) * slice_bytes <= 2 * static_cast<int64_t>(kLandBytes)) {
+        const uint32_t bar = smem_addr(smem) + kOffBars + 8 * kBarLand;
+        if (t < 32) {
+            fence_proxy_async_global();  // the peers' partials (acquired above) -> the copy engine
+            if (t == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(peers) * slice_bytes);
+            __syncwarp();
+            for (int slot = t; slot < peers; slot += 32) {
+                const int src = slot < j ? slot : slot + 1;
+                bulk_g2s(land0 + slot * slice_bytes,
+                         part + (it.item0 + src) * kPartFloats + (c0 >> 2) * lanes * 4, slice_bytes, bar);
+            }
+        }
+        bool landed = true;
+        mbar_wait(bar, 0, landed, p.a.status, p.budget_ns);
+        landed = __all_sync(0xffffffffu, landed);  // the TMEM loads below are warp-wide
+        const float4* land = reinterpret_cast<const float4*>(smem);
+        for (int g = cg; g < units && landed; g += 4) {  // warp-uniform
+            const int col = c0 + 4 * g;
+            const float4 own = have_o ? tmem_ld4(lane_base + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if (h >= p.lanes) continue;  // padding lanes are never stored
+            const float4 acc = tree_xor_n<float4>(P, [&](int k) {
+                if (k == 0) return own;
+                const int src = j ^ k;
+                return land[((src < j ? src : src - 1) * units + g) * lanes + h];
+            }, j, np);
+            const int cs = col - c0;
+            *reinterpret_cast<uint2*>(tile + h * (CW * 2) + ((((cs >> 3) ^ (h & mask))) << 4) +
+                                      ((cs >> 2) & 1) * 8) =
+                make_uint2(bf16x2(acc.x * inv, acc.y * inv), bf16x2(acc.z * inv, acc.w * inv));
+        }
+        __syncthreads();  // the tile is staged
+        if (t == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 10);
+        if (j == 0 && cg == 0 && h < p.lanes)
+            *lse = total > 0.f ? (m - p.log2_448 + log2f(total)) * 0.69314718055994530942f : -INFINITY;
+        if (t == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 11);
+        flush(tile, CW * 2, mask, p.lanes, oblock + c0);
+        return;
+    }
     issue(0);
     if (nbatch > 1) issue(1);
     for (int bt = 0; bt < nbatch; ++bt) {
