@@ -525,7 +525,8 @@ __device__ __forceinline__ int stage_mask(int chunks) { return min(chunks & -chu
 // k = 0 .. P - 1 (piece j ^ k; P = the unit's pieces rounded up to a power of
 // two), pieces src >= np absent (np: the pieces holding keys of lane h's own
 // row; all of the unit's pieces unless row groups), 4 columns at a time; L:
-// the unit's lanes (the partials' row stride).
+// the partials' row stride (part_stride).
+template <bool kNarrow>
 __device__ __forceinline__ void merge_cols(const float* part, int64_t item0, int j, int P, int np,
                                            int L, int h, int col, const float (&own)[16],
                                            float (&out)[16]) {
@@ -534,7 +535,8 @@ __device__ __forceinline__ void merge_cols(const float* part, int64_t item0, int
     for (int c0 = 0; c0 < 16; c0 += 4) {
         const float4 r = tree_xor_n<float4>(P, [&](int k) {
             if (k == 0) return make_float4(own[c0], own[c0 + 1], own[c0 + 2], own[c0 + 3]);
-            return ld_cg_v4(part + (item0 + (j ^ k)) * kPartFloats + (((col + c0) >> 2) * L + h) * 4);
+            return ld_cg_v4(part + (item0 + (j ^ k)) * kPartFloats +
+                            (((col + c0) >> 2) * (kNarrow ? L : kTcHeads) + h) * 4);
         }, j, np);
         out[c0] = r.x;
         out[c0 + 1] = r.y;
@@ -567,6 +569,11 @@ __device__ __forceinline__ float4 tmem_ld4(uint32_t taddr) {
 // ---- all 16 warps: exchange, merge, output ---------------------------------------
 // Warp w serves TMEM lane quarter w % 4 (thread = head h) and column group
 // cg = w / 4.
+// kNarrow: units of at most 64 lanes (row groups, H <= 64), whose partials
+// take the lanes as their row stride and whose merge lands every peer's slice
+// at once; wider units keep the stride of 128 (the launch picks the kernel
+// by the units' lanes).
+template <bool kNarrow>
 __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32_t tmem,
                                        const Item& it, int item, bool& ok) {
     const int warp = threadIdx.x >> 5;
@@ -615,10 +622,12 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
     uint64_t* ws_max = reinterpret_cast<uint64_t*>(p.ws_base + p.ws.max);
 
     // 1. This item's partials of the other owners' columns (16-byte unit u of
-    // lane h at (u * lanes + h): one warp-wide store covers 512 contiguous
-    // bytes, and an owner's slice is contiguous), and its sums; then one flag
-    // per owner. (Every SM exchanges at once here,
-    // so the phase is bound by L2 bandwidth; all 16 warps write.)
+    // lane h at (u * stride + h), stride = the lanes (narrow units) or 128:
+    // one warp-wide store covers 512 contiguous bytes, and an owner's slice
+    // from one piece is contiguous), and its sums; then one flag per owner.
+    // (Every SM exchanges at once here, so the phase is bound by L2
+    // bandwidth; all 16 warps write.)
+    const int stride = kNarrow ? p.lanes : kTcHeads;
     float* mine_part = part + static_cast<int64_t>(item) * kPartFloats;
     for (int q = 0; q < 8; ++q) {
         const int col = 128 * cg + 16 * q;
@@ -631,10 +640,10 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
             for (int i = 0; i < 16; ++i) v[i] = 0.f;
         }
         if (h >= p.lanes) continue;  // padding lanes are never merged
-        float* dst = mine_part + ((col >> 2) * p.lanes + h) * 4;
+        float* dst = mine_part + ((col >> 2) * stride + h) * 4;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            st_v4(dst + i * p.lanes * 4, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+            st_v4(dst + i * stride * 4, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
     }
     if (cg == 0) sums[static_cast<int64_t>(item) * kTcHeads + h] = l;
     __syncthreads();
@@ -683,7 +692,7 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
                 for (int i = 0; i < 16; ++i) own[i] = 0.f;
             }
             if (h < p.lanes) {
-                merge_cols(part, it.item0, j, P, np, p.lanes, h, col, own, acc);
+                merge_cols<kNarrow>(part, it.item0, j, P, np, stride, h, col, own, acc);
             } else {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) acc[i] = 0.f;  // padding lanes are never stored
@@ -734,7 +743,7 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
             for (int q = q0; q < peers * g4; q += R) {
                 const int src = slot < j ? slot : slot + 1;
                 const float* from = part + (it.item0 + src) * kPartFloats +
-                                    ((((c0 + cb) >> 2) + g) * lanes + hh) * 4;
+                                    ((((c0 + cb) >> 2) + g) * stride + hh) * 4;
                 cp_async16(dst0 + (q * lanes + hh) * 16, from);
                 for (g += R; g >= g4; g -= g4) ++slot;
             }
@@ -743,7 +752,7 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
     };
     const int units = CW / 4;  // 4-column groups of the slice
     const uint32_t slice_bytes = static_cast<uint32_t>(units * lanes * 16);
-    if (static_cast<int64_t>(peers) * slice_bytes <= 2 * static_cast<int64_t>(kLandBytes)) {
+    if (kNarrow && static_cast<int64_t>(peers) * slice_bytes <= 2 * static_cast<int64_t>(kLandBytes)) {
         const uint32_t bar = smem_addr(smem) + kOffBars + 8 * kBarLand;
         if (t < 32) {
             fence_proxy_async_global();  // the peers' partials (acquired above) -> the copy engine
@@ -815,6 +824,7 @@ __device__ __forceinline__ void finish(const TcsParams& p, uint8_t* smem, uint32
     flush(tile, CW * 2, mask, p.lanes, oblock + c0);
 }
 
+template <bool kNarrow>
 __global__ void __launch_bounds__(kTcThreads, 1)
     tcs_decode_kernel(const __grid_constant__ TcsMaps maps, const TcsParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -891,7 +901,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         ok = __syncthreads_and(ok) != 0;  // the partial sums of P are visible; one verdict
         if (threadIdx.x == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 5);
-        finish(p, smem, tmem, it, item, ok);
+        finish<kNarrow>(p, smem, tmem, it, item, ok);
         tc_fence_before();  // every TMEM read of this item precedes the next item's MMAs
         __syncthreads();
         if (threadIdx.x == 0) SMD_STAMP(g_trace_tcs, trace_row(item, p.grid), 8);
@@ -949,19 +959,23 @@ int tcs_max_grid() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
     int v = cached[dev].load();
     if (v > 0) return v;
-    if (cudaFuncSetAttribute(tcs_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tcs_decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(tcs_decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
-    int per_sm = 0, sms = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tcs_decode_kernel, kTcThreads,
+    int per_sm = 0, sms = 0, per_sm_narrow = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tcs_decode_kernel<false>, kTcThreads,
                                                       kSmemBytes) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm_narrow, tcs_decode_kernel<true>,
+                                                      kTcThreads, kSmemBytes) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
-    v = per_sm * sms;
+    v = std::min(per_sm, per_sm_narrow) * sms;
     cached[dev].store(v);
     return v;
 }
@@ -1017,7 +1031,9 @@ int launch_tcs(const CallArgs& a, const TcsConfig& cfg, cudaStream_t stream) {
     attr[0].val.cooperative = 1;
     lc.attrs = attr;
     lc.numAttrs = 1;
-    if (cudaLaunchKernelEx(&lc, tcs_decode_kernel, maps, prm) != cudaSuccess) {
+    const cudaError_t e = prm.lanes <= 64 ? cudaLaunchKernelEx(&lc, tcs_decode_kernel<true>, maps, prm)
+                                          : cudaLaunchKernelEx(&lc, tcs_decode_kernel<false>, maps, prm);
+    if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return SMD_ERR_LAUNCH;
     }
