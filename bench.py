@@ -514,7 +514,7 @@ def graph_timing(call, dev, calls: int = 100, replays: int = 5):
         return {"calls": calls, "us_per_call_min": round(min(per), 3),
                 "us_per_call_median": round(float(np.median(per)), 3),
                 "note": "warm back-to-back calls in one CUDA graph, no L2 flush"}
-    except Exception as exc:  # a capture this build cannot do is reported, not fatal
+    except Exception as exc:  # a capture that fails (e.g. an older PyTorch) is reported, not fatal
         torch.cuda.synchronize()
         return {"error": str(exc)[:200]}
 
