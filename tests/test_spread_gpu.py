@@ -66,6 +66,38 @@ def test_spread_matches_the_oracle(cuda, shape):
     check(out_g, lse_g, out_o, lse_o, f"spread {shape}")
 
 
+@pytest.mark.parametrize("H", [16, 48, 80, 112])
+def test_head_counts_below_128_on_both_unit_widths(cuda, H):
+    """Rows of fewer than 128 heads: up to 64 lanes take the narrow form of the
+    spread kernel (partials strided by the lanes, slices landed by bulk copies
+    for more than four pieces), more take the wide one (stride 128, padding
+    lanes). Ragged rows of up to 9 pieces; the oracle, and the cluster kernel's
+    bits on the rows it holds (up to 2048 keys)."""
+    import torch
+    from sparse_mla_decode_gb300 import binding
+    counts = [4500, 1, 0, 2048, 1537, 700]
+    case = inputs.random_case(900 + H, B=6, H=H, W=4500, N=30000, counts=counts, heavy_frac=0.02)
+    t = to_dev(case, cuda)
+    out_s, lse_s = spread(case, cuda, tensors=t)
+    out_o, lse_o = oracle_decode(case)
+    check(out_s, lse_s, out_o, lse_o, f"spread H={H}")
+    # the rows the cluster kernel holds (W <= 2048), decoded by it alone
+    short = [1, 2, 3, 4, 5]
+    sub = inputs.Case(case.name, case.q8[short], case.kv8, case.indices[short, :2048],
+                      case.counts[short], case.sm_scale, case.q_scale, case.k_scale,
+                      q16=case.q16[short])
+    st = torch.zeros(1, dtype=torch.int32, device=cuda)
+    q, kv, idx, cnt = to_dev(sub, cuda)
+    out_c, lse_c = binding.sparse_mla_decode(q, kv, idx, cnt, sub.sm_scale, sub.q_scale,
+                                             sub.k_scale, status=st, plan=dict(kernel=TC))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    out_c = out_c.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(out_c, out_s[short]), f"H={H}: out bits, spread vs cluster"
+    assert np.array_equal(lse_c.cpu().numpy().view(np.uint32), lse_s[short].view(np.uint32)), \
+        f"H={H}: lse bits, spread vs cluster"
+
+
 @pytest.mark.parametrize("W", [1024, 2048])
 def test_spread_is_the_cluster_kernel_where_they_split_alike(cuda, W):
     """Full rows: the cluster kernel's split (W / 512) is every row's piece
